@@ -1,0 +1,345 @@
+/*
+ * gqa_oracle.c -- plain, slow, fp64 CPU oracle for grouped-query attention over a
+ * KV cache with a sliding window, a sink logit, softcap and RoPE+append.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's CPU
+ * baseline may load this library.  It shares no code, header, table or constant with
+ * the CUDA library under sliding_window_gb300/, and it imports nothing from it.
+ *
+ * Sources (the pages this follows):
+ *   [P1] OpenVINO PR #37423 "[NPUW] Support GQA sliding-window and smooth-softmax in
+ *        DecomposeGQA", sections "Sliding window" and "smooth_softmax / head_sink".
+ *   [P2] tract PR #2645 "onnx: import GroupQueryAttention decode steps and its internal
+ *        rotary", section "What changed" (KV cache concat, do_rotary, bottom-right band).
+ *   [P3] ExecuTorch PR #21901 "Add sliding windows to the off-graph KV-cache reference",
+ *        Summary (per-layer window, mask rather than evict).
+ *   [P4] onnx-light-cpu "Attention Kernel Design", sections "Layouts and semantics",
+ *        "Compute paths" and "Scheduling, precision, and invariants".
+ *
+ * Every attention output here is the plain definition: for each query row, the set of
+ * visible cache slots is enumerated, every score is materialized in fp64, and the softmax
+ * (with the optional extra sink logit in its denominator) is taken over that set.  This
+ * is the shape of [P4]'s materialized path, carried out in double precision.
+ *
+ * Layouts (the library's boundary uses the same ones, [P4] "Layouts and semantics"):
+ *   q, out        [B, curr, Hq*D]     (rank-3, heads packed in the last dimension)
+ *   k, v (new)    [B, curr, Hkv*D]
+ *   past/present  [B, Hkv, cap, D]    (rank-4)
+ *   cos/sin cache [rope_len, D/2]
+ *   seqlens_k     [B] int32 = number of valid past tokens of each sequence
+ *   head_sink     [Hq] float, or NULL
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared [-fopenmp].
+ * -ffp-contract=off matters: the RoPE emulation rounds every product and every sum to
+ * fp32 separately, exactly as the kernel does.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ODT_F32 0
+#define ODT_F16 1
+#define ODT_BF16 2
+
+/* ------------------------------------------------------------------------------------
+ * Number formats.  Decoding and RNE rounding written from the IEEE-754 definitions of
+ * binary16 (1 sign, 5 exponent, 10 fraction bits, bias 15) and bfloat16 (1 sign,
+ * 8 exponent, 7 fraction bits, bias 127, i.e. the top half of a binary32).
+ * ---------------------------------------------------------------------------------- */
+
+static double decode_f16(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int f = h & 0x3ff;
+  double mag;
+  if (e == 0)
+    mag = ldexp((double)f, -24); /* subnormal: f * 2^-24 */
+  else if (e == 31)
+    mag = f ? NAN : INFINITY;
+  else
+    mag = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+  return sign ? -mag : mag;
+}
+
+static double decode_bf16(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float x;
+  memcpy(&x, &u, 4);
+  return (double)x;
+}
+
+/* Round a finite or non-finite double (which here always holds an fp32 value) to the
+ * nearest value of a binary format with `fbits` fraction bits, exponent bias `bias`
+ * and `ebits` exponent bits, ties to even, and return its encoding. */
+static uint32_t encode_rne(double x, int fbits, int ebits, int bias) {
+  uint32_t sign = signbit(x) ? 1u : 0u;
+  uint32_t emax_field = (1u << ebits) - 1u;
+  uint32_t out_sign = sign << (fbits + ebits);
+  if (isnan(x)) return out_sign | (emax_field << fbits) | (1u << (fbits - 1)); /* quiet NaN */
+  double a = fabs(x);
+  if (isinf(a)) return out_sign | (emax_field << fbits);
+  int emin = 1 - bias;                       /* exponent of the smallest normal */
+  double quantum_sub = ldexp(1.0, emin - fbits); /* spacing of subnormals */
+  if (a < ldexp(1.0, emin)) {
+    /* subnormal range: integer multiple of the quantum, RNE via rint (default mode) */
+    double n = rint(a / quantum_sub);
+    return out_sign | (uint32_t)n; /* n == 2^fbits encodes the smallest normal */
+  }
+  int e2;
+  double m = frexp(a, &e2);               /* a = m * 2^e2, m in [0.5, 1) */
+  int E = e2 - 1;                          /* a = (2m) * 2^E, 2m in [1, 2) */
+  double n = rint(ldexp(m, 1 + fbits));    /* 2m * 2^fbits rounded, in [2^fbits, 2^(fbits+1)] */
+  if (n == ldexp(1.0, fbits + 1)) {
+    n = ldexp(1.0, fbits);
+    E += 1;
+  }
+  if (E + bias >= (int)emax_field) return out_sign | (emax_field << fbits); /* overflow -> inf */
+  uint32_t frac = (uint32_t)(n - ldexp(1.0, fbits));
+  return out_sign | ((uint32_t)(E + bias) << fbits) | frac;
+}
+
+uint16_t oracle_encode_f16(float x) { return (uint16_t)encode_rne((double)x, 10, 5, 15); }
+uint16_t oracle_encode_bf16(float x) { return (uint16_t)encode_rne((double)x, 7, 8, 127); }
+double oracle_decode_f16(uint16_t h) { return decode_f16(h); }
+double oracle_decode_bf16(uint16_t h) { return decode_bf16(h); }
+
+/* Element idx of an array of the given dtype, as a double (exact for all three). */
+static double load_elem(const void *base, size_t idx, int dtype) {
+  if (dtype == ODT_F32) return (double)((const float *)base)[idx];
+  uint16_t h = ((const uint16_t *)base)[idx];
+  return dtype == ODT_F16 ? decode_f16(h) : decode_bf16(h);
+}
+
+static float load_f32(const void *base, size_t idx, int dtype) {
+  /* every f16/bf16 value is exactly representable in fp32 */
+  return (float)load_elem(base, idx, dtype);
+}
+
+static void store_from_f32(void *base, size_t idx, int dtype, float x) {
+  if (dtype == ODT_F32)
+    ((float *)base)[idx] = x;
+  else if (dtype == ODT_F16)
+    ((uint16_t *)base)[idx] = oracle_encode_f16(x);
+  else
+    ((uint16_t *)base)[idx] = oracle_encode_bf16(x);
+}
+
+static size_t elem_size(int dtype) { return dtype == ODT_F32 ? 4 : 2; }
+
+/* ------------------------------------------------------------------------------------
+ * Per-sequence validity.  A sequence whose past length is negative, whose past plus the
+ * new tokens do not fit the present capacity (or, when past and present are separate
+ * buffers, whose past does not fit the past capacity), or whose last RoPE position lies
+ * beyond the cos/sin cache, is rejected: its outputs are zeros and nothing of it is
+ * appended.  Bit 1 = bad seqlens_k, bit 2 = RoPE position out of range.  ([P4]
+ * "Scheduling, precision, and invariants": invalid combinations fail explicitly.)
+ * ---------------------------------------------------------------------------------- */
+int32_t oracle_sequence_status(int32_t past, int32_t curr, int32_t cap_past, int32_t cap_present,
+                               int32_t past_is_separate, int32_t do_rotary, int32_t rope_len) {
+  int32_t st = 0;
+  if (past < 0 || (int64_t)past + curr > cap_present || (past_is_separate && past > cap_past))
+    st |= 1;
+  else if (do_rotary && (int64_t)past + curr > rope_len)
+    st |= 2;
+  return st;
+}
+
+/* ------------------------------------------------------------------------------------
+ * RoPE + append, emulated bit for bit.
+ *
+ * [P2] "What changed": RoPE runs on the cos/sin cache halves widened to the head size,
+ * positions are 0..S-1 for a first prompt and start at seqlens_k for generated tokens,
+ * and K is rotated before it enters the cache; past_key/past_value are concatenated
+ * with the step and returned as present_key/present_value.
+ *
+ * Rotation (non-interleaved half split), for d in [0, D/2):
+ *     y[d]       = x[d] * c[d] - x[d + D/2] * s[d]
+ *     y[d + D/2] = x[d + D/2] * c[d] + x[d] * s[d]
+ * with c, s = cos/sin_cache[pos, d].  Each product and each sum is rounded to fp32, and
+ * the result is rounded to the storage dtype with ties to even.
+ *
+ * present rows [past_b, past_b + curr) receive the (rotated) new keys and the new values;
+ * when past is a separate buffer, rows [0, past_b) are copied from it; other rows are not
+ * touched.  q_rot (may be NULL) receives the rotated queries in q's layout.
+ * ---------------------------------------------------------------------------------- */
+static void rotate_row(const void *x, size_t xoff, const void *cosc, const void *sinc, size_t coff,
+                       int D, int dtype, void *y, size_t yoff) {
+  int half = D / 2;
+  for (int d = 0; d < half; ++d) {
+    float x1 = load_f32(x, xoff + d, dtype);
+    float x2 = load_f32(x, xoff + d + half, dtype);
+    float c = load_f32(cosc, coff + d, dtype);
+    float s = load_f32(sinc, coff + d, dtype);
+    float a = x1 * c;
+    float b = x2 * s;
+    float y1 = a - b;
+    float e = x2 * c;
+    float f = x1 * s;
+    float y2 = e + f;
+    store_from_f32(y, yoff + d, dtype, y1);
+    store_from_f32(y, yoff + d + half, dtype, y2);
+  }
+}
+
+void oracle_rope_append(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap_past,
+                        int32_t cap_present, int32_t rope_len, int32_t dtype, int32_t do_rotary,
+                        const void *q, const void *k, const void *v, const void *past_k,
+                        const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
+                        const void *sin_cache, void *q_rot, void *present_k, void *present_v,
+                        int32_t *status_out) {
+  size_t es = elem_size(dtype);
+  int separate = past_k != NULL && past_k != present_k;
+  int32_t status_all = 0;
+  for (int b = 0; b < B; ++b) {
+    int32_t past = seqlens_k[b];
+    int32_t st = oracle_sequence_status(past, curr, cap_past, cap_present, separate, do_rotary, rope_len);
+    status_all |= st;
+    if (st) continue;
+    for (int h = 0; h < Hkv; ++h) {
+      size_t dst_base = ((size_t)b * Hkv + h) * (size_t)cap_present * D;
+      if (separate) {
+        size_t src_base = ((size_t)b * Hkv + h) * (size_t)cap_past * D;
+        memcpy((char *)present_k + dst_base * es, (const char *)past_k + src_base * es, (size_t)past * D * es);
+        memcpy((char *)present_v + dst_base * es, (const char *)past_v + src_base * es, (size_t)past * D * es);
+      }
+      for (int i = 0; i < curr; ++i) {
+        size_t src = (((size_t)b * curr + i) * Hkv + h) * D;
+        size_t dst = dst_base + (size_t)(past + i) * D;
+        if (do_rotary)
+          rotate_row(k, src, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, present_k, dst);
+        else
+          memcpy((char *)present_k + dst * es, (const char *)k + src * es, (size_t)D * es);
+        memcpy((char *)present_v + dst * es, (const char *)v + src * es, (size_t)D * es);
+      }
+    }
+    if (q_rot) {
+      for (int i = 0; i < curr; ++i)
+        for (int h = 0; h < Hq; ++h) {
+          size_t off = (((size_t)b * curr + i) * Hq + h) * D;
+          if (do_rotary)
+            rotate_row(q, off, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, q_rot, off);
+          else
+            memcpy((char *)q_rot + off * es, (const char *)q + off * es, (size_t)D * es);
+        }
+    }
+  }
+  if (status_out) *status_out = status_all;
+}
+
+/* ------------------------------------------------------------------------------------
+ * The band predicate ([P1] "Sliding window", [P2] "What changed", [P3] Summary, [P4]
+ * "Compute paths").  Slot j of the present buffer holds absolute position j (the step is
+ * appended contiguously after the past).  A query at absolute position q_abs sees slot j
+ * iff
+ *     j < total                         (slots at or past seqlens_k + curr are stale)
+ *   and (not causal or j <= q_abs)      (bottom-right aligned causal band)
+ *   and (window < 0 or q_abs - j < window)   (masked when q_abs - k_abs >= window)
+ * ---------------------------------------------------------------------------------- */
+int32_t oracle_visible(int64_t q_abs, int64_t j, int64_t total, int32_t causal, int32_t window) {
+  if (j < 0 || j >= total) return 0;
+  if (causal && j > q_abs) return 0;
+  if (window >= 0 && q_abs - j >= window) return 0;
+  return 1;
+}
+
+/* ------------------------------------------------------------------------------------
+ * One query row over an explicit visibility mask.
+ *   s_j = scale * <q, k_j>;  if softcap > 0: s_j = softcap * tanh(s_j / softcap)
+ *   the sink z (when present) is one more logit in the denominator only, not scaled and
+ *   not capped ([P1] "smooth_softmax / head_sink": the extra logit joins the softmax
+ *   denominator and is sliced out);
+ *   out = sum_j exp(s_j - M) v_j / (exp(z - M) [if sink] + sum_j exp(s_j - M)),
+ *   M = max over the visible s_j and z;  a row with no visible slot gives zeros
+ *   ([P4] "A fully masked query row produces zeros rather than NaN").
+ * q is D doubles; k and v point at `n` rows of D elements of `dtype`.
+ * ---------------------------------------------------------------------------------- */
+void oracle_attend_row(const double *q, const void *k, const void *v, int64_t row0, int64_t n,
+                       const uint8_t *visible, int32_t D, int32_t dtype, double scale, double softcap,
+                       int32_t has_sink, double sink, double *out) {
+  double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double M = -INFINITY;
+  int any = 0;
+  for (int64_t j = 0; j < n; ++j) {
+    if (!visible[j]) continue;
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += q[d] * load_elem(k, (size_t)(row0 + j) * D + d, dtype);
+    double sj = scale * dot;
+    if (softcap > 0.0) sj = softcap * tanh(sj / softcap);
+    s[j] = sj;
+    if (sj > M) M = sj;
+    any = 1;
+  }
+  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  if (!any) {
+    free(s);
+    return;
+  }
+  if (has_sink && sink > M) M = sink;
+  double den = has_sink ? exp(sink - M) : 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    if (!visible[j]) continue;
+    double w = exp(s[j] - M);
+    den += w;
+    for (int d = 0; d < D; ++d) out[d] += w * load_elem(v, (size_t)(row0 + j) * D + d, dtype);
+  }
+  for (int d = 0; d < D; ++d) out[d] /= den;
+  free(s);
+}
+
+/* ------------------------------------------------------------------------------------
+ * Whole attention over the present cache, for a list of rows (or all rows).
+ * Row index r = ((b * curr) + i) * Hq + hq; out holds D doubles per listed row.
+ * Head mapping ([P4] "Layouts and semantics"): group_size G = Hq / Hkv and q head hq
+ * reads kv head hq / G, with no copy of K or V.
+ * q is the query as it enters the scores (already rotated when do_rotary).
+ * scale == 0 means 1/sqrt(D).  sink: head_sink[hq] when head_sink != NULL, else 0 when
+ * smooth_softmax, else none.
+ * Rejected sequences (oracle_sequence_status != 0) give zeros.
+ * ---------------------------------------------------------------------------------- */
+void oracle_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap_past,
+                      int32_t cap_present, int32_t rope_len, int32_t dtype, double scale,
+                      double softcap, int32_t window, int32_t causal, int32_t do_rotary,
+                      int32_t smooth_softmax, int32_t past_is_separate, const void *q,
+                      const void *present_k, const void *present_v, const int32_t *seqlens_k,
+                      const float *head_sink, const int64_t *rows, int64_t nrows, double *out) {
+  int G = Hq / Hkv;
+  if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  int64_t count = rows ? nrows : (int64_t)B * curr * Hq;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t t = 0; t < count; ++t) {
+    int64_t r = rows ? rows[t] : t;
+    int hq = (int)(r % Hq);
+    int i = (int)((r / Hq) % curr);
+    int b = (int)(r / ((int64_t)Hq * curr));
+    double *o = out + (size_t)t * D;
+    int32_t past = seqlens_k[b];
+    if (oracle_sequence_status(past, curr, cap_past, cap_present, past_is_separate, do_rotary, rope_len)) {
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      continue;
+    }
+    int hk = hq / G;
+    int64_t total = (int64_t)past + curr;
+    int64_t q_abs = (int64_t)past + i;
+    double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
+    uint8_t *vis = (uint8_t *)malloc((size_t)cap_present);
+    for (int64_t j = 0; j < cap_present; ++j) vis[j] = (uint8_t)oracle_visible(q_abs, j, total, causal, window);
+    int has_sink = head_sink != NULL || smooth_softmax;
+    double z = head_sink ? (double)head_sink[hq] : 0.0;
+    int64_t row0 = ((int64_t)b * Hkv + hk) * cap_present;
+    oracle_attend_row(qv, present_k, present_v, row0, cap_present, vis, D, dtype, scale, softcap, has_sink, z, o);
+    free(vis);
+    free(qv);
+  }
+}
+
+int32_t oracle_has_openmp(void) {
+#ifdef _OPENMP
+  return 1;
+#else
+  return 0;
+#endif
+}

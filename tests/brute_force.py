@@ -1,0 +1,57 @@
+"""Pure-Python brute force for tiny shapes: an independent second statement of the op, used
+only to pin the oracle.  It shares nothing with oracle/gqa_oracle.c: visible sets are built
+as Python set intersections, the sink is literally appended to the logit list and sliced
+out afterwards, and every sum is math.fsum.  Inputs are Python floats.
+
+Pages: OpenVINO PR #37423 ("Sliding window", "smooth_softmax / head_sink"), tract PR #2645
+("What changed"), onnx-light-cpu "Attention Kernel Design" ("Layouts and semantics",
+"Scheduling, precision, and invariants").
+"""
+import math
+
+
+def visible_set(past, curr, i, window, causal):
+    total = past + curr
+    q_abs = past + i
+    keep = set(range(total))
+    if causal:
+        keep &= set(range(q_abs + 1))
+    if window >= 0:
+        keep &= set(range(q_abs - window + 1, total + 1))
+    return keep
+
+
+def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, causal, scale,
+              softcap=0.0, sinks=None):
+    """q[b][i][hq] -> list of D floats; present_k[b][h][j] -> list of D floats.
+    sinks: None, or a list of Hq floats.  Returns out[b][i][hq] lists of D floats."""
+    G = Hq // Hkv
+    out = []
+    for b in range(B):
+        ob = []
+        for i in range(curr):
+            oi = []
+            for hq in range(Hq):
+                h = hq // G
+                keys = sorted(visible_set(seqlens[b], curr, i, window, causal))
+                logits = []
+                values = []
+                for j in keys:
+                    s = scale * math.fsum(a * c for a, c in zip(q[b][i][hq], present_k[b][h][j]))
+                    if softcap > 0:
+                        s = softcap * math.tanh(s / softcap)
+                    logits.append(s)
+                    values.append(present_v[b][h][j])
+                if not keys:
+                    oi.append([0.0] * D)
+                    continue
+                if sinks is not None:
+                    logits.append(sinks[hq])   # extra logit in the denominator ...
+                m = max(logits)
+                e = [math.exp(x - m) for x in logits]
+                den = math.fsum(e)
+                p = [x / den for x in e][: len(keys)]   # ... and sliced out
+                oi.append([math.fsum(p[t] * values[t][d] for t in range(len(keys))) for d in range(D)])
+            ob.append(oi)
+        out.append(ob)
+    return out
