@@ -1,0 +1,546 @@
+"""Benchmark of the sliding-window GQA hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch: RoPE/append of the step's new
+tokens into the KV cache, then attention of every query row over the cache.  The default
+workload is the windowed single-token bf16 decode (B=8, Hq=32, Hkv=8, D=128, past
+U[512, 4095], window 1024); its metric is the KV-read HBM bandwidth (GB/s over the
+algorithmic bytes: each visible KV row of each (b, kv head) once, plus q, out and the
+appended rows).  Prefill workloads report attention TFLOP/s (4*D per visible pair).
+
+Prints ONE JSON line on rank 0.  Inputs are seeded synthetic data, resident in HBM when the
+timed region starts; rotating buffer sets larger than L2 keep every step L2-cold.  Under
+torchrun each rank runs its own replica of the workload (weak scaling, no collective on the
+data path); the timed region is bracketed by a barrier and the max over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sliding_window_gb300.inputs import WORKLOAD_ORDER, WORKLOADS, draw_seqlens, make_case  # noqa: E402
+
+METRIC = "attention TFLOP/s (prefill) & KV-read HBM GB/s (decode), % of GB300 roofline"
+DEFAULT_WORKLOAD = WORKLOAD_ORDER[1]
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------------------
+# algorithmic accounting
+# --------------------------------------------------------------------------------------
+def esize(w):
+    return 4 if w.dtype == "f32" else 2
+
+
+def band(w, past, window):
+    """Union band [lo, hi) of the step's rows for one sequence."""
+    total = past + w.q_len
+    lo = 0 if window < 0 else max(0, past - window + 1)
+    return lo, total
+
+
+def kv_read_bytes(w, seqlens, window):
+    return sum((hi - lo) for lo, hi in (band(w, p, window) for p in seqlens.tolist())) * \
+        w.kv_heads * 2 * w.head_dim * esize(w)
+
+
+def io_bytes(w):
+    """q read + out written + new k/v read and appended."""
+    e = esize(w)
+    return w.batch * w.q_len * w.head_dim * e * (2 * w.q_heads + 4 * w.kv_heads)
+
+
+def visible_pairs(w, seqlens, window):
+    pairs = 0
+    for past in seqlens.tolist():
+        qa = np.arange(past, past + w.q_len, dtype=np.int64)
+        hi = qa + 1 if w.causal else np.full_like(qa, past + w.q_len)
+        lo = np.zeros_like(qa) if window < 0 else np.maximum(0, qa - window + 1)
+        pairs += int(np.maximum(0, hi - lo).sum())
+    return pairs * w.q_heads
+
+
+def step_work(w, seqs):
+    """(algorithmic units per step, kernel units per step, unit name) for a workload."""
+    if w.mode == "decode":
+        kv = sum(kv_read_bytes(w, s, win) for s, win in zip(seqs, w.windows))
+        io = io_bytes(w) * w.layers
+        return (kv + io) / 1e9, (kv + (io_bytes(w) - 4 * w.batch * w.q_len * w.kv_heads * w.head_dim * esize(w))
+                                 * w.layers) / 1e9, "GB/s"
+    flops = sum(4.0 * w.head_dim * visible_pairs(w, s, win) for s, win in zip(seqs, w.windows))
+    return flops / 1e12, flops / 1e12, "TFLOP/s"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.target = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.target = str(device_index)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------------------
+class Step:
+    """One buffer set of a workload (all layers) and the calls that make one step."""
+
+    def __init__(self, w, rank, set_index, device):
+        from sliding_window_gb300 import gqa
+        self.g = gqa
+        self.w = w
+        self.layers = []
+        for layer in range(w.layers):
+            # every buffer set of a rank draws the same past lengths, so every step does equal work
+            c = make_case(w, layer=layer, device=device, seed_offset=1000 * rank + set_index,
+                          seqlens=draw_seqlens(w, seed_offset=rank))
+            p = gqa.params_from_dict(c.params)
+            ws = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device=device)
+            L = dict(c=c, p=p, p_attend=gqa.params_from_dict(dict(c.params, do_rotary=0)), ws=ws,
+                     out=torch.empty_like(c.q), q_rot=torch.empty_like(c.q),
+                     status=torch.zeros(1, dtype=torch.int32, device=device))
+            self.layers.append(L)
+        self.fn = gqa.gqa_attention_decode if w.mode == "decode" else gqa.gqa_attention_prefill
+
+    def seqlens(self):
+        return [L["c"].seqlens_k.cpu().numpy() for L in self.layers]
+
+    def full(self, stream):
+        """One step through the public call: append (+RoPE) then attention, per layer."""
+        for L in self.layers:
+            c = L["c"]
+            self.g.check(self.fn(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin, c.head_sink,
+                                 L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "step")
+
+    def append_only(self, stream):
+        for L in self.layers:
+            c = L["c"]
+            self.g.check(self.g.gqa_rope_append_kv(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos,
+                                                   c.sin, L["q_rot"], c.past_k, c.past_v, L["status"], stream))
+
+    def attend_only(self, stream):
+        """The attention kernel alone (present already holds the step; q arrives rotated)."""
+        for L in self.layers:
+            c = L["c"]
+            q = L["q_rot"] if self.w.do_rotary else c.q
+            self.g.check(self.fn(L["p_attend"], q, None, None, None, None, c.seqlens_k, None, None, c.head_sink,
+                                 L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "attend")
+
+    def nbytes(self):
+        tot = 0
+        for L in self.layers:
+            c = L["c"]
+            for t in (c.q, c.k, c.v, c.past_k, c.past_v, L["out"], L["ws"], L["q_rot"]):
+                tot += t.numel() * t.element_size()
+        return tot
+
+
+def capture(fn_list, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        for f in fn_list:
+            f(stream)
+    return g
+
+
+def time_graphs(graphs_seq, stream):
+    """Replay graphs back to back on `stream` between two CUDA events on that stream."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for g in graphs_seq:
+            g.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def plan_graphs(steps_fns, K, per_graph, stream):
+    """Graphs that together run exactly K steps: full graphs of `per_graph` steps cycling over
+    the buffer sets, plus one remainder graph."""
+    n = len(steps_fns)
+    full = capture([steps_fns[i % n] for i in range(per_graph)], stream) if K >= per_graph else None
+    rem = K % per_graph
+    remg = capture([steps_fns[i % n] for i in range(rem)], stream) if rem else None
+    seq = [full] * (K // per_graph) + ([remg] if remg else [])
+    return seq
+
+
+def run_ours(args, rank, world, local_rank):
+    from sliding_window_gb300 import gqa  # noqa: F401  (fails loudly without the library)
+    w = WORKLOADS[args.workload]
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    first = Step(w, rank, 0, device)
+    per_set = first.nbytes()
+    nsets = max(1, math.ceil(3 * L2_BYTES / per_set))
+    sets = [first] + [Step(w, rank, i, device) for i in range(1, nsets)]
+    torch.cuda.synchronize()
+    units, kunits, unit = step_work(w, first.seqlens())
+    # every set draws the same past lengths, so every step does the same work
+    for s in sets[1:]:
+        assert all((a == b).all() for a, b in zip(s.seqlens(), first.seqlens()))
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            sets[i % nsets].full(stream)
+    stream.synchronize()
+    per_graph = max(1, min(args.steps, 64 if w.mode == "decode" else 4))
+    graphs = plan_graphs([s.full for s in sets], args.steps, per_graph, stream)
+    attend = plan_graphs([s.attend_only for s in sets], args.steps, per_graph, stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for g in graphs[: max(1, args.warmup // per_graph)]:
+            g.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    elapsed = time_graphs(graphs, stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    elapsed = float(t.item())
+    launches_per_step = 2 * w.layers  # append kernel + attention kernel per layer
+
+    # the dominant kernel (attention) alone, same steps and buffers, live CUDA events
+    for L in first.layers:
+        L["status"].zero_()
+    for s in sets:
+        with torch.cuda.stream(stream):
+            s.append_only(stream)
+    stream.synchronize()
+    k_elapsed = time_graphs(attend, stream)
+    # end to end through the public call with host buffers: H2D of the step's inputs from
+    # pinned memory, the call, D2H of the output, every step
+    e2e = run_e2e(args, sets, stream, w, units)
+    status = [int(L["status"].item()) for s in sets for L in s.layers]
+    if any(status):
+        raise RuntimeError("device status bits set during the bench: %s" % status)
+    return dict(w=w, elapsed=elapsed, units=units, kunits=kunits, unit=unit, clocks=clocks, nsets=nsets,
+                per_set=per_set, k_elapsed=k_elapsed, e2e=e2e, launches=launches_per_step * args.steps,
+                seqs=first.seqlens())
+
+
+def run_e2e(args, sets, stream, w, units):
+    """Every step: pinned host -> device copies of q, k, v and seqlens_k, the decode/prefill
+    call, device -> pinned host copy of out.  The KV cache stays resident (it is the op's
+    state); captured in CUDA graphs like the device-side loop."""
+    hosts = []
+    h2d = d2h = 0
+    for s in sets:
+        hs = []
+        for L in s.layers:
+            c = L["c"]
+            hq = {n: getattr(c, n).cpu().pin_memory() for n in ("q", "k", "v", "seqlens_k")}
+            ho = torch.empty(L["out"].shape, dtype=L["out"].dtype).pin_memory()
+            hs.append((hq, ho))
+        hosts.append(hs)
+    for (hq, ho), L in zip(hosts[0], sets[0].layers):
+        h2d += sum(t.numel() * t.element_size() for t in hq.values())
+        d2h += ho.numel() * ho.element_size()
+
+    def make(si):
+        s, hs = sets[si], hosts[si]
+
+        def f(stream):
+            for (hq, ho), L in zip(hs, s.layers):
+                c = L["c"]
+                for n in ("q", "k", "v", "seqlens_k"):
+                    getattr(c, n).copy_(hq[n], non_blocking=True)
+            s.full(stream)
+            for (hq, ho), L in zip(hs, s.layers):
+                ho.copy_(L["out"], non_blocking=True)
+        return f
+
+    fns = [make(i) for i in range(len(sets))]
+    per_graph = max(1, min(args.steps, 64 if w.mode == "decode" else 4))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fns[i % len(fns)](stream)
+    stream.synchronize()
+    graphs = plan_graphs(fns, args.steps, per_graph, stream)
+    stream.synchronize()
+    el = time_graphs(graphs, stream)
+    return dict(elapsed=el, h2d=h2d, d2h=d2h)
+
+
+def _storage(t):
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+class OracleSample:
+    """A bounded sample of the workload for the fp64 oracle as it stands.  Decode: the whole
+    step (append + attention, every layer) over the first n sequences, or the rows of the
+    first m kv-head groups of sequence 0 when one sequence is already too slow.  Prefill:
+    the append of sequence 0 and the attention of its first m query rows (all heads).
+    Sized so that one call takes about `budget_s` seconds."""
+
+    def __init__(self, w, budget_s):
+        import oracle
+        self.oracle = oracle
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        self.w = w
+        if w.mode == "decode":
+            n = 1
+            while True:
+                self._prepare(n, "sequences")
+                t = self._timed()
+                if t >= budget_s / 2 or n >= w.batch:
+                    break
+                n = min(w.batch, max(n + 1, int(n * budget_s / max(t, 1e-3) * 0.7)))
+            if t > 2 * budget_s:
+                g = max(1, int(w.kv_heads * budget_s / t))
+                self._prepare(1, "groups", g)
+        else:
+            m = min(w.q_len, 16)
+            while True:
+                self._prepare(1, "rows", m)
+                t = self._timed()
+                if t >= budget_s / 2 or m >= w.q_len:
+                    break
+                m = min(w.q_len, max(m + 1, int(m * budget_s / max(t, 1e-3) * 0.7)))
+
+    def _prepare(self, n, kind, count=0):
+        w = self.w.scaled(batch=n)
+        self.layers = []
+        units = 0.0
+        G = w.q_heads // w.kv_heads
+        for layer in range(w.layers):
+            c = make_case(w, layer=layer, device="cpu")
+            seq = c.seqlens_k.numpy()
+            ridx = None
+            if kind == "sequences":
+                units += step_work(w, [seq])[0]
+                desc = "%d of %d sequences, all rows (append + attention)" % (n, self.w.batch)
+            elif kind == "groups":
+                ridx = np.array([i * w.q_heads + h for i in range(w.q_len) for h in range(count * G)])
+                units += count / w.kv_heads * step_work(w, [seq])[0]
+                desc = "append + %d of %d kv-head groups of sequence 0 of %d" % (count, w.kv_heads, self.w.batch)
+            else:
+                ridx = np.array([i * w.q_heads + h for i in range(count) for h in range(w.q_heads)])
+                units += step_work(w.scaled(q_len=count), [seq])[0]
+                desc = "append + first %d of %d query rows (all heads) of sequence 0 of %d" % (
+                    count, w.q_len, self.w.batch)
+            self.layers.append(dict(p=c.params, q=_storage(c.q), k=_storage(c.k), v=_storage(c.v),
+                                    pk=_storage(c.past_k).copy(), pv=_storage(c.past_v).copy(), seq=seq,
+                                    cos=None if c.cos is None else _storage(c.cos),
+                                    sin=None if c.sin is None else _storage(c.sin),
+                                    sink=None if c.head_sink is None else c.head_sink.numpy(), rows=ridx))
+        self.units = units
+        self.sample = desc + (" x %d layers" % self.w.layers if self.w.layers > 1 else "")
+
+    def run(self):
+        o = self.oracle
+        for L in self.layers:
+            q_rot, pk, pv, _ = o.rope_append(L["p"], L["q"], L["k"], L["v"], L["pk"], L["pv"], L["seq"], L["cos"],
+                                             L["sin"], present_k=L["pk"], present_v=L["pv"])
+            o.attention(L["p"], q_rot, pk, pv, L["seq"], L["sink"], rows=L["rows"])
+        return self.units
+
+    def _timed(self):
+        t0 = time.perf_counter()
+        self.run()
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget_s=12.0):
+    s = OracleSample(w, budget_s / 4)
+    t0 = time.perf_counter()
+    units = 0.0
+    while True:
+        units += s.run()
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    unit = "GB/s" if w.mode == "decode" else "TFLOP/s"
+    return units / el, unit, s.sample, s.cores, el
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = {"decode_window_bf16": 100000, "specdecode_rotary_f16": 20000, "decode_long_bf16": 1500,
+                      "prefill_sink_softcap_bf16": 500, "prefill_fp32_tiny": 20000}[args.workload]
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        value, unit, sample, cores, t = reference_arm(w, args)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 6), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "global_batch": w.batch, "seq_len": w.q_len},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    r = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(report(args, w, r, world)))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def reference_arm(w, args):
+    """The oracle on the host cores: W untimed and K timed steps, each step a bounded sample
+    of the workload sized so that the whole run stays within a few minutes."""
+    per_step = max(0.05, min(10.0, 150.0 / (args.steps + args.warmup)))
+    s = OracleSample(w, per_step)
+    for _ in range(args.warmup):
+        s.run()
+    t0 = time.perf_counter()
+    units = sum(s.run() for _ in range(args.steps))
+    el = time.perf_counter() - t0
+    unit = "GB/s" if w.mode == "decode" else "TFLOP/s"
+    return units / el, unit, s.sample, s.cores, el
+
+
+def report(args, w, r, world):
+    peaks, src = load_peaks()
+    units, kunits, unit = r["units"], r["kunits"], r["unit"]
+    value = units * args.steps * world / r["elapsed"]
+    k_time = r["k_elapsed"] / args.steps
+    if unit == "GB/s":
+        peak, bound, punit = float(peaks["hbm_gbs"]), "hbm", "GB/s"
+    else:
+        peak, bound, punit = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), "tensor", "TFLOP/s"
+    achieved = kunits / k_time
+    traffic = load_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(r["elapsed"] / args.steps * 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": {"f32": "f32", "f16": "f16", "bf16": "bf16"}[w.dtype],
+        "data": "synthetic (seeded N(0,1) q/k/v, uniform past lengths, stale-slot garbage)",
+        "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
+                   "head_dim": w.head_dim, "new_tokens": w.q_len, "capacity": w.cap, "windows": list(w.windows),
+                   "layers": w.layers, "buffer_sets": r["nsets"], "bytes_per_set": r["per_set"],
+                   "l2": "rotating buffer sets totalling > 3x L2 (inputs larger than L2)",
+                   "tokens_per_s": round(w.batch * w.q_len * args.steps * world / r["elapsed"], 1),
+                   "peaks": src},
+        "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": punit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_split" if w.mode == "decode" else ("prefill_tc" if w.dtype != "f32"
+                                                                           else "attn_simt"),
+                     "kernel_ms": round(k_time * 1e3, 6), "peak_source": src},
+        "clocks": r["clocks"],
+        "gpu_launches": r["launches"],
+        "e2e": {"value": round(units * args.steps / r["e2e"]["elapsed"], 3), "unit": unit,
+                "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"]},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, u, sample, cores, t = cpu_baseline(w)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": u, "cores": cores, "kind": "oracle",
+                                "sample": sample, "seconds": round(t, 2)}
+    return line
+
+
+def load_traffic(name):
+    """dram bytes per launch of the dominant kernel from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(name)
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

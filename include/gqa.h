@@ -1,0 +1,165 @@
+/*
+ * gqa.h -- C ABI of the sliding-window grouped-query attention library (libgqa.so).
+ *
+ * The library computes grouped-query attention (GQA) over a KV cache with the semantics
+ * of com.microsoft.GroupQueryAttention / ONNX Attention, on one NVIDIA GB300 (sm_103a).
+ * Every step runs in the library's own CUDA kernels; nothing falls back to the CPU.
+ *
+ * Passages that define the operation (cited by page title and section):
+ *  [P1] OpenVINO PR #37423 "[NPUW] Support GQA sliding-window and smooth-softmax in
+ *       DecomposeGQA": "Sliding window" (mask key k_abs for query q_abs when
+ *       q_abs - k_abs >= local_window_size, in true absolute positions; multi-token
+ *       decode), "smooth_softmax / head_sink" (a per-head sink logit that joins the
+ *       softmax denominator and is then dropped; zero sink for plain smooth_softmax).
+ *  [P2] tract PR #2645 "onnx: import GroupQueryAttention decode steps and its internal
+ *       rotary": "What changed" (past_key/past_value concatenated with the step into
+ *       present_key/present_value; bottom-right causal band; do_rotary with positions
+ *       0..S-1 for a first prompt and seqlens_k onward for generated tokens; K rotated
+ *       before it enters the cache; causal=0 honoured).
+ *  [P3] ExecuTorch PR #21901 "Add sliding windows to the off-graph KV-cache reference":
+ *       the window is a per-layer setting and masks the cache rather than evicting it.
+ *  [P4] onnx-light-cpu "Attention Kernel Design": "Layouts and semantics" (rank-3
+ *       [B, L, H*D] tensors; group_size = q_heads / kv_heads maps q heads onto kv heads
+ *       without repeating K or V; softcap), "Compute paths" (streaming online softmax,
+ *       frontier block skipping), "Scheduling, precision, and invariants" (fp32
+ *       accumulation, output narrowed once; invalid combinations fail explicitly; a fully
+ *       masked row yields zeros, not NaN).
+ *
+ * Notation: B batch, Hq q heads, Hkv kv heads, G = Hq / Hkv, D head dim, curr = q_len new
+ * tokens per sequence, past_b = seqlens_k[b], total_b = past_b + curr, cap = capacity.
+ *
+ * Layouts (all row-major, dense, no padding):
+ *   q, out, q_rot   [B, curr, Hq*D]       element type = dtype
+ *   k, v            [B, curr, Hkv*D]      new keys / values of this step
+ *   past_k, past_v  [B, Hkv, cap_past, D]
+ *   present_k/_v    [B, Hkv, cap_present, D]  slot j holds absolute position j
+ *   cos/sin_cache   [rope_len, D/2]       dtype; rotation of half-split pairs (d, d+D/2)
+ *   seqlens_k       int32 [B] on the device (a [B,1] tensor works too) = valid past tokens
+ *   head_sink       fp32 [Hq] on the device, or NULL
+ *
+ * Semantics of one call, per sequence b, q head h, new token i (q_abs = past_b + i):
+ *   present[b, h/G, past_b + i] = rope(k[b, i, h/G], pos = past_b + i)   (rope only when
+ *   do_rotary), present_v likewise without rope; q is rotated the same way.
+ *   Slot j is visible iff j < total_b, (causal == 0 or j <= q_abs), and
+ *   (window < 0 or q_abs - j < window).
+ *   s_j = scale * <q_rot, k_j>; if softcap > 0, s_j = softcap * tanh(s_j / softcap).
+ *   out = sum_j e^{s_j - M} v_j / (sink_term + sum_j e^{s_j - M}), M the row max, where
+ *   sink_term = e^{z - M} with z = head_sink[h] (or z = 0 if smooth_softmax and head_sink
+ *   is NULL), else 0.  The sink is neither scaled nor capped.  A row with no visible slot
+ *   gives zeros.
+ *
+ * Ownership and memory: the caller owns every buffer; all pointers except the params
+ * struct are device pointers, 16-byte aligned.  The library allocates no memory (it uses
+ * the caller's workspace) and keeps no state between calls apart from the counters it
+ * leaves zeroed in the workspace.  present may alias past (same pointer): an in-place
+ * append that writes only rows [past_b, total_b).  Otherwise rows [0, past_b) of past are
+ * copied into present first; partially overlapping buffers are not allowed.  Rows of
+ * present at or beyond total_b are neither read nor written.
+ *
+ * Streams and errors: every call enqueues its kernels on `stream` (a cudaStream_t, NULL
+ * for the legacy default stream) and returns without synchronizing.  Problems visible on
+ * the host (bad shapes, NULL or misaligned pointers, a workspace that is too small, an
+ * unsupported combination) return an error code before anything is launched.  Problems
+ * that only the device can see (a seqlens_k outside [0, cap - curr], a RoPE position
+ * beyond rope_len, a pipeline wait that timed out) set bits in *dev_status (if non-NULL;
+ * bits are OR-ed in, the caller clears it) and that sequence's outputs are zeros with
+ * nothing of it appended.  Kernels never trap or assert.  Calls are reentrant; calls that
+ * share a workspace must not overlap on the device.
+ */
+#ifndef GQA_H_
+#define GQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_ABI_VERSION 1
+
+typedef int32_t gqa_status;
+#define GQA_OK 0
+#define GQA_ERR_INVALID_ARG 1  /* bad shape, attribute, NULL or misaligned pointer */
+#define GQA_ERR_UNSUPPORTED 2  /* valid per the op, not implemented by these kernels */
+#define GQA_ERR_CAPACITY 3     /* cap_present < curr, cap_past > cap_present, ... */
+#define GQA_ERR_CUDA 4         /* a CUDA runtime/driver call failed (launch, tensor map) */
+#define GQA_ERR_WORKSPACE 5    /* workspace NULL or smaller than gqa_workspace_bytes() */
+
+/* bits of *dev_status */
+#define GQA_DEV_BAD_SEQLEN 1   /* seqlens_k[b] < 0 or > cap - curr (or > cap_past) */
+#define GQA_DEV_BAD_ROPE_POS 2 /* past_b + curr > rope_len with do_rotary */
+#define GQA_DEV_TIMEOUT 4      /* a bounded pipeline wait gave up; outputs invalid */
+
+typedef enum { GQA_F32 = 0, GQA_F16 = 1, GQA_BF16 = 2 } gqa_dtype;
+
+/* Op attributes and shapes ([P1], [P2], [P4]). */
+typedef struct gqa_params {
+  int32_t batch;        /* B >= 1 */
+  int32_t q_heads;      /* Hq >= 1, divisible by kv_heads */
+  int32_t kv_heads;     /* Hkv >= 1 */
+  int32_t head_dim;     /* D: 64 or 128 */
+  int32_t q_len;        /* curr >= 1: prompt length (prefill) or new tokens (decode) */
+  int32_t cap_past;     /* rows per (b, kv head) of past_k/past_v (ignored when aliased) */
+  int32_t cap_present;  /* rows per (b, kv head) of present_k/present_v */
+  int32_t rope_len;     /* rows of cos/sin_cache (do_rotary only) */
+  int32_t dtype;        /* gqa_dtype of q, k, v, caches, cos/sin and out */
+  float scale;          /* score scale; 0 means 1/sqrt(D); must be >= 0 */
+  float softcap;        /* 0 means off; else > 0 */
+  int32_t window;       /* local_window_size: -1 = none, else >= 1 */
+  int32_t causal;       /* 1 = bottom-right causal band, 0 = none */
+  int32_t do_rotary;    /* 1 = rotate q and k with cos/sin_cache */
+  int32_t rotary_interleaved; /* must be 0 (half-split pairs only) */
+  int32_t smooth_softmax;     /* 1 = zero sink when head_sink is NULL */
+} gqa_params;
+
+/* Bytes of device workspace that gqa_attention_prefill / gqa_attention_decode need for
+ * these params (the larger of the two).  Depends only on the params.  The workspace must
+ * be zero-filled before its first use; every call leaves its counters at zero again.
+ * Returns 0 for params that fail validation. */
+size_t gqa_workspace_bytes(const gqa_params *p);
+
+/* Prefill / first prompt ([P2] "What changed"; [P4] "Compute paths"): RoPE (optional) and
+ * append of the curr new tokens, then attention of all curr query rows over present.
+ * bf16/f16 run the tensor-core kernel (tcgen05 + TMEM + TMA), f32 the fp32 SIMT kernel.
+ * seqlens_k may hold any valid past length (a prompt continued over a non-empty cache).
+ * k == NULL and v == NULL selects attention only: present must already hold the step's
+ * rows, q is used as given (already rotated), do_rotary must be 0 and past_k/past_v,
+ * cos/sin_cache are ignored. */
+gqa_status gqa_attention_prefill(const gqa_params *p, const void *q, const void *k, const void *v,
+                                 const void *past_k, const void *past_v, const int32_t *seqlens_k,
+                                 const void *cos_cache, const void *sin_cache, const float *head_sink,
+                                 void *out, void *present_k, void *present_v, void *workspace,
+                                 size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* Decode step ([P1] "Sliding window" generate branch, multi-token decode; [P2] decode
+ * steps): same arguments and semantics as gqa_attention_prefill, executed by the split-KV
+ * kernel: each CTA owns all G*curr query rows of one (b, kv head) and one chunk of its
+ * visible keys, reads each K/V byte once, and the last CTA of a group merges the partial
+ * (max, sum, acc) of the chunks.  For G*curr > 64 or f32 the fp32 SIMT kernel runs. */
+gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *k, const void *v,
+                                const void *past_k, const void *past_v, const int32_t *seqlens_k,
+                                const void *cos_cache, const void *sin_cache, const float *head_sink,
+                                void *out, void *present_k, void *present_v, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* RoPE + append alone ([P2] "What changed"): writes present rows [past_b, total_b) (K
+ * rotated when do_rotary), copies rows [0, past_b) when present does not alias past, and
+ * writes the rotated queries to q_rot (may be NULL; a plain copy when do_rotary == 0).
+ * Results are bit-exact: each product and sum is rounded to fp32, then the result to the
+ * dtype with ties to even. */
+gqa_status gqa_rope_append_kv(const gqa_params *p, const void *q, const void *k, const void *v,
+                              const void *past_k, const void *past_v, const int32_t *seqlens_k,
+                              const void *cos_cache, const void *sin_cache, void *q_rot, void *present_k,
+                              void *present_v, int32_t *dev_status, void *stream);
+
+/* Static description of a status code. */
+const char *gqa_status_string(gqa_status s);
+
+/* GQA_ABI_VERSION of the loaded library. */
+int32_t gqa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQA_H_ */

@@ -1,0 +1,288 @@
+// gqa_api.cu -- the C ABI of libgqa: host-side validation, planning and kernel launches.
+//
+// onnx-light-cpu "Attention Kernel Design", "Descriptor and invocation plan": attributes
+// and wiring are validated first, then a light plan (layouts, strides, head mapping,
+// total KV length) is rebuilt for every invocation; "Scheduling, precision, and
+// invariants": head counts positive and divisible, matching types, invalid pairings fail
+// explicitly.  Nothing here allocates memory or synchronizes the device.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "gqa.h"
+#include "launch.h"
+
+namespace gqa {
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-checkable validity of the params alone (no pointers).
+gqa_status check_params(const gqa_params *p) {
+  if (!p) return GQA_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->q_heads < 1 || p->kv_heads < 1 || p->q_len < 1) return GQA_ERR_INVALID_ARG;
+  if (p->q_heads % p->kv_heads != 0) return GQA_ERR_INVALID_ARG;
+  if (p->dtype != GQA_F32 && p->dtype != GQA_F16 && p->dtype != GQA_BF16) return GQA_ERR_INVALID_ARG;
+  if (!(p->scale >= 0.f) || !isfinite(p->scale)) return GQA_ERR_INVALID_ARG;
+  if (!(p->softcap >= 0.f) || !isfinite(p->softcap)) return GQA_ERR_INVALID_ARG;
+  if (p->window != -1 && p->window < 1) return GQA_ERR_INVALID_ARG;
+  if ((p->causal | 1) != 1 || (p->do_rotary | 1) != 1 || (p->smooth_softmax | 1) != 1) return GQA_ERR_INVALID_ARG;
+  if ((p->rotary_interleaved | 1) != 1) return GQA_ERR_INVALID_ARG;
+  if (p->rotary_interleaved) return GQA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128) return GQA_ERR_UNSUPPORTED;
+  if (p->cap_present < p->q_len || p->cap_past < 0) return GQA_ERR_CAPACITY;
+  if (p->do_rotary && p->rope_len < 1) return GQA_ERR_INVALID_ARG;
+  // TMA coordinates and the kernels' index arithmetic are 32-bit per dimension
+  const long long rows = (long long)p->batch * p->kv_heads;
+  if (rows > (1ll << 30) || (long long)p->q_len * p->q_heads > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool encode_kv_map(CUtensorMap *map, const void *base, int inner, int mid, long long outer, int box_mid, int esize) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)inner * esize, (cuuint64_t)inner * esize * mid};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_mid, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                  const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B, int box_rows, int esize) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * esize, (cuuint64_t)D * esize * H, (cuuint64_t)D * esize * H * L};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                  const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+DecodePlan decode_plan(const gqa_params &p) {
+  DecodePlan d;
+  const int G = p.q_heads / p.kv_heads;
+  d.rows = G * p.q_len;
+  d.mtiles = (d.rows + 15) / 16;
+  d.eligible = p.dtype != GQA_F32 &&
+               ((p.head_dim == 128 && d.mtiles <= 2) || (p.head_dim == 64 && d.mtiles <= 4));
+  // longest visible band of one (b, kv head): [max(0, past - W + 1), past + curr)
+  long long lmax = p.cap_present;
+  if (p.window > 0) lmax = std::min<long long>(lmax, (long long)p.window + p.q_len - 1);
+  d.lmax = (int)lmax;
+  // chunk size: spread the worst case over ~8 CTAs per SM of a 152-SM GB300, with chunks
+  // between 256 keys (per-CTA setup stays small) and 4096 keys (partials stay small)
+  const long long units = (long long)p.batch * p.kv_heads;
+  long long chunk = (lmax * units + 1215) / 1216;
+  chunk = (chunk + 63) / 64 * 64;
+  chunk = std::max<long long>(256, std::min<long long>(4096, chunk));
+  d.chunk = (int)chunk;
+  d.max_chunks = (int)((lmax + chunk - 1) / chunk);
+  return d;
+}
+
+WsLayout workspace_layout(const gqa_params &p, bool need_q_rot) {
+  WsLayout w;
+  const size_t es = p.dtype == GQA_F32 ? 4 : 2;
+  size_t off = 0;
+  if (need_q_rot) {
+    w.q_rot_off = off;
+    w.q_rot_bytes = (size_t)p.batch * p.q_len * p.q_heads * p.head_dim * es;
+    off = align_up(off + w.q_rot_bytes, kAlign);
+  }
+  DecodePlan d = decode_plan(p);
+  if (d.eligible && d.max_chunks > 1) {
+    const size_t slots = (size_t)p.batch * p.kv_heads * d.max_chunks * d.rows;
+    w.part_acc_off = off;
+    w.part_acc_bytes = slots * p.head_dim * sizeof(float);
+    off = align_up(off + w.part_acc_bytes, kAlign);
+    w.part_ml_off = off;
+    w.part_ml_bytes = slots * 2 * sizeof(float);
+    off = align_up(off + w.part_ml_bytes, kAlign);
+    w.tickets_off = off;
+    w.tickets_bytes = (size_t)p.batch * p.kv_heads * sizeof(int32_t);
+    off = align_up(off + w.tickets_bytes, kAlign);
+  }
+  w.total = off;
+  return w;
+}
+
+namespace {
+
+enum Mode { kPrefill, kDecode };
+
+// Validate the pointers and fill a Call.  Returns GQA_OK or the first error.
+gqa_status make_call(Call &c, const gqa_params *p, const void *q, const void *k, const void *v, const void *past_k,
+                     const void *past_v, const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                     const float *head_sink, void *out, void *present_k, void *present_v, int32_t *dev_status,
+                     void *stream) {
+  gqa_status s = check_params(p);
+  if (s != GQA_OK) return s;
+  c.p = *p;
+  if (c.p.scale == 0.f) c.p.scale = 1.f / sqrtf((float)p->head_dim);
+  c.G = p->q_heads / p->kv_heads;
+  c.esize = p->dtype == GQA_F32 ? 4 : 2;
+  if (!q || !seqlens_k || !present_k || !present_v) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(present_k) || !aligned16(present_v)) return GQA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seqlens_k) & 3u) || (reinterpret_cast<uintptr_t>(head_sink) & 3u))
+    return GQA_ERR_INVALID_ARG;
+  if ((k == nullptr) != (v == nullptr)) return GQA_ERR_INVALID_ARG;
+  c.append = k != nullptr;
+  if (c.append) {
+    if (!aligned16(k) || !aligned16(v)) return GQA_ERR_INVALID_ARG;
+    if ((past_k == nullptr) != (past_v == nullptr)) return GQA_ERR_INVALID_ARG;
+    const bool alias_k = past_k == nullptr || past_k == present_k;
+    const bool alias_v = past_v == nullptr || past_v == present_v;
+    if (alias_k != alias_v) return GQA_ERR_INVALID_ARG;
+    c.past_separate = !alias_k;
+    if (c.past_separate) {
+      if (!aligned16(past_k) || !aligned16(past_v)) return GQA_ERR_INVALID_ARG;
+      if (p->cap_past < 1) return GQA_ERR_CAPACITY;
+    }
+    if (p->do_rotary) {
+      if (!cos_cache || !sin_cache || !aligned16(cos_cache) || !aligned16(sin_cache)) return GQA_ERR_INVALID_ARG;
+    }
+  } else {
+    if (p->do_rotary) return GQA_ERR_INVALID_ARG;  // attention only: q arrives rotated
+    c.past_separate = 0;
+  }
+  c.q_in = q;
+  c.q = q;
+  c.k = k;
+  c.v = v;
+  c.past_k = past_k;
+  c.past_v = past_v;
+  c.seqlens = seqlens_k;
+  c.cos = cos_cache;
+  c.sin = sin_cache;
+  c.head_sink = head_sink;
+  c.out = out;
+  c.present_k = present_k;
+  c.present_v = present_v;
+  c.status = dev_status;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  return GQA_OK;
+}
+
+gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const void *k, const void *v,
+                         const void *past_k, const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
+                         const void *sin_cache, const float *head_sink, void *out, void *present_k, void *present_v,
+                         void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  Call c;
+  gqa_status s = make_call(c, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink, out, present_k,
+                           present_v, dev_status, stream);
+  if (s != GQA_OK) return s;
+  if (!out || !aligned16(out)) return GQA_ERR_INVALID_ARG;
+  const bool rotate = c.append && p->do_rotary;
+  const WsLayout wl = workspace_layout(c.p, rotate);
+  const DecodePlan dp = decode_plan(c.p);
+  const bool use_split = mode == kDecode && dp.eligible;
+  size_t need = (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
+  if (use_split && dp.max_chunks > 1) need = wl.total;
+  if (need > 0) {
+    if (!workspace || !aligned16(workspace)) return GQA_ERR_WORKSPACE;
+    if (workspace_bytes < need) return GQA_ERR_WORKSPACE;
+  }
+  c.ws = static_cast<char *>(workspace);
+  c.ws_bytes = workspace_bytes;
+  if (c.append) {
+    c.q_rot = rotate ? c.ws + wl.q_rot_off : nullptr;
+    s = launch_rope_append(c);
+    if (s != GQA_OK) return s;
+    if (rotate) c.q = c.q_rot;
+  }
+  if (mode == kDecode) return use_split ? launch_decode_split(c, dp, wl) : launch_attention_simt(c);
+  if (p->dtype == GQA_F32) return launch_attention_simt(c);
+  return launch_prefill_tc(c);
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+size_t gqa_workspace_bytes(const gqa_params *p) {
+  if (gqa::check_params(p) != GQA_OK) return 0;
+  return gqa::workspace_layout(*p, p->do_rotary != 0).total;
+}
+
+gqa_status gqa_attention_prefill(const gqa_params *p, const void *q, const void *k, const void *v,
+                                 const void *past_k, const void *past_v, const int32_t *seqlens_k,
+                                 const void *cos_cache, const void *sin_cache, const float *head_sink, void *out,
+                                 void *present_k, void *present_v, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream) {
+  return gqa::run_attention(gqa::kPrefill, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
+                            out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *k, const void *v,
+                                const void *past_k, const void *past_v, const int32_t *seqlens_k,
+                                const void *cos_cache, const void *sin_cache, const float *head_sink, void *out,
+                                void *present_k, void *present_v, void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, void *stream) {
+  return gqa::run_attention(gqa::kDecode, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
+                            out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_rope_append_kv(const gqa_params *p, const void *q, const void *k, const void *v, const void *past_k,
+                              const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
+                              const void *sin_cache, void *q_rot, void *present_k, void *present_v,
+                              int32_t *dev_status, void *stream) {
+  gqa::Call c;
+  if (!k || !v) return GQA_ERR_INVALID_ARG;
+  gqa_status s = gqa::make_call(c, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, nullptr, nullptr,
+                                present_k, present_v, dev_status, stream);
+  if (s != GQA_OK) return s;
+  if (q_rot && !gqa::aligned16(q_rot)) return GQA_ERR_INVALID_ARG;
+  c.q_rot = q_rot;
+  return gqa::launch_rope_append(c);
+}
+
+const char *gqa_status_string(gqa_status s) {
+  switch (s) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument (shape, attribute, NULL or misaligned pointer)";
+    case GQA_ERR_UNSUPPORTED: return "combination not supported by these kernels";
+    case GQA_ERR_CAPACITY: return "capacity too small for the step";
+    case GQA_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case GQA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+int32_t gqa_abi_version(void) { return GQA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// launch.h -- host-side plan shared by the C-ABI entry points and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gqa.h"
+
+namespace gqa {
+
+// One validated call: shapes and attributes plus every pointer the kernels need.
+struct Call {
+  gqa_params p;          // scale already resolved (0 -> 1/sqrt(D))
+  int G = 1;             // q heads per kv head
+  int esize = 2;         // bytes per element
+  const void *q = nullptr;        // query as it enters the scores (input q or q_rot)
+  const void *q_in = nullptr;     // caller's q (before rotation)
+  const void *k = nullptr, *v = nullptr;
+  const void *past_k = nullptr, *past_v = nullptr;
+  const int32_t *seqlens = nullptr;
+  const void *cos = nullptr, *sin = nullptr;
+  const float *head_sink = nullptr;
+  void *out = nullptr;
+  void *present_k = nullptr, *present_v = nullptr;
+  void *q_rot = nullptr;           // where K1 writes rotated q (nullptr: not needed)
+  int past_separate = 0;           // past and present are different buffers
+  int append = 1;                  // 0: attention only (present already holds the step)
+  int32_t *status = nullptr;
+  cudaStream_t stream = nullptr;
+  char *ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+// Split-KV decode plan.  The visible keys of one (b, kv head) form one band of at most
+// Lmax slots; it is cut into chunks of `chunk` keys (a multiple of 64), one CTA each.
+struct DecodePlan {
+  bool eligible = false;  // tensor-core split kernel handles these params
+  int rows = 0;           // R = G * curr query rows per CTA
+  int mtiles = 0;         // ceil(R / 16)
+  int lmax = 0;           // longest possible visible band
+  int chunk = 0;          // keys per CTA
+  int max_chunks = 0;     // grid extent along the band
+};
+
+struct WsLayout {
+  size_t q_rot_off = 0, q_rot_bytes = 0;
+  size_t part_acc_off = 0, part_acc_bytes = 0;
+  size_t part_ml_off = 0, part_ml_bytes = 0;
+  size_t tickets_off = 0, tickets_bytes = 0;
+  size_t total = 0;
+};
+
+DecodePlan decode_plan(const gqa_params &p);
+WsLayout workspace_layout(const gqa_params &p, bool need_q_rot);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda link).
+// 3D map over a [outer, mid, inner] tensor of 16-bit elements with a 128B-swizzled box of
+// {64, box_mid, 1}.  Returns false on failure.
+bool encode_kv_map(CUtensorMap *map, const void *base, int inner, int mid, long long outer, int box_mid,
+                   int esize);
+// 4D map over q laid out [B, L, H, D]: box {64, 1, box_rows, 1}, 128B swizzle.
+bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B, int box_rows, int esize);
+
+int device_sm_count();
+
+gqa_status launch_rope_append(const Call &c);
+gqa_status launch_attention_simt(const Call &c);
+gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayout &wl);
+gqa_status launch_prefill_tc(const Call &c);
+
+}  // namespace gqa

@@ -1,0 +1,177 @@
+// rope_append.cu -- K1: RoPE (optional) + append of the step's keys/values into present,
+// rotation of the queries, and the past -> present copy when the buffers are separate.
+//
+// tract PR #2645 "onnx: import GroupQueryAttention decode steps and its internal rotary",
+// "What changed": past_key/past_value are concatenated with the step into present; with
+// do_rotary the cos/sin cache halves are widened to the head size, positions run from
+// seqlens_k (0 for a first prompt), and K is rotated before it enters the cache.
+//
+// Rotation of the half-split pair (x1, x2) = (x[d], x[d + D/2]) at position pos:
+//   y1 = x1*c - x2*s,  y2 = x2*c + x1*s,  c, s = cos/sin_cache[pos, d]
+// every product and every sum rounded to fp32 on its own (no FMA contraction), then the
+// result rounded to the dtype with ties to even.  present is therefore bit-exact.
+#include "common.cuh"
+#include "launch.h"
+
+namespace gqa {
+namespace {
+
+template <typename T> struct Vec {
+  static constexpr int N = 16 / sizeof(T);  // elements per 16-byte access
+};
+
+template <typename T>
+__device__ __forceinline__ void rotate_chunk(const T *x1p, const T *x2p, const T *cp, const T *sp, T *y1p, T *y2p) {
+  constexpr int N = Vec<T>::N;
+  uint4 ux1 = *reinterpret_cast<const uint4 *>(x1p);
+  uint4 ux2 = *reinterpret_cast<const uint4 *>(x2p);
+  uint4 uc = *reinterpret_cast<const uint4 *>(cp);
+  uint4 us = *reinterpret_cast<const uint4 *>(sp);
+  const T *x1 = reinterpret_cast<const T *>(&ux1);
+  const T *x2 = reinterpret_cast<const T *>(&ux2);
+  const T *c = reinterpret_cast<const T *>(&uc);
+  const T *s = reinterpret_cast<const T *>(&us);
+  uint4 uy1, uy2;
+  T *y1 = reinterpret_cast<T *>(&uy1);
+  T *y2 = reinterpret_cast<T *>(&uy2);
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    float a1 = to_f32(x1[e]), a2 = to_f32(x2[e]), fc = to_f32(c[e]), fs = to_f32(s[e]);
+    y1[e] = from_f32<T>(__fsub_rn(__fmul_rn(a1, fc), __fmul_rn(a2, fs)));
+    y2[e] = from_f32<T>(__fadd_rn(__fmul_rn(a2, fc), __fmul_rn(a1, fs)));
+  }
+  *reinterpret_cast<uint4 *>(y1p) = uy1;
+  *reinterpret_cast<uint4 *>(y2p) = uy2;
+}
+
+struct RopeArgs {
+  const void *q, *k, *v, *cos, *sin;
+  void *q_rot, *present_k, *present_v;
+  const int32_t *seqlens;
+  int32_t *status;
+  int B, Hq, Hkv, D, curr, cap_present, cap_past, rope_len, do_rotary, past_separate;
+};
+
+// One block per (b, i).  Work items: (head, chunk) over Hq q heads (when q_rot is wanted),
+// Hkv k heads and Hkv v heads; each item handles N elements of each half of the row.
+template <typename T>
+__global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
+  constexpr int N = Vec<T>::N;
+  const int b = blockIdx.x / a.curr;
+  const int i = blockIdx.x % a.curr;
+  const int past = a.seqlens[b];
+  const int st = sequence_status(past, a.curr, a.cap_present, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
+  if (st) {
+    if (threadIdx.x == 0 && i == 0) report(a.status, st);
+    return;
+  }
+  const int pos = past + i;
+  const int half = a.D / 2;
+  const int per_head = half / N;
+  const int nq = a.q_rot ? a.Hq : 0;
+  const int items = (nq + 2 * a.Hkv) * per_head;
+  const T *cosr = reinterpret_cast<const T *>(a.cos) + (size_t)pos * half;
+  const T *sinr = reinterpret_cast<const T *>(a.sin) + (size_t)pos * half;
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    int head = it / per_head;
+    int c = (it % per_head) * N;
+    const T *src;
+    T *dst;
+    bool rot = a.do_rotary;
+    if (head < nq) {
+      size_t off = (((size_t)b * a.curr + i) * a.Hq + head) * a.D;
+      src = reinterpret_cast<const T *>(a.q) + off;
+      dst = reinterpret_cast<T *>(a.q_rot) + off;
+    } else {
+      head -= nq;
+      bool is_v = head >= a.Hkv;
+      int h = is_v ? head - a.Hkv : head;
+      size_t off = (((size_t)b * a.curr + i) * a.Hkv + h) * a.D;
+      src = reinterpret_cast<const T *>(is_v ? a.v : a.k) + off;
+      dst = reinterpret_cast<T *>(is_v ? a.present_v : a.present_k) +
+            (((size_t)b * a.Hkv + h) * a.cap_present + pos) * a.D;
+      rot = rot && !is_v;
+    }
+    if (rot) {
+      rotate_chunk<T>(src + c, src + half + c, cosr + c, sinr + c, dst + c, dst + half + c);
+    } else {
+      *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<const uint4 *>(src + c);
+      *reinterpret_cast<uint4 *>(dst + half + c) = *reinterpret_cast<const uint4 *>(src + half + c);
+    }
+  }
+}
+
+}  // namespace
+
+// Copy rows [0, past_b) of past into present when the buffers are separate.  grid
+// (B*Hkv, y): the y blocks of one (b, kv head) stride over its 16-byte words, K and V both.
+template <typename T>
+__global__ void __launch_bounds__(256) copy_past_words_kernel(const uint4 *past_k, const uint4 *past_v, uint4 *pres_k,
+                                                              uint4 *pres_v, const int32_t *seqlens, int Hkv,
+                                                              int cap_past, int cap_present, int D, int curr,
+                                                              int rope_len, int do_rotary) {
+  constexpr int N = 16 / sizeof(T);
+  const int bh = blockIdx.x;
+  const int b = bh / Hkv;
+  const int past = seqlens[b];
+  if (sequence_status(past, curr, cap_present, cap_past, 1, do_rotary, rope_len)) return;
+  const size_t row_words = (size_t)D / N;
+  const size_t words = (size_t)past * row_words;
+  const uint4 *sk = past_k + (size_t)bh * cap_past * row_words;
+  const uint4 *sv = past_v + (size_t)bh * cap_past * row_words;
+  uint4 *dk = pres_k + (size_t)bh * cap_present * row_words;
+  uint4 *dv = pres_v + (size_t)bh * cap_present * row_words;
+  for (size_t w = (size_t)blockIdx.y * blockDim.x + threadIdx.x; w < words; w += (size_t)gridDim.y * blockDim.x) {
+    dk[w] = sk[w];
+    dv[w] = sv[w];
+  }
+}
+
+template <typename T> static gqa_status launch_t(const Call &c) {
+  const gqa_params &p = c.p;
+  RopeArgs a;
+  a.q = c.q_in;
+  a.k = c.k;
+  a.v = c.v;
+  a.cos = c.cos;
+  a.sin = c.sin;
+  a.q_rot = c.q_rot;
+  a.present_k = c.present_k;
+  a.present_v = c.present_v;
+  a.seqlens = c.seqlens;
+  a.status = c.status;
+  a.B = p.batch;
+  a.Hq = p.q_heads;
+  a.Hkv = p.kv_heads;
+  a.D = p.head_dim;
+  a.curr = p.q_len;
+  a.cap_present = p.cap_present;
+  a.cap_past = p.cap_past;
+  a.rope_len = p.rope_len;
+  a.do_rotary = p.do_rotary;
+  a.past_separate = c.past_separate;
+  if (c.past_separate) {
+    dim3 grid(p.batch * p.kv_heads, 16);
+    copy_past_words_kernel<T><<<grid, 256, 0, c.stream>>>(
+        reinterpret_cast<const uint4 *>(c.past_k), reinterpret_cast<const uint4 *>(c.past_v),
+        reinterpret_cast<uint4 *>(c.present_k), reinterpret_cast<uint4 *>(c.present_v), c.seqlens, p.kv_heads,
+        p.cap_past, p.cap_present, p.head_dim, p.q_len, p.rope_len, p.do_rotary);
+    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  constexpr int N = Vec<T>::N;
+  int items = ((c.q_rot ? p.q_heads : 0) + 2 * p.kv_heads) * (p.head_dim / 2 / N);
+  int threads = items >= 256 ? 256 : ((items + 31) / 32) * 32;
+  rope_append_kernel<T><<<p.batch * p.q_len, threads, 0, c.stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status launch_rope_append(const Call &c) {
+  switch (c.p.dtype) {
+    case GQA_F32: return launch_t<float>(c);
+    case GQA_F16: return launch_t<__half>(c);
+    case GQA_BF16: return launch_t<__nv_bfloat16>(c);
+  }
+  return GQA_ERR_INVALID_ARG;
+}
+
+}  // namespace gqa

@@ -1,0 +1,157 @@
+"""Python binding of libgqa.so (ctypes): the same entry points as include/gqa.h, with
+argument marshalling only.  Tensors are passed as device pointers; every step of the
+computation runs in the library's CUDA kernels.  Importing this module loads the library
+and raises if it has not been built (there is no fallback of any kind).
+
+    from sliding_window_gb300 import gqa
+    p = gqa.params(batch=..., q_heads=..., ...)          # a gqa_params struct
+    ws = torch.zeros(gqa.gqa_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    gqa.check(gqa.gqa_attention_decode(p, q, k, v, past_k, past_v, seqlens_k, cos, sin,
+                                       head_sink, out, present_k, present_v, ws, status))
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libgqa.so")
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = 1
+GQA_ERR_UNSUPPORTED = 2
+GQA_ERR_CAPACITY = 3
+GQA_ERR_CUDA = 4
+GQA_ERR_WORKSPACE = 5
+GQA_DEV_BAD_SEQLEN = 1
+GQA_DEV_BAD_ROPE_POS = 2
+GQA_DEV_TIMEOUT = 4
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decode", "gqa_rope_append_kv",
+            "gqa_status_string", "gqa_abi_version"]
+
+
+class GqaParams(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("q_heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("q_len", ctypes.c_int32), ("cap_past", ctypes.c_int32),
+                ("cap_present", ctypes.c_int32), ("rope_len", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("softcap", ctypes.c_float), ("window", ctypes.c_int32),
+                ("causal", ctypes.c_int32), ("do_rotary", ctypes.c_int32), ("rotary_interleaved", ctypes.c_int32),
+                ("smooth_softmax", ctypes.c_int32)]
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        super().__init__("%s: gqa status %d (%s)" % (what or "gqa call", status, gqa_status_string(status)))
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libgqa.so is not built (%s); run `python -c \"import __graft_entry__ as g; "
+                          "g.build()\"` on a machine with the CUDA toolkit" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    pp = ctypes.POINTER(GqaParams)
+    lib.gqa_workspace_bytes.argtypes = [pp]
+    lib.gqa_workspace_bytes.restype = sz
+    for name in ("gqa_attention_prefill", "gqa_attention_decode"):
+        fn = getattr(lib, name)
+        fn.argtypes = [pp] + [vp] * 13 + [sz, vp, vp]
+        fn.restype = i32
+    lib.gqa_rope_append_kv.argtypes = [pp] + [vp] * 13
+    lib.gqa_rope_append_kv.restype = i32
+    lib.gqa_status_string.argtypes = [i32]
+    lib.gqa_status_string.restype = ctypes.c_char_p
+    lib.gqa_abi_version.argtypes = []
+    lib.gqa_abi_version.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def params(batch, q_heads, kv_heads, head_dim, q_len, cap_present, dtype, cap_past=None, rope_len=0, scale=0.0,
+           softcap=0.0, window=-1, causal=1, do_rotary=0, rotary_interleaved=0, smooth_softmax=0) -> GqaParams:
+    """Build a gqa_params struct (dtype: "f32" | "f16" | "bf16" or its integer code)."""
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    return GqaParams(batch, q_heads, kv_heads, head_dim, q_len, cap_present if cap_past is None else cap_past,
+                     cap_present, rope_len, dt, scale, softcap, window, causal, do_rotary, rotary_interleaved,
+                     smooth_softmax)
+
+
+def params_from_dict(d: dict) -> GqaParams:
+    return params(d["batch"], d["q_heads"], d["kv_heads"], d["head_dim"], d["q_len"], d["cap_present"], d["dtype"],
+                  cap_past=d.get("cap_past"), rope_len=d.get("rope_len", 0), scale=d.get("scale", 0.0),
+                  softcap=d.get("softcap", 0.0), window=d.get("window", -1), causal=d.get("causal", 1),
+                  do_rotary=d.get("do_rotary", 0), rotary_interleaved=d.get("rotary_interleaved", 0),
+                  smooth_softmax=d.get("smooth_softmax", 0))
+
+
+def _ptr(t):
+    """Device pointer of a CUDA tensor (or an int address, or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    if not t.is_cuda:
+        raise ValueError("libgqa takes device tensors; got a tensor on %s" % t.device)
+    if not t.is_contiguous():
+        raise ValueError("libgqa takes dense row-major tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def gqa_workspace_bytes(p: GqaParams) -> int:
+    return int(lib.gqa_workspace_bytes(ctypes.byref(p)))
+
+
+def gqa_attention_prefill(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink, out, present_k,
+                          present_v, workspace, dev_status, stream=None) -> int:
+    return int(lib.gqa_attention_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(past_k), _ptr(past_v),
+                                         _ptr(seqlens_k), _ptr(cos_cache), _ptr(sin_cache), _ptr(head_sink),
+                                         _ptr(out), _ptr(present_k), _ptr(present_v), _ptr(workspace),
+                                         _nbytes(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def gqa_attention_decode(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink, out, present_k,
+                         present_v, workspace, dev_status, stream=None) -> int:
+    return int(lib.gqa_attention_decode(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(past_k), _ptr(past_v),
+                                        _ptr(seqlens_k), _ptr(cos_cache), _ptr(sin_cache), _ptr(head_sink),
+                                        _ptr(out), _ptr(present_k), _ptr(present_v), _ptr(workspace),
+                                        _nbytes(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def gqa_rope_append_kv(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, q_rot, present_k, present_v,
+                       dev_status, stream=None) -> int:
+    return int(lib.gqa_rope_append_kv(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(past_k), _ptr(past_v),
+                                      _ptr(seqlens_k), _ptr(cos_cache), _ptr(sin_cache), _ptr(q_rot),
+                                      _ptr(present_k), _ptr(present_v), _ptr(dev_status), _stream(stream)))
+
+
+def gqa_status_string(status: int) -> str:
+    return lib.gqa_status_string(int(status)).decode()
+
+
+def gqa_abi_version() -> int:
+    return int(lib.gqa_abi_version())
+
+
+def check(status: int, what: str = "") -> None:
+    if status != GQA_OK:
+        raise GqaError(status, what)

@@ -1,0 +1,151 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function
+that include/gqa.h declares, the Python struct matches the C struct byte for byte, and
+invalid calls return their error codes before anything is launched (onnx-light-cpu
+"Attention Kernel Design", "Scheduling, precision, and invariants": invalid pairings fail
+explicitly)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa.h")
+
+
+@pytest.fixture(scope="module")
+def g():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sliding_window_gb300 import gqa
+    return gqa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(gqa_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(g):
+    names = declared_functions()
+    assert set(names) == set(g.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (gqa_\w+)", out))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(g.lib, n)
+
+
+def test_struct_layout_matches_header(g, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gqa.h"\nint main(void){\n'
+                   'printf("%zu", sizeof(gqa_params));\n'
+                   + "".join('printf(" %%zu", offsetof(gqa_params, %s));\n' % f for f, _ in g.GqaParams._fields_)
+                   + "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    vals = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()))
+    assert vals[0] == ctypes.sizeof(g.GqaParams)
+    assert vals[1:] == [getattr(g.GqaParams, f).offset for f, _ in g.GqaParams._fields_]
+
+
+def test_version_and_status_strings(g):
+    assert g.gqa_abi_version() == 1
+    for s in range(6):
+        assert g.gqa_status_string(s) and g.gqa_status_string(s) != "unknown status"
+    assert g.gqa_status_string(99) == "unknown status"
+
+
+def good_params(g, **kw):
+    d = dict(batch=2, q_heads=8, kv_heads=2, head_dim=128, q_len=1, cap_present=1024, dtype="bf16", window=256)
+    d.update(kw)
+    return g.params(**d)
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced: every case fails first
+
+
+def call(g, p, fn="gqa_attention_decode", ws_bytes=0, **ptrs):
+    names = ["q", "k", "v", "past_k", "past_v", "seqlens_k", "cos", "sin", "head_sink", "out", "present_k",
+             "present_v", "workspace"]
+    vals = {n: FAKE for n in names}
+    vals.update(ptrs)
+    args = [ctypes.c_void_p(vals[n]) if vals[n] is not None else None for n in names]
+    return getattr(g.lib, fn)(ctypes.byref(p), *args, ws_bytes, None, None)
+
+
+@pytest.mark.parametrize("fn", ["gqa_attention_decode", "gqa_attention_prefill"])
+@pytest.mark.parametrize("kw,code", [
+    (dict(q_heads=6, kv_heads=4), 1),          # heads not divisible
+    (dict(kv_heads=0), 1),
+    (dict(batch=0), 1),
+    (dict(q_len=0), 1),
+    (dict(head_dim=96), 2),                    # valid op, not implemented
+    (dict(dtype=7), 1),
+    (dict(window=0), 1),                       # window must be -1 or >= 1
+    (dict(window=-2), 1),
+    (dict(scale=-1.0), 1),
+    (dict(softcap=-2.0), 1),
+    (dict(causal=2), 1),
+    (dict(rotary_interleaved=1), 2),
+    (dict(cap_present=0), 3),
+    (dict(q_len=8, cap_present=4), 3),
+    (dict(do_rotary=1, rope_len=0), 1),
+])
+def test_invalid_params_rejected(g, fn, kw, code):
+    assert call(g, good_params(g, **kw), fn) == code
+    assert g.lib.gqa_workspace_bytes(ctypes.byref(good_params(g, **kw))) == 0
+
+
+@pytest.mark.parametrize("ptrs,code", [
+    (dict(q=None), 1), (dict(seqlens_k=None), 1), (dict(present_k=None), 1), (dict(out=None), 1),
+    (dict(k=None), 1),                              # k without v
+    (dict(q=FAKE + 8), 1), (dict(present_v=FAKE + 4), 1), (dict(out=FAKE + 2), 1),
+    (dict(seqlens_k=FAKE + 2), 1), (dict(past_k=None), 1),  # past_k without past_v
+])
+def test_invalid_pointers_rejected(g, ptrs, code):
+    assert call(g, good_params(g), **ptrs) == code
+
+
+def test_attention_only_rejects_rotary(g):
+    p = good_params(g, do_rotary=1, rope_len=4096)
+    assert call(g, p, k=None, v=None) == 1
+
+
+def test_rotary_needs_tables(g):
+    p = good_params(g, do_rotary=1, rope_len=4096)
+    assert call(g, p, cos=None) == 1
+
+
+def test_workspace_checked_before_launch(g):
+    p = good_params(g, batch=4, cap_present=8192, window=-1)
+    need = g.lib.gqa_workspace_bytes(ctypes.byref(p))
+    assert need > 0
+    assert call(g, p, ws_bytes=need - 1) == 5
+    assert call(g, p, ws_bytes=need, workspace=None) == 5
+    assert call(g, p, ws_bytes=need, workspace=FAKE + 8) == 5
+
+
+def test_workspace_sizes(g):
+    # single-token windowed decode whose band fits one chunk needs no workspace
+    assert g.lib.gqa_workspace_bytes(ctypes.byref(good_params(g, window=200))) == 0
+    # rotary needs room for the rotated queries: B*curr*Hq*D*2 bytes, 256-aligned
+    p = good_params(g, do_rotary=1, rope_len=64, window=100)
+    assert g.lib.gqa_workspace_bytes(ctypes.byref(p)) == 2 * 1 * 8 * 128 * 2
+    # long decode: partials for every chunk slot, fp32 acc + (m, l) + a ticket per group
+    p = good_params(g, batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1)
+    ws = g.lib.gqa_workspace_bytes(ctypes.byref(p))
+    chunks = 32768 // 4096
+    rows = 8
+    slots = 64 * 8 * chunks * rows
+    assert ws >= slots * 128 * 4 + slots * 8 + 64 * 8 * 4
+    # prefill-sized q_len never needs decode partials
+    p = good_params(g, batch=2, q_heads=64, kv_heads=8, q_len=8192, cap_present=8192, window=4096)
+    assert g.lib.gqa_workspace_bytes(ctypes.byref(p)) == 0
+
+
+def test_binding_refuses_host_tensors(g):
+    import torch
+    with pytest.raises(ValueError):
+        g._ptr(torch.zeros(4))

@@ -1,0 +1,77 @@
+"""The five named workloads at full size, in the launch configuration bench.py times,
+checked against the fp64 oracle: every row for the tiny fp32 prompt, sampled rows (with the
+band edges) for the large ones, and the appended present rows bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, out_rows, run_gpu
+from helpers import storage
+from sliding_window_gb300.inputs import WORKLOADS, make_case
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def sample_rows(w, n=192, seed=0):
+    rng = np.random.default_rng(seed)
+    B, L, H = w.batch, w.q_len, w.q_heads
+    rows = set(rng.integers(0, B * L * H, size=n).tolist())
+    for b in (0, B - 1):
+        for i in sorted({0, L - 1, L // 2, min(L - 1, 127), min(L - 1, 128), min(L - 1, 4095), min(L - 1, 4096)}):
+            for h in (0, H - 1):
+                rows.add((b * L + i) * H + h)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_workload(name, layer=0):
+    w = WORKLOADS[name]
+    dev = "cuda:0" if w.cap * w.batch * w.kv_heads * w.head_dim > (1 << 26) else "cpu"
+    c = make_case(w, layer=layer, device=dev)
+    # host copies of everything the oracle reads, taken before the in-place append
+    host = make_host(c)
+    r = run_gpu(c, w.mode)
+    assert r["status"] == 0
+    rows = None if w.batch * w.q_len * w.q_heads <= 4096 else sample_rows(w)
+    p = c.params
+    q_rot, pk, pv, st = oracle.rope_append(p, host["q"], host["k"], host["v"], host["past_k"], host["past_v"],
+                                           host["seq"], host["cos"], host["sin"], present_k=host["past_k"],
+                                           present_v=host["past_v"])
+    assert st == 0
+    gk, gv = r["present_k"], r["present_v"]
+    for b, past in enumerate(host["seq"].tolist()):
+        sl = slice(past, past + w.q_len)
+        np.testing.assert_array_equal(storage(gk[b, :, sl]), pk[b, :, sl])
+        np.testing.assert_array_equal(storage(gv[b, :, sl]), pv[b, :, sl])
+    ref = oracle.attention(p, q_rot, pk, pv, host["seq"], host["sink"], rows=rows)
+    got = out_rows(r["out"], c, rows)
+    assert_close(got, ref, w.dtype, name)
+
+
+def make_host(c):
+    return dict(q=storage(c.q), k=storage(c.k), v=storage(c.v), past_k=storage(c.past_k).copy(),
+                past_v=storage(c.past_v).copy(), seq=c.seqlens_k.cpu().numpy().copy(),
+                cos=None if c.cos is None else storage(c.cos), sin=None if c.sin is None else storage(c.sin),
+                sink=None if c.head_sink is None else c.head_sink.cpu().numpy())
+
+
+def test_prefill_fp32_tiny():
+    check_workload("prefill_fp32_tiny")
+
+
+def test_decode_window_bf16():
+    check_workload("decode_window_bf16")
+
+
+def test_prefill_sink_softcap_bf16():
+    check_workload("prefill_sink_softcap_bf16")
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_specdecode_rotary_f16(layer):
+    check_workload("specdecode_rotary_f16", layer)
+
+
+def test_decode_long_bf16():
+    check_workload("decode_long_bf16")
+    torch.cuda.empty_cache()
