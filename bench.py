@@ -227,10 +227,26 @@ def time_graphs(graphs_seq, stream):
     return start.elapsed_time(end) / 1e3
 
 
+class Eager:
+    """Stand-in for a captured graph that launches the steps directly (for profilers)."""
+
+    def __init__(self, fns, stream):
+        self.fns, self.stream = fns, stream
+
+    def replay(self):
+        for f in self.fns:
+            f(self.stream)
+
+
+USE_GRAPHS = True
+
+
 def plan_graphs(steps_fns, K, per_graph, stream):
     """Graphs that together run exactly K steps: full graphs of `per_graph` steps cycling over
     the buffer sets, plus one remainder graph."""
     n = len(steps_fns)
+    if not USE_GRAPHS:
+        return [Eager([steps_fns[i % n] for i in range(K)], stream)]
     full = capture([steps_fns[i % n] for i in range(per_graph)], stream) if K >= per_graph else None
     rem = K % per_graph
     remg = capture([steps_fns[i % n] for i in range(rem)], stream) if rem else None
@@ -447,7 +463,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOAD_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true", help="launch steps directly (for profilers)")
     args = ap.parse_args()
+    global USE_GRAPHS
+    USE_GRAPHS = not args.no_graphs
     w = WORKLOADS[args.workload]
     if args.steps is None:
         args.steps = {"decode_window_bf16": 100000, "specdecode_rotary_f16": 20000, "decode_long_bf16": 1500,

@@ -315,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // -------------------------------------------------------------- merge the 4 warps
-  named_bar_sync(1, kConsumers * 32);
-  if (flags[0]) aborted = true;
+  // one decision for all consumer warps: a timed-out wait anywhere aborts the whole CTA
+  aborted = named_bar_or(1, kConsumers * 32, aborted || flags[0] != 0);
   if (aborted) {
     // a wait timed out: the producer drains its copies and reports; take part in the
     // ticket so the group's counter stays consistent, write nothing
@@ -348,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   float *accbuf = reinterpret_cast<float *>(stages);  // [QROWS][D], stages are free now
-  for (int idx = threadIdx.x; idx < QROWS * D; idx += kConsumers * 32) accbuf[idx] = 0.f;
   named_bar_sync(1, kConsumers * 32);
   if (threadIdx.x < QROWS) {
     const int row = threadIdx.x;
@@ -361,21 +360,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     row_l[row] = ll;
   }
   named_bar_sync(1, kConsumers * 32);
+  // warps add their rescaled accumulators one after another (fixed order: deterministic)
+  for (int w = 0; w < kConsumers; ++w) {
+    if (cw == w) {
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int row = 16 * mt + (lane >> 2) + 8 * h;
-      const float mm = row_m[row];
-      const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
+        for (int h = 0; h < 2; ++h) {
+          const int row = 16 * mt + (lane >> 2) + 8 * h;
+          const float mm = row_m[row];
+          const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
 #pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        const int col = 8 * dn + 2 * (lane & 3);
-        atomicAdd(&accbuf[row * D + col], acc[mt][dn][2 * h] * f);
-        atomicAdd(&accbuf[row * D + col + 1], acc[mt][dn][2 * h + 1] * f);
-      }
+          for (int dn = 0; dn < D / 8; ++dn) {
+            float2 *dst = reinterpret_cast<float2 *>(&accbuf[row * D + 8 * dn + 2 * (lane & 3)]);
+            float2 prev = w == 0 ? make_float2(0.f, 0.f) : *dst;
+            *dst = make_float2(prev.x + acc[mt][dn][2 * h] * f, prev.y + acc[mt][dn][2 * h + 1] * f);
+          }
+        }
     }
-  named_bar_sync(1, kConsumers * 32);
+    named_bar_sync(1, kConsumers * 32);
+  }
 
   if (nchunks == 1) {
     // ------------------------------------------------------------ finish in place
