@@ -13,9 +13,11 @@
 
 namespace gqa {
 
-// A pipeline wait that has not completed after this long gives up, sets GQA_DEV_TIMEOUT
-// and lets the kernel drain and return instead of hanging the GPU.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// A pipeline wait that has not completed after this many SM cycles (about 2 s at 2 GHz,
+// 4 s at 1 GHz) gives up, sets GQA_DEV_TIMEOUT and lets the kernel drain and return
+// instead of hanging the GPU.  The SM cycle counter is cheap to read, unlike the global
+// timer, so the bound costs nothing on the fast path.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -99,12 +101,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // sets *abort itself so that every role of the CTA winds down.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = globaltimer();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
+    if ((it & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (clock64() - t0 > kWaitLimitCycles) {
         *abort = 1;
         return false;
       }

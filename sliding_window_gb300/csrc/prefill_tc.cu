@@ -19,6 +19,7 @@
 // softmax overlaps the other's MMAs.  KV tiles outside [window low, causal high] are never
 // visited; only tiles that cross a frontier evaluate the per-element predicate.
 // The sink starts the running state: m = z*log2(e), l = 1, so it is counted exactly once.
+#include <limits.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -29,7 +30,7 @@ namespace {
 
 constexpr int BM = 128;       // query rows per CTA (= TMEM lanes)
 constexpr int BN = 128;       // keys per tile
-constexpr int kThreads = 192; // 6 warps
+constexpr int kThreads = 384; // 12 warps: producer, MMA, 2 spare, 2 softmax warpgroups
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
 
 struct PrefillArgs {
@@ -42,18 +43,19 @@ struct PrefillArgs {
 };
 
 template <int D> struct PSmem {
-  static constexpr int kQ = 0;
-  static constexpr int kTile = BM * D * 2;  // Q, K or V tile bytes
-  static constexpr int kK = kQ + kTile;
-  static constexpr int kV = kK + kTile;
-  static constexpr int kBar = kV + kTile;   // 9 mbarriers
-  static constexpr int kTmemSlot = kBar + 9 * 8;
+  static constexpr int kTile = BM * D * 2;  // one Q, K or V tile
+  static constexpr int kQA = 0;
+  static constexpr int kQB = kQA + kTile;
+  static constexpr int kK = kQB + kTile;     // two stages
+  static constexpr int kV = kK + 2 * kTile;  // two stages
+  static constexpr int kBar = kV + 2 * kTile;
+  static constexpr int kTmemSlot = kBar + 16 * 8;
   static constexpr int kFlag = kTmemSlot + 8;
   static constexpr int kBytes = kFlag + 8;
-  // at least 80 KB so that no more than two CTAs (2 x 256 TMEM columns) share an SM and a
-  // third can never sit blocked in tcgen05.alloc
-  static constexpr int kAlloc = (kBytes + 1024) > 80 * 1024 ? (kBytes + 1024) : 80 * 1024;
-  static constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: D columns
+  // more than half of an SM's shared memory, so a CTA (512 TMEM columns) is always alone
+  // on its SM and can never sit blocked in tcgen05.alloc behind another one
+  static constexpr int kAlloc = (kBytes + 1024) > 116 * 1024 ? (kBytes + 1024) : 116 * 1024;
+  static constexpr uint32_t kTmemCols = 512;  // S_A, S_B (128 each), O_A, O_B (128 each)
 };
 
 // Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
@@ -150,10 +152,17 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-enum { B_Q = 0, B_KFULL, B_VFULL, B_KFREE, B_VFREE, B_SFULL, B_PFULL, B_OFULL, B_COUNT };
+// mbarriers (indices into bars[])
+enum {
+  B_Q = 0,
+  B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1,
+  B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,
+  B_SFULL_A, B_SFULL_B, B_PFULL_A, B_PFULL_B, B_OFULL_A, B_OFULL_B,
+  B_COUNT
+};
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 2)
+template <typename T, int D, bool SOFTCAP>
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, PrefillArgs a) {
   using L = PSmem<D>;
@@ -163,20 +172,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kFlag);
 
-  const int hq = blockIdx.x, b = blockIdx.z;
-  const int qt = gridDim.y - 1 - blockIdx.y;  // longest tiles first
+  // CTA = (pair of q heads of one kv group, q tile, batch); longest q tiles first
+  const int pairs_per_group = (a.G + 1) / 2;
+  const int hk = blockIdx.x / pairs_per_group;
+  const int hA = hk * a.G + 2 * (blockIdx.x % pairs_per_group);
+  const bool has_b = hA + 1 < (hk + 1) * a.G;
+  const int b = blockIdx.z;
+  const int qt = gridDim.y - 1 - blockIdx.y;
   const int q0 = qt * BM;
-  const int hk = hq / a.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int past = a.seqlens[b];
   const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
   T *out = reinterpret_cast<T *>(a.out);
   const int nrows = min(BM, a.curr - q0);
   if (st) {
-    if (threadIdx.x == 0 && qt == 0 && hq == 0) report(a.status, st);
-    for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
-      const int r = idx / D, d = idx % D;
-      out[(((size_t)b * a.curr + q0 + r) * a.Hq + hq) * D + d] = from_f32<T>(0.f);
+    if (threadIdx.x == 0 && qt == 0 && blockIdx.x == 0) report(a.status, st);
+    for (int idx = threadIdx.x; idx < (has_b ? 2 : 1) * nrows * D; idx += blockDim.x) {
+      const int hh = idx / (nrows * D), r = (idx / D) % nrows, d = idx % D;
+      out[(((size_t)b * a.curr + q0 + r) * a.Hq + hA + hh) * D + d] = from_f32<T>(0.f);
     }
     return;
   }
@@ -187,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int ntiles = (khi - klo + BN - 1) / BN;  // >= 1: every row sees itself
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], i == B_PFULL ? 4 : 1);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], (i == B_PFULL_A || i == B_PFULL_B) ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -196,10 +209,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;        // columns [0, 128): S, then P (bf16 pairs) in [0, 64)
-  const uint32_t tO = tmem + 128;  // columns [128, 128 + D): O
-  int kissued = 0, vissued = 0;    // producer thread: TMA tiles issued
-  int s_commits = 0, o_commits = 0;  // MMA thread: S and PV commits issued
+  // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [384,384+D); P_X overwrites
+  // the first 64 columns of S_X as packed pairs
+  int kissued = 0, vissued = 0;      // producer thread: TMA tiles issued
+  int s_commits = 0, o_commits = 0;  // MMA thread: last S and PV commit counts
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -207,76 +220,131 @@ __global__ void __launch_bounds__(kThreads, 2)
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      uint8_t *qs = smem + L::kQ, *ks = smem + L::kK, *vs = smem + L::kV;
-      mbar_expect_tx(&bars[B_Q], L::kTile);
+      mbar_expect_tx(&bars[B_Q], (has_b ? 2 : 1) * L::kTile);
 #pragma unroll
-      for (int db = 0; db < D / 64; ++db) tma_load_4d(qs + db * (BM * 128), &tmq, db * 64, hq, q0, b, &bars[B_Q]);
+      for (int db = 0; db < D / 64; ++db) {
+        tma_load_4d(smem + L::kQA + db * (BM * 128), &tmq, db * 64, hA, q0, b, &bars[B_Q]);
+        if (has_b) tma_load_4d(smem + L::kQB + db * (BM * 128), &tmq, db * 64, hA + 1, q0, b, &bars[B_Q]);
+      }
       const int bh = b * a.Hkv + hk;
       for (int t = 0; t < ntiles; ++t) {
-        const int k0 = klo + t * BN;
-        if (t > 0 && !mbar_wait(&bars[B_KFREE], (t - 1) & 1, abort_flag)) break;
-        mbar_expect_tx(&bars[B_KFULL], L::kTile);
+        const int s = t & 1, k0 = klo + t * BN;
+        if (t >= 2 && !mbar_wait(&bars[B_KEMPTY0 + s], ((t >> 1) - 1) & 1, abort_flag)) break;
+        mbar_expect_tx(&bars[B_KFULL0 + s], L::kTile);
 #pragma unroll
-        for (int db = 0; db < D / 64; ++db) tma_load_3d(ks + db * (BN * 128), &tmk, db * 64, k0, bh, &bars[B_KFULL]);
+        for (int db = 0; db < D / 64; ++db)
+          tma_load_3d(smem + L::kK + s * L::kTile + db * (BN * 128), &tmk, db * 64, k0, bh, &bars[B_KFULL0 + s]);
         ++kissued;
-        if (t > 0 && !mbar_wait(&bars[B_VFREE], (t - 1) & 1, abort_flag)) break;
-        mbar_expect_tx(&bars[B_VFULL], L::kTile);
+        if (t >= 2 && !mbar_wait(&bars[B_VEMPTY0 + s], ((t >> 1) - 1) & 1, abort_flag)) break;
+        mbar_expect_tx(&bars[B_VFULL0 + s], L::kTile);
 #pragma unroll
-        for (int db = 0; db < D / 64; ++db) tma_load_3d(vs + db * (BN * 128), &tmv, db * 64, k0, bh, &bars[B_VFULL]);
+        for (int db = 0; db < D / 64; ++db)
+          tma_load_3d(smem + L::kV + s * L::kTile + db * (BN * 128), &tmv, db * 64, k0, bh, &bars[B_VFULL0 + s]);
         ++vissued;
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    const uint32_t qs = smem_u32(smem + L::kQ), ks = smem_u32(smem + L::kK), vs = smem_u32(smem + L::kV);
+    const uint32_t qa = smem_u32(smem + L::kQA), qb = smem_u32(smem + L::kQB);
+    const uint32_t kbase = smem_u32(smem + L::kK), vbase = smem_u32(smem + L::kV);
     constexpr uint32_t id_s = idesc<T>(BM, BN, false);
     constexpr uint32_t id_pv = idesc<T>(BM, D, true);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_Q], 0, abort_flag));
-    for (int t = 0; ok && t < ntiles; ++t) {
-      const int k0 = klo + t * BN;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL], t & 1, abort_flag))) break;
+    auto issue_s = [&](int t, uint32_t q_s, uint32_t d_tmem) {
+      const uint32_t ks = kbase + (t & 1) * L::kTile;
+#pragma unroll
+      for (int k16 = 0; k16 < D / 16; ++k16) {
+        const uint32_t off = (k16 >> 2) * (BM * 128) + (k16 & 3) * 32;
+        mma_ss(d_tmem, sdesc(q_s + off, 16, 1024), sdesc(ks + off, 16, 1024), id_s, k16 > 0);
+      }
+    };
+    auto issue_pv = [&](int t, uint32_t p_tmem, uint32_t o_tmem) {
+      const uint32_t vs = vbase + (t & 1) * L::kTile;
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts(o_tmem, p_tmem + kk * 8, sdesc(vs + kk * 2048, BN * 128, 1024), id_pv, (t > 0 || kk > 0) ? 1u : 0u);
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_Q], 0, abort_flag)) &&
+              __all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0], 0, abort_flag));
+    if (ok) {
       tc_fence_after();
       if (lane == 0) {
-#pragma unroll
-        for (int ks16 = 0; ks16 < D / 16; ++ks16) {
-          const uint32_t off = (ks16 >> 2) * (BM * 128) + (ks16 & 3) * 32;
-          mma_ss(tS, sdesc(qs + off, 16, 1024), sdesc(ks + off, 16, 1024), id_s, ks16 > 0);
+        issue_s(0, qa, tmem + 0);
+        tc_commit(&bars[B_SFULL_A]);
+        if (has_b) {
+          issue_s(0, qb, tmem + 128);
+          tc_commit(&bars[B_SFULL_B]);
         }
-        tc_commit(&bars[B_SFULL]);
-        tc_commit(&bars[B_KFREE]);
+        tc_commit(&bars[B_KEMPTY0]);
       }
-      ++s_commits;
+      s_commits = 1;
       __syncwarp();
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL], t & 1, abort_flag))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL], t & 1, abort_flag))) break;
-      tc_fence_after();
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int s = t & 1, k0 = klo + t * BN;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL0 + s], (t >> 1) & 1, abort_flag))) break;
       if (k0 + BN > total) {  // stale slots may hold NaN/Inf: zero those V rows
         const int first = max(0, total - k0);
-        uint8_t *vbase = smem + L::kV;
+        uint8_t *vb = smem + L::kV + s * L::kTile;
         for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
           const int r = first + idx / (D / 8), ch = idx % (D / 8);
-          *reinterpret_cast<uint4 *>(vbase + (ch >> 3) * (BN * 128) + sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(vb + (ch >> 3) * (BN * 128) + sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_A], t & 1, abort_flag))) break;
+      tc_fence_after();
       if (lane == 0) {
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tO, tS + kk * 8, sdesc(vs + kk * 2048, BN * 128, 1024), id_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&bars[B_OFULL]);
-        tc_commit(&bars[B_VFREE]);
+        issue_pv(t, tmem + 0, tmem + 256);
+        tc_commit(&bars[B_OFULL_A]);
       }
       __syncwarp();
-      ++o_commits;
+      const bool next = t + 1 < ntiles;
+      if (next) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0 + (s ^ 1)], ((t + 1) >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(t + 1, qa, tmem + 0);
+          tc_commit(&bars[B_SFULL_A]);
+        }
+        __syncwarp();
+      }
+      if (has_b) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_B], t & 1, abort_flag))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(t, tmem + 128, tmem + 384);
+          tc_commit(&bars[B_OFULL_B]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) tc_commit(&bars[B_VEMPTY0 + s]);
+      o_commits = t + 1;
+      if (next) {
+        if (lane == 0) {
+          if (has_b) {
+            issue_s(t + 1, qb, tmem + 128);
+            tc_commit(&bars[B_SFULL_B]);
+          }
+          tc_commit(&bars[B_KEMPTY0 + (s ^ 1)]);
+        }
+        s_commits = t + 2;
+        __syncwarp();
+      }
     }
-  } else {
-    // ---------------------------------------------------------------- softmax warps
+  } else if (warp >= 4 && (warp < 8 || has_b)) {
+    // ---------------------------------------------------------------- softmax warpgroups
+    const int wg = (warp - 4) >> 2;  // 0: head A, 1: head B
+    const int hq = hA + wg;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // TMEM lane = query row within the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + wg * 128;
+    const uint32_t tO = tmem + lane_off + 256 + wg * 128;
+    uint64_t *sfull = &bars[B_SFULL_A + wg], *pfull = &bars[B_PFULL_A + wg], *ofull = &bars[B_OFULL_A + wg];
     const int qa = past + q0 + row;
     const float z2 = a.has_sink ? (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e : 0.f;
+    const float smul = a.score_mul, cmul = a.cap_mul;
     float m_ref = a.has_sink ? z2 : -INFINITY;  // reference max (log2 domain)
     float l = a.has_sink ? 1.f : 0.f;
     bool ok = true;
@@ -284,109 +352,103 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int k0 = klo + t * BN;
       const bool edge = !(k0 + BN - 1 < total && (!a.causal || k0 + BN - 1 <= qa_first) &&
                           (a.window < 0 || qa_last - k0 < a.window));
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_SFULL], t & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(sfull, t & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // pass 1: row max of the raw scores
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + lane_off + c * 32, r);
+      uint32_t r[BN];
+      {
+        uint32_t(&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+        uint32_t(&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+        uint32_t(&r2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[64]);
+        uint32_t(&r3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[96]);
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
         tmem_ld_wait();
+      }
+      if (edge) {  // band predicate on frontier tiles only
+        const int lo_vis = a.window > 0 ? qa - a.window + 1 : INT_MIN;
+        const int hi_vis = a.causal ? min(qa, total - 1) : total - 1;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(r[e]);
-          if (edge) {
-            const int key = k0 + c * 32 + e;
-            const bool vis = key < total && (!a.causal || key <= qa) && (a.window < 0 || qa - key < a.window);
-            x = vis ? x : -INFINITY;
-          }
-          mx = fmaxf(mx, x);
+        for (int e = 0; e < BN; ++e) {
+          const int key = k0 + e;
+          if (key < lo_vis || key > hi_vis) r[e] = __float_as_uint(-INFINITY);
         }
       }
+      float mx = __uint_as_float(r[0]);
+#pragma unroll
+      for (int e = 1; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
       float m_tile = -INFINITY;
-      if (mx != -INFINITY) m_tile = a.cap_mul != 0.f ? tanh_fast(mx * a.score_mul) * a.cap_mul : mx * a.score_mul;
-      // the rescale touches TMEM with warp-collective loads/stores: decide per warp, rows
-      // that did not need it rescale by 2^(m_ref - m_new) with m_new their own new max
+      if (mx != -INFINITY) m_tile = SOFTCAP ? tanh_fast(mx * smul) * cmul : mx * smul;
+      // lazy rescale: move the reference max only when it grows by more than 2^8
       const bool need = m_tile > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_tile != -INFINITY);
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? m_tile : m_ref;
-        const float alpha = need ? ex2(m_ref - m_new) : 1.f;  // 0 when m_ref = -inf
-        if (t > 0) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_OFULL], (t - 1) & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + lane_off + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, r);
-          }
-          tmem_st_wait();
-        }
-        l *= alpha;
-        m_ref = m_new;
-      }
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-      // pass 2: P = 2^(x - m_ref), row sum, P packed to the dtype into TMEM over S
+      const float m_new = need ? m_tile : m_ref;
+      const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32], pk[16];
-        tmem_ld32(tS + lane_off + c * 32, r);
-        tmem_ld_wait();
+      for (int half = 0; half < 2; ++half) {  // P in two halves keeps register pressure down
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
+        for (int e = 0; e < 64; e += 2) {
           float p2[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const float s = __uint_as_float(r[e + u]);
-            float x = a.cap_mul != 0.f ? tanh_fast(s * a.score_mul) * a.cap_mul : s * a.score_mul;
-            if (edge) {
-              const int key = k0 + c * 32 + e + u;
-              const bool vis = key < total && (!a.causal || key <= qa) && (a.window < 0 || qa - key < a.window);
-              x = vis ? x : -INFINITY;
-            }
-            p2[u] = ex2(x - m_use);
+            const float sv = __uint_as_float(r[half * 64 + e + u]);
+            const float x = SOFTCAP ? fmaf(tanh_fast(sv * smul), cmul, -m_use) : fmaf(sv, smul, -m_use);
+            p2[u] = ex2(x);
             rs += p2[u];
           }
           pk[e >> 1] = pack2<T>(p2[0], p2[1]);
         }
-        tmem_st16(tS + lane_off + c * 16, pk);
+        tmem_st32(tS + half * 32, pk);
+      }
+      l = l * alpha + rs;
+      m_ref = m_new;
+      if (__any_sync(0xffffffffu, need) && t > 0) {
+        // O holds PV of tiles < t: wait for the last of them, then scale it in TMEM
+        if (!__all_sync(0xffffffffu, mbar_wait(ofull, (t - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
       }
       tmem_st_wait();
-      l += rs;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_PFULL]);
+      if (lane == 0) mbar_arrive(pfull);
     }
     // epilogue: out = O / l
-    const bool fin = ok && !*abort_flag && mbar_wait(&bars[B_OFULL], (ntiles - 1) & 1, abort_flag);
+    const bool fin = ok && !*abort_flag && mbar_wait(ofull, (ntiles - 1) & 1, abort_flag);
     if (__all_sync(0xffffffffu, fin)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       T *orow = out + (((size_t)b * a.curr + q0 + row) * a.Hq + hq) * D;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tO + lane_off + c * 32, r);
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
         tmem_ld_wait();
         if (row < nrows) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 v;
-            v.x = pack2<T>(__uint_as_float(r[e + 0]) * inv, __uint_as_float(r[e + 1]) * inv);
-            v.y = pack2<T>(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
-            v.z = pack2<T>(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
-            v.w = pack2<T>(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
+            v.x = pack2<T>(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+            v.y = pack2<T>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            v.z = pack2<T>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            v.w = pack2<T>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
             *reinterpret_cast<uint4 *>(orow + c * 32 + e) = v;
           }
         }
@@ -401,13 +463,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     volatile int no_abort = 0;
     if (warp == 0 && lane == 0) {
       mbar_wait(&bars[B_Q], 0, &no_abort);
-      if (kissued) mbar_wait(&bars[B_KFULL], (kissued - 1) & 1, &no_abort);
-      if (vissued) mbar_wait(&bars[B_VFULL], (vissued - 1) & 1, &no_abort);
+      for (int t = max(0, kissued - 2); t < kissued; ++t) mbar_wait(&bars[B_KFULL0 + (t & 1)], (t >> 1) & 1, &no_abort);
+      for (int t = max(0, vissued - 2); t < vissued; ++t) mbar_wait(&bars[B_VFULL0 + (t & 1)], (t >> 1) & 1, &no_abort);
       report(a.status, GQA_DEV_TIMEOUT);
     }
     if (warp == 1 && lane == 0) {
-      if (s_commits) mbar_wait(&bars[B_SFULL], (s_commits - 1) & 1, &no_abort);
-      if (o_commits) mbar_wait(&bars[B_OFULL], (o_commits - 1) & 1, &no_abort);
+      if (s_commits) mbar_wait(&bars[B_SFULL_A], (s_commits - 1) & 1, &no_abort);
+      if (o_commits) mbar_wait(&bars[B_OFULL_A], (o_commits - 1) & 1, &no_abort);
+      if (has_b && o_commits) mbar_wait(&bars[B_OFULL_B], (o_commits - 1) & 1, &no_abort);
     }
   }
   if (warp == 1) {
@@ -417,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <typename T, int D> gqa_status launch_cfg(const Call &c, const PrefillArgs &a) {
+template <typename T, int D, bool SC> gqa_status launch_cfg(const Call &c, const PrefillArgs &a) {
   using L = PSmem<D>;
   const gqa_params &p = c.p;
   CUtensorMap tq, tk, tv;
@@ -425,10 +488,11 @@ template <typename T, int D> gqa_status launch_cfg(const Call &c, const PrefillA
   if (!encode_q_map(&tq, c.q, D, p.q_heads, p.q_len, p.batch, BM, 2)) return GQA_ERR_CUDA;
   if (!encode_kv_map(&tk, c.present_k, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
   if (!encode_kv_map(&tv, c.present_v, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
-  auto kern = prefill_tc_kernel<T, D>;
+  auto kern = prefill_tc_kernel<T, D, SC>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
-  dim3 grid(p.q_heads, (p.q_len + BM - 1) / BM, p.batch);
+  const int pairs = p.kv_heads * ((c.G + 1) / 2);
+  dim3 grid(pairs, (p.q_len + BM - 1) / BM, p.batch);
   kern<<<grid, kThreads, L::kAlloc, c.stream>>>(tq, tk, tv, a);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -452,15 +516,16 @@ template <typename T> gqa_status launch_t(const Call &c) {
   a.window = p.window;
   a.causal = p.causal;
   a.has_sink = (c.head_sink != nullptr) || p.smooth_softmax;
-  if (p.softcap > 0.f) {
+  const bool sc = p.softcap > 0.f;
+  if (sc) {
     a.score_mul = p.scale / p.softcap;
     a.cap_mul = p.softcap * kLog2e;
   } else {
     a.score_mul = p.scale * kLog2e;
     a.cap_mul = 0.f;
   }
-  if (p.head_dim == 128) return launch_cfg<T, 128>(c, a);
-  if (p.head_dim == 64) return launch_cfg<T, 64>(c, a);
+  if (p.head_dim == 128) return sc ? launch_cfg<T, 128, true>(c, a) : launch_cfg<T, 128, false>(c, a);
+  if (p.head_dim == 64) return sc ? launch_cfg<T, 64, true>(c, a) : launch_cfg<T, 64, false>(c, a);
   return GQA_ERR_UNSUPPORTED;
 }
 
