@@ -153,6 +153,27 @@ gqa_status gqa_rope_append_kv(const gqa_params *p, const void *q, const void *k,
                               const void *cos_cache, const void *sin_cache, void *q_rot, void *present_k,
                               void *present_v, int32_t *dev_status, void *stream);
 
+/* Decode without a workspace.  The paper has no counterpart: this entry point exists for
+ * callers that cannot allocate device memory where they run attention -- a plugin hosted by
+ * an inference engine that owns all device memory and gives its plugins no allocator, or a
+ * latency-critical loop in which a cudaMalloc (which can synchronize the device) is not
+ * acceptable.  Same arguments and semantics as gqa_attention_decode, without the workspace:
+ * the library keeps the scratch in one static device array of GQA_NOALLOC_SCRATCH_BYTES
+ * bytes, which every GPU that loads the library holds until the process exits.  Params
+ * that need more (gqa_workspace_bytes(p) > GQA_NOALLOC_SCRATCH_BYTES) return
+ * GQA_ERR_WORKSPACE with nothing launched.  The first call on each device looks up the
+ * array's device address with that device current; make that first call before any stream
+ * capture.  Every call clears the counters it relies on and reuses the same array, which
+ * keeps the previous call's contents, so calls that overlap on the GPU (other streams,
+ * other threads) race on it and must be serialized by the caller.  Nothing in this call
+ * allocates or frees memory. */
+#define GQA_NOALLOC_SCRATCH_BYTES (32u << 20)
+gqa_status gqa_attention_decode_noalloc(const gqa_params *p, const void *q, const void *k, const void *v,
+                                        const void *past_k, const void *past_v, const int32_t *seqlens_k,
+                                        const void *cos_cache, const void *sin_cache, const float *head_sink,
+                                        void *out, void *present_k, void *present_v, int32_t *dev_status,
+                                        void *stream);
+
 /* Static description of a status code. */
 const char *gqa_status_string(gqa_status s);
 

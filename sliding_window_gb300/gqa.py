@@ -32,7 +32,8 @@ DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decode", "gqa_rope_append_kv",
-            "gqa_status_string", "gqa_abi_version"]
+            "gqa_status_string", "gqa_abi_version", "gqa_attention_decode_noalloc"]
+NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES
 
 
 class GqaParams(ctypes.Structure):
@@ -65,6 +66,8 @@ def _load():
         fn.restype = i32
     lib.gqa_rope_append_kv.argtypes = [pp] + [vp] * 13
     lib.gqa_rope_append_kv.restype = i32
+    lib.gqa_attention_decode_noalloc.argtypes = [pp] + [vp] * 12 + [vp, vp]
+    lib.gqa_attention_decode_noalloc.restype = i32
     lib.gqa_status_string.argtypes = [i32]
     lib.gqa_status_string.restype = ctypes.c_char_p
     lib.gqa_abi_version.argtypes = []
@@ -135,6 +138,16 @@ def gqa_attention_decode(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_c
                                         _ptr(seqlens_k), _ptr(cos_cache), _ptr(sin_cache), _ptr(head_sink),
                                         _ptr(out), _ptr(present_k), _ptr(present_v), _ptr(workspace),
                                         _nbytes(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def gqa_attention_decode_noalloc(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink, out,
+                                 present_k, present_v, dev_status, stream=None) -> int:
+    """Decode with the library's static scratch instead of a workspace (for callers that
+    cannot allocate device memory; see include/gqa.h)."""
+    return int(lib.gqa_attention_decode_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(past_k),
+                                                _ptr(past_v), _ptr(seqlens_k), _ptr(cos_cache), _ptr(sin_cache),
+                                                _ptr(head_sink), _ptr(out), _ptr(present_k), _ptr(present_v),
+                                                _ptr(dev_status), _stream(stream)))
 
 
 def gqa_rope_append_kv(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, q_rot, present_k, present_v,
