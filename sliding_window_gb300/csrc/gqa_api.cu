@@ -97,20 +97,7 @@ DecodePlan decode_plan(const gqa_params &p) {
   const int G = p.q_heads / p.kv_heads;
   d.rows = G * p.q_len;
   d.mtiles = (d.rows + 15) / 16;
-  d.eligible = p.dtype != GQA_F32 &&
-               ((p.head_dim == 128 && d.mtiles <= 2) || (p.head_dim == 64 && d.mtiles <= 4));
-  // longest visible band of one (b, kv head): [max(0, past - W + 1), past + curr)
-  long long lmax = p.cap_present;
-  if (p.window > 0) lmax = std::min<long long>(lmax, (long long)p.window + p.q_len - 1);
-  d.lmax = (int)lmax;
-  // chunk size: spread the worst case over ~8 CTAs per SM of a 152-SM GB300, with chunks
-  // between 256 keys (per-CTA setup stays small) and 4096 keys (partials stay small)
-  const long long units = (long long)p.batch * p.kv_heads;
-  long long chunk = (lmax * units + 1215) / 1216;
-  chunk = (chunk + 63) / 64 * 64;
-  chunk = std::max<long long>(256, std::min<long long>(4096, chunk));
-  d.chunk = (int)chunk;
-  d.max_chunks = (int)((lmax + chunk - 1) / chunk);
+  d.eligible = p.dtype != GQA_F32 && (p.head_dim == 128 || p.head_dim == 64) && d.mtiles <= 2;
   return d;
 }
 
@@ -124,16 +111,17 @@ WsLayout workspace_layout(const gqa_params &p, bool need_q_rot) {
     off = align_up(off + w.q_rot_bytes, kAlign);
   }
   DecodePlan d = decode_plan(p);
-  if (d.eligible && d.max_chunks > 1) {
-    const size_t slots = (size_t)p.batch * p.kv_heads * d.max_chunks * d.rows;
+  if (d.eligible) {
+    const size_t groups = (size_t)p.batch * p.kv_heads;
+    const size_t slots = (size_t)kDecodeMaxCtas + groups;
     w.part_acc_off = off;
-    w.part_acc_bytes = slots * p.head_dim * sizeof(float);
+    w.part_acc_bytes = slots * d.rows * p.head_dim * sizeof(float);
     off = align_up(off + w.part_acc_bytes, kAlign);
     w.part_ml_off = off;
-    w.part_ml_bytes = slots * 2 * sizeof(float);
+    w.part_ml_bytes = slots * d.rows * 2 * sizeof(float);
     off = align_up(off + w.part_ml_bytes, kAlign);
     w.tickets_off = off;
-    w.tickets_bytes = (size_t)p.batch * p.kv_heads * sizeof(int32_t);
+    w.tickets_bytes = groups * sizeof(int32_t);
     off = align_up(off + w.tickets_bytes, kAlign);
   }
   w.total = off;
@@ -209,23 +197,29 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   const bool rotate = c.append && p->do_rotary;
   const WsLayout wl = workspace_layout(c.p, rotate);
   const DecodePlan dp = decode_plan(c.p);
-  const bool use_split = mode == kDecode && dp.eligible;
-  size_t need = (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
-  if (use_split && dp.max_chunks > 1) need = wl.total;
+  // the split decode kernel appends and rotates itself; every other path runs K1 first
+  const bool fused = mode == kDecode && dp.eligible;
+  size_t need = fused ? wl.total : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
   if (need > 0) {
     if (!workspace || !aligned16(workspace)) return GQA_ERR_WORKSPACE;
     if (workspace_bytes < need) return GQA_ERR_WORKSPACE;
   }
   c.ws = static_cast<char *>(workspace);
   c.ws_bytes = workspace_bytes;
+  if (fused) {
+    if (c.append && c.past_separate) {
+      s = launch_copy_past(c);
+      if (s != GQA_OK) return s;
+    }
+    return launch_decode_split(c, dp, wl);
+  }
   if (c.append) {
     c.q_rot = rotate ? c.ws + wl.q_rot_off : nullptr;
     s = launch_rope_append(c);
     if (s != GQA_OK) return s;
     if (rotate) c.q = c.q_rot;
   }
-  if (mode == kDecode) return use_split ? launch_decode_split(c, dp, wl) : launch_attention_simt(c);
-  if (p->dtype == GQA_F32) return launch_attention_simt(c);
+  if (mode == kDecode || p->dtype == GQA_F32) return launch_attention_simt(c);
   return launch_prefill_tc(c);
 }
 

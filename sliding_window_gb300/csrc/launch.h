@@ -33,15 +33,14 @@ struct Call {
   size_t ws_bytes = 0;
 };
 
-// Split-KV decode plan.  The visible keys of one (b, kv head) form one band of at most
-// Lmax slots; it is cut into chunks of `chunk` keys (a multiple of 64), one CTA each.
+// Split-KV decode plan.  The persistent decode kernel runs one CTA per SM (at most
+// kDecodeMaxCtas) over all groups' 128-key tiles; a group covered by several CTAs combines
+// through partial slots, of which there are at most grid + B*Hkv.
+constexpr int kDecodeMaxCtas = 1024;
 struct DecodePlan {
   bool eligible = false;  // tensor-core split kernel handles these params
-  int rows = 0;           // R = G * curr query rows per CTA
+  int rows = 0;           // R = G * curr query rows per item
   int mtiles = 0;         // ceil(R / 16)
-  int lmax = 0;           // longest possible visible band
-  int chunk = 0;          // keys per CTA
-  int max_chunks = 0;     // grid extent along the band
 };
 
 struct WsLayout {
@@ -66,6 +65,7 @@ bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B
 int device_sm_count();
 
 gqa_status launch_rope_append(const Call &c);
+gqa_status launch_copy_past(const Call &c);  // rows [0, past_b) of past into present only
 gqa_status launch_attention_simt(const Call &c);
 gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_prefill_tc(const Call &c);

@@ -127,6 +127,16 @@ __global__ void __launch_bounds__(256) copy_past_words_kernel(const uint4 *past_
   }
 }
 
+template <typename T> static gqa_status launch_copy_t(const Call &c) {
+  const gqa_params &p = c.p;
+  dim3 grid(p.batch * p.kv_heads, 16);
+  copy_past_words_kernel<T><<<grid, 256, 0, c.stream>>>(
+      reinterpret_cast<const uint4 *>(c.past_k), reinterpret_cast<const uint4 *>(c.past_v),
+      reinterpret_cast<uint4 *>(c.present_k), reinterpret_cast<uint4 *>(c.present_v), c.seqlens, p.kv_heads,
+      p.cap_past, p.cap_present, p.head_dim, p.q_len, p.rope_len, p.do_rotary);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
 template <typename T> static gqa_status launch_t(const Call &c) {
   const gqa_params &p = c.p;
   RopeArgs a;
@@ -151,18 +161,23 @@ template <typename T> static gqa_status launch_t(const Call &c) {
   a.do_rotary = p.do_rotary;
   a.past_separate = c.past_separate;
   if (c.past_separate) {
-    dim3 grid(p.batch * p.kv_heads, 16);
-    copy_past_words_kernel<T><<<grid, 256, 0, c.stream>>>(
-        reinterpret_cast<const uint4 *>(c.past_k), reinterpret_cast<const uint4 *>(c.past_v),
-        reinterpret_cast<uint4 *>(c.present_k), reinterpret_cast<uint4 *>(c.present_v), c.seqlens, p.kv_heads,
-        p.cap_past, p.cap_present, p.head_dim, p.q_len, p.rope_len, p.do_rotary);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    const gqa_status st = launch_copy_t<T>(c);
+    if (st != GQA_OK) return st;
   }
   constexpr int N = Vec<T>::N;
   int items = ((c.q_rot ? p.q_heads : 0) + 2 * p.kv_heads) * (p.head_dim / 2 / N);
   int threads = items >= 256 ? 256 : ((items + 31) / 32) * 32;
   rope_append_kernel<T><<<p.batch * p.q_len, threads, 0, c.stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status launch_copy_past(const Call &c) {
+  switch (c.p.dtype) {
+    case GQA_F32: return launch_copy_t<float>(c);
+    case GQA_F16: return launch_copy_t<__half>(c);
+    case GQA_BF16: return launch_copy_t<__nv_bfloat16>(c);
+  }
+  return GQA_ERR_INVALID_ARG;
 }
 
 gqa_status launch_rope_append(const Call &c) {

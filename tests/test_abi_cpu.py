@@ -127,22 +127,26 @@ def test_workspace_checked_before_launch(g):
     assert call(g, p, ws_bytes=need, workspace=FAKE + 8) == 5
 
 
+def decode_ws(B, Hkv, R, D):
+    """Split decode workspace: partial slots for up to 1024 CTAs plus one per (b, kv head)
+    group, fp32 acc [R][D] and (m, l) per slot, one ticket per group; 256-byte aligned."""
+    al = lambda x: (x + 255) // 256 * 256
+    slots = 1024 + B * Hkv
+    return al(slots * R * D * 4) + al(slots * R * 2 * 4) + al(B * Hkv * 4)
+
+
 def test_workspace_sizes(g):
-    # single-token windowed decode whose band fits one chunk needs no workspace
-    assert g.lib.gqa_workspace_bytes(ctypes.byref(good_params(g, window=200))) == 0
-    # rotary needs room for the rotated queries: B*curr*Hq*D*2 bytes, 256-aligned
-    p = good_params(g, do_rotary=1, rope_len=64, window=100)
-    assert g.lib.gqa_workspace_bytes(ctypes.byref(p)) == 2 * 1 * 8 * 128 * 2
-    # long decode: partials for every chunk slot, fp32 acc + (m, l) + a ticket per group
-    p = good_params(g, batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1)
-    ws = g.lib.gqa_workspace_bytes(ctypes.byref(p))
-    chunks = 32768 // 4096
-    rows = 8
-    slots = 64 * 8 * chunks * rows
-    assert ws >= slots * 128 * 4 + slots * 8 + 64 * 8 * 4
+    ws = lambda **kw: g.lib.gqa_workspace_bytes(ctypes.byref(good_params(g, **kw)))
+    # decode: B=2, Hq=8, Hkv=2 -> G=4, R=4 rows per group
+    assert ws(window=200) == decode_ws(2, 2, 4, 128)
+    # rotary adds room for the rotated queries (prefill path): B*curr*Hq*D*2 bytes
+    assert ws(do_rotary=1, rope_len=64, window=100) == 2 * 1 * 8 * 128 * 2 + decode_ws(2, 2, 4, 128)
+    # long decode: G=8, R=8
+    assert ws(batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1) == decode_ws(64, 8, 8, 128)
+    # more than 32 query rows per group at D=128: the SIMT kernel, no split workspace
+    assert ws(q_heads=64, kv_heads=2, q_len=2) == 0
     # prefill-sized q_len never needs decode partials
-    p = good_params(g, batch=2, q_heads=64, kv_heads=8, q_len=8192, cap_present=8192, window=4096)
-    assert g.lib.gqa_workspace_bytes(ctypes.byref(p)) == 0
+    assert ws(batch=2, q_heads=64, kv_heads=8, q_len=8192, cap_present=8192, window=4096) == 0
 
 
 def test_binding_refuses_host_tensors(g):

@@ -58,7 +58,7 @@ def test_noalloc_matches_workspace_decode_twice(case_id):
 
 def test_noalloc_rejects_params_beyond_its_scratch():
     from sliding_window_gb300 import gqa
-    p = gqa.params(batch=256, q_heads=64, kv_heads=8, head_dim=128, q_len=1, cap_present=65536, dtype="bf16")
+    p = gqa.params(batch=256, q_heads=64, kv_heads=8, head_dim=128, q_len=4, cap_present=65536, dtype="bf16")
     assert gqa.gqa_workspace_bytes(p) > gqa.NOALLOC_SCRATCH_BYTES
     dev = torch.device("cuda:0")
     dummy = torch.zeros(16, dtype=torch.uint8, device=dev)
