@@ -95,6 +95,7 @@ __device__ __forceinline__ int seq_tiles(const DecodeArgs &a, int b, int &past, 
 // One piece of one group handed to this CTA.
 struct Item {
   int b, h, past, lo, t0, n, j, parts;
+  long long slot0;  // partial slot of part 0 of this group (parts > 1 only)
 };
 
 // Walks this CTA's share [t_begin, t_end) of the global tile numbering, one item at a time.
@@ -154,9 +155,21 @@ struct ItemWalker {
     it.t0 = (int)(gtile - gstart);
     const long long stop = min(t_end, gstart + nt);
     it.n = (int)(stop - gtile);
-    const long long first = owner(gstart), last = owner(gstart + nt - 1);
-    it.parts = (int)(last - first + 1);
-    it.j = (int)(blockIdx.x - first);
+    const long long C = gridDim.x;
+    if (C >= T) {
+      // at most one tile per CTA: every tile of the group has its own owner, and the global
+      // tile index is a unique slot
+      it.parts = nt;
+      it.j = it.t0;
+      it.slot0 = gstart;
+    } else {
+      // every CTA owns at least one tile: the group's owners are consecutive CTAs, and
+      // first owner + group index is unique per group (< grid + B*Hkv)
+      const long long first = owner(gstart), last = owner(gstart + nt - 1);
+      it.parts = (int)(last - first + 1);
+      it.j = (int)(blockIdx.x - first);
+      it.slot0 = first + (long long)b * a->Hkv + h;
+    }
     gtile = stop;
     return true;
   }
@@ -561,8 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ---------------------------------------------------------- write the partial
-      // slots of group g: first owner + g + part (unique across groups, < gridDim.x + B*Hkv)
-      const size_t slot0 = (size_t)((long long)blockIdx.x - it.j + g);
+      const size_t slot0 = (size_t)it.slot0;
       {
         const size_t base = (slot0 + it.j) * R;
         float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * D);
