@@ -1,5 +1,5 @@
-// decode_split.cu -- K3 + K4: persistent split-KV decode with RoPE + append fused in and the
-// combine done by the last CTA of each (b, kv head) group.
+// decode_split.cu -- K3 + K4: split-KV decode with RoPE + append fused in and the combine
+// done by the last CTA of each (b, kv head) group.
 //
 // onnx-light-cpu "Attention Kernel Design": group_size = q_heads / kv_heads maps q heads
 // onto kv heads without repeating K or V ("Layouts and semantics"); the streaming
@@ -11,22 +11,23 @@
 // tract PR #2645, "What changed": the step's K (rotated) and V are appended to the cache at
 // seqlens_k and the query is rotated at the same positions; bottom-right band.
 //
-// Schedule (one GB300, HBM-bound): the visible band of group g = (b, kv head) is
-// [lo_b, total_b) with lo_b = max(0, past_b - window + 1), cut into 128-key tiles.  All
-// groups' tiles are numbered globally and the grid (one CTA per SM) takes equal contiguous
-// shares, so every SM streams about the same number of bytes and keeps ~192 KB of TMA
-// loads in flight from its first microsecond.  A share may cover the end of one group and
-// the start of the next: each covered piece is an "item".  Per item the CTA loads (and
-// rotates) the group's R = G*curr query rows, streams its tiles, and produces a partial
-// (m, l, acc); a group covered by one CTA finishes in place, otherwise the last CTA to
-// arrive (atomic ticket, no spin) adds the sink once, normalizes and writes the output.
+// Work decomposition (one GB300, HBM-bound): the visible band of group (b, kv head) is
+// [lo, total) with lo = max(0, past - window + 1); it is cut into S equal chunks (rounded
+// up to 64-key tiles, so no tile is read twice), one CTA each: CTA (chunk, kv head, b)
+// holds all R = G*curr query rows of the group and reads every K/V byte of its chunk once.
+// Each group's chunks are equal, so long and short sequences balance within a group; two
+// CTAs share an SM so one's prologue and epilogue overlap the other's streaming.
 //
-// Roles: warp 4 is the producer (TMA of K and V tiles through an NST-stage mbarrier ring;
-// before loading the tile that holds a group's new rows it writes them to present, K
-// rotated), warps 0-3 consume (each takes 32 keys of a tile, 16 at a time: S = Q K^T and
-// O += P V on mma.sync m16n8k16 with fp32 accumulation, exp2-domain online softmax with a
-// lazily rescaled reference max).  Five warps keep at most two per SM sub-partition, so
-// the consumers may hold all 255 registers.
+// Pipeline: four warps, each takes 16 keys of every 64-key tile: S = Q K^T and O += P V on
+// mma.sync m16n8k16 (fp32 accumulate), online softmax in the exp2 domain with a lazily
+// moved reference max.  K and V tiles arrive by TMA (128B swizzle) through an NST-stage
+// mbarrier ring; warp 0 refills a stage as soon as all four warps have released it, and
+// before loading the tile that holds the group's new rows it writes them to present (K
+// rotated) so the TMA reads them back.  The CTA merges its warps in shared memory; a
+// one-chunk group finishes in place, otherwise the CTA writes (m, l, acc) and the last CTA
+// of the group (atomic ticket, no spin-wait) adds the sink once, normalizes and writes out.
+// Launched with programmatic stream serialization: the prologue overlaps the previous
+// kernel's tail and griddepcontrol.wait orders every global read after it.
 #include <math.h>
 
 #include "common.cuh"
@@ -35,10 +36,9 @@
 namespace gqa {
 namespace {
 
-constexpr int KT = 128;  // keys per tile
-constexpr int kCW = 4;   // consumer warps (32 keys of a tile each, as two 16-key halves)
-constexpr int kThreads = (kCW + 1) * 32;
-constexpr int kConsumerThreads = kCW * 32;
+constexpr int KT = 64;         // keys per tile
+constexpr int kWarps = 4;      // 16 keys of a tile each
+constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleLog2 = 8.f;  // move the reference max only when it grows by > 2^8
 
 struct DecodeArgs {
@@ -49,12 +49,12 @@ struct DecodeArgs {
   void *out;              // [B, curr, Hq, D]
   const int32_t *seqlens;
   const float *head_sink;
-  float *part_acc;   // [slots][R][D]
-  float *part_ml;    // [slots][R][2]
-  int32_t *tickets;  // [B*Hkv]
+  float *part_acc;      // [B*Hkv][S][R][D]
+  float *part_ml;       // [B*Hkv][S][R][2]
+  int32_t *tickets;     // [B*Hkv]
   int32_t *status;
-  int B, Hq, Hkv, G, curr, R, cap, cap_past, past_separate, rope_len, do_rotary, append;
-  int window, causal, has_sink;
+  int Hq, Hkv, G, curr, R, cap, cap_past, past_separate, rope_len, do_rotary, append;
+  int window, causal, splits, has_sink;
   float score_mul;  // scale*log2(e), or scale/softcap with softcap
   float cap_mul;    // softcap*log2(e), 0 without softcap
 };
@@ -65,13 +65,13 @@ template <int D, int MT, int NST> struct Smem {
   static constexpr int kQRows = MT * 16;
   static constexpr int kStagesOff = 0;
   static constexpr int kQOff = NST * kStageBytes;
-  static constexpr int kAccOff = kQOff + kQRows * D * 2;         // merge buffer [QROWS][D] f32
-  static constexpr int kRedOff = kAccOff + kQRows * D * 4;        // red_m, red_l [kCW][QROWS]
-  static constexpr int kRowOff = kRedOff + 2 * kCW * kQRows * 4;  // row_m, row_l [QROWS]
-  static constexpr int kBarOff = kRowOff + 2 * kQRows * 4;        // full[NST], empty[NST]
-  static constexpr int kFlagOff = kBarOff + 2 * NST * 8;
+  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], empty[NST]
+  static constexpr int kRedOff = kBarOff + 2 * NST * 8;                   // red_m, red_l [4][QROWS]
+  static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l [QROWS]
+  static constexpr int kFlagOff = kRowOff + 2 * kQRows * 4;
   static constexpr int kBytes = kFlagOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+  static_assert(kQRows * D * 4 <= NST * kStageBytes, "merge buffer must fit in the stages");
 };
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -81,99 +81,6 @@ __device__ __forceinline__ void grid_launch_dependents() {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-
-// Tiles of every group of sequence b (0 for a rejected sequence) and its band start.
-__device__ __forceinline__ int seq_tiles(const DecodeArgs &a, int b, int &past, int &lo) {
-  past = a.seqlens[b];
-  lo = 0;
-  if (sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append, a.rope_len))
-    return 0;
-  lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
-  return (past + a.curr - lo + KT - 1) / KT;
-}
-
-// One piece of one group handed to this CTA.
-struct Item {
-  int b, h, past, lo, t0, n, j, parts;
-  long long slot0;  // partial slot of part 0 of this group (parts > 1 only)
-};
-
-// Walks this CTA's share [t_begin, t_end) of the global tile numbering, one item at a time.
-// Producer and consumers each run their own copy; it reads only seqlens_k.
-struct ItemWalker {
-  const DecodeArgs *a;
-  long long T, t_end, gtile;  // gtile: next global tile to hand out
-  int b, h, nt, past, lo;
-  long long gstart;  // global index of tile 0 of group (b, h)
-
-  __device__ void init(const DecodeArgs &args) {
-    a = &args;
-    T = 0;
-    for (int bb = 0; bb < a->B; ++bb) {
-      int p, l;
-      T += (long long)a->Hkv * seq_tiles(*a, bb, p, l);
-    }
-    const long long C = gridDim.x;
-    gtile = (blockIdx.x * T + C - 1) / C;
-    t_end = ((blockIdx.x + 1) * T + C - 1) / C;
-    b = 0;
-    h = 0;
-    gstart = 0;
-    nt = 0;
-    past = 0;
-    lo = 0;
-    if (gtile >= t_end) return;
-    for (; b < a->B; ++b) {  // locate the group holding the first tile of the share
-      nt = seq_tiles(*a, b, past, lo);
-      const long long span = (long long)a->Hkv * nt;
-      if (gtile < gstart + span) {
-        h = (int)((gtile - gstart) / nt);
-        gstart += (long long)h * nt;
-        return;
-      }
-      gstart += span;
-    }
-  }
-  // CTA owning global tile t: tile t belongs to floor(t * C / T)
-  __device__ long long owner(long long t) const { return t * (long long)gridDim.x / T; }
-  __device__ bool next(Item &it) {
-    if (gtile >= t_end) return false;
-    while (gtile >= gstart + nt) {  // advance to the group holding gtile
-      gstart += nt;
-      if (++h == a->Hkv) {
-        h = 0;
-        do {
-          ++b;
-          nt = seq_tiles(*a, b, past, lo);
-        } while (nt == 0);
-      }
-    }
-    it.b = b;
-    it.h = h;
-    it.past = past;
-    it.lo = lo;
-    it.t0 = (int)(gtile - gstart);
-    const long long stop = min(t_end, gstart + nt);
-    it.n = (int)(stop - gtile);
-    const long long C = gridDim.x;
-    if (C >= T) {
-      // at most one tile per CTA: every tile of the group has its own owner, and the global
-      // tile index is a unique slot
-      it.parts = nt;
-      it.j = it.t0;
-      it.slot0 = gstart;
-    } else {
-      // every CTA owns at least one tile: the group's owners are consecutive CTAs, and
-      // first owner + group index is unique per group (< grid + B*Hkv)
-      const long long first = owner(gstart), last = owner(gstart + nt - 1);
-      it.parts = (int)(last - first + 1);
-      it.j = (int)(blockIdx.x - first);
-      it.slot0 = first + (long long)b * a->Hkv + h;
-    }
-    gtile = stop;
-    return true;
-  }
-};
 
 template <typename T>
 __device__ __forceinline__ void rotate8(const T *x1p, const T *x2p, const T *cp, const T *sp, uint4 &o1, uint4 &o2) {
@@ -190,8 +97,40 @@ __device__ __forceinline__ void rotate8(const T *x1p, const T *x2p, const T *cp,
   }
 }
 
+// Warp-wide: write the step's rows [r0, r1) of kv head h of sequence b to present (K
+// rotated when do_rotary), then make the generic-proxy stores visible to TMA reads.
+template <typename T, int D>
+__device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, int past, int r0, int r1, int lane) {
+  const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
+  T *pk = reinterpret_cast<T *>(a.present_k), *pv = reinterpret_cast<T *>(a.present_v);
+  const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
+  constexpr int per_row = D / 16;  // pairs of 8-element chunks (x[d..], x[d+D/2..]) per row
+  const int nrows = r1 - r0;
+  for (int w = lane; w < nrows * per_row * 2; w += 32) {
+    const int which = w / (nrows * per_row);  // 0: k, 1: v
+    const int rr = (w / per_row) % nrows, c = (w % per_row) * 8;
+    const int pos = r0 + rr, i = pos - past;
+    const size_t src = (((size_t)b * a.curr + i) * a.Hkv + h) * D;
+    const size_t dst = (((size_t)b * a.Hkv + h) * a.cap + pos) * D;
+    if (which == 0 && a.do_rotary) {
+      uint4 y1, y2;
+      rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c,
+                 y1, y2);
+      *reinterpret_cast<uint4 *>(pk + dst + c) = y1;
+      *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = y2;
+    } else {
+      const T *x = which == 0 ? kin : vin;
+      T *y = which == 0 ? pk : pv;
+      *reinterpret_cast<uint4 *>(y + dst + c) = *reinterpret_cast<const uint4 *>(x + src + c);
+      *reinterpret_cast<uint4 *>(y + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(x + src + D / 2 + c);
+    }
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+}
+
 template <typename T, int D, int MT, int NST>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         DecodeArgs a) {
   using L = Smem<D, MT, NST>;
@@ -202,463 +141,425 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *stages = smem + L::kStagesOff;
   uint8_t *qs = smem + L::kQOff;
-  float *accbuf = reinterpret_cast<float *>(smem + L::kAccOff);
-  float *red_m = reinterpret_cast<float *>(smem + L::kRedOff);
-  float *red_l = red_m + kCW * QROWS;
-  float *row_m = reinterpret_cast<float *>(smem + L::kRowOff);
-  float *row_l = row_m + QROWS;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
   uint64_t *empty = full + NST;
+  float *red_m = reinterpret_cast<float *>(smem + L::kRedOff);
+  float *red_l = red_m + kWarps * QROWS;
+  float *row_m = reinterpret_cast<float *>(smem + L::kRowOff);
+  float *row_l = row_m + QROWS;
   volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlagOff);  // [0] abort, [1] last
 
+  const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = a.R;
   T *out = reinterpret_cast<T *>(a.out);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCW);
+      mbar_init(&empty[s], kWarps);
     }
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
-  }
-  if (warp == kCW && lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
-  // programmatic dependent launch: everything above may overlap the previous kernel; every
+  // programmatic dependent launch: the setup above may overlap the previous kernel; every
   // global read below must see its results
   grid_dependency_wait();
   __syncthreads();
 
-  ItemWalker walk;
-  walk.init(a);
-
-  if (warp == kCW) {
-    // ------------------------------------------------------------ producer warp
-    int tiles = 0;
-    bool ok = true;
-    Item it;
-    while (ok && walk.next(it)) {
-      const int bh = it.b * a.Hkv + it.h;
-      const int total = it.past + a.curr;
-      for (int t = it.t0; t < it.t0 + it.n; ++t) {
-        const int s = tiles % NST;
-        if (tiles >= NST && !__all_sync(0xffffffffu, mbar_wait(&empty[s], ((tiles / NST) - 1) & 1, flags))) {
-          ok = false;
-          break;
-        }
-        const int k0 = it.lo + t * KT;
-        if (a.append && k0 + KT > it.past && k0 < total) {
-          // this tile holds new rows: write them to present first (K rotated), then make the
-          // generic-proxy stores visible to the TMA reads below
-          const int r0 = max(it.past, k0), r1 = min(total, k0 + KT);
-          const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
-          T *pk = reinterpret_cast<T *>(a.present_k), *pv = reinterpret_cast<T *>(a.present_v);
-          const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
-          constexpr int per_row = D / 16;  // 8-element pairs (x[d], x[d + D/2]) per row
-          const int nrows = r1 - r0;
-          for (int w = lane; w < nrows * per_row * 2; w += 32) {
-            const int which = w / (nrows * per_row);  // 0: k, 1: v
-            const int rr = (w / per_row) % nrows, c = (w % per_row) * 8;
-            const int pos = r0 + rr, i = pos - it.past;
-            const size_t src = (((size_t)it.b * a.curr + i) * a.Hkv + it.h) * D;
-            const size_t dst = ((size_t)bh * a.cap + pos) * D;
-            if (which == 0 && a.do_rotary) {
-              uint4 y1, y2;
-              rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c,
-                         sn + (size_t)pos * (D / 2) + c, y1, y2);
-              *reinterpret_cast<uint4 *>(pk + dst + c) = y1;
-              *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = y2;
-            } else {
-              const T *x = which == 0 ? kin : vin;
-              T *y = which == 0 ? pk : pv;
-              *reinterpret_cast<uint4 *>(y + dst + c) = *reinterpret_cast<const uint4 *>(x + src + c);
-              *reinterpret_cast<uint4 *>(y + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(x + src + D / 2 + c);
-            }
-          }
-          fence_proxy_async_global();
-          __syncwarp();
-        }
-        if (lane == 0) {
-          mbar_expect_tx(&full[s], L::kStageBytes);
-          uint8_t *kdst = stages + s * L::kStageBytes;
-          uint8_t *vdst = kdst + L::kTileBytes;
-#pragma unroll
-          for (int db = 0; db < D / 64; ++db) {
-            tma_load_3d(kdst + db * (KT * 128), &tmk, db * 64, k0, bh, &full[s]);
-            tma_load_3d(vdst + db * (KT * 128), &tmv, db * 64, k0, bh, &full[s]);
-          }
-        }
-        __syncwarp();
-        ++tiles;
+  const int past = a.seqlens[b];
+  const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
+                                 a.rope_len);
+  if (st) {  // rejected sequence: zeros, nothing appended, reported once
+    if (split == 0) {
+      if (threadIdx.x == 0 && hkv == 0) report(a.status, st);
+      for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+        const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
+        out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
       }
     }
-    if (lane == 0 && flags[0]) {
-      // drain: every copy issued must land before the CTA may exit
+    return;
+  }
+  const int total = past + a.curr;
+  const int lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
+  const int len = total - lo;
+  const int chunk = ((len + a.splits - 1) / a.splits + KT - 1) / KT * KT;  // this group's chunk
+  const int nchunks = (len + chunk - 1) / chunk;
+  if (split >= nchunks) return;  // whole CTA idle (uniform)
+  const int c0 = lo + split * chunk;
+  const int c1 = min(total, c0 + chunk);
+  const int ntiles = (c1 - c0 + KT - 1) / KT;
+  const int bh = b * a.Hkv + hkv;
+  const bool appends = a.append && c1 > past;  // this chunk holds new rows [past, total)
+
+  // warp 0 fills the ring; the new rows go to present before the tile that holds them
+  auto issue = [&](int t) {
+    const int s = t % NST, k0 = c0 + t * KT;
+    if (appends && k0 + KT > past && k0 < total)
+      append_rows<T, D>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane);
+    if (lane == 0) {
+      mbar_expect_tx(&full[s], L::kStageBytes);
+      uint8_t *kdst = stages + s * L::kStageBytes;
+      uint8_t *vdst = kdst + L::kTileBytes;
+#pragma unroll
+      for (int db = 0; db < D / 64; ++db) {
+        tma_load_3d(kdst + db * (KT * 128), &tmk, db * 64, k0, bh, &full[s]);
+        tma_load_3d(vdst + db * (KT * 128), &tmv, db * 64, k0, bh, &full[s]);
+      }
+    }
+    __syncwarp();
+  };
+  int issued = 0;
+  if (warp == 0)
+    for (; issued < min(NST, ntiles); ++issued) issue(issued);
+
+  // Q rows r = i*G + g (token i, q head hkv*G + g), rotated at past + i, 128B-swizzled
+  {
+    const T *q = reinterpret_cast<const T *>(a.q);
+    const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
+    const bool rot = a.do_rotary && a.append;
+    for (int idx = threadIdx.x; idx < QROWS * (DCH / 2); idx += kThreads) {
+      const int r = idx / (DCH / 2), c = idx % (DCH / 2);  // chunk c of the first half
+      uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
+      if (r < R) {
+        const int i = r / a.G, g = r % a.G;
+        const T *src = q + (((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D;
+        if (rot) {
+          const size_t pos = (size_t)(past + i) * (D / 2);
+          rotate8<T>(src + c * 8, src + D / 2 + c * 8, cs + pos + c * 8, sn + pos + c * 8, y1, y2);
+        } else {
+          y1 = *reinterpret_cast<const uint4 *>(src + c * 8);
+          y2 = *reinterpret_cast<const uint4 *>(src + D / 2 + c * 8);
+        }
+      }
+      const int c2 = c + DCH / 2;
+      *reinterpret_cast<uint4 *>(qs + (c >> 3) * (QROWS * 128) + sw128(r, c & 7)) = y1;
+      *reinterpret_cast<uint4 *>(qs + (c2 >> 3) * (QROWS * 128) + sw128(r, c2 & 7)) = y2;
+    }
+  }
+  __syncthreads();
+
+  float m[MT][2], l[MT][2];
+  float acc[MT][D / 8][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      m[mt][h] = -INFINITY;
+      l[mt][h] = 0.f;
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][dn][e] = 0.f;
+  }
+  const uint32_t qs_u32 = smem_u32(qs);
+  const int q_abs_min = past, q_abs_max = past + a.curr - 1;
+  bool aborted = false;
+  int t_fail = ntiles;
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % NST;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (t / NST) & 1, flags))) {
+      aborted = true;
+      t_fail = t;
+      break;
+    }
+    const int kb = c0 + t * KT + 16 * warp;  // this warp's first key
+    const uint32_t ks_u32 = smem_u32(stages + s * L::kStageBytes);
+    const uint32_t vs_u32 = ks_u32 + L::kTileBytes;
+
+    // ---- S = Q K^T over this warp's 16 keys
+    float sacc[MT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][n][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t kb0, kb1, kb2, kb3;
+      {
+        const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
+        const int kch = 2 * ks + ((lane >> 3) & 1);
+        ldsm_x4(ks_u32 + (kch >> 3) * (KT * 128) + sw128(krow, kch & 7), kb0, kb1, kb2, kb3);
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t af[4];
+        const int qrow = 16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int qch = 2 * ks + (lane >> 4);
+        ldsm_x4(qs_u32 + (qch >> 3) * (QROWS * 128) + sw128(qrow, qch & 7), af[0], af[1], af[2], af[3]);
+        M::run(sacc[mt][0], af, kb0, kb1);
+        M::run(sacc[mt][1], af, kb2, kb3);
+      }
+    }
+
+    // ---- scale, softcap, band mask (only on warps whose keys cross a frontier)
+    const bool edge = !(kb >= c0 && kb + 15 < c1 && (!a.causal || kb + 15 <= q_abs_min) &&
+                        (a.window < 0 || q_abs_max - kb < a.window));
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x = sacc[mt][n][e];
+          x = a.cap_mul != 0.f ? tanh_fast(x * a.score_mul) * a.cap_mul : x * a.score_mul;
+          if (edge) {
+            const int row = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
+            const int key = kb + 8 * n + 2 * (lane & 3) + (e & 1);
+            const int qa = past + row / a.G;
+            const bool vis = row < R && key >= c0 && key < c1 && (!a.causal || key <= qa) &&
+                             (a.window < 0 || qa - key < a.window);
+            if (!vis) x = -INFINITY;
+          }
+          sacc[mt][n][e] = x;
+        }
+
+    // ---- online softmax, reference max moved lazily (rows lane/4 and lane/4 + 8)
+    uint32_t pa[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float p[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float mx = fmaxf(fmaxf(sacc[mt][0][2 * h], sacc[mt][0][2 * h + 1]),
+                         fmaxf(sacc[mt][1][2 * h], sacc[mt][1][2 * h + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if (mx > m[mt][h] + kRescaleLog2 || (m[mt][h] == -INFINITY && mx != -INFINITY)) {
+          const float alpha = ex2(m[mt][h] - mx);  // 0 while nothing was visible
+          l[mt][h] *= alpha;
+#pragma unroll
+          for (int dn = 0; dn < D / 8; ++dn) {
+            acc[mt][dn][2 * h] *= alpha;
+            acc[mt][dn][2 * h + 1] *= alpha;
+          }
+          m[mt][h] = mx;
+        }
+        const float m_use = m[mt][h] == -INFINITY ? 0.f : m[mt][h];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float pv = ex2(sacc[mt][n][2 * h + e] - m_use);
+            p[n][2 * h + e] = pv;
+            l[mt][h] += pv;
+          }
+      }
+      pa[mt][0] = M::pack(p[0][0], p[0][1]);
+      pa[mt][1] = M::pack(p[0][2], p[0][3]);
+      pa[mt][2] = M::pack(p[1][0], p[1][1]);
+      pa[mt][3] = M::pack(p[1][2], p[1][3]);
+    }
+
+    // ---- stale V rows (slots >= total) may hold NaN/Inf: zero them so 0 * V stays 0
+    const bool stale = kb + 16 > total;
+    if (stale) {
+      const int first = max(0, total - kb);
+      for (int idx = lane; idx < (16 - first) * DCH; idx += 32) {
+        const int r = 16 * warp + first + idx / DCH, ch = idx % DCH;
+        *reinterpret_cast<uint4 *>(stages + s * L::kStageBytes + L::kTileBytes + (ch >> 3) * (KT * 128) +
+                                   sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+
+    // ---- O += P V over this warp's 16 keys
+#pragma unroll
+    for (int dd = 0; dd < D / 16; ++dd) {
+      uint32_t v0, v1, v2, v3;
+      const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
+      const int vch = 2 * dd + (lane >> 4);
+      ldsm_x4_t(vs_u32 + (vch >> 3) * (KT * 128) + sw128(vrow, vch & 7), v0, v1, v2, v3);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        M::run(acc[mt][2 * dd], pa[mt], v0, v1);
+        M::run(acc[mt][2 * dd + 1], pa[mt], v2, v3);
+      }
+    }
+    if (stale) fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    // warp 0 refills the stage once all four warps are done with it
+    if (warp == 0 && issued < ntiles) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], (t / NST) & 1, flags))) {
+        aborted = true;
+        t_fail = t + 1;
+        break;
+      }
+      issue(issued++);
+    }
+  }
+
+  // -------------------------------------------------------------- merge the 4 warps
+  // one decision for the whole CTA: a timed-out wait anywhere aborts it
+  aborted = named_bar_or(1, kThreads, aborted || flags[0] != 0);
+  if (threadIdx.x == 0) grid_launch_dependents();  // streaming done: let the next kernel launch
+  if (aborted) {
+    // copies in flight must land before the CTA exits; take part in the ticket so the
+    // group's counter stays consistent, write nothing
+    if (threadIdx.x == 0) {
       volatile int no_abort = 0;
-      for (int t = max(0, tiles - NST); t < tiles; ++t) mbar_wait(&full[t % NST], (t / NST) & 1, &no_abort);
+      for (int t = t_fail; t < min(issued, t_fail + NST); ++t) mbar_wait(&full[t % NST], (t / NST) & 1, &no_abort);
       report(a.status, GQA_DEV_TIMEOUT);
+      if (nchunks > 1) {
+        __threadfence();
+        const int old = atomicAdd(&a.tickets[bh], 1);
+        if (old == nchunks - 1) a.tickets[bh] = 0;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float lv = l[mt][h];
+      lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+      lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+      if ((lane & 3) == 0) {
+        const int row = 16 * mt + (lane >> 2) + 8 * h;
+        red_m[warp * QROWS + row] = m[mt][h];
+        red_l[warp * QROWS + row] = lv;
+      }
+    }
+  __syncthreads();
+  if (threadIdx.x < QROWS) {
+    const int row = threadIdx.x;
+    float mm = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, red_m[w * QROWS + row]);
+    const float mu = mm == -INFINITY ? 0.f : mm;
+    float ll = 0.f;
+    for (int w = 0; w < kWarps; ++w) ll += red_l[w * QROWS + row] * ex2(red_m[w * QROWS + row] - mu);
+    row_m[row] = mm;
+    row_l[row] = ll;
+  }
+  __syncthreads();
+  float *accbuf = reinterpret_cast<float *>(stages);  // [QROWS][D]; every stage was consumed
+  // warps add their rescaled accumulators one after another (fixed order: deterministic)
+  for (int w = 0; w < kWarps; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = 16 * mt + (lane >> 2) + 8 * h;
+          const float mm = row_m[row];
+          const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
+#pragma unroll
+          for (int dn = 0; dn < D / 8; ++dn) {
+            float2 *dst = reinterpret_cast<float2 *>(&accbuf[row * D + 8 * dn + 2 * (lane & 3)]);
+            const float2 prev = w == 0 ? make_float2(0.f, 0.f) : *dst;
+            *dst = make_float2(prev.x + acc[mt][dn][2 * h] * f, prev.y + acc[mt][dn][2 * h + 1] * f);
+          }
+        }
+    }
+    __syncthreads();
+  }
+
+  if (nchunks == 1) {
+    // ------------------------------------------------------------ finish in place
+    for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+      const int r = idx / D, d = idx % D;
+      const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
+      const float mm = row_m[r];
+      float num = 0.f, den = 1.f;
+      if (mm != -INFINITY) {
+        float top = mm, sink_term = 0.f;
+        if (a.has_sink) {
+          const float z = (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e;
+          top = fmaxf(mm, z);
+          sink_term = ex2(z - top);
+        }
+        const float f = ex2(mm - top);
+        num = accbuf[idx] * f;
+        den = row_l[r] * f + sink_term;
+      }
+      out[(((size_t)b * a.curr + i) * a.Hq + hq) * D + d] = from_f32<T>(num / den);
     }
     return;
   }
 
-  // -------------------------------------------------------------- consumer warps
-  const int cw = warp;
-  const int ct = threadIdx.x;  // 0..127
-  // rejected sequences: zeros, reported once (spread over the grid)
-  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-    const int past = a.seqlens[b];
-    const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
-                                   a.rope_len);
-    if (!st) continue;
-    if (ct == 0) report(a.status, st);
-    const size_t n = (size_t)a.curr * a.Hq * D;
-    for (size_t idx = ct; idx < n; idx += kConsumerThreads) out[(size_t)b * n + idx] = from_f32<T>(0.f);
+  // -------------------------------------------------------------- write the partial
+  const size_t gbase = (size_t)bh * a.splits * R;
+  {
+    const size_t base = gbase + (size_t)split * R;
+    float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * D);
+    const float4 *src = reinterpret_cast<const float4 *>(accbuf);
+    for (int idx = threadIdx.x; idx < R * D / 4; idx += kThreads) pacc[idx] = src[idx];
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+      a.part_ml[(base + r) * 2] = row_m[r];
+      a.part_ml[(base + r) * 2 + 1] = row_l[r];
+    }
   }
-
-  const uint32_t qs_u32 = smem_u32(qs);
-  int tiles = 0;
-  bool aborted = false;
-  Item it, nx;
-  bool more = walk.next(it);
-  while (more) {
-    const int total = it.past + a.curr;
-    const int g = it.b * a.Hkv + it.h;
-    // ---- Q rows r = i*G + gg (token i, q head h*G + gg), rotated at past + i, 128B-swizzled
-    {
-      const T *q = reinterpret_cast<const T *>(a.q);
-      const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
-      const bool rot = a.do_rotary && a.append;
-      for (int idx = ct; idx < QROWS * (DCH / 2); idx += kConsumerThreads) {
-        const int r = idx / (DCH / 2), c = idx % (DCH / 2);  // chunk c of the first half
-        uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
-        if (r < R) {
-          const int i = r / a.G, gg = r % a.G;
-          const T *src = q + (((size_t)it.b * a.curr + i) * a.Hq + it.h * a.G + gg) * D;
-          if (rot) {
-            const size_t pos = (size_t)(it.past + i) * (D / 2);
-            rotate8<T>(src + c * 8, src + D / 2 + c * 8, cs + pos + c * 8, sn + pos + c * 8, y1, y2);
-          } else {
-            y1 = *reinterpret_cast<const uint4 *>(src + c * 8);
-            y2 = *reinterpret_cast<const uint4 *>(src + D / 2 + c * 8);
-          }
-        }
-        const int c2 = c + DCH / 2;
-        *reinterpret_cast<uint4 *>(qs + (c >> 3) * (QROWS * 128) + sw128(r, c & 7)) = y1;
-        *reinterpret_cast<uint4 *>(qs + (c2 >> 3) * (QROWS * 128) + sw128(r, c2 & 7)) = y2;
-      }
-    }
-    named_bar_sync(1, kConsumerThreads);
-
-    float m[MT][2], l[MT][2];
-    float acc[MT][D / 8][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        m[mt][h] = -INFINITY;
-        l[mt][h] = 0.f;
-      }
-#pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][dn][e] = 0.f;
-    }
-    const int q_abs_min = it.past, q_abs_max = it.past + a.curr - 1;
-
-    for (int t = it.t0; t < it.t0 + it.n; ++t, ++tiles) {
-      const int s = tiles % NST;
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (tiles / NST) & 1, flags))) {
-        aborted = true;
-        break;
-      }
-      const uint32_t ks_u32 = smem_u32(stages + s * L::kStageBytes);
-      const uint32_t vs_u32 = ks_u32 + L::kTileBytes;
-      bool stale_any = false;
-#pragma unroll 1
-      for (int sub = 0; sub < 2; ++sub) {
-      const int kr = 32 * cw + 16 * sub;  // this half's first row within the tile
-      const int kb = it.lo + t * KT + kr;  // and its first key
-
-      // ---- S = Q K^T over this warp's 16 keys
-      float sacc[MT][2][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[mt][nn][e] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t kb0, kb1, kb2, kb3;
-        {
-          const int krow = kr + ((lane >> 4) << 3) + (lane & 7);
-          const int kch = 2 * ks + ((lane >> 3) & 1);
-          ldsm_x4(ks_u32 + (kch >> 3) * (KT * 128) + sw128(krow, kch & 7), kb0, kb1, kb2, kb3);
-        }
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          uint32_t af[4];
-          const int qrow = 16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7);
-          const int qch = 2 * ks + (lane >> 4);
-          ldsm_x4(qs_u32 + (qch >> 3) * (QROWS * 128) + sw128(qrow, qch & 7), af[0], af[1], af[2], af[3]);
-          M::run(sacc[mt][0], af, kb0, kb1);
-          M::run(sacc[mt][1], af, kb2, kb3);
-        }
-      }
-
-      // ---- scale, softcap, band mask (only on warps whose keys cross a frontier)
-      const bool edge = !(kb + 15 < total && (!a.causal || kb + 15 <= q_abs_min) &&
-                          (a.window < 0 || q_abs_max - kb < a.window));
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float x = sacc[mt][nn][e];
-            x = a.cap_mul != 0.f ? tanh_fast(x * a.score_mul) * a.cap_mul : x * a.score_mul;
-            if (edge) {
-              const int row = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
-              const int key = kb + 8 * nn + 2 * (lane & 3) + (e & 1);
-              const int qa = it.past + row / a.G;
-              const bool vis = row < R && key < total && (!a.causal || key <= qa) &&
-                               (a.window < 0 || qa - key < a.window);
-              if (!vis) x = -INFINITY;
-            }
-            sacc[mt][nn][e] = x;
-          }
-
-      // ---- online softmax with a lazily moved reference max (rows lane/4 and lane/4 + 8)
-      uint32_t pa[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        float p[2][4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float mx = fmaxf(fmaxf(sacc[mt][0][2 * h], sacc[mt][0][2 * h + 1]),
-                           fmaxf(sacc[mt][1][2 * h], sacc[mt][1][2 * h + 1]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const bool need = mx > m[mt][h] + kRescaleLog2 || (m[mt][h] == -INFINITY && mx != -INFINITY);
-          if (need) {
-            const float alpha = ex2(m[mt][h] - mx);  // 0 while nothing was visible
-            l[mt][h] *= alpha;
-#pragma unroll
-            for (int dn = 0; dn < D / 8; ++dn) {
-              acc[mt][dn][2 * h] *= alpha;
-              acc[mt][dn][2 * h + 1] *= alpha;
-            }
-            m[mt][h] = mx;
-          }
-          const float m_use = m[mt][h] == -INFINITY ? 0.f : m[mt][h];
-#pragma unroll
-          for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float pv = ex2(sacc[mt][nn][2 * h + e] - m_use);
-              p[nn][2 * h + e] = pv;
-              l[mt][h] += pv;
-            }
-        }
-        pa[mt][0] = M::pack(p[0][0], p[0][1]);
-        pa[mt][1] = M::pack(p[0][2], p[0][3]);
-        pa[mt][2] = M::pack(p[1][0], p[1][1]);
-        pa[mt][3] = M::pack(p[1][2], p[1][3]);
-      }
-
-      // ---- stale V rows (slots >= total) may hold NaN/Inf: zero them so 0 * V stays 0
-      const bool stale = kb + 16 > total;
-      if (stale) {
-        const int first = max(0, total - kb);
-        for (int idx = lane; idx < (16 - first) * DCH; idx += 32) {
-          const int r = kr + first + idx / DCH, ch = idx % DCH;
-          *reinterpret_cast<uint4 *>(stages + s * L::kStageBytes + L::kTileBytes + (ch >> 3) * (KT * 128) +
-                                     sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-
-      // ---- O += P V over this warp's 16 keys
-#pragma unroll
-      for (int dd = 0; dd < D / 16; ++dd) {
-        uint32_t v0, v1, v2, v3;
-        const int vrow = kr + ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int vch = 2 * dd + (lane >> 4);
-        ldsm_x4_t(vs_u32 + (vch >> 3) * (KT * 128) + sw128(vrow, vch & 7), v0, v1, v2, v3);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          M::run(acc[mt][2 * dd], pa[mt], v0, v1);
-          M::run(acc[mt][2 * dd + 1], pa[mt], v2, v3);
-        }
-      }
-      stale_any |= stale;
-      }
-      if (stale_any) fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-
-    // one decision for all consumer warps: a timed-out wait anywhere aborts the CTA
-    aborted = named_bar_or(1, kConsumerThreads, aborted || flags[0] != 0);
-    if (aborted) break;
-    more = walk.next(nx);
-    if (!more && ct == 0) grid_launch_dependents();  // all tiles consumed: let the next kernel launch
-
-    // ---- merge the 8 warps: row stats, then accumulators in a fixed order (deterministic)
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float lv = l[mt][h];
-        lv += __shfl_xor_sync(0xffffffffu, lv, 1);
-        lv += __shfl_xor_sync(0xffffffffu, lv, 2);
-        if ((lane & 3) == 0) {
-          const int row = 16 * mt + (lane >> 2) + 8 * h;
-          red_m[cw * QROWS + row] = m[mt][h];
-          red_l[cw * QROWS + row] = lv;
-        }
-      }
-    named_bar_sync(1, kConsumerThreads);
-    if (ct < QROWS) {
-      float mm = -INFINITY;
-      for (int w = 0; w < kCW; ++w) mm = fmaxf(mm, red_m[w * QROWS + ct]);
-      const float mu = mm == -INFINITY ? 0.f : mm;
-      float ll = 0.f;
-      for (int w = 0; w < kCW; ++w) ll += red_l[w * QROWS + ct] * ex2(red_m[w * QROWS + ct] - mu);
-      row_m[ct] = mm;
-      row_l[ct] = ll;
-    }
-    named_bar_sync(1, kConsumerThreads);
-    for (int w = 0; w < kCW; ++w) {
-      if (cw == w) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int row = 16 * mt + (lane >> 2) + 8 * h;
-            const float mm = row_m[row];
-            const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
-#pragma unroll
-            for (int dn = 0; dn < D / 8; ++dn) {
-              float2 *dst = reinterpret_cast<float2 *>(&accbuf[row * D + 8 * dn + 2 * (lane & 3)]);
-              const float2 prev = w == 0 ? make_float2(0.f, 0.f) : *dst;
-              *dst = make_float2(prev.x + acc[mt][dn][2 * h] * f, prev.y + acc[mt][dn][2 * h + 1] * f);
-            }
-          }
-      }
-      named_bar_sync(1, kConsumerThreads);
-    }
-
-    if (it.parts == 1) {
-      // ---------------------------------------------------------- the group ends here
-      for (int idx = ct; idx < R * D; idx += kConsumerThreads) {
-        const int r = idx / D, d = idx % D;
-        const int i = r / a.G, gg = r % a.G, hq = it.h * a.G + gg;
-        const float mm = row_m[r];
-        float num = 0.f, den = 1.f;
-        if (mm != -INFINITY) {
-          float top = mm, sink_term = 0.f;
-          if (a.has_sink) {
-            const float z = (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e;
-            top = fmaxf(mm, z);
-            sink_term = ex2(z - top);
-          }
-          const float f = ex2(mm - top);
-          num = accbuf[idx] * f;
-          den = row_l[r] * f + sink_term;
-        }
-        out[(((size_t)it.b * a.curr + i) * a.Hq + hq) * D + d] = from_f32<T>(num / den);
-      }
-    } else {
-      // ---------------------------------------------------------- write the partial
-      const size_t slot0 = (size_t)it.slot0;
-      {
-        const size_t base = (slot0 + it.j) * R;
-        float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * D);
-        for (int idx = ct; idx < R * D / 4; idx += kConsumerThreads)
-          pacc[idx] = reinterpret_cast<const float4 *>(accbuf)[idx];
-        for (int r = ct; r < R; r += kConsumerThreads) {
-          a.part_ml[(base + r) * 2] = row_m[r];
-          a.part_ml[(base + r) * 2 + 1] = row_l[r];
-        }
-      }
-      __threadfence();
-      named_bar_sync(1, kConsumerThreads);
-      if (ct == 0) {
-        const int old = atomicAdd(&a.tickets[g], 1);
-        flags[1] = old == it.parts - 1;
-      }
-      named_bar_sync(1, kConsumerThreads);
-      if (flags[1]) {
-        // ------------------------------------------------------ last part: combine
-        __threadfence();
-        if (ct == 0) a.tickets[g] = 0;
-        for (int r = ct; r < R; r += kConsumerThreads) {
-          const int hq = it.h * a.G + r % a.G;
-          float mm = -INFINITY;
-          for (int c = 0; c < it.parts; ++c) mm = fmaxf(mm, __ldcg(&a.part_ml[((slot0 + c) * R + r) * 2]));
-          float top = mm, sink_term = 0.f;
-          if (mm != -INFINITY && a.has_sink) {
-            const float z = (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e;
-            top = fmaxf(mm, z);
-            sink_term = ex2(z - top);
-          }
-          float ll = sink_term;
-          if (mm != -INFINITY)
-            for (int c = 0; c < it.parts; ++c) {
-              const float mc = __ldcg(&a.part_ml[((slot0 + c) * R + r) * 2]);
-              ll += __ldcg(&a.part_ml[((slot0 + c) * R + r) * 2 + 1]) * ex2(mc - top);
-            }
-          row_m[r] = mm == -INFINITY ? -INFINITY : top;
-          row_l[r] = ll;
-        }
-        named_bar_sync(1, kConsumerThreads);
-        for (int idx = ct; idx < R * (D / 4); idx += kConsumerThreads) {
-          const int r = idx / (D / 4), d4 = idx % (D / 4);
-          const int i = r / a.G, gg = r % a.G, hq = it.h * a.G + gg;
-          const float top = row_m[r];
-          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-          float den = 1.f;
-          if (top != -INFINITY) {
-            for (int c = 0; c < it.parts; ++c) {
-              const float mc = __ldcg(&a.part_ml[((slot0 + c) * R + r) * 2]);
-              if (mc == -INFINITY) continue;
-              const float f = ex2(mc - top);
-              const float4 v =
-                  __ldcg(reinterpret_cast<const float4 *>(a.part_acc + ((slot0 + c) * R + r) * D) + d4);
-              sum.x += v.x * f;
-              sum.y += v.y * f;
-              sum.z += v.z * f;
-              sum.w += v.w * f;
-            }
-            den = row_l[r];
-          }
-          T *o = out + (((size_t)it.b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-          o[0] = from_f32<T>(sum.x / den);
-          o[1] = from_f32<T>(sum.y / den);
-          o[2] = from_f32<T>(sum.z / den);
-          o[3] = from_f32<T>(sum.w / den);
-        }
-      }
-    }
-    named_bar_sync(1, kConsumerThreads);  // qs, accbuf and row stats are reused by the next item
-    it = nx;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(&a.tickets[bh], 1);
+    flags[1] = old == nchunks - 1;
   }
-  if (aborted && ct == 0) {
-    // copies the producer may still have in flight must land before the CTA exits
-    volatile int no_abort = 0;
-    for (int t = tiles; t < tiles + NST; ++t) mbar_wait(&full[t % NST], (t / NST) & 1, &no_abort);
-    report(a.status, GQA_DEV_TIMEOUT);
+  __syncthreads();
+  if (!flags[1]) return;
+
+  // -------------------------------------------------------------- last CTA: combine
+  __threadfence();
+  if (threadIdx.x == 0) a.tickets[bh] = 0;
+  for (int r = threadIdx.x; r < R; r += kThreads) {
+    const int hq = hkv * a.G + r % a.G;
+    float mm = -INFINITY;
+    for (int c = 0; c < nchunks; ++c) mm = fmaxf(mm, __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2]));
+    float top = mm, sink_term = 0.f;
+    if (mm != -INFINITY && a.has_sink) {
+      const float z = (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e;
+      top = fmaxf(mm, z);
+      sink_term = ex2(z - top);
+    }
+    float ll = sink_term;
+    if (mm != -INFINITY)
+      for (int c = 0; c < nchunks; ++c) {
+        const float mc = __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2]);
+        ll += __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2 + 1]) * ex2(mc - top);
+      }
+    row_m[r] = mm == -INFINITY ? -INFINITY : top;
+    row_l[r] = ll;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < R * (D / 4); idx += kThreads) {
+    const int r = idx / (D / 4), d4 = idx % (D / 4);
+    const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
+    const float top = row_m[r];
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 1.f;
+    if (top != -INFINITY) {
+      for (int c = 0; c < nchunks; ++c) {
+        const float mc = __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2]);
+        if (mc == -INFINITY) continue;
+        const float f = ex2(mc - top);
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + (gbase + (size_t)c * R + r) * D) + d4);
+        sum.x += v.x * f;
+        sum.y += v.y * f;
+        sum.z += v.z * f;
+        sum.w += v.w * f;
+      }
+      den = row_l[r];
+    }
+    T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+    o[0] = from_f32<T>(sum.x / den);
+    o[1] = from_f32<T>(sum.y / den);
+    o[2] = from_f32<T>(sum.z / den);
+    o[3] = from_f32<T>(sum.w / den);
   }
 }
 
 template <typename T, int D, int MT, int NST>
 gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   using L = Smem<D, MT, NST>;
-  static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
+  static_assert(2 * (L::kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
   CUtensorMap tk, tv;
   const long long outer = (long long)c.p.batch * c.p.kv_heads;
   if (!encode_kv_map(&tk, c.present_k, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
@@ -666,10 +567,8 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   auto kern = decode_split_kernel<T, D, MT, NST>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
-  int sms = device_sm_count();
-  if (sms <= 0) return GQA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(std::min(sms, kDecodeMaxCtas));
+  cfg.gridDim = dim3(dp.splits, c.p.kv_heads, c.p.batch);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = c.stream;
@@ -699,7 +598,6 @@ template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, c
   a.part_ml = reinterpret_cast<float *>(c.ws + wl.part_ml_off);
   a.tickets = reinterpret_cast<int32_t *>(c.ws + wl.tickets_off);
   a.status = c.status;
-  a.B = p.batch;
   a.Hq = p.q_heads;
   a.Hkv = p.kv_heads;
   a.G = c.G;
@@ -713,6 +611,7 @@ template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, c
   a.append = c.append;
   a.window = p.window;
   a.causal = p.causal;
+  a.splits = dp.splits;
   a.has_sink = (c.head_sink != nullptr) || p.smooth_softmax;
   if (p.softcap > 0.f) {
     a.score_mul = p.scale / p.softcap;
@@ -727,6 +626,8 @@ template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, c
   } else if (p.head_dim == 64) {
     if (dp.mtiles == 1) return launch_cfg<T, 64, 1, 6>(c, dp, a);
     if (dp.mtiles == 2) return launch_cfg<T, 64, 2, 6>(c, dp, a);
+    if (dp.mtiles == 3) return launch_cfg<T, 64, 3, 6>(c, dp, a);
+    if (dp.mtiles == 4) return launch_cfg<T, 64, 4, 6>(c, dp, a);
   }
   return GQA_ERR_UNSUPPORTED;
 }

@@ -97,7 +97,18 @@ DecodePlan decode_plan(const gqa_params &p) {
   const int G = p.q_heads / p.kv_heads;
   d.rows = G * p.q_len;
   d.mtiles = (d.rows + 15) / 16;
-  d.eligible = p.dtype != GQA_F32 && (p.head_dim == 128 || p.head_dim == 64) && d.mtiles <= 2;
+  d.eligible = p.dtype != GQA_F32 &&
+               ((p.head_dim == 128 && d.mtiles <= 2) || (p.head_dim == 64 && d.mtiles <= 4));
+  // longest visible band of one group: [max(0, past - W + 1), past + curr)
+  long long lmax = p.cap_present;
+  if (p.window > 0) lmax = std::min<long long>(lmax, (long long)p.window + p.q_len - 1);
+  // chunks per group: enough CTAs for two waves of a 152-SM GB300 at two CTAs per SM
+  // (608), chunks of at most 4096 keys (partials stay small) and at least 256 keys
+  // (per-CTA setup stays small)
+  const long long units = (long long)p.batch * p.kv_heads;
+  long long s = std::max<long long>((608 + units - 1) / units, (lmax + 4095) / 4096);
+  s = std::min<long long>(s, std::max<long long>(1, (lmax + 255) / 256));
+  d.splits = (int)std::max<long long>(1, s);
   return d;
 }
 
@@ -111,9 +122,9 @@ WsLayout workspace_layout(const gqa_params &p, bool need_q_rot) {
     off = align_up(off + w.q_rot_bytes, kAlign);
   }
   DecodePlan d = decode_plan(p);
-  if (d.eligible) {
+  if (d.eligible && d.splits > 1) {
     const size_t groups = (size_t)p.batch * p.kv_heads;
-    const size_t slots = (size_t)kDecodeMaxCtas + groups;
+    const size_t slots = groups * d.splits;
     w.part_acc_off = off;
     w.part_acc_bytes = slots * d.rows * p.head_dim * sizeof(float);
     off = align_up(off + w.part_acc_bytes, kAlign);
@@ -199,7 +210,7 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   const DecodePlan dp = decode_plan(c.p);
   // the split decode kernel appends and rotates itself; every other path runs K1 first
   const bool fused = mode == kDecode && dp.eligible;
-  size_t need = fused ? wl.total : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
+  size_t need = fused ? (dp.splits > 1 ? wl.total : 0) : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
   if (need > 0) {
     if (!workspace || !aligned16(workspace)) return GQA_ERR_WORKSPACE;
     if (workspace_bytes < need) return GQA_ERR_WORKSPACE;

@@ -33,14 +33,13 @@ struct Call {
   size_t ws_bytes = 0;
 };
 
-// Split-KV decode plan.  The persistent decode kernel runs one CTA per SM (at most
-// kDecodeMaxCtas) over all groups' 128-key tiles; a group covered by several CTAs combines
-// through partial slots, of which there are at most grid + B*Hkv.
-constexpr int kDecodeMaxCtas = 1024;
+// Split-KV decode plan.  The visible band of each (b, kv head) group is cut into `splits`
+// equal chunks (one CTA each); `splits` depends on the params only, so the workspace does.
 struct DecodePlan {
-  bool eligible = false;  // tensor-core split kernel handles these params
-  int rows = 0;           // R = G * curr query rows per item
+  bool eligible = false;  // the split kernel handles these params
+  int rows = 0;           // R = G * curr query rows per CTA
   int mtiles = 0;         // ceil(R / 16)
+  int splits = 1;         // chunks per group
 };
 
 struct WsLayout {

@@ -20,7 +20,6 @@
 // visited; only tiles that cross a frontier evaluate the per-element predicate.
 // The sink starts the running state: m = z*log2(e), l = 1, so it is counted exactly once.
 #include <limits.h>
-#include <type_traits>
 #include <math.h>
 
 #include "common.cuh"
@@ -142,19 +141,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// tanh(x) for |x| <= kTanhPolyMax on the FMA pipe: the odd Taylor series of tanh through
-// x^9, tanh x = x (1 - x^2/3 + 2x^4/15 - 17x^6/315 + 62x^8/2835) + O(x^11); at |x| = 0.3 the
-// first dropped term is 1382/155925 x^11 < 2e-8, below fp32 rounding of the result.
-constexpr float kTanhPolyMax = 0.3f;
-__device__ __forceinline__ float tanh_poly(float x) {
-  const float x2 = x * x;
-  float p = fmaf(x2, 62.f / 2835.f, -17.f / 315.f);
-  p = fmaf(p, x2, 2.f / 15.f);
-  p = fmaf(p, x2, -1.f / 3.f);
-  p = fmaf(p, x2, 1.f);
-  return x * p;
-}
 
 template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
@@ -392,15 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key < lo_vis || key > hi_vis) r[e] = __float_as_uint(-INFINITY);
         }
       }
-      float mx = __uint_as_float(r[0]), mn = mx;
+      float mx = __uint_as_float(r[0]);
 #pragma unroll
-      for (int e = 1; e < BN; ++e) {
-        mx = fmaxf(mx, __uint_as_float(r[e]));
-        if (SOFTCAP) mn = fminf(mn, __uint_as_float(r[e]));
-      }
-      // softcap: the polynomial tanh serves the whole warp when every |score| of its tile
-      // is in range (masked tiles hold -inf and take the MUFU path)
-      const bool poly = SOFTCAP && __all_sync(0xffffffffu, fmaxf(mx, -mn) * smul <= kTanhPolyMax);
+      for (int e = 1; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
       float m_tile = -INFINITY;
       if (mx != -INFINITY) m_tile = SOFTCAP ? tanh_fast(mx * smul) * cmul : mx * smul;
       // lazy rescale: move the reference max only when it grows by more than 2^8
@@ -410,37 +390,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       float rs = 0.f;
       // P = 2^(x - m) in two halves (keeps register pressure down), packed to the dtype and
-      // stored over the first columns of S; the tanh variant is chosen once per warp
-      auto make_p = [&](auto poly_tag) {
-        constexpr bool kPoly = decltype(poly_tag)::value;
+      // stored over the first columns of S
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            float p2[2];
+        for (int e = 0; e < 64; e += 2) {
+          float p2[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const float sv = __uint_as_float(r[half * 64 + e + u]);
-              float x;
-              if (SOFTCAP) {
-                const float y = sv * smul;
-                x = fmaf(kPoly ? tanh_poly(y) : tanh_fast(y), cmul, -m_use);
-              } else {
-                x = fmaf(sv, smul, -m_use);
-              }
-              p2[u] = ex2(x);
-              rs += p2[u];
-            }
-            pk[e >> 1] = pack2<T>(p2[0], p2[1]);
+          for (int u = 0; u < 2; ++u) {
+            const float sv = __uint_as_float(r[half * 64 + e + u]);
+            const float x = SOFTCAP ? fmaf(tanh_fast(sv * smul), cmul, -m_use) : fmaf(sv, smul, -m_use);
+            p2[u] = ex2(x);
+            rs += p2[u];
           }
-          tmem_st32(tS + half * 32, pk);
+          pk[e >> 1] = pack2<T>(p2[0], p2[1]);
         }
-      };
-      if (poly)
-        make_p(std::true_type{});
-      else
-        make_p(std::false_type{});
+        tmem_st32(tS + half * 32, pk);
+      }
       l = l * alpha + rs;
       m_ref = m_new;
       if (__any_sync(0xffffffffu, need) && t > 0) {

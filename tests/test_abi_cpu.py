@@ -119,7 +119,7 @@ def test_rotary_needs_tables(g):
 
 
 def test_workspace_checked_before_launch(g):
-    p = good_params(g, batch=4, cap_present=8192, window=-1)
+    p = good_params(g, batch=4, cap_present=8192, window=-1)  # 8 chunks per group
     need = g.lib.gqa_workspace_bytes(ctypes.byref(p))
     assert need > 0
     assert call(g, p, ws_bytes=need - 1) == 5
@@ -127,24 +127,39 @@ def test_workspace_checked_before_launch(g):
     assert call(g, p, ws_bytes=need, workspace=FAKE + 8) == 5
 
 
-def decode_ws(B, Hkv, R, D):
-    """Split decode workspace: partial slots for up to 1024 CTAs plus one per (b, kv head)
-    group, fp32 acc [R][D] and (m, l) per slot, one ticket per group; 256-byte aligned."""
+def splits(B, Hkv, cap, window, curr=1):
+    """Chunks per group: two waves of 608 CTAs, chunks of 256..4096 keys."""
+    lmax = cap if window < 0 else min(cap, window + curr - 1)
+    units = B * Hkv
+    s = max(-(-608 // units), -(-lmax // 4096))
+    return max(1, min(s, max(1, -(-lmax // 256))))
+
+
+def decode_ws(B, Hkv, R, D, S):
+    """Split decode workspace: fp32 acc [R][D] and (m, l) per (group, chunk) slot, one ticket
+    per group; 256-byte aligned; nothing when a group is one chunk."""
+    if S == 1:
+        return 0
     al = lambda x: (x + 255) // 256 * 256
-    slots = 1024 + B * Hkv
+    slots = B * Hkv * S
     return al(slots * R * D * 4) + al(slots * R * 2 * 4) + al(B * Hkv * 4)
 
 
 def test_workspace_sizes(g):
     ws = lambda **kw: g.lib.gqa_workspace_bytes(ctypes.byref(good_params(g, **kw)))
     # decode: B=2, Hq=8, Hkv=2 -> G=4, R=4 rows per group
-    assert ws(window=200) == decode_ws(2, 2, 4, 128)
+    S = splits(2, 2, 1024, 200)
+    assert S == 1 and ws(window=200) == 0  # the band fits one chunk
+    S = splits(2, 2, 1024, -1)
+    assert S == 4 and ws(window=-1) == decode_ws(2, 2, 4, 128, S)
     # rotary adds room for the rotated queries (prefill path): B*curr*Hq*D*2 bytes
-    assert ws(do_rotary=1, rope_len=64, window=100) == 2 * 1 * 8 * 128 * 2 + decode_ws(2, 2, 4, 128)
-    # long decode: G=8, R=8
-    assert ws(batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1) == decode_ws(64, 8, 8, 128)
+    assert ws(do_rotary=1, rope_len=64, window=-1) == 2 * 1 * 8 * 128 * 2 + decode_ws(2, 2, 4, 128, S)
+    # long decode: G=8, R=8, 8 chunks of up to 4096 keys
+    S = splits(64, 8, 32768, -1)
+    assert S == 8
+    assert ws(batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1) == decode_ws(64, 8, 8, 128, S)
     # more than 32 query rows per group at D=128: the SIMT kernel, no split workspace
-    assert ws(q_heads=64, kv_heads=2, q_len=2) == 0
+    assert ws(q_heads=64, kv_heads=2, q_len=2, window=-1) == 0
     # prefill-sized q_len never needs decode partials
     assert ws(batch=2, q_heads=64, kv_heads=8, q_len=8192, cap_present=8192, window=4096) == 0
 
