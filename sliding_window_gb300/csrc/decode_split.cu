@@ -40,6 +40,7 @@ constexpr int KT = 64;         // keys per tile
 constexpr int kWarps = 4;      // 16 keys of a tile each
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleLog2 = 8.f;  // move the reference max only when it grows by > 2^8
+constexpr int kMaxSplits = kDecodeMaxSplits;
 
 struct DecodeArgs {
   const void *q;          // [B, curr, Hq, D] as given (rotated here when do_rotary)
@@ -71,7 +72,9 @@ template <int D, int MT, int NST> struct Smem {
   static constexpr int kFlagOff = kRowOff + 2 * kQRows * 4;
   static constexpr int kBytes = kFlagOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
-  static_assert(kQRows * D * 4 <= NST * kStageBytes, "merge buffer must fit in the stages");
+  // per-warp merge regions and the combine's chunk statistics reuse the stages
+  static_assert(kWarps * kQRows * D * 4 <= NST * kStageBytes, "merge regions must fit in the stages");
+  static_assert(2 * kMaxSplits * kQRows * 4 <= NST * kStageBytes, "chunk statistics must fit in the stages");
 };
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -169,20 +172,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   grid_dependency_wait();
   __syncthreads();
 
+  // the past length and the raw query rows are loaded together: their latencies overlap
   const int past = a.seqlens[b];
-  const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
-                                 a.rope_len);
-  if (st) {  // rejected sequence: zeros, nothing appended, reported once
-    if (split == 0) {
-      if (threadIdx.x == 0 && hkv == 0) report(a.status, st);
-      for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
-        const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
-        out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
-      }
+  constexpr int QITEMS = (QROWS * (DCH / 2) + kThreads - 1) / kThreads;  // chunk pairs per thread
+  uint4 qraw[QITEMS][2];
+#pragma unroll
+  for (int u = 0; u < QITEMS; ++u) {
+    const int idx = threadIdx.x + u * kThreads;
+    const int r = idx / (DCH / 2), c = idx % (DCH / 2);
+    qraw[u][0] = qraw[u][1] = make_uint4(0, 0, 0, 0);
+    if (idx < QROWS * (DCH / 2) && r < R) {
+      const T *src = reinterpret_cast<const T *>(a.q) +
+                     (((size_t)b * a.curr + r / a.G) * a.Hq + hkv * a.G + r % a.G) * D;
+      qraw[u][0] = *reinterpret_cast<const uint4 *>(src + c * 8);
+      qraw[u][1] = *reinterpret_cast<const uint4 *>(src + D / 2 + c * 8);
     }
-    return;
   }
-  const int total = past + a.curr;
+  const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
+                                 a.rope_len);  const int total = past + a.curr;
   const int lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
   const int len = total - lo;
   const int chunk = ((len + a.splits - 1) / a.splits + KT - 1) / KT * KT;  // this group's chunk
@@ -217,22 +224,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // Q rows r = i*G + g (token i, q head hkv*G + g), rotated at past + i, 128B-swizzled
   {
-    const T *q = reinterpret_cast<const T *>(a.q);
     const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
     const bool rot = a.do_rotary && a.append;
-    for (int idx = threadIdx.x; idx < QROWS * (DCH / 2); idx += kThreads) {
+#pragma unroll
+    for (int u = 0; u < QITEMS; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx >= QROWS * (DCH / 2)) break;
       const int r = idx / (DCH / 2), c = idx % (DCH / 2);  // chunk c of the first half
-      uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
-      if (r < R) {
-        const int i = r / a.G, g = r % a.G;
-        const T *src = q + (((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D;
-        if (rot) {
-          const size_t pos = (size_t)(past + i) * (D / 2);
-          rotate8<T>(src + c * 8, src + D / 2 + c * 8, cs + pos + c * 8, sn + pos + c * 8, y1, y2);
-        } else {
-          y1 = *reinterpret_cast<const uint4 *>(src + c * 8);
-          y2 = *reinterpret_cast<const uint4 *>(src + D / 2 + c * 8);
-        }
+      uint4 y1 = qraw[u][0], y2 = qraw[u][1];
+      if (rot && r < R) {
+        const size_t pos = (size_t)(past + r / a.G) * (D / 2);
+        rotate8<T>(reinterpret_cast<const T *>(&qraw[u][0]), reinterpret_cast<const T *>(&qraw[u][1]),
+                   cs + pos + c * 8, sn + pos + c * 8, y1, y2);
       }
       const int c2 = c + DCH / 2;
       *reinterpret_cast<uint4 *>(qs + (c >> 3) * (QROWS * 128) + sw128(r, c & 7)) = y1;
@@ -440,35 +443,44 @@ __global__ void __launch_bounds__(kThreads, 2)
     row_l[row] = ll;
   }
   __syncthreads();
-  float *accbuf = reinterpret_cast<float *>(stages);  // [QROWS][D]; every stage was consumed
-  // warps add their rescaled accumulators one after another (fixed order: deterministic)
-  for (int w = 0; w < kWarps; ++w) {
-    if (warp == w) {
+  // every warp writes its rescaled accumulator to its own region (the stages are free now),
+  // then all threads sum the four regions in a fixed order (deterministic)
+  float *wacc = reinterpret_cast<float *>(stages);  // [kWarps][QROWS][D]
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = 16 * mt + (lane >> 2) + 8 * h;
-          const float mm = row_m[row];
-          const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
+    for (int h = 0; h < 2; ++h) {
+      const int row = 16 * mt + (lane >> 2) + 8 * h;
+      const float mm = row_m[row];
+      const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
+      float *dst = wacc + ((size_t)warp * QROWS + row) * D + 2 * (lane & 3);
 #pragma unroll
-          for (int dn = 0; dn < D / 8; ++dn) {
-            float2 *dst = reinterpret_cast<float2 *>(&accbuf[row * D + 8 * dn + 2 * (lane & 3)]);
-            const float2 prev = w == 0 ? make_float2(0.f, 0.f) : *dst;
-            *dst = make_float2(prev.x + acc[mt][dn][2 * h] * f, prev.y + acc[mt][dn][2 * h + 1] * f);
-          }
-        }
+      for (int dn = 0; dn < D / 8; ++dn)
+        *reinterpret_cast<float2 *>(dst + 8 * dn) = make_float2(acc[mt][dn][2 * h] * f, acc[mt][dn][2 * h + 1] * f);
     }
-    __syncthreads();
-  }
+  __syncthreads();
+  auto merged = [&](int idx4) {  // float4 idx4 of the CTA's [R][D] accumulator
+    const float4 *w4 = reinterpret_cast<const float4 *>(wacc);
+    float4 v = w4[idx4];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+      const float4 u = w4[w * (QROWS * D / 4) + idx4];
+      v.x += u.x;
+      v.y += u.y;
+      v.z += u.z;
+      v.w += u.w;
+    }
+    return v;
+  };
 
   if (nchunks == 1) {
     // ------------------------------------------------------------ finish in place
-    for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
-      const int r = idx / D, d = idx % D;
+    for (int idx = threadIdx.x; idx < R * (D / 4); idx += kThreads) {
+      const int r = idx / (D / 4), d4 = idx % (D / 4);
       const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
       const float mm = row_m[r];
-      float num = 0.f, den = 1.f;
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 1.f;
       if (mm != -INFINITY) {
         float top = mm, sink_term = 0.f;
         if (a.has_sink) {
@@ -477,10 +489,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           sink_term = ex2(z - top);
         }
         const float f = ex2(mm - top);
-        num = accbuf[idx] * f;
+        num = merged(idx);
+        num.x *= f;
+        num.y *= f;
+        num.z *= f;
+        num.w *= f;
         den = row_l[r] * f + sink_term;
       }
-      out[(((size_t)b * a.curr + i) * a.Hq + hq) * D + d] = from_f32<T>(num / den);
+      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+      o[0] = from_f32<T>(num.x / den);
+      o[1] = from_f32<T>(num.y / den);
+      o[2] = from_f32<T>(num.z / den);
+      o[3] = from_f32<T>(num.w / den);
     }
     return;
   }
@@ -490,12 +510,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   {
     const size_t base = gbase + (size_t)split * R;
     float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * D);
-    const float4 *src = reinterpret_cast<const float4 *>(accbuf);
-    for (int idx = threadIdx.x; idx < R * D / 4; idx += kThreads) pacc[idx] = src[idx];
-    for (int r = threadIdx.x; r < R; r += kThreads) {
-      a.part_ml[(base + r) * 2] = row_m[r];
-      a.part_ml[(base + r) * 2 + 1] = row_l[r];
-    }
+    for (int idx = threadIdx.x; idx < R * D / 4; idx += kThreads) pacc[idx] = merged(idx);
+    for (int r = threadIdx.x; r < R; r += kThreads)
+      reinterpret_cast<float2 *>(a.part_ml)[base + r] = make_float2(row_m[r], row_l[r]);
   }
   __threadfence();
   __syncthreads();
@@ -509,10 +526,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   // -------------------------------------------------------------- last CTA: combine
   __threadfence();
   if (threadIdx.x == 0) a.tickets[bh] = 0;
+  // chunk statistics staged in shared memory with all loads in flight at once
+  float *cm = reinterpret_cast<float *>(stages);  // [nchunks][R] max, then scale factor
+  float *cl = cm + a.splits * R;                    // [nchunks][R] sum
+  for (int idx = threadIdx.x; idx < nchunks * R; idx += kThreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + gbase + idx);
+    cm[idx] = ml.x;
+    cl[idx] = ml.y;
+  }
+  __syncthreads();
   for (int r = threadIdx.x; r < R; r += kThreads) {
     const int hq = hkv * a.G + r % a.G;
     float mm = -INFINITY;
-    for (int c = 0; c < nchunks; ++c) mm = fmaxf(mm, __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2]));
+    for (int c = 0; c < nchunks; ++c) mm = fmaxf(mm, cm[c * R + r]);
     float top = mm, sink_term = 0.f;
     if (mm != -INFINITY && a.has_sink) {
       const float z = (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e;
@@ -520,39 +546,48 @@ __global__ void __launch_bounds__(kThreads, 2)
       sink_term = ex2(z - top);
     }
     float ll = sink_term;
-    if (mm != -INFINITY)
-      for (int c = 0; c < nchunks; ++c) {
-        const float mc = __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2]);
-        ll += __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2 + 1]) * ex2(mc - top);
-      }
-    row_m[r] = mm == -INFINITY ? -INFINITY : top;
-    row_l[r] = ll;
+    for (int c = 0; c < nchunks; ++c) {
+      const float f = mm == -INFINITY ? 0.f : ex2(cm[c * R + r] - top);  // 0 for empty chunks
+      ll += cl[c * R + r] * f;
+      cm[c * R + r] = f;
+    }
+    row_l[r] = mm == -INFINITY ? 0.f : ll;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < R * (D / 4); idx += kThreads) {
+  // chunk-outer: every thread keeps its outputs in registers and issues one independent
+  // load per output per chunk
+  constexpr int kPer = (MT * 16 * D / 4 + kThreads - 1) / kThreads;
+  float4 sum[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) sum[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 *pa4 = reinterpret_cast<const float4 *>(a.part_acc + gbase * D);
+#pragma unroll 4
+  for (int c = 0; c < nchunks; ++c) {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx < R * (D / 4)) {
+        const float f = cm[c * R + idx / (D / 4)];
+        const float4 v = __ldcg(pa4 + (size_t)c * R * (D / 4) + idx);
+        sum[u].x += v.x * f;
+        sum[u].y += v.y * f;
+        sum[u].z += v.z * f;
+        sum[u].w += v.w * f;
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = threadIdx.x + u * kThreads;
+    if (idx >= R * (D / 4)) continue;
     const int r = idx / (D / 4), d4 = idx % (D / 4);
     const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
-    const float top = row_m[r];
-    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    float den = 1.f;
-    if (top != -INFINITY) {
-      for (int c = 0; c < nchunks; ++c) {
-        const float mc = __ldcg(&a.part_ml[(gbase + (size_t)c * R + r) * 2]);
-        if (mc == -INFINITY) continue;
-        const float f = ex2(mc - top);
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part_acc + (gbase + (size_t)c * R + r) * D) + d4);
-        sum.x += v.x * f;
-        sum.y += v.y * f;
-        sum.z += v.z * f;
-        sum.w += v.w * f;
-      }
-      den = row_l[r];
-    }
+    const float den = row_l[r] > 0.f ? row_l[r] : 1.f;  // no visible key: the sums are 0
     T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-    o[0] = from_f32<T>(sum.x / den);
-    o[1] = from_f32<T>(sum.y / den);
-    o[2] = from_f32<T>(sum.z / den);
-    o[3] = from_f32<T>(sum.w / den);
+    o[0] = from_f32<T>(sum[u].x / den);
+    o[1] = from_f32<T>(sum[u].y / den);
+    o[2] = from_f32<T>(sum[u].z / den);
+    o[3] = from_f32<T>(sum[u].w / den);
   }
 }
 

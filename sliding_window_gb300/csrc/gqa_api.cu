@@ -108,6 +108,7 @@ DecodePlan decode_plan(const gqa_params &p) {
   const long long units = (long long)p.batch * p.kv_heads;
   long long s = std::max<long long>((608 + units - 1) / units, (lmax + 4095) / 4096);
   s = std::min<long long>(s, std::max<long long>(1, (lmax + 255) / 256));
+  s = std::min<long long>(s, kDecodeMaxSplits);
   d.splits = (int)std::max<long long>(1, s);
   return d;
 }

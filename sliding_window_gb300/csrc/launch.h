@@ -35,6 +35,7 @@ struct Call {
 
 // Split-KV decode plan.  The visible band of each (b, kv head) group is cut into `splits`
 // equal chunks (one CTA each); `splits` depends on the params only, so the workspace does.
+constexpr int kDecodeMaxSplits = 64;
 struct DecodePlan {
   bool eligible = false;  // the split kernel handles these params
   int rows = 0;           // R = G * curr query rows per CTA

@@ -213,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the first 64 columns of S_X as packed pairs
   int kissued = 0, vissued = 0;      // producer thread: TMA tiles issued
   int s_commits = 0, o_commits = 0;  // MMA thread: last S and PV commit counts
-
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
@@ -378,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key < lo_vis || key > hi_vis) r[e] = __float_as_uint(-INFINITY);
         }
       }
-      float mx = __uint_as_float(r[0]);
+      float mx = -INFINITY;
 #pragma unroll
-      for (int e = 1; e < BN; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
+      for (int e = 0; e < BN; e += 2) mx = fmax3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
       float m_tile = -INFINITY;
       if (mx != -INFINITY) m_tile = SOFTCAP ? tanh_fast(mx * smul) * cmul : mx * smul;
       // lazy rescale: move the reference max only when it grows by more than 2^8
@@ -388,26 +387,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = need ? m_tile : m_ref;
       const float alpha = need ? ex2(m_ref - m_new) : 1.f;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      float rs = 0.f;
       // P = 2^(x - m) in two halves (keeps register pressure down), packed to the dtype and
-      // stored over the first columns of S
+      // stored over the first columns of S; elementwise math two lanes per instruction
+      uint64_t rs2 = 0;  // (0.f, 0.f)
+      const uint64_t smul2 = f2_pack(smul, smul), cmul2 = f2_pack(cmul, cmul), negm2 = f2_pack(-m_use, -m_use);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
-          float p2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float sv = __uint_as_float(r[half * 64 + e + u]);
-            const float x = SOFTCAP ? fmaf(tanh_fast(sv * smul), cmul, -m_use) : fmaf(sv, smul, -m_use);
-            p2[u] = ex2(x);
-            rs += p2[u];
+          const uint64_t sv = f2_pack(__uint_as_float(r[half * 64 + e]), __uint_as_float(r[half * 64 + e + 1]));
+          uint64_t x;
+          if (SOFTCAP) {
+            const float2 y = f2_unpack(f2_mul(sv, smul2));
+            x = f2_fma(f2_pack(tanh_fast(y.x), tanh_fast(y.y)), cmul2, negm2);
+          } else {
+            x = f2_fma(sv, smul2, negm2);
           }
-          pk[e >> 1] = pack2<T>(p2[0], p2[1]);
+          const float2 xf = f2_unpack(x);
+          const float p0 = ex2(xf.x), p1 = ex2(xf.y);
+          rs2 = f2_add(rs2, f2_pack(p0, p1));
+          pk[e >> 1] = pack2<T>(p0, p1);
         }
         tmem_st32(tS + half * 32, pk);
       }
+      const float2 rsf = f2_unpack(rs2);
+      const float rs = rsf.x + rsf.y;
       l = l * alpha + rs;
       m_ref = m_new;
       if (__any_sync(0xffffffffu, need) && t > 0) {

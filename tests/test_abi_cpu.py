@@ -132,7 +132,7 @@ def splits(B, Hkv, cap, window, curr=1):
     lmax = cap if window < 0 else min(cap, window + curr - 1)
     units = B * Hkv
     s = max(-(-608 // units), -(-lmax // 4096))
-    return max(1, min(s, max(1, -(-lmax // 256))))
+    return min(64, max(1, min(s, max(1, -(-lmax // 256)))))
 
 
 def decode_ws(B, Hkv, R, D, S):
