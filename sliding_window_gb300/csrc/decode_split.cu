@@ -189,7 +189,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
-                                 a.rope_len);  const int total = past + a.curr;
+                                 a.rope_len);
+  if (st) {  // rejected sequence: zeros, nothing appended, reported once
+    if (split == 0) {
+      if (threadIdx.x == 0 && hkv == 0) report(a.status, st);
+      for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+        const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
+        out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
+      }
+    }
+    return;
+  }
+  const int total = past + a.curr;
   const int lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
   const int len = total - lo;
   const int chunk = ((len + a.splits - 1) / a.splits + KT - 1) / KT * KT;  // this group's chunk
