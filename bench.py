@@ -552,11 +552,16 @@ def report(args, w, r, world):
 
 
 def load_traffic(name):
-    """dram bytes per launch of the dominant kernel from the committed ncu summary, if any."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per launch of the dominant kernel, from the committed ncu
+    summary; None when there is none or the kernel source changed since it was taken."""
+    import hashlib
     try:
-        with open(path) as f:
-            return json.load(f).get(name)
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            e = json.load(f)[name]
+        with open(os.path.join(ROOT, e["source"]), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != e["sha1"]:
+                return None
+        return e["dram_bytes_per_launch"]
     except Exception:
         return None
 
