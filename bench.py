@@ -155,17 +155,38 @@ class ClockSampler:
 # our arm
 # --------------------------------------------------------------------------------------
 class Step:
-    """One buffer set of a workload (all layers) and the calls that make one step."""
+    """One buffer set of a workload (all layers) and the calls that make one step.  The
+    step's per-call inputs (q, k, v, seqlens_k of every layer) live in one device staging
+    buffer, so an end-to-end step moves them host->device in a single copy."""
+
+    INPUTS = ("q", "k", "v", "seqlens_k")
 
     def __init__(self, w, rank, set_index, device):
         from sliding_window_gb300 import gqa
         self.g = gqa
         self.w = w
         self.layers = []
+        cases = []
         for layer in range(w.layers):
             # every buffer set of a rank draws the same past lengths, so every step does equal work
-            c = make_case(w, layer=layer, device=device, seed_offset=1000 * rank + set_index,
-                          seqlens=draw_seqlens(w, seed_offset=rank))
+            cases.append(make_case(w, layer=layer, device=device, seed_offset=1000 * rank + set_index,
+                                   seqlens=draw_seqlens(w, seed_offset=rank)))
+        offs, total = [], 0
+        for c in cases:
+            for n in self.INPUTS:
+                t = getattr(c, n)
+                offs.append(total)
+                total += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.stage = torch.empty(total, dtype=torch.uint8, device=device)
+        it = iter(offs)
+        for c in cases:
+            for n in self.INPUTS:
+                t = getattr(c, n)
+                o = next(it)
+                view = self.stage[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                view.copy_(t)
+                setattr(c, n, view)
+        for c in cases:
             p = gqa.params_from_dict(c.params)
             ws = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device=device)
             L = dict(c=c, p=p, p_attend=gqa.params_from_dict(dict(c.params, do_rotary=0)), ws=ws,
@@ -173,6 +194,14 @@ class Step:
                      status=torch.zeros(1, dtype=torch.int32, device=device))
             self.layers.append(L)
         self.fn = gqa.gqa_attention_decode if w.mode == "decode" else gqa.gqa_attention_prefill
+        # all layers' outputs side by side, for one device->host copy per step
+        self.out_all = torch.empty(sum(L["out"].numel() for L in self.layers), dtype=self.layers[0]["out"].dtype,
+                                   device=device)
+        o = 0
+        for L in self.layers:
+            n = L["out"].numel()
+            L["out"] = self.out_all[o:o + n].view(L["out"].shape)
+            o += n
 
     def seqlens(self):
         return [L["c"].seqlens_k.cpu().numpy() for L in self.layers]
@@ -202,8 +231,9 @@ class Step:
         tot = 0
         for L in self.layers:
             c = L["c"]
-            for t in (c.q, c.k, c.v, c.past_k, c.past_v, L["out"], L["ws"], L["q_rot"]):
+            for t in (c.past_k, c.past_v, L["ws"], L["q_rot"]):
                 tot += t.numel() * t.element_size()
+        tot += self.stage.numel() + self.out_all.numel() * self.out_all.element_size()
         return tot
 
 
@@ -318,34 +348,25 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_e2e(args, sets, stream, w, units):
-    """Every step: pinned host -> device copies of q, k, v and seqlens_k, the decode/prefill
-    call, device -> pinned host copy of out.  The KV cache stays resident (it is the op's
-    state); captured in CUDA graphs like the device-side loop."""
+    """Every step: the step's inputs (q, k, v, seqlens_k of all layers) copied host->device
+    from pinned memory in one copy, the public decode/prefill call per layer, the outputs
+    copied device->host in one copy.  The KV cache stays resident (it is the op's state);
+    captured in CUDA graphs like the device-side loop."""
     hosts = []
-    h2d = d2h = 0
     for s in sets:
-        hs = []
-        for L in s.layers:
-            c = L["c"]
-            hq = {n: getattr(c, n).cpu().pin_memory() for n in ("q", "k", "v", "seqlens_k")}
-            ho = torch.empty(L["out"].shape, dtype=L["out"].dtype).pin_memory()
-            hs.append((hq, ho))
-        hosts.append(hs)
-    for (hq, ho), L in zip(hosts[0], sets[0].layers):
-        h2d += sum(t.numel() * t.element_size() for t in hq.values())
-        d2h += ho.numel() * ho.element_size()
+        hs = s.stage.cpu().pin_memory()
+        ho = torch.empty(s.out_all.shape, dtype=s.out_all.dtype).pin_memory()
+        hosts.append((hs, ho))
+    h2d = hosts[0][0].numel()
+    d2h = hosts[0][1].numel() * hosts[0][1].element_size()
 
     def make(si):
-        s, hs = sets[si], hosts[si]
+        s, (hs, ho) = sets[si], hosts[si]
 
         def f(stream):
-            for (hq, ho), L in zip(hs, s.layers):
-                c = L["c"]
-                for n in ("q", "k", "v", "seqlens_k"):
-                    getattr(c, n).copy_(hq[n], non_blocking=True)
+            s.stage.copy_(hs, non_blocking=True)
             s.full(stream)
-            for (hq, ho), L in zip(hs, s.layers):
-                ho.copy_(L["out"], non_blocking=True)
+            ho.copy_(s.out_all, non_blocking=True)
         return f
 
     fns = [make(i) for i in range(len(sets))]

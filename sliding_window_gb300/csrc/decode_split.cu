@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <typename T, int D, int MT, int NST>
 gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   using L = Smem<D, MT, NST>;
-  static_assert(2 * (L::kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
   CUtensorMap tk, tv;
   const long long outer = (long long)c.p.batch * c.p.kv_heads;
   if (!encode_kv_map(&tk, c.present_k, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
@@ -665,6 +665,10 @@ template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, c
   } else {
     a.score_mul = p.scale * kLog2e;
     a.cap_mul = 0.f;
+  }
+  if (dp.deep) {  // 192 KB of stages: one CTA per SM
+    if (p.head_dim == 128 && dp.mtiles == 1) return launch_cfg<T, 128, 1, 6>(c, dp, a);
+    if (p.head_dim == 64 && dp.mtiles == 1) return launch_cfg<T, 64, 1, 12>(c, dp, a);
   }
   if (p.head_dim == 128) {
     if (dp.mtiles == 1) return launch_cfg<T, 128, 1, 3>(c, dp, a);

@@ -106,6 +106,13 @@ DecodePlan decode_plan(const gqa_params &p) {
   // (608), chunks of at most 4096 keys (partials stay small) and at least 256 keys
   // (per-CTA setup stays small)
   const long long units = (long long)p.batch * p.kv_heads;
+  if (d.rows <= 16 && units <= 152 && lmax <= 8192) {
+    // small bandwidth-bound step: one CTA per group streams the whole band through a deep
+    // ring, alone on its SM; no chunk partials to combine and no workspace
+    d.splits = 1;
+    d.deep = true;
+    return d;
+  }
   long long s = std::max<long long>((608 + units - 1) / units, (lmax + 4095) / 4096);
   s = std::min<long long>(s, std::max<long long>(1, (lmax + 255) / 256));
   s = std::min<long long>(s, kDecodeMaxSplits);

@@ -41,6 +41,7 @@ struct DecodePlan {
   int rows = 0;           // R = G * curr query rows per CTA
   int mtiles = 0;         // ceil(R / 16)
   int splits = 1;         // chunks per group
+  bool deep = false;      // one CTA per SM with a deep ring (small bandwidth-bound steps)
 };
 
 struct WsLayout {

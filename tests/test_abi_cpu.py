@@ -119,7 +119,7 @@ def test_rotary_needs_tables(g):
 
 
 def test_workspace_checked_before_launch(g):
-    p = good_params(g, batch=4, cap_present=8192, window=-1)  # 8 chunks per group
+    p = good_params(g, batch=4, cap_present=16384, window=-1)  # band too long for one chunk
     need = g.lib.gqa_workspace_bytes(ctypes.byref(p))
     assert need > 0
     assert call(g, p, ws_bytes=need - 1) == 5
@@ -127,10 +127,13 @@ def test_workspace_checked_before_launch(g):
     assert call(g, p, ws_bytes=need, workspace=FAKE + 8) == 5
 
 
-def splits(B, Hkv, cap, window, curr=1):
-    """Chunks per group: two waves of 608 CTAs, chunks of 256..4096 keys."""
+def splits(B, Hkv, cap, window, curr=1, R=4):
+    """Chunks per group: one for small bandwidth-bound steps (<= 16 rows, <= 152 groups,
+    band <= 8192 keys), else two waves of 608 CTAs with chunks of 256..4096 keys."""
     lmax = cap if window < 0 else min(cap, window + curr - 1)
     units = B * Hkv
+    if R <= 16 and units <= 152 and lmax <= 8192:
+        return 1
     s = max(-(-608 // units), -(-lmax // 4096))
     return min(64, max(1, min(s, max(1, -(-lmax // 256)))))
 
@@ -150,12 +153,13 @@ def test_workspace_sizes(g):
     # decode: B=2, Hq=8, Hkv=2 -> G=4, R=4 rows per group
     S = splits(2, 2, 1024, 200)
     assert S == 1 and ws(window=200) == 0  # the band fits one chunk
-    S = splits(2, 2, 1024, -1)
-    assert S == 4 and ws(window=-1) == decode_ws(2, 2, 4, 128, S)
+    S = splits(2, 2, 16384, -1)
+    assert S == 64 and ws(window=-1, cap_present=16384) == decode_ws(2, 2, 4, 128, S)
     # rotary adds room for the rotated queries (prefill path): B*curr*Hq*D*2 bytes
-    assert ws(do_rotary=1, rope_len=64, window=-1) == 2 * 1 * 8 * 128 * 2 + decode_ws(2, 2, 4, 128, S)
+    assert ws(do_rotary=1, rope_len=64, window=-1, cap_present=16384) == \
+        2 * 1 * 8 * 128 * 2 + decode_ws(2, 2, 4, 128, S)
     # long decode: G=8, R=8, 8 chunks of up to 4096 keys
-    S = splits(64, 8, 32768, -1)
+    S = splits(64, 8, 32768, -1, R=8)
     assert S == 8
     assert ws(batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1) == decode_ws(64, 8, 8, 128, S)
     # more than 32 query rows per group at D=128: the SIMT kernel, no split workspace
