@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from gpu_util import assert_close
-from sliding_window_gb300.inputs import WORKLOADS, Workload, make_case
+from sliding_window_gb300.inputs import Workload, make_case
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,10 @@ def _tensors(case, dev):
 def test_noalloc_matches_workspace_decode_twice(case_id):
     from sliding_window_gb300 import gqa
     if case_id == "window_decode":
-        case = make_case(WORKLOADS["decode_window_bf16"])
+        # a band long enough to be split across CTAs, so the call needs its chunk partials
+        w = Workload("noalloc_win", 76, "decode", "bf16", 8, 32, 8, 128, 1, 16384, 9000, 16383, windows=(12000,),
+                     head_sink=True)
+        case = make_case(w)
     else:
         w = Workload("noalloc_rot", 77, "decode", "f16", 4, 32, 4, 128, 4, 6000, 1000, 5990, windows=(-1,),
                      smooth_softmax=1, do_rotary=1, rope_len=6000)
