@@ -135,8 +135,10 @@ gqa_status gqa_attention_prefill(const gqa_params *p, const void *q, const void 
 /* Decode step ([P1] "Sliding window" generate branch, multi-token decode; [P2] decode
  * steps): same arguments and semantics as gqa_attention_prefill, executed by the split-KV
  * kernel: each CTA owns all G*curr query rows of one (b, kv head) and one chunk of its
- * visible keys, reads each K/V byte once, and the last CTA of a group merges the partial
- * (max, sum, acc) of the chunks.  For G*curr > 64 or f32 the fp32 SIMT kernel runs. */
+ * visible keys and reads each K/V byte once.  The partial (max, sum, acc) of a group's
+ * chunks are merged in distributed shared memory when the chunks form one thread-block
+ * cluster (2..8 chunks, launch of one wave), else by the last CTA of the group through the
+ * workspace.  For G*curr > 64 (D=64) or > 32 (D=128), or f32, the fp32 SIMT kernel runs. */
 gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *k, const void *v,
                                 const void *past_k, const void *past_v, const int32_t *seqlens_k,
                                 const void *cos_cache, const void *sin_cache, const float *head_sink,

@@ -41,6 +41,7 @@ constexpr int kWarps = 4;      // 16 keys of a tile each
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleLog2 = 8.f;  // move the reference max only when it grows by > 2^8
 constexpr int kMaxSplits = kDecodeMaxSplits;
+constexpr int kMaxCluster = kDecodeMaxCluster;  // chunks combined through distributed shared memory
 
 struct DecodeArgs {
   const void *q;          // [B, curr, Hq, D] as given (rotated here when do_rotary)
@@ -75,6 +76,8 @@ template <int D, int MT, int NST> struct Smem {
   // per-warp merge regions and the combine's chunk statistics reuse the stages
   static_assert(kWarps * kQRows * D * 4 <= NST * kStageBytes, "merge regions must fit in the stages");
   static_assert(2 * kMaxSplits * kQRows * 4 <= NST * kStageBytes, "chunk statistics must fit in the stages");
+  static_assert(((kWarps + 1) * kQRows * D + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <= NST * kStageBytes,
+                "cluster exchange buffers must fit in the stages");
 };
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -132,7 +135,7 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
   __syncwarp();
 }
 
-template <typename T, int D, int MT, int NST>
+template <typename T, int D, int MT, int NST, bool CL>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         DecodeArgs a) {
@@ -205,12 +208,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int len = total - lo;
   const int chunk = ((len + a.splits - 1) / a.splits + KT - 1) / KT * KT;  // this group's chunk
   const int nchunks = (len + chunk - 1) / chunk;
-  if (split >= nchunks) return;  // whole CTA idle (uniform)
+  // a CTA past the group's last chunk has nothing to stream; in a cluster it still takes
+  // part in the exchange (its rows carry m = -inf), otherwise it leaves now
+  const bool idle = split >= nchunks;
+  if (idle && (!CL || nchunks == 1)) return;
   const int c0 = lo + split * chunk;
   const int c1 = min(total, c0 + chunk);
-  const int ntiles = (c1 - c0 + KT - 1) / KT;
+  const int ntiles = idle ? 0 : (c1 - c0 + KT - 1) / KT;
   const int bh = b * a.Hkv + hkv;
-  const bool appends = a.append && c1 > past;  // this chunk holds new rows [past, total)
+  const bool appends = !idle && a.append && c1 > past;  // this chunk holds new rows [past, total)
 
   // warp 0 fills the ring; the new rows go to present before the tile that holds them
   auto issue = [&](int t) {
@@ -415,20 +421,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   aborted = named_bar_or(1, kThreads, aborted || flags[0] != 0);
   if (threadIdx.x == 0) grid_launch_dependents();  // streaming done: let the next kernel launch
   if (aborted) {
-    // copies in flight must land before the CTA exits; take part in the ticket so the
-    // group's counter stays consistent, write nothing
+    // copies in flight must land before the CTA exits; take part in the ticket (or the
+    // cluster exchange, with no visible key) so the group stays consistent, write nothing
     if (threadIdx.x == 0) {
       volatile int no_abort = 0;
       for (int t = t_fail; t < min(issued, t_fail + NST); ++t) mbar_wait(&full[t % NST], (t / NST) & 1, &no_abort);
       report(a.status, GQA_DEV_TIMEOUT);
-      if (nchunks > 1) {
+      if (!CL && nchunks > 1) {
         __threadfence();
         const int old = atomicAdd(&a.tickets[bh], 1);
         if (old == nchunks - 1) a.tickets[bh] = 0;
       }
     }
-    return;
+    if constexpr (CL) {
+      if (nchunks == 1) return;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) m[mt][0] = m[mt][1] = -INFINITY;
+    } else {
+      return;
+    }
   }
+  // cluster: this CTA's stages are free (nothing in flight), peers may write into them once
+  // every CTA has arrived
+  if (CL && nchunks > 1) cluster_arrive();
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -514,6 +529,74 @@ __global__ void __launch_bounds__(kThreads, 2)
       o[3] = from_f32<T>(num.w / den);
     }
     return;
+  }
+
+  if (CL) {
+    // ------------------------------------------------------------ cluster exchange
+    // the group's chunks are the CTAs of one cluster.  CTA `rank` owns float4 slice
+    // [rank * per, (rank + 1) * per) of the group's [R][D] output; every CTA pushes its
+    // (m, l) rows and the matching slice of its accumulator into the owner's shared memory
+    // (after the wacc regions), then combines its own slice from local data only
+    const int S = gridDim.x, rank = split;
+    const int n4 = R * (D / 4), per = (n4 + S - 1) / S;
+    float *rcv = wacc + kWarps * QROWS * D;                 // [S][per] float4 slices
+    float *rcv_m = rcv + QROWS * D + 4 * kMaxCluster;       // [S][QROWS] chunk maxima
+    float *rcv_l = rcv_m + kMaxCluster * QROWS;             // [S][QROWS] chunk sums
+    cluster_wait();  // every CTA has finished streaming: its stages may be written
+    const uint32_t rcv_s = smem_u32(rcv), rm_s = smem_u32(rcv_m), rl_s = smem_u32(rcv_l);
+    for (int idx = threadIdx.x; idx < n4; idx += kThreads) {
+      const int dst = idx / per;
+      cluster_st4(cluster_map(rcv_s + 16 * (rank * per + idx - dst * per), dst), merged(idx));
+    }
+    for (int t = threadIdx.x; t < S * R; t += kThreads) {
+      const int k = t / R, r = t % R;
+      cluster_st(cluster_map(rm_s + 4 * (rank * QROWS + r), k), row_m[r]);
+      cluster_st(cluster_map(rl_s + 4 * (rank * QROWS + r), k), row_l[r]);
+    }
+    cluster_sync();  // the partials sent to this CTA have landed
+    // per row: chunk weights (in place of the maxima) and the denominator (in row_l)
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+      float top = -INFINITY;
+      for (int k = 0; k < S; ++k) top = fmaxf(top, rcv_m[k * QROWS + r]);
+      const float mvis = top;
+      float ll = 0.f;
+      if (mvis != -INFINITY && a.has_sink) {
+        const float z = (a.head_sink ? a.head_sink[hkv * a.G + r % a.G] : 0.f) * kLog2e;
+        top = fmaxf(top, z);
+        ll = ex2(z - top);
+      }
+      for (int k = 0; k < S; ++k) {
+        const float mk = rcv_m[k * QROWS + r];
+        const float f = mk != -INFINITY ? ex2(mk - top) : 0.f;
+        if (f != 0.f) ll += rcv_l[k * QROWS + r] * f;
+        rcv_m[k * QROWS + r] = f;
+      }
+      row_l[r] = mvis == -INFINITY ? 0.f : ll;
+    }
+    __syncthreads();
+    const float4 *rcv4 = reinterpret_cast<const float4 *>(rcv);
+    const int lo4 = rank * per, hi4 = min(n4, lo4 + per);
+    for (int idx = lo4 + threadIdx.x; idx < hi4; idx += kThreads) {
+      const int r = idx / (D / 4), d4 = idx % (D / 4);
+      const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < S; ++k) {
+        const float f = rcv_m[k * QROWS + r];
+        if (f == 0.f) continue;  // chunk without a visible key (its accumulator is not read)
+        const float4 v = rcv4[k * per + idx - lo4];
+        sum.x += v.x * f;
+        sum.y += v.y * f;
+        sum.z += v.z * f;
+        sum.w += v.w * f;
+      }
+      const float den = row_l[r] > 0.f ? row_l[r] : 1.f;
+      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+      o[0] = from_f32<T>(sum.x / den);
+      o[1] = from_f32<T>(sum.y / den);
+      o[2] = from_f32<T>(sum.z / den);
+      o[3] = from_f32<T>(sum.w / den);
+    }
+    return;  // nothing reads this CTA's shared memory any more
   }
 
   // -------------------------------------------------------------- write the partial
@@ -602,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <typename T, int D, int MT, int NST>
+template <typename T, int D, int MT, int NST, bool CL>
 gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   using L = Smem<D, MT, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
@@ -610,7 +693,7 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   const long long outer = (long long)c.p.batch * c.p.kv_heads;
   if (!encode_kv_map(&tk, c.present_k, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
   if (!encode_kv_map(&tv, c.present_v, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
-  auto kern = decode_split_kernel<T, D, MT, NST>;
+  auto kern = decode_split_kernel<T, D, MT, NST, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -618,14 +701,23 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = c.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (CL) {  // the chunks of one group form one cluster
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = dp.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
+
+template <typename T, bool CL> gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a);
 
 template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   const gqa_params &p = c.p;
@@ -666,18 +758,19 @@ template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, c
     a.score_mul = p.scale * kLog2e;
     a.cap_mul = 0.f;
   }
-  if (dp.deep) {  // 192 KB of stages: one CTA per SM
-    if (p.head_dim == 128 && dp.mtiles == 1) return launch_cfg<T, 128, 1, 6>(c, dp, a);
-    if (p.head_dim == 64 && dp.mtiles == 1) return launch_cfg<T, 64, 1, 12>(c, dp, a);
-  }
-  if (p.head_dim == 128) {
-    if (dp.mtiles == 1) return launch_cfg<T, 128, 1, 3>(c, dp, a);
-    if (dp.mtiles == 2) return launch_cfg<T, 128, 2, 3>(c, dp, a);
-  } else if (p.head_dim == 64) {
-    if (dp.mtiles == 1) return launch_cfg<T, 64, 1, 6>(c, dp, a);
-    if (dp.mtiles == 2) return launch_cfg<T, 64, 2, 6>(c, dp, a);
-    if (dp.mtiles == 3) return launch_cfg<T, 64, 3, 6>(c, dp, a);
-    if (dp.mtiles == 4) return launch_cfg<T, 64, 4, 6>(c, dp, a);
+  if (dp.cluster) return dispatch<T, true>(c, dp, a);
+  return dispatch<T, false>(c, dp, a);
+}
+
+template <typename T, bool CL> gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
+  if (c.p.head_dim == 128) {
+    if (dp.mtiles == 1) return launch_cfg<T, 128, 1, 3, CL>(c, dp, a);
+    if (dp.mtiles == 2) return launch_cfg<T, 128, 2, 3, CL>(c, dp, a);
+  } else if (c.p.head_dim == 64) {
+    if (dp.mtiles == 1) return launch_cfg<T, 64, 1, 6, CL>(c, dp, a);
+    if (dp.mtiles == 2) return launch_cfg<T, 64, 2, 6, CL>(c, dp, a);
+    if (dp.mtiles == 3) return launch_cfg<T, 64, 3, 6, CL>(c, dp, a);
+    if (dp.mtiles == 4) return launch_cfg<T, 64, 4, 6, CL>(c, dp, a);
   }
   return GQA_ERR_UNSUPPORTED;
 }

@@ -106,17 +106,14 @@ DecodePlan decode_plan(const gqa_params &p) {
   // (608), chunks of at most 4096 keys (partials stay small) and at least 256 keys
   // (per-CTA setup stays small)
   const long long units = (long long)p.batch * p.kv_heads;
-  if (d.rows <= 16 && units <= 152 && lmax <= 8192) {
-    // small bandwidth-bound step: one CTA per group streams the whole band through a deep
-    // ring, alone on its SM; no chunk partials to combine and no workspace
-    d.splits = 1;
-    d.deep = true;
-    return d;
-  }
   long long s = std::max<long long>((608 + units - 1) / units, (lmax + 4095) / 4096);
   s = std::min<long long>(s, std::max<long long>(1, (lmax + 255) / 256));
   s = std::min<long long>(s, kDecodeMaxSplits);
   d.splits = (int)std::max<long long>(1, s);
+  // a launch that fits one wave (two CTAs on each of 152 SMs) combines its chunks through
+  // distributed shared memory; longer launches keep the workspace partials, since clusters
+  // of up to 8 CTAs leave SMs of a GPC unused once CTAs queue for slots
+  d.cluster = d.splits >= 2 && d.splits <= kDecodeMaxCluster && units * d.splits <= 304;
   return d;
 }
 
@@ -130,7 +127,7 @@ WsLayout workspace_layout(const gqa_params &p, bool need_q_rot) {
     off = align_up(off + w.q_rot_bytes, kAlign);
   }
   DecodePlan d = decode_plan(p);
-  if (d.eligible && d.splits > 1) {
+  if (d.eligible && d.splits > 1 && !d.cluster) {  // cluster groups combine in shared memory
     const size_t groups = (size_t)p.batch * p.kv_heads;
     const size_t slots = groups * d.splits;
     w.part_acc_off = off;
@@ -218,7 +215,7 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   const DecodePlan dp = decode_plan(c.p);
   // the split decode kernel appends and rotates itself; every other path runs K1 first
   const bool fused = mode == kDecode && dp.eligible;
-  size_t need = fused ? (dp.splits > 1 ? wl.total : 0) : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
+  size_t need = fused ? (dp.splits > 1 && !dp.cluster ? wl.total : 0) : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
   if (need > 0) {
     if (!workspace || !aligned16(workspace)) return GQA_ERR_WORKSPACE;
     if (workspace_bytes < need) return GQA_ERR_WORKSPACE;

@@ -36,12 +36,13 @@ struct Call {
 // Split-KV decode plan.  The visible band of each (b, kv head) group is cut into `splits`
 // equal chunks (one CTA each); `splits` depends on the params only, so the workspace does.
 constexpr int kDecodeMaxSplits = 64;
+constexpr int kDecodeMaxCluster = 8;  // portable cluster size
 struct DecodePlan {
   bool eligible = false;  // the split kernel handles these params
   int rows = 0;           // R = G * curr query rows per CTA
   int mtiles = 0;         // ceil(R / 16)
   int splits = 1;         // chunks per group
-  bool deep = false;      // one CTA per SM with a deep ring (small bandwidth-bound steps)
+  bool cluster = false;   // 2..8 chunks: one cluster per group, combined in shared memory
 };
 
 struct WsLayout {

@@ -128,20 +128,18 @@ def test_workspace_checked_before_launch(g):
 
 
 def splits(B, Hkv, cap, window, curr=1, R=4):
-    """Chunks per group: one for small bandwidth-bound steps (<= 16 rows, <= 152 groups,
-    band <= 8192 keys), else two waves of 608 CTAs with chunks of 256..4096 keys."""
+    """Chunks per group: two waves of 608 CTAs, chunks of 256..4096 keys, at most 64."""
     lmax = cap if window < 0 else min(cap, window + curr - 1)
     units = B * Hkv
-    if R <= 16 and units <= 152 and lmax <= 8192:
-        return 1
     s = max(-(-608 // units), -(-lmax // 4096))
     return min(64, max(1, min(s, max(1, -(-lmax // 256)))))
 
 
 def decode_ws(B, Hkv, R, D, S):
     """Split decode workspace: fp32 acc [R][D] and (m, l) per (group, chunk) slot, one ticket
-    per group; 256-byte aligned; nothing when a group is one chunk."""
-    if S == 1:
+    per group; 256-byte aligned.  Nothing when a group is one chunk, nor when its 2..8 chunks
+    form one thread-block cluster (launches of at most 304 CTAs) and combine in shared memory."""
+    if S == 1 or (S <= 8 and B * Hkv * S <= 304):
         return 0
     al = lambda x: (x + 255) // 256 * 256
     slots = B * Hkv * S
@@ -161,7 +159,19 @@ def test_workspace_sizes(g):
     # long decode: G=8, R=8, 8 chunks of up to 4096 keys
     S = splits(64, 8, 32768, -1, R=8)
     assert S == 8
-    assert ws(batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1) == decode_ws(64, 8, 8, 128, S)
+    assert ws(batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1) == decode_ws(64, 8, 8, 128, S) > 0
+    # one wave of clusters (8 groups x 8 chunks): combined in shared memory, no workspace
+    S = splits(1, 8, 2048, -1, R=8)
+    assert S == 8
+    assert ws(batch=1, q_heads=64, kv_heads=8, cap_present=2048, window=-1) == decode_ws(1, 8, 8, 128, S) == 0
+    # the sliding-window decode: 64 groups x 4 chunks of 256 keys
+    S = splits(8, 8, 4096, 1024, R=4)
+    assert S == 4
+    assert ws(batch=8, q_heads=32, kv_heads=8, cap_present=4096, window=1024) == 0
+    # ten chunks in one wave: past the cluster size, back to partials in the workspace
+    S = splits(2, 8, 2560, -1, R=8)
+    assert S == 10
+    assert ws(batch=2, q_heads=64, kv_heads=8, cap_present=2560, window=-1) == decode_ws(2, 8, 8, 128, S) > 0
     # more than 32 query rows per group at D=128: the SIMT kernel, no split workspace
     assert ws(q_heads=64, kv_heads=2, q_len=2, window=-1) == 0
     # prefill-sized q_len never needs decode partials

@@ -56,6 +56,36 @@ def test_decode_chunk_boundaries(seqlens):
     assert_close(out_rows(r["out"], c), ref, "bf16")
 
 
+def plan_splits(B, Hkv, cap, window, curr):
+    """Chunks per group as the library plans them (mirrors the host planner's rule)."""
+    lmax = cap if window < 0 else min(cap, window + curr - 1)
+    s = max(-(-608 // (B * Hkv)), -(-lmax // 4096))
+    return min(64, max(1, min(s, max(1, -(-lmax // 256)))))
+
+
+@pytest.mark.parametrize("dgc", [(128, 8, 1), (128, 4, 4), (128, 8, 4), (64, 16, 4), (64, 8, 1)])
+@pytest.mark.parametrize("cap,S", [(520, 3), (1100, 5), (2000, 8)])
+@pytest.mark.parametrize("sink,softcap", [("head", 0.0), ("smooth", 30.0), ("none", 0.0)])
+def test_decode_cluster_combine(dgc, cap, S, sink, softcap):
+    """Groups of 2..8 chunks combined through distributed shared memory: sequences of one
+    chunk (finished in place), of fewer chunks than the cluster (idle CTAs still take part)
+    and of every chunk; output slices that do not divide evenly among the CTAs."""
+    D, G, curr = dgc
+    B, Hkv = 4, 2
+    assert plan_splits(B, Hkv, cap, -1, curr) == S and B * Hkv * S <= 304
+    w = Workload("decc", 340, "decode", "f16" if softcap else "bf16", B, G * Hkv, Hkv, D, curr, cap, 0, cap - curr,
+                 softcap=softcap, head_sink=sink == "head", smooth_softmax=int(sink == "smooth"))
+    seqlens = np.array([0, 70, cap // 2 + 3, cap - curr], np.int32)
+    c = make_case(w, seed_offset=S, seqlens=seqlens)
+    r = run_gpu(c, "decode")
+    assert r["status"] == 0
+    ref, pk, pv, st = oracle_ref(c)
+    assert st == 0
+    np.testing.assert_array_equal(storage(r["present_k"]), pk)
+    np.testing.assert_array_equal(storage(r["present_v"]), pv)
+    assert_close(out_rows(r["out"], c), ref, w.dtype, "cluster %s" % ((dgc, cap, S, sink, softcap),))
+
+
 @pytest.mark.parametrize("garbage", ["huge", "nonfinite"])
 def test_stale_slots_do_not_change_output(garbage):
     base = small_case("bf16", 128, 8, 2, 50, "head", 0.0, seed=5)
