@@ -69,8 +69,8 @@ template <int D, int MT, int NST> struct Smem {
   static constexpr int kQOff = NST * kStageBytes;
   static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], empty[NST]
   static constexpr int kRedOff = kBarOff + 2 * NST * 8;                   // red_m, red_l [4][QROWS]
-  static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l [QROWS]
-  static constexpr int kFlagOff = kRowOff + 2 * kQRows * 4;
+  static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l, sink [QROWS]
+  static constexpr int kFlagOff = kRowOff + 3 * kQRows * 4;
   static constexpr int kBytes = kFlagOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
   // per-warp merge regions and the combine's chunk statistics reuse the stages
@@ -79,6 +79,19 @@ template <int D, int MT, int NST> struct Smem {
   static_assert(((kWarps + 1) * kQRows * D + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <= NST * kStageBytes,
                 "cluster exchange buffers must fit in the stages");
 };
+
+// four consecutive outputs in one 8-byte store
+template <typename T> __device__ __forceinline__ void store4(T *o, float x, float y, float z, float w) {
+  union {
+    T e[4];
+    uint2 u;
+  } v;
+  v.e[0] = from_f32<T>(x);
+  v.e[1] = from_f32<T>(y);
+  v.e[2] = from_f32<T>(z);
+  v.e[3] = from_f32<T>(w);
+  *reinterpret_cast<uint2 *>(o) = v.u;
+}
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() {
@@ -153,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float *red_l = red_m + kWarps * QROWS;
   float *row_m = reinterpret_cast<float *>(smem + L::kRowOff);
   float *row_l = row_m + QROWS;
+  float *sink_z = row_l + QROWS;  // sink logit of row r in the exp2 domain (0 when smooth_softmax)
   volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlagOff);  // [0] abort, [1] last
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
@@ -175,8 +189,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   grid_dependency_wait();
   __syncthreads();
 
-  // the past length and the raw query rows are loaded together: their latencies overlap
+  // the past length, the sink logits and the raw query rows are loaded together: their
+  // latencies overlap
   const int past = a.seqlens[b];
+  const float zsink = (threadIdx.x < R && a.head_sink) ? a.head_sink[hkv * a.G + threadIdx.x % a.G] : 0.f;
   constexpr int QITEMS = (QROWS * (DCH / 2) + kThreads - 1) / kThreads;  // chunk pairs per thread
   uint4 qraw[QITEMS][2];
 #pragma unroll
@@ -259,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       *reinterpret_cast<uint4 *>(qs + (c2 >> 3) * (QROWS * 128) + sw128(r, c2 & 7)) = y2;
     }
   }
+  if (threadIdx.x < QROWS) sink_z[threadIdx.x] = zsink * kLog2e;
   __syncthreads();
 
   float m[MT][2], l[MT][2];
@@ -443,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   // cluster: this CTA's stages are free (nothing in flight), peers may write into them once
   // every CTA has arrived
-  if (CL && nchunks > 1) cluster_arrive();
+  if (CL && nchunks > 1) cluster_arrive_relaxed();
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -510,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (mm != -INFINITY) {
         float top = mm, sink_term = 0.f;
         if (a.has_sink) {
-          const float z = (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e;
+          const float z = sink_z[r];
           top = fmaxf(mm, z);
           sink_term = ex2(z - top);
         }
@@ -523,10 +540,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         den = row_l[r] * f + sink_term;
       }
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-      o[0] = from_f32<T>(num.x / den);
-      o[1] = from_f32<T>(num.y / den);
-      o[2] = from_f32<T>(num.z / den);
-      o[3] = from_f32<T>(num.w / den);
+      store4(o, num.x / den, num.y / den, num.z / den, num.w / den);
     }
     return;
   }
@@ -561,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float mvis = top;
       float ll = 0.f;
       if (mvis != -INFINITY && a.has_sink) {
-        const float z = (a.head_sink ? a.head_sink[hkv * a.G + r % a.G] : 0.f) * kLog2e;
+        const float z = sink_z[r];
         top = fmaxf(top, z);
         ll = ex2(z - top);
       }
@@ -591,10 +605,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const float den = row_l[r] > 0.f ? row_l[r] : 1.f;
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-      o[0] = from_f32<T>(sum.x / den);
-      o[1] = from_f32<T>(sum.y / den);
-      o[2] = from_f32<T>(sum.z / den);
-      o[3] = from_f32<T>(sum.w / den);
+      store4(o, sum.x / den, sum.y / den, sum.z / den, sum.w / den);
     }
     return;  // nothing reads this CTA's shared memory any more
   }
@@ -630,12 +641,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   for (int r = threadIdx.x; r < R; r += kThreads) {
-    const int hq = hkv * a.G + r % a.G;
     float mm = -INFINITY;
     for (int c = 0; c < nchunks; ++c) mm = fmaxf(mm, cm[c * R + r]);
     float top = mm, sink_term = 0.f;
     if (mm != -INFINITY && a.has_sink) {
-      const float z = (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e;
+      const float z = sink_z[r];
       top = fmaxf(mm, z);
       sink_term = ex2(z - top);
     }
@@ -678,10 +688,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
     const float den = row_l[r] > 0.f ? row_l[r] : 1.f;  // no visible key: the sums are 0
     T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-    o[0] = from_f32<T>(sum[u].x / den);
-    o[1] = from_f32<T>(sum[u].y / den);
-    o[2] = from_f32<T>(sum[u].z / den);
-    o[3] = from_f32<T>(sum[u].w / den);
+    store4(o, sum[u].x / den, sum[u].y / den, sum[u].z / den, sum[u].w / den);
   }
 }
 
