@@ -73,10 +73,13 @@ template <int D, int MT, int NST> struct Smem {
   static constexpr int kFlagOff = kRowOff + 3 * kQRows * 4;
   static constexpr int kBytes = kFlagOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
-  // per-warp merge regions and the combine's chunk statistics reuse the stages
-  static_assert(kWarps * kQRows * D * 4 <= NST * kStageBytes, "merge regions must fit in the stages");
+  // per-warp merge regions (rows padded by 4 floats: the fragment stores of one warp
+  // instruction then spread over all banks) and the combine's chunk statistics reuse the stages
+  static constexpr int kAccStride = D + 4;
+  static_assert(kWarps * kQRows * kAccStride * 4 <= NST * kStageBytes, "merge regions must fit in the stages");
   static_assert(2 * kMaxSplits * kQRows * 4 <= NST * kStageBytes, "chunk statistics must fit in the stages");
-  static_assert(((kWarps + 1) * kQRows * D + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <= NST * kStageBytes,
+  static_assert((kWarps * kQRows * kAccStride + kQRows * D + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <=
+                    NST * kStageBytes,
                 "cluster exchange buffers must fit in the stages");
 };
 
@@ -488,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   // every warp writes its rescaled accumulator to its own region (the stages are free now),
   // then all threads sum the four regions in a fixed order (deterministic)
-  float *wacc = reinterpret_cast<float *>(stages);  // [kWarps][QROWS][D]
+  constexpr int AST = L::kAccStride;
+  float *wacc = reinterpret_cast<float *>(stages);  // [kWarps][QROWS][AST]
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -496,18 +500,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int row = 16 * mt + (lane >> 2) + 8 * h;
       const float mm = row_m[row];
       const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
-      float *dst = wacc + ((size_t)warp * QROWS + row) * D + 2 * (lane & 3);
+      float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane & 3);
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn)
         *reinterpret_cast<float2 *>(dst + 8 * dn) = make_float2(acc[mt][dn][2 * h] * f, acc[mt][dn][2 * h + 1] * f);
     }
   __syncthreads();
   auto merged = [&](int idx4) {  // float4 idx4 of the CTA's [R][D] accumulator
-    const float4 *w4 = reinterpret_cast<const float4 *>(wacc);
-    float4 v = w4[idx4];
+    const float4 *w4 = reinterpret_cast<const float4 *>(wacc) + (idx4 / (D / 4)) * (AST / 4) + idx4 % (D / 4);
+    float4 v = w4[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) {
-      const float4 u = w4[w * (QROWS * D / 4) + idx4];
+      const float4 u = w4[w * (QROWS * AST / 4)];
       v.x += u.x;
       v.y += u.y;
       v.z += u.z;
@@ -553,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // (after the wacc regions), then combines its own slice from local data only
     const int S = gridDim.x, rank = split;
     const int n4 = R * (D / 4), per = (n4 + S - 1) / S;
-    float *rcv = wacc + kWarps * QROWS * D;                 // [S][per] float4 slices
+    float *rcv = wacc + kWarps * QROWS * AST;               // [S][per] float4 slices
     float *rcv_m = rcv + QROWS * D + 4 * kMaxCluster;       // [S][QROWS] chunk maxima
     float *rcv_l = rcv_m + kMaxCluster * QROWS;             // [S][QROWS] chunk sums
     cluster_wait();  // every CTA has finished streaming: its stages may be written
