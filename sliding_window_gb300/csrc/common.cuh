@@ -131,7 +131,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up (returns false) when
-// *abort is set by another thread or when kWaitLimitNs has passed, in which case it
+// *abort is set by another thread or when kWaitLimitCycles have passed, in which case it
 // sets *abort itself so that every role of the CTA winds down.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -145,6 +145,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         return false;
       }
     }
+  }
+}
+
+// As mbar_wait, for a phase completed by other CTAs of the cluster: acquire at cluster scope,
+// so their stores are visible once it returns true.  Bounded by kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 15u) == 15u && clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
 
@@ -219,6 +237,20 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
 // the next cluster barrier.
 __device__ __forceinline__ void cluster_st(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Stores into another CTA's shared memory that complete a transaction count on an mbarrier
+// of that CTA (both addresses from cluster_map): the receiver waits on its own barrier
+// instead of a cluster-wide one.
+__device__ __forceinline__ void cluster_st_async4(uint32_t addr, float4 v, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_st_async2(uint32_t addr, float x, float y, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(x), "f"(y), "r"(mbar)
+               : "memory");
 }
 __device__ __forceinline__ void cluster_st4(uint32_t addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),

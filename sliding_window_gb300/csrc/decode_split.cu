@@ -67,8 +67,8 @@ template <int D, int MT, int NST> struct Smem {
   static constexpr int kQRows = MT * 16;
   static constexpr int kStagesOff = 0;
   static constexpr int kQOff = NST * kStageBytes;
-  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], empty[NST]
-  static constexpr int kRedOff = kBarOff + 2 * NST * 8;                   // red_m, red_l [4][QROWS]
+  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], empty[NST], xbar
+  static constexpr int kRedOff = kBarOff + (2 * NST + 1) * 8;             // red_m, red_l [4][QROWS]
   static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l, sink [QROWS]
   static constexpr int kFlagOff = kRowOff + 3 * kQRows * 4;
   static constexpr int kBytes = kFlagOff + 16;
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t *qs = smem + L::kQOff;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
   uint64_t *empty = full + NST;
+  uint64_t *xbar = empty + NST;  // cluster exchange: the partials sent to this CTA have landed
   float *red_m = reinterpret_cast<float *>(smem + L::kRedOff);
   float *red_l = red_m + kWarps * QROWS;
   float *row_m = reinterpret_cast<float *>(smem + L::kRowOff);
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kWarps);
     }
+    mbar_init(xbar, 1);
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
@@ -437,8 +439,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // -------------------------------------------------------------- merge the 4 warps
-  // one decision for the whole CTA: a timed-out wait anywhere aborts it
-  aborted = named_bar_or(1, kThreads, aborted || flags[0] != 0);
+  // per-warp row statistics (outside the stages: safe while aborted copies still land)
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float lv = l[mt][h];
+      lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+      lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+      if ((lane & 3) == 0) {
+        const int row = 16 * mt + (lane >> 2) + 8 * h;
+        red_m[warp * QROWS + row] = m[mt][h];
+        red_l[warp * QROWS + row] = lv;
+      }
+    }
+  // one decision for the whole CTA (a timed-out wait anywhere aborts it), taken by the
+  // barrier that publishes the statistics
+  aborted = __syncthreads_or(aborted || flags[0] != 0);
   if (threadIdx.x == 0) grid_launch_dependents();  // streaming done: let the next kernel launch
   if (aborted) {
     // copies in flight must land before the CTA exits; take part in the ticket (or the
@@ -457,6 +474,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (nchunks == 1) return;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) m[mt][0] = m[mt][1] = -INFINITY;
+      for (int i = threadIdx.x; i < kWarps * QROWS; i += kThreads) red_m[i] = -INFINITY;
+      __syncthreads();  // uniform branch; thread 0 has drained the copies
     } else {
       return;
     }
@@ -464,20 +483,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   // cluster: this CTA's stages are free (nothing in flight), peers may write into them once
   // every CTA has arrived
   if (CL && nchunks > 1) cluster_arrive_relaxed();
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float lv = l[mt][h];
-      lv += __shfl_xor_sync(0xffffffffu, lv, 1);
-      lv += __shfl_xor_sync(0xffffffffu, lv, 2);
-      if ((lane & 3) == 0) {
-        const int row = 16 * mt + (lane >> 2) + 8 * h;
-        red_m[warp * QROWS + row] = m[mt][h];
-        red_l[warp * QROWS + row] = lv;
-      }
-    }
-  __syncthreads();
   if (threadIdx.x < QROWS) {
     const int row = threadIdx.x;
     float mm = -INFINITY;
@@ -498,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = 16 * mt + (lane >> 2) + 8 * h;
+      if (row >= R) continue;  // padding rows of the MMA tile are never read
       const float mm = row_m[row];
       const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
       float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane & 3);
@@ -544,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         den = row_l[r] * f + sink_term;
       }
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-      store4(o, num.x / den, num.y / den, num.z / den, num.w / den);
+      const float inv = __frcp_rn(den);
+      store4(o, num.x * inv, num.y * inv, num.z * inv, num.w * inv);
     }
     return;
   }
@@ -554,62 +561,67 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the group's chunks are the CTAs of one cluster.  CTA `rank` owns float4 slice
     // [rank * per, (rank + 1) * per) of the group's [R][D] output; every CTA pushes its
     // (m, l) rows and the matching slice of its accumulator into the owner's shared memory
-    // (after the wacc regions), then combines its own slice from local data only
+    // (after the wacc regions) with asynchronous stores that count down the owner's xbar.
+    // The owner waits for exactly those bytes and combines its slice from local data; once
+    // they have landed nothing else writes to or reads from its shared memory, so it may exit
     const int S = gridDim.x, rank = split;
     const int n4 = R * (D / 4), per = (n4 + S - 1) / S;
     float *rcv = wacc + kWarps * QROWS * AST;               // [S][per] float4 slices
-    float *rcv_m = rcv + QROWS * D + 4 * kMaxCluster;       // [S][QROWS] chunk maxima
-    float *rcv_l = rcv_m + kMaxCluster * QROWS;             // [S][QROWS] chunk sums
+    float2 *rcv_ml = reinterpret_cast<float2 *>(rcv + QROWS * D + 4 * kMaxCluster);  // [S][QROWS] (m, l)
     cluster_wait();  // every CTA has finished streaming: its stages may be written
-    const uint32_t rcv_s = smem_u32(rcv), rm_s = smem_u32(rcv_m), rl_s = smem_u32(rcv_l);
-    for (int idx = threadIdx.x; idx < n4; idx += kThreads) {
-      const int dst = idx / per;
-      cluster_st4(cluster_map(rcv_s + 16 * (rank * per + idx - dst * per), dst), merged(idx));
-    }
+    const uint32_t rcv_s = smem_u32(rcv), rml_s = smem_u32(rcv_ml), xb_s = smem_u32(xbar);
     for (int t = threadIdx.x; t < S * R; t += kThreads) {
       const int k = t / R, r = t % R;
-      cluster_st(cluster_map(rm_s + 4 * (rank * QROWS + r), k), row_m[r]);
-      cluster_st(cluster_map(rl_s + 4 * (rank * QROWS + r), k), row_l[r]);
+      cluster_st_async2(cluster_map(rml_s + 8 * (rank * QROWS + r), k), row_m[r], row_l[r], cluster_map(xb_s, k));
     }
-    cluster_sync();  // the partials sent to this CTA have landed
-    // per row: chunk weights (in place of the maxima) and the denominator (in row_l)
-    for (int r = threadIdx.x; r < R; r += kThreads) {
-      float top = -INFINITY;
-      for (int k = 0; k < S; ++k) top = fmaxf(top, rcv_m[k * QROWS + r]);
-      const float mvis = top;
-      float ll = 0.f;
-      if (mvis != -INFINITY && a.has_sink) {
-        const float z = sink_z[r];
-        top = fmaxf(top, z);
-        ll = ex2(z - top);
-      }
-      for (int k = 0; k < S; ++k) {
-        const float mk = rcv_m[k * QROWS + r];
-        const float f = mk != -INFINITY ? ex2(mk - top) : 0.f;
-        if (f != 0.f) ll += rcv_l[k * QROWS + r] * f;
-        rcv_m[k * QROWS + r] = f;
-      }
-      row_l[r] = mvis == -INFINITY ? 0.f : ll;
+    for (int idx = threadIdx.x; idx < n4; idx += kThreads) {
+      const int dst = idx / per;
+      cluster_st_async4(cluster_map(rcv_s + 16 * (rank * per + idx - dst * per), dst), merged(idx),
+                        cluster_map(xb_s, dst));
     }
-    __syncthreads();
-    const float4 *rcv4 = reinterpret_cast<const float4 *>(rcv);
     const int lo4 = rank * per, hi4 = min(n4, lo4 + per);
+    if (threadIdx.x == 0) mbar_expect_tx(xbar, S * (max(0, hi4 - lo4) * 16 + R * 8));
+    if (!mbar_wait_cluster(xbar, 0)) {  // a peer never delivered: nothing valid to combine
+      if (threadIdx.x == 0) report(a.status, GQA_DEV_TIMEOUT);
+      return;
+    }
+    // each output float4 weighs the chunks of its row itself: no second pass, no barrier
+    const float4 *rcv4 = reinterpret_cast<const float4 *>(rcv);
     for (int idx = lo4 + threadIdx.x; idx < hi4; idx += kThreads) {
       const int r = idx / (D / 4), d4 = idx % (D / 4);
       const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
-      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = 0; k < S; ++k) {
-        const float f = rcv_m[k * QROWS + r];
-        if (f == 0.f) continue;  // chunk without a visible key (its accumulator is not read)
-        const float4 v = rcv4[k * per + idx - lo4];
-        sum.x += v.x * f;
-        sum.y += v.y * f;
-        sum.z += v.z * f;
-        sum.w += v.w * f;
+      float mk[kMaxCluster];
+      float top = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kMaxCluster; ++k) {
+        mk[k] = k < S ? rcv_ml[k * QROWS + r].x : -INFINITY;
+        top = fmaxf(top, mk[k]);
       }
-      const float den = row_l[r] > 0.f ? row_l[r] : 1.f;
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 1.f;  // no visible key: the sums stay 0
+      if (top != -INFINITY) {
+        float ll = 0.f;
+        if (a.has_sink) {
+          const float z = sink_z[r];
+          top = fmaxf(top, z);
+          ll = ex2(z - top);
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxCluster; ++k) {
+          if (mk[k] == -INFINITY) continue;  // past the cluster, or a chunk without a visible key
+          const float f = ex2(mk[k] - top);
+          ll += rcv_ml[k * QROWS + r].y * f;
+          const float4 v = rcv4[k * per + idx - lo4];
+          sum.x += v.x * f;
+          sum.y += v.y * f;
+          sum.z += v.z * f;
+          sum.w += v.w * f;
+        }
+        den = ll;
+      }
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-      store4(o, sum.x / den, sum.y / den, sum.z / den, sum.w / den);
+      const float inv = __frcp_rn(den);
+      store4(o, sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
     }
     return;  // nothing reads this CTA's shared memory any more
   }
@@ -692,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
     const float den = row_l[r] > 0.f ? row_l[r] : 1.f;  // no visible key: the sums are 0
     T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
-    store4(o, sum[u].x / den, sum[u].y / den, sum[u].z / den, sum[u].w / den);
+    const float inv = __frcp_rn(den);
+    store4(o, sum[u].x * inv, sum[u].y * inv, sum[u].z * inv, sum[u].w * inv);
   }
 }
 
