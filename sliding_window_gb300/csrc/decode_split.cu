@@ -248,11 +248,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_expect_tx(&full[s], L::kStageBytes);
       uint8_t *kdst = stages + s * L::kStageBytes;
       uint8_t *vdst = kdst + L::kTileBytes;
-#pragma unroll
-      for (int db = 0; db < D / 64; ++db) {
-        tma_load_3d(kdst + db * (KT * 128), &tmk, db * 64, k0, bh, &full[s]);
-        tma_load_3d(vdst + db * (KT * 128), &tmv, db * 64, k0, bh, &full[s]);
-      }
+      tma_load_4d(kdst, &tmk, 0, k0, 0, bh, &full[s]);  // [D/64][KT][64], one copy each
+      tma_load_4d(vdst, &tmv, 0, k0, 0, bh, &full[s]);
     }
     __syncwarp();
   };
@@ -715,8 +712,8 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
   CUtensorMap tk, tv;
   const long long outer = (long long)c.p.batch * c.p.kv_heads;
-  if (!encode_kv_map(&tk, c.present_k, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
-  if (!encode_kv_map(&tv, c.present_v, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_tile_map(&tk, c.present_k, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_tile_map(&tv, c.present_v, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
   auto kern = decode_split_kernel<T, D, MT, NST, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;

@@ -79,6 +79,23 @@ bool encode_kv_map(CUtensorMap *map, const void *base, int inner, int mid, long 
   return r == CUDA_SUCCESS;
 }
 
+bool encode_kv_tile_map(CUtensorMap *map, const void *base, int D, int rows, long long outer, int box_rows,
+                        int esize) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  // dims (64 columns, row, 64-column half, group): strides need not increase, so one box
+  // {64, box_rows, D/64, 1} lands as [half][row][64 columns], the same image as D/64
+  // separate 3D boxes of 64 columns
+  cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64), (cuuint64_t)outer};
+  cuuint64_t strides[3] = {(cuuint64_t)D * esize, (cuuint64_t)64 * esize, (cuuint64_t)rows * D * esize};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (cuuint32_t)(D / 64), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B, int box_rows, int esize) {
   auto fn = encode_fn();
   if (!fn) return false;

@@ -61,6 +61,10 @@ WsLayout workspace_layout(const gqa_params &p, bool need_q_rot);
 // {64, box_mid, 1}.  Returns false on failure.
 bool encode_kv_map(CUtensorMap *map, const void *base, int inner, int mid, long long outer, int box_mid,
                    int esize);
+// 4D map over the same [outer, rows, D] tensor of 16-bit elements whose single box of
+// box_rows rows lands as [D/64][box_rows][64 columns], 128B-swizzled: one copy per tile.
+bool encode_kv_tile_map(CUtensorMap *map, const void *base, int D, int rows, long long outer, int box_rows,
+                        int esize);
 // 4D map over q laid out [B, L, H, D]: box {64, 1, box_rows, 1}, 128B swizzle.
 bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B, int box_rows, int esize);
 
