@@ -76,3 +76,16 @@ def test_prefill_stale_garbage_is_masked():
     r = run_gpu(c, "prefill")
     ref, *_ = oracle_ref(c)
     assert_close(out_rows(r["out"], c), ref, "bf16")
+
+
+@pytest.mark.parametrize("dtype,softcap", [("bf16", 0.0), ("f16", 0.0), ("bf16", 50.0)])
+def test_prefill_tc_sharp_scores(dtype, softcap):
+    """Scale 1 (scores of standard deviation ~11): exponents far below -125 in tiles with no
+    masked key, where part of exp2 runs as a polynomial with its argument clamped."""
+    w = Workload("presharp", 420, "prefill", dtype, 2, 8, 2, 128, 700, 740, 0, 0, windows=(-1,), scale=1.0,
+                 softcap=softcap, head_sink=True)
+    c = make_case(w, seed_offset=1)
+    r = run_gpu(c, "prefill")
+    assert r["status"] == 0
+    ref, *_ = oracle_ref(c)
+    assert_close(out_rows(r["out"], c), ref, dtype, "sharp %s" % ((dtype, softcap),))
