@@ -321,11 +321,9 @@ def run_ours(args, rank, world, local_rank):
     elapsed = time_graphs(graphs, stream)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    t = torch.tensor([elapsed], dtype=torch.float64, device=device)
     if world > 1:
         torch.distributed.barrier()
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, world, device)
     launches_per_step = 2 * w.layers  # append kernel + attention kernel per layer
 
     # the dominant kernel (attention) alone, same steps and buffers, live CUDA events
@@ -338,13 +336,32 @@ def run_ours(args, rank, world, local_rank):
     k_elapsed = time_graphs(attend, stream)
     # end to end through the public call with host buffers: H2D of the step's inputs from
     # pinned memory, the call, D2H of the output, every step
+    if world > 1:
+        torch.distributed.barrier()
     e2e = run_e2e(args, sets, stream, w, units)
+    if world > 1:
+        torch.distributed.barrier()
+    e2e["elapsed"] = max_over_ranks(e2e["elapsed"], world, device)
     status = [int(L["status"].item()) for s in sets for L in s.layers]
     if any(status):
         raise RuntimeError("device status bits set during the bench: %s" % status)
     return dict(w=w, elapsed=elapsed, units=units, kunits=kunits, unit=unit, clocks=clocks, nsets=nsets,
                 per_set=per_set, k_elapsed=k_elapsed, e2e=e2e, launches=launches_per_step * args.steps,
                 seqs=first.seqlens())
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of one float over all ranks: a job's time is its slowest rank's."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank_step: float, steps: int, world: int, elapsed: float) -> float:
+    """Whole-job throughput: every rank processes the same per-step work (weak scaling)."""
+    return units_per_rank_step * steps * world / elapsed
 
 
 def run_e2e(args, sets, stream, w, units):
@@ -536,7 +553,7 @@ def reference_arm(w, args):
 def report(args, w, r, world):
     peaks, src = load_peaks()
     units, kunits, unit = r["units"], r["kunits"], r["unit"]
-    value = units * args.steps * world / r["elapsed"]
+    value = job_rate(units, args.steps, world, r["elapsed"])
     k_time = r["k_elapsed"] / args.steps
     if unit == "GB/s":
         peak, bound, punit = float(peaks["hbm_gbs"]), "hbm", "GB/s"
@@ -562,7 +579,7 @@ def report(args, w, r, world):
                      "kernel_ms": round(k_time * 1e3, 6), "peak_source": src},
         "clocks": r["clocks"],
         "gpu_launches": r["launches"],
-        "e2e": {"value": round(units * args.steps / r["e2e"]["elapsed"], 3), "unit": unit,
+        "e2e": {"value": round(job_rate(units, args.steps, world, r["e2e"]["elapsed"]), 3), "unit": unit,
                 "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"]},
     }
     if not args.no_cpu_baseline and world == 1:
