@@ -78,6 +78,12 @@ def _load():
         lib.oracle_attend_row.argtypes = [vp, vp, vp, i64, i64, vp, i32, i32, f64, f64, i32, f64, vp]
         lib.oracle_attend_row.restype = None
         lib.oracle_attention.argtypes = [i32] * 9 + [f64, f64] + [i32] * 5 + [vp] * 6 + [i64, vp]
+        lib.oracle_ring_valid.argtypes = [i32] * 3
+        lib.oracle_ring_valid.restype = i32
+        lib.oracle_ring_status.argtypes = [i32] * 4
+        lib.oracle_ring_status.restype = i32
+        lib.oracle_rope_append_ring.argtypes = [i32] * 9 + [vp] * 9 + [ctypes.POINTER(i32)]
+        lib.oracle_attention_ring.argtypes = [i32] * 8 + [f64, f64] + [i32] * 4 + [vp] * 6 + [i64, vp]
         lib.oracle_attention.restype = None
         lib.oracle_has_openmp.restype = i32
         _lib = lib
@@ -222,7 +228,65 @@ def attention(p: dict, q_rot, present_k, present_v, seqlens_k, head_sink=None, r
 def gqa(p: dict, q, k, v, past_k, past_v, seqlens_k, cos_cache=None, sin_cache=None, head_sink=None,
         rows=None):
     """Whole step: append (+RoPE) into present, then attention.  Returns
-    (out_fp64, present_k, present_v, q_rot, status_bits)."""
+    (out_fp64, present_k, present_v, q_rot, status_bits).  p["kv_ring"] = 1 selects the
+    ring layout (present updated in place from past_k/past_v, which hold the ring)."""
+    if p.get("kv_ring", 0):
+        q_rot, pk, pv, st = rope_append_ring(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache)
+        out = attention_ring(p, q_rot, pk, pv, seqlens_k, head_sink, rows)
+        return out, pk, pv, q_rot, st
     q_rot, pk, pv, st = rope_append(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache)
     out = attention(p, q_rot, pk, pv, seqlens_k, head_sink, rows)
     return out, pk, pv, q_rot, st
+
+
+# --------------------------------------------------------------------------------------
+# Ring layout ([P1] "Sliding window": the rolling sliding_window_cache buffer)
+# --------------------------------------------------------------------------------------
+def ring_valid(curr: int, cap: int, window: int) -> bool:
+    """A ring of cap slots can serve a step of curr tokens with window W iff
+    W >= 1 and W + curr - 1 <= cap."""
+    return bool(_load().oracle_ring_valid(curr, cap, window))
+
+
+def rope_append_ring(p: dict, q, k, v, ring_k, ring_v, seqlens_k, cos_cache=None, sin_cache=None):
+    """Append (+RoPE) into a ring of p["cap_present"] slots: position p goes to slot
+    p mod cap.  Works on copies of ring_k/ring_v; returns (q_rot, ring_k, ring_v, status)."""
+    lib = _load()
+    dt = p["dtype"]
+    q, k, v = _bits(q, dt), _bits(k, dt), _bits(v, dt)
+    rk, rv = _bits(ring_k, dt).copy(), _bits(ring_v, dt).copy()
+    q_rot = np.empty_like(q)
+    st = ctypes.c_int32(0)
+    cs = _bits(cos_cache, dt) if cos_cache is not None else None
+    sn = _bits(sin_cache, dt) if sin_cache is not None else None
+    seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    lib.oracle_rope_append_ring(p["batch"], p["q_heads"], p["kv_heads"], p["head_dim"], p["q_len"],
+                                p["cap_present"], p.get("rope_len", 0), DTYPE_CODES[dt], int(p.get("do_rotary", 0)),
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(seq), _ptr(cs), _ptr(sn), _ptr(q_rot),
+                                _ptr(rk), _ptr(rv), ctypes.byref(st))
+    return q_rot, rk, rv, int(st.value)
+
+
+def attention_ring(p: dict, q_rot, ring_k, ring_v, seqlens_k, head_sink=None, rows=None) -> np.ndarray:
+    """Attention in fp64 over a ring cache (same conventions as attention())."""
+    lib = _load()
+    dt = p["dtype"]
+    qb = _bits(q_rot, dt)
+    kb, vb = _bits(ring_k, dt), _bits(ring_v, dt)
+    seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    sink = None if head_sink is None else np.ascontiguousarray(head_sink, dtype=np.float32)
+    B, Hq, D, curr = p["batch"], p["q_heads"], p["head_dim"], p["q_len"]
+    if rows is None:
+        ridx, n = None, B * curr * Hq
+    else:
+        ridx = np.ascontiguousarray(rows, dtype=np.int64)
+        n = ridx.shape[0]
+    out = np.zeros((n, D), dtype=np.float64)
+    lib.oracle_attention_ring(B, Hq, p["kv_heads"], D, curr, p["cap_present"], p.get("rope_len", 0),
+                              DTYPE_CODES[dt], float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)),
+                              int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
+                              int(p.get("smooth_softmax", 0)), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq),
+                              _ptr(sink), _ptr(ridx), n, _ptr(out))
+    if rows is None:
+        return out.reshape(B, curr, Hq, D)
+    return out

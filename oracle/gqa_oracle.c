@@ -336,6 +336,122 @@ void oracle_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t cur
   }
 }
 
+/* ------------------------------------------------------------------------------------
+ * Ring layout of the present cache ([P1] "Sliding window": sliding_window_cache, the
+ * physical rolling KV buffer whose memory is bounded by the window; [P3] Summary: a window
+ * is a per-layer setting).  The cache has cap slots and absolute position p lives in slot
+ * p mod cap, so only the last cap positions are resident.  It is valid only with a window
+ * W >= 1 such that W + curr - 1 <= cap: every key that a query of the step can see is then
+ * still resident after the step's own rows were written (the oldest key the first query
+ * sees, past - W + 1, is at least total - cap).  The band predicate is unchanged; only the
+ * slot of a position differs.  The append has no separate past (the ring is updated in
+ * place) and no capacity limit on the past length.
+ * ---------------------------------------------------------------------------------- */
+int32_t oracle_ring_valid(int32_t curr, int32_t cap, int32_t window) {
+  return window >= 1 && curr >= 1 && (int64_t)window + curr - 1 <= cap;
+}
+
+int32_t oracle_ring_status(int32_t past, int32_t curr, int32_t do_rotary, int32_t rope_len) {
+  if (past < 0) return 1;
+  if (do_rotary && (int64_t)past + curr > rope_len) return 2;
+  return 0;
+}
+
+void oracle_rope_append_ring(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap,
+                             int32_t rope_len, int32_t dtype, int32_t do_rotary, const void *q, const void *k,
+                             const void *v, const int32_t *seqlens_k, const void *cos_cache,
+                             const void *sin_cache, void *q_rot, void *present_k, void *present_v,
+                             int32_t *status_out) {
+  size_t es = elem_size(dtype);
+  int32_t status_all = 0;
+  for (int b = 0; b < B; ++b) {
+    int32_t past = seqlens_k[b];
+    int32_t st = oracle_ring_status(past, curr, do_rotary, rope_len);
+    status_all |= st;
+    if (st) continue;
+    for (int h = 0; h < Hkv; ++h) {
+      size_t base = ((size_t)b * Hkv + h) * (size_t)cap * D;
+      for (int i = 0; i < curr; ++i) {
+        int64_t pos = (int64_t)past + i;
+        size_t src = (((size_t)b * curr + i) * Hkv + h) * D;
+        size_t dst = base + (size_t)(pos % cap) * D;
+        if (do_rotary)
+          rotate_row(k, src, cos_cache, sin_cache, (size_t)pos * (D / 2), D, dtype, present_k, dst);
+        else
+          memcpy((char *)present_k + dst * es, (const char *)k + src * es, (size_t)D * es);
+        memcpy((char *)present_v + dst * es, (const char *)v + src * es, (size_t)D * es);
+      }
+    }
+    if (q_rot) {
+      for (int i = 0; i < curr; ++i)
+        for (int h = 0; h < Hq; ++h) {
+          size_t off = (((size_t)b * curr + i) * Hq + h) * D;
+          if (do_rotary)
+            rotate_row(q, off, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, q_rot, off);
+          else
+            memcpy((char *)q_rot + off * es, (const char *)q + off * es, (size_t)D * es);
+        }
+    }
+  }
+  if (status_out) *status_out = status_all;
+}
+
+/* Attention over a ring cache: the resident positions [max(0, total - cap), total) are
+ * gathered into position order (position p from slot p mod cap) and each row is the same
+ * oracle_attend_row over them, with the same band predicate as the linear layout.  Rows of
+ * rejected sequences, and every row when the ring cannot hold the band, are zeros. */
+void oracle_attention_ring(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap,
+                           int32_t rope_len, int32_t dtype, double scale, double softcap, int32_t window,
+                           int32_t causal, int32_t do_rotary, int32_t smooth_softmax, const void *q,
+                           const void *present_k, const void *present_v, const int32_t *seqlens_k,
+                           const float *head_sink, const int64_t *rows, int64_t nrows, double *out) {
+  int G = Hq / Hkv;
+  size_t es = elem_size(dtype);
+  if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  int valid = oracle_ring_valid(curr, cap, window);
+  int64_t count = rows ? nrows : (int64_t)B * curr * Hq;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t t = 0; t < count; ++t) {
+    int64_t r = rows ? rows[t] : t;
+    int hq = (int)(r % Hq);
+    int i = (int)((r / Hq) % curr);
+    int b = (int)(r / ((int64_t)Hq * curr));
+    double *o = out + (size_t)t * D;
+    int32_t past = seqlens_k[b];
+    if (!valid || oracle_ring_status(past, curr, do_rotary, rope_len)) {
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      continue;
+    }
+    int hk = hq / G;
+    int64_t total = (int64_t)past + curr;
+    int64_t q_abs = (int64_t)past + i;
+    int64_t first = total > cap ? total - cap : 0;  /* oldest resident position */
+    int64_t n = total - first;
+    char *kg = (char *)malloc((size_t)n * D * es);
+    char *vg = (char *)malloc((size_t)n * D * es);
+    uint8_t *vis = (uint8_t *)malloc((size_t)n);
+    size_t base = ((size_t)b * Hkv + hk) * (size_t)cap * D;
+    for (int64_t j = 0; j < n; ++j) {
+      int64_t pos = first + j;
+      size_t src = base + (size_t)(pos % cap) * D;
+      memcpy(kg + (size_t)j * D * es, (const char *)present_k + src * es, (size_t)D * es);
+      memcpy(vg + (size_t)j * D * es, (const char *)present_v + src * es, (size_t)D * es);
+      vis[j] = (uint8_t)oracle_visible(q_abs, pos, total, causal, window);
+    }
+    double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
+    int has_sink = head_sink != NULL || smooth_softmax;
+    double z = head_sink ? (double)head_sink[hq] : 0.0;
+    oracle_attend_row(qv, kg, vg, 0, n, vis, D, dtype, scale, softcap, has_sink, z, o);
+    free(qv);
+    free(vis);
+    free(vg);
+    free(kg);
+  }
+}
+
 int32_t oracle_has_openmp(void) {
 #ifdef _OPENMP
   return 1;

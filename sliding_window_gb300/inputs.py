@@ -46,6 +46,7 @@ class Workload:
     rope_len: int = 0
     rope_theta: float = 10000.0
     garbage_std: float = 10.0
+    kv_ring: int = 0        # 1: the cache is a ring of `cap` slots, position p in slot p % cap
 
     @property
     def layers(self) -> int:
@@ -59,7 +60,7 @@ class Workload:
                     cap_present=self.cap, rope_len=self.rope_len, dtype=self.dtype,
                     scale=self.scale, softcap=self.softcap, window=self.windows[layer],
                     causal=self.causal, do_rotary=self.do_rotary, rotary_interleaved=0,
-                    smooth_softmax=self.smooth_softmax)
+                    smooth_softmax=self.smooth_softmax, kv_ring=self.kv_ring)
 
     def scaled(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -98,7 +99,7 @@ def rope_tables(rope_len: int, head_dim: int, theta: float, dtype: str, device="
 
 def draw_seqlens(w: Workload, seed_offset: int = 0) -> np.ndarray:
     rng = np.random.default_rng(2000 + w.index + 7919 * seed_offset)
-    hi = min(w.past_hi, w.cap - w.q_len)
+    hi = w.past_hi if w.kv_ring else min(w.past_hi, w.cap - w.q_len)
     return rng.integers(w.past_lo, hi, endpoint=True, size=w.batch).astype(np.int32)
 
 
@@ -139,7 +140,9 @@ class Case:
 def make_case(w: Workload, layer: int = 0, device="cpu", seed_offset: int = 0, garbage: str = "normal",
               seqlens: np.ndarray | None = None) -> Case:
     """Draw one layer of a workload.  Past rows [0, seqlens_k[b]) are N(0,1); rows beyond
-    are stale garbage (N(0, garbage_std^2), +-1e4, or NaN/+-Inf) that must never be read."""
+    are stale garbage (N(0, garbage_std^2), +-1e4, or NaN/+-Inf) that must never be read.
+    For a ring cache the resident slots (every slot once the past fills the ring) are
+    N(0,1) and only slots of a ring that has not wrapped yet hold garbage."""
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
     gen.manual_seed(1000 + w.index + 104729 * layer + 7919 * seed_offset)
@@ -160,7 +163,7 @@ def make_case(w: Workload, layer: int = 0, device="cpu", seed_offset: int = 0, g
     past_v = torch.empty(B, Hkv, cap, D, dtype=t, device=dev)
     # rows are drawn per sequence so that the large caches never need an fp32 copy in full
     for b in range(B):
-        n = int(seq[b])
+        n = min(int(seq[b]), cap) if w.kv_ring else int(seq[b])
         for buf in (past_k, past_v):
             tmp = torch.empty(Hkv, cap, D, dtype=torch.float32, device=dev)
             tmp[:, :n].normal_(0.0, 1.0, generator=gen)
