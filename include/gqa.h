@@ -48,6 +48,17 @@
  *   is NULL), else 0.  The sink is neither scaled nor capped.  A row with no visible slot
  *   gives zeros.
  *
+ * Ring cache (kv_ring = 1; [P1] "Sliding window": sliding_window_cache, the rolling KV
+ * buffer whose memory is bounded by the window): present holds cap_present slots and
+ * absolute position p lives in slot p mod cap_present, so a layer with window W needs
+ * only W + curr - 1 slots whatever the sequence length.  Requires window >= 1 and
+ * window + q_len - 1 <= cap_present (else GQA_ERR_CAPACITY: a key the step sees would
+ * already be overwritten), cap_present a multiple of 64 (else GQA_ERR_UNSUPPORTED),
+ * present aliasing past (the ring is updated in place; else GQA_ERR_INVALID_ARG), and the
+ * decode entry points on the split-KV kernel's shapes (bf16/f16; prefill returns
+ * GQA_ERR_UNSUPPORTED).  seqlens_k is the absolute past length and may exceed cap_present;
+ * the band predicate is unchanged.  gqa_rope_append_kv appends into a ring the same way.
+ *
  * Ownership and memory: the caller owns every buffer; all pointers except the params
  * struct are device pointers, 16-byte aligned.  The library allocates no memory (it uses
  * the caller's workspace) and keeps no state between calls apart from the counters it
@@ -76,7 +87,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 1
+#define GQA_ABI_VERSION 2
 
 typedef int32_t gqa_status;
 #define GQA_OK 0
@@ -111,6 +122,7 @@ typedef struct gqa_params {
   int32_t do_rotary;    /* 1 = rotate q and k with cos/sin_cache */
   int32_t rotary_interleaved; /* must be 0 (half-split pairs only) */
   int32_t smooth_softmax;     /* 1 = zero sink when head_sink is NULL */
+  int32_t kv_ring;            /* 1 = present is a ring of cap_present slots (see below) */
 } gqa_params;
 
 /* Bytes of device workspace that gqa_attention_prefill / gqa_attention_decode need for

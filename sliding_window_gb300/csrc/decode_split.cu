@@ -28,6 +28,7 @@
 // of the group (atomic ticket, no spin-wait) adds the sink once, normalizes and writes out.
 // Launched with programmatic stream serialization: the prologue overlaps the previous
 // kernel's tail and griddepcontrol.wait orders every global read after it.
+#include <limits.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -56,7 +57,7 @@ struct DecodeArgs {
   int32_t *tickets;     // [B*Hkv]
   int32_t *status;
   int Hq, Hkv, G, curr, R, cap, cap_past, past_separate, rope_len, do_rotary, append;
-  int window, causal, splits, has_sink;
+  int window, causal, splits, has_sink, ring;
   float score_mul;  // scale*log2(e), or scale/softcap with softcap
   float cap_mul;    // softcap*log2(e), 0 without softcap
 };
@@ -133,7 +134,7 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
     const int rr = (w / per_row) % nrows, c = (w % per_row) * 8;
     const int pos = r0 + rr, i = pos - past;
     const size_t src = (((size_t)b * a.curr + i) * a.Hkv + h) * D;
-    const size_t dst = (((size_t)b * a.Hkv + h) * a.cap + pos) * D;
+    const size_t dst = (((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos)) * D;
     if (which == 0 && a.do_rotary) {
       uint4 y1, y2;
       rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c,
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       qraw[u][1] = *reinterpret_cast<const uint4 *>(src + D / 2 + c * 8);
     }
   }
-  const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
+  const int st = sequence_status(past, a.curr, a.ring ? INT_MAX : a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
                                  a.rope_len);
   if (st) {  // rejected sequence: zeros, nothing appended, reported once
     if (split == 0) {
@@ -225,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     return;
   }
   const int total = past + a.curr;
-  const int lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
+  // a ring starts its tiles on 64-position boundaries (the capacity is a multiple of 64, so
+  // a tile never straddles the wrap); the keys before the band are masked like any other
+  const int lo = a.ring ? max(0, past - a.window + 1) & ~(KT - 1) : (a.window > 0 ? max(0, past - a.window + 1) : 0);
   const int len = total - lo;
   const int chunk = ((len + a.splits - 1) / a.splits + KT - 1) / KT * KT;  // this group's chunk
   const int nchunks = (len + chunk - 1) / chunk;
@@ -248,8 +251,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_expect_tx(&full[s], L::kStageBytes);
       uint8_t *kdst = stages + s * L::kStageBytes;
       uint8_t *vdst = kdst + L::kTileBytes;
-      tma_load_4d(kdst, &tmk, 0, k0, 0, bh, &full[s]);  // [D/64][KT][64], one copy each
-      tma_load_4d(vdst, &tmv, 0, k0, 0, bh, &full[s]);
+      const int row = a.ring ? k0 % a.cap : k0;
+      tma_load_4d(kdst, &tmk, 0, row, 0, bh, &full[s]);  // [D/64][KT][64], one copy each
+      tma_load_4d(vdst, &tmv, 0, row, 0, bh, &full[s]);
     }
     __syncwarp();
   };
@@ -763,6 +767,7 @@ template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, c
   a.curr = p.q_len;
   a.R = dp.rows;
   a.cap = p.cap_present;
+  a.ring = p.kv_ring;
   a.cap_past = p.cap_past;
   a.past_separate = c.past_separate;
   a.rope_len = p.rope_len;

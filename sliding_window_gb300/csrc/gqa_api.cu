@@ -32,11 +32,16 @@ gqa_status check_params(const gqa_params *p) {
   if (!(p->softcap >= 0.f) || !isfinite(p->softcap)) return GQA_ERR_INVALID_ARG;
   if (p->window != -1 && p->window < 1) return GQA_ERR_INVALID_ARG;
   if ((p->causal | 1) != 1 || (p->do_rotary | 1) != 1 || (p->smooth_softmax | 1) != 1) return GQA_ERR_INVALID_ARG;
-  if ((p->rotary_interleaved | 1) != 1) return GQA_ERR_INVALID_ARG;
+  if ((p->rotary_interleaved | 1) != 1 || (p->kv_ring | 1) != 1) return GQA_ERR_INVALID_ARG;
   if (p->rotary_interleaved) return GQA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return GQA_ERR_UNSUPPORTED;
   if (p->cap_present < p->q_len || p->cap_past < 0) return GQA_ERR_CAPACITY;
   if (p->do_rotary && p->rope_len < 1) return GQA_ERR_INVALID_ARG;
+  if (p->kv_ring) {  // position p in slot p % cap: every key the step sees must still be resident
+    if (p->window < 1) return GQA_ERR_INVALID_ARG;
+    if ((long long)p->window + p->q_len - 1 > p->cap_present) return GQA_ERR_CAPACITY;
+    if (p->cap_present % 64 != 0) return GQA_ERR_UNSUPPORTED;  // 64-key tiles never straddle the wrap
+  }
   // TMA coordinates and the kernels' index arithmetic are 32-bit per dimension
   const long long rows = (long long)p->batch * p->kv_heads;
   if (rows > (1ll << 30) || (long long)p->q_len * p->q_heads > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
@@ -189,6 +194,7 @@ gqa_status make_call(Call &c, const gqa_params *p, const void *q, const void *k,
     const bool alias_v = past_v == nullptr || past_v == present_v;
     if (alias_k != alias_v) return GQA_ERR_INVALID_ARG;
     c.past_separate = !alias_k;
+    if (c.past_separate && p->kv_ring) return GQA_ERR_INVALID_ARG;  // a ring is updated in place
     if (c.past_separate) {
       if (!aligned16(past_k) || !aligned16(past_v)) return GQA_ERR_INVALID_ARG;
       if (p->cap_past < 1) return GQA_ERR_CAPACITY;
@@ -232,6 +238,7 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   const DecodePlan dp = decode_plan(c.p);
   // the split decode kernel appends and rotates itself; every other path runs K1 first
   const bool fused = mode == kDecode && dp.eligible;
+  if (p->kv_ring && !fused) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads a ring
   size_t need = fused ? (dp.splits > 1 && !dp.cluster ? wl.total : 0) : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
   if (need > 0) {
     if (!workspace || !aligned16(workspace)) return GQA_ERR_WORKSPACE;

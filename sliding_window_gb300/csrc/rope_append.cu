@@ -10,6 +10,8 @@
 //   y1 = x1*c - x2*s,  y2 = x2*c + x1*s,  c, s = cos/sin_cache[pos, d]
 // every product and every sum rounded to fp32 on its own (no FMA contraction), then the
 // result rounded to the dtype with ties to even.  present is therefore bit-exact.
+#include <limits.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -50,6 +52,7 @@ struct RopeArgs {
   const int32_t *seqlens;
   int32_t *status;
   int B, Hq, Hkv, D, curr, cap_present, cap_past, rope_len, do_rotary, past_separate;
+  int ring;  // present is a ring: position p in slot p % cap_present
 };
 
 // One block per (b, i).  Work items: (head, chunk) over Hq q heads (when q_rot is wanted),
@@ -60,7 +63,8 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
   const int b = blockIdx.x / a.curr;
   const int i = blockIdx.x % a.curr;
   const int past = a.seqlens[b];
-  const int st = sequence_status(past, a.curr, a.cap_present, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
+  const int st = sequence_status(past, a.curr, a.ring ? INT_MAX : a.cap_present, a.cap_past, a.past_separate,
+                                 a.do_rotary, a.rope_len);
   if (st) {
     if (threadIdx.x == 0 && i == 0) report(a.status, st);
     return;
@@ -89,7 +93,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
       size_t off = (((size_t)b * a.curr + i) * a.Hkv + h) * a.D;
       src = reinterpret_cast<const T *>(is_v ? a.v : a.k) + off;
       dst = reinterpret_cast<T *>(is_v ? a.present_v : a.present_k) +
-            (((size_t)b * a.Hkv + h) * a.cap_present + pos) * a.D;
+            (((size_t)b * a.Hkv + h) * a.cap_present + (a.ring ? pos % a.cap_present : pos)) * a.D;
       rot = rot && !is_v;
     }
     if (rot) {
@@ -156,6 +160,7 @@ template <typename T> static gqa_status launch_t(const Call &c) {
   a.D = p.head_dim;
   a.curr = p.q_len;
   a.cap_present = p.cap_present;
+  a.ring = p.kv_ring;
   a.cap_past = p.cap_past;
   a.rope_len = p.rope_len;
   a.do_rotary = p.do_rotary;

@@ -42,7 +42,7 @@ class GqaParams(ctypes.Structure):
                 ("cap_present", ctypes.c_int32), ("rope_len", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("softcap", ctypes.c_float), ("window", ctypes.c_int32),
                 ("causal", ctypes.c_int32), ("do_rotary", ctypes.c_int32), ("rotary_interleaved", ctypes.c_int32),
-                ("smooth_softmax", ctypes.c_int32)]
+                ("smooth_softmax", ctypes.c_int32), ("kv_ring", ctypes.c_int32)]
 
 
 class GqaError(RuntimeError):
@@ -79,12 +79,13 @@ lib = _load()
 
 
 def params(batch, q_heads, kv_heads, head_dim, q_len, cap_present, dtype, cap_past=None, rope_len=0, scale=0.0,
-           softcap=0.0, window=-1, causal=1, do_rotary=0, rotary_interleaved=0, smooth_softmax=0) -> GqaParams:
+           softcap=0.0, window=-1, causal=1, do_rotary=0, rotary_interleaved=0, smooth_softmax=0,
+           kv_ring=0) -> GqaParams:
     """Build a gqa_params struct (dtype: "f32" | "f16" | "bf16" or its integer code)."""
     dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
     return GqaParams(batch, q_heads, kv_heads, head_dim, q_len, cap_present if cap_past is None else cap_past,
                      cap_present, rope_len, dt, scale, softcap, window, causal, do_rotary, rotary_interleaved,
-                     smooth_softmax)
+                     smooth_softmax, kv_ring)
 
 
 def params_from_dict(d: dict) -> GqaParams:
@@ -92,7 +93,7 @@ def params_from_dict(d: dict) -> GqaParams:
                   cap_past=d.get("cap_past"), rope_len=d.get("rope_len", 0), scale=d.get("scale", 0.0),
                   softcap=d.get("softcap", 0.0), window=d.get("window", -1), causal=d.get("causal", 1),
                   do_rotary=d.get("do_rotary", 0), rotary_interleaved=d.get("rotary_interleaved", 0),
-                  smooth_softmax=d.get("smooth_softmax", 0))
+                  smooth_softmax=d.get("smooth_softmax", 0), kv_ring=d.get("kv_ring", 0))
 
 
 def _ptr(t):

@@ -59,6 +59,12 @@ def oracle_ref(case: Case, rows=None, host_present=None):
     p = case.params
     cs = None if case.cos is None else storage(case.cos)
     sn = None if case.sin is None else storage(case.sin)
+    if p.get("kv_ring", 0):
+        q_rot, pk, pv, st = oracle.rope_append_ring(p, storage(case.q), storage(case.k), storage(case.v),
+                                                    storage(case.past_k), storage(case.past_v),
+                                                    case.seqlens_k.cpu().numpy(), cs, sn)
+        sink = None if case.head_sink is None else case.head_sink.cpu().numpy()
+        return oracle.attention_ring(p, q_rot, pk, pv, case.seqlens_k.cpu().numpy(), sink, rows=rows), pk, pv, st
     if host_present is None:
         q_rot, pk, pv, st = oracle.rope_append(p, storage(case.q), storage(case.k), storage(case.v),
                                                storage(case.past_k), storage(case.past_v),

@@ -51,7 +51,7 @@ def test_struct_layout_matches_header(g, tmp_path):
 
 
 def test_version_and_status_strings(g):
-    assert g.gqa_abi_version() == 1
+    assert g.gqa_abi_version() == 2
     for s in range(6):
         assert g.gqa_status_string(s) and g.gqa_status_string(s) != "unknown status"
     assert g.gqa_status_string(99) == "unknown status"
@@ -92,6 +92,10 @@ def call(g, p, fn="gqa_attention_decode", ws_bytes=0, **ptrs):
     (dict(cap_present=0), 3),
     (dict(q_len=8, cap_present=4), 3),
     (dict(do_rotary=1, rope_len=0), 1),
+    (dict(kv_ring=2), 1),
+    (dict(kv_ring=1, window=-1), 1),            # a ring needs a window
+    (dict(kv_ring=1, window=1024, q_len=2), 3),  # W + curr - 1 > cap: a visible key would be overwritten
+    (dict(kv_ring=1, window=100, cap_present=1000), 2),  # ring capacity not a multiple of 64
 ])
 def test_invalid_params_rejected(g, fn, kw, code):
     assert call(g, good_params(g, **kw), fn) == code
@@ -106,6 +110,13 @@ def test_invalid_params_rejected(g, fn, kw, code):
 ])
 def test_invalid_pointers_rejected(g, ptrs, code):
     assert call(g, good_params(g), **ptrs) == code
+
+
+def test_ring_rules(g):
+    ring = good_params(g, kv_ring=1, window=1000, cap_present=1024, q_len=4)
+    assert call(g, ring, past_k=FAKE + 4096, past_v=FAKE + 4096) == 1  # a ring is updated in place
+    assert call(g, ring, fn="gqa_attention_prefill") == 2            # only the decode kernel reads a ring
+    assert call(g, good_params(g, kv_ring=1, window=1000, cap_present=1024, q_len=4, dtype="f32")) == 2
 
 
 def test_attention_only_rejects_rotary(g):
