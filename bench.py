@@ -469,6 +469,11 @@ class OracleSample:
     def run(self):
         o = self.oracle
         for L in self.layers:
+            if L["p"].get("kv_ring", 0):
+                q_rot, pk, pv, _ = o.rope_append_ring(L["p"], L["q"], L["k"], L["v"], L["pk"], L["pv"], L["seq"],
+                                                      L["cos"], L["sin"])
+                o.attention_ring(L["p"], q_rot, pk, pv, L["seq"], L["sink"], rows=L["rows"])
+                continue
             q_rot, pk, pv, _ = o.rope_append(L["p"], L["q"], L["k"], L["v"], L["pk"], L["pv"], L["seq"], L["cos"],
                                              L["sin"], present_k=L["pk"], present_v=L["pv"])
             o.attention(L["p"], q_rot, pk, pv, L["seq"], L["sink"], rows=L["rows"])
@@ -498,7 +503,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graphs", action="store_true", help="launch steps directly (for profilers)")
@@ -508,7 +513,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.steps is None:
         args.steps = {"decode_window_bf16": 100000, "specdecode_rotary_f16": 20000, "decode_long_bf16": 1500,
-                      "prefill_sink_softcap_bf16": 500, "prefill_fp32_tiny": 20000}[args.workload]
+                      "prefill_sink_softcap_bf16": 500, "prefill_fp32_tiny": 20000,
+                      "decode_window_ring_bf16": 100000}[args.workload]
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -79,6 +79,10 @@ WORKLOADS = {
                  windows=(-1, 4096), smooth_softmax=1, do_rotary=1, rope_len=32768),
         Workload("decode_long_bf16", 4, "decode", "bf16", 64, 64, 8, 128, 1, 32768, 8192, 32767,
                  windows=(-1,), head_sink=True),
+        # the windowed decode over a ring of 1024 slots (W + curr - 1 = 1024): the same band,
+        # a quarter of the cache memory
+        Workload("decode_window_ring_bf16", 5, "decode", "bf16", 8, 32, 8, 128, 1, 1024, 512, 4095,
+                 windows=(1024,), kv_ring=1),
     ]
 }
 

@@ -1,4 +1,4 @@
-"""The five named workloads at full size, in the launch configuration bench.py times,
+"""The five named workloads (and the ring-cache variant of the windowed decode) at full size, in the launch configuration bench.py times,
 checked against the fp64 oracle: every row for the tiny fp32 prompt, sampled rows (with the
 band edges) for the large ones, and the appended present rows bit for bit."""
 import numpy as np
@@ -75,3 +75,21 @@ def test_specdecode_rotary_f16(layer):
 def test_decode_long_bf16():
     check_workload("decode_long_bf16")
     torch.cuda.empty_cache()
+
+
+def test_decode_window_ring_bf16():
+    """The windowed decode over a ring of 1024 slots: sequences up to 4096 long, so most
+    rings have wrapped; the appended slots bit for bit, sampled rows against the ring oracle."""
+    w = WORKLOADS["decode_window_ring_bf16"]
+    c = make_case(w, device="cpu")
+    host = make_host(c)
+    r = run_gpu(c, w.mode)
+    assert r["status"] == 0
+    p = c.params
+    q_rot, pk, pv, st = oracle.rope_append_ring(p, host["q"], host["k"], host["v"], host["past_k"], host["past_v"],
+                                                host["seq"], host["cos"], host["sin"])
+    assert st == 0
+    np.testing.assert_array_equal(storage(r["present_k"]), pk)
+    np.testing.assert_array_equal(storage(r["present_v"]), pv)
+    ref = oracle.attention_ring(p, q_rot, pk, pv, host["seq"], host["sink"])
+    assert_close(out_rows(r["out"], c), ref, w.dtype, w.name)
