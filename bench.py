@@ -367,8 +367,10 @@ def job_rate(units_per_rank_step: float, steps: int, world: int, elapsed: float)
 def run_e2e(args, sets, stream, w, units):
     """Every step: the step's inputs (q, k, v, seqlens_k of all layers) copied host->device
     from pinned memory in one copy, the public decode/prefill call per layer, the outputs
-    copied device->host in one copy.  The KV cache stays resident (it is the op's state);
-    captured in CUDA graphs like the device-side loop."""
+    copied device->host in one copy.  The KV cache stays resident (it is the op's state).
+    The copies run on their own streams, so step i+1's input copy and step i-1's output copy
+    overlap step i's kernels; a buffer set is reused only after its previous kernels and
+    output copy are done.  Captured in CUDA graphs like the device-side loop."""
     hosts = []
     for s in sets:
         hs = s.stage.cpu().pin_memory()
@@ -376,23 +378,49 @@ def run_e2e(args, sets, stream, w, units):
         hosts.append((hs, ho))
     h2d = hosts[0][0].numel()
     d2h = hosts[0][1].numel() * hosts[0][1].element_size()
+    h2d_s, d2h_s = torch.cuda.Stream(stream.device), torch.cuda.Stream(stream.device)
+    n = len(sets)
 
-    def make(si):
-        s, (hs, ho) = sets[si], hosts[si]
+    def steps(count):
+        def issue(stream):
+            h2d_s.wait_stream(stream)
+            d2h_s.wait_stream(stream)
+            kern, outd = [], []
+            for j in range(count):
+                s, (hs, ho) = sets[j % n], hosts[j % n]
+                with torch.cuda.stream(h2d_s):
+                    if j >= n:
+                        h2d_s.wait_event(kern[j - n])  # the set's stage was read by its last kernels
+                    s.stage.copy_(hs, non_blocking=True)
+                    e_in = torch.cuda.Event()
+                    e_in.record(h2d_s)
+                stream.wait_event(e_in)
+                if j >= n:
+                    stream.wait_event(outd[j - n])  # the set's output was copied out
+                s.full(stream)
+                e_k = torch.cuda.Event()
+                e_k.record(stream)
+                kern.append(e_k)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(e_k)
+                    ho.copy_(s.out_all, non_blocking=True)
+                    e_out = torch.cuda.Event()
+                    e_out.record(d2h_s)
+                    outd.append(e_out)
+            stream.wait_stream(h2d_s)
+            stream.wait_stream(d2h_s)
+        return issue
 
-        def f(stream):
-            s.stage.copy_(hs, non_blocking=True)
-            s.full(stream)
-            ho.copy_(s.out_all, non_blocking=True)
-        return f
-
-    fns = [make(i) for i in range(len(sets))]
     per_graph = max(1, min(args.steps, 64 if w.mode == "decode" else 4))
     with torch.cuda.stream(stream):
-        for i in range(3):
-            fns[i % len(fns)](stream)
+        steps(min(3, args.steps))(stream)
     stream.synchronize()
-    graphs = plan_graphs(fns, args.steps, per_graph, stream)
+    if USE_GRAPHS:
+        full = capture([steps(per_graph)], stream) if args.steps >= per_graph else None
+        rem = args.steps % per_graph
+        graphs = [full] * (args.steps // per_graph) + ([capture([steps(rem)], stream)] if rem else [])
+    else:
+        graphs = [Eager([steps(args.steps)], stream)]
     stream.synchronize()
     el = time_graphs(graphs, stream)
     return dict(elapsed=el, h2d=h2d, d2h=d2h)
