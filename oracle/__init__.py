@@ -84,6 +84,10 @@ def _load():
         lib.oracle_ring_status.restype = i32
         lib.oracle_rope_append_ring.argtypes = [i32] * 9 + [vp] * 9 + [ctypes.POINTER(i32)]
         lib.oracle_attention_ring.argtypes = [i32] * 8 + [f64, f64] + [i32] * 4 + [vp] * 6 + [i64, vp]
+        lib.oracle_paged_status.argtypes = [i32] * 6 + [vp, i32, i32]
+        lib.oracle_paged_status.restype = i32
+        lib.oracle_rope_append_paged.argtypes = [i32] * 12 + [vp] * 10 + [ctypes.POINTER(i32)]
+        lib.oracle_attention_paged.argtypes = [i32] * 10 + [f64, f64] + [i32] * 4 + [vp] * 7 + [i64, vp]
         lib.oracle_attention.restype = None
         lib.oracle_has_openmp.restype = i32
         _lib = lib
@@ -287,6 +291,58 @@ def attention_ring(p: dict, q_rot, ring_k, ring_v, seqlens_k, head_sink=None, ro
                               int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
                               int(p.get("smooth_softmax", 0)), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq),
                               _ptr(sink), _ptr(ridx), n, _ptr(out))
+    if rows is None:
+        return out.reshape(B, curr, Hq, D)
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# Paged layout ([P3] Summary: a cell cache with per-sequence membership)
+# --------------------------------------------------------------------------------------
+def rope_append_paged(p: dict, q, k, v, pool_k, pool_v, seqlens_k, table, num_pages, page=64, cos_cache=None,
+                      sin_cache=None):
+    """Append (+RoPE) into a paged pool [num_pages, Hkv, page, D] through a block table
+    [B, max_pages]; works on copies of the pools.  Returns (q_rot, pool_k, pool_v, status)."""
+    lib = _load()
+    dt = p["dtype"]
+    q, k, v = _bits(q, dt), _bits(k, dt), _bits(v, dt)
+    pk, pv = _bits(pool_k, dt).copy(), _bits(pool_v, dt).copy()
+    tab = np.ascontiguousarray(table, dtype=np.int32)
+    q_rot = np.empty_like(q)
+    st = ctypes.c_int32(0)
+    cs = _bits(cos_cache, dt) if cos_cache is not None else None
+    sn = _bits(sin_cache, dt) if sin_cache is not None else None
+    seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    lib.oracle_rope_append_paged(p["batch"], p["q_heads"], p["kv_heads"], p["head_dim"], p["q_len"], page,
+                                 tab.shape[1], num_pages, p.get("rope_len", 0), DTYPE_CODES[dt],
+                                 int(p.get("do_rotary", 0)), int(p.get("window", -1)), _ptr(tab), _ptr(q), _ptr(k),
+                                 _ptr(v), _ptr(seq), _ptr(cs), _ptr(sn), _ptr(q_rot), _ptr(pk), _ptr(pv),
+                                 ctypes.byref(st))
+    return q_rot, pk, pv, int(st.value)
+
+
+def attention_paged(p: dict, q_rot, pool_k, pool_v, seqlens_k, table, num_pages, page=64, head_sink=None,
+                    rows=None) -> np.ndarray:
+    """Attention in fp64 over a paged cache (same conventions as attention())."""
+    lib = _load()
+    dt = p["dtype"]
+    qb = _bits(q_rot, dt)
+    kb, vb = _bits(pool_k, dt), _bits(pool_v, dt)
+    tab = np.ascontiguousarray(table, dtype=np.int32)
+    seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    sink = None if head_sink is None else np.ascontiguousarray(head_sink, dtype=np.float32)
+    B, Hq, D, curr = p["batch"], p["q_heads"], p["head_dim"], p["q_len"]
+    if rows is None:
+        ridx, n = None, B * curr * Hq
+    else:
+        ridx = np.ascontiguousarray(rows, dtype=np.int64)
+        n = ridx.shape[0]
+    out = np.zeros((n, D), dtype=np.float64)
+    lib.oracle_attention_paged(B, Hq, p["kv_heads"], D, curr, page, tab.shape[1], num_pages, p.get("rope_len", 0),
+                               DTYPE_CODES[dt], float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)),
+                               int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
+                               int(p.get("smooth_softmax", 0)), _ptr(tab), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq),
+                               _ptr(sink), _ptr(ridx), n, _ptr(out))
     if rows is None:
         return out.reshape(B, curr, Hq, D)
     return out

@@ -452,6 +452,127 @@ void oracle_attention_ring(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_
   }
 }
 
+/* ------------------------------------------------------------------------------------
+ * Paged layout of the present cache ([P3] Summary: a cell cache whose slots belong to
+ * sequences through a per-step occupancy/membership plan, masked rather than evicted).
+ * Here the cache is a pool of pages of `page` positions, [num_pages][Hkv][page][D], and a
+ * block table [B][max_pages] names the page that holds positions [n*page, (n+1)*page) of
+ * sequence b.  The logical capacity is max_pages * page; the band predicate is unchanged.
+ * A sequence whose table entries for the positions it reads or writes ([lo, total) with lo
+ * the band's first position, rounded down to a page) fall outside [0, num_pages) is
+ * rejected like a bad seqlens_k: bit 4, zeros, nothing written.
+ * ---------------------------------------------------------------------------------- */
+int32_t oracle_paged_status(int32_t past, int32_t curr, int32_t cap, int32_t do_rotary, int32_t rope_len,
+                            int32_t window, const int32_t *table_row, int32_t page, int32_t num_pages) {
+  int32_t st = oracle_sequence_status(past, curr, 0, cap, 0, do_rotary, rope_len);
+  if (st) return st;
+  int64_t total = (int64_t)past + curr;
+  int64_t lo = window > 0 ? (past - window + 1 > 0 ? past - window + 1 : 0) : 0;
+  for (int64_t n = lo / page; n * page < total; ++n)
+    if (table_row[n] < 0 || table_row[n] >= num_pages) return 4;
+  return 0;
+}
+
+static size_t paged_row(int32_t b, int32_t h, int64_t pos, int32_t Hkv, int32_t page, const int32_t *table,
+                        int32_t max_pages) {
+  int32_t pg = table[(size_t)b * max_pages + pos / page];
+  return ((size_t)pg * Hkv + h) * page + (size_t)(pos % page);
+}
+
+void oracle_rope_append_paged(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t page,
+                              int32_t max_pages, int32_t num_pages, int32_t rope_len, int32_t dtype,
+                              int32_t do_rotary, int32_t window, const int32_t *table, const void *q, const void *k,
+                              const void *v, const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                              void *q_rot, void *pool_k, void *pool_v, int32_t *status_out) {
+  size_t es = elem_size(dtype);
+  int32_t status_all = 0;
+  int32_t cap = max_pages * page;
+  for (int b = 0; b < B; ++b) {
+    int32_t past = seqlens_k[b];
+    int32_t st = oracle_paged_status(past, curr, cap, do_rotary, rope_len, window, table + (size_t)b * max_pages,
+                                     page, num_pages);
+    status_all |= st;
+    if (st) continue;
+    for (int h = 0; h < Hkv; ++h)
+      for (int i = 0; i < curr; ++i) {
+        int64_t pos = (int64_t)past + i;
+        size_t src = (((size_t)b * curr + i) * Hkv + h) * D;
+        size_t dst = paged_row(b, h, pos, Hkv, page, table, max_pages) * D;
+        if (do_rotary)
+          rotate_row(k, src, cos_cache, sin_cache, (size_t)pos * (D / 2), D, dtype, pool_k, dst);
+        else
+          memcpy((char *)pool_k + dst * es, (const char *)k + src * es, (size_t)D * es);
+        memcpy((char *)pool_v + dst * es, (const char *)v + src * es, (size_t)D * es);
+      }
+    if (q_rot) {
+      for (int i = 0; i < curr; ++i)
+        for (int h = 0; h < Hq; ++h) {
+          size_t off = (((size_t)b * curr + i) * Hq + h) * D;
+          if (do_rotary)
+            rotate_row(q, off, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, q_rot, off);
+          else
+            memcpy((char *)q_rot + off * es, (const char *)q + off * es, (size_t)D * es);
+        }
+    }
+  }
+  if (status_out) *status_out = status_all;
+}
+
+/* Attention over a paged cache: positions [0, total) gathered in order from their pages,
+ * then the same oracle_attend_row and band predicate as the contiguous layout. */
+void oracle_attention_paged(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t page,
+                            int32_t max_pages, int32_t num_pages, int32_t rope_len, int32_t dtype, double scale,
+                            double softcap, int32_t window, int32_t causal, int32_t do_rotary,
+                            int32_t smooth_softmax, const int32_t *table, const void *q, const void *pool_k,
+                            const void *pool_v, const int32_t *seqlens_k, const float *head_sink,
+                            const int64_t *rows, int64_t nrows, double *out) {
+  int G = Hq / Hkv;
+  size_t es = elem_size(dtype);
+  int32_t cap = max_pages * page;
+  if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  int64_t count = rows ? nrows : (int64_t)B * curr * Hq;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t t = 0; t < count; ++t) {
+    int64_t r = rows ? rows[t] : t;
+    int hq = (int)(r % Hq);
+    int i = (int)((r / Hq) % curr);
+    int b = (int)(r / ((int64_t)Hq * curr));
+    double *o = out + (size_t)t * D;
+    int32_t past = seqlens_k[b];
+    if (oracle_paged_status(past, curr, cap, do_rotary, rope_len, window, table + (size_t)b * max_pages, page,
+                            num_pages)) {
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      continue;
+    }
+    int hk = hq / G;
+    int64_t total = (int64_t)past + curr;
+    int64_t q_abs = (int64_t)past + i;
+    int64_t first = window > 0 ? ((past - window + 1 > 0 ? past - window + 1 : 0) / page) * page : 0;
+    int64_t n = total - first;  /* positions before `first` are never visible */
+    char *kg = (char *)malloc((size_t)n * D * es);
+    char *vg = (char *)malloc((size_t)n * D * es);
+    uint8_t *vis = (uint8_t *)malloc((size_t)n);
+    for (int64_t j = 0; j < n; ++j) {
+      int64_t pos = first + j;
+      size_t src = paged_row(b, hk, pos, Hkv, page, table, max_pages) * D;
+      memcpy(kg + (size_t)j * D * es, (const char *)pool_k + src * es, (size_t)D * es);
+      memcpy(vg + (size_t)j * D * es, (const char *)pool_v + src * es, (size_t)D * es);
+      vis[j] = (uint8_t)oracle_visible(q_abs, pos, total, causal, window);
+    }
+    double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
+    int has_sink = head_sink != NULL || smooth_softmax;
+    double z = head_sink ? (double)head_sink[hq] : 0.0;
+    oracle_attend_row(qv, kg, vg, 0, n, vis, D, dtype, scale, softcap, has_sink, z, o);
+    free(qv);
+    free(vis);
+    free(vg);
+    free(kg);
+  }
+}
+
 int32_t oracle_has_openmp(void) {
 #ifdef _OPENMP
   return 1;
