@@ -101,6 +101,7 @@ typedef int32_t gqa_status;
 #define GQA_DEV_BAD_SEQLEN 1   /* seqlens_k[b] < 0 or > cap - curr (or > cap_past) */
 #define GQA_DEV_BAD_ROPE_POS 2 /* past_b + curr > rope_len with do_rotary */
 #define GQA_DEV_TIMEOUT 4      /* a bounded pipeline wait gave up; outputs invalid */
+#define GQA_DEV_BAD_PAGE 8     /* a block-table entry the step uses is outside [0, num_pages) */
 
 typedef enum { GQA_F32 = 0, GQA_F16 = 1, GQA_BF16 = 2 } gqa_dtype;
 
@@ -187,6 +188,25 @@ gqa_status gqa_attention_decode_noalloc(const gqa_params *p, const void *q, cons
                                         const void *cos_cache, const void *sin_cache, const float *head_sink,
                                         void *out, void *present_k, void *present_v, int32_t *dev_status,
                                         void *stream);
+
+/* Decode over a paged KV cache ([P3] Summary: a cell cache whose slots belong to sequences
+ * and are masked, not evicted).  The cache is a pool of pages of 64 positions,
+ * k_pool/v_pool [num_pages, Hkv, 64, D] (dtype), shared by all sequences; block_table is
+ * int32 [B, max_pages] on the device, entry n of row b naming the page that holds positions
+ * [64n, 64n + 64) of sequence b.  p->cap_present must be 64 * max_pages (the logical
+ * capacity of a sequence); p->cap_past is ignored and p->kv_ring must be 0.  The step's rows
+ * are written into their pages (in place: there is no separate past).  Only the entries for
+ * the positions the step reads or writes ([first page of the band, last new position]) are
+ * read; a sequence for which one of them lies outside [0, num_pages) gets zeros, nothing
+ * written, and GQA_DEV_BAD_PAGE.  Otherwise the same semantics, kernel, workspace
+ * (gqa_workspace_bytes) and errors as gqa_attention_decode, including k = v = NULL for
+ * attention only; shapes outside the split-KV kernel's envelope return GQA_ERR_UNSUPPORTED. */
+gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const void *k, const void *v,
+                                      const int32_t *seqlens_k, const int32_t *block_table, int32_t max_pages,
+                                      int32_t num_pages, const void *cos_cache, const void *sin_cache,
+                                      const float *head_sink, void *out, void *k_pool, void *v_pool,
+                                      void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                      void *stream);
 
 /* Static description of a status code. */
 const char *gqa_status_string(gqa_status s);

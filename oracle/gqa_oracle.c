@@ -460,7 +460,7 @@ void oracle_attention_ring(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_
  * sequence b.  The logical capacity is max_pages * page; the band predicate is unchanged.
  * A sequence whose table entries for the positions it reads or writes ([lo, total) with lo
  * the band's first position, rounded down to a page) fall outside [0, num_pages) is
- * rejected like a bad seqlens_k: bit 4, zeros, nothing written.
+ * rejected like a bad seqlens_k: bit 8, zeros, nothing written.
  * ---------------------------------------------------------------------------------- */
 int32_t oracle_paged_status(int32_t past, int32_t curr, int32_t cap, int32_t do_rotary, int32_t rope_len,
                             int32_t window, const int32_t *table_row, int32_t page, int32_t num_pages) {
@@ -469,7 +469,7 @@ int32_t oracle_paged_status(int32_t past, int32_t curr, int32_t cap, int32_t do_
   int64_t total = (int64_t)past + curr;
   int64_t lo = window > 0 ? (past - window + 1 > 0 ? past - window + 1 : 0) : 0;
   for (int64_t n = lo / page; n * page < total; ++n)
-    if (table_row[n] < 0 || table_row[n] >= num_pages) return 4;
+    if (table_row[n] < 0 || table_row[n] >= num_pages) return 8;
   return 0;
 }
 

@@ -58,6 +58,8 @@ struct DecodeArgs {
   int32_t *status;
   int Hq, Hkv, G, curr, R, cap, cap_past, past_separate, rope_len, do_rotary, append;
   int window, causal, splits, has_sink, ring;
+  const int32_t *table;  // paged cache: [B][max_pages] page of positions [64n, 64n + 64); null otherwise
+  int max_pages, num_pages;
   float score_mul;  // scale*log2(e), or scale/softcap with softcap
   float cap_mul;    // softcap*log2(e), 0 without softcap
 };
@@ -134,7 +136,9 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
     const int rr = (w / per_row) % nrows, c = (w % per_row) * 8;
     const int pos = r0 + rr, i = pos - past;
     const size_t src = (((size_t)b * a.curr + i) * a.Hkv + h) * D;
-    const size_t dst = (((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos)) * D;
+    const size_t dst =
+        a.table ? (((size_t)a.table[(size_t)b * a.max_pages + pos / KT] * a.Hkv + h) * KT + pos % KT) * D
+                : (((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos)) * D;
     if (which == 0 && a.do_rotary) {
       uint4 y1, y2;
       rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c,
@@ -226,9 +230,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     return;
   }
   const int total = past + a.curr;
-  // a ring starts its tiles on 64-position boundaries (the capacity is a multiple of 64, so
-  // a tile never straddles the wrap); the keys before the band are masked like any other
-  const int lo = a.ring ? max(0, past - a.window + 1) & ~(KT - 1) : (a.window > 0 ? max(0, past - a.window + 1) : 0);
+  // a ring or a paged cache starts its tiles on 64-position boundaries (a tile is then one
+  // page, or never straddles the ring's wrap); the keys before the band are masked like any
+  // other
+  const int band_lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
+  const int lo = (a.ring || a.table) ? band_lo & ~(KT - 1) : band_lo;
+  if (a.table) {
+    // every page the group reads or writes must exist; the same decision in every CTA
+    const int32_t *trow = a.table + (size_t)b * a.max_pages;
+    bool bad = false;
+    for (int n = lo / KT + (int)threadIdx.x; n * KT < total; n += kThreads) bad |= trow[n] < 0 || trow[n] >= a.num_pages;
+    if (__syncthreads_or(bad)) {
+      if (split == 0) {
+        if (threadIdx.x == 0 && hkv == 0) report(a.status, GQA_DEV_BAD_PAGE);
+        for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+          const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
+          out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
+        }
+      }
+      return;
+    }
+  }
   const int len = total - lo;
   const int chunk = ((len + a.splits - 1) / a.splits + KT - 1) / KT * KT;  // this group's chunk
   const int nchunks = (len + chunk - 1) / chunk;
@@ -251,9 +273,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_expect_tx(&full[s], L::kStageBytes);
       uint8_t *kdst = stages + s * L::kStageBytes;
       uint8_t *vdst = kdst + L::kTileBytes;
-      const int row = a.ring ? k0 % a.cap : k0;
-      tma_load_4d(kdst, &tmk, 0, row, 0, bh, &full[s]);  // [D/64][KT][64], one copy each
-      tma_load_4d(vdst, &tmv, 0, row, 0, bh, &full[s]);
+      int row = a.ring ? k0 % a.cap : k0, group = bh;
+      if (a.table) {  // the tile is one page: rows [0, 64) of (page, kv head)
+        group = a.table[(size_t)b * a.max_pages + k0 / KT] * a.Hkv + hkv;
+        row = 0;
+      }
+      tma_load_4d(kdst, &tmk, 0, row, 0, group, &full[s]);  // [D/64][KT][64], one copy each
+      tma_load_4d(vdst, &tmv, 0, row, 0, group, &full[s]);
     }
     __syncwarp();
   };
@@ -715,9 +741,12 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   using L = Smem<D, MT, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
   CUtensorMap tk, tv;
-  const long long outer = (long long)c.p.batch * c.p.kv_heads;
-  if (!encode_kv_tile_map(&tk, c.present_k, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
-  if (!encode_kv_tile_map(&tv, c.present_v, D, c.p.cap_present, outer, KT, 2)) return GQA_ERR_CUDA;
+  // contiguous or ring: [B*Hkv][cap][D]; paged: [num_pages*Hkv][64][D]
+  const bool paged = c.block_table != nullptr;
+  const long long outer = paged ? (long long)c.num_pages * c.p.kv_heads : (long long)c.p.batch * c.p.kv_heads;
+  const int rows = paged ? KT : c.p.cap_present;
+  if (!encode_kv_tile_map(&tk, c.present_k, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_tile_map(&tv, c.present_v, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
   auto kern = decode_split_kernel<T, D, MT, NST, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
@@ -768,6 +797,9 @@ template <typename T> gqa_status launch_t(const Call &c, const DecodePlan &dp, c
   a.R = dp.rows;
   a.cap = p.cap_present;
   a.ring = p.kv_ring;
+  a.table = c.block_table;
+  a.max_pages = c.max_pages;
+  a.num_pages = c.num_pages;
   a.cap_past = p.cap_past;
   a.past_separate = c.past_separate;
   a.rope_len = p.rope_len;

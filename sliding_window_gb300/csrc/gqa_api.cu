@@ -291,6 +291,35 @@ gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
 
+gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const void *k, const void *v,
+                                      const int32_t *seqlens_k, const int32_t *block_table, int32_t max_pages,
+                                      int32_t num_pages, const void *cos_cache, const void *sin_cache,
+                                      const float *head_sink, void *out, void *k_pool, void *v_pool,
+                                      void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                      void *stream) {
+  gqa::Call c;
+  gqa_status s = gqa::make_call(c, p, q, k, v, nullptr, nullptr, seqlens_k, cos_cache, sin_cache, head_sink, out,
+                                k_pool, v_pool, dev_status, stream);
+  if (s != GQA_OK) return s;
+  if (p->kv_ring) return GQA_ERR_INVALID_ARG;
+  if (!block_table || (reinterpret_cast<uintptr_t>(block_table) & 3u)) return GQA_ERR_INVALID_ARG;
+  if (max_pages < 1 || num_pages < 1) return GQA_ERR_INVALID_ARG;
+  if ((long long)max_pages * 64 != p->cap_present) return GQA_ERR_CAPACITY;
+  if ((long long)num_pages * p->kv_heads > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
+  if (!out || !gqa::aligned16(out)) return GQA_ERR_INVALID_ARG;
+  c.block_table = block_table;
+  c.max_pages = max_pages;
+  c.num_pages = num_pages;
+  const gqa::DecodePlan dp = gqa::decode_plan(c.p);
+  if (!dp.eligible) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads pages
+  const gqa::WsLayout wl = gqa::workspace_layout(c.p, c.append && p->do_rotary);
+  const size_t need = dp.splits > 1 && !dp.cluster ? wl.total : 0;
+  if (need > 0 && (!workspace || !gqa::aligned16(workspace) || workspace_bytes < need)) return GQA_ERR_WORKSPACE;
+  c.ws = static_cast<char *>(workspace);
+  c.ws_bytes = workspace_bytes;
+  return gqa::launch_decode_split(c, dp, wl);
+}
+
 gqa_status gqa_rope_append_kv(const gqa_params *p, const void *q, const void *k, const void *v, const void *past_k,
                               const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
                               const void *sin_cache, void *q_rot, void *present_k, void *present_v,

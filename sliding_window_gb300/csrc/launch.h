@@ -27,6 +27,10 @@ struct Call {
   void *q_rot = nullptr;           // where K1 writes rotated q (nullptr: not needed)
   int past_separate = 0;           // past and present are different buffers
   int append = 1;                  // 0: attention only (present already holds the step)
+  // paged cache: present_k/v are pools [num_pages][Hkv][64][D], the table maps
+  // (sequence, position / 64) to a page
+  const int32_t *block_table = nullptr;
+  int max_pages = 0, num_pages = 0;
   int32_t *status = nullptr;
   cudaStream_t stream = nullptr;
   char *ws = nullptr;

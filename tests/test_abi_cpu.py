@@ -119,6 +119,32 @@ def test_ring_rules(g):
     assert call(g, good_params(g, kv_ring=1, window=1000, cap_present=1024, q_len=4, dtype="f32")) == 2
 
 
+def call_paged(g, p, table=FAKE, max_pages=16, num_pages=40, ws_bytes=0, **ptrs):
+    names = ["q", "k", "v", "seqlens_k", "cos", "sin", "head_sink", "out", "k_pool", "v_pool", "workspace"]
+    vals = {n: FAKE for n in names}
+    vals.update(ptrs)
+    a = [ctypes.c_void_p(vals[n]) if vals[n] is not None else None for n in names]
+    tab = ctypes.c_void_p(table) if table is not None else None
+    return g.lib.gqa_attention_decode_paged(ctypes.byref(p), a[0], a[1], a[2], a[3], tab, max_pages, num_pages,
+                                            a[4], a[5], a[6], a[7], a[8], a[9], a[10], ws_bytes, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(table=None), 1), (dict(table=FAKE + 2), 1),      # missing or misaligned block table
+    (dict(max_pages=0), 1), (dict(num_pages=0), 1),
+    (dict(max_pages=15), 3),                              # cap_present must be 64 * max_pages
+    (dict(out=None), 1), (dict(k_pool=FAKE + 8), 1),
+])
+def test_paged_invalid_arguments(g, kw, code):
+    assert call_paged(g, good_params(g), **kw) == code
+
+
+def test_paged_rejects_ring_and_unsupported_shapes(g):
+    assert call_paged(g, good_params(g, kv_ring=1, window=1000)) == 1
+    assert call_paged(g, good_params(g, dtype="f32")) == 2          # only the split decode kernel reads pages
+    assert call_paged(g, good_params(g, q_heads=64, q_len=2)) == 2  # 64 rows per group at D=128
+
+
 def test_attention_only_rejects_rotary(g):
     p = good_params(g, do_rotary=1, rope_len=4096)
     assert call(g, p, k=None, v=None) == 1
