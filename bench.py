@@ -192,6 +192,18 @@ class Step:
             L = dict(c=c, p=p, p_attend=gqa.params_from_dict(dict(c.params, do_rotary=0)), ws=ws,
                      out=torch.empty_like(c.q), q_rot=torch.empty_like(c.q),
                      status=torch.zeros(1, dtype=torch.int32, device=device))
+            if w.kv_paged:  # the same rows, moved into a shuffled pool of 64-position pages
+                B, Hkv, cap, D = c.past_k.shape
+                mp = cap // gqa.PAGE
+                perm = torch.randperm(B * mp, generator=torch.Generator().manual_seed(77 + set_index))
+                L["table"] = perm.view(B, mp).to(torch.int32).to(device)
+                L["npages"] = B * mp
+                for name in ("k", "v"):
+                    lin = getattr(c, "past_" + name).view(B, Hkv, mp, gqa.PAGE, D).permute(0, 2, 1, 3, 4)
+                    pool = torch.empty(B * mp, Hkv, gqa.PAGE, D, dtype=lin.dtype, device=device)
+                    pool[perm.to(device)] = lin.reshape(B * mp, Hkv, gqa.PAGE, D)
+                    L["pool_" + name] = pool
+                c.past_k = c.past_v = None
             self.layers.append(L)
         self.fn = gqa.gqa_attention_decode if w.mode == "decode" else gqa.gqa_attention_prefill
         # all layers' outputs side by side, for one device->host copy per step
@@ -210,10 +222,20 @@ class Step:
         """One step through the public call: append (+RoPE) then attention, per layer."""
         for L in self.layers:
             c = L["c"]
+            if self.w.kv_paged:
+                self.g.check(self.g.gqa_attention_decode_paged(L["p"], c.q, c.k, c.v, c.seqlens_k, L["table"],
+                                                               L["npages"], c.cos, c.sin, c.head_sink, L["out"],
+                                                               L["pool_k"], L["pool_v"], L["ws"], L["status"],
+                                                               stream), "paged step")
+                continue
             self.g.check(self.fn(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin, c.head_sink,
                                  L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "step")
 
     def append_only(self, stream):
+        if self.w.kv_paged:  # the paged call appends itself: one full (untimed) step puts the rows in
+            assert not self.w.do_rotary
+            self.full(stream)
+            return
         for L in self.layers:
             c = L["c"]
             self.g.check(self.g.gqa_rope_append_kv(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos,
@@ -224,6 +246,12 @@ class Step:
         for L in self.layers:
             c = L["c"]
             q = L["q_rot"] if self.w.do_rotary else c.q
+            if self.w.kv_paged:
+                self.g.check(self.g.gqa_attention_decode_paged(L["p_attend"], q, None, None, c.seqlens_k, L["table"],
+                                                               L["npages"], None, None, c.head_sink, L["out"],
+                                                               L["pool_k"], L["pool_v"], L["ws"], L["status"],
+                                                               stream), "paged attend")
+                continue
             self.g.check(self.fn(L["p_attend"], q, None, None, None, None, c.seqlens_k, None, None, c.head_sink,
                                  L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "attend")
 
@@ -231,7 +259,9 @@ class Step:
         tot = 0
         for L in self.layers:
             c = L["c"]
-            for t in (c.past_k, c.past_v, L["ws"], L["q_rot"]):
+            for t in (c.past_k, c.past_v, L.get("pool_k"), L.get("pool_v"), L["ws"], L["q_rot"]):
+                if t is None:
+                    continue
                 tot += t.numel() * t.element_size()
         tot += self.stage.numel() + self.out_all.numel() * self.out_all.element_size()
         return tot
@@ -542,7 +572,7 @@ def main():
     if args.steps is None:
         args.steps = {"decode_window_bf16": 100000, "specdecode_rotary_f16": 20000, "decode_long_bf16": 1500,
                       "prefill_sink_softcap_bf16": 500, "prefill_fp32_tiny": 20000,
-                      "decode_window_ring_bf16": 100000}[args.workload]
+                      "decode_window_ring_bf16": 100000, "decode_window_paged_bf16": 100000}[args.workload]
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

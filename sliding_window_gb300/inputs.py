@@ -47,6 +47,7 @@ class Workload:
     rope_theta: float = 10000.0
     garbage_std: float = 10.0
     kv_ring: int = 0        # 1: the cache is a ring of `cap` slots, position p in slot p % cap
+    kv_paged: int = 0       # 1: the cache is a shared pool of 64-position pages behind a block table
 
     @property
     def layers(self) -> int:
@@ -83,6 +84,9 @@ WORKLOADS = {
         # a quarter of the cache memory
         Workload("decode_window_ring_bf16", 5, "decode", "bf16", 8, 32, 8, 128, 1, 1024, 512, 4095,
                  windows=(1024,), kv_ring=1),
+        # the windowed decode over a paged cache: the same rows in a shuffled pool of pages
+        Workload("decode_window_paged_bf16", 6, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
+                 windows=(1024,), kv_paged=1),
     ]
 }
 

@@ -93,3 +93,36 @@ def test_decode_window_ring_bf16():
     np.testing.assert_array_equal(storage(r["present_v"]), pv)
     ref = oracle.attention_ring(p, q_rot, pk, pv, host["seq"], host["sink"])
     assert_close(out_rows(r["out"], c), ref, w.dtype, w.name)
+
+
+def test_decode_window_paged_bf16():
+    """The windowed decode through a shuffled pool of 64-position pages: the pages written bit
+    for bit, sampled rows against the paged oracle."""
+    from sliding_window_gb300 import gqa
+    w = WORKLOADS["decode_window_paged_bf16"]
+    c = make_case(w, device="cpu")
+    B, Hkv, cap, D = c.past_k.shape
+    mp = cap // gqa.PAGE
+    table = np.random.default_rng(5).permutation(B * mp).reshape(B, mp).astype(np.int32)
+    pools = []
+    for lin in (storage(c.past_k), storage(c.past_v)):
+        pool = np.empty((B * mp, Hkv, gqa.PAGE, D), dtype=lin.dtype)
+        pool[table.ravel()] = lin.reshape(B, Hkv, mp, gqa.PAGE, D).transpose(0, 2, 1, 3, 4).reshape(-1, Hkv, gqa.PAGE, D)
+        pools.append(pool)
+    dev = [torch.from_numpy(x).view(torch.int16).view(torch.bfloat16).cuda() for x in pools]
+    p = gqa.params_from_dict(c.params)
+    out = torch.empty(c.q.shape, dtype=c.q.dtype, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device="cuda")
+    gqa.check(gqa.gqa_attention_decode_paged(p, c.q.cuda(), c.k.cuda(), c.v.cuda(), c.seqlens_k.cuda(),
+                                             torch.from_numpy(table).cuda(), B * mp, None, None, None, out, dev[0],
+                                             dev[1], ws, st), "paged")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    q_rot, pk, pv, s = oracle.rope_append_paged(c.params, storage(c.q), storage(c.k), storage(c.v), pools[0],
+                                                pools[1], c.seqlens_k.numpy(), table, B * mp)
+    assert s == 0
+    np.testing.assert_array_equal(storage(dev[0]), pk)
+    np.testing.assert_array_equal(storage(dev[1]), pv)
+    ref = oracle.attention_paged(c.params, q_rot, pk, pv, c.seqlens_k.numpy(), table, B * mp)
+    assert_close(out_rows(out, c), ref, w.dtype, w.name)
