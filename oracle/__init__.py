@@ -84,6 +84,8 @@ def _load():
         lib.oracle_ring_status.restype = i32
         lib.oracle_rope_append_ring.argtypes = [i32] * 9 + [vp] * 9 + [ctypes.POINTER(i32)]
         lib.oracle_attention_ring.argtypes = [i32] * 8 + [f64, f64] + [i32] * 4 + [vp] * 6 + [i64, vp]
+        lib.oracle_attention_masked.argtypes = [i32] * 8 + [f64, f64] + [i32] * 5 + [vp, i64, i64, i64, i32] + \
+            [vp] * 6 + [i64, vp]
         lib.oracle_paged_status.argtypes = [i32] * 6 + [vp, i32, i32]
         lib.oracle_paged_status.restype = i32
         lib.oracle_rope_append_paged.argtypes = [i32] * 12 + [vp] * 10 + [ctypes.POINTER(i32)]
@@ -343,6 +345,41 @@ def attention_paged(p: dict, q_rot, pool_k, pool_v, seqlens_k, table, num_pages,
                                int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
                                int(p.get("smooth_softmax", 0)), _ptr(tab), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq),
                                _ptr(sink), _ptr(ridx), n, _ptr(out))
+    if rows is None:
+        return out.reshape(B, curr, Hq, D)
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# Attention masks ([P4] "Layouts and semantics"; [P2] "What changed": attention_bias)
+# --------------------------------------------------------------------------------------
+def attention_masked(p: dict, q_rot, present_k, present_v, seqlens_k, mask, kind: str, head_sink=None,
+                     rows=None) -> np.ndarray:
+    """Attention in fp64 with a mask broadcastable to [B, Hq, curr, keys] (numpy array with
+    4 dims, size-1 dims broadcast): kind "bool" (nonzero keeps) or "add" (values of the
+    dtype, storage bits for f16/bf16, added to the scaled score before the softcap)."""
+    lib = _load()
+    dt = p["dtype"]
+    qb = _bits(q_rot, dt)
+    kb, vb = _bits(present_k, dt), _bits(present_v, dt)
+    seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    sink = None if head_sink is None else np.ascontiguousarray(head_sink, dtype=np.float32)
+    m = np.ascontiguousarray(mask, dtype=np.uint8) if kind == "bool" else _bits(mask, dt)
+    assert m.ndim == 4
+    st = [0 if m.shape[d] == 1 else int(np.prod(m.shape[d + 1:])) for d in range(3)]
+    B, Hq, D, curr = p["batch"], p["q_heads"], p["head_dim"], p["q_len"]
+    if rows is None:
+        ridx, n = None, B * curr * Hq
+    else:
+        ridx = np.ascontiguousarray(rows, dtype=np.int64)
+        n = ridx.shape[0]
+    out = np.zeros((n, D), dtype=np.float64)
+    lib.oracle_attention_masked(B, Hq, p["kv_heads"], D, curr, p["cap_present"], p.get("rope_len", 0),
+                                DTYPE_CODES[dt], float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)),
+                                int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
+                                int(p.get("smooth_softmax", 0)), 1 if kind == "bool" else 2, _ptr(m), st[0], st[1],
+                                st[2], m.shape[3], _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq), _ptr(sink), _ptr(ridx), n,
+                                _ptr(out))
     if rows is None:
         return out.reshape(B, curr, Hq, D)
     return out

@@ -244,8 +244,8 @@ int32_t oracle_visible(int64_t q_abs, int64_t j, int64_t total, int32_t causal, 
 }
 
 /* ------------------------------------------------------------------------------------
- * One query row over an explicit visibility mask.
- *   s_j = scale * <q, k_j>;  if softcap > 0: s_j = softcap * tanh(s_j / softcap)
+ * One query row over an explicit visibility mask (and, optionally, an additive bias).
+ *   s_j = scale * <q, k_j> [+ bias_j];  if softcap > 0: s_j = softcap * tanh(s_j / softcap)
  *   the sink z (when present) is one more logit in the denominator only, not scaled and
  *   not capped ([P1] "smooth_softmax / head_sink": the extra logit joins the softmax
  *   denominator and is sliced out);
@@ -254,9 +254,9 @@ int32_t oracle_visible(int64_t q_abs, int64_t j, int64_t total, int32_t causal, 
  *   ([P4] "A fully masked query row produces zeros rather than NaN").
  * q is D doubles; k and v point at `n` rows of D elements of `dtype`.
  * ---------------------------------------------------------------------------------- */
-void oracle_attend_row(const double *q, const void *k, const void *v, int64_t row0, int64_t n,
-                       const uint8_t *visible, int32_t D, int32_t dtype, double scale, double softcap,
-                       int32_t has_sink, double sink, double *out) {
+void oracle_attend_row_bias(const double *q, const void *k, const void *v, int64_t row0, int64_t n,
+                            const uint8_t *visible, const double *bias, int32_t D, int32_t dtype, double scale,
+                            double softcap, int32_t has_sink, double sink, double *out) {
   double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   double M = -INFINITY;
   int any = 0;
@@ -265,6 +265,7 @@ void oracle_attend_row(const double *q, const void *k, const void *v, int64_t ro
     double dot = 0.0;
     for (int d = 0; d < D; ++d) dot += q[d] * load_elem(k, (size_t)(row0 + j) * D + d, dtype);
     double sj = scale * dot;
+    if (bias) sj += bias[j];
     if (softcap > 0.0) sj = softcap * tanh(sj / softcap);
     s[j] = sj;
     if (sj > M) M = sj;
@@ -285,6 +286,12 @@ void oracle_attend_row(const double *q, const void *k, const void *v, int64_t ro
   }
   for (int d = 0; d < D; ++d) out[d] /= den;
   free(s);
+}
+
+void oracle_attend_row(const double *q, const void *k, const void *v, int64_t row0, int64_t n,
+                       const uint8_t *visible, int32_t D, int32_t dtype, double scale, double softcap,
+                       int32_t has_sink, double sink, double *out) {
+  oracle_attend_row_bias(q, k, v, row0, n, visible, NULL, D, dtype, scale, softcap, has_sink, sink, out);
 }
 
 /* ------------------------------------------------------------------------------------
@@ -570,6 +577,65 @@ void oracle_attention_paged(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32
     free(vis);
     free(vg);
     free(kg);
+  }
+}
+
+/* ------------------------------------------------------------------------------------
+ * Attention masks ([P4] "Layouts and semantics": boolean and FLOAT additive broadcast masks
+ * next to the bottom-right causal band; [P2] "What changed": attention_bias is summed with
+ * the causal band).  The mask is indexed [b][hq][i][j] with element strides stride_b,
+ * stride_h, stride_i (0 broadcasts that dimension) and contiguous keys j = absolute
+ * position (slot) in [0, keys).  kind 1: uint8, nonzero keeps the key, zero removes it
+ * from the row's softmax like the band does.  kind 2: values of the dtype added to the
+ * scaled score before the softcap (matmul, mask, softcap, softmax).  The band, the sink and
+ * the fully-masked-row rule are unchanged; the contiguous layout only.
+ * ---------------------------------------------------------------------------------- */
+void oracle_attention_masked(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap_present,
+                             int32_t rope_len, int32_t dtype, double scale, double softcap, int32_t window,
+                             int32_t causal, int32_t do_rotary, int32_t smooth_softmax, int32_t mask_kind,
+                             const void *mask, int64_t stride_b, int64_t stride_h, int64_t stride_i, int32_t keys,
+                             const void *q, const void *present_k, const void *present_v, const int32_t *seqlens_k,
+                             const float *head_sink, const int64_t *rows, int64_t nrows, double *out) {
+  int G = Hq / Hkv;
+  if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  int64_t count = rows ? nrows : (int64_t)B * curr * Hq;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t t = 0; t < count; ++t) {
+    int64_t r = rows ? rows[t] : t;
+    int hq = (int)(r % Hq);
+    int i = (int)((r / Hq) % curr);
+    int b = (int)(r / ((int64_t)Hq * curr));
+    double *o = out + (size_t)t * D;
+    int32_t past = seqlens_k[b];
+    if (oracle_sequence_status(past, curr, 0, cap_present, 0, do_rotary, rope_len) ||
+        (int64_t)past + curr > keys) {
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      continue;
+    }
+    int hk = hq / G;
+    int64_t total = (int64_t)past + curr;
+    int64_t q_abs = (int64_t)past + i;
+    size_t mrow = (size_t)(b * stride_b + hq * stride_h + i * stride_i);
+    double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
+    uint8_t *vis = (uint8_t *)malloc((size_t)cap_present);
+    double *bias = mask_kind == 2 ? (double *)malloc(sizeof(double) * (size_t)cap_present) : NULL;
+    for (int64_t j = 0; j < cap_present; ++j) {
+      vis[j] = (uint8_t)oracle_visible(q_abs, j, total, causal, window);
+      if (!vis[j]) continue;
+      if (mask_kind == 1) vis[j] = ((const uint8_t *)mask)[mrow + (size_t)j] != 0;
+      if (mask_kind == 2) bias[j] = load_elem(mask, mrow + (size_t)j, dtype);
+    }
+    int has_sink = head_sink != NULL || smooth_softmax;
+    double z = head_sink ? (double)head_sink[hq] : 0.0;
+    int64_t row0 = ((int64_t)b * Hkv + hk) * cap_present;
+    oracle_attend_row_bias(qv, present_k, present_v, row0, cap_present, vis, bias, D, dtype, scale, softcap,
+                           has_sink, z, o);
+    free(bias);
+    free(vis);
+    free(qv);
   }
 }
 

@@ -22,9 +22,11 @@ def visible_set(past, curr, i, window, causal):
 
 
 def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, causal, scale,
-              softcap=0.0, sinks=None):
+              softcap=0.0, sinks=None, keep=None, bias=None):
     """q[b][i][hq] -> list of D floats; present_k[b][h][j] -> list of D floats.
-    sinks: None, or a list of Hq floats.  Returns out[b][i][hq] lists of D floats."""
+    sinks: None, or a list of Hq floats.  keep(b, hq, i, j) -> bool removes keys from the
+    row (a boolean mask); bias(b, hq, i, j) -> float is added to the scaled score before
+    the softcap (an additive mask).  Returns out[b][i][hq] lists of D floats."""
     G = Hq // Hkv
     out = []
     for b in range(B):
@@ -34,10 +36,14 @@ def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, cau
             for hq in range(Hq):
                 h = hq // G
                 keys = sorted(visible_set(seqlens[b], curr, i, window, causal))
+                if keep is not None:
+                    keys = [j for j in keys if keep(b, hq, i, j)]
                 logits = []
                 values = []
                 for j in keys:
                     s = scale * math.fsum(a * c for a, c in zip(q[b][i][hq], present_k[b][h][j]))
+                    if bias is not None:
+                        s = s + bias(b, hq, i, j)
                     if softcap > 0:
                         s = softcap * math.tanh(s / softcap)
                     logits.append(s)
