@@ -208,6 +208,36 @@ gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const 
                                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                       void *stream);
 
+/* Attention mask ([P4] "Layouts and semantics": boolean and FLOAT additive broadcast
+ * masks next to the bottom-right causal band; [P2] "What changed": attention_bias summed
+ * with the band).  Element [b][hq][i][j] (batch, q head, new token, key = absolute
+ * position) is at data + b*stride_b + hq*stride_h + i*stride_i + j elements; a stride of 0
+ * broadcasts that dimension, and the keys are contiguous.  kind GQA_MASK_KEEP: uint8, zero
+ * removes the key from the row's softmax exactly like the band does.  kind GQA_MASK_ADD:
+ * values of the params' dtype added to the scaled score before the softcap (score, mask,
+ * softcap, softmax).  keys: the extent of the key dimension; a sequence with
+ * seqlens_k + q_len > keys is rejected (GQA_DEV_BAD_SEQLEN, zeros).  The band, the sink and
+ * the fully-masked-row rule are unchanged. */
+#define GQA_MASK_KEEP 1
+#define GQA_MASK_ADD 2
+typedef struct gqa_mask {
+  const void *data;
+  int32_t kind;
+  int32_t keys;
+  int64_t stride_b, stride_h, stride_i;
+} gqa_mask;
+
+/* Decode step with an attention mask: gqa_attention_decode's arguments and semantics plus
+ * *mask (device data, host struct).  Runs the split-KV kernel only: f32 params, or shapes
+ * outside its envelope, return GQA_ERR_UNSUPPORTED.  Ring caches (kv_ring) are allowed;
+ * the mask stays indexed by absolute position. */
+gqa_status gqa_attention_decode_masked(const gqa_params *p, const gqa_mask *mask, const void *q, const void *k,
+                                       const void *v, const void *past_k, const void *past_v,
+                                       const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                       const float *head_sink, void *out, void *present_k, void *present_v,
+                                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                       void *stream);
+
 /* Static description of a status code. */
 const char *gqa_status_string(gqa_status s);
 

@@ -1,0 +1,921 @@
+#pragma once
+// decode_split.cuh -- K3 + K4: split-KV decode with RoPE + append fused in and the combine
+// done by the last CTA of each (b, kv head) group.
+//
+// onnx-light-cpu "Attention Kernel Design": group_size = q_heads / kv_heads maps q heads
+// onto kv heads without repeating K or V ("Layouts and semantics"); the streaming
+// recurrence keeps a running max, denominator and unnormalized output per row and skips
+// blocks outside the frontiers ("Compute paths"); fp32 accumulation, output narrowed once,
+// fully masked rows give zeros ("Scheduling, precision, and invariants").
+// OpenVINO PR #37423: window in true absolute positions, multi-token decode ("Sliding
+// window"); sink logit in the denominator only ("smooth_softmax / head_sink").
+// tract PR #2645, "What changed": the step's K (rotated) and V are appended to the cache at
+// seqlens_k and the query is rotated at the same positions; bottom-right band.
+//
+// Work decomposition (one GB300, HBM-bound): the visible band of group (b, kv head) is
+// [lo, total) with lo = max(0, past - window + 1); it is cut into S equal chunks (rounded
+// up to 64-key tiles, so no tile is read twice), one CTA each: CTA (chunk, kv head, b)
+// holds all R = G*curr query rows of the group and reads every K/V byte of its chunk once.
+// Each group's chunks are equal, so long and short sequences balance within a group; two
+// CTAs share an SM so one's prologue and epilogue overlap the other's streaming.
+//
+// Pipeline: four warps, each takes 16 keys of every 64-key tile: S = Q K^T and O += P V on
+// mma.sync m16n8k16 (fp32 accumulate), online softmax in the exp2 domain with a lazily
+// moved reference max.  K and V tiles arrive by TMA (128B swizzle) through an NST-stage
+// mbarrier ring; warp 0 refills a stage as soon as all four warps have released it, and
+// before loading the tile that holds the group's new rows it writes them to present (K
+// rotated) so the TMA reads them back.  The CTA merges its warps in shared memory; a
+// one-chunk group finishes in place, otherwise the CTA writes (m, l, acc) and the last CTA
+// of the group (atomic ticket, no spin-wait) adds the sink once, normalizes and writes out.
+// Launched with programmatic stream serialization: the prologue overlaps the previous
+// kernel's tail and griddepcontrol.wait orders every global read after it.
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace gqa {
+namespace {
+
+constexpr int KT = 64;         // keys per tile
+constexpr int kWarps = 4;      // 16 keys of a tile each
+constexpr int kThreads = kWarps * 32;
+constexpr float kRescaleLog2 = 8.f;  // move the reference max only when it grows by > 2^8
+constexpr int kMaxSplits = kDecodeMaxSplits;
+constexpr int kMaxCluster = kDecodeMaxCluster;  // chunks combined through distributed shared memory
+
+struct DecodeArgs {
+  const void *q;          // [B, curr, Hq, D] as given (rotated here when do_rotary)
+  const void *k, *v;      // [B, curr, Hkv, D] new rows, or NULL (attention only)
+  const void *cos, *sin;  // [rope_len, D/2]
+  void *present_k, *present_v;
+  void *out;              // [B, curr, Hq, D]
+  const int32_t *seqlens;
+  const float *head_sink;
+  float *part_acc;      // [B*Hkv][S][R][D]
+  float *part_ml;       // [B*Hkv][S][R][2]
+  int32_t *tickets;     // [B*Hkv]
+  int32_t *status;
+  int Hq, Hkv, G, curr, R, cap, cap_past, past_separate, rope_len, do_rotary, append;
+  int window, causal, splits, has_sink, ring;
+  const int32_t *table;  // paged cache: [B][max_pages] page of positions [64n, 64n + 64); null otherwise
+  int max_pages, num_pages;
+  // attention mask (masked kernels only): element [b][hq][i][key] at
+  // b*msb + hq*msh + i*msi + key; kind 1 = uint8 keep flags, 2 = additive values of T
+  const void *mask;
+  long long msb, msh, msi;
+  int mask_kind, mask_keys;
+  float mask_mul;  // 1 / scale: an additive value joins the raw dot product before scaling
+  float score_mul;  // scale*log2(e), or scale/softcap with softcap
+  float cap_mul;    // softcap*log2(e), 0 without softcap
+};
+
+template <int D, int MT, int NST> struct Smem {
+  static constexpr int kTileBytes = KT * D * 2;  // one K or V tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kQRows = MT * 16;
+  static constexpr int kStagesOff = 0;
+  static constexpr int kQOff = NST * kStageBytes;
+  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], empty[NST], xbar
+  static constexpr int kRedOff = kBarOff + (2 * NST + 1) * 8;             // red_m, red_l [4][QROWS]
+  static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l, sink [QROWS]
+  static constexpr int kFlagOff = kRowOff + 3 * kQRows * 4;
+  static constexpr int kBytes = kFlagOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
+  // per-warp merge regions (rows padded by 4 floats: the fragment stores of one warp
+  // instruction then spread over all banks) and the combine's chunk statistics reuse the stages
+  static constexpr int kAccStride = D + 4;
+  static_assert(kWarps * kQRows * kAccStride * 4 <= NST * kStageBytes, "merge regions must fit in the stages");
+  static_assert(2 * kMaxSplits * kQRows * 4 <= NST * kStageBytes, "chunk statistics must fit in the stages");
+  static_assert((kWarps * kQRows * kAccStride + kQRows * D + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <=
+                    NST * kStageBytes,
+                "cluster exchange buffers must fit in the stages");
+};
+
+// four consecutive outputs in one 8-byte store
+template <typename T> __device__ __forceinline__ void store4(T *o, float x, float y, float z, float w) {
+  union {
+    T e[4];
+    uint2 u;
+  } v;
+  v.e[0] = from_f32<T>(x);
+  v.e[1] = from_f32<T>(y);
+  v.e[2] = from_f32<T>(z);
+  v.e[3] = from_f32<T>(w);
+  *reinterpret_cast<uint2 *>(o) = v.u;
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ void rotate8(const T *x1p, const T *x2p, const T *cp, const T *sp, uint4 &o1, uint4 &o2) {
+  uint4 ux1 = *reinterpret_cast<const uint4 *>(x1p), ux2 = *reinterpret_cast<const uint4 *>(x2p);
+  uint4 uc = *reinterpret_cast<const uint4 *>(cp), us = *reinterpret_cast<const uint4 *>(sp);
+  const T *x1 = reinterpret_cast<const T *>(&ux1), *x2 = reinterpret_cast<const T *>(&ux2);
+  const T *c = reinterpret_cast<const T *>(&uc), *s = reinterpret_cast<const T *>(&us);
+  T *y1 = reinterpret_cast<T *>(&o1), *y2 = reinterpret_cast<T *>(&o2);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float a1 = to_f32(x1[e]), a2 = to_f32(x2[e]), fc = to_f32(c[e]), fs = to_f32(s[e]);
+    y1[e] = from_f32<T>(__fsub_rn(__fmul_rn(a1, fc), __fmul_rn(a2, fs)));
+    y2[e] = from_f32<T>(__fadd_rn(__fmul_rn(a2, fc), __fmul_rn(a1, fs)));
+  }
+}
+
+// Warp-wide: write the step's rows [r0, r1) of kv head h of sequence b to present (K
+// rotated when do_rotary), then make the generic-proxy stores visible to TMA reads.
+template <typename T, int D>
+__device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, int past, int r0, int r1, int lane) {
+  const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
+  T *pk = reinterpret_cast<T *>(a.present_k), *pv = reinterpret_cast<T *>(a.present_v);
+  const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
+  constexpr int per_row = D / 16;  // pairs of 8-element chunks (x[d..], x[d+D/2..]) per row
+  const int nrows = r1 - r0;
+  for (int w = lane; w < nrows * per_row * 2; w += 32) {
+    const int which = w / (nrows * per_row);  // 0: k, 1: v
+    const int rr = (w / per_row) % nrows, c = (w % per_row) * 8;
+    const int pos = r0 + rr, i = pos - past;
+    const size_t src = (((size_t)b * a.curr + i) * a.Hkv + h) * D;
+    const size_t dst =
+        a.table ? (((size_t)a.table[(size_t)b * a.max_pages + pos / KT] * a.Hkv + h) * KT + pos % KT) * D
+                : (((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos)) * D;
+    if (which == 0 && a.do_rotary) {
+      uint4 y1, y2;
+      rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c,
+                 y1, y2);
+      *reinterpret_cast<uint4 *>(pk + dst + c) = y1;
+      *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = y2;
+    } else {
+      const T *x = which == 0 ? kin : vin;
+      T *y = which == 0 ? pk : pv;
+      *reinterpret_cast<uint4 *>(y + dst + c) = *reinterpret_cast<const uint4 *>(x + src + c);
+      *reinterpret_cast<uint4 *>(y + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(x + src + D / 2 + c);
+    }
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+}
+
+template <typename T, int D, int MT, int NST, bool CL, bool MK>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                        DecodeArgs a) {
+  using L = Smem<D, MT, NST>;
+  using M = Mma16816<T>;
+  constexpr int QROWS = L::kQRows;
+  constexpr int DCH = D / 8;  // 16-byte chunks per row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *stages = smem + L::kStagesOff;
+  uint8_t *qs = smem + L::kQOff;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+  uint64_t *empty = full + NST;
+  uint64_t *xbar = empty + NST;  // cluster exchange: the partials sent to this CTA have landed
+  float *red_m = reinterpret_cast<float *>(smem + L::kRedOff);
+  float *red_l = red_m + kWarps * QROWS;
+  float *row_m = reinterpret_cast<float *>(smem + L::kRowOff);
+  float *row_l = row_m + QROWS;
+  float *sink_z = row_l + QROWS;  // sink logit of row r in the exp2 domain (0 when smooth_softmax)
+  volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlagOff);  // [0] abort, [1] last
+
+  const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = a.R;
+  T *out = reinterpret_cast<T *>(a.out);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    mbar_init(xbar, 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  // programmatic dependent launch: the setup above may overlap the previous kernel; every
+  // global read below must see its results
+  grid_dependency_wait();
+  __syncthreads();
+
+  // the past length, the sink logits and the raw query rows are loaded together: their
+  // latencies overlap
+  const int past = a.seqlens[b];
+  const float zsink = (threadIdx.x < R && a.head_sink) ? a.head_sink[hkv * a.G + threadIdx.x % a.G] : 0.f;
+  constexpr int QITEMS = (QROWS * (DCH / 2) + kThreads - 1) / kThreads;  // chunk pairs per thread
+  uint4 qraw[QITEMS][2];
+#pragma unroll
+  for (int u = 0; u < QITEMS; ++u) {
+    const int idx = threadIdx.x + u * kThreads;
+    const int r = idx / (DCH / 2), c = idx % (DCH / 2);
+    qraw[u][0] = qraw[u][1] = make_uint4(0, 0, 0, 0);
+    if (idx < QROWS * (DCH / 2) && r < R) {
+      const T *src = reinterpret_cast<const T *>(a.q) +
+                     (((size_t)b * a.curr + r / a.G) * a.Hq + hkv * a.G + r % a.G) * D;
+      qraw[u][0] = *reinterpret_cast<const uint4 *>(src + c * 8);
+      qraw[u][1] = *reinterpret_cast<const uint4 *>(src + D / 2 + c * 8);
+    }
+  }
+  int st = sequence_status(past, a.curr, a.ring ? INT_MAX : a.cap, a.cap_past, a.past_separate, a.do_rotary && a.append,
+                                 a.rope_len);
+  if (MK && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // the mask must cover every key
+  if (st) {  // rejected sequence: zeros, nothing appended, reported once
+    if (split == 0) {
+      if (threadIdx.x == 0 && hkv == 0) report(a.status, st);
+      for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+        const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
+        out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
+      }
+    }
+    return;
+  }
+  const int total = past + a.curr;
+  // a ring or a paged cache starts its tiles on 64-position boundaries (a tile is then one
+  // page, or never straddles the ring's wrap); the keys before the band are masked like any
+  // other
+  const int band_lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
+  const int lo = (a.ring || a.table) ? band_lo & ~(KT - 1) : band_lo;
+  if (a.table) {
+    // every page the group reads or writes must exist; the same decision in every CTA
+    const int32_t *trow = a.table + (size_t)b * a.max_pages;
+    bool bad = false;
+    for (int n = lo / KT + (int)threadIdx.x; n * KT < total; n += kThreads) bad |= trow[n] < 0 || trow[n] >= a.num_pages;
+    if (__syncthreads_or(bad)) {
+      if (split == 0) {
+        if (threadIdx.x == 0 && hkv == 0) report(a.status, GQA_DEV_BAD_PAGE);
+        for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
+          const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
+          out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
+        }
+      }
+      return;
+    }
+  }
+  const int len = total - lo;
+  const int chunk = ((len + a.splits - 1) / a.splits + KT - 1) / KT * KT;  // this group's chunk
+  const int nchunks = (len + chunk - 1) / chunk;
+  // a CTA past the group's last chunk has nothing to stream; in a cluster it still takes
+  // part in the exchange (its rows carry m = -inf), otherwise it leaves now
+  const bool idle = split >= nchunks;
+  if (idle && (!CL || nchunks == 1)) return;
+  const int c0 = lo + split * chunk;
+  const int c1 = min(total, c0 + chunk);
+  const int ntiles = idle ? 0 : (c1 - c0 + KT - 1) / KT;
+  const int bh = b * a.Hkv + hkv;
+  const bool appends = !idle && a.append && c1 > past;  // this chunk holds new rows [past, total)
+
+  // warp 0 fills the ring; the new rows go to present before the tile that holds them
+  auto issue = [&](int t) {
+    const int s = t % NST, k0 = c0 + t * KT;
+    if (appends && k0 + KT > past && k0 < total)
+      append_rows<T, D>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane);
+    if (lane == 0) {
+      mbar_expect_tx(&full[s], L::kStageBytes);
+      uint8_t *kdst = stages + s * L::kStageBytes;
+      uint8_t *vdst = kdst + L::kTileBytes;
+      int row = a.ring ? k0 % a.cap : k0, group = bh;
+      if (a.table) {  // the tile is one page: rows [0, 64) of (page, kv head)
+        group = a.table[(size_t)b * a.max_pages + k0 / KT] * a.Hkv + hkv;
+        row = 0;
+      }
+      tma_load_4d(kdst, &tmk, 0, row, 0, group, &full[s]);  // [D/64][KT][64], one copy each
+      tma_load_4d(vdst, &tmv, 0, row, 0, group, &full[s]);
+    }
+    __syncwarp();
+  };
+  int issued = 0;
+  if (warp == 0)
+    for (; issued < min(NST, ntiles); ++issued) issue(issued);
+
+  // Q rows r = i*G + g (token i, q head hkv*G + g), rotated at past + i, 128B-swizzled
+  {
+    const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
+    const bool rot = a.do_rotary && a.append;
+#pragma unroll
+    for (int u = 0; u < QITEMS; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx >= QROWS * (DCH / 2)) break;
+      const int r = idx / (DCH / 2), c = idx % (DCH / 2);  // chunk c of the first half
+      uint4 y1 = qraw[u][0], y2 = qraw[u][1];
+      if (rot && r < R) {
+        const size_t pos = (size_t)(past + r / a.G) * (D / 2);
+        rotate8<T>(reinterpret_cast<const T *>(&qraw[u][0]), reinterpret_cast<const T *>(&qraw[u][1]),
+                   cs + pos + c * 8, sn + pos + c * 8, y1, y2);
+      }
+      const int c2 = c + DCH / 2;
+      *reinterpret_cast<uint4 *>(qs + (c >> 3) * (QROWS * 128) + sw128(r, c & 7)) = y1;
+      *reinterpret_cast<uint4 *>(qs + (c2 >> 3) * (QROWS * 128) + sw128(r, c2 & 7)) = y2;
+    }
+  }
+  if (threadIdx.x < QROWS) sink_z[threadIdx.x] = zsink * kLog2e;
+  __syncthreads();
+
+  float m[MT][2], l[MT][2];
+  float acc[MT][D / 8][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      m[mt][h] = -INFINITY;
+      l[mt][h] = 0.f;
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mt][dn][e] = 0.f;
+  }
+  const uint32_t qs_u32 = smem_u32(qs);
+  const int q_abs_min = past, q_abs_max = past + a.curr - 1;
+  bool aborted = false;
+  int t_fail = ntiles;
+
+  // masked kernels: this thread's mask values for a tile (rows 16*mt + lane/4 + 8h, keys
+  // kb + 8n + 2*(lane%4) + {0,1}), 16 bits each, packed in pairs; loaded one tile ahead
+  uint32_t mcur[MK ? MT : 1][2][2], mnext[MK ? MT : 1][2][2];
+  auto load_mask = [&](int t, uint32_t (&mv)[MK ? MT : 1][2][2]) {
+    const int kb = c0 + t * KT + 16 * warp;
+    const uint32_t dflt = a.mask_kind == 1 ? 1u : 0u;  // keep / no bias where there is no row
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = 16 * mt + (lane >> 2) + 8 * h;
+          const int key = kb + 8 * n + 2 * (lane & 3);
+          uint32_t lo = dflt, hi = dflt;
+          if (row < R) {
+            const int i = row / a.G, g = row % a.G;
+            const long long base = b * a.msb + (long long)(hkv * a.G + g) * a.msh + i * a.msi;
+            if (a.mask_kind == 1) {
+              const uint8_t *mp = reinterpret_cast<const uint8_t *>(a.mask) + base;
+              if (key < a.mask_keys) lo = mp[key];
+              if (key + 1 < a.mask_keys) hi = mp[key + 1];
+            } else {
+              const uint16_t *mp = reinterpret_cast<const uint16_t *>(a.mask) + base;
+              if (key < a.mask_keys) lo = mp[key];
+              if (key + 1 < a.mask_keys) hi = mp[key + 1];
+            }
+          }
+          mv[MK ? mt : 0][n][h] = lo | (hi << 16);
+        }
+  };
+  if constexpr (MK) {
+    if (ntiles > 0) load_mask(0, mcur);
+  }
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % NST;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (t / NST) & 1, flags))) {
+      aborted = true;
+      t_fail = t;
+      break;
+    }
+    const int kb = c0 + t * KT + 16 * warp;  // this warp's first key
+    if constexpr (MK) {
+      if (t + 1 < ntiles) load_mask(t + 1, mnext);
+    }
+    const uint32_t ks_u32 = smem_u32(stages + s * L::kStageBytes);
+    const uint32_t vs_u32 = ks_u32 + L::kTileBytes;
+
+    // ---- S = Q K^T over this warp's 16 keys
+    float sacc[MT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][n][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t kb0, kb1, kb2, kb3;
+      {
+        const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
+        const int kch = 2 * ks + ((lane >> 3) & 1);
+        ldsm_x4(ks_u32 + (kch >> 3) * (KT * 128) + sw128(krow, kch & 7), kb0, kb1, kb2, kb3);
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t af[4];
+        const int qrow = 16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int qch = 2 * ks + (lane >> 4);
+        ldsm_x4(qs_u32 + (qch >> 3) * (QROWS * 128) + sw128(qrow, qch & 7), af[0], af[1], af[2], af[3]);
+        M::run(sacc[mt][0], af, kb0, kb1);
+        M::run(sacc[mt][1], af, kb2, kb3);
+      }
+    }
+
+    // ---- scale, softcap, band mask (only on warps whose keys cross a frontier)
+    const bool edge = !(kb >= c0 && kb + 15 < c1 && (!a.causal || kb + 15 <= q_abs_min) &&
+                        (a.window < 0 || q_abs_max - kb < a.window));
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x = sacc[mt][n][e];
+          bool dropped = false;
+          if constexpr (MK) {
+            const uint32_t bits = (mcur[mt][n][e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+            if (a.mask_kind == 1) {
+              dropped = bits == 0;
+            } else {
+              T bv;
+              *reinterpret_cast<uint16_t *>(&bv) = (uint16_t)bits;
+              x = fmaf(to_f32(bv), a.mask_mul, x);  // the bias joins before the scale and softcap
+            }
+          }
+          x = a.cap_mul != 0.f ? tanh_fast(x * a.score_mul) * a.cap_mul : x * a.score_mul;
+          if (dropped) x = -INFINITY;
+          if (edge) {
+            const int row = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
+            const int key = kb + 8 * n + 2 * (lane & 3) + (e & 1);
+            const int qa = past + row / a.G;
+            const bool vis = row < R && key >= c0 && key < c1 && (!a.causal || key <= qa) &&
+                             (a.window < 0 || qa - key < a.window);
+            if (!vis) x = -INFINITY;
+          }
+          sacc[mt][n][e] = x;
+        }
+
+    // ---- online softmax, reference max moved lazily (rows lane/4 and lane/4 + 8)
+    uint32_t pa[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float p[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float mx = fmaxf(fmaxf(sacc[mt][0][2 * h], sacc[mt][0][2 * h + 1]),
+                         fmaxf(sacc[mt][1][2 * h], sacc[mt][1][2 * h + 1]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if (mx > m[mt][h] + kRescaleLog2 || (m[mt][h] == -INFINITY && mx != -INFINITY)) {
+          const float alpha = ex2(m[mt][h] - mx);  // 0 while nothing was visible
+          l[mt][h] *= alpha;
+#pragma unroll
+          for (int dn = 0; dn < D / 8; ++dn) {
+            acc[mt][dn][2 * h] *= alpha;
+            acc[mt][dn][2 * h + 1] *= alpha;
+          }
+          m[mt][h] = mx;
+        }
+        const float m_use = m[mt][h] == -INFINITY ? 0.f : m[mt][h];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float pv = ex2(sacc[mt][n][2 * h + e] - m_use);
+            p[n][2 * h + e] = pv;
+            l[mt][h] += pv;
+          }
+      }
+      pa[mt][0] = M::pack(p[0][0], p[0][1]);
+      pa[mt][1] = M::pack(p[0][2], p[0][3]);
+      pa[mt][2] = M::pack(p[1][0], p[1][1]);
+      pa[mt][3] = M::pack(p[1][2], p[1][3]);
+    }
+
+    // ---- stale V rows (slots >= total) may hold NaN/Inf: zero them so 0 * V stays 0
+    const bool stale = kb + 16 > total;
+    if (stale) {
+      const int first = max(0, total - kb);
+      for (int idx = lane; idx < (16 - first) * DCH; idx += 32) {
+        const int r = 16 * warp + first + idx / DCH, ch = idx % DCH;
+        *reinterpret_cast<uint4 *>(stages + s * L::kStageBytes + L::kTileBytes + (ch >> 3) * (KT * 128) +
+                                   sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+
+    // ---- O += P V over this warp's 16 keys
+#pragma unroll
+    for (int dd = 0; dd < D / 16; ++dd) {
+      uint32_t v0, v1, v2, v3;
+      const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
+      const int vch = 2 * dd + (lane >> 4);
+      ldsm_x4_t(vs_u32 + (vch >> 3) * (KT * 128) + sw128(vrow, vch & 7), v0, v1, v2, v3);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        M::run(acc[mt][2 * dd], pa[mt], v0, v1);
+        M::run(acc[mt][2 * dd + 1], pa[mt], v2, v3);
+      }
+    }
+    if (stale) fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    // warp 0 refills the stage once all four warps are done with it
+    if (warp == 0 && issued < ntiles) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], (t / NST) & 1, flags))) {
+        aborted = true;
+        t_fail = t + 1;
+        break;
+      }
+      issue(issued++);
+    }
+    if constexpr (MK) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          mcur[mt][n][0] = mnext[mt][n][0];
+          mcur[mt][n][1] = mnext[mt][n][1];
+        }
+    }
+  }
+
+  // -------------------------------------------------------------- merge the 4 warps
+  // per-warp row statistics (outside the stages: safe while aborted copies still land)
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float lv = l[mt][h];
+      lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+      lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+      if ((lane & 3) == 0) {
+        const int row = 16 * mt + (lane >> 2) + 8 * h;
+        red_m[warp * QROWS + row] = m[mt][h];
+        red_l[warp * QROWS + row] = lv;
+      }
+    }
+  // one decision for the whole CTA (a timed-out wait anywhere aborts it), taken by the
+  // barrier that publishes the statistics
+  aborted = __syncthreads_or(aborted || flags[0] != 0);
+  if (threadIdx.x == 0) grid_launch_dependents();  // streaming done: let the next kernel launch
+  if (aborted) {
+    // copies in flight must land before the CTA exits; take part in the ticket (or the
+    // cluster exchange, with no visible key) so the group stays consistent, write nothing
+    if (threadIdx.x == 0) {
+      volatile int no_abort = 0;
+      for (int t = t_fail; t < min(issued, t_fail + NST); ++t) mbar_wait(&full[t % NST], (t / NST) & 1, &no_abort);
+      report(a.status, GQA_DEV_TIMEOUT);
+      if (!CL && nchunks > 1) {
+        __threadfence();
+        const int old = atomicAdd(&a.tickets[bh], 1);
+        if (old == nchunks - 1) a.tickets[bh] = 0;
+      }
+    }
+    if constexpr (CL) {
+      if (nchunks == 1) return;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) m[mt][0] = m[mt][1] = -INFINITY;
+      for (int i = threadIdx.x; i < kWarps * QROWS; i += kThreads) red_m[i] = -INFINITY;
+      __syncthreads();  // uniform branch; thread 0 has drained the copies
+    } else {
+      return;
+    }
+  }
+  // cluster: this CTA's stages are free (nothing in flight), peers may write into them once
+  // every CTA has arrived
+  if (CL && nchunks > 1) cluster_arrive_relaxed();
+  if (threadIdx.x < QROWS) {
+    const int row = threadIdx.x;
+    float mm = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, red_m[w * QROWS + row]);
+    const float mu = mm == -INFINITY ? 0.f : mm;
+    float ll = 0.f;
+    for (int w = 0; w < kWarps; ++w) ll += red_l[w * QROWS + row] * ex2(red_m[w * QROWS + row] - mu);
+    row_m[row] = mm;
+    row_l[row] = ll;
+  }
+  __syncthreads();
+  // every warp writes its rescaled accumulator to its own region (the stages are free now),
+  // then all threads sum the four regions in a fixed order (deterministic)
+  constexpr int AST = L::kAccStride;
+  float *wacc = reinterpret_cast<float *>(stages);  // [kWarps][QROWS][AST]
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = 16 * mt + (lane >> 2) + 8 * h;
+      if (row >= R) continue;  // padding rows of the MMA tile are never read
+      const float mm = row_m[row];
+      const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
+      float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane & 3);
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn)
+        *reinterpret_cast<float2 *>(dst + 8 * dn) = make_float2(acc[mt][dn][2 * h] * f, acc[mt][dn][2 * h + 1] * f);
+    }
+  __syncthreads();
+  auto merged = [&](int idx4) {  // float4 idx4 of the CTA's [R][D] accumulator
+    const float4 *w4 = reinterpret_cast<const float4 *>(wacc) + (idx4 / (D / 4)) * (AST / 4) + idx4 % (D / 4);
+    float4 v = w4[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+      const float4 u = w4[w * (QROWS * AST / 4)];
+      v.x += u.x;
+      v.y += u.y;
+      v.z += u.z;
+      v.w += u.w;
+    }
+    return v;
+  };
+
+  if (nchunks == 1) {
+    // ------------------------------------------------------------ finish in place
+    for (int idx = threadIdx.x; idx < R * (D / 4); idx += kThreads) {
+      const int r = idx / (D / 4), d4 = idx % (D / 4);
+      const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
+      const float mm = row_m[r];
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 1.f;
+      if (mm != -INFINITY) {
+        float top = mm, sink_term = 0.f;
+        if (a.has_sink) {
+          const float z = sink_z[r];
+          top = fmaxf(mm, z);
+          sink_term = ex2(z - top);
+        }
+        const float f = ex2(mm - top);
+        num = merged(idx);
+        num.x *= f;
+        num.y *= f;
+        num.z *= f;
+        num.w *= f;
+        den = row_l[r] * f + sink_term;
+      }
+      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+      const float inv = __frcp_rn(den);
+      store4(o, num.x * inv, num.y * inv, num.z * inv, num.w * inv);
+    }
+    return;
+  }
+
+  if (CL) {
+    // ------------------------------------------------------------ cluster exchange
+    // the group's chunks are the CTAs of one cluster.  CTA `rank` owns float4 slice
+    // [rank * per, (rank + 1) * per) of the group's [R][D] output; every CTA pushes its
+    // (m, l) rows and the matching slice of its accumulator into the owner's shared memory
+    // (after the wacc regions) with asynchronous stores that count down the owner's xbar.
+    // The owner waits for exactly those bytes and combines its slice from local data; once
+    // they have landed nothing else writes to or reads from its shared memory, so it may exit
+    const int S = gridDim.x, rank = split;
+    const int n4 = R * (D / 4), per = (n4 + S - 1) / S;
+    float *rcv = wacc + kWarps * QROWS * AST;               // [S][per] float4 slices
+    float2 *rcv_ml = reinterpret_cast<float2 *>(rcv + QROWS * D + 4 * kMaxCluster);  // [S][QROWS] (m, l)
+    cluster_wait();  // every CTA has finished streaming: its stages may be written
+    const uint32_t rcv_s = smem_u32(rcv), rml_s = smem_u32(rcv_ml), xb_s = smem_u32(xbar);
+    for (int t = threadIdx.x; t < S * R; t += kThreads) {
+      const int k = t / R, r = t % R;
+      cluster_st_async2(cluster_map(rml_s + 8 * (rank * QROWS + r), k), row_m[r], row_l[r], cluster_map(xb_s, k));
+    }
+    for (int idx = threadIdx.x; idx < n4; idx += kThreads) {
+      const int dst = idx / per;
+      cluster_st_async4(cluster_map(rcv_s + 16 * (rank * per + idx - dst * per), dst), merged(idx),
+                        cluster_map(xb_s, dst));
+    }
+    const int lo4 = rank * per, hi4 = min(n4, lo4 + per);
+    if (threadIdx.x == 0) mbar_expect_tx(xbar, S * (max(0, hi4 - lo4) * 16 + R * 8));
+    if (!mbar_wait_cluster(xbar, 0)) {  // a peer never delivered: nothing valid to combine
+      if (threadIdx.x == 0) report(a.status, GQA_DEV_TIMEOUT);
+      return;
+    }
+    // each output float4 weighs the chunks of its row itself: no second pass, no barrier
+    const float4 *rcv4 = reinterpret_cast<const float4 *>(rcv);
+    for (int idx = lo4 + threadIdx.x; idx < hi4; idx += kThreads) {
+      const int r = idx / (D / 4), d4 = idx % (D / 4);
+      const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
+      float mk[kMaxCluster];
+      float top = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kMaxCluster; ++k) {
+        mk[k] = k < S ? rcv_ml[k * QROWS + r].x : -INFINITY;
+        top = fmaxf(top, mk[k]);
+      }
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 1.f;  // no visible key: the sums stay 0
+      if (top != -INFINITY) {
+        float ll = 0.f;
+        if (a.has_sink) {
+          const float z = sink_z[r];
+          top = fmaxf(top, z);
+          ll = ex2(z - top);
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxCluster; ++k) {
+          if (mk[k] == -INFINITY) continue;  // past the cluster, or a chunk without a visible key
+          const float f = ex2(mk[k] - top);
+          ll += rcv_ml[k * QROWS + r].y * f;
+          const float4 v = rcv4[k * per + idx - lo4];
+          sum.x += v.x * f;
+          sum.y += v.y * f;
+          sum.z += v.z * f;
+          sum.w += v.w * f;
+        }
+        den = ll;
+      }
+      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+      const float inv = __frcp_rn(den);
+      store4(o, sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
+    }
+    return;  // nothing reads this CTA's shared memory any more
+  }
+
+  // -------------------------------------------------------------- write the partial
+  const size_t gbase = (size_t)bh * a.splits * R;
+  {
+    const size_t base = gbase + (size_t)split * R;
+    float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * D);
+    for (int idx = threadIdx.x; idx < R * D / 4; idx += kThreads) pacc[idx] = merged(idx);
+    for (int r = threadIdx.x; r < R; r += kThreads)
+      reinterpret_cast<float2 *>(a.part_ml)[base + r] = make_float2(row_m[r], row_l[r]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(&a.tickets[bh], 1);
+    flags[1] = old == nchunks - 1;
+  }
+  __syncthreads();
+  if (!flags[1]) return;
+
+  // -------------------------------------------------------------- last CTA: combine
+  __threadfence();
+  if (threadIdx.x == 0) a.tickets[bh] = 0;
+  // chunk statistics staged in shared memory with all loads in flight at once
+  float *cm = reinterpret_cast<float *>(stages);  // [nchunks][R] max, then scale factor
+  float *cl = cm + a.splits * R;                    // [nchunks][R] sum
+  for (int idx = threadIdx.x; idx < nchunks * R; idx += kThreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + gbase + idx);
+    cm[idx] = ml.x;
+    cl[idx] = ml.y;
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < R; r += kThreads) {
+    float mm = -INFINITY;
+    for (int c = 0; c < nchunks; ++c) mm = fmaxf(mm, cm[c * R + r]);
+    float top = mm, sink_term = 0.f;
+    if (mm != -INFINITY && a.has_sink) {
+      const float z = sink_z[r];
+      top = fmaxf(mm, z);
+      sink_term = ex2(z - top);
+    }
+    float ll = sink_term;
+    for (int c = 0; c < nchunks; ++c) {
+      const float f = mm == -INFINITY ? 0.f : ex2(cm[c * R + r] - top);  // 0 for empty chunks
+      ll += cl[c * R + r] * f;
+      cm[c * R + r] = f;
+    }
+    row_l[r] = mm == -INFINITY ? 0.f : ll;
+  }
+  __syncthreads();
+  // chunk-outer: every thread keeps its outputs in registers and issues one independent
+  // load per output per chunk
+  constexpr int kPer = (MT * 16 * D / 4 + kThreads - 1) / kThreads;
+  float4 sum[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) sum[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 *pa4 = reinterpret_cast<const float4 *>(a.part_acc + gbase * D);
+#pragma unroll 4
+  for (int c = 0; c < nchunks; ++c) {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = threadIdx.x + u * kThreads;
+      if (idx < R * (D / 4)) {
+        const float f = cm[c * R + idx / (D / 4)];
+        const float4 v = __ldcg(pa4 + (size_t)c * R * (D / 4) + idx);
+        sum[u].x += v.x * f;
+        sum[u].y += v.y * f;
+        sum[u].z += v.z * f;
+        sum[u].w += v.w * f;
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = threadIdx.x + u * kThreads;
+    if (idx >= R * (D / 4)) continue;
+    const int r = idx / (D / 4), d4 = idx % (D / 4);
+    const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
+    const float den = row_l[r] > 0.f ? row_l[r] : 1.f;  // no visible key: the sums are 0
+    T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+    const float inv = __frcp_rn(den);
+    store4(o, sum[u].x * inv, sum[u].y * inv, sum[u].z * inv, sum[u].w * inv);
+  }
+}
+
+template <typename T, int D, int MT, int NST, bool CL, bool MK>
+gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
+  using L = Smem<D, MT, NST>;
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
+  CUtensorMap tk, tv;
+  // contiguous or ring: [B*Hkv][cap][D]; paged: [num_pages*Hkv][64][D]
+  const bool paged = c.block_table != nullptr;
+  const long long outer = paged ? (long long)c.num_pages * c.p.kv_heads : (long long)c.p.batch * c.p.kv_heads;
+  const int rows = paged ? KT : c.p.cap_present;
+  if (!encode_kv_tile_map(&tk, c.present_k, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_tile_map(&tv, c.present_v, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
+  auto kern = decode_split_kernel<T, D, MT, NST, CL, MK>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(dp.splits, c.p.kv_heads, c.p.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (CL) {  // the chunks of one group form one cluster
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = dp.splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+template <typename T, bool CL, bool MK> gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a);
+
+template <typename T, bool MK> gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
+  const gqa_params &p = c.p;
+  DecodeArgs a;
+  a.q = c.q_in;
+  a.k = c.k;
+  a.v = c.v;
+  a.cos = c.cos;
+  a.sin = c.sin;
+  a.present_k = c.present_k;
+  a.present_v = c.present_v;
+  a.out = c.out;
+  a.seqlens = c.seqlens;
+  a.head_sink = c.head_sink;
+  a.part_acc = reinterpret_cast<float *>(c.ws + wl.part_acc_off);
+  a.part_ml = reinterpret_cast<float *>(c.ws + wl.part_ml_off);
+  a.tickets = reinterpret_cast<int32_t *>(c.ws + wl.tickets_off);
+  a.status = c.status;
+  a.Hq = p.q_heads;
+  a.Hkv = p.kv_heads;
+  a.G = c.G;
+  a.curr = p.q_len;
+  a.R = dp.rows;
+  a.cap = p.cap_present;
+  a.ring = p.kv_ring;
+  a.table = c.block_table;
+  a.max_pages = c.max_pages;
+  a.num_pages = c.num_pages;
+  a.mask = c.mask;
+  a.mask_kind = c.mask_kind;
+  a.mask_keys = c.mask_keys;
+  a.msb = c.mask_sb;
+  a.msh = c.mask_sh;
+  a.msi = c.mask_si;
+  a.mask_mul = 1.f / p.scale;
+  a.cap_past = p.cap_past;
+  a.past_separate = c.past_separate;
+  a.rope_len = p.rope_len;
+  a.do_rotary = p.do_rotary;
+  a.append = c.append;
+  a.window = p.window;
+  a.causal = p.causal;
+  a.splits = dp.splits;
+  a.has_sink = (c.head_sink != nullptr) || p.smooth_softmax;
+  if (p.softcap > 0.f) {
+    a.score_mul = p.scale / p.softcap;
+    a.cap_mul = p.softcap * kLog2e;
+  } else {
+    a.score_mul = p.scale * kLog2e;
+    a.cap_mul = 0.f;
+  }
+  if (dp.cluster) return dispatch<T, true, MK>(c, dp, a);
+  return dispatch<T, false, MK>(c, dp, a);
+}
+
+template <typename T, bool CL, bool MK> gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
+  if (c.p.head_dim == 128) {
+    if (dp.mtiles == 1) return launch_cfg<T, 128, 1, 3, CL, MK>(c, dp, a);
+    if (dp.mtiles == 2) return launch_cfg<T, 128, 2, 3, CL, MK>(c, dp, a);
+  } else if (c.p.head_dim == 64) {
+    if (dp.mtiles == 1) return launch_cfg<T, 64, 1, 6, CL, MK>(c, dp, a);
+    if (dp.mtiles == 2) return launch_cfg<T, 64, 2, 6, CL, MK>(c, dp, a);
+    if (dp.mtiles == 3) return launch_cfg<T, 64, 3, 6, CL, MK>(c, dp, a);
+    if (dp.mtiles == 4) return launch_cfg<T, 64, 4, 6, CL, MK>(c, dp, a);
+  }
+  return GQA_ERR_UNSUPPORTED;
+}
+
+// The decode launch for one dtype switch; each .cu file instantiates one MK (masked or
+// not), so the two sets of kernels compile in parallel.
+template <bool MK> gqa_status launch_decode_split_any(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
+  switch (c.p.dtype) {
+    case GQA_F16: return launch_t<__half, MK>(c, dp, wl);
+    case GQA_BF16: return launch_t<__nv_bfloat16, MK>(c, dp, wl);
+  }
+  return GQA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace gqa

@@ -1,0 +1,12 @@
+// decode_split_masked.cu -- K3+K4 with a boolean or additive attention mask (the kernel
+// itself is in decode_split.cuh; a separate translation unit so both sets compile in
+// parallel).
+#include "decode_split.cuh"
+
+namespace gqa {
+
+gqa_status launch_decode_split_masked(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
+  return launch_decode_split_any<true>(c, dp, wl);
+}
+
+}  // namespace gqa

@@ -227,7 +227,8 @@ gqa_status make_call(Call &c, const gqa_params *p, const void *q, const void *k,
 gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const void *k, const void *v,
                          const void *past_k, const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
                          const void *sin_cache, const float *head_sink, void *out, void *present_k, void *present_v,
-                         void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+                         void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream,
+                         const gqa_mask *mask = nullptr) {
   Call c;
   gqa_status s = make_call(c, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink, out, present_k,
                            present_v, dev_status, stream);
@@ -239,6 +240,18 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   // the split decode kernel appends and rotates itself; every other path runs K1 first
   const bool fused = mode == kDecode && dp.eligible;
   if (p->kv_ring && !fused) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads a ring
+  if (mask) {
+    if (!fused) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel applies a mask
+    if (!mask->data || (mask->kind != GQA_MASK_KEEP && mask->kind != GQA_MASK_ADD)) return GQA_ERR_INVALID_ARG;
+    if (mask->kind == GQA_MASK_ADD && (reinterpret_cast<uintptr_t>(mask->data) & 1u)) return GQA_ERR_INVALID_ARG;
+    if (mask->keys < 1 || mask->stride_b < 0 || mask->stride_h < 0 || mask->stride_i < 0) return GQA_ERR_INVALID_ARG;
+    c.mask = mask->data;
+    c.mask_kind = mask->kind;
+    c.mask_keys = mask->keys;
+    c.mask_sb = mask->stride_b;
+    c.mask_sh = mask->stride_h;
+    c.mask_si = mask->stride_i;
+  }
   size_t need = fused ? (dp.splits > 1 && !dp.cluster ? wl.total : 0) : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
   if (need > 0) {
     if (!workspace || !aligned16(workspace)) return GQA_ERR_WORKSPACE;
@@ -251,7 +264,7 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
       s = launch_copy_past(c);
       if (s != GQA_OK) return s;
     }
-    return launch_decode_split(c, dp, wl);
+    return mask ? launch_decode_split_masked(c, dp, wl) : launch_decode_split(c, dp, wl);
   }
   if (c.append) {
     c.q_rot = rotate ? c.ws + wl.q_rot_off : nullptr;
@@ -289,6 +302,17 @@ gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *
                                 int32_t *dev_status, void *stream) {
   return gqa::run_attention(gqa::kDecode, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_attention_decode_masked(const gqa_params *p, const gqa_mask *mask, const void *q, const void *k,
+                                       const void *v, const void *past_k, const void *past_v,
+                                       const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                       const float *head_sink, void *out, void *present_k, void *present_v,
+                                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                       void *stream) {
+  if (!mask) return GQA_ERR_INVALID_ARG;
+  return gqa::run_attention(gqa::kDecode, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
+                            out, present_k, present_v, workspace, workspace_bytes, dev_status, stream, mask);
 }
 
 gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const void *k, const void *v,

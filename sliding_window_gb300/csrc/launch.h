@@ -31,6 +31,11 @@ struct Call {
   // (sequence, position / 64) to a page
   const int32_t *block_table = nullptr;
   int max_pages = 0, num_pages = 0;
+  // attention mask: element [b][hq][i][key] at b*mask_sb + hq*mask_sh + i*mask_si + key,
+  // kind 1 = uint8 keep flags, 2 = additive values of the dtype; keys < mask_keys
+  const void *mask = nullptr;
+  int mask_kind = 0, mask_keys = 0;
+  long long mask_sb = 0, mask_sh = 0, mask_si = 0;
   int32_t *status = nullptr;
   cudaStream_t stream = nullptr;
   char *ws = nullptr;
@@ -78,6 +83,7 @@ gqa_status launch_rope_append(const Call &c);
 gqa_status launch_copy_past(const Call &c);  // rows [0, past_b) of past into present only
 gqa_status launch_attention_simt(const Call &c);
 gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayout &wl);
+gqa_status launch_decode_split_masked(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_prefill_tc(const Call &c);
 
 }  // namespace gqa

@@ -50,6 +50,19 @@ def test_struct_layout_matches_header(g, tmp_path):
     assert vals[1:] == [getattr(g.GqaParams, f).offset for f, _ in g.GqaParams._fields_]
 
 
+def test_mask_struct_layout_matches_header(g, tmp_path):
+    src = tmp_path / "mask.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "gqa.h"\nint main(void){\n'
+                   'printf("%zu", sizeof(gqa_mask));\n'
+                   + "".join('printf(" %%zu", offsetof(gqa_mask, %s));\n' % f for f, _ in g.GqaMask._fields_)
+                   + "return 0;}\n")
+    exe = tmp_path / "mask"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    vals = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True).stdout.split()))
+    assert vals[0] == ctypes.sizeof(g.GqaMask)
+    assert vals[1:] == [getattr(g.GqaMask, f).offset for f, _ in g.GqaMask._fields_]
+
+
 def test_version_and_status_strings(g):
     assert g.gqa_abi_version() == 2
     for s in range(6):
@@ -143,6 +156,34 @@ def test_paged_rejects_ring_and_unsupported_shapes(g):
     assert call_paged(g, good_params(g, kv_ring=1, window=1000)) == 1
     assert call_paged(g, good_params(g, dtype="f32")) == 2          # only the split decode kernel reads pages
     assert call_paged(g, good_params(g, q_heads=64, q_len=2)) == 2  # 64 rows per group at D=128
+
+
+def call_masked(g, p, mask, **ptrs):
+    names = ["q", "k", "v", "past_k", "past_v", "seqlens_k", "cos", "sin", "head_sink", "out", "present_k",
+             "present_v", "workspace"]
+    vals = {n: FAKE for n in names}
+    vals.update(ptrs)
+    a = [ctypes.c_void_p(vals[n]) if vals[n] is not None else None for n in names]
+    m = ctypes.byref(mask) if mask is not None else None
+    return g.lib.gqa_attention_decode_masked(ctypes.byref(p), m, *a, 0, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(data=None), 1), (dict(kind=3), 1), (dict(keys=0), 1), (dict(stride_h=-1), 1),
+    (dict(data=FAKE + 1, kind=2), 1),                       # additive values must be 2-byte aligned
+])
+def test_masked_invalid_arguments(g, kw, code):
+    d = dict(data=FAKE, kind=1, keys=1024, stride_b=0, stride_h=0, stride_i=0)
+    d.update(kw)
+    m = g.GqaMask(d["data"], d["kind"], d["keys"], d["stride_b"], d["stride_h"], d["stride_i"])
+    assert call_masked(g, good_params(g), m) == code
+
+
+def test_masked_needs_a_mask_and_the_split_kernel(g):
+    m = g.GqaMask(FAKE, 1, 1024, 0, 0, 0)
+    assert call_masked(g, good_params(g), None) == 1
+    assert call_masked(g, good_params(g, dtype="f32"), m) == 2
+    assert call_masked(g, good_params(g, q_heads=64, q_len=2), m) == 2
 
 
 def test_attention_only_rejects_rotary(g):
