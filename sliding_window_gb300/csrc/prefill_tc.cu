@@ -144,6 +144,30 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Frontier tiles with a softcap: clear the packed P of the keys outside [lo_vis, hi_vis]
+// in this lane's 64 TMEM columns of P and return how many there were.  Kept out of line so
+// that the softmax loop around it compiles as without it.
+__device__ __noinline__ int clear_masked_p(uint32_t tP, int k0, int lo_vis, int hi_vis) {
+  int nm = 0;
+  tmem_st_wait();
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t pk[32];
+    tmem_ld32(tP + half * 32, pk);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+      const int key = k0 + half * 64 + e;
+      if (key < lo_vis || key > hi_vis) {
+        pk[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+        ++nm;
+      }
+    }
+    tmem_st32(tP + half * 32, pk);
+  }
+  return nm;
+}
+
 // mbarriers (indices into bars[])
 enum {
   B_Q = 0,
@@ -404,7 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tS + half * 32, pk);
       }
       const float2 rsf = f2_unpack(rs2);
-      const float rs = rsf.x + rsf.y;
+      float rs = rsf.x + rsf.y;
+      if (SOFTCAP && edge) {
+        // a masked key's -inf came out of tanh as -1, i.e. a score of -softcap: clear its P
+        // (the same value for every masked key of the row) in TMEM and take it out of the
+        // row sum, so that a masked key has exactly zero weight.  Frontier tiles only.
+        const int lo_vis = a.window > 0 ? qa - a.window + 1 : INT_MIN;
+        const int hi_vis = a.causal ? min(qa, total - 1) : total - 1;
+        const float pm = ex2(fmaf(-1.f, cmul, -m_use));
+        rs -= (float)clear_masked_p(tS, k0, lo_vis, hi_vis) * pm;
+      }
       l = l * alpha + rs;
       m_ref = m_new;
       if (__any_sync(0xffffffffu, need) && t > 0) {

@@ -89,3 +89,13 @@ def test_prefill_tc_sharp_scores(dtype, softcap):
     assert r["status"] == 0
     ref, *_ = oracle_ref(c)
     assert_close(out_rows(r["out"], c), ref, dtype, "sharp %s" % ((dtype, softcap),))
+
+
+@pytest.mark.parametrize("softcap", [0.5, 2.0])
+def test_prefill_tc_small_softcap_masks_exactly(softcap):
+    """With a small softcap every capped score is within [-softcap, softcap], so a key removed
+    by the band must get exactly zero weight, not the weight of a score of -softcap."""
+    c = prefill_case("bf16", 128, 2, 300, 70, "head", softcap, seed=11)
+    r = run_gpu(c, "prefill")
+    ref, *_ = oracle_ref(c)
+    assert_close(out_rows(r["out"], c), ref, "bf16", "softcap %g" % softcap)
