@@ -354,7 +354,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     elapsed = max_over_ranks(elapsed, world, device)
-    launches_per_step = 2 * w.layers  # append kernel + attention kernel per layer
+    launches_per_step = w.layers * kernels_per_layer(w)
 
     # the dominant kernel (attention) alone, same steps and buffers, live CUDA events
     for L in first.layers:
@@ -378,6 +378,16 @@ def run_ours(args, rank, world, local_rank):
     return dict(w=w, elapsed=elapsed, units=units, kunits=kunits, unit=unit, clocks=clocks, nsets=nsets,
                 per_set=per_set, k_elapsed=k_elapsed, e2e=e2e, launches=launches_per_step * args.steps,
                 seqs=first.seqlens())
+
+
+def kernels_per_layer(w) -> int:
+    """Kernel launches of one layer's call: the split-KV decode kernel appends and rotates
+    itself (one launch); every other path runs the RoPE/append kernel, then attention."""
+    rows = (w.q_heads // w.kv_heads) * w.q_len
+    mtiles = (rows + 15) // 16
+    fused = w.mode == "decode" and w.dtype != "f32" and (
+        (w.head_dim == 128 and mtiles <= 2) or (w.head_dim == 64 and mtiles <= 4))
+    return 1 if fused else 2
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
