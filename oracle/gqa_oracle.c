@@ -251,7 +251,9 @@ int32_t oracle_visible(int64_t q_abs, int64_t j, int64_t total, int32_t causal, 
  *   denominator and is sliced out);
  *   out = sum_j exp(s_j - M) v_j / (exp(z - M) [if sink] + sum_j exp(s_j - M)),
  *   M = max over the visible s_j and z;  a row with no visible slot gives zeros
- *   ([P4] "A fully masked query row produces zeros rather than NaN").
+ *   ([P4] "A fully masked query row produces zeros rather than NaN").  A score of -inf
+ *   (an additive mask value of -inf without a softcap) has weight exactly zero, so a row
+ *   whose scores are all -inf is fully masked and gives zeros too, not 0/0.
  * q is D doubles; k and v point at `n` rows of D elements of `dtype`.
  * ---------------------------------------------------------------------------------- */
 void oracle_attend_row_bias(const double *q, const void *k, const void *v, int64_t row0, int64_t n,
@@ -268,6 +270,7 @@ void oracle_attend_row_bias(const double *q, const void *k, const void *v, int64
     if (bias) sj += bias[j];
     if (softcap > 0.0) sj = softcap * tanh(sj / softcap);
     s[j] = sj;
+    if (sj == -INFINITY) continue;  /* an additive -inf removes the key: weight exp(-inf) = 0 */
     if (sj > M) M = sj;
     any = 1;
   }

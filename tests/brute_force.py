@@ -46,9 +46,11 @@ def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, cau
                         s = s + bias(b, hq, i, j)
                     if softcap > 0:
                         s = softcap * math.tanh(s / softcap)
+                    if s == -math.inf:
+                        continue   # exp(-inf) = 0: the key carries no weight
                     logits.append(s)
                     values.append(present_v[b][h][j])
-                if not keys:
+                if not values:
                     oi.append([0.0] * D)
                     continue
                 if sinks is not None:
@@ -56,8 +58,8 @@ def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, cau
                 m = max(logits)
                 e = [math.exp(x - m) for x in logits]
                 den = math.fsum(e)
-                p = [x / den for x in e][: len(keys)]   # ... and sliced out
-                oi.append([math.fsum(p[t] * values[t][d] for t in range(len(keys))) for d in range(D)])
+                p = [x / den for x in e][: len(values)]   # ... and sliced out
+                oi.append([math.fsum(p[t] * values[t][d] for t in range(len(values))) for d in range(D)])
             ob.append(oi)
         out.append(ob)
     return out

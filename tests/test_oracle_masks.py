@@ -88,3 +88,36 @@ def test_additive_constant_per_row_cancels_without_softcap():
     ref, *_ = run_oracle(c)
     const = np.full((2, 4, 2, 16), 3.25, np.float32)
     np.testing.assert_allclose(run_masked(c, const, "add"), ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_additive_minus_inf_equals_key_removal_without_softcap(dtype):
+    """0 / -inf additive values remove exactly the -inf keys, like a boolean mask; a row whose
+    keys all carry -inf is fully masked and gives zeros (with or without a sink)."""
+    for sink in (False, True):
+        c = tiny(B=2, Hq=4, Hkv=2, D=8, curr=3, cap=16, dtype=dtype, window=6, head_sink=sink, seed=8)
+        rng = np.random.default_rng(8)
+        keep = (rng.random((2, 4, 3, 16)) < 0.6).astype(np.uint8)
+        keep[1, 2, 1, :] = 0  # one row with every key removed
+        vals = np.where(keep != 0, 0.0, -np.inf)
+        add = oracle.encode(vals, dtype) if dtype != "f32" else vals.astype(np.float32)
+        out_add = run_masked(c, add, "add")
+        np.testing.assert_array_equal(out_add, run_masked(c, keep, "bool"))
+        assert np.all(out_add[1, 1, 2] == 0.0)
+        assert np.isfinite(out_add).all()
+
+
+def test_additive_minus_inf_under_softcap_is_the_capped_floor():
+    """With a softcap the bias joins before the cap, so -inf becomes the finite score -softcap
+    (tanh(-inf) = -1): the key keeps a small weight.  Brute force agrees."""
+    B, Hq, Hkv, D, curr, cap, softcap = 1, 2, 1, 8, 2, 10, 1.5
+    c = tiny(B, Hq, Hkv, D, curr, cap, "f32", np.array([6], np.int32), -1, 1, softcap, False, seed=9)
+    vals = np.zeros((1, 1, curr, cap))
+    vals[0, 0, :, ::2] = -np.inf
+    out = run_masked(c, vals.astype(np.float32), "add")
+    pk, pv = concat_present(c)
+    q = as_f64(c.q).reshape(B, curr, Hq, D)
+    want = brute_force.attention(nested(q), nested(pk), nested(pv), [6], B, Hq, Hkv, D, curr, -1, 1,
+                                 1.0 / math.sqrt(D), softcap, None, bias=lambda b, h, i, j: float(vals[0, 0, i, j]))
+    np.testing.assert_allclose(out, np.array(want), rtol=0, atol=1e-12)
+    assert np.isfinite(out).all()
