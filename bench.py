@@ -192,6 +192,9 @@ class Step:
             L = dict(c=c, p=p, p_attend=gqa.params_from_dict(dict(c.params, do_rotary=0)), ws=ws,
                      out=torch.empty_like(c.q), q_rot=torch.empty_like(c.q),
                      status=torch.zeros(1, dtype=torch.int32, device=device))
+            if w.mask:  # device-resident like the cache (a bias computed or reused on the device)
+                L["mask_t"] = c.extra["mask"]
+                L["mask"] = gqa.mask_from_tensor(L["mask_t"], gqa.MASK_ADD)
             if w.kv_paged:  # the same rows, moved into a shuffled pool of 64-position pages
                 B, Hkv, cap, D = c.past_k.shape
                 mp = cap // gqa.PAGE
@@ -206,6 +209,7 @@ class Step:
                 c.past_k = c.past_v = None
             self.layers.append(L)
         self.fn = gqa.gqa_attention_decode if w.mode == "decode" else gqa.gqa_attention_prefill
+        self.fn_masked = gqa.gqa_attention_decode_masked if w.mode == "decode" else gqa.gqa_attention_prefill_masked
         # all layers' outputs side by side, for one device->host copy per step
         self.out_all = torch.empty(sum(L["out"].numel() for L in self.layers), dtype=self.layers[0]["out"].dtype,
                                    device=device)
@@ -228,8 +232,8 @@ class Step:
                                                                L["pool_k"], L["pool_v"], L["ws"], L["status"],
                                                                stream), "paged step")
                 continue
-            self.g.check(self.fn(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin, c.head_sink,
-                                 L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "step")
+            self.g.check(self.call(L, L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin,
+                                   c.head_sink, L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "step")
 
     def append_only(self, stream):
         if self.w.kv_paged:  # the paged call appends itself: one full (untimed) step puts the rows in
@@ -252,14 +256,20 @@ class Step:
                                                                L["pool_k"], L["pool_v"], L["ws"], L["status"],
                                                                stream), "paged attend")
                 continue
-            self.g.check(self.fn(L["p_attend"], q, None, None, None, None, c.seqlens_k, None, None, c.head_sink,
-                                 L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "attend")
+            self.g.check(self.call(L, L["p_attend"], q, None, None, None, None, c.seqlens_k, None, None, c.head_sink,
+                                   L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "attend")
+
+    def call(self, L, p, *args):
+        """The layer's public call: the masked entry point when the workload has a mask."""
+        if "mask" in L:
+            return self.fn_masked(p, L["mask"], *args)
+        return self.fn(p, *args)
 
     def nbytes(self):
         tot = 0
         for L in self.layers:
             c = L["c"]
-            for t in (c.past_k, c.past_v, L.get("pool_k"), L.get("pool_v"), L["ws"], L["q_rot"]):
+            for t in (c.past_k, c.past_v, L.get("pool_k"), L.get("pool_v"), L.get("mask_t"), L["ws"], L["q_rot"]):
                 if t is None:
                     continue
                 tot += t.numel() * t.element_size()
@@ -530,7 +540,8 @@ class OracleSample:
                                     pk=_storage(c.past_k).copy(), pv=_storage(c.past_v).copy(), seq=seq,
                                     cos=None if c.cos is None else _storage(c.cos),
                                     sin=None if c.sin is None else _storage(c.sin),
-                                    sink=None if c.head_sink is None else c.head_sink.numpy(), rows=ridx))
+                                    sink=None if c.head_sink is None else c.head_sink.numpy(), rows=ridx,
+                                    mask=_storage(c.extra["mask"]) if "mask" in c.extra else None))
         self.units = units
         self.sample = desc + (" x %d layers" % self.w.layers if self.w.layers > 1 else "")
 
@@ -544,6 +555,9 @@ class OracleSample:
                 continue
             q_rot, pk, pv, _ = o.rope_append(L["p"], L["q"], L["k"], L["v"], L["pk"], L["pv"], L["seq"], L["cos"],
                                              L["sin"], present_k=L["pk"], present_v=L["pv"])
+            if L["mask"] is not None:
+                o.attention_masked(L["p"], q_rot, pk, pv, L["seq"], L["mask"], "add", L["sink"], rows=L["rows"])
+                continue
             o.attention(L["p"], q_rot, pk, pv, L["seq"], L["sink"], rows=L["rows"])
         return self.units
 
@@ -645,7 +659,8 @@ def report(args, w, r, world):
                    "layers": w.layers, "buffer_sets": r["nsets"], "bytes_per_set": r["per_set"],
                    "l2": "rotating buffer sets totalling > 3x L2 (inputs larger than L2)",
                    "tokens_per_s": round(w.batch * w.q_len * args.steps * world / r["elapsed"], 1),
-                   "peaks": src},
+                   "peaks": src, **({"mask": "additive bias [B, 1, S, cap] %s, device-resident" % w.dtype}
+                                    if w.mask else {})},
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": punit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_split" if w.mode == "decode" else ("prefill_tc" if w.dtype != "f32"

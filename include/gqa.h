@@ -87,7 +87,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 2
+#define GQA_ABI_VERSION 3
 
 typedef int32_t gqa_status;
 #define GQA_OK 0
@@ -228,15 +228,28 @@ typedef struct gqa_mask {
 } gqa_mask;
 
 /* Decode step with an attention mask: gqa_attention_decode's arguments and semantics plus
- * *mask (device data, host struct).  Runs the split-KV kernel only: f32 params, or shapes
- * outside its envelope, return GQA_ERR_UNSUPPORTED.  Ring caches (kv_ring) are allowed;
- * the mask stays indexed by absolute position. */
+ * *mask (device data, host struct).  Shapes inside the split-KV kernel's envelope run it
+ * (ring caches, kv_ring, are allowed there; the mask stays indexed by absolute position);
+ * f32 params and other shapes run the CUDA-core kernel (a ring then returns
+ * GQA_ERR_UNSUPPORTED).  An additive mask's data is aligned to its element size. */
 gqa_status gqa_attention_decode_masked(const gqa_params *p, const gqa_mask *mask, const void *q, const void *k,
                                        const void *v, const void *past_k, const void *past_v,
                                        const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
                                        const float *head_sink, void *out, void *present_k, void *present_v,
                                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                        void *stream);
+
+/* Prefill (or any step) with an attention mask: gqa_attention_prefill's arguments and
+ * semantics plus *mask, as for gqa_attention_decode_masked.  bf16/f16 with head_dim 64 or
+ * 128 and a mask whose data address and non-zero strides (in bytes) are multiples of 16
+ * run the tensor-core kernel, which stages the mask by TMA; any other mask, and f32, run
+ * the CUDA-core kernel (same results within the dtype's tolerance, slower). */
+gqa_status gqa_attention_prefill_masked(const gqa_params *p, const gqa_mask *mask, const void *q, const void *k,
+                                        const void *v, const void *past_k, const void *past_v,
+                                        const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                        const float *head_sink, void *out, void *present_k, void *present_v,
+                                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                        void *stream);
 
 /* Static description of a status code. */
 const char *gqa_status_string(gqa_status s);

@@ -6,6 +6,8 @@
 // keeps a running maximum, denominator and unnormalized output per query row while it
 // visits key blocks; frontiers skip blocks that no row of the block can see.
 // OpenVINO PR #37423, "Sliding window": a key is masked when q_abs - k_abs >= window.
+// onnx-light-cpu "Layouts and semantics": an optional boolean mask removes keys like the
+// band; an optional additive mask joins the scaled score before the softcap.
 // The sink logit (PR #37423, "smooth_softmax / head_sink") joins the denominator at the
 // end; a row with no visible key gives zeros ("Scheduling, precision, and invariants").
 #include <math.h>
@@ -27,6 +29,11 @@ struct SimtArgs {
   int32_t *status;
   int Hq, Hkv, G, D, curr, cap, cap_past, past_separate, rope_len, do_rotary, window, causal, has_sink;
   float scale, softcap;
+  // attention mask (kind 0: none, 1: uint8 keep flags, 2: additive values of T), element
+  // [b][hq][i][key] at b*msb + hq*msh + i*msi + key
+  const void *mask;
+  int mask_kind, mask_keys;
+  long long msb, msh, msi;
 };
 
 template <typename T>
@@ -42,7 +49,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   const int hk = hq / a.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int past = a.seqlens[b];
-  const int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
+  int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
+  if (a.mask_kind && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // mask too short
   T *out = reinterpret_cast<T *>(a.out);
   const int nrows = min(kRows, a.curr - i0);
   if (st) {
@@ -91,11 +99,14 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
       const int qa = past + i0 + r;
       const int j = kt + lane;
       bool vis = j < hi && (!a.causal || j <= qa) && (a.window < 0 || qa - j < a.window);
+      const long long mi = b * a.msb + hq * a.msh + (long long)(i0 + r) * a.msi + j;
+      if (vis && a.mask_kind == 1) vis = reinterpret_cast<const uint8_t *>(a.mask)[mi] != 0;
       float s = -INFINITY;
       if (vis) {
         float dot = 0.f;
         for (int d = 0; d < D; ++d) dot = fmaf(qs[r * D + d], ks[lane * (D + 1) + d], dot);
         s = dot * a.scale;
+        if (a.mask_kind == 2) s += to_f32(reinterpret_cast<const T *>(a.mask)[mi]);  // -inf: weight 0
         if (a.softcap > 0.f) s = a.softcap * tanhf(s / a.softcap);
       }
       float tmax = s;
@@ -169,6 +180,12 @@ template <typename T> gqa_status launch_t(const Call &c) {
   a.has_sink = (c.head_sink != nullptr) || p.smooth_softmax;
   a.scale = p.scale;
   a.softcap = p.softcap;
+  a.mask = c.mask;
+  a.mask_kind = c.mask ? c.mask_kind : 0;
+  a.mask_keys = c.mask_keys;
+  a.msb = c.mask_sb;
+  a.msh = c.mask_sh;
+  a.msi = c.mask_si;
   const int D = p.head_dim;
   size_t smem = sizeof(float) * (kRows * D + kKeys * (D + 1) + kKeys * D + 4 * kKeys);
   // D <= 128: at most 41.5 KB of shared memory, under the 48 KB default limit

@@ -114,6 +114,27 @@ bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B
   return r == CUDA_SUCCESS;
 }
 
+bool encode_mask_map(CUtensorMap *map, const void *base, int keys, int I, int H, int B, long long si_bytes,
+                     long long sh_bytes, long long sb_bytes, int box_keys, int box_rows, int esize) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  // a broadcast dimension (stride 0) becomes an extent of 1 read at coordinate 0, with the
+  // packed stride it would have had (never used)
+  const cuuint64_t row = ((cuuint64_t)keys * esize + 15) / 16 * 16;
+  cuuint64_t dims[4] = {(cuuint64_t)keys, (cuuint64_t)(si_bytes ? I : 1), (cuuint64_t)(sh_bytes ? H : 1),
+                        (cuuint64_t)(sb_bytes ? B : 1)};
+  cuuint64_t strides[3];
+  strides[0] = si_bytes ? (cuuint64_t)si_bytes : row;
+  strides[1] = sh_bytes ? (cuuint64_t)sh_bytes : strides[0] * dims[1];
+  strides[2] = sb_bytes ? (cuuint64_t)sb_bytes : strides[1] * dims[2];
+  cuuint32_t box[4] = {(cuuint32_t)box_keys, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                  const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 DecodePlan decode_plan(const gqa_params &p) {
   DecodePlan d;
   const int G = p.q_heads / p.kv_heads;
@@ -224,6 +245,16 @@ gqa_status make_call(Call &c, const gqa_params *p, const void *q, const void *k,
   return GQA_OK;
 }
 
+// The tensor-core prefill reads the mask by TMA: 16-byte aligned data and strides.  Other
+// masks go to the CUDA-core kernel.
+bool mask_tma_ok(const Call &c) {
+  const long long es = c.mask_kind == GQA_MASK_ADD ? 2 : 1;
+  const long long lim = 1ll << 39;
+  return (reinterpret_cast<uintptr_t>(c.mask) & 15u) == 0 && (c.mask_si * es) % 16 == 0 &&
+         (c.mask_sh * es) % 16 == 0 && (c.mask_sb * es) % 16 == 0 && c.mask_si * es < lim && c.mask_sh * es < lim &&
+         c.mask_sb * es < lim && (c.p.head_dim == 128 || c.p.head_dim == 64);
+}
+
 gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const void *k, const void *v,
                          const void *past_k, const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
                          const void *sin_cache, const float *head_sink, void *out, void *present_k, void *present_v,
@@ -241,9 +272,9 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   const bool fused = mode == kDecode && dp.eligible;
   if (p->kv_ring && !fused) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads a ring
   if (mask) {
-    if (!fused) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel applies a mask
     if (!mask->data || (mask->kind != GQA_MASK_KEEP && mask->kind != GQA_MASK_ADD)) return GQA_ERR_INVALID_ARG;
-    if (mask->kind == GQA_MASK_ADD && (reinterpret_cast<uintptr_t>(mask->data) & 1u)) return GQA_ERR_INVALID_ARG;
+    if (mask->kind == GQA_MASK_ADD && (reinterpret_cast<uintptr_t>(mask->data) & (c.esize - 1)))
+      return GQA_ERR_INVALID_ARG;
     if (mask->keys < 1 || mask->stride_b < 0 || mask->stride_h < 0 || mask->stride_i < 0) return GQA_ERR_INVALID_ARG;
     c.mask = mask->data;
     c.mask_kind = mask->kind;
@@ -273,6 +304,7 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
     if (rotate) c.q = c.q_rot;
   }
   if (mode == kDecode || p->dtype == GQA_F32) return launch_attention_simt(c);
+  if (mask) return mask_tma_ok(c) ? launch_prefill_tc_masked(c) : launch_attention_simt(c);
   return launch_prefill_tc(c);
 }
 
@@ -312,6 +344,17 @@ gqa_status gqa_attention_decode_masked(const gqa_params *p, const gqa_mask *mask
                                        void *stream) {
   if (!mask) return GQA_ERR_INVALID_ARG;
   return gqa::run_attention(gqa::kDecode, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
+                            out, present_k, present_v, workspace, workspace_bytes, dev_status, stream, mask);
+}
+
+gqa_status gqa_attention_prefill_masked(const gqa_params *p, const gqa_mask *mask, const void *q, const void *k,
+                                        const void *v, const void *past_k, const void *past_v,
+                                        const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                        const float *head_sink, void *out, void *present_k, void *present_v,
+                                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                        void *stream) {
+  if (!mask) return GQA_ERR_INVALID_ARG;
+  return gqa::run_attention(gqa::kPrefill, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream, mask);
 }
 

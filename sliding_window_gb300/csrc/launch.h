@@ -77,6 +77,11 @@ bool encode_kv_tile_map(CUtensorMap *map, const void *base, int D, int rows, lon
 // 4D map over q laid out [B, L, H, D]: box {64, 1, box_rows, 1}, 128B swizzle.
 bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B, int box_rows, int esize);
 
+// 4D map over an attention mask [B][H][I][keys] of 1- or 2-byte elements with byte strides
+// (0 = broadcast dimension): box {box_keys, box_rows, 1, 1}, 128B swizzle.
+bool encode_mask_map(CUtensorMap *map, const void *base, int keys, int I, int H, int B, long long si_bytes,
+                     long long sh_bytes, long long sb_bytes, int box_keys, int box_rows, int esize);
+
 int device_sm_count();
 
 gqa_status launch_rope_append(const Call &c);
@@ -85,5 +90,6 @@ gqa_status launch_attention_simt(const Call &c);
 gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_decode_split_masked(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_prefill_tc(const Call &c);
+gqa_status launch_prefill_tc_masked(const Call &c);  // c.mask set: kind 1 or 2
 
 }  // namespace gqa

@@ -1,0 +1,686 @@
+// prefill_tc.cuh -- K2: flash-attention forward on the 5th-generation tensor cores.
+//
+// onnx-light-cpu "Attention Kernel Design": streaming online softmax over KV blocks with
+// a running max, denominator and unnormalized output per row; causal/padding frontiers
+// skip whole blocks ("Compute paths"); fp32 accumulation, output narrowed once; a fully
+// masked row gives zeros ("Scheduling, precision, and invariants").  OpenVINO PR #37423:
+// window band in absolute positions ("Sliding window"); the sink joins the denominator
+// ("smooth_softmax / head_sink").  tract PR #2645 ("What changed"): bottom-right band.
+//
+// One CTA = one tile of 128 query rows of one (b, q head).  Roles (6 warps):
+//   warp 0  producer: TMA loads of the Q tile once, then one K and one V tile (128 keys,
+//           128B swizzle) per step, each into a single buffer released by tcgen05.commit
+//   warp 1  TMEM owner + MMA issuer (one thread): S = Q K^T (M=128, N=128, K=D) into TMEM,
+//           then O += P V with P read from TMEM (it overwrites S in place, bf16 pairs)
+//   warps 2-5  softmax: thread = one TMEM lane = one query row; tcgen05.ld of S, band mask
+//           on frontier tiles only, scale/softcap, exp2 online softmax with a lazily
+//           rescaled reference max, P back to TMEM with tcgen05.st, final O / l epilogue
+// Two CTAs share an SM (96 KB shared memory and 256 TMEM columns each), so one CTA's
+// softmax overlaps the other's MMAs.  KV tiles outside [window low, causal high] are never
+// visited; only tiles that cross a frontier evaluate the per-element predicate.
+// The sink starts the running state: m = z*log2(e), l = 1, so it is counted exactly once.
+//
+// With an attention mask (MK = 1 boolean keep flags, 2 additive values; onnx-light-cpu
+// "Layouts and semantics"), warp 2 streams the mask's [128 rows x 128 keys] tile of each
+// head into shared memory by TMA, one buffer per head released by that head's softmax; the
+// softmax applies it to S before the row maximum.  Key tiles then start on 16-key
+// boundaries (the TMA rule for the mask's inner coordinate); the extra keys lie outside the
+// band.  With an additive mask and D = 128 the K ring has one stage, to make room.
+#pragma once
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace gqa {
+namespace {
+
+constexpr int BM = 128;       // query rows per CTA (= TMEM lanes)
+constexpr int BN = 128;       // keys per tile
+constexpr int kThreads = 384; // 12 warps: producer, MMA, 2 spare, 2 softmax warpgroups
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by more than 2^8
+
+struct PrefillArgs {
+  void *out;
+  const int32_t *seqlens;
+  const float *head_sink;
+  int32_t *status;
+  int Hq, Hkv, G, curr, cap, cap_past, past_separate, rope_len, do_rotary, window, causal, has_sink;
+  float score_mul, cap_mul;  // as in the decode kernel
+  // attention mask (MK > 0): keys < mask_keys; a broadcast dimension reads coordinate 0
+  int mask_keys, mask_bcast_b, mask_bcast_h, mask_bcast_i;
+  float bias_mul;  // 1 / scale: an additive value joins the raw dot product before scaling
+};
+
+template <int D, int MK> struct PSmem {
+  static constexpr int kTile = BM * D * 2;  // one Q, K or V tile
+  static constexpr int kKStages = (MK == 2 && D == 128) ? 1 : 2;
+  static constexpr int kMaskTile = MK == 1 ? BM * BN : MK == 2 ? BM * BN * 2 : 0;  // one head's
+  static constexpr int kQA = 0;
+  static constexpr int kQB = kQA + kTile;
+  static constexpr int kK = kQB + kTile;
+  static constexpr int kV = kK + kKStages * kTile;  // two stages
+  static constexpr int kM = kV + 2 * kTile;         // mask tiles of heads A and B
+  static constexpr int kBar = kM + 2 * kMaskTile;
+  static constexpr int kTmemSlot = kBar + 24 * 8;
+  static constexpr int kFlag = kTmemSlot + 8;
+  static constexpr int kBytes = kFlag + 8;
+  // more than half of an SM's shared memory, so a CTA (512 TMEM columns) is always alone
+  // on its SM and can never sit blocked in tcgen05.alloc behind another one
+  static constexpr int kAlloc = (kBytes + 1024) > 116 * 1024 ? (kBytes + 1024) : 116 * 1024;
+  static constexpr uint32_t kTmemCols = 512;  // S_A, S_B (128 each), O_A, O_B (128 each)
+};
+
+// Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for sm_10x
+  d |= (uint64_t)2 << 61;  // 128B swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with fp32 accumulation.
+template <typename T> __host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                        // D format: f32
+         | ((DT<T>::code == GQA_BF16 ? 1u : 0u) << 7)     // A format: bf16 / f16
+         | ((DT<T>::code == GQA_BF16 ? 1u : 0u) << 10)    // B format
+         | ((b_mn_major ? 1u : 0u) << 16)                 // B major-ness
+         | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+#define GQA_REG32(r) \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), \
+      "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),   \
+      "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),  \
+      "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : GQA_REG32(r)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Frontier tiles with a softcap: clear the packed P of the keys outside [lo_vis, hi_vis]
+// in this lane's 64 TMEM columns of P and return how many there were.  Kept out of line so
+// that the softmax loop around it compiles as without it.
+__device__ __noinline__ int clear_masked_p(uint32_t tP, int k0, int lo_vis, int hi_vis) {
+  int nm = 0;
+  tmem_st_wait();
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t pk[32];
+    tmem_ld32(tP + half * 32, pk);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+      const int key = k0 + half * 64 + e;
+      if (key < lo_vis || key > hi_vis) {
+        pk[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+        ++nm;
+      }
+    }
+    tmem_st32(tP + half * 32, pk);
+  }
+  return nm;
+}
+
+// mbarriers (indices into bars[])
+enum {
+  B_Q = 0,
+  B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1,
+  B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,
+  B_SFULL_A, B_SFULL_B, B_PFULL_A, B_PFULL_B, B_OFULL_A, B_OFULL_B,
+  B_MFULL_A, B_MFULL_B, B_MEMPTY_A, B_MEMPTY_B,
+  B_COUNT
+};
+static_assert(B_COUNT <= 24, "barrier region");
+
+template <typename T, int D, bool SOFTCAP, int MK>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmm,
+                      PrefillArgs a) {
+  using L = PSmem<D, MK>;
+  constexpr int KST = L::kKStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kFlag);
+
+  // CTA = (pair of q heads of one kv group, q tile, batch); longest q tiles first
+  const int pairs_per_group = (a.G + 1) / 2;
+  const int hk = blockIdx.x / pairs_per_group;
+  const int hA = hk * a.G + 2 * (blockIdx.x % pairs_per_group);
+  const bool has_b = hA + 1 < (hk + 1) * a.G;
+  const int b = blockIdx.z;
+  const int qt = gridDim.y - 1 - blockIdx.y;
+  const int q0 = qt * BM;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int past = a.seqlens[b];
+  int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
+  if (MK && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // the mask must cover every key
+  T *out = reinterpret_cast<T *>(a.out);
+  const int nrows = min(BM, a.curr - q0);
+  if (st) {
+    if (threadIdx.x == 0 && qt == 0 && blockIdx.x == 0) report(a.status, st);
+    for (int idx = threadIdx.x; idx < (has_b ? 2 : 1) * nrows * D; idx += blockDim.x) {
+      const int hh = idx / (nrows * D), r = (idx / D) % nrows, d = idx % D;
+      out[(((size_t)b * a.curr + q0 + r) * a.Hq + hA + hh) * D + d] = from_f32<T>(0.f);
+    }
+    return;
+  }
+  const int total = past + a.curr;
+  const int qa_first = past + q0, qa_last = past + q0 + nrows - 1;
+  int klo = a.window > 0 ? max(0, qa_first - a.window + 1) : 0;
+  if (MK) klo &= ~15;  // the mask's TMA coordinate: a multiple of 16 bytes
+  const int khi = a.causal ? min(total, qa_last + 1) : total;
+  const int ntiles = (khi - klo + BN - 1) / BN;  // >= 1: every row sees itself
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(&bars[i], (i == B_PFULL_A || i == B_PFULL_B || i == B_MEMPTY_A || i == B_MEMPTY_B) ? 4 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [384,384+D); P_X overwrites
+  // the first 64 columns of S_X as packed pairs
+  int kissued = 0, vissued = 0;      // producer thread: TMA tiles issued
+  int missued[2] = {0, 0};           // mask producer thread: tiles issued per head
+  int s_commits = 0, o_commits = 0;  // MMA thread: last S and PV commit counts
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_expect_tx(&bars[B_Q], (has_b ? 2 : 1) * L::kTile);
+#pragma unroll
+      for (int db = 0; db < D / 64; ++db) {
+        tma_load_4d(smem + L::kQA + db * (BM * 128), &tmq, db * 64, hA, q0, b, &bars[B_Q]);
+        if (has_b) tma_load_4d(smem + L::kQB + db * (BM * 128), &tmq, db * 64, hA + 1, q0, b, &bars[B_Q]);
+      }
+      const int bh = b * a.Hkv + hk;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t & 1, k0 = klo + t * BN, sk = t % KST;
+        if (t >= KST && !mbar_wait(&bars[B_KEMPTY0 + sk], ((t / KST) - 1) & 1, abort_flag)) break;
+        mbar_expect_tx(&bars[B_KFULL0 + sk], L::kTile);
+#pragma unroll
+        for (int db = 0; db < D / 64; ++db)
+          tma_load_3d(smem + L::kK + sk * L::kTile + db * (BN * 128), &tmk, db * 64, k0, bh, &bars[B_KFULL0 + sk]);
+        ++kissued;
+        if (t >= 2 && !mbar_wait(&bars[B_VEMPTY0 + s], ((t >> 1) - 1) & 1, abort_flag)) break;
+        mbar_expect_tx(&bars[B_VFULL0 + s], L::kTile);
+#pragma unroll
+        for (int db = 0; db < D / 64; ++db)
+          tma_load_3d(smem + L::kV + s * L::kTile + db * (BN * 128), &tmv, db * 64, k0, bh, &bars[B_VFULL0 + s]);
+        ++vissued;
+      }
+    }
+  } else if (MK && warp == 2) {
+    // ---------------------------------------------------------------- mask producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmm);
+      const int mrows = a.mask_bcast_i ? 1 : BM;
+      const uint32_t bytes = (uint32_t)mrows * 128u * (MK == 2 ? 2u : 1u);
+      const int mb = a.mask_bcast_b ? 0 : b, mq = a.mask_bcast_i ? 0 : q0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int k0 = klo + t * BN;
+        bool fine = true;
+        for (int h = 0; h < (has_b ? 2 : 1); ++h) {
+          if (t >= 1 && !mbar_wait(&bars[B_MEMPTY_A + h], (t - 1) & 1, abort_flag)) {
+            fine = false;
+            break;
+          }
+          const int mh = a.mask_bcast_h ? 0 : hA + h;
+          uint8_t *dst = smem + L::kM + h * L::kMaskTile;
+          mbar_expect_tx(&bars[B_MFULL_A + h], bytes);
+          tma_load_4d(dst, &tmm, k0, mq, mh, mb, &bars[B_MFULL_A + h]);
+          if (MK == 2) tma_load_4d(dst + BM * 128, &tmm, k0 + 64, mq, mh, mb, &bars[B_MFULL_A + h]);
+          missued[h] = t + 1;
+        }
+        if (!fine) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    const uint32_t qa = smem_u32(smem + L::kQA), qb = smem_u32(smem + L::kQB);
+    const uint32_t kbase = smem_u32(smem + L::kK), vbase = smem_u32(smem + L::kV);
+    constexpr uint32_t id_s = idesc<T>(BM, BN, false);
+    constexpr uint32_t id_pv = idesc<T>(BM, D, true);
+    auto issue_s = [&](int t, uint32_t q_s, uint32_t d_tmem) {
+      const uint32_t ks = kbase + (t % KST) * L::kTile;
+#pragma unroll
+      for (int k16 = 0; k16 < D / 16; ++k16) {
+        const uint32_t off = (k16 >> 2) * (BM * 128) + (k16 & 3) * 32;
+        mma_ss(d_tmem, sdesc(q_s + off, 16, 1024), sdesc(ks + off, 16, 1024), id_s, k16 > 0);
+      }
+    };
+    auto issue_pv = [&](int t, uint32_t p_tmem, uint32_t o_tmem) {
+      const uint32_t vs = vbase + (t & 1) * L::kTile;
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts(o_tmem, p_tmem + kk * 8, sdesc(vs + kk * 2048, BN * 128, 1024), id_pv, (t > 0 || kk > 0) ? 1u : 0u);
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_Q], 0, abort_flag)) &&
+              __all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0], 0, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(0, qa, tmem + 0);
+        tc_commit(&bars[B_SFULL_A]);
+        if (has_b) {
+          issue_s(0, qb, tmem + 128);
+          tc_commit(&bars[B_SFULL_B]);
+        }
+        tc_commit(&bars[B_KEMPTY0]);
+      }
+      s_commits = 1;
+      __syncwarp();
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const int s = t & 1, k0 = klo + t * BN;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL0 + s], (t >> 1) & 1, abort_flag))) break;
+      if (k0 + BN > total) {  // stale slots may hold NaN/Inf: zero those V rows
+        const int first = max(0, total - k0);
+        uint8_t *vb = smem + L::kV + s * L::kTile;
+        for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
+          const int r = first + idx / (D / 8), ch = idx % (D / 8);
+          *reinterpret_cast<uint4 *>(vb + (ch >> 3) * (BN * 128) + sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_A], t & 1, abort_flag))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv(t, tmem + 0, tmem + 256);
+        tc_commit(&bars[B_OFULL_A]);
+      }
+      __syncwarp();
+      const bool next = t + 1 < ntiles;
+      if (next) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0 + (t + 1) % KST], ((t + 1) / KST) & 1, abort_flag)))
+          break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_s(t + 1, qa, tmem + 0);
+          tc_commit(&bars[B_SFULL_A]);
+        }
+        __syncwarp();
+      }
+      if (has_b) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_B], t & 1, abort_flag))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv(t, tmem + 128, tmem + 384);
+          tc_commit(&bars[B_OFULL_B]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) tc_commit(&bars[B_VEMPTY0 + s]);
+      o_commits = t + 1;
+      if (next) {
+        if (lane == 0) {
+          if (has_b) {
+            issue_s(t + 1, qb, tmem + 128);
+            tc_commit(&bars[B_SFULL_B]);
+          }
+          tc_commit(&bars[B_KEMPTY0 + (t + 1) % KST]);
+        }
+        s_commits = t + 2;
+        __syncwarp();
+      }
+    }
+  } else if (warp >= 4 && (warp < 8 || has_b)) {
+    // ---------------------------------------------------------------- softmax warpgroups
+    const int wg = (warp - 4) >> 2;  // 0: head A, 1: head B
+    const int hq = hA + wg;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // TMEM lane = query row within the tile
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + wg * 128;
+    const uint32_t tO = tmem + lane_off + 256 + wg * 128;
+    uint64_t *sfull = &bars[B_SFULL_A + wg], *pfull = &bars[B_PFULL_A + wg], *ofull = &bars[B_OFULL_A + wg];
+    const int qa = past + q0 + row;
+    const float z2 = a.has_sink ? (a.head_sink ? a.head_sink[hq] : 0.f) * kLog2e : 0.f;
+    const float smul = a.score_mul, cmul = a.cap_mul;
+    float m_ref = a.has_sink ? z2 : -INFINITY;  // reference max (log2 domain)
+    float l = a.has_sink ? 1.f : 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int k0 = klo + t * BN;
+      const bool edge = !(k0 + BN - 1 < total && (!a.causal || k0 + BN - 1 <= qa_first) &&
+                          (a.window < 0 || qa_last - k0 < a.window));
+      if (!__all_sync(0xffffffffu, mbar_wait(sfull, t & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[BN];
+      {
+        uint32_t(&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+        uint32_t(&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+        uint32_t(&r2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[64]);
+        uint32_t(&r3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[96]);
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_ld_wait();
+      }
+      if constexpr (MK != 0) {
+        // this row's mask values for keys [k0, k0 + 128), 16-byte chunks of the 128B-swizzled
+        // tile (row-broadcast masks hold one row)
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_MFULL_A + wg], t & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const int mr = a.mask_bcast_i ? 0 : row;
+        const uint8_t *mrow = smem + L::kM + wg * L::kMaskTile + mr * 128;
+        if constexpr (MK == 1) {
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(mrow + ((ch ^ (mr & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (((w[e >> 2] >> (8 * (e & 3))) & 0xFFu) == 0u) r[ch * 16 + e] = __float_as_uint(-INFINITY);
+          }
+        } else {
+          const float bm = a.bias_mul;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 v = *reinterpret_cast<const uint4 *>(mrow + hf * (BM * 128) + ((ch ^ (mr & 7)) << 4));
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                T bv;
+                *reinterpret_cast<uint16_t *>(&bv) = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+                float x = fmaf(to_f32(bv), bm, __uint_as_float(r[hf * 64 + ch * 8 + e]));
+                // under a softcap an additive -inf is the finite score -softcap (tanh(-inf) = -1),
+                // so keep it finite here; -inf stays reserved for removed keys
+                if (SOFTCAP) x = fmaxf(x, -FLT_MAX);
+                r[hf * 64 + ch * 8 + e] = __float_as_uint(x);
+              }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_MEMPTY_A + wg]);
+      }
+      if (edge) {  // band predicate on frontier tiles only
+        const int lo_vis = a.window > 0 ? qa - a.window + 1 : INT_MIN;
+        const int hi_vis = a.causal ? min(qa, total - 1) : total - 1;
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const int key = k0 + e;
+          if (key < lo_vis || key > hi_vis) r[e] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BN; e += 2) mx = fmax3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+      float m_tile = -INFINITY;
+      if (mx != -INFINITY) m_tile = SOFTCAP ? tanh_fast(mx * smul) * cmul : mx * smul;
+      // lazy rescale: move the reference max only when it grows by more than 2^8
+      const bool need = m_tile > m_ref + kRescaleLog2 || (m_ref == -INFINITY && m_tile != -INFINITY);
+      const float m_new = need ? m_tile : m_ref;
+      const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      // P = 2^(x - m) in two halves (keeps register pressure down), packed to the dtype and
+      // stored over the first columns of S; elementwise math two lanes per instruction
+      uint64_t rs2 = 0;  // (0.f, 0.f)
+      const uint64_t smul2 = f2_pack(smul, smul), cmul2 = f2_pack(cmul, cmul), negm2 = f2_pack(-m_use, -m_use);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const uint64_t sv = f2_pack(__uint_as_float(r[half * 64 + e]), __uint_as_float(r[half * 64 + e + 1]));
+          uint64_t x;
+          if (SOFTCAP) {
+            const float2 y = f2_unpack(f2_mul(sv, smul2));
+            x = f2_fma(f2_pack(tanh_fast(y.x), tanh_fast(y.y)), cmul2, negm2);
+          } else {
+            x = f2_fma(sv, smul2, negm2);
+          }
+          const float2 xf = f2_unpack(x);
+          float p0 = ex2(xf.x), p1 = ex2(xf.y);
+          if (MK != 0 && SOFTCAP) {  // removed keys (band or mask) have weight exactly zero
+            if (r[half * 64 + e] == __float_as_uint(-INFINITY)) p0 = 0.f;
+            if (r[half * 64 + e + 1] == __float_as_uint(-INFINITY)) p1 = 0.f;
+          }
+          rs2 = f2_add(rs2, f2_pack(p0, p1));
+          pk[e >> 1] = pack2<T>(p0, p1);
+        }
+        tmem_st32(tS + half * 32, pk);
+      }
+      const float2 rsf = f2_unpack(rs2);
+      float rs = rsf.x + rsf.y;
+      if (MK == 0 && SOFTCAP && edge) {
+        // a masked key's -inf came out of tanh as -1, i.e. a score of -softcap: clear its P
+        // (the same value for every masked key of the row) in TMEM and take it out of the
+        // row sum, so that a masked key has exactly zero weight.  Frontier tiles only.
+        const int lo_vis = a.window > 0 ? qa - a.window + 1 : INT_MIN;
+        const int hi_vis = a.causal ? min(qa, total - 1) : total - 1;
+        const float pm = ex2(fmaf(-1.f, cmul, -m_use));
+        rs -= (float)clear_masked_p(tS, k0, lo_vis, hi_vis) * pm;
+      }
+      l = l * alpha + rs;
+      m_ref = m_new;
+      if (__any_sync(0xffffffffu, need) && t > 0) {
+        // O holds PV of tiles < t: wait for the last of them, then scale it in TMEM
+        if (!__all_sync(0xffffffffu, mbar_wait(ofull, (t - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull);
+    }
+    // epilogue: out = O / l
+    const bool fin = ok && !*abort_flag && mbar_wait(ofull, (ntiles - 1) & 1, abort_flag);
+    if (__all_sync(0xffffffffu, fin)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T *orow = out + (((size_t)b * a.curr + q0 + row) * a.Hq + hq) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait();
+        if (row < nrows) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = pack2<T>(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+            v.y = pack2<T>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            v.z = pack2<T>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            v.w = pack2<T>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + c * 32 + e) = v;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait timed out somewhere.  Copies and MMAs already issued must land before the
+    // CTA exits and before its TMEM is freed; these waits are bounded too.
+    volatile int no_abort = 0;
+    if (warp == 0 && lane == 0) {
+      mbar_wait(&bars[B_Q], 0, &no_abort);
+      for (int t = max(0, kissued - KST); t < kissued; ++t)
+        mbar_wait(&bars[B_KFULL0 + t % KST], (t / KST) & 1, &no_abort);
+      for (int t = max(0, vissued - 2); t < vissued; ++t) mbar_wait(&bars[B_VFULL0 + (t & 1)], (t >> 1) & 1, &no_abort);
+      report(a.status, GQA_DEV_TIMEOUT);
+    }
+    if (MK && warp == 2 && lane == 0) {
+      for (int h = 0; h < 2; ++h)
+        if (missued[h]) mbar_wait(&bars[B_MFULL_A + h], (missued[h] - 1) & 1, &no_abort);
+    }
+    if (warp == 1 && lane == 0) {
+      if (s_commits) mbar_wait(&bars[B_SFULL_A], (s_commits - 1) & 1, &no_abort);
+      if (o_commits) mbar_wait(&bars[B_OFULL_A], (o_commits - 1) & 1, &no_abort);
+      if (has_b && o_commits) mbar_wait(&bars[B_OFULL_B], (o_commits - 1) & 1, &no_abort);
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <typename T, int D, bool SC, int MK> gqa_status launch_cfg(const Call &c, const PrefillArgs &a) {
+  using L = PSmem<D, MK>;
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory per CTA");
+  const gqa_params &p = c.p;
+  CUtensorMap tq, tk, tv, tm;
+  const long long outer = (long long)p.batch * p.kv_heads;
+  if (!encode_q_map(&tq, c.q, D, p.q_heads, p.q_len, p.batch, BM, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_map(&tk, c.present_k, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_map(&tv, c.present_v, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
+  if (MK) {
+    const int es = MK == 2 ? 2 : 1;
+    if (!encode_mask_map(&tm, c.mask, c.mask_keys, p.q_len, p.q_heads, p.batch, c.mask_si * es, c.mask_sh * es,
+                         c.mask_sb * es, 128 / es, c.mask_si == 0 ? 1 : BM, es))
+      return GQA_ERR_CUDA;
+  } else {
+    tm = tq;  // unused
+  }
+  auto kern = prefill_tc_kernel<T, D, SC, MK>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  const int pairs = p.kv_heads * ((c.G + 1) / 2);
+  dim3 grid(pairs, (p.q_len + BM - 1) / BM, p.batch);
+  kern<<<grid, kThreads, L::kAlloc, c.stream>>>(tq, tk, tv, tm, a);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+template <typename T, int MK> gqa_status launch_t(const Call &c) {
+  const gqa_params &p = c.p;
+  PrefillArgs a;
+  a.out = c.out;
+  a.seqlens = c.seqlens;
+  a.head_sink = c.head_sink;
+  a.status = c.status;
+  a.Hq = p.q_heads;
+  a.Hkv = p.kv_heads;
+  a.G = c.G;
+  a.curr = p.q_len;
+  a.cap = p.cap_present;
+  a.cap_past = p.cap_past;
+  a.past_separate = c.past_separate;
+  a.rope_len = p.rope_len;
+  a.do_rotary = c.append ? p.do_rotary : 0;
+  a.window = p.window;
+  a.causal = p.causal;
+  a.has_sink = (c.head_sink != nullptr) || p.smooth_softmax;
+  a.mask_keys = c.mask_keys;
+  a.mask_bcast_b = c.mask_sb == 0;
+  a.mask_bcast_h = c.mask_sh == 0;
+  a.mask_bcast_i = c.mask_si == 0;
+  a.bias_mul = 1.f / p.scale;
+  const bool sc = p.softcap > 0.f;
+  if (sc) {
+    a.score_mul = p.scale / p.softcap;
+    a.cap_mul = p.softcap * kLog2e;
+  } else {
+    a.score_mul = p.scale * kLog2e;
+    a.cap_mul = 0.f;
+  }
+  if (p.head_dim == 128) return sc ? launch_cfg<T, 128, true, MK>(c, a) : launch_cfg<T, 128, false, MK>(c, a);
+  if (p.head_dim == 64) return sc ? launch_cfg<T, 64, true, MK>(c, a) : launch_cfg<T, 64, false, MK>(c, a);
+  return GQA_ERR_UNSUPPORTED;
+}
+
+template <int MK> gqa_status launch_prefill_tc_any(const Call &c) {
+  switch (c.p.dtype) {
+    case GQA_F16: return launch_t<__half, MK>(c);
+    case GQA_BF16: return launch_t<__nv_bfloat16, MK>(c);
+  }
+  return GQA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace gqa

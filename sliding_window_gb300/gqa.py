@@ -33,7 +33,7 @@ TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decode", "gqa_rope_append_kv",
             "gqa_status_string", "gqa_abi_version", "gqa_attention_decode_noalloc", "gqa_attention_decode_paged",
-            "gqa_attention_decode_masked"]
+            "gqa_attention_decode_masked", "gqa_attention_prefill_masked"]
 MASK_KEEP, MASK_ADD = 1, 2
 PAGE = 64  # positions per page of a paged cache
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES
@@ -56,9 +56,12 @@ class GqaMask(ctypes.Structure):
 def mask_from_tensor(m, kind: int) -> GqaMask:
     """A gqa_mask for a CUDA tensor of 4 dims [B or 1, Hq or 1, q_len or 1, keys] (size-1
     dims broadcast; the key dim contiguous).  kind MASK_KEEP: uint8/bool; MASK_ADD: the dtype."""
-    assert m.dim() == 4 and m.stride(3) == 1
-    st = [0 if m.shape[d] == 1 else m.stride(d) for d in range(3)]
-    return GqaMask(_ptr(m), kind, m.shape[3], st[0], st[1], st[2])
+    if m.dim() != 4 or m.stride(3) != 1:
+        raise ValueError("a mask is a 4-dim tensor with contiguous keys")
+    if not m.is_cuda:
+        raise ValueError("libgqa takes device tensors; got a mask on %s" % m.device)
+    st = [0 if m.shape[d] == 1 else m.stride(d) for d in range(3)]  # any other strides are explicit
+    return GqaMask(m.data_ptr(), kind, m.shape[3], st[0], st[1], st[2])
 
 
 class GqaError(RuntimeError):
@@ -88,6 +91,8 @@ def _load():
     lib.gqa_attention_decode_paged.restype = i32
     lib.gqa_attention_decode_masked.argtypes = [pp, ctypes.POINTER(GqaMask)] + [vp] * 13 + [sz, vp, vp]
     lib.gqa_attention_decode_masked.restype = i32
+    lib.gqa_attention_prefill_masked.argtypes = [pp, ctypes.POINTER(GqaMask)] + [vp] * 13 + [sz, vp, vp]
+    lib.gqa_attention_prefill_masked.restype = i32
     lib.gqa_status_string.argtypes = [i32]
     lib.gqa_status_string.restype = ctypes.c_char_p
     lib.gqa_abi_version.argtypes = []
@@ -179,6 +184,16 @@ def gqa_attention_decode_masked(p, mask: "GqaMask", q, k, v, past_k, past_v, seq
                                                _ptr(sin_cache), _ptr(head_sink), _ptr(out), _ptr(present_k),
                                                _ptr(present_v), _ptr(workspace), _nbytes(workspace),
                                                _ptr(dev_status), _stream(stream)))
+
+
+def gqa_attention_prefill_masked(p, mask: "GqaMask", q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache,
+                                 head_sink, out, present_k, present_v, workspace, dev_status, stream=None) -> int:
+    """Prefill (or any step) with a boolean or additive attention mask (see include/gqa.h)."""
+    return int(lib.gqa_attention_prefill_masked(ctypes.byref(p), ctypes.byref(mask), _ptr(q), _ptr(k), _ptr(v),
+                                                _ptr(past_k), _ptr(past_v), _ptr(seqlens_k), _ptr(cos_cache),
+                                                _ptr(sin_cache), _ptr(head_sink), _ptr(out), _ptr(present_k),
+                                                _ptr(present_v), _ptr(workspace), _nbytes(workspace),
+                                                _ptr(dev_status), _stream(stream)))
 
 
 def gqa_attention_decode_paged(p, q, k, v, seqlens_k, block_table, num_pages, cos_cache, sin_cache, head_sink, out,

@@ -48,6 +48,7 @@ class Workload:
     garbage_std: float = 10.0
     kv_ring: int = 0        # 1: the cache is a ring of `cap` slots, position p in slot p % cap
     kv_paged: int = 0       # 1: the cache is a shared pool of 64-position pages behind a block table
+    mask: str = ""          # "add": an additive attention bias [B, 1, S, cap] of the dtype, N(0,1)
 
     @property
     def layers(self) -> int:
@@ -87,6 +88,9 @@ WORKLOADS = {
         # the windowed decode over a paged cache: the same rows in a shuffled pool of pages
         Workload("decode_window_paged_bf16", 6, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
                  windows=(1024,), kv_paged=1),
+        # the long prompt with a dense additive attention bias, broadcast over the heads
+        Workload("prefill_bias_bf16", 7, "prefill", "bf16", 2, 64, 8, 128, 8192, 8192, 0, 0,
+                 windows=(4096,), softcap=50.0, head_sink=True, mask="add"),
     ]
 }
 
@@ -184,8 +188,18 @@ def make_case(w: Workload, layer: int = 0, device="cpu", seed_offset: int = 0, g
     sink = None
     if w.head_sink:
         sink = torch.randn(Hq, generator=gen, device=dev, dtype=torch.float32)
+    extra = {}
+    if w.mask == "add":  # its own stream: the other inputs match the unmasked workload's draw
+        mg = torch.Generator(device=dev)
+        mg.manual_seed(6000 + w.index + 104729 * layer + 7919 * seed_offset)
+        m = torch.empty(B, 1, L, cap, dtype=t, device=dev)
+        for b in range(B):
+            m[b].copy_(torch.randn(1, L, cap, generator=mg, device=dev, dtype=torch.float32))
+        extra["mask"] = m
+    elif w.mask:
+        raise ValueError(w.mask)
     return Case(w, layer, w.params(layer), q, k, v, past_k, past_v,
-                torch.from_numpy(seq).to(dev), cos, sin, sink)
+                torch.from_numpy(seq).to(dev), cos, sin, sink, extra)
 
 
 def small_variant(w: Workload, **kw) -> Workload:

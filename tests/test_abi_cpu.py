@@ -64,7 +64,7 @@ def test_mask_struct_layout_matches_header(g, tmp_path):
 
 
 def test_version_and_status_strings(g):
-    assert g.gqa_abi_version() == 2
+    assert g.gqa_abi_version() == 3
     for s in range(6):
         assert g.gqa_status_string(s) and g.gqa_status_string(s) != "unknown status"
     assert g.gqa_status_string(99) == "unknown status"
@@ -158,32 +158,38 @@ def test_paged_rejects_ring_and_unsupported_shapes(g):
     assert call_paged(g, good_params(g, q_heads=64, q_len=2)) == 2  # 64 rows per group at D=128
 
 
-def call_masked(g, p, mask, **ptrs):
+def call_masked(g, p, mask, fn="gqa_attention_decode_masked", **ptrs):
     names = ["q", "k", "v", "past_k", "past_v", "seqlens_k", "cos", "sin", "head_sink", "out", "present_k",
              "present_v", "workspace"]
     vals = {n: FAKE for n in names}
     vals.update(ptrs)
     a = [ctypes.c_void_p(vals[n]) if vals[n] is not None else None for n in names]
     m = ctypes.byref(mask) if mask is not None else None
-    return g.lib.gqa_attention_decode_masked(ctypes.byref(p), m, *a, 0, None, None)
+    return getattr(g.lib, fn)(ctypes.byref(p), m, *a, 0, None, None)
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(data=None), 1), (dict(kind=3), 1), (dict(keys=0), 1), (dict(stride_h=-1), 1),
     (dict(data=FAKE + 1, kind=2), 1),                       # additive values must be 2-byte aligned
 ])
-def test_masked_invalid_arguments(g, kw, code):
+@pytest.mark.parametrize("fn", ["gqa_attention_decode_masked", "gqa_attention_prefill_masked"])
+def test_masked_invalid_arguments(g, kw, code, fn):
     d = dict(data=FAKE, kind=1, keys=1024, stride_b=0, stride_h=0, stride_i=0)
     d.update(kw)
     m = g.GqaMask(d["data"], d["kind"], d["keys"], d["stride_b"], d["stride_h"], d["stride_i"])
-    assert call_masked(g, good_params(g), m) == code
+    assert call_masked(g, good_params(g), m, fn) == code
 
 
-def test_masked_needs_a_mask_and_the_split_kernel(g):
+@pytest.mark.parametrize("fn", ["gqa_attention_decode_masked", "gqa_attention_prefill_masked"])
+def test_masked_argument_rules(g, fn):
     m = g.GqaMask(FAKE, 1, 1024, 0, 0, 0)
-    assert call_masked(g, good_params(g), None) == 1
-    assert call_masked(g, good_params(g, dtype="f32"), m) == 2
-    assert call_masked(g, good_params(g, q_heads=64, q_len=2), m) == 2
+    assert call_masked(g, good_params(g), None, fn) == 1
+    # f32 additive values are aligned to 4 bytes
+    assert call_masked(g, good_params(g, dtype="f32"), g.GqaMask(FAKE + 2, 2, 1024, 0, 0, 0), fn) == 1
+    # a ring is read by the split decode kernel only: f32, large groups and prefill reject it
+    ring = dict(kv_ring=1, window=1000, cap_present=1024)
+    assert call_masked(g, good_params(g, dtype="f32", **ring), m, fn) == 2
+    assert call_masked(g, good_params(g, q_heads=64, q_len=2, **ring), m, fn) == 2
 
 
 def test_attention_only_rejects_rotary(g):

@@ -1,4 +1,4 @@
-"""The five named workloads (and the ring-cache variant of the windowed decode) at full size, in the launch configuration bench.py times,
+"""The five named workloads (and the ring, paged and attention-bias variants) at full size, in the launch configuration bench.py times,
 checked against the fp64 oracle: every row for the tiny fp32 prompt, sampled rows (with the
 band edges) for the large ones, and the appended present rows bit for bit."""
 import numpy as np
@@ -126,3 +126,32 @@ def test_decode_window_paged_bf16():
     np.testing.assert_array_equal(storage(dev[1]), pv)
     ref = oracle.attention_paged(c.params, q_rot, pk, pv, c.seqlens_k.numpy(), table, B * mp)
     assert_close(out_rows(out, c), ref, w.dtype, w.name)
+
+
+def test_prefill_bias_bf16():
+    """The long prompt with a dense additive bias [B, 1, S, S] through the masked prefill
+    entry point (TMA-staged mask): sampled rows (band edges included) against the masked
+    oracle, the appended rows bit for bit."""
+    from sliding_window_gb300 import gqa
+    w = WORKLOADS["prefill_bias_bf16"]
+    c = make_case(w, device="cuda:0")
+    host = make_host(c)
+    mask_host = storage(c.extra["mask"])
+    p = gqa.params_from_dict(c.params)
+    out = torch.full_like(c.q, float("nan"))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device="cuda")
+    m = gqa.mask_from_tensor(c.extra["mask"], gqa.MASK_ADD)
+    gqa.check(gqa.gqa_attention_prefill_masked(p, m, c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin,
+                                               c.head_sink, out, c.past_k, c.past_v, ws, st), "prefill bias")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    q_rot, pk, pv, s = oracle.rope_append(c.params, host["q"], host["k"], host["v"], host["past_k"],
+                                          host["past_v"], host["seq"], host["cos"], host["sin"],
+                                          present_k=host["past_k"], present_v=host["past_v"])
+    assert s == 0
+    np.testing.assert_array_equal(storage(c.past_k[:, :, : w.q_len]), pk[:, :, : w.q_len])
+    rows = sample_rows(w)
+    ref = oracle.attention_masked(c.params, q_rot, pk, pv, host["seq"], mask_host, "add", host["sink"], rows=rows)
+    assert_close(out_rows(out, c, rows), ref, w.dtype, w.name)
+    torch.cuda.empty_cache()
