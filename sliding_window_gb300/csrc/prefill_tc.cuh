@@ -20,12 +20,13 @@
 // visited; only tiles that cross a frontier evaluate the per-element predicate.
 // The sink starts the running state: m = z*log2(e), l = 1, so it is counted exactly once.
 //
-// With an attention mask (MK = 1 boolean keep flags, 2 additive values; onnx-light-cpu
-// "Layouts and semantics"), warp 2 streams the mask's [128 rows x 128 keys] tile of each
-// head into shared memory by TMA, one buffer per head released by that head's softmax; the
-// softmax applies it to S before the row maximum.  Key tiles then start on 16-key
-// boundaries (the TMA rule for the mask's inner coordinate); the extra keys lie outside the
-// band.  With an additive mask and D = 128 the K ring has one stage, to make room.
+// With an attention mask (MK = 1 boolean keep flags, 2 additive values per head, 3 additive
+// values shared by the heads; onnx-light-cpu "Layouts and semantics"), warp 2 streams the
+// mask's [128 rows x 128 keys] tile into shared memory by TMA, one buffer per head (MK 1,
+// 2) or one for both (MK 3) released by the softmax that reads it; the softmax applies it
+// to S before the row maximum.  Key tiles then start on 16-key boundaries (the TMA rule for
+// the mask's inner coordinate); the extra keys lie outside the band.  With per-head
+// additive tiles and D = 128 the K ring has one stage, to make room.
 #pragma once
 #include <float.h>
 #include <limits.h>
@@ -56,14 +57,17 @@ struct PrefillArgs {
 
 template <int D, int MK> struct PSmem {
   static constexpr int kTile = BM * D * 2;  // one Q, K or V tile
-  static constexpr int kKStages = (MK == 2 && D == 128) ? 1 : 2;
-  static constexpr int kMaskTile = MK == 1 ? BM * BN : MK == 2 ? BM * BN * 2 : 0;  // one head's
+  static constexpr int kMaskTile = MK == 1 ? BM * BN : MK >= 2 ? BM * BN * 2 : 0;  // one buffer
+  static constexpr int kMaskRing = MK == 3 ? 2 : 1;  // shared tiles in flight (MK 3)
+  static constexpr int kMaskBufs = MK == 3 ? kMaskRing : 2;
+  // the K ring gives up a stage when the mask buffers need more than 32 KB at D = 128
+  static constexpr int kKStages = (D == 128 && kMaskBufs * kMaskTile > 32 * 1024) ? 1 : 2;
   static constexpr int kQA = 0;
   static constexpr int kQB = kQA + kTile;
   static constexpr int kK = kQB + kTile;
   static constexpr int kV = kK + kKStages * kTile;  // two stages
   static constexpr int kM = kV + 2 * kTile;         // mask tiles of heads A and B
-  static constexpr int kBar = kM + 2 * kMaskTile;
+  static constexpr int kBar = kM + kMaskBufs * kMaskTile;
   static constexpr int kTmemSlot = kBar + 24 * 8;
   static constexpr int kFlag = kTmemSlot + 8;
   static constexpr int kBytes = kFlag + 8;
@@ -159,6 +163,16 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Two additive mask values (one 32-bit word of the dtype) as a pair of floats.
+template <typename T> __device__ __forceinline__ uint64_t bias_pair(uint32_t w);
+template <> __device__ __forceinline__ uint64_t bias_pair<__nv_bfloat16>(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <> __device__ __forceinline__ uint64_t bias_pair<__half>(uint32_t w) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+  return f2_pack(f.x, f.y);
+}
+
 // Frontier tiles with a softcap: clear the packed P of the keys outside [lo_vis, hi_vis]
 // in this lane's 64 TMEM columns of P and return how many there were.  Kept out of line so
 // that the softmax loop around it compiles as without it.
@@ -238,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(&bars[i], (i == B_PFULL_A || i == B_PFULL_B || i == B_MEMPTY_A || i == B_MEMPTY_B) ? 4 : 1);
+      mbar_init(&bars[i], ((i == B_MEMPTY_A || i == B_MEMPTY_B) && MK == 3 && has_b) ? 8  // both heads read it
+                          : (i == B_PFULL_A || i == B_PFULL_B || i == B_MEMPTY_A || i == B_MEMPTY_B) ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -250,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [384,384+D); P_X overwrites
   // the first 64 columns of S_X as packed pairs
   int kissued = 0, vissued = 0;      // producer thread: TMA tiles issued
-  int missued[2] = {0, 0};           // mask producer thread: tiles issued per head
+  int missued[2] = {0, 0};           // mask producer thread: loads issued per buffer
   int s_commits = 0, o_commits = 0;  // MMA thread: last S and PV commit counts
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -286,22 +301,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmm);
       const int mrows = a.mask_bcast_i ? 1 : BM;
-      const uint32_t bytes = (uint32_t)mrows * 128u * (MK == 2 ? 2u : 1u);
+      const uint32_t bytes = (uint32_t)mrows * 128u * (MK >= 2 ? 2u : 1u);
       const int mb = a.mask_bcast_b ? 0 : b, mq = a.mask_bcast_i ? 0 : q0;
       for (int t = 0; t < ntiles; ++t) {
         const int k0 = klo + t * BN;
         bool fine = true;
-        for (int h = 0; h < (has_b ? 2 : 1); ++h) {
-          if (t >= 1 && !mbar_wait(&bars[B_MEMPTY_A + h], (t - 1) & 1, abort_flag)) {
+        // MK 1, 2: one buffer per head; MK 3: the shared tile goes to ring slot t % kMaskRing
+        for (int h = 0; h < (MK != 3 && has_b ? 2 : 1); ++h) {
+          const int slot = MK == 3 ? t % L::kMaskRing : h, use = MK == 3 ? t / L::kMaskRing : t;
+          if (use >= 1 && !mbar_wait(&bars[B_MEMPTY_A + slot], (use - 1) & 1, abort_flag)) {
             fine = false;
             break;
           }
           const int mh = a.mask_bcast_h ? 0 : hA + h;
-          uint8_t *dst = smem + L::kM + h * L::kMaskTile;
-          mbar_expect_tx(&bars[B_MFULL_A + h], bytes);
-          tma_load_4d(dst, &tmm, k0, mq, mh, mb, &bars[B_MFULL_A + h]);
-          if (MK == 2) tma_load_4d(dst + BM * 128, &tmm, k0 + 64, mq, mh, mb, &bars[B_MFULL_A + h]);
-          missued[h] = t + 1;
+          uint8_t *dst = smem + L::kM + slot * L::kMaskTile;
+          mbar_expect_tx(&bars[B_MFULL_A + slot], bytes);
+          tma_load_4d(dst, &tmm, k0, mq, mh, mb, &bars[B_MFULL_A + slot]);
+          if (MK >= 2) tma_load_4d(dst + BM * 128, &tmm, k0 + 64, mq, mh, mb, &bars[B_MFULL_A + slot]);
+          missued[slot] = use + 1;
         }
         if (!fine) break;
       }
@@ -436,12 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (MK != 0) {
         // this row's mask values for keys [k0, k0 + 128), 16-byte chunks of the 128B-swizzled
         // tile (row-broadcast masks hold one row)
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_MFULL_A + wg], t & 1, abort_flag))) {
+        const int mbuf = MK == 3 ? t % L::kMaskRing : wg, muse = MK == 3 ? t / L::kMaskRing : t;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_MFULL_A + mbuf], muse & 1, abort_flag))) {
           ok = false;
           break;
         }
         const int mr = a.mask_bcast_i ? 0 : row;
-        const uint8_t *mrow = smem + L::kM + wg * L::kMaskTile + mr * 128;
+        const uint8_t *mrow = smem + L::kM + mbuf * L::kMaskTile + mr * 128;
         if constexpr (MK == 1) {
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
@@ -452,7 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (((w[e >> 2] >> (8 * (e & 3))) & 0xFFu) == 0u) r[ch * 16 + e] = __float_as_uint(-INFINITY);
           }
         } else {
-          const float bm = a.bias_mul;
+          // r += bias / scale, two keys per instruction (an additive -inf makes r -inf: weight
+          // 0 without a softcap, the score -softcap through tanh with one)
+          const uint64_t bm2 = f2_pack(a.bias_mul, a.bias_mul);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -460,19 +480,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint4 v = *reinterpret_cast<const uint4 *>(mrow + hf * (BM * 128) + ((ch ^ (mr & 7)) << 4));
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                T bv;
-                *reinterpret_cast<uint16_t *>(&bv) = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
-                float x = fmaf(to_f32(bv), bm, __uint_as_float(r[hf * 64 + ch * 8 + e]));
-                // under a softcap an additive -inf is the finite score -softcap (tanh(-inf) = -1),
-                // so keep it finite here; -inf stays reserved for removed keys
-                if (SOFTCAP) x = fmaxf(x, -FLT_MAX);
-                r[hf * 64 + ch * 8 + e] = __float_as_uint(x);
+              for (int e = 0; e < 8; e += 2) {
+                uint32_t &r0 = r[hf * 64 + ch * 8 + e], &r1 = r[hf * 64 + ch * 8 + e + 1];
+                const float2 y = f2_unpack(f2_fma(bias_pair<T>(w[e >> 1]), bm2, f2_pack(__uint_as_float(r0),
+                                                                                         __uint_as_float(r1))));
+                r0 = __float_as_uint(y.x);
+                r1 = __float_as_uint(y.y);
               }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_MEMPTY_A + wg]);
+        if (lane == 0) mbar_arrive(&bars[B_MEMPTY_A + mbuf]);
       }
       if (edge) {  // band predicate on frontier tiles only
         const int lo_vis = a.window > 0 ? qa - a.window + 1 : INT_MIN;
@@ -486,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = -INFINITY;
 #pragma unroll
       for (int e = 0; e < BN; e += 2) mx = fmax3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+      // under a softcap an additive -inf still scores -softcap: the maximum counts it
+      if (MK >= 2 && SOFTCAP) mx = fmaxf(mx, -FLT_MAX);
       float m_tile = -INFINITY;
       if (mx != -INFINITY) m_tile = SOFTCAP ? tanh_fast(mx * smul) * cmul : mx * smul;
       // lazy rescale: move the reference max only when it grows by more than 2^8
@@ -512,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float2 xf = f2_unpack(x);
           float p0 = ex2(xf.x), p1 = ex2(xf.y);
-          if (MK != 0 && SOFTCAP) {  // removed keys (band or mask) have weight exactly zero
+          if (MK == 1 && SOFTCAP) {  // removed keys (band or mask) have weight exactly zero
             if (r[half * 64 + e] == __float_as_uint(-INFINITY)) p0 = 0.f;
             if (r[half * 64 + e + 1] == __float_as_uint(-INFINITY)) p1 = 0.f;
           }
@@ -523,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float2 rsf = f2_unpack(rs2);
       float rs = rsf.x + rsf.y;
-      if (MK == 0 && SOFTCAP && edge) {
+      if (MK != 1 && SOFTCAP && edge) {
         // a masked key's -inf came out of tanh as -1, i.e. a score of -softcap: clear its P
         // (the same value for every masked key of the row) in TMEM and take it out of the
         // row sum, so that a masked key has exactly zero weight.  Frontier tiles only.
@@ -621,7 +641,7 @@ template <typename T, int D, bool SC, int MK> gqa_status launch_cfg(const Call &
   if (!encode_kv_map(&tk, c.present_k, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
   if (!encode_kv_map(&tv, c.present_v, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
   if (MK) {
-    const int es = MK == 2 ? 2 : 1;
+    const int es = MK >= 2 ? 2 : 1;
     if (!encode_mask_map(&tm, c.mask, c.mask_keys, p.q_len, p.q_heads, p.batch, c.mask_si * es, c.mask_sh * es,
                          c.mask_sb * es, 128 / es, c.mask_si == 0 ? 1 : BM, es))
       return GQA_ERR_CUDA;

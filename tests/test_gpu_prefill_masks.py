@@ -195,3 +195,17 @@ def test_prefill_mask_shorter_than_a_sequence_rejects_it():
     out, *_, st = run(c, mask, "bool")
     assert st & 1
     assert np.all(out_rows(out, c) == 0.0)
+
+
+@pytest.mark.parametrize("kind,shape,softcap", [("bool", "b1ik", 0.0), ("add", "b1ik", 25.0), ("add", "full", 0.0),
+                                                ("add", "b11k", 25.0)])
+def test_odd_group_size(kind, shape, softcap):
+    """G = 3: the last CTA of each kv group holds one q head (a shared mask tile read by one
+    softmax warpgroup)."""
+    c = case("prefill", "bf16", 128, 3, 200, 64, 150, softcap=softcap, sink="smooth", seed=18)
+    B, Hq = c.q.shape[0], c.params["q_heads"]
+    mask = draw_mask(kind, mask_shape(shape, B, Hq, 200, 272), "bf16", np.random.default_rng(18))
+    out, *_, st = run(c, mask, kind)
+    ref, *_ = oracle_masked(c, mask, kind)
+    assert st == 0
+    assert_close(out_rows(out, c), ref, "bf16", "G=3 %s %s" % (kind, shape))
