@@ -34,6 +34,12 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def v_dim(p: dict) -> int:
+    """The V head dimension: v_head_dim when given and nonzero, else head_dim ([P4] "Layouts
+    and semantics": it may differ from the Q/K head dimension)."""
+    return int(p.get("v_head_dim", 0) or p["head_dim"])
 _lock = threading.Lock()
 _lib = None
 
@@ -73,18 +79,18 @@ def _load():
         lib.oracle_sequence_status.restype = i32
         lib.oracle_visible.argtypes = [i64, i64, i64, i32, i32]
         lib.oracle_visible.restype = i32
-        lib.oracle_rope_append.argtypes = [i32] * 10 + [vp] * 11 + [ctypes.POINTER(i32)]
+        lib.oracle_rope_append.argtypes = [i32] * 11 + [vp] * 11 + [ctypes.POINTER(i32)]
         lib.oracle_rope_append.restype = None
-        lib.oracle_attend_row.argtypes = [vp, vp, vp, i64, i64, vp, i32, i32, f64, f64, i32, f64, vp]
+        lib.oracle_attend_row.argtypes = [vp, vp, vp, i64, i64, vp, i32, i32, i32, f64, f64, i32, f64, vp]
         lib.oracle_attend_row.restype = None
-        lib.oracle_attention.argtypes = [i32] * 9 + [f64, f64] + [i32] * 5 + [vp] * 6 + [i64, vp]
+        lib.oracle_attention.argtypes = [i32] * 10 + [f64, f64] + [i32] * 5 + [vp] * 6 + [i64, vp]
         lib.oracle_ring_valid.argtypes = [i32] * 3
         lib.oracle_ring_valid.restype = i32
         lib.oracle_ring_status.argtypes = [i32] * 4
         lib.oracle_ring_status.restype = i32
         lib.oracle_rope_append_ring.argtypes = [i32] * 9 + [vp] * 9 + [ctypes.POINTER(i32)]
         lib.oracle_attention_ring.argtypes = [i32] * 8 + [f64, f64] + [i32] * 4 + [vp] * 6 + [i64, vp]
-        lib.oracle_attention_masked.argtypes = [i32] * 8 + [f64, f64] + [i32] * 5 + [vp, i64, i64, i64, i32] + \
+        lib.oracle_attention_masked.argtypes = [i32] * 9 + [f64, f64] + [i32] * 5 + [vp, i64, i64, i64, i32] + \
             [vp] * 6 + [i64, vp]
         lib.oracle_paged_status.argtypes = [i32] * 6 + [vp, i32, i32]
         lib.oracle_paged_status.restype = i32
@@ -174,7 +180,7 @@ def rope_append(p: dict, q, k, v, past_k, past_v, seqlens_k, cos_cache=None, sin
     cs = _bits(cos_cache, dt) if cos_cache is not None else None
     sn = _bits(sin_cache, dt) if sin_cache is not None else None
     seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
-    lib.oracle_rope_append(p["batch"], p["q_heads"], p["kv_heads"], p["head_dim"], p["q_len"],
+    lib.oracle_rope_append(p["batch"], p["q_heads"], p["kv_heads"], p["head_dim"], v_dim(p), p["q_len"],
                            p.get("cap_past", p["cap_present"]), p["cap_present"], p.get("rope_len", 0),
                            DTYPE_CODES[dt], int(p.get("do_rotary", 0)),
                            _ptr(q), _ptr(k), _ptr(v), _ptr(pk), _ptr(pv), _ptr(seq), _ptr(cs), _ptr(sn),
@@ -187,13 +193,15 @@ def rope_append(p: dict, q, k, v, past_k, past_v, seqlens_k, cos_cache=None, sin
 # --------------------------------------------------------------------------------------
 def attend_row(q: np.ndarray, k: np.ndarray, v: np.ndarray, visible_mask: np.ndarray, dtype: str,
                scale: float, softcap: float = 0.0, sink=None) -> np.ndarray:
-    """One query row (q: D floats) over n cache rows with an explicit visibility mask."""
+    """One query row (q: D floats) over n cache rows (k: [n, D], v: [n, Dv]) with an
+    explicit visibility mask; returns Dv floats."""
     lib = _load()
     qd = np.ascontiguousarray(q, dtype=np.float64)
     kb, vb = _bits(k, dtype), _bits(v, dtype)
     vis = np.ascontiguousarray(visible_mask, dtype=np.uint8)
-    out = np.zeros(qd.shape[0], dtype=np.float64)
-    lib.oracle_attend_row(_ptr(qd), _ptr(kb), _ptr(vb), 0, vis.shape[0], _ptr(vis), qd.shape[0],
+    dv = vb.size // max(1, vis.shape[0])
+    out = np.zeros(dv, dtype=np.float64)
+    lib.oracle_attend_row(_ptr(qd), _ptr(kb), _ptr(vb), 0, vis.shape[0], _ptr(vis), qd.shape[0], dv,
                           DTYPE_CODES[dtype], float(scale), float(softcap), int(sink is not None),
                           float(sink if sink is not None else 0.0), _ptr(out))
     return out
@@ -213,21 +221,21 @@ def attention(p: dict, q_rot, present_k, present_v, seqlens_k, head_sink=None, r
     kb, vb = _bits(present_k, dt), _bits(present_v, dt)
     seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
     sink = None if head_sink is None else np.ascontiguousarray(head_sink, dtype=np.float32)
-    B, Hq, D, curr = p["batch"], p["q_heads"], p["head_dim"], p["q_len"]
+    B, Hq, D, curr, Dv = p["batch"], p["q_heads"], p["head_dim"], p["q_len"], v_dim(p)
     if rows is None:
         ridx, n = None, B * curr * Hq
     else:
         ridx = np.ascontiguousarray(rows, dtype=np.int64)
         n = ridx.shape[0]
-    out = np.zeros((n, D), dtype=np.float64)
-    lib.oracle_attention(B, Hq, p["kv_heads"], D, curr, p.get("cap_past", p["cap_present"]),
+    out = np.zeros((n, Dv), dtype=np.float64)
+    lib.oracle_attention(B, Hq, p["kv_heads"], D, Dv, curr, p.get("cap_past", p["cap_present"]),
                          p["cap_present"], p.get("rope_len", 0), DTYPE_CODES[dt],
                          float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)), int(p.get("window", -1)),
                          int(p.get("causal", 1)), int(p.get("do_rotary", 0)), int(p.get("smooth_softmax", 0)),
                          int(past_is_separate), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq), _ptr(sink),
                          _ptr(ridx), n, _ptr(out))
     if rows is None:
-        return out.reshape(B, curr, Hq, D)
+        return out.reshape(B, curr, Hq, Dv)
     return out
 
 
@@ -367,19 +375,19 @@ def attention_masked(p: dict, q_rot, present_k, present_v, seqlens_k, mask, kind
     m = np.ascontiguousarray(mask, dtype=np.uint8) if kind == "bool" else _bits(mask, dt)
     assert m.ndim == 4
     st = [0 if m.shape[d] == 1 else int(np.prod(m.shape[d + 1:])) for d in range(3)]
-    B, Hq, D, curr = p["batch"], p["q_heads"], p["head_dim"], p["q_len"]
+    B, Hq, D, curr, Dv = p["batch"], p["q_heads"], p["head_dim"], p["q_len"], v_dim(p)
     if rows is None:
         ridx, n = None, B * curr * Hq
     else:
         ridx = np.ascontiguousarray(rows, dtype=np.int64)
         n = ridx.shape[0]
-    out = np.zeros((n, D), dtype=np.float64)
-    lib.oracle_attention_masked(B, Hq, p["kv_heads"], D, curr, p["cap_present"], p.get("rope_len", 0),
+    out = np.zeros((n, Dv), dtype=np.float64)
+    lib.oracle_attention_masked(B, Hq, p["kv_heads"], D, Dv, curr, p["cap_present"], p.get("rope_len", 0),
                                 DTYPE_CODES[dt], float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)),
                                 int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
                                 int(p.get("smooth_softmax", 0)), 1 if kind == "bool" else 2, _ptr(m), st[0], st[1],
                                 st[2], m.shape[3], _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq), _ptr(sink), _ptr(ridx), n,
                                 _ptr(out))
     if rows is None:
-        return out.reshape(B, curr, Hq, D)
+        return out.reshape(B, curr, Hq, Dv)
     return out

@@ -182,7 +182,7 @@ static void rotate_row(const void *x, size_t xoff, const void *cosc, const void 
   }
 }
 
-void oracle_rope_append(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap_past,
+void oracle_rope_append(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv, int32_t curr, int32_t cap_past,
                         int32_t cap_present, int32_t rope_len, int32_t dtype, int32_t do_rotary,
                         const void *q, const void *k, const void *v, const void *past_k,
                         const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
@@ -198,10 +198,13 @@ void oracle_rope_append(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t c
     if (st) continue;
     for (int h = 0; h < Hkv; ++h) {
       size_t dst_base = ((size_t)b * Hkv + h) * (size_t)cap_present * D;
+      size_t dst_base_v = ((size_t)b * Hkv + h) * (size_t)cap_present * Dv;
       if (separate) {
         size_t src_base = ((size_t)b * Hkv + h) * (size_t)cap_past * D;
+        size_t src_base_v = ((size_t)b * Hkv + h) * (size_t)cap_past * Dv;
         memcpy((char *)present_k + dst_base * es, (const char *)past_k + src_base * es, (size_t)past * D * es);
-        memcpy((char *)present_v + dst_base * es, (const char *)past_v + src_base * es, (size_t)past * D * es);
+        memcpy((char *)present_v + dst_base_v * es, (const char *)past_v + src_base_v * es,
+               (size_t)past * Dv * es);
       }
       for (int i = 0; i < curr; ++i) {
         size_t src = (((size_t)b * curr + i) * Hkv + h) * D;
@@ -210,7 +213,9 @@ void oracle_rope_append(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t c
           rotate_row(k, src, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, present_k, dst);
         else
           memcpy((char *)present_k + dst * es, (const char *)k + src * es, (size_t)D * es);
-        memcpy((char *)present_v + dst * es, (const char *)v + src * es, (size_t)D * es);
+        size_t src_v = (((size_t)b * curr + i) * Hkv + h) * Dv;
+        size_t dst_v = dst_base_v + (size_t)(past + i) * Dv;
+        memcpy((char *)present_v + dst_v * es, (const char *)v + src_v * es, (size_t)Dv * es);
       }
     }
     if (q_rot) {
@@ -254,11 +259,13 @@ int32_t oracle_visible(int64_t q_abs, int64_t j, int64_t total, int32_t causal, 
  *   ([P4] "A fully masked query row produces zeros rather than NaN").  A score of -inf
  *   (an additive mask value of -inf without a softcap) has weight exactly zero, so a row
  *   whose scores are all -inf is fully masked and gives zeros too, not 0/0.
- * q is D doubles; k and v point at `n` rows of D elements of `dtype`.
+ * q is D doubles; k points at `n` rows of D elements of `dtype`, v at `n` rows of Dv
+ * ([P4] "Layouts and semantics": the V head dimension may differ from the Q/K one); out
+ * holds Dv doubles.
  * ---------------------------------------------------------------------------------- */
 void oracle_attend_row_bias(const double *q, const void *k, const void *v, int64_t row0, int64_t n,
-                            const uint8_t *visible, const double *bias, int32_t D, int32_t dtype, double scale,
-                            double softcap, int32_t has_sink, double sink, double *out) {
+                            const uint8_t *visible, const double *bias, int32_t D, int32_t Dv, int32_t dtype,
+                            double scale, double softcap, int32_t has_sink, double sink, double *out) {
   double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   double M = -INFINITY;
   int any = 0;
@@ -274,7 +281,7 @@ void oracle_attend_row_bias(const double *q, const void *k, const void *v, int64
     if (sj > M) M = sj;
     any = 1;
   }
-  for (int d = 0; d < D; ++d) out[d] = 0.0;
+  for (int d = 0; d < Dv; ++d) out[d] = 0.0;
   if (!any) {
     free(s);
     return;
@@ -285,21 +292,21 @@ void oracle_attend_row_bias(const double *q, const void *k, const void *v, int64
     if (!visible[j]) continue;
     double w = exp(s[j] - M);
     den += w;
-    for (int d = 0; d < D; ++d) out[d] += w * load_elem(v, (size_t)(row0 + j) * D + d, dtype);
+    for (int d = 0; d < Dv; ++d) out[d] += w * load_elem(v, (size_t)(row0 + j) * Dv + d, dtype);
   }
-  for (int d = 0; d < D; ++d) out[d] /= den;
+  for (int d = 0; d < Dv; ++d) out[d] /= den;
   free(s);
 }
 
 void oracle_attend_row(const double *q, const void *k, const void *v, int64_t row0, int64_t n,
-                       const uint8_t *visible, int32_t D, int32_t dtype, double scale, double softcap,
+                       const uint8_t *visible, int32_t D, int32_t Dv, int32_t dtype, double scale, double softcap,
                        int32_t has_sink, double sink, double *out) {
-  oracle_attend_row_bias(q, k, v, row0, n, visible, NULL, D, dtype, scale, softcap, has_sink, sink, out);
+  oracle_attend_row_bias(q, k, v, row0, n, visible, NULL, D, Dv, dtype, scale, softcap, has_sink, sink, out);
 }
 
 /* ------------------------------------------------------------------------------------
  * Whole attention over the present cache, for a list of rows (or all rows).
- * Row index r = ((b * curr) + i) * Hq + hq; out holds D doubles per listed row.
+ * Row index r = ((b * curr) + i) * Hq + hq; out holds Dv doubles per listed row.
  * Head mapping ([P4] "Layouts and semantics"): group_size G = Hq / Hkv and q head hq
  * reads kv head hq / G, with no copy of K or V.
  * q is the query as it enters the scores (already rotated when do_rotary).
@@ -307,7 +314,7 @@ void oracle_attend_row(const double *q, const void *k, const void *v, int64_t ro
  * smooth_softmax, else none.
  * Rejected sequences (oracle_sequence_status != 0) give zeros.
  * ---------------------------------------------------------------------------------- */
-void oracle_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap_past,
+void oracle_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv, int32_t curr, int32_t cap_past,
                       int32_t cap_present, int32_t rope_len, int32_t dtype, double scale,
                       double softcap, int32_t window, int32_t causal, int32_t do_rotary,
                       int32_t smooth_softmax, int32_t past_is_separate, const void *q,
@@ -324,10 +331,10 @@ void oracle_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t cur
     int hq = (int)(r % Hq);
     int i = (int)((r / Hq) % curr);
     int b = (int)(r / ((int64_t)Hq * curr));
-    double *o = out + (size_t)t * D;
+    double *o = out + (size_t)t * Dv;
     int32_t past = seqlens_k[b];
     if (oracle_sequence_status(past, curr, cap_past, cap_present, past_is_separate, do_rotary, rope_len)) {
-      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int d = 0; d < Dv; ++d) o[d] = 0.0;
       continue;
     }
     int hk = hq / G;
@@ -340,7 +347,8 @@ void oracle_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t cur
     int has_sink = head_sink != NULL || smooth_softmax;
     double z = head_sink ? (double)head_sink[hq] : 0.0;
     int64_t row0 = ((int64_t)b * Hkv + hk) * cap_present;
-    oracle_attend_row(qv, present_k, present_v, row0, cap_present, vis, D, dtype, scale, softcap, has_sink, z, o);
+    oracle_attend_row(qv, present_k, present_v, row0, cap_present, vis, D, Dv, dtype, scale, softcap, has_sink, z,
+                      o);
     free(vis);
     free(qv);
   }
@@ -454,7 +462,7 @@ void oracle_attention_ring(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_
     for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
     int has_sink = head_sink != NULL || smooth_softmax;
     double z = head_sink ? (double)head_sink[hq] : 0.0;
-    oracle_attend_row(qv, kg, vg, 0, n, vis, D, dtype, scale, softcap, has_sink, z, o);
+    oracle_attend_row(qv, kg, vg, 0, n, vis, D, D, dtype, scale, softcap, has_sink, z, o);
     free(qv);
     free(vis);
     free(vg);
@@ -575,7 +583,7 @@ void oracle_attention_paged(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32
     for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
     int has_sink = head_sink != NULL || smooth_softmax;
     double z = head_sink ? (double)head_sink[hq] : 0.0;
-    oracle_attend_row(qv, kg, vg, 0, n, vis, D, dtype, scale, softcap, has_sink, z, o);
+    oracle_attend_row(qv, kg, vg, 0, n, vis, D, D, dtype, scale, softcap, has_sink, z, o);
     free(qv);
     free(vis);
     free(vg);
@@ -593,7 +601,8 @@ void oracle_attention_paged(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32
  * scaled score before the softcap (matmul, mask, softcap, softmax).  The band, the sink and
  * the fully-masked-row rule are unchanged; the contiguous layout only.
  * ---------------------------------------------------------------------------------- */
-void oracle_attention_masked(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t curr, int32_t cap_present,
+void oracle_attention_masked(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv, int32_t curr,
+                             int32_t cap_present,
                              int32_t rope_len, int32_t dtype, double scale, double softcap, int32_t window,
                              int32_t causal, int32_t do_rotary, int32_t smooth_softmax, int32_t mask_kind,
                              const void *mask, int64_t stride_b, int64_t stride_h, int64_t stride_i, int32_t keys,
@@ -610,11 +619,11 @@ void oracle_attention_masked(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int3
     int hq = (int)(r % Hq);
     int i = (int)((r / Hq) % curr);
     int b = (int)(r / ((int64_t)Hq * curr));
-    double *o = out + (size_t)t * D;
+    double *o = out + (size_t)t * Dv;
     int32_t past = seqlens_k[b];
     if (oracle_sequence_status(past, curr, 0, cap_present, 0, do_rotary, rope_len) ||
         (int64_t)past + curr > keys) {
-      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int d = 0; d < Dv; ++d) o[d] = 0.0;
       continue;
     }
     int hk = hq / G;
@@ -634,7 +643,7 @@ void oracle_attention_masked(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int3
     int has_sink = head_sink != NULL || smooth_softmax;
     double z = head_sink ? (double)head_sink[hq] : 0.0;
     int64_t row0 = ((int64_t)b * Hkv + hk) * cap_present;
-    oracle_attend_row_bias(qv, present_k, present_v, row0, cap_present, vis, bias, D, dtype, scale, softcap,
+    oracle_attend_row_bias(qv, present_k, present_v, row0, cap_present, vis, bias, D, Dv, dtype, scale, softcap,
                            has_sink, z, o);
     free(bias);
     free(vis);

@@ -49,6 +49,7 @@ class Workload:
     kv_ring: int = 0        # 1: the cache is a ring of `cap` slots, position p in slot p % cap
     kv_paged: int = 0       # 1: the cache is a shared pool of 64-position pages behind a block table
     mask: str = ""          # "add": an additive attention bias [B, 1, S, cap] of the dtype, N(0,1)
+    v_head_dim: int = 0     # Dv; 0: the same as head_dim
 
     @property
     def layers(self) -> int:
@@ -62,7 +63,7 @@ class Workload:
                     cap_present=self.cap, rope_len=self.rope_len, dtype=self.dtype,
                     scale=self.scale, softcap=self.softcap, window=self.windows[layer],
                     causal=self.causal, do_rotary=self.do_rotary, rotary_interleaved=0,
-                    smooth_softmax=self.smooth_softmax, kv_ring=self.kv_ring)
+                    smooth_softmax=self.smooth_softmax, kv_ring=self.kv_ring, v_head_dim=self.v_head_dim)
 
     def scaled(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -163,21 +164,22 @@ def make_case(w: Workload, layer: int = 0, device="cpu", seed_offset: int = 0, g
     junk.manual_seed(5000 + w.index + 104729 * layer + 7919 * seed_offset)
     t = TORCH_DTYPES[w.dtype]
     B, Hq, Hkv, D, L, cap = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.q_len, w.cap
+    Dv = w.v_head_dim or D
 
     def randn(*shape):
         return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(t)
 
     q = randn(B, L, Hq * D)
     k = randn(B, L, Hkv * D)
-    v = randn(B, L, Hkv * D)
+    v = randn(B, L, Hkv * Dv)
     seq = draw_seqlens(w, seed_offset) if seqlens is None else np.asarray(seqlens, dtype=np.int32)
     past_k = torch.empty(B, Hkv, cap, D, dtype=t, device=dev)
-    past_v = torch.empty(B, Hkv, cap, D, dtype=t, device=dev)
+    past_v = torch.empty(B, Hkv, cap, Dv, dtype=t, device=dev)
     # rows are drawn per sequence so that the large caches never need an fp32 copy in full
     for b in range(B):
         n = min(int(seq[b]), cap) if w.kv_ring else int(seq[b])
         for buf in (past_k, past_v):
-            tmp = torch.empty(Hkv, cap, D, dtype=torch.float32, device=dev)
+            tmp = torch.empty(Hkv, cap, buf.shape[-1], dtype=torch.float32, device=dev)
             tmp[:, :n].normal_(0.0, 1.0, generator=gen)
             _fill_garbage(tmp[:, n:], garbage, w.garbage_std, junk)
             buf[b].copy_(tmp)

@@ -22,12 +22,14 @@ def visible_set(past, curr, i, window, causal):
 
 
 def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, causal, scale,
-              softcap=0.0, sinks=None, keep=None, bias=None):
+              softcap=0.0, sinks=None, keep=None, bias=None, Dv=None):
     """q[b][i][hq] -> list of D floats; present_k[b][h][j] -> list of D floats.
     sinks: None, or a list of Hq floats.  keep(b, hq, i, j) -> bool removes keys from the
     row (a boolean mask); bias(b, hq, i, j) -> float is added to the scaled score before
-    the softcap (an additive mask).  Returns out[b][i][hq] lists of D floats."""
+    the softcap (an additive mask).  present_v rows hold Dv floats (default D).  Returns
+    out[b][i][hq] lists of Dv floats."""
     G = Hq // Hkv
+    Dv = D if Dv is None else Dv
     out = []
     for b in range(B):
         ob = []
@@ -51,7 +53,7 @@ def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, cau
                     logits.append(s)
                     values.append(present_v[b][h][j])
                 if not values:
-                    oi.append([0.0] * D)
+                    oi.append([0.0] * Dv)
                     continue
                 if sinks is not None:
                     logits.append(sinks[hq])   # extra logit in the denominator ...
@@ -59,7 +61,7 @@ def attention(q, present_k, present_v, seqlens, B, Hq, Hkv, D, curr, window, cau
                 e = [math.exp(x - m) for x in logits]
                 den = math.fsum(e)
                 p = [x / den for x in e][: len(values)]   # ... and sliced out
-                oi.append([math.fsum(p[t] * values[t][d] for t in range(len(values))) for d in range(D)])
+                oi.append([math.fsum(p[t] * values[t][d] for t in range(len(values))) for d in range(Dv)])
             ob.append(oi)
         out.append(ob)
     return out

@@ -22,10 +22,11 @@ from sliding_window_gb300.inputs import Workload, make_case
 
 
 def tiny(B=2, Hq=4, Hkv=2, D=8, curr=1, cap=12, dtype="f32", seqlens=None, window=-1, causal=1,
-         softcap=0.0, head_sink=False, smooth=0, rotary=0, rope_len=0, scale=0.0, seed=0, garbage="normal"):
+         softcap=0.0, head_sink=False, smooth=0, rotary=0, rope_len=0, scale=0.0, seed=0, garbage="normal",
+         Dv=0):
     w = Workload("tiny", 50 + seed, "decode", dtype, B, Hq, Hkv, D, curr, cap, 0, cap - curr,
                  windows=(window,), causal=causal, scale=scale, softcap=softcap, head_sink=head_sink,
-                 smooth_softmax=smooth, do_rotary=rotary, rope_len=rope_len)
+                 smooth_softmax=smooth, do_rotary=rotary, rope_len=rope_len, v_head_dim=Dv)
     return make_case(w, seed_offset=seed, seqlens=seqlens, garbage=garbage)
 
 
@@ -42,10 +43,11 @@ def run_oracle(c, rows=None):
 def concat_present(c):
     """Independent statement of past->present concat (no rotary): fp64 copies."""
     B, Hq, Hkv, D, L = c.w.batch, c.w.q_heads, c.w.kv_heads, c.w.head_dim, c.w.q_len
+    Dv = c.w.v_head_dim or D
     pk = as_f64(c.past_k).copy()
     pv = as_f64(c.past_v).copy()
     k = as_f64(c.k).reshape(B, L, Hkv, D)
-    v = as_f64(c.v).reshape(B, L, Hkv, D)
+    v = as_f64(c.v).reshape(B, L, Hkv, Dv)
     for b in range(B):
         s = int(c.seqlens_k[b])
         pk[b, :, s:s + L] = k[b].transpose(1, 0, 2)
