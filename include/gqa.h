@@ -20,19 +20,24 @@
  *       the window is a per-layer setting and masks the cache rather than evicting it.
  *  [P4] onnx-light-cpu "Attention Kernel Design": "Layouts and semantics" (rank-3
  *       [B, L, H*D] tensors; group_size = q_heads / kv_heads maps q heads onto kv heads
- *       without repeating K or V; softcap), "Compute paths" (streaming online softmax,
+ *       without repeating K or V; softcap; a V head dimension that may differ from the
+ *       Q/K one), "Compute paths" (streaming online softmax,
  *       frontier block skipping), "Scheduling, precision, and invariants" (fp32
  *       accumulation, output narrowed once; invalid combinations fail explicitly; a fully
  *       masked row yields zeros, not NaN).
  *
- * Notation: B batch, Hq q heads, Hkv kv heads, G = Hq / Hkv, D head dim, curr = q_len new
- * tokens per sequence, past_b = seqlens_k[b], total_b = past_b + curr, cap = capacity.
+ * Notation: B batch, Hq q heads, Hkv kv heads, G = Hq / Hkv, D head dim of q and k, Dv
+ * head dim of v and out (v_head_dim, D when 0), curr = q_len new tokens per sequence,
+ * past_b = seqlens_k[b], total_b = past_b + curr, cap = capacity.
  *
  * Layouts (all row-major, dense, no padding):
- *   q, out, q_rot   [B, curr, Hq*D]       element type = dtype
- *   k, v            [B, curr, Hkv*D]      new keys / values of this step
- *   past_k, past_v  [B, Hkv, cap_past, D]
- *   present_k/_v    [B, Hkv, cap_present, D]  slot j holds absolute position j
+ *   q, q_rot        [B, curr, Hq*D]       element type = dtype
+ *   out             [B, curr, Hq*Dv]
+ *   k               [B, curr, Hkv*D]      new keys of this step
+ *   v               [B, curr, Hkv*Dv]     new values of this step
+ *   past_k          [B, Hkv, cap_past, D]       past_v  [B, Hkv, cap_past, Dv]
+ *   present_k       [B, Hkv, cap_present, D]    present_v [B, Hkv, cap_present, Dv]
+ *                   slot j holds absolute position j
  *   cos/sin_cache   [rope_len, D/2]       dtype; rotation of half-split pairs (d, d+D/2)
  *   seqlens_k       int32 [B] on the device (a [B,1] tensor works too) = valid past tokens
  *   head_sink       fp32 [Hq] on the device, or NULL
@@ -87,7 +92,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 3
+#define GQA_ABI_VERSION 4
 
 typedef int32_t gqa_status;
 #define GQA_OK 0
@@ -124,6 +129,10 @@ typedef struct gqa_params {
   int32_t rotary_interleaved; /* must be 0 (half-split pairs only) */
   int32_t smooth_softmax;     /* 1 = zero sink when head_sink is NULL */
   int32_t kv_ring;            /* 1 = present is a ring of cap_present slots (see below) */
+  int32_t v_head_dim;         /* Dv: 0 = head_dim, else 64 or 128 ([P4] "Layouts and
+                                 semantics"); Dv != D only with the contiguous cache
+                                 (kv_ring 0, not the paged entry point), else
+                                 GQA_ERR_UNSUPPORTED */
 } gqa_params;
 
 /* Bytes of device workspace that gqa_attention_prefill / gqa_attention_decode need for

@@ -22,12 +22,12 @@ constexpr int kRows = 16;   // query rows per CTA (4 per warp)
 constexpr int kKeys = 32;   // keys per shared-memory tile
 
 struct SimtArgs {
-  const void *q, *kc, *vc;  // q [B, curr, Hq, D]; caches [B, Hkv, cap, D]
+  const void *q, *kc, *vc;  // q [B, curr, Hq, D]; caches [B, Hkv, cap, D] and [B, Hkv, cap, Dv]
   void *out;
   const int32_t *seqlens;
   const float *head_sink;
   int32_t *status;
-  int Hq, Hkv, G, D, curr, cap, cap_past, past_separate, rope_len, do_rotary, window, causal, has_sink;
+  int Hq, Hkv, G, D, Dv, curr, cap, cap_past, past_separate, rope_len, do_rotary, window, causal, has_sink;
   float scale, softcap;
   // attention mask (kind 0: none, 1: uint8 keep flags, 2: additive values of T), element
   // [b][hq][i][key] at b*msb + hq*msh + i*msi + key
@@ -39,11 +39,11 @@ struct SimtArgs {
 template <typename T>
 __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   extern __shared__ float sm[];
-  const int D = a.D;
+  const int D = a.D, Dv = a.Dv;
   float *qs = sm;                          // [kRows][D]
   float *ks = qs + kRows * D;              // [kKeys][D + 1]
-  float *vs = ks + kKeys * (D + 1);        // [kKeys][D]
-  float *ps = vs + kKeys * D;              // [4 warps][kKeys]
+  float *vs = ks + kKeys * (D + 1);        // [kKeys][Dv]
+  float *ps = vs + kKeys * Dv;             // [4 warps][kKeys]
   const int b = blockIdx.z, hq = blockIdx.y;
   const int i0 = blockIdx.x * kRows;
   const int hk = hq / a.G;
@@ -55,9 +55,9 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   const int nrows = min(kRows, a.curr - i0);
   if (st) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && hq == 0) report(a.status, st);
-    for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
-      int r = idx / D, d = idx % D;
-      out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * D + d] = from_f32<T>(0.f);
+    for (int idx = threadIdx.x; idx < nrows * Dv; idx += blockDim.x) {
+      int r = idx / Dv, d = idx % Dv;
+      out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d] = from_f32<T>(0.f);
     }
     return;
   }
@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   const int lo = a.window > 0 ? max(0, qa_lo - a.window + 1) : 0;
   const int hi = a.causal ? min(total, qa_hi + 1) : total;
   const T *kc = reinterpret_cast<const T *>(a.kc) + ((size_t)b * a.Hkv + hk) * a.cap * D;
-  const T *vc = reinterpret_cast<const T *>(a.vc) + ((size_t)b * a.Hkv + hk) * a.cap * D;
-  constexpr int kMaxDSlots = 4;  // D <= 128
+  const T *vc = reinterpret_cast<const T *>(a.vc) + ((size_t)b * a.Hkv + hk) * a.cap * Dv;
+  constexpr int kMaxDSlots = 4;  // Dv <= 128
   float m[4], l[4], acc[4][kMaxDSlots];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -82,14 +82,16 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
 #pragma unroll
     for (int s = 0; s < kMaxDSlots; ++s) acc[t][s] = 0.f;
   }
-  const int dslots = D / 32;
+  const int dslots = Dv / 32;
   for (int kt = lo; kt < hi; kt += kKeys) {
     __syncthreads();
     for (int idx = threadIdx.x; idx < kKeys * D; idx += blockDim.x) {
       int j = idx / D, d = idx % D;
-      bool in = kt + j < hi;
-      ks[j * (D + 1) + d] = in ? to_f32(kc[(size_t)(kt + j) * D + d]) : 0.f;
-      vs[j * D + d] = in ? to_f32(vc[(size_t)(kt + j) * D + d]) : 0.f;
+      ks[j * (D + 1) + d] = kt + j < hi ? to_f32(kc[(size_t)(kt + j) * D + d]) : 0.f;
+    }
+    for (int idx = threadIdx.x; idx < kKeys * Dv; idx += blockDim.x) {
+      int j = idx / Dv, d = idx % Dv;
+      vs[j * Dv + d] = kt + j < hi ? to_f32(vc[(size_t)(kt + j) * Dv + d]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
         if (s2 >= dslots) break;
         const int d = lane + 32 * s2;
         float x = acc[t][s2] * alpha;
-        for (int jj = 0; jj < kKeys; ++jj) x = fmaf(ps[warp * kKeys + jj], vs[jj * D + d], x);
+        for (int jj = 0; jj < kKeys; ++jj) x = fmaf(ps[warp * kKeys + jj], vs[jj * Dv + d], x);
         acc[t][s2] = x;
       }
       __syncwarp();
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
     }
     for (int s2 = 0; s2 < dslots; ++s2) {
       const int d = lane + 32 * s2;
-      out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * D + d] = from_f32<T>(acc[t][s2] * num_scale / den);
+      out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d] = from_f32<T>(acc[t][s2] * num_scale / den);
     }
   }
 }
@@ -169,6 +171,7 @@ template <typename T> gqa_status launch_t(const Call &c) {
   a.Hkv = p.kv_heads;
   a.G = c.G;
   a.D = p.head_dim;
+  a.Dv = c.Dv;
   a.curr = p.q_len;
   a.cap = p.cap_present;
   a.cap_past = p.cap_past;
@@ -187,8 +190,8 @@ template <typename T> gqa_status launch_t(const Call &c) {
   a.msh = c.mask_sh;
   a.msi = c.mask_si;
   const int D = p.head_dim;
-  size_t smem = sizeof(float) * (kRows * D + kKeys * (D + 1) + kKeys * D + 4 * kKeys);
-  // D <= 128: at most 41.5 KB of shared memory, under the 48 KB default limit
+  size_t smem = sizeof(float) * (kRows * D + kKeys * (D + 1) + kKeys * c.Dv + 4 * kKeys);
+  // D, Dv <= 128: at most 41.5 KB of shared memory, under the 48 KB default limit
   dim3 grid((p.q_len + kRows - 1) / kRows, p.q_heads, p.batch);
   attn_simt_kernel<T><<<grid, 128, smem, c.stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;

@@ -5,7 +5,8 @@
 namespace gqa {
 
 gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
-  return launch_decode_split_any<false>(c, dp, wl);
+  if (c.Dv != c.p.head_dim) return launch_decode_split_vdim(c, dp, wl);  // its own translation unit
+  return launch_decode_split_impl<false, false>(c, dp, wl);
 }
 
 }  // namespace gqa

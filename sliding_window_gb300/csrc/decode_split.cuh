@@ -47,13 +47,13 @@ constexpr int kMaxCluster = kDecodeMaxCluster;  // chunks combined through distr
 
 struct DecodeArgs {
   const void *q;          // [B, curr, Hq, D] as given (rotated here when do_rotary)
-  const void *k, *v;      // [B, curr, Hkv, D] new rows, or NULL (attention only)
+  const void *k, *v;      // [B, curr, Hkv, D] / [B, curr, Hkv, DV] new rows, or NULL (attention only)
   const void *cos, *sin;  // [rope_len, D/2]
   void *present_k, *present_v;
-  void *out;              // [B, curr, Hq, D]
+  void *out;              // [B, curr, Hq, DV]
   const int32_t *seqlens;
   const float *head_sink;
-  float *part_acc;      // [B*Hkv][S][R][D]
+  float *part_acc;      // [B*Hkv][S][R][DV]
   float *part_ml;       // [B*Hkv][S][R][2]
   int32_t *tickets;     // [B*Hkv]
   int32_t *status;
@@ -71,9 +71,10 @@ struct DecodeArgs {
   float cap_mul;    // softcap*log2(e), 0 without softcap
 };
 
-template <int D, int MT, int NST> struct Smem {
-  static constexpr int kTileBytes = KT * D * 2;  // one K or V tile
-  static constexpr int kStageBytes = 2 * kTileBytes;
+template <int D, int DV, int MT, int NST> struct Smem {
+  static constexpr int kTileBytes = KT * D * 2;  // one K tile; the V tile follows it
+  static constexpr int kVTileBytes = KT * DV * 2;
+  static constexpr int kStageBytes = kTileBytes + kVTileBytes;
   static constexpr int kQRows = MT * 16;
   static constexpr int kStagesOff = 0;
   static constexpr int kQOff = NST * kStageBytes;
@@ -85,10 +86,10 @@ template <int D, int MT, int NST> struct Smem {
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
   // per-warp merge regions (rows padded by 4 floats: the fragment stores of one warp
   // instruction then spread over all banks) and the combine's chunk statistics reuse the stages
-  static constexpr int kAccStride = D + 4;
+  static constexpr int kAccStride = DV + 4;
   static_assert(kWarps * kQRows * kAccStride * 4 <= NST * kStageBytes, "merge regions must fit in the stages");
   static_assert(2 * kMaxSplits * kQRows * 4 <= NST * kStageBytes, "chunk statistics must fit in the stages");
-  static_assert((kWarps * kQRows * kAccStride + kQRows * D + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <=
+  static_assert((kWarps * kQRows * kAccStride + kQRows * DV + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <=
                     NST * kStageBytes,
                 "cluster exchange buffers must fit in the stages");
 };
@@ -131,46 +132,51 @@ __device__ __forceinline__ void rotate8(const T *x1p, const T *x2p, const T *cp,
 
 // Warp-wide: write the step's rows [r0, r1) of kv head h of sequence b to present (K
 // rotated when do_rotary), then make the generic-proxy stores visible to TMA reads.
-template <typename T, int D>
+template <typename T, int D, int DV>
 __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, int past, int r0, int r1, int lane) {
   const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
   T *pk = reinterpret_cast<T *>(a.present_k), *pv = reinterpret_cast<T *>(a.present_v);
   const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
-  constexpr int per_row = D / 16;  // pairs of 8-element chunks (x[d..], x[d+D/2..]) per row
+  constexpr int kper = D / 16;  // pairs of 8-element chunks (x[d..], x[d+D/2..]) per K row
+  constexpr int vper = DV / 8;  // 8-element chunks per V row
   const int nrows = r1 - r0;
-  for (int w = lane; w < nrows * per_row * 2; w += 32) {
-    const int which = w / (nrows * per_row);  // 0: k, 1: v
-    const int rr = (w / per_row) % nrows, c = (w % per_row) * 8;
+  for (int w = lane; w < nrows * (kper + vper); w += 32) {
+    const bool isk = w < nrows * kper;
+    const int wv = isk ? w : w - nrows * kper, per = isk ? kper : vper;
+    const int rr = wv / per, c = (wv % per) * 8;
     const int pos = r0 + rr, i = pos - past;
-    const size_t src = (((size_t)b * a.curr + i) * a.Hkv + h) * D;
-    const size_t dst =
-        a.table ? (((size_t)a.table[(size_t)b * a.max_pages + pos / KT] * a.Hkv + h) * KT + pos % KT) * D
-                : (((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos)) * D;
-    if (which == 0 && a.do_rotary) {
-      uint4 y1, y2;
-      rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c,
-                 y1, y2);
-      *reinterpret_cast<uint4 *>(pk + dst + c) = y1;
-      *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = y2;
+    const size_t row = a.table ? ((size_t)a.table[(size_t)b * a.max_pages + pos / KT] * a.Hkv + h) * KT + pos % KT
+                               : ((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos);
+    const size_t tok = ((size_t)b * a.curr + i) * a.Hkv + h;
+    if (isk) {
+      const size_t src = tok * D, dst = row * D;
+      if (a.do_rotary) {
+        uint4 y1, y2;
+        rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c,
+                   sn + (size_t)pos * (D / 2) + c, y1, y2);
+        *reinterpret_cast<uint4 *>(pk + dst + c) = y1;
+        *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = y2;
+      } else {
+        *reinterpret_cast<uint4 *>(pk + dst + c) = *reinterpret_cast<const uint4 *>(kin + src + c);
+        *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(kin + src + D / 2 + c);
+      }
     } else {
-      const T *x = which == 0 ? kin : vin;
-      T *y = which == 0 ? pk : pv;
-      *reinterpret_cast<uint4 *>(y + dst + c) = *reinterpret_cast<const uint4 *>(x + src + c);
-      *reinterpret_cast<uint4 *>(y + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(x + src + D / 2 + c);
+      *reinterpret_cast<uint4 *>(pv + row * DV + c) = *reinterpret_cast<const uint4 *>(vin + tok * DV + c);
     }
   }
   fence_proxy_async_global();
   __syncwarp();
 }
 
-template <typename T, int D, int MT, int NST, bool CL, bool MK>
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         DecodeArgs a) {
-  using L = Smem<D, MT, NST>;
+  using L = Smem<D, DV, MT, NST>;
   using M = Mma16816<T>;
   constexpr int QROWS = L::kQRows;
-  constexpr int DCH = D / 8;  // 16-byte chunks per row
+  constexpr int DCH = D / 8;    // 16-byte chunks per q / K row
+  constexpr int VCH = DV / 8;   // 16-byte chunks per V row
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *stages = smem + L::kStagesOff;
@@ -230,9 +236,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (st) {  // rejected sequence: zeros, nothing appended, reported once
     if (split == 0) {
       if (threadIdx.x == 0 && hkv == 0) report(a.status, st);
-      for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
-        const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
-        out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
+      for (int idx = threadIdx.x; idx < R * DV; idx += kThreads) {
+        const int r = idx / DV, d = idx % DV, i = r / a.G, g = r % a.G;
+        out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d] = from_f32<T>(0.f);
       }
     }
     return;
@@ -251,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (__syncthreads_or(bad)) {
       if (split == 0) {
         if (threadIdx.x == 0 && hkv == 0) report(a.status, GQA_DEV_BAD_PAGE);
-        for (int idx = threadIdx.x; idx < R * D; idx += kThreads) {
-          const int r = idx / D, d = idx % D, i = r / a.G, g = r % a.G;
-          out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * D + d] = from_f32<T>(0.f);
+        for (int idx = threadIdx.x; idx < R * DV; idx += kThreads) {
+          const int r = idx / DV, d = idx % DV, i = r / a.G, g = r % a.G;
+          out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d] = from_f32<T>(0.f);
         }
       }
       return;
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto issue = [&](int t) {
     const int s = t % NST, k0 = c0 + t * KT;
     if (appends && k0 + KT > past && k0 < total)
-      append_rows<T, D>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane);
+      append_rows<T, D, DV>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane);
     if (lane == 0) {
       mbar_expect_tx(&full[s], L::kStageBytes);
       uint8_t *kdst = stages + s * L::kStageBytes;
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         group = a.table[(size_t)b * a.max_pages + k0 / KT] * a.Hkv + hkv;
         row = 0;
       }
-      tma_load_4d(kdst, &tmk, 0, row, 0, group, &full[s]);  // [D/64][KT][64], one copy each
+      tma_load_4d(kdst, &tmk, 0, row, 0, group, &full[s]);  // [D/64][KT][64], [DV/64][KT][64]: one copy each
       tma_load_4d(vdst, &tmv, 0, row, 0, group, &full[s]);
     }
     __syncwarp();
@@ -319,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
 
   float m[MT][2], l[MT][2];
-  float acc[MT][D / 8][4];
+  float acc[MT][DV / 8][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       l[mt][h] = 0.f;
     }
 #pragma unroll
-    for (int dn = 0; dn < D / 8; ++dn)
+    for (int dn = 0; dn < DV / 8; ++dn)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][dn][e] = 0.f;
   }
@@ -462,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float alpha = ex2(m[mt][h] - mx);  // 0 while nothing was visible
           l[mt][h] *= alpha;
 #pragma unroll
-          for (int dn = 0; dn < D / 8; ++dn) {
+          for (int dn = 0; dn < DV / 8; ++dn) {
             acc[mt][dn][2 * h] *= alpha;
             acc[mt][dn][2 * h + 1] *= alpha;
           }
@@ -488,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool stale = kb + 16 > total;
     if (stale) {
       const int first = max(0, total - kb);
-      for (int idx = lane; idx < (16 - first) * DCH; idx += 32) {
-        const int r = 16 * warp + first + idx / DCH, ch = idx % DCH;
+      for (int idx = lane; idx < (16 - first) * VCH; idx += 32) {
+        const int r = 16 * warp + first + idx / VCH, ch = idx % VCH;
         *reinterpret_cast<uint4 *>(stages + s * L::kStageBytes + L::kTileBytes + (ch >> 3) * (KT * 128) +
                                    sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
       }
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---- O += P V over this warp's 16 keys
 #pragma unroll
-    for (int dd = 0; dd < D / 16; ++dd) {
+    for (int dd = 0; dd < DV / 16; ++dd) {
       uint32_t v0, v1, v2, v3;
       const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
       const int vch = 2 * dd + (lane >> 4);
@@ -602,12 +608,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
       float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane & 3);
 #pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn)
+      for (int dn = 0; dn < DV / 8; ++dn)
         *reinterpret_cast<float2 *>(dst + 8 * dn) = make_float2(acc[mt][dn][2 * h] * f, acc[mt][dn][2 * h + 1] * f);
     }
   __syncthreads();
-  auto merged = [&](int idx4) {  // float4 idx4 of the CTA's [R][D] accumulator
-    const float4 *w4 = reinterpret_cast<const float4 *>(wacc) + (idx4 / (D / 4)) * (AST / 4) + idx4 % (D / 4);
+  auto merged = [&](int idx4) {  // float4 idx4 of the CTA's [R][DV] accumulator
+    const float4 *w4 = reinterpret_cast<const float4 *>(wacc) + (idx4 / (DV / 4)) * (AST / 4) + idx4 % (DV / 4);
     float4 v = w4[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) {
@@ -622,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (nchunks == 1) {
     // ------------------------------------------------------------ finish in place
-    for (int idx = threadIdx.x; idx < R * (D / 4); idx += kThreads) {
-      const int r = idx / (D / 4), d4 = idx % (D / 4);
+    for (int idx = threadIdx.x; idx < R * (DV / 4); idx += kThreads) {
+      const int r = idx / (DV / 4), d4 = idx % (DV / 4);
       const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
       const float mm = row_m[r];
       float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -643,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         num.w *= f;
         den = row_l[r] * f + sink_term;
       }
-      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
       const float inv = __frcp_rn(den);
       store4(o, num.x * inv, num.y * inv, num.z * inv, num.w * inv);
     }
@@ -653,15 +659,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (CL) {
     // ------------------------------------------------------------ cluster exchange
     // the group's chunks are the CTAs of one cluster.  CTA `rank` owns float4 slice
-    // [rank * per, (rank + 1) * per) of the group's [R][D] output; every CTA pushes its
+    // [rank * per, (rank + 1) * per) of the group's [R][DV] output; every CTA pushes its
     // (m, l) rows and the matching slice of its accumulator into the owner's shared memory
     // (after the wacc regions) with asynchronous stores that count down the owner's xbar.
     // The owner waits for exactly those bytes and combines its slice from local data; once
     // they have landed nothing else writes to or reads from its shared memory, so it may exit
     const int S = gridDim.x, rank = split;
-    const int n4 = R * (D / 4), per = (n4 + S - 1) / S;
+    const int n4 = R * (DV / 4), per = (n4 + S - 1) / S;
     float *rcv = wacc + kWarps * QROWS * AST;               // [S][per] float4 slices
-    float2 *rcv_ml = reinterpret_cast<float2 *>(rcv + QROWS * D + 4 * kMaxCluster);  // [S][QROWS] (m, l)
+    float2 *rcv_ml = reinterpret_cast<float2 *>(rcv + QROWS * DV + 4 * kMaxCluster);  // [S][QROWS] (m, l)
     cluster_wait();  // every CTA has finished streaming: its stages may be written
     const uint32_t rcv_s = smem_u32(rcv), rml_s = smem_u32(rcv_ml), xb_s = smem_u32(xbar);
     for (int t = threadIdx.x; t < S * R; t += kThreads) {
@@ -682,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // each output float4 weighs the chunks of its row itself: no second pass, no barrier
     const float4 *rcv4 = reinterpret_cast<const float4 *>(rcv);
     for (int idx = lo4 + threadIdx.x; idx < hi4; idx += kThreads) {
-      const int r = idx / (D / 4), d4 = idx % (D / 4);
+      const int r = idx / (DV / 4), d4 = idx % (DV / 4);
       const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
       float mk[kMaxCluster];
       float top = -INFINITY;
@@ -713,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         den = ll;
       }
-      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+      T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
       const float inv = __frcp_rn(den);
       store4(o, sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
     }
@@ -724,8 +730,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const size_t gbase = (size_t)bh * a.splits * R;
   {
     const size_t base = gbase + (size_t)split * R;
-    float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * D);
-    for (int idx = threadIdx.x; idx < R * D / 4; idx += kThreads) pacc[idx] = merged(idx);
+    float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * DV);
+    for (int idx = threadIdx.x; idx < R * DV / 4; idx += kThreads) pacc[idx] = merged(idx);
     for (int r = threadIdx.x; r < R; r += kThreads)
       reinterpret_cast<float2 *>(a.part_ml)[base + r] = make_float2(row_m[r], row_l[r]);
   }
@@ -770,19 +776,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   // chunk-outer: every thread keeps its outputs in registers and issues one independent
   // load per output per chunk
-  constexpr int kPer = (MT * 16 * D / 4 + kThreads - 1) / kThreads;
+  constexpr int kPer = (MT * 16 * DV / 4 + kThreads - 1) / kThreads;
   float4 sum[kPer];
 #pragma unroll
   for (int u = 0; u < kPer; ++u) sum[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 *pa4 = reinterpret_cast<const float4 *>(a.part_acc + gbase * D);
+  const float4 *pa4 = reinterpret_cast<const float4 *>(a.part_acc + gbase * DV);
 #pragma unroll 4
   for (int c = 0; c < nchunks; ++c) {
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int idx = threadIdx.x + u * kThreads;
-      if (idx < R * (D / 4)) {
-        const float f = cm[c * R + idx / (D / 4)];
-        const float4 v = __ldcg(pa4 + (size_t)c * R * (D / 4) + idx);
+      if (idx < R * (DV / 4)) {
+        const float f = cm[c * R + idx / (DV / 4)];
+        const float4 v = __ldcg(pa4 + (size_t)c * R * (DV / 4) + idx);
         sum[u].x += v.x * f;
         sum[u].y += v.y * f;
         sum[u].z += v.z * f;
@@ -793,28 +799,28 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
     const int idx = threadIdx.x + u * kThreads;
-    if (idx >= R * (D / 4)) continue;
-    const int r = idx / (D / 4), d4 = idx % (D / 4);
+    if (idx >= R * (DV / 4)) continue;
+    const int r = idx / (DV / 4), d4 = idx % (DV / 4);
     const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
     const float den = row_l[r] > 0.f ? row_l[r] : 1.f;  // no visible key: the sums are 0
-    T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * D + d4 * 4;
+    T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
     const float inv = __frcp_rn(den);
     store4(o, sum[u].x * inv, sum[u].y * inv, sum[u].z * inv, sum[u].w * inv);
   }
 }
 
-template <typename T, int D, int MT, int NST, bool CL, bool MK>
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK>
 gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
-  using L = Smem<D, MT, NST>;
+  using L = Smem<D, DV, MT, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
   CUtensorMap tk, tv;
-  // contiguous or ring: [B*Hkv][cap][D]; paged: [num_pages*Hkv][64][D]
+  // contiguous or ring: [B*Hkv][cap][D] and [..][DV]; paged: [num_pages*Hkv][64][D]
   const bool paged = c.block_table != nullptr;
   const long long outer = paged ? (long long)c.num_pages * c.p.kv_heads : (long long)c.p.batch * c.p.kv_heads;
   const int rows = paged ? KT : c.p.cap_present;
   if (!encode_kv_tile_map(&tk, c.present_k, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
-  if (!encode_kv_tile_map(&tv, c.present_v, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
-  auto kern = decode_split_kernel<T, D, MT, NST, CL, MK>;
+  if (!encode_kv_tile_map(&tv, c.present_v, DV, rows, outer, KT, 2)) return GQA_ERR_CUDA;
+  auto kern = decode_split_kernel<T, D, DV, MT, NST, CL, MK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -838,9 +844,10 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-template <typename T, bool CL, bool MK> gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a);
+template <typename T, bool CL, bool MK, bool MIXED>
+gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a);
 
-template <typename T, bool MK> gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
+template <typename T, bool MK, bool MIXED> gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   const gqa_params &p = c.p;
   DecodeArgs a;
   a.q = c.q_in;
@@ -890,29 +897,43 @@ template <typename T, bool MK> gqa_status launch_t(const Call &c, const DecodePl
     a.score_mul = p.scale * kLog2e;
     a.cap_mul = 0.f;
   }
-  if (dp.cluster) return dispatch<T, true, MK>(c, dp, a);
-  return dispatch<T, false, MK>(c, dp, a);
+  if (dp.cluster) return dispatch<T, true, MK, MIXED>(c, dp, a);
+  return dispatch<T, false, MK, MIXED>(c, dp, a);
 }
 
-template <typename T, bool CL, bool MK> gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
-  if (c.p.head_dim == 128) {
-    if (dp.mtiles == 1) return launch_cfg<T, 128, 1, 3, CL, MK>(c, dp, a);
-    if (dp.mtiles == 2) return launch_cfg<T, 128, 2, 3, CL, MK>(c, dp, a);
-  } else if (c.p.head_dim == 64) {
-    if (dp.mtiles == 1) return launch_cfg<T, 64, 1, 6, CL, MK>(c, dp, a);
-    if (dp.mtiles == 2) return launch_cfg<T, 64, 2, 6, CL, MK>(c, dp, a);
-    if (dp.mtiles == 3) return launch_cfg<T, 64, 3, 6, CL, MK>(c, dp, a);
-    if (dp.mtiles == 4) return launch_cfg<T, 64, 4, 6, CL, MK>(c, dp, a);
+// (D, DV, MT, NST): equal head dims (MIXED false) or V head dim != Q/K head dim (MIXED true,
+// up to 32 query rows per group; four stages of 24 KB)
+template <typename T, bool CL, bool MK, bool MIXED>
+gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
+  const int D = c.p.head_dim, DV = c.Dv;
+  if constexpr (!MIXED) {
+    if (D == 128 && DV == 128) {
+      if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 3, CL, MK>(c, dp, a);
+      if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 3, CL, MK>(c, dp, a);
+    } else if (D == 64 && DV == 64) {
+      if (dp.mtiles == 1) return launch_cfg<T, 64, 64, 1, 6, CL, MK>(c, dp, a);
+      if (dp.mtiles == 2) return launch_cfg<T, 64, 64, 2, 6, CL, MK>(c, dp, a);
+      if (dp.mtiles == 3) return launch_cfg<T, 64, 64, 3, 6, CL, MK>(c, dp, a);
+      if (dp.mtiles == 4) return launch_cfg<T, 64, 64, 4, 6, CL, MK>(c, dp, a);
+    }
+  } else {
+    if (D == 128 && DV == 64) {
+      if (dp.mtiles == 1) return launch_cfg<T, 128, 64, 1, 4, CL, MK>(c, dp, a);
+      if (dp.mtiles == 2) return launch_cfg<T, 128, 64, 2, 4, CL, MK>(c, dp, a);
+    } else if (D == 64 && DV == 128) {
+      if (dp.mtiles == 1) return launch_cfg<T, 64, 128, 1, 4, CL, MK>(c, dp, a);
+      if (dp.mtiles == 2) return launch_cfg<T, 64, 128, 2, 4, CL, MK>(c, dp, a);
+    }
   }
   return GQA_ERR_UNSUPPORTED;
 }
 
-// The decode launch for one dtype switch; each .cu file instantiates one MK (masked or
-// not), so the two sets of kernels compile in parallel.
-template <bool MK> gqa_status launch_decode_split_any(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
+// The decode launch for one dtype switch; each .cu file instantiates one (MK, MIXED) pair
+// (masked or not, equal or different head dims), so the sets compile in parallel.
+template <bool MK, bool MIXED> gqa_status launch_decode_split_impl(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   switch (c.p.dtype) {
-    case GQA_F16: return launch_t<__half, MK>(c, dp, wl);
-    case GQA_BF16: return launch_t<__nv_bfloat16, MK>(c, dp, wl);
+    case GQA_F16: return launch_t<__half, MK, MIXED>(c, dp, wl);
+    case GQA_BF16: return launch_t<__nv_bfloat16, MK, MIXED>(c, dp, wl);
   }
   return GQA_ERR_UNSUPPORTED;
 }

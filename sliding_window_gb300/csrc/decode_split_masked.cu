@@ -6,7 +6,8 @@
 namespace gqa {
 
 gqa_status launch_decode_split_masked(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
-  return launch_decode_split_any<true>(c, dp, wl);
+  if (c.Dv != c.p.head_dim) return launch_decode_split_vdim(c, dp, wl);  // its own translation unit
+  return launch_decode_split_impl<true, false>(c, dp, wl);
 }
 
 }  // namespace gqa

@@ -35,6 +35,9 @@ gqa_status check_params(const gqa_params *p) {
   if ((p->rotary_interleaved | 1) != 1 || (p->kv_ring | 1) != 1) return GQA_ERR_INVALID_ARG;
   if (p->rotary_interleaved) return GQA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return GQA_ERR_UNSUPPORTED;
+  if (p->v_head_dim < 0) return GQA_ERR_INVALID_ARG;
+  if (p->v_head_dim != 0 && p->v_head_dim != 64 && p->v_head_dim != 128) return GQA_ERR_UNSUPPORTED;
+  if (p->kv_ring && p->v_head_dim != 0 && p->v_head_dim != p->head_dim) return GQA_ERR_UNSUPPORTED;
   if (p->cap_present < p->q_len || p->cap_past < 0) return GQA_ERR_CAPACITY;
   if (p->do_rotary && p->rope_len < 1) return GQA_ERR_INVALID_ARG;
   if (p->kv_ring) {  // position p in slot p % cap: every key the step sees must still be resident
@@ -140,8 +143,10 @@ DecodePlan decode_plan(const gqa_params &p) {
   const int G = p.q_heads / p.kv_heads;
   d.rows = G * p.q_len;
   d.mtiles = (d.rows + 15) / 16;
+  const int dv = p.v_head_dim ? p.v_head_dim : p.head_dim;
   d.eligible = p.dtype != GQA_F32 &&
-               ((p.head_dim == 128 && d.mtiles <= 2) || (p.head_dim == 64 && d.mtiles <= 4));
+               (dv != p.head_dim ? d.mtiles <= 2  // different V head dim: up to 32 rows per group
+                                 : (p.head_dim == 128 && d.mtiles <= 2) || (p.head_dim == 64 && d.mtiles <= 4));
   // longest visible band of one group: [max(0, past - W + 1), past + curr)
   long long lmax = p.cap_present;
   if (p.window > 0) lmax = std::min<long long>(lmax, (long long)p.window + p.q_len - 1);
@@ -174,7 +179,7 @@ WsLayout workspace_layout(const gqa_params &p, bool need_q_rot) {
     const size_t groups = (size_t)p.batch * p.kv_heads;
     const size_t slots = groups * d.splits;
     w.part_acc_off = off;
-    w.part_acc_bytes = slots * d.rows * p.head_dim * sizeof(float);
+    w.part_acc_bytes = slots * d.rows * (p.v_head_dim ? p.v_head_dim : p.head_dim) * sizeof(float);
     off = align_up(off + w.part_acc_bytes, kAlign);
     w.part_ml_off = off;
     w.part_ml_bytes = slots * d.rows * 2 * sizeof(float);
@@ -201,6 +206,7 @@ gqa_status make_call(Call &c, const gqa_params *p, const void *q, const void *k,
   c.p = *p;
   if (c.p.scale == 0.f) c.p.scale = 1.f / sqrtf((float)p->head_dim);
   c.G = p->q_heads / p->kv_heads;
+  c.Dv = p->v_head_dim ? p->v_head_dim : p->head_dim;
   c.esize = p->dtype == GQA_F32 ? 4 : 2;
   if (!q || !seqlens_k || !present_k || !present_v) return GQA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(present_k) || !aligned16(present_v)) return GQA_ERR_INVALID_ARG;
@@ -252,7 +258,7 @@ bool mask_tma_ok(const Call &c) {
   const long long lim = 1ll << 39;
   return (reinterpret_cast<uintptr_t>(c.mask) & 15u) == 0 && (c.mask_si * es) % 16 == 0 &&
          (c.mask_sh * es) % 16 == 0 && (c.mask_sb * es) % 16 == 0 && c.mask_si * es < lim && c.mask_sh * es < lim &&
-         c.mask_sb * es < lim && (c.p.head_dim == 128 || c.p.head_dim == 64);
+         c.mask_sb * es < lim && (c.p.head_dim == 128 || c.p.head_dim == 64) && c.Dv == c.p.head_dim;
 }
 
 gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const void *k, const void *v,
@@ -369,6 +375,7 @@ gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const 
                                 k_pool, v_pool, dev_status, stream);
   if (s != GQA_OK) return s;
   if (p->kv_ring) return GQA_ERR_INVALID_ARG;
+  if (c.Dv != p->head_dim) return GQA_ERR_UNSUPPORTED;  // pages hold K and V rows of one width
   if (!block_table || (reinterpret_cast<uintptr_t>(block_table) & 3u)) return GQA_ERR_INVALID_ARG;
   if (max_pages < 1 || num_pages < 1) return GQA_ERR_INVALID_ARG;
   if ((long long)max_pages * 64 != p->cap_present) return GQA_ERR_CAPACITY;

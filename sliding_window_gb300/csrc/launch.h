@@ -15,6 +15,7 @@ struct Call {
   gqa_params p;          // scale already resolved (0 -> 1/sqrt(D))
   int G = 1;             // q heads per kv head
   int esize = 2;         // bytes per element
+  int Dv = 0;            // V head dim (v_head_dim, or head_dim when 0)
   const void *q = nullptr;        // query as it enters the scores (input q or q_rot)
   const void *q_in = nullptr;     // caller's q (before rotation)
   const void *k = nullptr, *v = nullptr;
@@ -89,7 +90,9 @@ gqa_status launch_copy_past(const Call &c);  // rows [0, past_b) of past into pr
 gqa_status launch_attention_simt(const Call &c);
 gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_decode_split_masked(const Call &c, const DecodePlan &dp, const WsLayout &wl);
+gqa_status launch_decode_split_vdim(const Call &c, const DecodePlan &dp, const WsLayout &wl);  // Dv != D
 gqa_status launch_prefill_tc(const Call &c);
 gqa_status launch_prefill_tc_masked(const Call &c);  // c.mask set: kind 1 or 2
+gqa_status launch_prefill_tc_vdim(const Call &c);    // Dv != D, no mask
 
 }  // namespace gqa

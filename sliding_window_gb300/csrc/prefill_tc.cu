@@ -4,6 +4,9 @@
 
 namespace gqa {
 
-gqa_status launch_prefill_tc(const Call &c) { return launch_prefill_tc_any<0>(c); }
+gqa_status launch_prefill_tc(const Call &c) {
+  if (c.Dv != c.p.head_dim) return launch_prefill_tc_vdim(c);  // its own translation unit
+  return launch_prefill_tc_any<0, false>(c);
+}
 
 }  // namespace gqa

@@ -11,7 +11,8 @@
 //   warp 0  producer: TMA loads of the Q tile once, then one K and one V tile (128 keys,
 //           128B swizzle) per step, each into a single buffer released by tcgen05.commit
 //   warp 1  TMEM owner + MMA issuer (one thread): S = Q K^T (M=128, N=128, K=D) into TMEM,
-//           then O += P V with P read from TMEM (it overwrites S in place, bf16 pairs)
+//           then O += P V (N = DV, the V head dim) with P read from TMEM (it overwrites S in
+//           place, bf16 pairs)
 //   warps 2-5  softmax: thread = one TMEM lane = one query row; tcgen05.ld of S, band mask
 //           on frontier tiles only, scale/softcap, exp2 online softmax with a lazily
 //           rescaled reference max, P back to TMEM with tcgen05.st, final O / l epilogue
@@ -55,18 +56,20 @@ struct PrefillArgs {
   float bias_mul;  // 1 / scale: an additive value joins the raw dot product before scaling
 };
 
-template <int D, int MK> struct PSmem {
-  static constexpr int kTile = BM * D * 2;  // one Q, K or V tile
+template <int D, int DV, int MK> struct PSmem {
+  static constexpr int kTile = BM * D * 2;    // one Q or K tile
+  static constexpr int kVTile = BN * DV * 2;  // one V tile
   static constexpr int kMaskTile = MK == 1 ? BM * BN : MK >= 2 ? BM * BN * 2 : 0;  // one buffer
   static constexpr int kMaskRing = MK == 3 ? 2 : 1;  // shared tiles in flight (MK 3)
   static constexpr int kMaskBufs = MK == 3 ? kMaskRing : 2;
-  // the K ring gives up a stage when the mask buffers need more than 32 KB at D = 128
-  static constexpr int kKStages = (D == 128 && kMaskBufs * kMaskTile > 32 * 1024) ? 1 : 2;
+  // the K ring gives up a stage when two would not leave room for the mask buffers
+  static constexpr int kKStages =
+      (4 * kTile + 2 * kVTile + kMaskBufs * kMaskTile + 2048 > 227 * 1024) ? 1 : 2;
   static constexpr int kQA = 0;
   static constexpr int kQB = kQA + kTile;
   static constexpr int kK = kQB + kTile;
   static constexpr int kV = kK + kKStages * kTile;  // two stages
-  static constexpr int kM = kV + 2 * kTile;         // mask tiles of heads A and B
+  static constexpr int kM = kV + 2 * kVTile;        // mask tiles
   static constexpr int kBar = kM + kMaskBufs * kMaskTile;
   static constexpr int kTmemSlot = kBar + 24 * 8;
   static constexpr int kFlag = kTmemSlot + 8;
@@ -208,12 +211,12 @@ enum {
 };
 static_assert(B_COUNT <= 24, "barrier region");
 
-template <typename T, int D, bool SOFTCAP, int MK>
+template <typename T, int D, int DV, bool SOFTCAP, int MK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmm,
                       PrefillArgs a) {
-  using L = PSmem<D, MK>;
+  using L = PSmem<D, DV, MK>;
   constexpr int KST = L::kKStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -237,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nrows = min(BM, a.curr - q0);
   if (st) {
     if (threadIdx.x == 0 && qt == 0 && blockIdx.x == 0) report(a.status, st);
-    for (int idx = threadIdx.x; idx < (has_b ? 2 : 1) * nrows * D; idx += blockDim.x) {
-      const int hh = idx / (nrows * D), r = (idx / D) % nrows, d = idx % D;
-      out[(((size_t)b * a.curr + q0 + r) * a.Hq + hA + hh) * D + d] = from_f32<T>(0.f);
+    for (int idx = threadIdx.x; idx < (has_b ? 2 : 1) * nrows * DV; idx += blockDim.x) {
+      const int hh = idx / (nrows * DV), r = (idx / DV) % nrows, d = idx % DV;
+      out[(((size_t)b * a.curr + q0 + r) * a.Hq + hA + hh) * DV + d] = from_f32<T>(0.f);
     }
     return;
   }
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+D) O_B [384,384+D); P_X overwrites
+  // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+DV) O_B [384,384+DV); P_X overwrites
   // the first 64 columns of S_X as packed pairs
   int kissued = 0, vissued = 0;      // producer thread: TMA tiles issued
   int missued[2] = {0, 0};           // mask producer thread: loads issued per buffer
@@ -289,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + L::kK + sk * L::kTile + db * (BN * 128), &tmk, db * 64, k0, bh, &bars[B_KFULL0 + sk]);
         ++kissued;
         if (t >= 2 && !mbar_wait(&bars[B_VEMPTY0 + s], ((t >> 1) - 1) & 1, abort_flag)) break;
-        mbar_expect_tx(&bars[B_VFULL0 + s], L::kTile);
+        mbar_expect_tx(&bars[B_VFULL0 + s], L::kVTile);
 #pragma unroll
-        for (int db = 0; db < D / 64; ++db)
-          tma_load_3d(smem + L::kV + s * L::kTile + db * (BN * 128), &tmv, db * 64, k0, bh, &bars[B_VFULL0 + s]);
+        for (int db = 0; db < DV / 64; ++db)
+          tma_load_3d(smem + L::kV + s * L::kVTile + db * (BN * 128), &tmv, db * 64, k0, bh, &bars[B_VFULL0 + s]);
         ++vissued;
       }
     }
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t qa = smem_u32(smem + L::kQA), qb = smem_u32(smem + L::kQB);
     const uint32_t kbase = smem_u32(smem + L::kK), vbase = smem_u32(smem + L::kV);
     constexpr uint32_t id_s = idesc<T>(BM, BN, false);
-    constexpr uint32_t id_pv = idesc<T>(BM, D, true);
+    constexpr uint32_t id_pv = idesc<T>(BM, DV, true);
     auto issue_s = [&](int t, uint32_t q_s, uint32_t d_tmem) {
       const uint32_t ks = kbase + (t % KST) * L::kTile;
 #pragma unroll
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     auto issue_pv = [&](int t, uint32_t p_tmem, uint32_t o_tmem) {
-      const uint32_t vs = vbase + (t & 1) * L::kTile;
+      const uint32_t vs = vbase + (t & 1) * L::kVTile;
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
         mma_ts(o_tmem, p_tmem + kk * 8, sdesc(vs + kk * 2048, BN * 128, 1024), id_pv, (t > 0 || kk > 0) ? 1u : 0u);
@@ -364,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL0 + s], (t >> 1) & 1, abort_flag))) break;
       if (k0 + BN > total) {  // stale slots may hold NaN/Inf: zero those V rows
         const int first = max(0, total - k0);
-        uint8_t *vb = smem + L::kV + s * L::kTile;
-        for (int idx = lane; idx < (BN - first) * (D / 8); idx += 32) {
-          const int r = first + idx / (D / 8), ch = idx % (D / 8);
+        uint8_t *vb = smem + L::kV + s * L::kVTile;
+        for (int idx = lane; idx < (BN - first) * (DV / 8); idx += 32) {
+          const int r = first + idx / (DV / 8), ch = idx % (DV / 8);
           *reinterpret_cast<uint4 *>(vb + (ch >> 3) * (BN * 128) + sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DV / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait();
@@ -581,9 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__all_sync(0xffffffffu, fin)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      T *orow = out + (((size_t)b * a.curr + q0 + row) * a.Hq + hq) * D;
+      T *orow = out + (((size_t)b * a.curr + q0 + row) * a.Hq + hq) * DV;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait();
@@ -631,15 +634,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D, bool SC, int MK> gqa_status launch_cfg(const Call &c, const PrefillArgs &a) {
-  using L = PSmem<D, MK>;
+template <typename T, int D, int DV, bool SC, int MK> gqa_status launch_cfg(const Call &c, const PrefillArgs &a) {
+  using L = PSmem<D, DV, MK>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory per CTA");
   const gqa_params &p = c.p;
   CUtensorMap tq, tk, tv, tm;
   const long long outer = (long long)p.batch * p.kv_heads;
   if (!encode_q_map(&tq, c.q, D, p.q_heads, p.q_len, p.batch, BM, 2)) return GQA_ERR_CUDA;
   if (!encode_kv_map(&tk, c.present_k, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
-  if (!encode_kv_map(&tv, c.present_v, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_map(&tv, c.present_v, DV, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
   if (MK) {
     const int es = MK >= 2 ? 2 : 1;
     if (!encode_mask_map(&tm, c.mask, c.mask_keys, p.q_len, p.q_heads, p.batch, c.mask_si * es, c.mask_sh * es,
@@ -648,7 +651,7 @@ template <typename T, int D, bool SC, int MK> gqa_status launch_cfg(const Call &
   } else {
     tm = tq;  // unused
   }
-  auto kern = prefill_tc_kernel<T, D, SC, MK>;
+  auto kern = prefill_tc_kernel<T, D, DV, SC, MK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
   const int pairs = p.kv_heads * ((c.G + 1) / 2);
@@ -657,7 +660,7 @@ template <typename T, int D, bool SC, int MK> gqa_status launch_cfg(const Call &
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-template <typename T, int MK> gqa_status launch_t(const Call &c) {
+template <typename T, int MK, bool MIXED> gqa_status launch_t(const Call &c) {
   const gqa_params &p = c.p;
   PrefillArgs a;
   a.out = c.out;
@@ -689,15 +692,22 @@ template <typename T, int MK> gqa_status launch_t(const Call &c) {
     a.score_mul = p.scale * kLog2e;
     a.cap_mul = 0.f;
   }
-  if (p.head_dim == 128) return sc ? launch_cfg<T, 128, true, MK>(c, a) : launch_cfg<T, 128, false, MK>(c, a);
-  if (p.head_dim == 64) return sc ? launch_cfg<T, 64, true, MK>(c, a) : launch_cfg<T, 64, false, MK>(c, a);
+  const int D = p.head_dim, DV = c.Dv;
+  if constexpr (!MIXED) {
+    if (D == 128 && DV == 128) return sc ? launch_cfg<T, 128, 128, true, MK>(c, a) : launch_cfg<T, 128, 128, false, MK>(c, a);
+    if (D == 64 && DV == 64) return sc ? launch_cfg<T, 64, 64, true, MK>(c, a) : launch_cfg<T, 64, 64, false, MK>(c, a);
+  } else {  // V head dim != Q/K head dim
+    if (D == 128 && DV == 64) return sc ? launch_cfg<T, 128, 64, true, MK>(c, a) : launch_cfg<T, 128, 64, false, MK>(c, a);
+    if (D == 64 && DV == 128) return sc ? launch_cfg<T, 64, 128, true, MK>(c, a) : launch_cfg<T, 64, 128, false, MK>(c, a);
+  }
   return GQA_ERR_UNSUPPORTED;
 }
 
-template <int MK> gqa_status launch_prefill_tc_any(const Call &c) {
+// one dtype switch per (MK, MIXED); each .cu file instantiates its own set
+template <int MK, bool MIXED> gqa_status launch_prefill_tc_any(const Call &c) {
   switch (c.p.dtype) {
-    case GQA_F16: return launch_t<__half, MK>(c);
-    case GQA_BF16: return launch_t<__nv_bfloat16, MK>(c);
+    case GQA_F16: return launch_t<__half, MK, MIXED>(c);
+    case GQA_BF16: return launch_t<__nv_bfloat16, MK, MIXED>(c);
   }
   return GQA_ERR_UNSUPPORTED;
 }

@@ -6,10 +6,10 @@
 namespace gqa {
 
 gqa_status launch_prefill_tc_masked(const Call &c) {
-  if (c.mask_kind == GQA_MASK_KEEP) return launch_prefill_tc_any<1>(c);
+  if (c.mask_kind == GQA_MASK_KEEP) return launch_prefill_tc_any<1, false>(c);
   // a head-broadcast additive mask is staged once for both heads of a CTA (MK 3), which
   // leaves the K ring its two stages
-  if (c.mask_kind == GQA_MASK_ADD) return c.mask_sh == 0 ? launch_prefill_tc_any<3>(c) : launch_prefill_tc_any<2>(c);
+  if (c.mask_kind == GQA_MASK_ADD) return c.mask_sh == 0 ? launch_prefill_tc_any<3, false>(c) : launch_prefill_tc_any<2, false>(c);
   return GQA_ERR_INVALID_ARG;
 }
 

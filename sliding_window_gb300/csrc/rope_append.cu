@@ -51,12 +51,13 @@ struct RopeArgs {
   void *q_rot, *present_k, *present_v;
   const int32_t *seqlens;
   int32_t *status;
-  int B, Hq, Hkv, D, curr, cap_present, cap_past, rope_len, do_rotary, past_separate;
+  int B, Hq, Hkv, D, Dv, curr, cap_present, cap_past, rope_len, do_rotary, past_separate;
   int ring;  // present is a ring: position p in slot p % cap_present
 };
 
-// One block per (b, i).  Work items: (head, chunk) over Hq q heads (when q_rot is wanted),
-// Hkv k heads and Hkv v heads; each item handles N elements of each half of the row.
+// One block per (b, i).  Work items: (head, chunk) over Hq q heads (when q_rot is wanted)
+// and Hkv k heads, each N elements of each half of the row; then (v head, chunk) over Hkv
+// v heads, N elements of a row of Dv each.
 template <typename T>
 __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
   constexpr int N = Vec<T>::N;
@@ -73,10 +74,19 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
   const int half = a.D / 2;
   const int per_head = half / N;
   const int nq = a.q_rot ? a.Hq : 0;
-  const int items = (nq + 2 * a.Hkv) * per_head;
+  const int items_qk = (nq + a.Hkv) * per_head, v_per_head = a.Dv / N;
+  const int items = items_qk + a.Hkv * v_per_head;
   const T *cosr = reinterpret_cast<const T *>(a.cos) + (size_t)pos * half;
   const T *sinr = reinterpret_cast<const T *>(a.sin) + (size_t)pos * half;
+  const size_t slot = a.ring ? pos % a.cap_present : pos;
   for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    if (it >= items_qk) {  // v: a plain copy of one 16-byte chunk
+      const int h = (it - items_qk) / v_per_head, c = ((it - items_qk) % v_per_head) * N;
+      const T *src = reinterpret_cast<const T *>(a.v) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.Dv;
+      T *dst = reinterpret_cast<T *>(a.present_v) + (((size_t)b * a.Hkv + h) * a.cap_present + slot) * a.Dv;
+      *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<const uint4 *>(src + c);
+      continue;
+    }
     int head = it / per_head;
     int c = (it % per_head) * N;
     const T *src;
@@ -87,14 +97,9 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
       src = reinterpret_cast<const T *>(a.q) + off;
       dst = reinterpret_cast<T *>(a.q_rot) + off;
     } else {
-      head -= nq;
-      bool is_v = head >= a.Hkv;
-      int h = is_v ? head - a.Hkv : head;
-      size_t off = (((size_t)b * a.curr + i) * a.Hkv + h) * a.D;
-      src = reinterpret_cast<const T *>(is_v ? a.v : a.k) + off;
-      dst = reinterpret_cast<T *>(is_v ? a.present_v : a.present_k) +
-            (((size_t)b * a.Hkv + h) * a.cap_present + (a.ring ? pos % a.cap_present : pos)) * a.D;
-      rot = rot && !is_v;
+      const int h = head - nq;
+      src = reinterpret_cast<const T *>(a.k) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.D;
+      dst = reinterpret_cast<T *>(a.present_k) + (((size_t)b * a.Hkv + h) * a.cap_present + slot) * a.D;
     }
     if (rot) {
       rotate_chunk<T>(src + c, src + half + c, cosr + c, sinr + c, dst + c, dst + half + c);
@@ -112,22 +117,24 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
 template <typename T>
 __global__ void __launch_bounds__(256) copy_past_words_kernel(const uint4 *past_k, const uint4 *past_v, uint4 *pres_k,
                                                               uint4 *pres_v, const int32_t *seqlens, int Hkv,
-                                                              int cap_past, int cap_present, int D, int curr,
-                                                              int rope_len, int do_rotary) {
+                                                              int cap_past, int cap_present, int D, int Dv,
+                                                              int curr, int rope_len, int do_rotary) {
   constexpr int N = 16 / sizeof(T);
   const int bh = blockIdx.x;
   const int b = bh / Hkv;
   const int past = seqlens[b];
   if (sequence_status(past, curr, cap_present, cap_past, 1, do_rotary, rope_len)) return;
-  const size_t row_words = (size_t)D / N;
-  const size_t words = (size_t)past * row_words;
-  const uint4 *sk = past_k + (size_t)bh * cap_past * row_words;
-  const uint4 *sv = past_v + (size_t)bh * cap_past * row_words;
-  uint4 *dk = pres_k + (size_t)bh * cap_present * row_words;
-  uint4 *dv = pres_v + (size_t)bh * cap_present * row_words;
+  const size_t kw = (size_t)D / N, vw = (size_t)Dv / N;  // 16-byte words per K / V row
+  const size_t kwords = (size_t)past * kw, words = kwords + (size_t)past * vw;
+  const uint4 *sk = past_k + (size_t)bh * cap_past * kw;
+  const uint4 *sv = past_v + (size_t)bh * cap_past * vw;
+  uint4 *dk = pres_k + (size_t)bh * cap_present * kw;
+  uint4 *dv = pres_v + (size_t)bh * cap_present * vw;
   for (size_t w = (size_t)blockIdx.y * blockDim.x + threadIdx.x; w < words; w += (size_t)gridDim.y * blockDim.x) {
-    dk[w] = sk[w];
-    dv[w] = sv[w];
+    if (w < kwords)
+      dk[w] = sk[w];
+    else
+      dv[w - kwords] = sv[w - kwords];
   }
 }
 
@@ -137,7 +144,7 @@ template <typename T> static gqa_status launch_copy_t(const Call &c) {
   copy_past_words_kernel<T><<<grid, 256, 0, c.stream>>>(
       reinterpret_cast<const uint4 *>(c.past_k), reinterpret_cast<const uint4 *>(c.past_v),
       reinterpret_cast<uint4 *>(c.present_k), reinterpret_cast<uint4 *>(c.present_v), c.seqlens, p.kv_heads,
-      p.cap_past, p.cap_present, p.head_dim, p.q_len, p.rope_len, p.do_rotary);
+      p.cap_past, p.cap_present, p.head_dim, c.Dv, p.q_len, p.rope_len, p.do_rotary);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -158,6 +165,7 @@ template <typename T> static gqa_status launch_t(const Call &c) {
   a.Hq = p.q_heads;
   a.Hkv = p.kv_heads;
   a.D = p.head_dim;
+  a.Dv = c.Dv;
   a.curr = p.q_len;
   a.cap_present = p.cap_present;
   a.ring = p.kv_ring;
@@ -170,7 +178,7 @@ template <typename T> static gqa_status launch_t(const Call &c) {
     if (st != GQA_OK) return st;
   }
   constexpr int N = Vec<T>::N;
-  int items = ((c.q_rot ? p.q_heads : 0) + 2 * p.kv_heads) * (p.head_dim / 2 / N);
+  int items = ((c.q_rot ? p.q_heads : 0) + p.kv_heads) * (p.head_dim / 2 / N) + p.kv_heads * (c.Dv / N);
   int threads = items >= 256 ? 256 : ((items + 31) / 32) * 32;
   rope_append_kernel<T><<<p.batch * p.q_len, threads, 0, c.stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;

@@ -45,7 +45,7 @@ class GqaParams(ctypes.Structure):
                 ("cap_present", ctypes.c_int32), ("rope_len", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("softcap", ctypes.c_float), ("window", ctypes.c_int32),
                 ("causal", ctypes.c_int32), ("do_rotary", ctypes.c_int32), ("rotary_interleaved", ctypes.c_int32),
-                ("smooth_softmax", ctypes.c_int32), ("kv_ring", ctypes.c_int32)]
+                ("smooth_softmax", ctypes.c_int32), ("kv_ring", ctypes.c_int32), ("v_head_dim", ctypes.c_int32)]
 
 
 class GqaMask(ctypes.Structure):
@@ -61,7 +61,9 @@ def mask_from_tensor(m, kind: int) -> GqaMask:
     if not m.is_cuda:
         raise ValueError("libgqa takes device tensors; got a mask on %s" % m.device)
     st = [0 if m.shape[d] == 1 else m.stride(d) for d in range(3)]  # any other strides are explicit
-    return GqaMask(m.data_ptr(), kind, m.shape[3], st[0], st[1], st[2])
+    g = GqaMask(m.data_ptr(), kind, m.shape[3], st[0], st[1], st[2])
+    g.tensor = m  # the struct holds a raw pointer: keep the memory alive as long as the struct
+    return g
 
 
 class GqaError(RuntimeError):
@@ -105,12 +107,12 @@ lib = _load()
 
 def params(batch, q_heads, kv_heads, head_dim, q_len, cap_present, dtype, cap_past=None, rope_len=0, scale=0.0,
            softcap=0.0, window=-1, causal=1, do_rotary=0, rotary_interleaved=0, smooth_softmax=0,
-           kv_ring=0) -> GqaParams:
+           kv_ring=0, v_head_dim=0) -> GqaParams:
     """Build a gqa_params struct (dtype: "f32" | "f16" | "bf16" or its integer code)."""
     dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
     return GqaParams(batch, q_heads, kv_heads, head_dim, q_len, cap_present if cap_past is None else cap_past,
                      cap_present, rope_len, dt, scale, softcap, window, causal, do_rotary, rotary_interleaved,
-                     smooth_softmax, kv_ring)
+                     smooth_softmax, kv_ring, v_head_dim)
 
 
 def params_from_dict(d: dict) -> GqaParams:
@@ -118,7 +120,8 @@ def params_from_dict(d: dict) -> GqaParams:
                   cap_past=d.get("cap_past"), rope_len=d.get("rope_len", 0), scale=d.get("scale", 0.0),
                   softcap=d.get("softcap", 0.0), window=d.get("window", -1), causal=d.get("causal", 1),
                   do_rotary=d.get("do_rotary", 0), rotary_interleaved=d.get("rotary_interleaved", 0),
-                  smooth_softmax=d.get("smooth_softmax", 0), kv_ring=d.get("kv_ring", 0))
+                  smooth_softmax=d.get("smooth_softmax", 0), kv_ring=d.get("kv_ring", 0),
+                  v_head_dim=d.get("v_head_dim", 0))
 
 
 def _ptr(t):

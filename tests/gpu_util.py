@@ -34,7 +34,8 @@ def run_gpu(case: Case, mode: str, separate_present: bool = False, attend_only: 
         present_v = torch.full_like(past_v, float("nan"))
     else:
         present_k, present_v = past_k, past_v
-    out = torch.full_like(q, float("nan"))
+    dv = case.w.v_head_dim or case.w.head_dim
+    out = torch.full((q.shape[0], q.shape[1], case.w.q_heads * dv), float("nan"), dtype=q.dtype, device=dev)
     status = torch.full((1,), status_init, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device=dev)
@@ -93,9 +94,10 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
 
 
 def out_rows(out: torch.Tensor, case: Case, rows=None) -> np.ndarray:
-    """GPU output as fp64 [B, curr, Hq, D] (or [len(rows), D])."""
+    """GPU output as fp64 [B, curr, Hq, Dv] (or [len(rows), Dv])."""
     w = case.w
-    o = out.detach().to(torch.float64).cpu().numpy().reshape(w.batch * w.q_len * w.q_heads, w.head_dim)
+    dv = w.v_head_dim or w.head_dim
+    o = out.detach().to(torch.float64).cpu().numpy().reshape(w.batch * w.q_len * w.q_heads, dv)
     if rows is None:
-        return o.reshape(w.batch, w.q_len, w.q_heads, w.head_dim)
+        return o.reshape(w.batch, w.q_len, w.q_heads, dv)
     return o[np.asarray(rows)]

@@ -64,7 +64,7 @@ def test_mask_struct_layout_matches_header(g, tmp_path):
 
 
 def test_version_and_status_strings(g):
-    assert g.gqa_abi_version() == 3
+    assert g.gqa_abi_version() == 4
     for s in range(6):
         assert g.gqa_status_string(s) and g.gqa_status_string(s) != "unknown status"
     assert g.gqa_status_string(99) == "unknown status"
@@ -109,6 +109,9 @@ def call(g, p, fn="gqa_attention_decode", ws_bytes=0, **ptrs):
     (dict(kv_ring=1, window=-1), 1),            # a ring needs a window
     (dict(kv_ring=1, window=1024, q_len=2), 3),  # W + curr - 1 > cap: a visible key would be overwritten
     (dict(kv_ring=1, window=100, cap_present=1000), 2),  # ring capacity not a multiple of 64
+    (dict(v_head_dim=-1), 1),
+    (dict(v_head_dim=96), 2),                                  # V head dim 64 or 128 only
+    (dict(kv_ring=1, window=1000, v_head_dim=64), 2),          # a ring holds K and V rows of one width
 ])
 def test_invalid_params_rejected(g, fn, kw, code):
     assert call(g, good_params(g, **kw), fn) == code
@@ -154,6 +157,7 @@ def test_paged_invalid_arguments(g, kw, code):
 
 def test_paged_rejects_ring_and_unsupported_shapes(g):
     assert call_paged(g, good_params(g, kv_ring=1, window=1000)) == 1
+    assert call_paged(g, good_params(g, v_head_dim=64)) == 2       # pages hold K and V rows of one width
     assert call_paged(g, good_params(g, dtype="f32")) == 2          # only the split decode kernel reads pages
     assert call_paged(g, good_params(g, q_heads=64, q_len=2)) == 2  # 64 rows per group at D=128
 
@@ -237,6 +241,9 @@ def test_workspace_sizes(g):
     assert S == 1 and ws(window=200) == 0  # the band fits one chunk
     S = splits(2, 2, 16384, -1)
     assert S == 64 and ws(window=-1, cap_present=16384) == decode_ws(2, 2, 4, 128, S)
+    # partial accumulators are rows of the V head dim
+    assert ws(window=-1, cap_present=16384, v_head_dim=64) == decode_ws(2, 2, 4, 64, S)
+    assert ws(window=-1, cap_present=16384, head_dim=64, v_head_dim=128) == decode_ws(2, 2, 4, 128, S)
     # rotary adds room for the rotated queries (prefill path): B*curr*Hq*D*2 bytes
     assert ws(do_rotary=1, rope_len=64, window=-1, cap_present=16384) == \
         2 * 1 * 8 * 128 * 2 + decode_ws(2, 2, 4, 128, S)
