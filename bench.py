@@ -47,6 +47,10 @@ def esize(w):
     return 4 if w.dtype == "f32" else 2
 
 
+def vdim(w):
+    return w.v_head_dim or w.head_dim
+
+
 def band(w, past, window):
     """Union band [lo, hi) of the step's rows for one sequence."""
     total = past + w.q_len
@@ -56,13 +60,13 @@ def band(w, past, window):
 
 def kv_read_bytes(w, seqlens, window):
     return sum((hi - lo) for lo, hi in (band(w, p, window) for p in seqlens.tolist())) * \
-        w.kv_heads * 2 * w.head_dim * esize(w)
+        w.kv_heads * (w.head_dim + vdim(w)) * esize(w)
 
 
 def io_bytes(w):
     """q read + out written + new k/v read and appended."""
     e = esize(w)
-    return w.batch * w.q_len * w.head_dim * e * (2 * w.q_heads + 4 * w.kv_heads)
+    return w.batch * w.q_len * e * (w.q_heads + 2 * w.kv_heads) * (w.head_dim + vdim(w))
 
 
 def visible_pairs(w, seqlens, window):
@@ -80,9 +84,9 @@ def step_work(w, seqs):
     if w.mode == "decode":
         kv = sum(kv_read_bytes(w, s, win) for s, win in zip(seqs, w.windows))
         io = io_bytes(w) * w.layers
-        return (kv + io) / 1e9, (kv + (io_bytes(w) - 4 * w.batch * w.q_len * w.kv_heads * w.head_dim * esize(w))
-                                 * w.layers) / 1e9, "GB/s"
-    flops = sum(4.0 * w.head_dim * visible_pairs(w, s, win) for s, win in zip(seqs, w.windows))
+        append = 2 * w.batch * w.q_len * w.kv_heads * (w.head_dim + vdim(w)) * esize(w)
+        return (kv + io) / 1e9, (kv + (io_bytes(w) - append) * w.layers) / 1e9, "GB/s"
+    flops = sum(2.0 * (w.head_dim + vdim(w)) * visible_pairs(w, s, win) for s, win in zip(seqs, w.windows))
     return flops / 1e12, flops / 1e12, "TFLOP/s"
 
 
@@ -396,7 +400,7 @@ def kernels_per_layer(w) -> int:
     rows = (w.q_heads // w.kv_heads) * w.q_len
     mtiles = (rows + 15) // 16
     fused = w.mode == "decode" and w.dtype != "f32" and (
-        (w.head_dim == 128 and mtiles <= 2) or (w.head_dim == 64 and mtiles <= 4))
+        mtiles <= 2 if vdim(w) != w.head_dim else (w.head_dim == 128 and mtiles <= 2) or (w.head_dim == 64 and mtiles <= 4))
     return 1 if fused else 2
 
 

@@ -89,6 +89,9 @@ WORKLOADS = {
         # the windowed decode over a paged cache: the same rows in a shuffled pool of pages
         Workload("decode_window_paged_bf16", 6, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
                  windows=(1024,), kv_paged=1),
+        # the windowed decode with a V head dim of 64 under a Q/K head dim of 128
+        Workload("decode_window_vdim_bf16", 8, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
+                 windows=(1024,), v_head_dim=64),
         # the long prompt with a dense additive attention bias, broadcast over the heads
         Workload("prefill_bias_bf16", 7, "prefill", "bf16", 2, 64, 8, 128, 8192, 8192, 0, 0,
                  windows=(4096,), softcap=50.0, head_sink=True, mask="add"),

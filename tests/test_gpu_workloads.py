@@ -77,6 +77,10 @@ def test_decode_long_bf16():
     torch.cuda.empty_cache()
 
 
+def test_decode_window_vdim_bf16():
+    check_workload("decode_window_vdim_bf16")
+
+
 def test_decode_window_ring_bf16():
     """The windowed decode over a ring of 1024 slots: sequences up to 4096 long, so most
     rings have wrapped; the appended slots bit for bit, sampled rows against the ring oracle."""
