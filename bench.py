@@ -600,7 +600,8 @@ def main():
     if args.steps is None:
         args.steps = {"decode_window_bf16": 100000, "specdecode_rotary_f16": 20000, "decode_long_bf16": 1500,
                       "prefill_sink_softcap_bf16": 500, "prefill_fp32_tiny": 20000,
-                      "decode_window_ring_bf16": 100000, "decode_window_paged_bf16": 100000}[args.workload]
+                      "decode_window_ring_bf16": 100000, "decode_window_paged_bf16": 100000,
+                      "decode_window_vdim_bf16": 100000, "prefill_bias_bf16": 400}.get(args.workload, 1000)
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

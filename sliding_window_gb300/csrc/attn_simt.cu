@@ -36,10 +36,12 @@ struct SimtArgs {
   long long msb, msh, msi;
 };
 
-template <typename T>
+// MASKED: a mask is given (compiled out otherwise); SAMEV: Dv == D (the common case keeps
+// one load per element of both tiles and no V-width arithmetic)
+template <typename T, bool MASKED, bool SAMEV>
 __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   extern __shared__ float sm[];
-  const int D = a.D, Dv = a.Dv;
+  const int D = a.D, Dv = SAMEV ? a.D : a.Dv, Dw = SAMEV ? D : (D > Dv ? D : Dv);
   float *qs = sm;                          // [kRows][D]
   float *ks = qs + kRows * D;              // [kKeys][D + 1]
   float *vs = ks + kKeys * (D + 1);        // [kKeys][Dv]
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int past = a.seqlens[b];
   int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
-  if (a.mask_kind && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // mask too short
+  if (MASKED && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // mask too short
   T *out = reinterpret_cast<T *>(a.out);
   const int nrows = min(kRows, a.curr - i0);
   if (st) {
@@ -85,13 +87,12 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   const int dslots = Dv / 32;
   for (int kt = lo; kt < hi; kt += kKeys) {
     __syncthreads();
-    for (int idx = threadIdx.x; idx < kKeys * D; idx += blockDim.x) {
-      int j = idx / D, d = idx % D;
-      ks[j * (D + 1) + d] = kt + j < hi ? to_f32(kc[(size_t)(kt + j) * D + d]) : 0.f;
-    }
-    for (int idx = threadIdx.x; idx < kKeys * Dv; idx += blockDim.x) {
-      int j = idx / Dv, d = idx % Dv;
-      vs[j * Dv + d] = kt + j < hi ? to_f32(vc[(size_t)(kt + j) * Dv + d]) : 0.f;
+    // one pass over both tiles, so the K and V loads of a thread are in flight together
+    for (int idx = threadIdx.x; idx < kKeys * Dw; idx += blockDim.x) {
+      const int j = idx / Dw, d = idx % Dw;
+      const bool in = kt + j < hi;
+      if (SAMEV || d < D) ks[j * (D + 1) + d] = in ? to_f32(kc[(size_t)(kt + j) * D + d]) : 0.f;
+      if (SAMEV || d < Dv) vs[j * Dv + d] = in ? to_f32(vc[(size_t)(kt + j) * Dv + d]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -101,14 +102,20 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
       const int qa = past + i0 + r;
       const int j = kt + lane;
       bool vis = j < hi && (!a.causal || j <= qa) && (a.window < 0 || qa - j < a.window);
-      const long long mi = b * a.msb + hq * a.msh + (long long)(i0 + r) * a.msi + j;
-      if (vis && a.mask_kind == 1) vis = reinterpret_cast<const uint8_t *>(a.mask)[mi] != 0;
+      float bias = 0.f;
+      if (MASKED && vis) {
+        const long long mi = b * a.msb + hq * a.msh + (long long)(i0 + r) * a.msi + j;
+        if (a.mask_kind == 1)
+          vis = reinterpret_cast<const uint8_t *>(a.mask)[mi] != 0;
+        else
+          bias = to_f32(reinterpret_cast<const T *>(a.mask)[mi]);  // -inf: weight 0
+      }
       float s = -INFINITY;
       if (vis) {
         float dot = 0.f;
         for (int d = 0; d < D; ++d) dot = fmaf(qs[r * D + d], ks[lane * (D + 1) + d], dot);
         s = dot * a.scale;
-        if (a.mask_kind == 2) s += to_f32(reinterpret_cast<const T *>(a.mask)[mi]);  // -inf: weight 0
+        if (MASKED && a.mask_kind == 2) s += bias;
         if (a.softcap > 0.f) s = a.softcap * tanhf(s / a.softcap);
       }
       float tmax = s;
@@ -193,7 +200,10 @@ template <typename T> gqa_status launch_t(const Call &c) {
   size_t smem = sizeof(float) * (kRows * D + kKeys * (D + 1) + kKeys * c.Dv + 4 * kKeys);
   // D, Dv <= 128: at most 41.5 KB of shared memory, under the 48 KB default limit
   dim3 grid((p.q_len + kRows - 1) / kRows, p.q_heads, p.batch);
-  attn_simt_kernel<T><<<grid, 128, smem, c.stream>>>(a);
+  const bool masked = c.mask != nullptr, samev = c.Dv == D;
+  auto kern = masked ? (samev ? attn_simt_kernel<T, true, true> : attn_simt_kernel<T, true, false>)
+                     : (samev ? attn_simt_kernel<T, false, true> : attn_simt_kernel<T, false, false>);
+  kern<<<grid, 128, smem, c.stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

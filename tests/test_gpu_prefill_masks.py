@@ -133,7 +133,7 @@ def test_padded_rows_take_the_tma_path(kind):
     assert_close(out_rows(out, c), ref, "f16", "padded %s" % kind)
 
 
-@pytest.mark.parametrize("mode,kind", itertools.product(["prefill", "decode"], ["bool", "add"]))
+@pytest.mark.parametrize("mode,kind", list(itertools.product(["prefill", "decode"], ["bool", "add"])))
 def test_f32_masks_on_the_cuda_core_kernel(mode, kind):
     S, past = (130, 50) if mode == "prefill" else (1, 900)
     c = case(mode, "f32", 64, 4, S, past, 300, sink="head", softcap=0.0 if kind == "bool" else 15.0, seed=13)

@@ -55,14 +55,14 @@ def test_split_decode_vdim(dtype, dims, gc, capw):
     check(c, "decode", dtype, "decode vdim %s" % ((dtype, dims, gc, capw),))
 
 
-@pytest.mark.parametrize("dims,separate", itertools.product(DIMS, [False, True]))
+@pytest.mark.parametrize("dims,separate", list(itertools.product(DIMS, [False, True])))
 def test_decode_vdim_separate_past(dims, separate):
     D, Dv = dims
     c = case("decode", "bf16", D, Dv, 4, 2, 1500, 10, 1400, 512, rotary=1, seed=5)
     check(c, "decode", "bf16", "decode vdim separate=%s" % separate, separate=separate)
 
 
-@pytest.mark.parametrize("dims,kind", itertools.product(DIMS, ["bool", "add"]))
+@pytest.mark.parametrize("dims,kind", list(itertools.product(DIMS, ["bool", "add"])))
 def test_masked_decode_vdim(dims, kind):
     from sliding_window_gb300 import gqa
     D, Dv = dims
@@ -106,7 +106,7 @@ def test_prefill_vdim(dtype, dims, spw, softcap):
     check(c, "prefill", dtype, "prefill vdim %s" % ((dtype, dims, spw, softcap),))
 
 
-@pytest.mark.parametrize("mode,dims", itertools.product(["prefill", "decode"], DIMS))
+@pytest.mark.parametrize("mode,dims", list(itertools.product(["prefill", "decode"], DIMS)))
 def test_cuda_core_kernel_vdim(mode, dims):
     """f32 (the CUDA-core kernel) in both modes, and a bf16 decode with 64 rows per group."""
     D, Dv = dims
