@@ -1,0 +1,56 @@
+"""The bench's algorithmic accounting, checked against counts written out by hand from the
+definitions: decode reads every visible K row (D elements) and V row (Dv elements) of each
+(b, kv head) once, plus q read, out written and the new K/V read and appended; prefill does
+2·D (scores) + 2·Dv (weighted sum) flops per visible (query, key) pair.  Also the launch
+count the bench claims per layer."""
+import numpy as np
+import pytest
+
+import bench
+from sliding_window_gb300.inputs import WORKLOADS
+
+
+def test_decode_bytes_by_hand():
+    w = WORKLOADS["decode_window_bf16"].scaled(batch=2)
+    seqs = [np.array([100, 3000], dtype=np.int32)]
+    # band lengths: window 1024 -> seq 100: [0, 101) = 101 keys; seq 3000: [1977, 3001) = 1024 keys
+    keys = 101 + 1024
+    kv = keys * w.kv_heads * (128 + 128) * 2
+    io = 2 * 1 * 2 * (w.q_heads + 2 * w.kv_heads) * (128 + 128)
+    units, kunits, unit = bench.step_work(w, seqs)
+    assert unit == "GB/s"
+    assert units == pytest.approx((kv + io) / 1e9, rel=0, abs=1e-15)
+    append = 2 * 2 * 1 * w.kv_heads * 256 * 2
+    assert kunits == pytest.approx((kv + io - append) / 1e9, rel=0, abs=1e-15)
+
+
+def test_decode_bytes_with_a_narrower_v():
+    w = WORKLOADS["decode_window_vdim_bf16"].scaled(batch=1)
+    seqs = [np.array([5000 - 1], dtype=np.int32)]
+    units, _, _ = bench.step_work(w, seqs)
+    kv = 1024 * w.kv_heads * (128 + 64) * 2
+    io = 1 * 1 * 2 * (w.q_heads + 2 * w.kv_heads) * (128 + 64)
+    assert units == pytest.approx((kv + io) / 1e9, rel=0, abs=1e-15)
+
+
+@pytest.mark.parametrize("dv", [0, 64])
+def test_prefill_flops_by_hand(dv):
+    w = WORKLOADS["prefill_sink_softcap_bf16"].scaled(batch=1, q_len=10, cap=10, windows=(4,), v_head_dim=dv)
+    seqs = [np.array([0], dtype=np.int32)]
+    # causal with window 4 over a 10-token prompt: row i sees min(i + 1, 4) keys
+    pairs = sum(min(i + 1, 4) for i in range(10)) * w.q_heads
+    d = 128 + (dv or 128)
+    flops, kflops, unit = bench.step_work(w, seqs)
+    assert unit == "TFLOP/s" and flops == kflops == pytest.approx(2 * d * pairs / 1e12, rel=1e-12)
+
+
+@pytest.mark.parametrize("name,launches", [
+    ("prefill_fp32_tiny", 2), ("decode_window_bf16", 1), ("prefill_sink_softcap_bf16", 2),
+    ("specdecode_rotary_f16", 1), ("decode_long_bf16", 1), ("decode_window_ring_bf16", 1),
+    ("decode_window_paged_bf16", 1), ("decode_window_vdim_bf16", 1), ("prefill_bias_bf16", 2)])
+def test_kernels_per_layer(name, launches):
+    """One fused launch for the split-KV decode (it appends and rotates itself), else the
+    RoPE/append kernel and the attention kernel.  The speculative decode's 8 q heads x 4
+    tokens = 32 rows per group at D = 128 fit the split kernel."""
+    w = WORKLOADS[name]
+    assert bench.kernels_per_layer(w) == launches
