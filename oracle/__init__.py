@@ -97,6 +97,12 @@ def _load():
         lib.oracle_rope_append_paged.argtypes = [i32] * 12 + [vp] * 10 + [ctypes.POINTER(i32)]
         lib.oracle_attention_paged.argtypes = [i32] * 10 + [f64, f64] + [i32] * 4 + [vp] * 7 + [i64, vp]
         lib.oracle_attention.restype = None
+        lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_encode_e4m3.restype = ctypes.c_uint8
+        lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+        lib.oracle_decode_e4m3.restype = f64
+        lib.oracle_rope_append_q8.argtypes = [i32] * 10 + [vp] * 11 + [ctypes.POINTER(i32)]
+        lib.oracle_attention_q8.argtypes = [i32] * 9 + [f64, f64] + [i32] * 4 + [vp] * 8 + [i64, vp]
         lib.oracle_has_openmp.restype = i32
         _lib = lib
         return lib
@@ -388,6 +394,76 @@ def attention_masked(p: dict, q_rot, present_k, present_v, seqlens_k, mask, kind
                                 int(p.get("smooth_softmax", 0)), 1 if kind == "bool" else 2, _ptr(m), st[0], st[1],
                                 st[2], m.shape[3], _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq), _ptr(sink), _ptr(ridx), n,
                                 _ptr(out))
+    if rows is None:
+        return out.reshape(B, curr, Hq, Dv)
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# Quantized (f8 E4M3) KV cache: codes with one scale per kv head for K and for V
+# --------------------------------------------------------------------------------------
+def encode_e4m3(x) -> np.ndarray:
+    """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating at +-448
+    (infinity included), NaN to NaN."""
+    lib = _load()
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    return np.array([lib.oracle_encode_e4m3(float(v)) for v in a.ravel()], dtype=np.uint8).reshape(a.shape)
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    return np.array([lib.oracle_decode_e4m3(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def rope_append_q8(p: dict, q, k, v, present_k8, present_v8, seqlens_k, k_scale, v_scale, cos_cache=None,
+                   sin_cache=None):
+    """Append into an E4M3 cache in place: K (rotated, rounded to the dtype) and V divided by
+    their kv head's scale in fp32 and encoded.  present_k8 [B, Hkv, cap, D] and present_v8
+    [B, Hkv, cap, Dv] are uint8 arrays updated in place.  Returns (q_rot, status_bits)."""
+    lib = _load()
+    dt = p["dtype"]
+    q, k, v = _bits(q, dt), _bits(k, dt), _bits(v, dt)
+    assert present_k8.dtype == np.uint8 and present_k8.flags.c_contiguous
+    assert present_v8.dtype == np.uint8 and present_v8.flags.c_contiguous
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    cs = _bits(cos_cache, dt) if cos_cache is not None else None
+    sn = _bits(sin_cache, dt) if sin_cache is not None else None
+    seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    q_rot = np.empty_like(q)
+    st = ctypes.c_int32(0)
+    lib.oracle_rope_append_q8(p["batch"], p["q_heads"], p["kv_heads"], p["head_dim"], v_dim(p), p["q_len"],
+                              p["cap_present"], p.get("rope_len", 0), DTYPE_CODES[dt], int(p.get("do_rotary", 0)),
+                              _ptr(q), _ptr(k), _ptr(v), _ptr(seq), _ptr(cs), _ptr(sn), _ptr(ks), _ptr(vs),
+                              _ptr(q_rot), _ptr(present_k8), _ptr(present_v8), ctypes.byref(st))
+    return q_rot, int(st.value)
+
+
+def attention_q8(p: dict, q_rot, present_k8, present_v8, seqlens_k, k_scale, v_scale, head_sink=None,
+                 rows=None) -> np.ndarray:
+    """Attention in fp64 over the dequantized E4M3 cache (code * scale of its kv head)."""
+    lib = _load()
+    dt = p["dtype"]
+    qb = _bits(q_rot, dt)
+    kb = np.ascontiguousarray(present_k8, dtype=np.uint8)
+    vb = np.ascontiguousarray(present_v8, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    seq = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    sink = None if head_sink is None else np.ascontiguousarray(head_sink, dtype=np.float32)
+    B, Hq, D, curr, Dv = p["batch"], p["q_heads"], p["head_dim"], p["q_len"], v_dim(p)
+    if rows is None:
+        ridx, n = None, B * curr * Hq
+    else:
+        ridx = np.ascontiguousarray(rows, dtype=np.int64)
+        n = ridx.shape[0]
+    out = np.zeros((n, Dv), dtype=np.float64)
+    lib.oracle_attention_q8(B, Hq, p["kv_heads"], D, Dv, curr, p["cap_present"], p.get("rope_len", 0),
+                            DTYPE_CODES[dt], float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)),
+                            int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
+                            int(p.get("smooth_softmax", 0)), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(ks), _ptr(vs),
+                            _ptr(seq), _ptr(sink), _ptr(ridx), n, _ptr(out))
     if rows is None:
         return out.reshape(B, curr, Hq, Dv)
     return out

@@ -41,6 +41,7 @@
 #define ODT_F32 0
 #define ODT_F16 1
 #define ODT_BF16 2
+#define ODT_F64 3 /* internal: dequantized rows of a quantized cache */
 
 /* ------------------------------------------------------------------------------------
  * Number formats.  Decoding and RNE rounding written from the IEEE-754 definitions of
@@ -106,6 +107,7 @@ double oracle_decode_bf16(uint16_t h) { return decode_bf16(h); }
 
 /* Element idx of an array of the given dtype, as a double (exact for all three). */
 static double load_elem(const void *base, size_t idx, int dtype) {
+  if (dtype == ODT_F64) return ((const double *)base)[idx];
   if (dtype == ODT_F32) return (double)((const float *)base)[idx];
   uint16_t h = ((const uint16_t *)base)[idx];
   return dtype == ODT_F16 ? decode_f16(h) : decode_bf16(h);
@@ -648,6 +650,145 @@ void oracle_attention_masked(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int3
     free(bias);
     free(vis);
     free(qv);
+  }
+}
+
+/* ------------------------------------------------------------------------------------
+ * Quantized KV cache.  The pages leave a quantized cache out of their own designs ([P1]
+ * puts i8/i4/f8 KV out of its scope at the end of "smooth_softmax / head_sink"; [P2] "What
+ * changed" rejects quantized KV); the reading taken here is the plainest one for an f8
+ * cache: present K and V hold 8-bit floating-point codes of the E4M3
+ * kind (1 sign, 4 exponent bits with bias 7, 3 fraction bits; no infinities; the code
+ * S.1111.111 is NaN, so the largest magnitude is 1.75 * 2^8 = 448), one float scale per kv
+ * head for K and one for V.  The stored value of an element is code * scale.
+ *
+ * Append: the row is first formed in the storage dtype exactly as in oracle_rope_append
+ * (K rotated and rounded to the dtype), then each element x becomes
+ *     code = e4m3(fp32(x) / fp32(scale))      (IEEE fp32 division)
+ * rounded to nearest, ties to even, saturating: a magnitude beyond 448 (including one
+ * that rounds past it, and infinity) gives the code of +-448, NaN gives NaN.
+ * Attention is oracle_attention's definition over the dequantized rows code * scale,
+ * computed in fp64.  The cache is updated in place (no separate past).
+ * ---------------------------------------------------------------------------------- */
+double oracle_decode_e4m3(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int e = (c >> 3) & 0xf;
+  int f = c & 7;
+  double mag;
+  if (e == 15 && f == 7)
+    mag = NAN;
+  else if (e == 0)
+    mag = ldexp((double)f, -9); /* subnormal: f/8 * 2^(1-7) */
+  else
+    mag = ldexp((double)(8 + f), e - 10); /* (1 + f/8) * 2^(e-7) */
+  return sign ? -mag : mag;
+}
+
+uint8_t oracle_encode_e4m3(float x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  if (isnan(x)) return (uint8_t)(sign | 0x7f);
+  double a = fabs((double)x);
+  if (a >= 464.0) return (uint8_t)(sign | 0x7e); /* 464 is the tie 448 | 480: saturate */
+  if (a < ldexp(1.0, -6)) {                       /* subnormal range, quantum 2^-9 */
+    double n = rint(a / ldexp(1.0, -9));         /* n == 8 is the smallest normal */
+    return (uint8_t)(sign | (uint8_t)n);
+  }
+  int e2;
+  double m = frexp(a, &e2); /* a = m * 2^e2, m in [0.5, 1) */
+  int E = e2 - 1;
+  double n = rint(ldexp(m, 4)); /* 2m * 8 rounded, in [8, 16] */
+  if (n == 16.0) {
+    n = 8.0;
+    E += 1;
+  }
+  return (uint8_t)(sign | (uint8_t)((E + 7) << 3) | (uint8_t)(n - 8.0));
+}
+
+void oracle_rope_append_q8(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv, int32_t curr, int32_t cap,
+                           int32_t rope_len, int32_t dtype, int32_t do_rotary, const void *q, const void *k,
+                           const void *v, const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                           const float *k_scale, const float *v_scale, void *q_rot, uint8_t *present_k,
+                           uint8_t *present_v, int32_t *status_out) {
+  size_t es = elem_size(dtype);
+  int32_t status_all = 0;
+  void *row = malloc(es * (size_t)(D > Dv ? D : Dv));
+  for (int b = 0; b < B; ++b) {
+    int32_t past = seqlens_k[b];
+    int32_t st = oracle_sequence_status(past, curr, 0, cap, 0, do_rotary, rope_len);
+    status_all |= st;
+    if (st) continue;
+    for (int h = 0; h < Hkv; ++h)
+      for (int i = 0; i < curr; ++i) {
+        size_t src = (((size_t)b * curr + i) * Hkv + h) * D;
+        size_t dst = (((size_t)b * Hkv + h) * cap + (size_t)(past + i)) * D;
+        if (do_rotary)
+          rotate_row(k, src, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, row, 0);
+        else
+          memcpy(row, (const char *)k + src * es, (size_t)D * es);
+        for (int d = 0; d < D; ++d) present_k[dst + d] = oracle_encode_e4m3(load_f32(row, d, dtype) / k_scale[h]);
+        size_t src_v = (((size_t)b * curr + i) * Hkv + h) * Dv;
+        size_t dst_v = (((size_t)b * Hkv + h) * cap + (size_t)(past + i)) * Dv;
+        for (int d = 0; d < Dv; ++d)
+          present_v[dst_v + d] = oracle_encode_e4m3(load_f32(v, src_v + d, dtype) / v_scale[h]);
+      }
+    if (q_rot) {
+      for (int i = 0; i < curr; ++i)
+        for (int h = 0; h < Hq; ++h) {
+          size_t off = (((size_t)b * curr + i) * Hq + h) * D;
+          if (do_rotary)
+            rotate_row(q, off, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, q_rot, off);
+          else
+            memcpy((char *)q_rot + off * es, (const char *)q + off * es, (size_t)D * es);
+        }
+    }
+  }
+  free(row);
+  if (status_out) *status_out = status_all;
+}
+
+void oracle_attention_q8(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv, int32_t curr, int32_t cap,
+                         int32_t rope_len, int32_t dtype, double scale, double softcap, int32_t window,
+                         int32_t causal, int32_t do_rotary, int32_t smooth_softmax, const void *q,
+                         const uint8_t *present_k, const uint8_t *present_v, const float *k_scale,
+                         const float *v_scale, const int32_t *seqlens_k, const float *head_sink,
+                         const int64_t *rows, int64_t nrows, double *out) {
+  int G = Hq / Hkv;
+  if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  int64_t count = rows ? nrows : (int64_t)B * curr * Hq;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t t = 0; t < count; ++t) {
+    int64_t r = rows ? rows[t] : t;
+    int hq = (int)(r % Hq);
+    int i = (int)((r / Hq) % curr);
+    int b = (int)(r / ((int64_t)Hq * curr));
+    double *o = out + (size_t)t * Dv;
+    int32_t past = seqlens_k[b];
+    if (oracle_sequence_status(past, curr, 0, cap, 0, do_rotary, rope_len)) {
+      for (int d = 0; d < Dv; ++d) o[d] = 0.0;
+      continue;
+    }
+    int hk = hq / G;
+    int64_t total = (int64_t)past + curr;
+    int64_t q_abs = (int64_t)past + i;
+    /* the dequantized rows of slots [0, total) of this kv head */
+    double *kd = (double *)malloc(sizeof(double) * (size_t)(total * D));
+    double *vd = (double *)malloc(sizeof(double) * (size_t)(total * Dv));
+    size_t kb = ((size_t)b * Hkv + hk) * (size_t)cap * D, vb = ((size_t)b * Hkv + hk) * (size_t)cap * Dv;
+    for (int64_t j = 0; j < total * D; ++j) kd[j] = oracle_decode_e4m3(present_k[kb + (size_t)j]) * (double)k_scale[hk];
+    for (int64_t j = 0; j < total * Dv; ++j) vd[j] = oracle_decode_e4m3(present_v[vb + (size_t)j]) * (double)v_scale[hk];
+    double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
+    uint8_t *vis = (uint8_t *)malloc((size_t)total);
+    for (int64_t j = 0; j < total; ++j) vis[j] = (uint8_t)oracle_visible(q_abs, j, total, causal, window);
+    int has_sink = head_sink != NULL || smooth_softmax;
+    double z = head_sink ? (double)head_sink[hq] : 0.0;
+    oracle_attend_row(qv, kd, vd, 0, total, vis, D, Dv, ODT_F64, scale, softcap, has_sink, z, o);
+    free(vis);
+    free(qv);
+    free(vd);
+    free(kd);
   }
 }
 
