@@ -92,7 +92,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 4
+#define GQA_ABI_VERSION 5
 
 typedef int32_t gqa_status;
 #define GQA_OK 0
@@ -259,6 +259,32 @@ gqa_status gqa_attention_prefill_masked(const gqa_params *p, const gqa_mask *mas
                                         const float *head_sink, void *out, void *present_k, void *present_v,
                                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                         void *stream);
+
+/* f8 KV cache.  The pages leave a quantized cache out of their own designs ([P1] puts
+ * i8/i4/f8 KV out of its scope; [P2] "What changed" rejects quantized KV); this is the
+ * plainest reading for an f8 cache.  present_k [B, Hkv, cap_present, D] and present_v
+ * [B, Hkv, cap_present, Dv] hold one byte per element: an E4M3 code (1 sign, 4 exponent
+ * bits with bias 7, 3 fraction bits, no infinities, S.1111.111 = NaN, largest magnitude
+ * 448).  The stored value of an element is code * scale, with k_scale[h] / v_scale[h]
+ * (fp32, device, [Hkv]) the scales of kv head h.  The step's K (rotated and rounded to the
+ * dtype first, as without quantization) and V rows are appended as the codes of
+ * fp32(x) / scale: nearest, ties to even, saturating at +-448 (infinity too), NaN to NaN.
+ * Attention is the op's definition over the stored values.  The cache is updated in place
+ * (no separate past; k = v = NULL for attention only); q, out, k, v, cos/sin keep the
+ * params' dtype; kv_ring returns GQA_ERR_UNSUPPORTED.  Same workspace (gqa_workspace_bytes),
+ * status and errors as gqa_attention_decode / gqa_attention_prefill.  Decode with D = Dv =
+ * 128 inside the split-KV kernel's envelope runs that kernel (f8 tiles by TMA, widened to f16
+ * in shared memory per warp, f16 MMAs); every other shape runs the CUDA-core kernel. */
+gqa_status gqa_attention_decode_q8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                   const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                   const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                   uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream);
+gqa_status gqa_attention_prefill_q8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                    const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                    uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
+                                    int32_t *dev_status, void *stream);
 
 /* Static description of a status code. */
 const char *gqa_status_string(gqa_status s);

@@ -34,11 +34,13 @@ struct SimtArgs {
   const void *mask;
   int mask_kind, mask_keys;
   long long msb, msh, msi;
+  const float *k_scale, *v_scale;  // f8 cache: one scale per kv head (Q8 kernels)
 };
 
 // MASKED: a mask is given (compiled out otherwise); SAMEV: Dv == D (the common case keeps
-// one load per element of both tiles and no V-width arithmetic)
-template <typename T, bool MASKED, bool SAMEV>
+// one load per element of both tiles and no V-width arithmetic); Q8: the caches hold E4M3
+// codes, the K scale joins the score scale and the V scale the output
+template <typename T, bool MASKED, bool SAMEV, bool Q8>
 __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   extern __shared__ float sm[];
   const int D = a.D, Dv = SAMEV ? a.D : a.Dv, Dw = SAMEV ? D : (D > Dv ? D : Dv);
@@ -75,6 +77,10 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   const int hi = a.causal ? min(total, qa_hi + 1) : total;
   const T *kc = reinterpret_cast<const T *>(a.kc) + ((size_t)b * a.Hkv + hk) * a.cap * D;
   const T *vc = reinterpret_cast<const T *>(a.vc) + ((size_t)b * a.Hkv + hk) * a.cap * Dv;
+  const uint8_t *kc8 = reinterpret_cast<const uint8_t *>(a.kc) + ((size_t)b * a.Hkv + hk) * a.cap * D;
+  const uint8_t *vc8 = reinterpret_cast<const uint8_t *>(a.vc) + ((size_t)b * a.Hkv + hk) * a.cap * Dv;
+  const float score_scale = Q8 ? a.scale * a.k_scale[hk] : a.scale;
+  const float out_scale = Q8 ? a.v_scale[hk] : 1.f;
   constexpr int kMaxDSlots = 4;  // Dv <= 128
   float m[4], l[4], acc[4][kMaxDSlots];
 #pragma unroll
@@ -91,8 +97,13 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
     for (int idx = threadIdx.x; idx < kKeys * Dw; idx += blockDim.x) {
       const int j = idx / Dw, d = idx % Dw;
       const bool in = kt + j < hi;
-      if (SAMEV || d < D) ks[j * (D + 1) + d] = in ? to_f32(kc[(size_t)(kt + j) * D + d]) : 0.f;
-      if (SAMEV || d < Dv) vs[j * Dv + d] = in ? to_f32(vc[(size_t)(kt + j) * Dv + d]) : 0.f;
+      if (Q8) {
+        if (SAMEV || d < D) ks[j * (D + 1) + d] = in ? e4m3_to_f32(kc8[(size_t)(kt + j) * D + d]) : 0.f;
+        if (SAMEV || d < Dv) vs[j * Dv + d] = in ? e4m3_to_f32(vc8[(size_t)(kt + j) * Dv + d]) : 0.f;
+      } else {
+        if (SAMEV || d < D) ks[j * (D + 1) + d] = in ? to_f32(kc[(size_t)(kt + j) * D + d]) : 0.f;
+        if (SAMEV || d < Dv) vs[j * Dv + d] = in ? to_f32(vc[(size_t)(kt + j) * Dv + d]) : 0.f;
+      }
     }
     __syncthreads();
 #pragma unroll
@@ -114,7 +125,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
       if (vis) {
         float dot = 0.f;
         for (int d = 0; d < D; ++d) dot = fmaf(qs[r * D + d], ks[lane * (D + 1) + d], dot);
-        s = dot * a.scale;
+        s = dot * score_scale;
         if (MASKED && a.mask_kind == 2) s += bias;
         if (a.softcap > 0.f) s = a.softcap * tanhf(s / a.softcap);
       }
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
     }
     for (int s2 = 0; s2 < dslots; ++s2) {
       const int d = lane + 32 * s2;
-      out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d] = from_f32<T>(acc[t][s2] * num_scale / den);
+      out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d] = from_f32<T>(acc[t][s2] * num_scale / den * out_scale);
     }
   }
 }
@@ -196,13 +207,17 @@ template <typename T> gqa_status launch_t(const Call &c) {
   a.msb = c.mask_sb;
   a.msh = c.mask_sh;
   a.msi = c.mask_si;
+  a.k_scale = c.k_scale;
+  a.v_scale = c.v_scale;
   const int D = p.head_dim;
   size_t smem = sizeof(float) * (kRows * D + kKeys * (D + 1) + kKeys * c.Dv + 4 * kKeys);
   // D, Dv <= 128: at most 41.5 KB of shared memory, under the 48 KB default limit
   dim3 grid((p.q_len + kRows - 1) / kRows, p.q_heads, p.batch);
   const bool masked = c.mask != nullptr, samev = c.Dv == D;
-  auto kern = masked ? (samev ? attn_simt_kernel<T, true, true> : attn_simt_kernel<T, true, false>)
-                     : (samev ? attn_simt_kernel<T, false, true> : attn_simt_kernel<T, false, false>);
+  if (masked && c.q8) return GQA_ERR_UNSUPPORTED;
+  auto kern = c.q8 ? (samev ? attn_simt_kernel<T, false, true, true> : attn_simt_kernel<T, false, false, true>)
+              : masked ? (samev ? attn_simt_kernel<T, true, true, false> : attn_simt_kernel<T, true, false, false>)
+                       : (samev ? attn_simt_kernel<T, false, true, false> : attn_simt_kernel<T, false, false, false>);
   kern<<<grid, 128, smem, c.stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }

@@ -34,6 +34,25 @@ template <> __device__ __forceinline__ float from_f32<float>(float x) { return x
 template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// f8 E4M3 codes of a quantized KV cache, through the hardware conversions.  Both 8-bit
+// halves of the pair carry the same value, so the result does not depend on which half an
+// instruction reads or writes.  To a code: nearest, ties to even, saturating at +-448
+// (infinity too), NaN to NaN.  From a code: exact (every E4M3 value is an f16 value).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(x));
+  return (uint8_t)(r & 0xFFu);
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+  return r;
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  const uint32_t h = e4m3x2_to_f16x2((uint16_t)(c | (c << 8)));
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
 // Per-sequence validity shared by every kernel: the same rule decides what is appended
 // and which outputs are zeroed.  Returns GQA_DEV_* bits (0 = valid).
 __device__ __forceinline__ int sequence_status(int past, int curr, int cap_present, int cap_past,

@@ -1,4 +1,5 @@
 #pragma once
+#include <type_traits>
 // decode_split.cuh -- K3 + K4: split-KV decode with RoPE + append fused in and the combine
 // done by the last CTA of each (b, kv head) group.
 //
@@ -69,15 +70,22 @@ struct DecodeArgs {
   float mask_mul;  // 1 / scale: an additive value joins the raw dot product before scaling
   float score_mul;  // scale*log2(e), or scale/softcap with softcap
   float cap_mul;    // softcap*log2(e), 0 without softcap
+  const float *k_scale, *v_scale;  // f8 cache (Q8 kernels): one scale per kv head
 };
 
-template <int D, int DV, int MT, int NST> struct Smem {
-  static constexpr int kTileBytes = KT * D * 2;  // one K tile; the V tile follows it
-  static constexpr int kVTileBytes = KT * DV * 2;
+template <int D, int DV, int MT, int NST, bool Q8 = false> struct Smem {
+  static constexpr int kEs = Q8 ? 1 : 2;  // bytes per cached element (E4M3 codes or the dtype)
+  static constexpr int kTileBytes = KT * D * kEs;  // one K tile; the V tile follows it
+  static constexpr int kVTileBytes = KT * DV * kEs;
   static constexpr int kStageBytes = kTileBytes + kVTileBytes;
+  // Q8: every warp widens its 16 keys of the stage to f16 here (the layout of a 16-bit
+  // stage), right after the stages, so the two form one region for the merge below
+  static constexpr int kConvBytes = Q8 ? KT * (D + DV) * 2 : 0;
+  static constexpr int kReuseBytes = NST * kStageBytes + kConvBytes;
   static constexpr int kQRows = MT * 16;
   static constexpr int kStagesOff = 0;
-  static constexpr int kQOff = NST * kStageBytes;
+  static constexpr int kConvOff = NST * kStageBytes;
+  static constexpr int kQOff = kReuseBytes;
   static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], empty[NST], xbar
   static constexpr int kRedOff = kBarOff + (2 * NST + 1) * 8;             // red_m, red_l [4][QROWS]
   static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l, sink [QROWS]
@@ -87,10 +95,10 @@ template <int D, int DV, int MT, int NST> struct Smem {
   // per-warp merge regions (rows padded by 4 floats: the fragment stores of one warp
   // instruction then spread over all banks) and the combine's chunk statistics reuse the stages
   static constexpr int kAccStride = DV + 4;
-  static_assert(kWarps * kQRows * kAccStride * 4 <= NST * kStageBytes, "merge regions must fit in the stages");
-  static_assert(2 * kMaxSplits * kQRows * 4 <= NST * kStageBytes, "chunk statistics must fit in the stages");
+  static_assert(kWarps * kQRows * kAccStride * 4 <= kReuseBytes, "merge regions must fit in the stages");
+  static_assert(2 * kMaxSplits * kQRows * 4 <= kReuseBytes, "chunk statistics must fit in the stages");
   static_assert((kWarps * kQRows * kAccStride + kQRows * DV + 4 * kMaxCluster + 2 * kMaxCluster * kQRows) * 4 <=
-                    NST * kStageBytes,
+                    kReuseBytes,
                 "cluster exchange buffers must fit in the stages");
 };
 
@@ -130,9 +138,48 @@ __device__ __forceinline__ void rotate8(const T *x1p, const T *x2p, const T *cp,
   }
 }
 
+// Eight values of the dtype as eight E4M3 codes of x / scale (fp32 division), one 8-byte word.
+template <typename T> __device__ __forceinline__ uint2 codes8(const uint4 &x, float scale) {
+  const T *e = reinterpret_cast<const T *>(&x);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j >> 2] |= (uint32_t)f32_to_e4m3(__fdiv_rn(to_f32(e[j]), scale)) << (8 * (j & 3));
+  return make_uint2(w[0], w[1]);
+}
+
+// Eight values of the dtype as eight f16 values (exact for any value in the f16 range).
+template <typename T> __device__ __forceinline__ uint4 to_half8(const uint4 &x) {
+  const T *e = reinterpret_cast<const T *>(&x);
+  uint4 r;
+  uint32_t *w = reinterpret_cast<uint32_t *>(&r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2 h = __floats2half2_rn(to_f32(e[2 * j]), to_f32(e[2 * j + 1]));
+    w[j] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  return r;
+}
+
+// Sixteen E4M3 codes (one 16-byte chunk) as sixteen f16 values, two 16-byte chunks.  Each
+// code goes through the pair conversion with both halves equal, so no lane order is assumed.
+__device__ __forceinline__ void widen16(const uint4 &codes, uint4 &lo, uint4 &hi) {
+  const uint32_t in[4] = {codes.x, codes.y, codes.z, codes.w};
+  uint32_t out[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t c0 = (in[j >> 1] >> (16 * (j & 1))) & 0xFFu, c1 = (in[j >> 1] >> (16 * (j & 1) + 8)) & 0xFFu;
+    const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(c0 | (c0 << 8))) & 0xFFFFu;
+    const uint32_t h1 = e4m3x2_to_f16x2((uint16_t)(c1 | (c1 << 8))) & 0xFFFFu;
+    out[j] = h0 | (h1 << 16);
+  }
+  lo = make_uint4(out[0], out[1], out[2], out[3]);
+  hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
 // Warp-wide: write the step's rows [r0, r1) of kv head h of sequence b to present (K
-// rotated when do_rotary), then make the generic-proxy stores visible to TMA reads.
-template <typename T, int D, int DV>
+// rotated when do_rotary; as E4M3 codes of an f8 cache when Q8), then make the
+// generic-proxy stores visible to TMA reads.
+template <typename T, int D, int DV, bool Q8 = false>
 __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, int past, int r0, int r1, int lane) {
   const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
   T *pk = reinterpret_cast<T *>(a.present_k), *pv = reinterpret_cast<T *>(a.present_v);
@@ -148,7 +195,23 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
     const size_t row = a.table ? ((size_t)a.table[(size_t)b * a.max_pages + pos / KT] * a.Hkv + h) * KT + pos % KT
                                : ((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos);
     const size_t tok = ((size_t)b * a.curr + i) * a.Hkv + h;
-    if (isk) {
+    if (Q8) {
+      uint8_t *p8 = reinterpret_cast<uint8_t *>(isk ? a.present_k : a.present_v);
+      if (isk) {
+        const size_t src = tok * D, dst = row * D;
+        uint4 y1 = *reinterpret_cast<const uint4 *>(kin + src + c);
+        uint4 y2 = *reinterpret_cast<const uint4 *>(kin + src + D / 2 + c);
+        if (a.do_rotary)
+          rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c,
+                     sn + (size_t)pos * (D / 2) + c, y1, y2);
+        const float sc = a.k_scale[h];
+        *reinterpret_cast<uint2 *>(p8 + dst + c) = codes8<T>(y1, sc);
+        *reinterpret_cast<uint2 *>(p8 + dst + D / 2 + c) = codes8<T>(y2, sc);
+      } else {
+        *reinterpret_cast<uint2 *>(p8 + row * DV + c) =
+            codes8<T>(*reinterpret_cast<const uint4 *>(vin + tok * DV + c), a.v_scale[h]);
+      }
+    } else if (isk) {
       const size_t src = tok * D, dst = row * D;
       if (a.do_rotary) {
         uint4 y1, y2;
@@ -168,12 +231,15 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
   __syncwarp();
 }
 
-template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK>
+// Q8: the cache holds E4M3 codes (one scale per kv head for K and V).  Each warp widens its
+// keys of a stage to f16 in shared memory and the MMAs run on f16 (q converted exactly);
+// the K scale joins the score scale and the V scale the output.
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         DecodeArgs a) {
-  using L = Smem<D, DV, MT, NST>;
-  using M = Mma16816<T>;
+  using L = Smem<D, DV, MT, NST, Q8>;
+  using M = Mma16816<typename std::conditional<Q8, __half, T>::type>;
   constexpr int QROWS = L::kQRows;
   constexpr int DCH = D / 8;    // 16-byte chunks per q / K row
   constexpr int VCH = DV / 8;   // 16-byte chunks per V row
@@ -215,6 +281,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   // the past length, the sink logits and the raw query rows are loaded together: their
   // latencies overlap
   const int past = a.seqlens[b];
+  const float smul = Q8 ? a.score_mul * a.k_scale[hkv] : a.score_mul;  // the K scale joins the score scale
+  const float vsc = Q8 ? a.v_scale[hkv] : 1.f;                           // and the V scale the output
   const float zsink = (threadIdx.x < R && a.head_sink) ? a.head_sink[hkv * a.G + threadIdx.x % a.G] : 0.f;
   constexpr int QITEMS = (QROWS * (DCH / 2) + kThreads - 1) / kThreads;  // chunk pairs per thread
   uint4 qraw[QITEMS][2];
@@ -282,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto issue = [&](int t) {
     const int s = t % NST, k0 = c0 + t * KT;
     if (appends && k0 + KT > past && k0 < total)
-      append_rows<T, D, DV>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane);
+      append_rows<T, D, DV, Q8>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane);
     if (lane == 0) {
       mbar_expect_tx(&full[s], L::kStageBytes);
       uint8_t *kdst = stages + s * L::kStageBytes;
@@ -292,8 +360,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         group = a.table[(size_t)b * a.max_pages + k0 / KT] * a.Hkv + hkv;
         row = 0;
       }
-      tma_load_4d(kdst, &tmk, 0, row, 0, group, &full[s]);  // [D/64][KT][64], [DV/64][KT][64]: one copy each
-      tma_load_4d(vdst, &tmv, 0, row, 0, group, &full[s]);
+      if constexpr (Q8) {  // [KT][128] codes each, one copy each
+        tma_load_3d(kdst, &tmk, 0, row, group, &full[s]);
+        tma_load_3d(vdst, &tmv, 0, row, group, &full[s]);
+      } else {  // [D/64][KT][64], [DV/64][KT][64]: one copy each
+        tma_load_4d(kdst, &tmk, 0, row, 0, group, &full[s]);
+        tma_load_4d(vdst, &tmv, 0, row, 0, group, &full[s]);
+      }
     }
     __syncwarp();
   };
@@ -315,6 +388,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         const size_t pos = (size_t)(past + r / a.G) * (D / 2);
         rotate8<T>(reinterpret_cast<const T *>(&qraw[u][0]), reinterpret_cast<const T *>(&qraw[u][1]),
                    cs + pos + c * 8, sn + pos + c * 8, y1, y2);
+      }
+      if (Q8) {  // the MMAs run on f16
+        y1 = to_half8<T>(y1);
+        y2 = to_half8<T>(y2);
       }
       const int c2 = c + DCH / 2;
       *reinterpret_cast<uint4 *>(qs + (c >> 3) * (QROWS * 128) + sw128(r, c & 7)) = y1;
@@ -389,8 +466,29 @@ __global__ void __launch_bounds__(kThreads, 2)
     if constexpr (MK) {
       if (t + 1 < ntiles) load_mask(t + 1, mnext);
     }
-    const uint32_t ks_u32 = smem_u32(stages + s * L::kStageBytes);
-    const uint32_t vs_u32 = ks_u32 + L::kTileBytes;
+    if constexpr (Q8) {
+      // widen this warp's 16 keys of the stage (rows of 128 codes, 128B-swizzled) to f16 in
+      // the layout of a 16-bit stage; only this warp reads these rows
+      static_assert(!Q8 || (D == 128 && DV == 128), "f8 cache: D = Dv = 128");
+      const uint8_t *k8 = stages + s * L::kStageBytes, *v8 = k8 + L::kTileBytes;
+      uint8_t *kc = smem + L::kConvOff, *vc = kc + KT * D * 2;
+      const int r = 16 * warp + (lane >> 1);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = (lane & 1) * 4 + cc;  // codes [16c, 16c + 16) of the row
+        const int e0 = 2 * c, e1 = 2 * c + 1;  // their f16 chunks
+        uint4 lo, hi;
+        widen16(*reinterpret_cast<const uint4 *>(k8 + r * 128 + ((c ^ (r & 7)) << 4)), lo, hi);
+        *reinterpret_cast<uint4 *>(kc + (e0 >> 3) * (KT * 128) + sw128(r, e0 & 7)) = lo;
+        *reinterpret_cast<uint4 *>(kc + (e1 >> 3) * (KT * 128) + sw128(r, e1 & 7)) = hi;
+        widen16(*reinterpret_cast<const uint4 *>(v8 + r * 128 + ((c ^ (r & 7)) << 4)), lo, hi);
+        *reinterpret_cast<uint4 *>(vc + (e0 >> 3) * (KT * 128) + sw128(r, e0 & 7)) = lo;
+        *reinterpret_cast<uint4 *>(vc + (e1 >> 3) * (KT * 128) + sw128(r, e1 & 7)) = hi;
+      }
+      __syncwarp();
+    }
+    const uint32_t ks_u32 = Q8 ? smem_u32(smem + L::kConvOff) : smem_u32(stages + s * L::kStageBytes);
+    const uint32_t vs_u32 = ks_u32 + (Q8 ? KT * D * 2 : L::kTileBytes);
 
     // ---- S = Q K^T over this warp's 16 keys
     float sacc[MT][2][4];
@@ -440,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               x = fmaf(to_f32(bv), a.mask_mul, x);  // the bias joins before the scale and softcap
             }
           }
-          x = a.cap_mul != 0.f ? tanh_fast(x * a.score_mul) * a.cap_mul : x * a.score_mul;
+          x = a.cap_mul != 0.f ? tanh_fast(x * smul) * a.cap_mul : x * smul;
           if (dropped) x = -INFINITY;
           if (edge) {
             const int row = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
@@ -496,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int first = max(0, total - kb);
       for (int idx = lane; idx < (16 - first) * VCH; idx += 32) {
         const int r = 16 * warp + first + idx / VCH, ch = idx % VCH;
-        *reinterpret_cast<uint4 *>(stages + s * L::kStageBytes + L::kTileBytes + (ch >> 3) * (KT * 128) +
+        *reinterpret_cast<uint4 *>((Q8 ? smem + L::kConvOff + KT * D * 2 : stages + s * L::kStageBytes + L::kTileBytes) +
+                                   (ch >> 3) * (KT * 128) +
                                    sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
@@ -650,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         den = row_l[r] * f + sink_term;
       }
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
-      const float inv = __frcp_rn(den);
+      const float inv = __frcp_rn(den) * vsc;
       store4(o, num.x * inv, num.y * inv, num.z * inv, num.w * inv);
     }
     return;
@@ -720,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         den = ll;
       }
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
-      const float inv = __frcp_rn(den);
+      const float inv = __frcp_rn(den) * vsc;
       store4(o, sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
     }
     return;  // nothing reads this CTA's shared memory any more
@@ -804,23 +903,28 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int i = r / a.G, g = r % a.G, hq = hkv * a.G + g;
     const float den = row_l[r] > 0.f ? row_l[r] : 1.f;  // no visible key: the sums are 0
     T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
-    const float inv = __frcp_rn(den);
+    const float inv = __frcp_rn(den) * vsc;
     store4(o, sum[u].x * inv, sum[u].y * inv, sum[u].z * inv, sum[u].w * inv);
   }
 }
 
-template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK>
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false>
 gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
-  using L = Smem<D, DV, MT, NST>;
+  using L = Smem<D, DV, MT, NST, Q8>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
   CUtensorMap tk, tv;
   // contiguous or ring: [B*Hkv][cap][D] and [..][DV]; paged: [num_pages*Hkv][64][D]
   const bool paged = c.block_table != nullptr;
   const long long outer = paged ? (long long)c.num_pages * c.p.kv_heads : (long long)c.p.batch * c.p.kv_heads;
   const int rows = paged ? KT : c.p.cap_present;
-  if (!encode_kv_tile_map(&tk, c.present_k, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
-  if (!encode_kv_tile_map(&tv, c.present_v, DV, rows, outer, KT, 2)) return GQA_ERR_CUDA;
-  auto kern = decode_split_kernel<T, D, DV, MT, NST, CL, MK>;
+  if (Q8) {  // [B*Hkv][cap][128] codes: a 64-row box of whole 128-byte rows
+    if (!encode_kv8_map(&tk, c.present_k, D, rows, outer, KT)) return GQA_ERR_CUDA;
+    if (!encode_kv8_map(&tv, c.present_v, DV, rows, outer, KT)) return GQA_ERR_CUDA;
+  } else {
+    if (!encode_kv_tile_map(&tk, c.present_k, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
+    if (!encode_kv_tile_map(&tv, c.present_v, DV, rows, outer, KT, 2)) return GQA_ERR_CUDA;
+  }
+  auto kern = decode_split_kernel<T, D, DV, MT, NST, CL, MK, Q8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -844,10 +948,11 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-template <typename T, bool CL, bool MK, bool MIXED>
+template <typename T, bool CL, bool MK, bool MIXED, bool Q8>
 gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a);
 
-template <typename T, bool MK, bool MIXED> gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
+template <typename T, bool MK, bool MIXED, bool Q8 = false>
+gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   const gqa_params &p = c.p;
   DecodeArgs a;
   a.q = c.q_in;
@@ -897,16 +1002,23 @@ template <typename T, bool MK, bool MIXED> gqa_status launch_t(const Call &c, co
     a.score_mul = p.scale * kLog2e;
     a.cap_mul = 0.f;
   }
-  if (dp.cluster) return dispatch<T, true, MK, MIXED>(c, dp, a);
-  return dispatch<T, false, MK, MIXED>(c, dp, a);
+  a.k_scale = c.k_scale;
+  a.v_scale = c.v_scale;
+  if (dp.cluster) return dispatch<T, true, MK, MIXED, Q8>(c, dp, a);
+  return dispatch<T, false, MK, MIXED, Q8>(c, dp, a);
 }
 
 // (D, DV, MT, NST): equal head dims (MIXED false) or V head dim != Q/K head dim (MIXED true,
 // up to 32 query rows per group; four stages of 24 KB)
-template <typename T, bool CL, bool MK, bool MIXED>
+template <typename T, bool CL, bool MK, bool MIXED, bool Q8>
 gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   const int D = c.p.head_dim, DV = c.Dv;
-  if constexpr (!MIXED) {
+  if constexpr (Q8) {  // f8 cache: D = Dv = 128, four 16 KB stages and a 32 KB f16 tile
+    if (D == 128 && DV == 128 && !MK && !MIXED) {
+      if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 4, CL, false, true>(c, dp, a);
+      if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 4, CL, false, true>(c, dp, a);
+    }
+  } else if constexpr (!MIXED) {
     if (D == 128 && DV == 128) {
       if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 3, CL, MK>(c, dp, a);
       if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 3, CL, MK>(c, dp, a);
@@ -930,10 +1042,11 @@ gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
 
 // The decode launch for one dtype switch; each .cu file instantiates one (MK, MIXED) pair
 // (masked or not, equal or different head dims), so the sets compile in parallel.
-template <bool MK, bool MIXED> gqa_status launch_decode_split_impl(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
+template <bool MK, bool MIXED, bool Q8 = false>
+gqa_status launch_decode_split_impl(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   switch (c.p.dtype) {
-    case GQA_F16: return launch_t<__half, MK, MIXED>(c, dp, wl);
-    case GQA_BF16: return launch_t<__nv_bfloat16, MK, MIXED>(c, dp, wl);
+    case GQA_F16: return launch_t<__half, MK, MIXED, Q8>(c, dp, wl);
+    case GQA_BF16: return launch_t<__nv_bfloat16, MK, MIXED, Q8>(c, dp, wl);
   }
   return GQA_ERR_UNSUPPORTED;
 }

@@ -104,6 +104,19 @@ bool encode_kv_tile_map(CUtensorMap *map, const void *base, int D, int rows, lon
   return r == CUDA_SUCCESS;
 }
 
+bool encode_kv8_map(CUtensorMap *map, const void *base, int inner, int rows, long long outer, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)inner * rows};
+  cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B, int box_rows, int esize) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -314,6 +327,43 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   return launch_prefill_tc(c);
 }
 
+// f8 (E4M3) cache: the step's K/V quantized on append, attention over code * scale.  The
+// split decode kernel takes D = Dv = 128 shapes in its envelope; everything else runs the
+// RoPE/append kernel and the CUDA-core kernel.
+gqa_status run_attention_q8(Mode mode, const gqa_params *p, const void *q, const void *k, const void *v,
+                            const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                            const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                            uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, void *stream) {
+  Call c;
+  gqa_status s = make_call(c, p, q, k, v, nullptr, nullptr, seqlens_k, cos_cache, sin_cache, head_sink, out,
+                           present_k, present_v, dev_status, stream);
+  if (s != GQA_OK) return s;
+  if (p->kv_ring) return GQA_ERR_UNSUPPORTED;
+  if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return GQA_ERR_INVALID_ARG;
+  if (!out || !aligned16(out)) return GQA_ERR_INVALID_ARG;
+  c.q8 = 1;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  const bool rotate = c.append && p->do_rotary;
+  const WsLayout wl = workspace_layout(c.p, rotate);
+  const DecodePlan dp = decode_plan(c.p);
+  const bool fused = mode == kDecode && dp.eligible && p->head_dim == 128 && c.Dv == 128;
+  const size_t need = fused ? (dp.splits > 1 && !dp.cluster ? wl.total : 0) : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
+  if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return GQA_ERR_WORKSPACE;
+  c.ws = static_cast<char *>(workspace);
+  c.ws_bytes = workspace_bytes;
+  if (fused) return launch_decode_split_q8(c, dp, wl);
+  if (c.append) {
+    c.q_rot = rotate ? c.ws + wl.q_rot_off : nullptr;
+    s = launch_rope_append(c);
+    if (s != GQA_OK) return s;
+    if (rotate) c.q = c.q_rot;
+  }
+  return launch_attention_simt(c);
+}
+
 }  // namespace
 }  // namespace gqa
 
@@ -362,6 +412,24 @@ gqa_status gqa_attention_prefill_masked(const gqa_params *p, const gqa_mask *mas
   if (!mask) return GQA_ERR_INVALID_ARG;
   return gqa::run_attention(gqa::kPrefill, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream, mask);
+}
+
+gqa_status gqa_attention_decode_q8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                   const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                   const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                   uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream) {
+  return gqa::run_attention_q8(gqa::kDecode, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale,
+                               out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_attention_prefill_q8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                    const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                    uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
+                                    int32_t *dev_status, void *stream) {
+  return gqa::run_attention_q8(gqa::kPrefill, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
+                               v_scale, out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
 
 gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const void *k, const void *v,

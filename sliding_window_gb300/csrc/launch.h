@@ -37,6 +37,9 @@ struct Call {
   const void *mask = nullptr;
   int mask_kind = 0, mask_keys = 0;
   long long mask_sb = 0, mask_sh = 0, mask_si = 0;
+  // f8 cache: present_k/v hold E4M3 codes; the stored value is code * scale of the kv head
+  int q8 = 0;
+  const float *k_scale = nullptr, *v_scale = nullptr;
   int32_t *status = nullptr;
   cudaStream_t stream = nullptr;
   char *ws = nullptr;
@@ -75,6 +78,9 @@ bool encode_kv_map(CUtensorMap *map, const void *base, int inner, int mid, long 
 // box_rows rows lands as [D/64][box_rows][64 columns], 128B-swizzled: one copy per tile.
 bool encode_kv_tile_map(CUtensorMap *map, const void *base, int D, int rows, long long outer, int box_rows,
                         int esize);
+// 3D map over an f8 cache [outer, rows, inner] of bytes (inner <= 128): box {inner, box_rows,
+// 1}, 128B-swizzled rows.
+bool encode_kv8_map(CUtensorMap *map, const void *base, int inner, int rows, long long outer, int box_rows);
 // 4D map over q laid out [B, L, H, D]: box {64, 1, box_rows, 1}, 128B swizzle.
 bool encode_q_map(CUtensorMap *map, const void *base, int D, int H, int L, int B, int box_rows, int esize);
 
@@ -91,6 +97,7 @@ gqa_status launch_attention_simt(const Call &c);
 gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_decode_split_masked(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_decode_split_vdim(const Call &c, const DecodePlan &dp, const WsLayout &wl);  // Dv != D
+gqa_status launch_decode_split_q8(const Call &c, const DecodePlan &dp, const WsLayout &wl);    // f8 cache, D = Dv = 128
 gqa_status launch_prefill_tc(const Call &c);
 gqa_status launch_prefill_tc_masked(const Call &c);  // c.mask set: kind 1 or 2
 gqa_status launch_prefill_tc_vdim(const Call &c);    // Dv != D, no mask

@@ -53,7 +53,25 @@ struct RopeArgs {
   int32_t *status;
   int B, Hq, Hkv, D, Dv, curr, cap_present, cap_past, rope_len, do_rotary, past_separate;
   int ring;  // present is a ring: position p in slot p % cap_present
+  // f8 cache: present_k/v hold E4M3 codes of x / scale (fp32 division), one scale per kv head
+  int q8;
+  const float *k_scale, *v_scale;
 };
+
+// N consecutive codes of x[e] / scale, stored as one N-byte word
+template <typename T, int N> __device__ __forceinline__ void store_codes(uint8_t *dst, const T *x, float scale) {
+  uint32_t w[N / 4];
+#pragma unroll
+  for (int j = 0; j < N / 4; ++j) {
+    w[j] = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[j] |= (uint32_t)f32_to_e4m3(__fdiv_rn(to_f32(x[4 * j + e]), scale)) << (8 * e);
+  }
+  if constexpr (N == 8)
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+  else
+    *reinterpret_cast<uint32_t *>(dst) = w[0];
+}
 
 // One block per (b, i).  Work items: (head, chunk) over Hq q heads (when q_rot is wanted)
 // and Hkv k heads, each N elements of each half of the row; then (v head, chunk) over Hkv
@@ -80,10 +98,17 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
   const T *sinr = reinterpret_cast<const T *>(a.sin) + (size_t)pos * half;
   const size_t slot = a.ring ? pos % a.cap_present : pos;
   for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    if (it >= items_qk) {  // v: a plain copy of one 16-byte chunk
+    if (it >= items_qk) {  // v: a plain copy of one 16-byte chunk (or its codes)
       const int h = (it - items_qk) / v_per_head, c = ((it - items_qk) % v_per_head) * N;
       const T *src = reinterpret_cast<const T *>(a.v) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.Dv;
-      T *dst = reinterpret_cast<T *>(a.present_v) + (((size_t)b * a.Hkv + h) * a.cap_present + slot) * a.Dv;
+      const size_t row = ((size_t)b * a.Hkv + h) * a.cap_present + slot;
+      if (a.q8) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(src + c);
+        store_codes<T, N>(reinterpret_cast<uint8_t *>(a.present_v) + row * a.Dv + c, reinterpret_cast<const T *>(&x),
+                          a.v_scale[h]);
+        continue;
+      }
+      T *dst = reinterpret_cast<T *>(a.present_v) + row * a.Dv;
       *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<const uint4 *>(src + c);
       continue;
     }
@@ -99,7 +124,22 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
     } else {
       const int h = head - nq;
       src = reinterpret_cast<const T *>(a.k) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.D;
-      dst = reinterpret_cast<T *>(a.present_k) + (((size_t)b * a.Hkv + h) * a.cap_present + slot) * a.D;
+      const size_t row = ((size_t)b * a.Hkv + h) * a.cap_present + slot;
+      if (a.q8) {  // the row in the dtype as without quantization, then its codes
+        uint4 y1, y2;
+        T *p1 = reinterpret_cast<T *>(&y1), *p2 = reinterpret_cast<T *>(&y2);
+        if (rot) {
+          rotate_chunk<T>(src + c, src + half + c, cosr + c, sinr + c, p1, p2);
+        } else {
+          y1 = *reinterpret_cast<const uint4 *>(src + c);
+          y2 = *reinterpret_cast<const uint4 *>(src + half + c);
+        }
+        uint8_t *k8 = reinterpret_cast<uint8_t *>(a.present_k) + row * a.D;
+        store_codes<T, N>(k8 + c, p1, a.k_scale[h]);
+        store_codes<T, N>(k8 + half + c, p2, a.k_scale[h]);
+        continue;
+      }
+      dst = reinterpret_cast<T *>(a.present_k) + row * a.D;
     }
     if (rot) {
       rotate_chunk<T>(src + c, src + half + c, cosr + c, sinr + c, dst + c, dst + half + c);
@@ -173,6 +213,9 @@ template <typename T> static gqa_status launch_t(const Call &c) {
   a.rope_len = p.rope_len;
   a.do_rotary = p.do_rotary;
   a.past_separate = c.past_separate;
+  a.q8 = c.q8;
+  a.k_scale = c.k_scale;
+  a.v_scale = c.v_scale;
   if (c.past_separate) {
     const gqa_status st = launch_copy_t<T>(c);
     if (st != GQA_OK) return st;

@@ -33,7 +33,8 @@ TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decode", "gqa_rope_append_kv",
             "gqa_status_string", "gqa_abi_version", "gqa_attention_decode_noalloc", "gqa_attention_decode_paged",
-            "gqa_attention_decode_masked", "gqa_attention_prefill_masked"]
+            "gqa_attention_decode_masked", "gqa_attention_prefill_masked", "gqa_attention_decode_q8",
+            "gqa_attention_prefill_q8"]
 MASK_KEEP, MASK_ADD = 1, 2
 PAGE = 64  # positions per page of a paged cache
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES
@@ -95,6 +96,9 @@ def _load():
     lib.gqa_attention_decode_masked.restype = i32
     lib.gqa_attention_prefill_masked.argtypes = [pp, ctypes.POINTER(GqaMask)] + [vp] * 13 + [sz, vp, vp]
     lib.gqa_attention_prefill_masked.restype = i32
+    for name in ("gqa_attention_decode_q8", "gqa_attention_prefill_q8"):
+        getattr(lib, name).argtypes = [pp] + [vp] * 13 + [sz, vp, vp]
+        getattr(lib, name).restype = i32
     lib.gqa_status_string.argtypes = [i32]
     lib.gqa_status_string.restype = ctypes.c_char_p
     lib.gqa_abi_version.argtypes = []
@@ -197,6 +201,28 @@ def gqa_attention_prefill_masked(p, mask: "GqaMask", q, k, v, past_k, past_v, se
                                                 _ptr(sin_cache), _ptr(head_sink), _ptr(out), _ptr(present_k),
                                                 _ptr(present_v), _ptr(workspace), _nbytes(workspace),
                                                 _ptr(dev_status), _stream(stream)))
+
+
+def _q8(name, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale, out, present_k8, present_v8,
+        workspace, dev_status, stream):
+    return int(getattr(lib, name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(seqlens_k), _ptr(cos_cache),
+                                  _ptr(sin_cache), _ptr(head_sink), _ptr(k_scale), _ptr(v_scale), _ptr(out),
+                                  _ptr(present_k8), _ptr(present_v8), _ptr(workspace), _nbytes(workspace),
+                                  _ptr(dev_status), _stream(stream)))
+
+
+def gqa_attention_decode_q8(p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale, out,
+                            present_k8, present_v8, workspace, dev_status, stream=None) -> int:
+    """Decode over an f8 (E4M3) cache with per-kv-head scales (see include/gqa.h)."""
+    return _q8("gqa_attention_decode_q8", p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale,
+               out, present_k8, present_v8, workspace, dev_status, stream)
+
+
+def gqa_attention_prefill_q8(p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale, out,
+                             present_k8, present_v8, workspace, dev_status, stream=None) -> int:
+    """Prefill over an f8 (E4M3) cache with per-kv-head scales (see include/gqa.h)."""
+    return _q8("gqa_attention_prefill_q8", p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale,
+               out, present_k8, present_v8, workspace, dev_status, stream)
 
 
 def gqa_attention_decode_paged(p, q, k, v, seqlens_k, block_table, num_pages, cos_cache, sin_cache, head_sink, out,
