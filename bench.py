@@ -58,15 +58,19 @@ def band(w, past, window):
     return lo, total
 
 
+def cache_esize(w):
+    return 1 if w.kv_q8 else esize(w)
+
+
 def kv_read_bytes(w, seqlens, window):
     return sum((hi - lo) for lo, hi in (band(w, p, window) for p in seqlens.tolist())) * \
-        w.kv_heads * (w.head_dim + vdim(w)) * esize(w)
+        w.kv_heads * (w.head_dim + vdim(w)) * cache_esize(w)
 
 
 def io_bytes(w):
-    """q read + out written + new k/v read and appended."""
-    e = esize(w)
-    return w.batch * w.q_len * e * (w.q_heads + 2 * w.kv_heads) * (w.head_dim + vdim(w))
+    """q read + out written + new k/v read and appended (in the cache's element size)."""
+    e, ec = esize(w), cache_esize(w)
+    return w.batch * w.q_len * (w.q_heads * e + w.kv_heads * (e + ec)) * (w.head_dim + vdim(w))
 
 
 def visible_pairs(w, seqlens, window):
@@ -84,7 +88,7 @@ def step_work(w, seqs):
     if w.mode == "decode":
         kv = sum(kv_read_bytes(w, s, win) for s, win in zip(seqs, w.windows))
         io = io_bytes(w) * w.layers
-        append = 2 * w.batch * w.q_len * w.kv_heads * (w.head_dim + vdim(w)) * esize(w)
+        append = w.batch * w.q_len * w.kv_heads * (w.head_dim + vdim(w)) * (esize(w) + cache_esize(w))
         return (kv + io) / 1e9, (kv + (io_bytes(w) - append) * w.layers) / 1e9, "GB/s"
     flops = sum(2.0 * (w.head_dim + vdim(w)) * visible_pairs(w, s, win) for s, win in zip(seqs, w.windows))
     return flops / 1e12, flops / 1e12, "TFLOP/s"
@@ -196,6 +200,8 @@ class Step:
             L = dict(c=c, p=p, p_attend=gqa.params_from_dict(dict(c.params, do_rotary=0)), ws=ws,
                      out=torch.empty_like(c.q), q_rot=torch.empty_like(c.q),
                      status=torch.zeros(1, dtype=torch.int32, device=device))
+            if w.kv_q8:  # the cache is f8 codes: the dtype caches are replaced by them
+                c.past_k, c.past_v = c.extra["k8"], c.extra["v8"]
             if w.mask:  # device-resident like the cache (a bias computed or reused on the device)
                 L["mask_t"] = c.extra["mask"]
                 L["mask"] = gqa.mask_from_tensor(L["mask_t"], gqa.MASK_ADD)
@@ -214,6 +220,7 @@ class Step:
             self.layers.append(L)
         self.fn = gqa.gqa_attention_decode if w.mode == "decode" else gqa.gqa_attention_prefill
         self.fn_masked = gqa.gqa_attention_decode_masked if w.mode == "decode" else gqa.gqa_attention_prefill_masked
+        self.fn_q8 = gqa.gqa_attention_decode_q8 if w.mode == "decode" else gqa.gqa_attention_prefill_q8
         # all layers' outputs side by side, for one device->host copy per step
         self.out_all = torch.empty(sum(L["out"].numel() for L in self.layers), dtype=self.layers[0]["out"].dtype,
                                    device=device)
@@ -240,7 +247,7 @@ class Step:
                                    c.head_sink, L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "step")
 
     def append_only(self, stream):
-        if self.w.kv_paged:  # the paged call appends itself: one full (untimed) step puts the rows in
+        if self.w.kv_paged or self.w.kv_q8:  # the call appends itself: one full (untimed) step puts the rows in
             assert not self.w.do_rotary
             self.full(stream)
             return
@@ -263,8 +270,15 @@ class Step:
             self.g.check(self.call(L, L["p_attend"], q, None, None, None, None, c.seqlens_k, None, None, c.head_sink,
                                    L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "attend")
 
-    def call(self, L, p, *args):
-        """The layer's public call: the masked entry point when the workload has a mask."""
+    def call(self, L, p, q, k, v, past_k, past_v, seqlens, cos, sin, sink, out, present_k, present_v, ws, st,
+             stream):
+        """The layer's public call: the masked entry point when the workload has a mask, the
+        f8-cache one when its cache is quantized."""
+        if self.w.kv_q8:
+            c = L["c"]
+            return self.fn_q8(p, q, k, v, seqlens, cos, sin, sink, c.extra["k_scale"], c.extra["v_scale"], out,
+                              present_k, present_v, ws, st, stream)
+        args = (q, k, v, past_k, past_v, seqlens, cos, sin, sink, out, present_k, present_v, ws, st, stream)
         if "mask" in L:
             return self.fn_masked(p, L["mask"], *args)
         return self.fn(p, *args)
@@ -545,13 +559,22 @@ class OracleSample:
                                     cos=None if c.cos is None else _storage(c.cos),
                                     sin=None if c.sin is None else _storage(c.sin),
                                     sink=None if c.head_sink is None else c.head_sink.numpy(), rows=ridx,
-                                    mask=_storage(c.extra["mask"]) if "mask" in c.extra else None))
+                                    mask=_storage(c.extra["mask"]) if "mask" in c.extra else None,
+                                    q8=None if "k8" not in c.extra else (
+                                        c.extra["k8"].numpy().copy(), c.extra["v8"].numpy().copy(),
+                                        c.extra["k_scale"].numpy(), c.extra["v_scale"].numpy())))
         self.units = units
         self.sample = desc + (" x %d layers" % self.w.layers if self.w.layers > 1 else "")
 
     def run(self):
         o = self.oracle
         for L in self.layers:
+            if L["q8"] is not None:
+                k8, v8, ks, vs = L["q8"]
+                q_rot, _ = o.rope_append_q8(L["p"], L["q"], L["k"], L["v"], k8, v8, L["seq"], ks, vs, L["cos"],
+                                            L["sin"])
+                o.attention_q8(L["p"], q_rot, k8, v8, L["seq"], ks, vs, L["sink"], rows=L["rows"])
+                continue
             if L["p"].get("kv_ring", 0):
                 q_rot, pk, pv, _ = o.rope_append_ring(L["p"], L["q"], L["k"], L["v"], L["pk"], L["pv"], L["seq"],
                                                       L["cos"], L["sin"])
@@ -601,7 +624,8 @@ def main():
         args.steps = {"decode_window_bf16": 100000, "specdecode_rotary_f16": 20000, "decode_long_bf16": 1500,
                       "prefill_sink_softcap_bf16": 500, "prefill_fp32_tiny": 20000,
                       "decode_window_ring_bf16": 100000, "decode_window_paged_bf16": 100000,
-                      "decode_window_vdim_bf16": 100000, "prefill_bias_bf16": 400}.get(args.workload, 1000)
+                      "decode_window_vdim_bf16": 100000, "prefill_bias_bf16": 400,
+                      "decode_window_q8_bf16": 100000}.get(args.workload, 1000)
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

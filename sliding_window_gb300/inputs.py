@@ -50,6 +50,7 @@ class Workload:
     kv_paged: int = 0       # 1: the cache is a shared pool of 64-position pages behind a block table
     mask: str = ""          # "add": an additive attention bias [B, 1, S, cap] of the dtype, N(0,1)
     v_head_dim: int = 0     # Dv; 0: the same as head_dim
+    kv_q8: int = 0          # 1: the cache holds f8 E4M3 codes with one scale per kv head for K and V
 
     @property
     def layers(self) -> int:
@@ -92,6 +93,9 @@ WORKLOADS = {
         # the windowed decode with a V head dim of 64 under a Q/K head dim of 128
         Workload("decode_window_vdim_bf16", 8, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
                  windows=(1024,), v_head_dim=64),
+        # the windowed decode over an f8 cache (one byte per cached element)
+        Workload("decode_window_q8_bf16", 9, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
+                 windows=(1024,), kv_q8=1),
         # the long prompt with a dense additive attention bias, broadcast over the heads
         Workload("prefill_bias_bf16", 7, "prefill", "bf16", 2, 64, 8, 128, 8192, 8192, 0, 0,
                  windows=(4096,), softcap=50.0, head_sink=True, mask="add"),
@@ -203,6 +207,23 @@ def make_case(w: Workload, layer: int = 0, device="cpu", seed_offset: int = 0, g
         extra["mask"] = m
     elif w.mask:
         raise ValueError(w.mask)
+    if w.kv_q8:
+        # f8 cache: the past as random finite E4M3 codes (sign, exponent field 1..11, fraction)
+        # drawn directly as bytes, scales U[0.01, 0.02] per kv head; q/k/v stay in the dtype
+        qg = torch.Generator(device=dev)
+        qg.manual_seed(7000 + w.index + 104729 * layer + 7919 * seed_offset)
+        Dv = w.v_head_dim or D
+
+        def codes(*shape):
+            sign = torch.randint(0, 2, shape, generator=qg, device=dev, dtype=torch.int32) << 7
+            expo = torch.randint(1, 12, shape, generator=qg, device=dev, dtype=torch.int32) << 3
+            frac = torch.randint(0, 8, shape, generator=qg, device=dev, dtype=torch.int32)
+            return (sign | expo | frac).to(torch.uint8)
+
+        extra["k8"] = codes(B, Hkv, cap, D)
+        extra["v8"] = codes(B, Hkv, cap, Dv)
+        extra["k_scale"] = torch.rand(Hkv, generator=qg, device=dev, dtype=torch.float32) * 0.01 + 0.01
+        extra["v_scale"] = torch.rand(Hkv, generator=qg, device=dev, dtype=torch.float32) * 0.01 + 0.01
     return Case(w, layer, w.params(layer), q, k, v, past_k, past_v,
                 torch.from_numpy(seq).to(dev), cos, sin, sink, extra)
 
