@@ -54,3 +54,15 @@ def test_kernels_per_layer(name, launches):
     tokens = 32 rows per group at D = 128 fit the split kernel."""
     w = WORKLOADS[name]
     assert bench.kernels_per_layer(w) == launches
+
+
+def test_f8_cache_bytes_by_hand():
+    """An f8 cache: one byte per cached element read and appended; q, out and the new rows
+    read in the dtype."""
+    w = WORKLOADS["decode_window_q8_bf16"].scaled(batch=1)
+    seqs = [np.array([2000], dtype=np.int32)]
+    units, kunits, _ = bench.step_work(w, seqs)
+    kv = 1024 * w.kv_heads * 256 * 1
+    io = 1 * 1 * (w.q_heads * 2 + w.kv_heads * (2 + 1)) * 256
+    assert units == pytest.approx((kv + io) / 1e9, rel=0, abs=1e-15)
+    assert kunits == pytest.approx((kv + io - w.kv_heads * 256 * 3) / 1e9, rel=0, abs=1e-15)
