@@ -64,8 +64,9 @@
  * GQA_ERR_UNSUPPORTED).  seqlens_k is the absolute past length and may exceed cap_present;
  * the band predicate is unchanged.  gqa_rope_append_kv appends into a ring the same way.
  *
- * Ownership and memory: the caller owns every buffer; all pointers except the params
- * struct are device pointers, 16-byte aligned.  The library allocates no memory (it uses
+ * Ownership and memory: the caller owns every buffer; all pointers except the params and
+ * mask structs are device pointers, 16-byte aligned (seqlens_k, head_sink and the f8
+ * scales 4-byte aligned).  The library allocates no memory (it uses
  * the caller's workspace) and keeps no state between calls apart from the counters it
  * leaves zeroed in the workspace.  present may alias past (same pointer): an in-place
  * append that writes only rows [past_b, total_b).  Otherwise rows [0, past_b) of past are
@@ -160,7 +161,8 @@ gqa_status gqa_attention_prefill(const gqa_params *p, const void *q, const void 
  * visible keys and reads each K/V byte once.  The partial (max, sum, acc) of a group's
  * chunks are merged in distributed shared memory when the chunks form one thread-block
  * cluster (2..8 chunks, launch of one wave), else by the last CTA of the group through the
- * workspace.  For G*curr > 64 (D=64) or > 32 (D=128), or f32, the fp32 SIMT kernel runs. */
+ * workspace.  For G*curr > 64 (D=64) or > 32 (D=128 or Dv != D), or f32, the fp32 SIMT
+ * kernel runs. */
 gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *k, const void *v,
                                 const void *past_k, const void *past_v, const int32_t *seqlens_k,
                                 const void *cos_cache, const void *sin_cache, const float *head_sink,
@@ -177,7 +179,7 @@ gqa_status gqa_rope_append_kv(const gqa_params *p, const void *q, const void *k,
                               const void *cos_cache, const void *sin_cache, void *q_rot, void *present_k,
                               void *present_v, int32_t *dev_status, void *stream);
 
-/* Decode without a workspace.  The paper has no counterpart: this entry point exists for
+/* Decode without a workspace.  No page describes this entry point; it exists for
  * callers that cannot allocate device memory where they run attention -- a plugin hosted by
  * an inference engine that owns all device memory and gives its plugins no allocator, or a
  * latency-critical loop in which a cudaMalloc (which can synchronize the device) is not
