@@ -13,9 +13,9 @@
 
 namespace gqa {
 
-// A pipeline wait that has not completed after this many SM cycles (about 2 s at 2 GHz,
-// 4 s at 1 GHz) gives up, sets GQA_DEV_TIMEOUT and lets the kernel drain and return
-// instead of hanging the GPU.  The SM cycle counter is cheap to read, unlike the global
+// A pipeline wait that has not completed after this many SM cycles (about 2 s at the
+// GB300's 2.07 GHz maximum SM clock, up to 4 s at 1 GHz) gives up, sets GQA_DEV_TIMEOUT
+// and lets the kernel drain and return instead of hanging the GPU.  The SM cycle counter is cheap to read, unlike the global
 // timer, so the bound costs nothing on the fast path.
 constexpr long long kWaitLimitCycles = 4000000000ll;
 

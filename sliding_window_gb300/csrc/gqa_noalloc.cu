@@ -46,14 +46,21 @@ extern "C" gqa_status gqa_attention_decode_noalloc(const gqa_params *p, const vo
                                                    const float *head_sink, void *out, void *present_k,
                                                    void *present_v, int32_t *dev_status, void *stream) {
   if (!p) return GQA_ERR_INVALID_ARG;
-  const size_t need = gqa_workspace_bytes(p);  // 0 for invalid params: the call below rejects them
+  // validate before anything else: the scratch layout below is only meaningful (and only
+  // bounded by the array) for params that pass the checks
+  const size_t need = gqa_workspace_bytes(p);  // 0 for invalid params, or when no scratch is needed
+  if (need == 0)
+    return gqa_attention_decode(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink, out,
+                                present_k, present_v, nullptr, 0, dev_status, stream);
   if (need > (size_t)GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_WORKSPACE;
+  const gqa::WsLayout wl = gqa::workspace_layout(*p, p->do_rotary != 0);
+  if (wl.total > (size_t)GQA_NOALLOC_SCRATCH_BYTES || wl.tickets_off + wl.tickets_bytes > wl.total)
+    return GQA_ERR_WORKSPACE;
   void *scratch = nullptr;
   gqa_status s = scratch_address(&scratch);
   if (s != GQA_OK) return s;
   // the split tickets must start at zero: the array keeps whatever the previous call left
   // (normally zeros, but not after a call whose waits timed out), so clear them every call
-  const gqa::WsLayout wl = gqa::workspace_layout(*p, p->do_rotary != 0);
   if (wl.tickets_bytes > 0 &&
       cudaMemsetAsync(static_cast<char *>(scratch) + wl.tickets_off, 0, wl.tickets_bytes,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

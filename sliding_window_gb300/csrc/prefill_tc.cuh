@@ -7,18 +7,24 @@
 // window band in absolute positions ("Sliding window"); the sink joins the denominator
 // ("smooth_softmax / head_sink").  tract PR #2645 ("What changed"): bottom-right band.
 //
-// One CTA = one tile of 128 query rows of one (b, q head).  Roles (6 warps):
-//   warp 0  producer: TMA loads of the Q tile once, then one K and one V tile (128 keys,
-//           128B swizzle) per step, each into a single buffer released by tcgen05.commit
-//   warp 1  TMEM owner + MMA issuer (one thread): S = Q K^T (M=128, N=128, K=D) into TMEM,
-//           then O += P V (N = DV, the V head dim) with P read from TMEM (it overwrites S in
-//           place, bf16 pairs)
-//   warps 2-5  softmax: thread = one TMEM lane = one query row; tcgen05.ld of S, band mask
-//           on frontier tiles only, scale/softcap, exp2 online softmax with a lazily
-//           rescaled reference max, P back to TMEM with tcgen05.st, final O / l epilogue
-// Two CTAs share an SM (96 KB shared memory and 256 TMEM columns each), so one CTA's
-// softmax overlaps the other's MMAs.  KV tiles outside [window low, causal high] are never
-// visited; only tiles that cross a frontier evaluate the per-element predicate.
+// One CTA = one tile of 128 query rows of TWO q heads of the same kv group (they share
+// every K/V tile and have the same band), 12 warps, one CTA per SM (about 198 KB of shared
+// memory and all 512 TMEM columns: S_A, S_B, O_A, O_B, 128 columns each).  Roles:
+//   warp 0  producer: TMA loads of both Q tiles once, then K tiles (128 keys, 128B swizzle)
+//           through a ring of kKStages and V tiles through two stages, each released by a
+//           tcgen05.commit of the MMAs that read it
+//   warp 1  TMEM owner + MMA issuer (one thread): S = Q K^T (M=128, N=128, K=D) into TMEM
+//           per head, then O += P V (N = DV, the V head dim) with P read from TMEM (it
+//           overwrites the first columns of S in place as packed pairs); the issue order
+//           S_A(t), S_B(t), PV_A(t-1), ... interleaves the heads so one head's softmax
+//           overlaps the other head's MMAs
+//   warp 2  mask producer (masked kernels only; idle otherwise), warp 3 idle
+//   warps 4-7 and 8-11  one softmax warpgroup per head: thread = one TMEM lane = one query
+//           row; tcgen05.ld of S, band mask on frontier tiles only, scale/softcap, exp2
+//           online softmax with a lazily rescaled reference max, P back to TMEM with
+//           tcgen05.st, final O / l epilogue
+// KV tiles outside [window low, causal high] are never visited; only tiles that cross a
+// frontier evaluate the per-element predicate.
 // The sink starts the running state: m = z*log2(e), l = 1, so it is counted exactly once.
 //
 // With an attention mask (MK = 1 boolean keep flags, 2 additive values per head, 3 additive

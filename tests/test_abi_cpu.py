@@ -296,3 +296,30 @@ def test_q8_invalid_arguments(g, fn, ptrs, code):
 @pytest.mark.parametrize("fn", ["gqa_attention_decode_q8", "gqa_attention_prefill_q8"])
 def test_q8_rejects_a_ring(g, fn):
     assert call_q8(g, good_params(g, kv_ring=1, window=1000), fn) == 2
+
+
+def call_noalloc(g, p, **ptrs):
+    names = ["q", "k", "v", "past_k", "past_v", "seqlens_k", "cos", "sin", "head_sink", "out", "present_k",
+             "present_v"]
+    vals = {n: FAKE for n in names}
+    vals.update(ptrs)
+    a = [ctypes.c_void_p(vals[n]) if vals[n] is not None else None for n in names]
+    return g.lib.gqa_attention_decode_noalloc(ctypes.byref(p), *a, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kv_heads=0), 1),                                   # would divide by zero in the scratch plan
+    (dict(batch=1 << 20, dtype=7), 1),                       # invalid dtype with a huge batch
+    (dict(batch=1 << 20, head_dim=96), 2),                   # unsupported head dim with a huge batch
+    (dict(batch=1 << 20, window=-1, cap_present=1 << 16, kv_ring=2), 1),
+])
+def test_noalloc_validates_before_touching_its_scratch(g, kw, code):
+    """Invalid params are rejected by the same checks as gqa_attention_decode, before the
+    entry point plans or clears anything in its static scratch (no GPU is needed: nothing
+    is launched, and no CUDA call is made)."""
+    assert call_noalloc(g, good_params(g, **kw)) == code
+
+
+def test_noalloc_rejects_pointers_like_decode(g):
+    assert call_noalloc(g, good_params(g), q=None) == 1
+    assert call_noalloc(g, good_params(g), out=FAKE + 2) == 1

@@ -80,8 +80,8 @@ def test_prefill_stale_garbage_is_masked():
 
 @pytest.mark.parametrize("dtype,softcap", [("bf16", 0.0), ("f16", 0.0), ("bf16", 50.0)])
 def test_prefill_tc_sharp_scores(dtype, softcap):
-    """Scale 1 (scores of standard deviation ~11): exponents far below -125 in tiles with no
-    masked key, where part of exp2 runs as a polynomial with its argument clamped."""
+    """Scale 1 (scores of standard deviation ~11): exp2 arguments far below -125 in tiles
+    with no masked key, whose weights must flush to zero without NaN."""
     w = Workload("presharp", 420, "prefill", dtype, 2, 8, 2, 128, 700, 740, 0, 0, windows=(-1,), scale=1.0,
                  softcap=softcap, head_sink=True)
     c = make_case(w, seed_offset=1)

@@ -4,13 +4,14 @@ It exists for callers that cannot allocate device memory where they run attentio
 plugin inside an engine that owns all device memory, a latency-critical loop where a
 cudaMalloc is not acceptable); it keeps its scratch in a static device array of the
 library.  These tests call it through the C ABI twice in a row and compare each output
-with gqa_attention_decode's on the same inputs, within the decode parity tolerance.
+with gqa_attention_decode's on the same inputs, within the decode parity tolerance, and
+with the fp64 oracle on sampled rows.
 Collected last on purpose, so that a failure here never hides another test's result."""
 import numpy as np
 import pytest
 import torch
 
-from gpu_util import assert_close
+from gpu_util import assert_close, oracle_ref, out_rows
 from sliding_window_gb300.inputs import Workload, make_case
 
 pytestmark = pytest.mark.gpu
@@ -48,6 +49,13 @@ def test_noalloc_matches_workspace_decode_twice(case_id):
                                        t["head_sink"], ref, pk, pv, ws, status))
     torch.cuda.synchronize()
     ref64 = ref.double().cpu().numpy()
+    # the oracle on the same rounded inputs, on a sample of rows (every sequence, first and
+    # last q head of each kv group)
+    G = w.q_heads // w.kv_heads
+    rows = np.array([(b * w.q_len + i) * w.q_heads + h for b in range(w.batch) for i in range(w.q_len)
+                     for h in range(w.q_heads) if h % G in (0, G - 1)], dtype=np.int64)
+    want, _, _, st = oracle_ref(case, rows=rows)
+    assert st == 0
     for _ in range(2):  # two calls in a row share (and must clean up) the static scratch
         qk, qv = t["past_k"].clone(), t["past_v"].clone()
         out = torch.full_like(t["q"], float("nan"))
@@ -56,6 +64,7 @@ def test_noalloc_matches_workspace_decode_twice(case_id):
         torch.cuda.synchronize()
         assert status.item() == 0
         assert_close(out.double().cpu().numpy(), ref64, case.w.dtype, "noalloc vs workspace decode")
+        assert_close(out_rows(out, case, rows), want, case.w.dtype, "noalloc vs oracle")
         assert torch.equal(qk.view(torch.int16), pk.view(torch.int16))
 
 
