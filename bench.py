@@ -1,13 +1,18 @@
 """Benchmark of the sliding-window GQA hot path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--only]
+                    [--impl ours|reference] [--no-cpu-baseline] [--no-e2e] [--no-graphs]
 
 A step is one pass of the whole path over one batch: RoPE/append of the step's new
-tokens into the KV cache, then attention of every query row over the cache.  The default
-workload is the windowed single-token bf16 decode (B=8, Hq=32, Hkv=8, D=128, past
-U[512, 4095], window 1024); its metric is the KV-read HBM bandwidth (GB/s over the
-algorithmic bytes: each visible KV row of each (b, kv head) once, plus q, out and the
-appended rows).  Prefill workloads report attention TFLOP/s (4*D per visible pair).
+tokens into the KV cache, then attention of every query row over the cache (every layer
+of the workload).  The headline is the largest named workload that fits one GPU, the
+large-batch long-context bf16 decode (B=64, Hq=64, Hkv=8, D=128, past U[8192, 32767], per-head
+sink); its metric is the KV-read HBM bandwidth (GB/s over the algorithmic bytes: each
+visible KV row of each (b, kv head) once, plus q, out and the appended rows).  The same
+JSON line carries a record per other named workload under "workloads" (the long prefill
+with sink and softcap, the windowed decode, the speculative decode with rotary, the tiny
+fp32 prompt), each with its own timing, roofline, e2e and oracle baseline; prefill
+workloads report attention TFLOP/s (2*(D + Dv) per visible pair).
 
 Prints ONE JSON line on rank 0.  Inputs are seeded synthetic data, resident in HBM when the
 timed region starts; rotating buffer sets larger than L2 keep every step L2-cold.  Under
@@ -32,10 +37,9 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from sliding_window_gb300.inputs import WORKLOAD_ORDER, WORKLOADS, draw_seqlens, make_case  # noqa: E402
+from sliding_window_gb300.inputs import WORKLOADS, draw_seqlens, make_case  # noqa: E402
 
 METRIC = "attention TFLOP/s (prefill) & KV-read HBM GB/s (decode), % of GB300 roofline"
-DEFAULT_WORKLOAD = WORKLOAD_ORDER[1]
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -246,29 +250,27 @@ class Step:
             self.g.check(self.call(L, L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin,
                                    c.head_sink, L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "step")
 
-    def append_only(self, stream):
-        if self.w.kv_paged or self.w.kv_q8:  # the call appends itself: one full (untimed) step puts the rows in
-            assert not self.w.do_rotary
-            self.full(stream)
-            return
-        for L in self.layers:
-            c = L["c"]
-            self.g.check(self.g.gqa_rope_append_kv(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos,
-                                                   c.sin, L["q_rot"], c.past_k, c.past_v, L["status"], stream))
+    def append_layer(self, i, stream):
+        """The RoPE/append call of layer i alone (the split-KV decode appends itself)."""
+        L = self.layers[i]
+        c = L["c"]
+        self.g.check(self.g.gqa_rope_append_kv(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin,
+                                               L["q_rot"], c.past_k, c.past_v, L["status"], stream), "append")
 
-    def attend_only(self, stream):
-        """The attention kernel alone (present already holds the step; q arrives rotated)."""
-        for L in self.layers:
-            c = L["c"]
-            q = L["q_rot"] if self.w.do_rotary else c.q
-            if self.w.kv_paged:
-                self.g.check(self.g.gqa_attention_decode_paged(L["p_attend"], q, None, None, c.seqlens_k, L["table"],
-                                                               L["npages"], None, None, c.head_sink, L["out"],
-                                                               L["pool_k"], L["pool_v"], L["ws"], L["status"],
-                                                               stream), "paged attend")
-                continue
-            self.g.check(self.call(L, L["p_attend"], q, None, None, None, None, c.seqlens_k, None, None, c.head_sink,
-                                   L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "attend")
+    def attend_layer(self, i, stream):
+        """The attention-only call of layer i (present already holds the step; q arrives
+        rotated): the same attention launch as the combined call makes after its append."""
+        L = self.layers[i]
+        c = L["c"]
+        q = L["q_rot"] if self.w.do_rotary else c.q
+        if self.w.kv_paged:
+            self.g.check(self.g.gqa_attention_decode_paged(L["p_attend"], q, None, None, c.seqlens_k, L["table"],
+                                                           L["npages"], None, None, c.head_sink, L["out"],
+                                                           L["pool_k"], L["pool_v"], L["ws"], L["status"],
+                                                           stream), "paged attend")
+            return
+        self.g.check(self.call(L, L["p_attend"], q, None, None, None, None, c.seqlens_k, None, None, c.head_sink,
+                               L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "attend")
 
     def call(self, L, p, q, k, v, past_k, past_v, seqlens, cos, sin, sink, out, present_k, present_v, ws, st,
              stream):
@@ -342,9 +344,11 @@ def plan_graphs(steps_fns, K, per_graph, stream):
     return seq
 
 
-def run_ours(args, rank, world, local_rank):
+def run_workload(w, steps, warmup, rank, world, local_rank, with_e2e=True):
+    """Time `steps` steps of workload `w` on this rank (K steps between a barrier and a
+    synchronize on both sides, max over ranks), then the dominant kernel from the step's own
+    launches, then the end-to-end call with host buffers.  Frees its buffers on return."""
     from sliding_window_gb300 import gqa  # noqa: F401  (fails loudly without the library)
-    w = WORKLOADS[args.workload]
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
@@ -358,54 +362,161 @@ def run_ours(args, rank, world, local_rank):
     for s in sets[1:]:
         assert all((a == b).all() for a, b in zip(s.seqlens(), first.seqlens()))
     with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
+        for i in range(max(3, warmup)):
             sets[i % nsets].full(stream)
     stream.synchronize()
-    per_graph = max(1, min(args.steps, 64 if w.mode == "decode" else 4))
-    graphs = plan_graphs([s.full for s in sets], args.steps, per_graph, stream)
-    attend = plan_graphs([s.attend_only for s in sets], args.steps, per_graph, stream)
+    per_graph = max(1, min(steps, 64 if w.mode == "decode" else 4))
+    graphs = plan_graphs([s.full for s in sets], steps, per_graph, stream)
     stream.synchronize()
+    warm_graphs(graphs, stream, warmup, per_graph)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    elapsed = time_graphs(graphs, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed = max_over_ranks(elapsed, world, device)
+    kpl = kernels_per_layer(w)
+    launches = w.layers * kpl * steps
+
+    # the dominant kernel: a fused decode step is nothing but its launches (one per layer),
+    # so the kernel's average launch time is the step's time per launch; otherwise the step's
+    # two launches (RoPE/append, then attention) replayed from a graph that records CUDA
+    # events around every attention launch
+    if kpl == 1:
+        k_time = elapsed / (steps * w.layers)
+        k_units = units / w.layers
+        k_how = "step graph: the step is this kernel's launches only (ms_per_step / launches per step)"
+    else:
+        k_time, k_how = time_attention_launches(sets, steps, stream, warmup)
+        k_units = kunits / w.layers
+    e2e = None
+    if with_e2e:
+        if world > 1:
+            torch.distributed.barrier()
+        e2e = run_e2e(steps, warmup, sets, stream, w)
+        if world > 1:
+            torch.distributed.barrier()
+        e2e["elapsed"] = max_over_ranks(e2e["elapsed"], world, device)
+    status = [int(L["status"].item()) for s in sets for L in s.layers]
+    if any(status):
+        raise RuntimeError("device status bits set during the bench of %s: %s" % (w.name, status))
+    r = dict(w=w, steps=steps, warmup=warmup, elapsed=elapsed, units=units, unit=unit, clocks=clocks, nsets=nsets,
+             per_set=per_set, k_time=k_time, k_units=k_units, k_how=k_how, e2e=e2e, launches=launches,
+             seqs=first.seqlens())
+    del graphs, sets, first
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return r
+
+
+def warm_graphs(graphs, stream, warmup, per_graph):
+    """Replay every distinct graph once (its first launch uploads it to the device), then
+    enough more to cover `warmup` steps."""
+    seen = []
     with torch.cuda.stream(stream):
-        for g in graphs[: max(1, args.warmup // per_graph)]:
+        for g in graphs:
+            if not any(g is x for x in seen):
+                seen.append(g)
+                g.replay()
+        for g in graphs[: max(0, warmup // per_graph - len(seen))]:
             g.replay()
     stream.synchronize()
 
-    sampler = ClockSampler(local_rank) if rank == 0 else None
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.start()
-    elapsed = time_graphs(graphs, stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop() if sampler else None
-    if world > 1:
-        torch.distributed.barrier()
-    elapsed = max_over_ranks(elapsed, world, device)
-    launches_per_step = w.layers * kernels_per_layer(w)
 
-    # the dominant kernel (attention) alone, same steps and buffers, live CUDA events
-    for L in first.layers:
-        L["status"].zero_()
-    for s in sets:
-        with torch.cuda.stream(stream):
-            s.append_only(stream)
-    stream.synchronize()
-    k_elapsed = time_graphs(attend, stream)
-    # end to end through the public call with host buffers: H2D of the step's inputs from
-    # pinned memory, the call, D2H of the output, every step
-    if world > 1:
-        torch.distributed.barrier()
-    e2e = run_e2e(args, sets, stream, w, units)
-    if world > 1:
-        torch.distributed.barrier()
-    e2e["elapsed"] = max_over_ranks(e2e["elapsed"], world, device)
-    status = [int(L["status"].item()) for s in sets for L in s.layers]
-    if any(status):
-        raise RuntimeError("device status bits set during the bench: %s" % status)
-    return dict(w=w, elapsed=elapsed, units=units, kunits=kunits, unit=unit, clocks=clocks, nsets=nsets,
-                per_set=per_set, k_elapsed=k_elapsed, e2e=e2e, launches=launches_per_step * args.steps,
-                seqs=first.seqlens())
+_CUDART = None
+
+
+def _cudart():
+    """The CUDA runtime library this process already loaded (through torch)."""
+    global _CUDART
+    if _CUDART is None:
+        import ctypes
+        import glob
+        names = ["libcudart.so.13", "libcudart.so.12", "libcudart.so"]
+        cands = names + sorted(glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib",
+                                                      "libcudart.so*"))) + ["/usr/local/cuda/lib64/libcudart.so"]
+        for n in cands:
+            try:
+                lib = ctypes.CDLL(n)
+                lib.cudaEventElapsedTime.restype = ctypes.c_int
+                _CUDART = lib
+                break
+            except OSError:
+                continue
+        if _CUDART is None:
+            raise RuntimeError("libcudart not found")
+    return _CUDART
+
+
+def event_ms(a, b) -> float:
+    """Milliseconds between two completed timing events.  Events recorded as nodes of a
+    CUDA graph are read with cudaEventElapsedTime directly (torch's own check refuses them)."""
+    import ctypes
+    try:
+        return a.elapsed_time(b)
+    except RuntimeError:
+        ms = ctypes.c_float(0.0)
+        rc = _cudart().cudaEventElapsedTime(ctypes.byref(ms), ctypes.c_void_p(a.cuda_event),
+                                            ctypes.c_void_p(b.cuda_event))
+        if rc != 0:
+            raise RuntimeError("cudaEventElapsedTime failed with %d" % rc)
+        return ms.value
+
+
+def time_attention_launches(sets, steps, stream, warmup):
+    """Average duration of the step's attention launch: each step as its two launches
+    (the RoPE/append call, then the attention-only call, which launches the attention
+    kernel with the same arguments as the combined call), CUDA events recorded on the
+    launching stream right before and after every attention launch, all inside CUDA graphs
+    of the same steps.  Returns (seconds per launch, how it was timed)."""
+    n = len(sets)
+    per_graph = max(1, min(steps, 4))
+
+    def step_fn(s, evs):
+        def f(stream):
+            for L in range(len(s.layers)):
+                s.append_layer(L, stream)
+                a = torch.cuda.Event(enable_timing=True, external=True)
+                b = torch.cuda.Event(enable_timing=True, external=True)
+                a.record(stream)
+                s.attend_layer(L, stream)
+                b.record(stream)
+                evs.append((a, b))
+        return f
+
+    def run(use_graphs):
+        graphs = []
+        done = 0
+        while done < steps:
+            k = min(per_graph, steps - done)
+            evs = []
+            fns = [step_fn(sets[(done + i) % n], evs) for i in range(k)]
+            graphs.append((capture(fns, stream) if use_graphs else Eager(fns, stream), evs))
+            done += k
+        graphs[0][0].replay()  # first launch uploads the graph
+        stream.synchronize()
+        total, count = 0.0, 0
+        for g, evs in graphs:
+            g.replay()
+            stream.synchronize()
+            for a, b in evs:
+                total += event_ms(a, b) / 1e3
+                count += 1
+        return total / max(1, count)
+
+    if USE_GRAPHS:
+        try:
+            return run(True), "CUDA events around each attention launch inside graphs of the step's two calls"
+        except RuntimeError:
+            torch.cuda.synchronize()
+    return run(False), "CUDA events around each attention launch of the step's two calls, launched directly"
 
 
 def kernels_per_layer(w) -> int:
@@ -432,7 +543,7 @@ def job_rate(units_per_rank_step: float, steps: int, world: int, elapsed: float)
     return units_per_rank_step * steps * world / elapsed
 
 
-def run_e2e(args, sets, stream, w, units):
+def run_e2e(steps_k, warmup, sets, stream, w):
     """Every step: the step's inputs (q, k, v, seqlens_k of all layers) copied host->device
     from pinned memory in one copy, the public decode/prefill call per layer, the outputs
     copied device->host in one copy.  The KV cache stays resident (it is the op's state).
@@ -479,17 +590,18 @@ def run_e2e(args, sets, stream, w, units):
             stream.wait_stream(d2h_s)
         return issue
 
-    per_graph = max(1, min(args.steps, 64 if w.mode == "decode" else 4))
+    per_graph = max(1, min(steps_k, 64 if w.mode == "decode" else 4))
     with torch.cuda.stream(stream):
-        steps(min(3, args.steps))(stream)
+        steps(min(3, steps_k))(stream)
     stream.synchronize()
     if USE_GRAPHS:
-        full = capture([steps(per_graph)], stream) if args.steps >= per_graph else None
-        rem = args.steps % per_graph
-        graphs = [full] * (args.steps // per_graph) + ([capture([steps(rem)], stream)] if rem else [])
+        full = capture([steps(per_graph)], stream) if steps_k >= per_graph else None
+        rem = steps_k % per_graph
+        graphs = [full] * (steps_k // per_graph) + ([capture([steps(rem)], stream)] if rem else [])
     else:
-        graphs = [Eager([steps(args.steps)], stream)]
+        graphs = [Eager([steps(steps_k)], stream)]
     stream.synchronize()
+    warm_graphs(graphs, stream, warmup, per_graph)
     el = time_graphs(graphs, stream)
     return dict(elapsed=el, h2d=h2d, d2h=d2h)
 
@@ -607,25 +719,38 @@ def cpu_baseline(w, budget_s=12.0):
     return units / el, unit, s.sample, s.cores, el
 
 
+# the headline (the largest configuration that fits one GPU) and the other four named
+# workloads, each reported in the same line with its own timing, roofline, e2e and oracle
+# baseline; a sub-workload runs at least this many steps, so its timed region is >= ~10 ms
+HEADLINE = "decode_long_bf16"
+SUB_WORKLOADS = {"prefill_sink_softcap_bf16": 8, "decode_window_bf16": 1000, "specdecode_rotary_f16": 100,
+                 "prefill_fp32_tiny": 300}
+DEFAULT_STEPS = {"decode_window_bf16": 20000, "specdecode_rotary_f16": 2000, "decode_long_bf16": 200,
+                 "prefill_sink_softcap_bf16": 100, "prefill_fp32_tiny": 5000, "decode_window_ring_bf16": 20000,
+                 "decode_window_paged_bf16": 20000, "decode_window_vdim_bf16": 20000, "prefill_bias_bf16": 80,
+                 "decode_window_q8_bf16": 20000}
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (the SIMT path's
+# ALU roofline; no measured figure exists for it)
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
+    ap.add_argument("--only", action="store_true", help="time the headline workload alone (no sub-records)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graphs", action="store_true", help="launch steps directly (for profilers)")
     args = ap.parse_args()
     global USE_GRAPHS
     USE_GRAPHS = not args.no_graphs
     w = WORKLOADS[args.workload]
     if args.steps is None:
-        args.steps = {"decode_window_bf16": 100000, "specdecode_rotary_f16": 20000, "decode_long_bf16": 1500,
-                      "prefill_sink_softcap_bf16": 500, "prefill_fp32_tiny": 20000,
-                      "decode_window_ring_bf16": 100000, "decode_window_paged_bf16": 100000,
-                      "decode_window_vdim_bf16": 100000, "prefill_bias_bf16": 400,
-                      "decode_window_q8_bf16": 100000}.get(args.workload, 1000)
+        args.steps = DEFAULT_STEPS.get(args.workload, 1000)
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -636,9 +761,9 @@ def main():
             return
         value, unit, sample, cores, t = reference_arm(w, args)
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 6), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name, "global_batch": w.batch, "seq_len": w.q_len},
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 6),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": w.name, "global_batch": w.batch, "seq_len": w.q_len},
                 "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
                 "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -646,9 +771,17 @@ def main():
 
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    r = run_ours(args, rank, world, local_rank)
+    r = run_workload(w, args.steps, args.warmup, rank, world, local_rank, with_e2e=not args.no_e2e)
+    subs = []
+    if not args.only and args.workload == HEADLINE:
+        for name, min_steps in SUB_WORKLOADS.items():
+            subs.append(run_workload(WORKLOADS[name], max(args.steps, min_steps), args.warmup, rank, world,
+                                     local_rank, with_e2e=not args.no_e2e))
     if rank == 0:
-        print(json.dumps(report(args, w, r, world)))
+        line = report(args, r, world, headline=True)
+        if subs:
+            line["workloads"] = {x["w"].name: report(args, x, world, headline=False) for x in subs}
+        print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -667,41 +800,56 @@ def reference_arm(w, args):
     return units / el, unit, s.sample, s.cores, el
 
 
-def report(args, w, r, world):
+def roofline_peak(w, peaks, src):
+    """(bound, peak, unit, source) of a workload's dominant kernel."""
+    if w.mode == "decode":
+        return "hbm", float(peaks["hbm_gbs"]), "GB/s", src
+    if w.dtype == "f32":
+        return "alu", FP32_SIMT_TFLOPS, "TFLOP/s", "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"
+    # a kernel timed alone against the burst figure (a prefill step is one long launch)
+    return "tensor", float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), "TFLOP/s", src
+
+
+def kernel_name(w):
+    if w.mode == "decode":
+        return "decode_split" if kernels_per_layer(w) == 1 else "attn_simt"
+    return "attn_simt" if w.dtype == "f32" else "prefill_tc"
+
+
+def report(args, r, world, headline):
+    w = r["w"]
     peaks, src = load_peaks()
-    units, kunits, unit = r["units"], r["kunits"], r["unit"]
-    value = job_rate(units, args.steps, world, r["elapsed"])
-    k_time = r["k_elapsed"] / args.steps
-    if unit == "GB/s":
-        peak, bound, punit = float(peaks["hbm_gbs"]), "hbm", "GB/s"
-    else:
-        peak, bound, punit = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), "tensor", "TFLOP/s"
-    achieved = kunits / k_time
-    traffic = load_traffic(w.name)
-    line = {
-        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(r["elapsed"] / args.steps * 1e3, 6), "higher_is_better": True,
+    units, unit, steps = r["units"], r["unit"], r["steps"]
+    value = job_rate(units, steps, world, r["elapsed"])
+    bound, peak, punit, psrc = roofline_peak(w, peaks, src)
+    achieved = r["k_units"] / r["k_time"]
+    line = {}
+    if headline:
+        line.update({"metric": METRIC})
+    line.update({
+        "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": steps,
+        "warmup": r["warmup"], "ms_per_step": round(r["elapsed"] / steps * 1e3, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": {"f32": "f32", "f16": "f16", "bf16": "bf16"}[w.dtype],
         "data": "synthetic (seeded N(0,1) q/k/v, uniform past lengths, stale-slot garbage)",
         "config": {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads, "kv_heads": w.kv_heads,
                    "head_dim": w.head_dim, "new_tokens": w.q_len, "capacity": w.cap, "windows": list(w.windows),
                    "layers": w.layers, "buffer_sets": r["nsets"], "bytes_per_set": r["per_set"],
                    "l2": "rotating buffer sets totalling > 3x L2 (inputs larger than L2)",
-                   "tokens_per_s": round(w.batch * w.q_len * args.steps * world / r["elapsed"], 1),
+                   "tokens_per_s": round(w.batch * w.q_len * steps * world / r["elapsed"], 1),
                    "peaks": src, **({"mask": "additive bias [B, 1, S, cap] %s, device-resident" % w.dtype}
                                     if w.mask else {})},
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": punit,
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_split" if w.mode == "decode" else ("prefill_tc" if w.dtype != "f32"
-                                                                           else "attn_simt"),
-                     "kernel_ms": round(k_time * 1e3, 6), "peak_source": src},
+                     "frac": round(achieved / peak, 4), "traffic": load_traffic(w.name),
+                     "kernel": kernel_name(w), "kernel_ms": round(r["k_time"] * 1e3, 6), "peak_source": psrc,
+                     "kernel_timing": r["k_how"]},
         "clocks": r["clocks"],
         "gpu_launches": r["launches"],
-        "e2e": {"value": round(job_rate(units, args.steps, world, r["e2e"]["elapsed"]), 3), "unit": unit,
-                "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"]},
-    }
+    })
+    if r["e2e"] is not None:
+        line["e2e"] = {"value": round(job_rate(units, steps, world, r["e2e"]["elapsed"]), 3), "unit": unit,
+                       "h2d_bytes_per_step": r["e2e"]["h2d"], "d2h_bytes_per_step": r["e2e"]["d2h"]}
     if not args.no_cpu_baseline and world == 1:
-        v, u, sample, cores, t = cpu_baseline(w)
+        v, u, sample, cores, t = cpu_baseline(w, budget_s=12.0 if headline else 4.0)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": u, "cores": cores, "kind": "oracle",
                                 "sample": sample, "seconds": round(t, 2)}
     return line

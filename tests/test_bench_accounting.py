@@ -66,3 +66,24 @@ def test_f8_cache_bytes_by_hand():
     io = 1 * 1 * (w.q_heads * 2 + w.kv_heads * (2 + 1)) * 256
     assert units == pytest.approx((kv + io) / 1e9, rel=0, abs=1e-15)
     assert kunits == pytest.approx((kv + io - w.kv_heads * 256 * 3) / 1e9, rel=0, abs=1e-15)
+
+
+@pytest.mark.parametrize("name,kernel,bound", [
+    ("decode_long_bf16", "decode_split", "hbm"), ("decode_window_bf16", "decode_split", "hbm"),
+    ("specdecode_rotary_f16", "decode_split", "hbm"), ("prefill_sink_softcap_bf16", "prefill_tc", "tensor"),
+    ("prefill_fp32_tiny", "attn_simt", "alu")])
+def test_dominant_kernel_and_bound(name, kernel, bound):
+    w = WORKLOADS[name]
+    assert bench.kernel_name(w) == kernel
+    b, peak, unit, _ = bench.roofline_peak(w, {"hbm_gbs": 6777.6, "bf16_tflops": 1929.0}, "measured")
+    assert b == bound
+    assert unit == ("GB/s" if bound == "hbm" else "TFLOP/s")
+    if bound == "alu":  # 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz
+        assert peak == pytest.approx(80.55, abs=0.01)
+
+
+def test_headline_is_the_largest_single_gpu_workload_and_subrecords_cover_the_rest():
+    named = ["prefill_fp32_tiny", "decode_window_bf16", "prefill_sink_softcap_bf16", "specdecode_rotary_f16",
+             "decode_long_bf16"]
+    assert bench.HEADLINE == "decode_long_bf16"
+    assert set(bench.SUB_WORKLOADS) | {bench.HEADLINE} == set(named)
