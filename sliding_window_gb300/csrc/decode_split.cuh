@@ -86,11 +86,22 @@ template <int D, int DV, int MT, int NST, bool Q8 = false> struct Smem {
   static constexpr int kStagesOff = 0;
   static constexpr int kConvOff = NST * kStageBytes;
   static constexpr int kQOff = kReuseBytes;
-  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], empty[NST], xbar
-  static constexpr int kRedOff = kBarOff + (2 * NST + 1) * 8;             // red_m, red_l [4][QROWS]
+  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], xbar
+  static constexpr int kRedOff = kBarOff + (NST + 1) * 8;                 // red_m, red_l [4][QROWS]
   static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l, sink [QROWS]
   static constexpr int kFlagOff = kRowOff + 3 * kQRows * 4;
-  static constexpr int kBytes = kFlagOff + 16;
+  // per stage: how many warps are done with its current tile (counts up, never reset);
+  // then the number of tiles issued so far
+  static constexpr int kCntOff = kFlagOff + 16;
+  // the step's new K and V rows of this kv head, copied in at the start when they fit
+  static constexpr int kNewOff = (kCntOff + (NST + 1) * 4 + 15) / 16 * 16;
+  static constexpr int kNewBytes = 2048;
+  // cluster combine: the partials the other chunks send to this CTA, in a region of their
+  // own when they fit (one 16-row MMA tile), so that peers may send before this CTA has
+  // finished streaming
+  static constexpr int kRcvOff = kNewOff + kNewBytes;
+  static constexpr int kRcvBytes = MT == 1 ? 5120 : 0;
+  static constexpr int kBytes = kRcvOff + kRcvBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
   // per-warp merge regions (rows padded by 4 floats: the fragment stores of one warp
   // instruction then spread over all banks) and the combine's chunk statistics reuse the stages
@@ -179,8 +190,11 @@ __device__ __forceinline__ void widen16(const uint4 &codes, uint4 &lo, uint4 &hi
 // Warp-wide: write the step's rows [r0, r1) of kv head h of sequence b to present (K
 // rotated when do_rotary; as E4M3 codes of an f8 cache when Q8), then make the
 // generic-proxy stores visible to TMA reads.
+// `staged` (shared memory, or null): the rows as [curr][D + DV] copied in at the kernel's
+// start, read instead of k and v.
 template <typename T, int D, int DV, bool Q8 = false>
-__device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, int past, int r0, int r1, int lane) {
+__device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, int past, int r0, int r1, int lane,
+                                            const uint8_t *staged = nullptr) {
   const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
   T *pk = reinterpret_cast<T *>(a.present_k), *pv = reinterpret_cast<T *>(a.present_v);
   const T *cs = reinterpret_cast<const T *>(a.cos), *sn = reinterpret_cast<const T *>(a.sin);
@@ -195,36 +209,39 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
     const size_t row = a.table ? ((size_t)a.table[(size_t)b * a.max_pages + pos / KT] * a.Hkv + h) * KT + pos % KT
                                : ((size_t)b * a.Hkv + h) * a.cap + (a.ring ? pos % a.cap : pos);
     const size_t tok = ((size_t)b * a.curr + i) * a.Hkv + h;
+    const T *krow = staged ? reinterpret_cast<const T *>(staged + (size_t)i * (D + DV) * sizeof(T)) : kin + tok * D;
+    const T *vrow = staged ? reinterpret_cast<const T *>(staged + (size_t)i * (D + DV) * sizeof(T)) + D
+                           : vin + tok * DV;
     if (Q8) {
       uint8_t *p8 = reinterpret_cast<uint8_t *>(isk ? a.present_k : a.present_v);
       if (isk) {
-        const size_t src = tok * D, dst = row * D;
-        uint4 y1 = *reinterpret_cast<const uint4 *>(kin + src + c);
-        uint4 y2 = *reinterpret_cast<const uint4 *>(kin + src + D / 2 + c);
+        const size_t dst = row * D;
+        uint4 y1 = *reinterpret_cast<const uint4 *>(krow + c);
+        uint4 y2 = *reinterpret_cast<const uint4 *>(krow + D / 2 + c);
         if (a.do_rotary)
-          rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c,
-                     sn + (size_t)pos * (D / 2) + c, y1, y2);
+          rotate8<T>(krow + c, krow + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c, y1,
+                     y2);
         const float sc = a.k_scale[h];
         *reinterpret_cast<uint2 *>(p8 + dst + c) = codes8<T>(y1, sc);
         *reinterpret_cast<uint2 *>(p8 + dst + D / 2 + c) = codes8<T>(y2, sc);
       } else {
         *reinterpret_cast<uint2 *>(p8 + row * DV + c) =
-            codes8<T>(*reinterpret_cast<const uint4 *>(vin + tok * DV + c), a.v_scale[h]);
+            codes8<T>(*reinterpret_cast<const uint4 *>(vrow + c), a.v_scale[h]);
       }
     } else if (isk) {
-      const size_t src = tok * D, dst = row * D;
+      const size_t dst = row * D;
       if (a.do_rotary) {
         uint4 y1, y2;
-        rotate8<T>(kin + src + c, kin + src + D / 2 + c, cs + (size_t)pos * (D / 2) + c,
-                   sn + (size_t)pos * (D / 2) + c, y1, y2);
+        rotate8<T>(krow + c, krow + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c, y1,
+                   y2);
         *reinterpret_cast<uint4 *>(pk + dst + c) = y1;
         *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = y2;
       } else {
-        *reinterpret_cast<uint4 *>(pk + dst + c) = *reinterpret_cast<const uint4 *>(kin + src + c);
-        *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(kin + src + D / 2 + c);
+        *reinterpret_cast<uint4 *>(pk + dst + c) = *reinterpret_cast<const uint4 *>(krow + c);
+        *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(krow + D / 2 + c);
       }
     } else {
-      *reinterpret_cast<uint4 *>(pv + row * DV + c) = *reinterpret_cast<const uint4 *>(vin + tok * DV + c);
+      *reinterpret_cast<uint4 *>(pv + row * DV + c) = *reinterpret_cast<const uint4 *>(vrow + c);
     }
   }
   fence_proxy_async_global();
@@ -248,14 +265,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t *stages = smem + L::kStagesOff;
   uint8_t *qs = smem + L::kQOff;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
-  uint64_t *empty = full + NST;
-  uint64_t *xbar = empty + NST;  // cluster exchange: the partials sent to this CTA have landed
+  uint64_t *xbar = full + NST;  // cluster exchange: the partials sent to this CTA have landed
   float *red_m = reinterpret_cast<float *>(smem + L::kRedOff);
   float *red_l = red_m + kWarps * QROWS;
   float *row_m = reinterpret_cast<float *>(smem + L::kRowOff);
   float *row_l = row_m + QROWS;
   float *sink_z = row_l + QROWS;  // sink logit of row r in the exp2 domain (0 when smooth_softmax)
   volatile int *flags = reinterpret_cast<volatile int *>(smem + L::kFlagOff);  // [0] abort, [1] last
+  int *done_cnt = reinterpret_cast<int *>(smem + L::kCntOff);                 // [NST]
+  int *n_issued = done_cnt + NST;
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -264,8 +282,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
+      done_cnt[s] = 0;
     }
+    *n_issued = 0;
     mbar_init(xbar, 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -274,9 +293,34 @@ __global__ void __launch_bounds__(kThreads, 2)
     tma_prefetch_desc(&tmv);
   }
   // programmatic dependent launch: the setup above may overlap the previous kernel; every
-  // global read below must see its results
+  // global read below must see its results.  The next kernel may launch right away: its
+  // CTAs take SM slots this launch leaves free and wait there for this grid to complete.
   grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   __syncthreads();
+  // cluster: arrive once the barriers are initialized (released to the other CTAs); the
+  // matching wait comes before the first write into another CTA's shared memory
+  if constexpr (CL) cluster_arrive();
+
+  // the step's new K/V rows of this kv head do not depend on the past length: warp 0 (the
+  // one that appends them) copies them into shared memory now, so the append never waits
+  // on global memory.  Every chunk of the group does this; only the last one uses them.
+  uint8_t *newrows = smem + L::kNewOff;
+  const bool staged = a.append && a.curr * (D + DV) * (int)sizeof(T) <= L::kNewBytes;
+  if (staged && warp == 0) {
+    const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
+    constexpr int per_row = (D + DV) / 8;  // 16-byte chunks of one K row, then of one V row
+    for (int idx = lane; idx < a.curr * per_row; idx += 32) {
+      const int i = idx / per_row, ch = idx % per_row;
+      const size_t tok = ((size_t)b * a.curr + i) * a.Hkv + blockIdx.y;
+      cp_async16(newrows + (size_t)idx * 16, ch < D / 8 ? kin + tok * D + ch * 8 : vin + tok * DV + (ch - D / 8) * 8);
+    }
+    cp_async_commit();
+  }
+  // every exit of warp 0 first waits for those copies (none may land after the CTA is gone)
+  auto drain_staged = [&] {
+    if (staged && warp == 0) cp_async_wait_all();
+  };
 
   // the past length, the sink logits and the raw query rows are loaded together: their
   // latencies overlap
@@ -309,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d] = from_f32<T>(0.f);
       }
     }
+    drain_staged();
     return;
   }
   const int total = past + a.curr;
@@ -330,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d] = from_f32<T>(0.f);
         }
       }
+      drain_staged();
       return;
     }
   }
@@ -339,27 +385,43 @@ __global__ void __launch_bounds__(kThreads, 2)
   // a CTA past the group's last chunk has nothing to stream; in a cluster it still takes
   // part in the exchange (its rows carry m = -inf), otherwise it leaves now
   const bool idle = split >= nchunks;
-  if (idle && (!CL || nchunks == 1)) return;
+  if (idle && (!CL || nchunks == 1)) {
+    drain_staged();
+    return;
+  }
   const int c0 = lo + split * chunk;
   const int c1 = min(total, c0 + chunk);
   const int ntiles = idle ? 0 : (c1 - c0 + KT - 1) / KT;
   const int bh = b * a.Hkv + hkv;
   const bool appends = !idle && a.append && c1 > past;  // this chunk holds new rows [past, total)
 
-  // warp 0 fills the ring; the new rows go to present before the tile that holds them
+  // warp 0 fills the ring; the new rows go to present before the tile that holds them.
+  // (row, group) coordinates of tile t in the cache's tensor maps
+  auto tile_coord = [&](int t, int &row, int &group) {
+    const int k0 = c0 + t * KT;
+    row = a.ring ? k0 % a.cap : k0;
+    group = bh;
+    if (a.table) {  // the tile is one page: rows [0, 64) of (page, kv head)
+      group = a.table[(size_t)b * a.max_pages + k0 / KT] * a.Hkv + hkv;
+      row = 0;
+    }
+  };
   auto issue = [&](int t) {
     const int s = t % NST, k0 = c0 + t * KT;
-    if (appends && k0 + KT > past && k0 < total)
-      append_rows<T, D, DV, Q8>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane);
+    if (appends && k0 + KT > past && k0 < total) {
+      if (staged) {  // warp 0 copied them; other warps issue only after the barrier that follows
+        if (warp == 0) cp_async_wait_all();
+        __syncwarp();
+      }
+      append_rows<T, D, DV, Q8>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane,
+                                staged ? newrows : nullptr);
+    }
     if (lane == 0) {
       mbar_expect_tx(&full[s], L::kStageBytes);
       uint8_t *kdst = stages + s * L::kStageBytes;
       uint8_t *vdst = kdst + L::kTileBytes;
-      int row = a.ring ? k0 % a.cap : k0, group = bh;
-      if (a.table) {  // the tile is one page: rows [0, 64) of (page, kv head)
-        group = a.table[(size_t)b * a.max_pages + k0 / KT] * a.Hkv + hkv;
-        row = 0;
-      }
+      int row, group;
+      tile_coord(t, row, group);
       if constexpr (Q8) {  // [KT][128] codes each, one copy each
         tma_load_3d(kdst, &tmk, 0, row, group, &full[s]);
         tma_load_3d(vdst, &tmv, 0, row, group, &full[s]);
@@ -367,12 +429,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_4d(kdst, &tmk, 0, row, 0, group, &full[s]);
         tma_load_4d(vdst, &tmv, 0, row, 0, group, &full[s]);
       }
+      atomicMax(n_issued, t + 1);
     }
     __syncwarp();
   };
-  int issued = 0;
-  if (warp == 0)
-    for (; issued < min(NST, ntiles); ++issued) issue(issued);
+  if (warp == 0) {
+    for (int t = 0; t < min(NST, ntiles); ++t) issue(t);
+  }
 
   // Q rows r = i*G + g (token i, q head hkv*G + g), rotated at past + i, 128B-swizzled
   {
@@ -399,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   if (threadIdx.x < QROWS) sink_z[threadIdx.x] = zsink * kLog2e;
+  drain_staged();  // the staged rows are visible to every warp after this barrier
   __syncthreads();
 
   float m[MT][2], l[MT][2];
@@ -417,12 +481,36 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   const uint32_t qs_u32 = smem_u32(qs);
   const int q_abs_min = past, q_abs_max = past + a.curr - 1;
+  // absolute query position of this thread's rows (16*mt + lane/4 + 8h of the MMA tile), for
+  // the band predicate on frontier tiles; padding rows (>= R) are marked invalid
+  int qa_row[MT][2];
+  bool row_ok[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = 16 * mt + (lane >> 2) + 8 * h;
+      row_ok[mt][h] = row < R;
+      qa_row[mt][h] = past + (row < R ? row / a.G : 0);
+    }
   bool aborted = false;
   int t_fail = ntiles;
 
   // masked kernels: this thread's mask values for a tile (rows 16*mt + lane/4 + 8h, keys
   // kb + 8n + 2*(lane%4) + {0,1}), 16 bits each, packed in pairs; loaded one tile ahead
   uint32_t mcur[MK ? MT : 1][2][2], mnext[MK ? MT : 1][2][2];
+  // the mask row of each of this thread's rows (element offset of key 0), once per CTA
+  long long mrow_base[MK ? MT : 1][2];
+  if constexpr (MK) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = 16 * mt + (lane >> 2) + 8 * h;
+        const int i = row < R ? row / a.G : 0, g = row < R ? row % a.G : 0;
+        mrow_base[mt][h] = b * a.msb + (long long)(hkv * a.G + g) * a.msh + i * a.msi;
+      }
+  }
   auto load_mask = [&](int t, uint32_t (&mv)[MK ? MT : 1][2][2]) {
     const int kb = c0 + t * KT + 16 * warp;
     const uint32_t dflt = a.mask_kind == 1 ? 1u : 0u;  // keep / no bias where there is no row
@@ -432,12 +520,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int row = 16 * mt + (lane >> 2) + 8 * h;
           const int key = kb + 8 * n + 2 * (lane & 3);
           uint32_t lo = dflt, hi = dflt;
-          if (row < R) {
-            const int i = row / a.G, g = row % a.G;
-            const long long base = b * a.msb + (long long)(hkv * a.G + g) * a.msh + i * a.msi;
+          if (row_ok[mt][h]) {
+            const long long base = mrow_base[MK ? mt : 0][h];
             if (a.mask_kind == 1) {
               const uint8_t *mp = reinterpret_cast<const uint8_t *>(a.mask) + base;
               if (key < a.mask_keys) lo = mp[key];
@@ -490,14 +576,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t ks_u32 = Q8 ? smem_u32(smem + L::kConvOff) : smem_u32(stages + s * L::kStageBytes);
     const uint32_t vs_u32 = ks_u32 + (Q8 ? KT * D * 2 : L::kTileBytes);
 
-    // ---- S = Q K^T over this warp's 16 keys
-    float sacc[MT][2][4];
+    // ---- S = Q K^T over this warp's 16 keys, the k steps split over two independent
+    // accumulator chains (even and odd steps) that are added at the end
+    float sacc[MT][2][4], sodd[MT][2][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][n][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sacc[mt][n][e] = sodd[mt][n][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t kb0, kb1, kb2, kb3;
@@ -512,10 +599,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int qrow = 16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7);
         const int qch = 2 * ks + (lane >> 4);
         ldsm_x4(qs_u32 + (qch >> 3) * (QROWS * 128) + sw128(qrow, qch & 7), af[0], af[1], af[2], af[3]);
-        M::run(sacc[mt][0], af, kb0, kb1);
-        M::run(sacc[mt][1], af, kb2, kb3);
+        M::run((ks & 1) ? sodd[mt][0] : sacc[mt][0], af, kb0, kb1);
+        M::run((ks & 1) ? sodd[mt][1] : sacc[mt][1], af, kb2, kb3);
       }
     }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][n][e] += sodd[mt][n][e];
 
     // ---- scale, softcap, band mask (only on warps whose keys cross a frontier)
     const bool edge = !(kb >= c0 && kb + 15 < c1 && (!a.causal || kb + 15 <= q_abs_min) &&
@@ -541,10 +634,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           x = a.cap_mul != 0.f ? tanh_fast(x * smul) * a.cap_mul : x * smul;
           if (dropped) x = -INFINITY;
           if (edge) {
-            const int row = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
             const int key = kb + 8 * n + 2 * (lane & 3) + (e & 1);
-            const int qa = past + row / a.G;
-            const bool vis = row < R && key >= c0 && key < c1 && (!a.causal || key <= qa) &&
+            const int qa = qa_row[mt][e >> 1];
+            const bool vis = row_ok[mt][e >> 1] && key >= c0 && key < c1 && (!a.causal || key <= qa) &&
                              (a.window < 0 || qa - key < a.window);
             if (!vis) x = -INFINITY;
           }
@@ -616,15 +708,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (stale) fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    // warp 0 refills the stage once all four warps are done with it
-    if (warp == 0 && issued < ntiles) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], (t / NST) & 1, flags))) {
-        aborted = true;
-        t_fail = t + 1;
-        break;
+    // the last of the four warps to finish with the stage refills it: nobody waits for the
+    // others (the count only grows; every fourth arrival is a tile's last)
+    if (t + NST < ntiles) {
+      int last = 0;
+      if (lane == 0) {
+        __threadfence_block();  // this warp's reads of the stage are ordered before its count
+        last = (atomicAdd(&done_cnt[s], 1) % kWarps) == kWarps - 1;
+        if (last) __threadfence_block();
       }
-      issue(issued++);
+      if (__shfl_sync(0xffffffffu, last, 0)) issue(t + NST);
     }
     if constexpr (MK) {
 #pragma unroll
@@ -636,6 +729,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
   }
+
+  drain_staged();  // long complete by now
 
   // -------------------------------------------------------------- merge the 4 warps
   // per-warp row statistics (outside the stages: safe while aborted copies still land)
@@ -655,13 +750,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   // one decision for the whole CTA (a timed-out wait anywhere aborts it), taken by the
   // barrier that publishes the statistics
   aborted = __syncthreads_or(aborted || flags[0] != 0);
-  if (threadIdx.x == 0) grid_launch_dependents();  // streaming done: let the next kernel launch
   if (aborted) {
     // copies in flight must land before the CTA exits; take part in the ticket (or the
     // cluster exchange, with no visible key) so the group stays consistent, write nothing
     if (threadIdx.x == 0) {
       volatile int no_abort = 0;
-      for (int t = t_fail; t < min(issued, t_fail + NST); ++t) mbar_wait(&full[t % NST], (t / NST) & 1, &no_abort);
+      for (int t = t_fail; t < min(*n_issued, t_fail + NST); ++t) mbar_wait(&full[t % NST], (t / NST) & 1, &no_abort);
       report(a.status, GQA_DEV_TIMEOUT);
       if (!CL && nchunks > 1) {
         __threadfence();
@@ -679,9 +773,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       return;
     }
   }
-  // cluster: this CTA's stages are free (nothing in flight), peers may write into them once
-  // every CTA has arrived
-  if (CL && nchunks > 1) cluster_arrive_relaxed();
+  // cluster exchange: into the dedicated region when the partials fit (no barrier needed
+  // now: every CTA arrived at the start), else into the stages, which peers may only write
+  // once every CTA of the cluster has finished streaming (a second barrier phase)
+  const int S_cl = gridDim.x, n4_cl = R * (DV / 4), per_cl = (n4_cl + S_cl - 1) / S_cl;
+  const bool rcv_own = CL && S_cl * per_cl * 16 + S_cl * QROWS * 8 <= L::kRcvBytes;
+  if (CL && nchunks > 1 && !rcv_own) {
+    cluster_wait();            // first phase: completed at the start
+    cluster_arrive_relaxed();  // this CTA's stages are free (nothing in flight)
+  }
+  // row statistics over the four warps (threads < QROWS), and every warp's accumulator
+  // rescaled to the row maximum (each lane takes the maximum of its own rows from the warps'
+  // maxima) in its own region of the now free stages; all threads then sum the four regions
+  // in a fixed order (deterministic)
   if (threadIdx.x < QROWS) {
     const int row = threadIdx.x;
     float mm = -INFINITY;
@@ -692,9 +796,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     row_m[row] = mm;
     row_l[row] = ll;
   }
-  __syncthreads();
-  // every warp writes its rescaled accumulator to its own region (the stages are free now),
-  // then all threads sum the four regions in a fixed order (deterministic)
   constexpr int AST = L::kAccStride;
   float *wacc = reinterpret_cast<float *>(stages);  // [kWarps][QROWS][AST]
 #pragma unroll
@@ -703,7 +804,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int h = 0; h < 2; ++h) {
       const int row = 16 * mt + (lane >> 2) + 8 * h;
       if (row >= R) continue;  // padding rows of the MMA tile are never read
-      const float mm = row_m[row];
+      float mm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, red_m[w * QROWS + row]);
       const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
       float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane & 3);
 #pragma unroll
@@ -763,11 +866,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     // (after the wacc regions) with asynchronous stores that count down the owner's xbar.
     // The owner waits for exactly those bytes and combines its slice from local data; once
     // they have landed nothing else writes to or reads from its shared memory, so it may exit
-    const int S = gridDim.x, rank = split;
-    const int n4 = R * (DV / 4), per = (n4 + S - 1) / S;
-    float *rcv = wacc + kWarps * QROWS * AST;               // [S][per] float4 slices
-    float2 *rcv_ml = reinterpret_cast<float2 *>(rcv + QROWS * DV + 4 * kMaxCluster);  // [S][QROWS] (m, l)
-    cluster_wait();  // every CTA has finished streaming: its stages may be written
+    const int S = S_cl, rank = split;
+    const int n4 = n4_cl, per = per_cl;
+    // [S][per] float4 slices, then [S][QROWS] (m, l)
+    float *rcv = rcv_own ? reinterpret_cast<float *>(smem + L::kRcvOff) : wacc + kWarps * QROWS * AST;
+    float2 *rcv_ml = reinterpret_cast<float2 *>(rcv + (rcv_own ? S * per * 4 : QROWS * DV + 4 * kMaxCluster));
+    // dedicated region: the start's phase (every peer's barriers are initialized); stages:
+    // the second phase (every peer has finished streaming)
+    cluster_wait();
     const uint32_t rcv_s = smem_u32(rcv), rml_s = smem_u32(rcv_ml), xb_s = smem_u32(xbar);
     for (int t = threadIdx.x; t < S * R; t += kThreads) {
       const int k = t / R, r = t % R;
@@ -1008,8 +1114,9 @@ gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   return dispatch<T, false, MK, MIXED, Q8>(c, dp, a);
 }
 
-// (D, DV, MT, NST): equal head dims (MIXED false) or V head dim != Q/K head dim (MIXED true,
-// up to 32 query rows per group; four stages of 24 KB)
+// (D, DV, MT, NST): equal head dims (MIXED false; at D = 128 three 32 KB stages, two CTAs per
+// SM) or V head dim != Q/K head dim (MIXED true, up to 32 query rows per group; four stages
+// of 24 KB)
 template <typename T, bool CL, bool MK, bool MIXED, bool Q8>
 gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   const int D = c.p.head_dim, DV = c.Dv;

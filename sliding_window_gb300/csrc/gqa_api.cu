@@ -151,7 +151,7 @@ bool encode_mask_map(CUtensorMap *map, const void *base, int keys, int I, int H,
   return r == CUDA_SUCCESS;
 }
 
-DecodePlan decode_plan(const gqa_params &p) {
+DecodePlan decode_plan(const gqa_params &p, int sms) {
   DecodePlan d;
   const int G = p.q_heads / p.kv_heads;
   d.rows = G * p.q_len;
@@ -160,21 +160,24 @@ DecodePlan decode_plan(const gqa_params &p) {
   d.eligible = p.dtype != GQA_F32 &&
                (dv != p.head_dim ? d.mtiles <= 2  // different V head dim: up to 32 rows per group
                                  : (p.head_dim == 128 && d.mtiles <= 2) || (p.head_dim == 64 && d.mtiles <= 4));
+  if (sms < 1) sms = 1;
   // longest visible band of one group: [max(0, past - W + 1), past + curr)
   long long lmax = p.cap_present;
   if (p.window > 0) lmax = std::min<long long>(lmax, (long long)p.window + p.q_len - 1);
-  // chunks per group: enough CTAs for two waves of a 152-SM GB300 at two CTAs per SM
-  // (608), chunks of at most 4096 keys (partials stay small) and at least 256 keys
-  // (per-CTA setup stays small)
   const long long units = (long long)p.batch * p.kv_heads;
-  long long s = std::max<long long>((608 + units - 1) / units, (lmax + 4095) / 4096);
+  // chunks per group: as many as one wave of the GPU holds (two CTAs per SM), but chunks of
+  // at most 4096 keys (partials stay small) and at least 256 keys (per-CTA setup stays
+  // small).  Measured on few groups with long bands (64 groups of up to 16k keys): one wave
+  // of 4 chunks per group beats two or more waves of shorter chunks.
+  const long long slots = 2ll * sms;
+  long long s = std::max<long long>(slots / units, (lmax + 4095) / 4096);
   s = std::min<long long>(s, std::max<long long>(1, (lmax + 255) / 256));
   s = std::min<long long>(s, kDecodeMaxSplits);
   d.splits = (int)std::max<long long>(1, s);
-  // a launch that fits one wave (two CTAs on each of 152 SMs) combines its chunks through
+  // a launch that fits one wave (two CTAs on every SM) combines its chunks through
   // distributed shared memory; longer launches keep the workspace partials, since clusters
   // of up to 8 CTAs leave SMs of a GPC unused once CTAs queue for slots
-  d.cluster = d.splits >= 2 && d.splits <= kDecodeMaxCluster && units * d.splits <= 304;
+  d.cluster = d.splits >= 2 && d.splits <= kDecodeMaxCluster && units * d.splits <= slots;
   return d;
 }
 
@@ -187,8 +190,9 @@ WsLayout workspace_layout(const gqa_params &p, bool need_q_rot) {
     w.q_rot_bytes = (size_t)p.batch * p.q_len * p.q_heads * p.head_dim * es;
     off = align_up(off + w.q_rot_bytes, kAlign);
   }
-  DecodePlan d = decode_plan(p);
-  if (d.eligible && d.splits > 1 && !d.cluster) {  // cluster groups combine in shared memory
+  // the partials of the largest plan a GPU could choose (the splits grow with the SM count)
+  DecodePlan d = decode_plan(p, kPlanMaxSms);
+  if (d.eligible && d.splits > 1) {
     const size_t groups = (size_t)p.batch * p.kv_heads;
     const size_t slots = groups * d.splits;
     w.part_acc_off = off;
@@ -286,7 +290,7 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   if (!out || !aligned16(out)) return GQA_ERR_INVALID_ARG;
   const bool rotate = c.append && p->do_rotary;
   const WsLayout wl = workspace_layout(c.p, rotate);
-  const DecodePlan dp = decode_plan(c.p);
+  const DecodePlan dp = decode_plan(c.p, device_sm_count());
   // the split decode kernel appends and rotates itself; every other path runs K1 first
   const bool fused = mode == kDecode && dp.eligible;
   if (p->kv_ring && !fused) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads a ring
@@ -348,7 +352,7 @@ gqa_status run_attention_q8(Mode mode, const gqa_params *p, const void *q, const
   c.v_scale = v_scale;
   const bool rotate = c.append && p->do_rotary;
   const WsLayout wl = workspace_layout(c.p, rotate);
-  const DecodePlan dp = decode_plan(c.p);
+  const DecodePlan dp = decode_plan(c.p, device_sm_count());
   const bool fused = mode == kDecode && dp.eligible && p->head_dim == 128 && c.Dv == 128;
   const size_t need = fused ? (dp.splits > 1 && !dp.cluster ? wl.total : 0) : (rotate ? wl.q_rot_off + wl.q_rot_bytes : 0);
   if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return GQA_ERR_WORKSPACE;
@@ -452,7 +456,7 @@ gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const 
   c.block_table = block_table;
   c.max_pages = max_pages;
   c.num_pages = num_pages;
-  const gqa::DecodePlan dp = gqa::decode_plan(c.p);
+  const gqa::DecodePlan dp = gqa::decode_plan(c.p, gqa::device_sm_count());
   if (!dp.eligible) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads pages
   const gqa::WsLayout wl = gqa::workspace_layout(c.p, c.append && p->do_rotary);
   const size_t need = dp.splits > 1 && !dp.cluster ? wl.total : 0;

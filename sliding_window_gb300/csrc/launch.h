@@ -47,9 +47,12 @@ struct Call {
 };
 
 // Split-KV decode plan.  The visible band of each (b, kv head) group is cut into `splits`
-// equal chunks (one CTA each); `splits` depends on the params only, so the workspace does.
+// equal chunks (one CTA each).  The plan depends on the params and the GPU's SM count; the
+// workspace is sized for the largest plan any GPU of up to kPlanMaxSms SMs could choose, so
+// that it depends on the params only.
 constexpr int kDecodeMaxSplits = 64;
 constexpr int kDecodeMaxCluster = 8;  // portable cluster size
+constexpr int kPlanMaxSms = 512;
 struct DecodePlan {
   bool eligible = false;  // the split kernel handles these params
   int rows = 0;           // R = G * curr query rows per CTA
@@ -66,7 +69,9 @@ struct WsLayout {
   size_t total = 0;
 };
 
-DecodePlan decode_plan(const gqa_params &p);
+// sms: the SM count of the GPU that runs the kernel (device_sm_count()), or kPlanMaxSms for
+// the upper bound that sizes the workspace.
+DecodePlan decode_plan(const gqa_params &p, int sms);
 WsLayout workspace_layout(const gqa_params &p, bool need_q_rot);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda link).

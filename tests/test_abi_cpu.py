@@ -215,19 +215,20 @@ def test_workspace_checked_before_launch(g):
     assert call(g, p, ws_bytes=need, workspace=FAKE + 8) == 5
 
 
-def splits(B, Hkv, cap, window, curr=1, R=4):
-    """Chunks per group: two waves of 608 CTAs, chunks of 256..4096 keys, at most 64."""
+def bound_splits(B, Hkv, cap, window, curr=1):
+    """Chunks per group of the largest plan any GPU of up to 512 SMs would choose (it sizes
+    the workspace): one wave of two CTAs per SM (1024 slots), chunks of at most 4096 keys
+    and at least 256 keys, at most 64 chunks."""
     lmax = cap if window < 0 else min(cap, window + curr - 1)
     units = B * Hkv
-    s = max(-(-608 // units), -(-lmax // 4096))
+    s = max(1024 // units, -(-lmax // 4096))
     return min(64, max(1, min(s, max(1, -(-lmax // 256)))))
 
 
 def decode_ws(B, Hkv, R, D, S):
     """Split decode workspace: fp32 acc [R][D] and (m, l) per (group, chunk) slot, one ticket
-    per group; 256-byte aligned.  Nothing when a group is one chunk, nor when its 2..8 chunks
-    form one thread-block cluster (launches of at most 304 CTAs) and combine in shared memory."""
-    if S == 1 or (S <= 8 and B * Hkv * S <= 304):
+    per group; 256-byte aligned.  Nothing when a group is one chunk."""
+    if S == 1:
         return 0
     al = lambda x: (x + 255) // 256 * 256
     slots = B * Hkv * S
@@ -237,9 +238,9 @@ def decode_ws(B, Hkv, R, D, S):
 def test_workspace_sizes(g):
     ws = lambda **kw: g.lib.gqa_workspace_bytes(ctypes.byref(good_params(g, **kw)))
     # decode: B=2, Hq=8, Hkv=2 -> G=4, R=4 rows per group
-    S = splits(2, 2, 1024, 200)
+    S = bound_splits(2, 2, 1024, 200)
     assert S == 1 and ws(window=200) == 0  # the band fits one chunk
-    S = splits(2, 2, 16384, -1)
+    S = bound_splits(2, 2, 16384, -1)
     assert S == 64 and ws(window=-1, cap_present=16384) == decode_ws(2, 2, 4, 128, S)
     # partial accumulators are rows of the V head dim
     assert ws(window=-1, cap_present=16384, v_head_dim=64) == decode_ws(2, 2, 4, 64, S)
@@ -248,21 +249,13 @@ def test_workspace_sizes(g):
     assert ws(do_rotary=1, rope_len=64, window=-1, cap_present=16384) == \
         2 * 1 * 8 * 128 * 2 + decode_ws(2, 2, 4, 128, S)
     # long decode: G=8, R=8, 8 chunks of up to 4096 keys
-    S = splits(64, 8, 32768, -1, R=8)
+    S = bound_splits(64, 8, 32768, -1)
     assert S == 8
     assert ws(batch=64, q_heads=64, kv_heads=8, cap_present=32768, window=-1) == decode_ws(64, 8, 8, 128, S) > 0
-    # one wave of clusters (8 groups x 8 chunks): combined in shared memory, no workspace
-    S = splits(1, 8, 2048, -1, R=8)
-    assert S == 8
-    assert ws(batch=1, q_heads=64, kv_heads=8, cap_present=2048, window=-1) == decode_ws(1, 8, 8, 128, S) == 0
-    # the sliding-window decode: 64 groups x 4 chunks of 256 keys
-    S = splits(8, 8, 4096, 1024, R=4)
+    # the sliding-window decode: 64 groups, bands of at most 1024 keys -> 4 chunks
+    S = bound_splits(8, 8, 4096, 1024)
     assert S == 4
-    assert ws(batch=8, q_heads=32, kv_heads=8, cap_present=4096, window=1024) == 0
-    # ten chunks in one wave: past the cluster size, back to partials in the workspace
-    S = splits(2, 8, 2560, -1, R=8)
-    assert S == 10
-    assert ws(batch=2, q_heads=64, kv_heads=8, cap_present=2560, window=-1) == decode_ws(2, 8, 8, 128, S) > 0
+    assert ws(batch=8, q_heads=32, kv_heads=8, cap_present=4096, window=1024) == decode_ws(8, 8, 4, 128, S)
     # more than 32 query rows per group at D=128: the SIMT kernel, no split workspace
     assert ws(q_heads=64, kv_heads=2, q_len=2, window=-1) == 0
     # prefill-sized q_len never needs decode partials
