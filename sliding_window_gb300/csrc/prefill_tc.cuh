@@ -510,9 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key < lo_vis || key > hi_vis) r[e] = __float_as_uint(-INFINITY);
         }
       }
-      float mx = -INFINITY;
+      // row maximum over four independent chains (a single chain of 64 dependent steps was
+      // a measured latency bottleneck), combined at the end
+      float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int e = 0; e < BN; e += 2) mx = fmax3(mx, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+      for (int e = 0; e < BN; e += 2)
+        mxs[(e >> 1) & 3] = fmax3(mxs[(e >> 1) & 3], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+      float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
       // under a softcap an additive -inf still scores -softcap: the maximum counts it
       if (MK >= 2 && SOFTCAP) mx = fmaxf(mx, -FLT_MAX);
       float m_tile = -INFINITY;
@@ -524,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       // P = 2^(x - m) in two halves (keeps register pressure down), packed to the dtype and
       // stored over the first columns of S; elementwise math two lanes per instruction
-      uint64_t rs2 = 0;  // (0.f, 0.f)
+      uint64_t rs2[2] = {0, 0};  // (0.f, 0.f): two independent row-sum chains
       const uint64_t smul2 = f2_pack(smul, smul), cmul2 = f2_pack(cmul, cmul), negm2 = f2_pack(-m_use, -m_use);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -545,12 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r[half * 64 + e] == __float_as_uint(-INFINITY)) p0 = 0.f;
             if (r[half * 64 + e + 1] == __float_as_uint(-INFINITY)) p1 = 0.f;
           }
-          rs2 = f2_add(rs2, f2_pack(p0, p1));
+          rs2[(e >> 1) & 1] = f2_add(rs2[(e >> 1) & 1], f2_pack(p0, p1));
           pk[e >> 1] = pack2<T>(p0, p1);
         }
         tmem_st32(tS + half * 32, pk);
       }
-      const float2 rsf = f2_unpack(rs2);
+      const float2 rsf = f2_unpack(f2_add(rs2[0], rs2[1]));
       float rs = rsf.x + rsf.y;
       if (MK != 1 && SOFTCAP && edge) {
         // a masked key's -inf came out of tanh as -1, i.e. a score of -softcap: clear its P
