@@ -93,7 +93,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 5
+#define GQA_ABI_VERSION 6
 
 typedef int32_t gqa_status;
 #define GQA_OK 0
@@ -293,6 +293,18 @@ const char *gqa_status_string(gqa_status s);
 
 /* GQA_ABI_VERSION of the loaded library. */
 int32_t gqa_abi_version(void);
+
+/* Test hook for the failure path ([P4] "Scheduling, precision, and invariants": invalid
+ * situations fail explicitly).  Every pipeline wait in the tensor-core prefill and split-KV
+ * decode kernels is bounded (about 2 s by default); a wait that gives up sets
+ * GQA_DEV_TIMEOUT, lets the copies and MMAs its CTA already issued land (those waits keep the
+ * full bound), frees the CTA's tensor memory and returns, and the call's outputs are then
+ * invalid.  With cycles > 0, every later launch of those kernels (in this process) first
+ * waits on an mbarrier that nothing completes and bounds its pipeline waits by `cycles` SM
+ * cycles, so that this path runs deterministically; the workspace stays usable for the next
+ * call.  cycles == 0 restores normal operation; cycles < 0 returns GQA_ERR_INVALID_ARG.
+ * Not for production use. */
+gqa_status gqa_test_stall_waits(int64_t cycles);
 
 #ifdef __cplusplus
 }

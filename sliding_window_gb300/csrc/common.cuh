@@ -150,16 +150,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up (returns false) when
-// *abort is set by another thread or when kWaitLimitCycles have passed, in which case it
-// sets *abort itself so that every role of the CTA winds down.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+// *abort is set by another thread or when `limit` SM cycles have passed, in which case it
+// sets *abort itself so that every role of the CTA winds down.  Pipeline waits pass the
+// launch's limit (kWaitLimitCycles unless a test shortened it); the waits that drain copies
+// and MMAs already in flight keep the full bound.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         *abort = 1;
         return false;
       }

@@ -71,6 +71,8 @@ struct DecodeArgs {
   float score_mul;  // scale*log2(e), or scale/softcap with softcap
   float cap_mul;    // softcap*log2(e), 0 without softcap
   const float *k_scale, *v_scale;  // f8 cache (Q8 kernels): one scale per kv head
+  long long wait_limit;  // SM cycles after which a pipeline wait gives up
+  int stall;             // test hook: the first wait is on a barrier nothing completes
 };
 
 template <int D, int DV, int MT, int NST, bool Q8 = false> struct Smem {
@@ -86,8 +88,8 @@ template <int D, int DV, int MT, int NST, bool Q8 = false> struct Smem {
   static constexpr int kStagesOff = 0;
   static constexpr int kConvOff = NST * kStageBytes;
   static constexpr int kQOff = kReuseBytes;
-  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], xbar
-  static constexpr int kRedOff = kBarOff + (NST + 1) * 8;                 // red_m, red_l [4][QROWS]
+  static constexpr int kBarOff = kQOff + kQRows * D * 2;                  // full[NST], xbar, stall
+  static constexpr int kRedOff = kBarOff + (NST + 2) * 8;                 // red_m, red_l [4][QROWS]
   static constexpr int kRowOff = kRedOff + 2 * kWarps * kQRows * 4;       // row_m, row_l, sink [QROWS]
   static constexpr int kFlagOff = kRowOff + 3 * kQRows * 4;
   // per stage: how many warps are done with its current tile (counts up, never reset);
@@ -266,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t *qs = smem + L::kQOff;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
   uint64_t *xbar = full + NST;  // cluster exchange: the partials sent to this CTA have landed
+  uint64_t *stallbar = xbar + 1;  // never completed (failure-path test hook)
   float *red_m = reinterpret_cast<float *>(smem + L::kRedOff);
   float *red_l = red_m + kWarps * QROWS;
   float *row_m = reinterpret_cast<float *>(smem + L::kRowOff);
@@ -286,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     *n_issued = 0;
     mbar_init(xbar, 1);
+    mbar_init(stallbar, 1);
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
@@ -541,9 +545,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (ntiles > 0) load_mask(0, mcur);
   }
 
-  for (int t = 0; t < ntiles; ++t) {
+  if (a.stall && ntiles > 0 &&  // failure-path test hook: a wait that nothing completes
+      !__all_sync(0xffffffffu, mbar_wait(stallbar, 0, flags, a.wait_limit))) {
+    aborted = true;
+    t_fail = 0;
+  }
+  for (int t = 0; t < (aborted ? 0 : ntiles); ++t) {
     const int s = t % NST;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (t / NST) & 1, flags))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (t / NST) & 1, flags, a.wait_limit))) {
       aborted = true;
       t_fail = t;
       break;
@@ -1110,6 +1119,8 @@ gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   }
   a.k_scale = c.k_scale;
   a.v_scale = c.v_scale;
+  a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitLimitCycles;
+  a.stall = c.stall;
   if (dp.cluster) return dispatch<T, true, MK, MIXED, Q8>(c, dp, a);
   return dispatch<T, false, MK, MIXED, Q8>(c, dp, a);
 }

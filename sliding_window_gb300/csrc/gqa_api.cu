@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "gqa.h"
@@ -19,6 +20,9 @@ namespace gqa {
 namespace {
 
 constexpr size_t kAlign = 256;
+// failure-path test hook (gqa_test_stall_waits): 0, or the SM cycles after which the kernels'
+// pipeline waits give up, their first wait being on a barrier that nothing completes
+std::atomic<long long> g_test_stall{0};
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -265,6 +269,8 @@ gqa_status make_call(Call &c, const gqa_params *p, const void *q, const void *k,
   c.present_v = present_v;
   c.status = dev_status;
   c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.wait_limit = g_test_stall.load(std::memory_order_relaxed);
+  c.stall = c.wait_limit > 0;
   return GQA_OK;
 }
 
@@ -493,5 +499,11 @@ const char *gqa_status_string(gqa_status s) {
 }
 
 int32_t gqa_abi_version(void) { return GQA_ABI_VERSION; }
+
+gqa_status gqa_test_stall_waits(int64_t cycles) {
+  if (cycles < 0) return GQA_ERR_INVALID_ARG;
+  gqa::g_test_stall.store(cycles, std::memory_order_relaxed);
+  return GQA_OK;
+}
 
 }  // extern "C"

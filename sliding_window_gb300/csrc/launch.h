@@ -41,6 +41,11 @@ struct Call {
   int q8 = 0;
   const float *k_scale = nullptr, *v_scale = nullptr;
   int32_t *status = nullptr;
+  // failure-path test hook (gqa_test_stall_waits): the limit of the kernels' pipeline waits
+  // in SM cycles (0: the kernels' default), and whether their first wait is on a barrier
+  // that nothing completes
+  long long wait_limit = 0;
+  int stall = 0;
   cudaStream_t stream = nullptr;
   char *ws = nullptr;
   size_t ws_bytes = 0;

@@ -60,6 +60,8 @@ struct PrefillArgs {
   // attention mask (MK > 0): keys < mask_keys; a broadcast dimension reads coordinate 0
   int mask_keys, mask_bcast_b, mask_bcast_h, mask_bcast_i;
   float bias_mul;  // 1 / scale: an additive value joins the raw dot product before scaling
+  long long wait_limit;  // SM cycles after which a pipeline wait gives up
+  int stall;             // test hook: the first wait is on a barrier nothing completes
 };
 
 template <int D, int DV, int MK> struct PSmem {
@@ -213,6 +215,7 @@ enum {
   B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,
   B_SFULL_A, B_SFULL_B, B_PFULL_A, B_PFULL_B, B_OFULL_A, B_OFULL_B,
   B_MFULL_A, B_MFULL_B, B_MEMPTY_A, B_MEMPTY_B,
+  B_STALL,  // never completed (failure-path test hook)
   B_COUNT
 };
 static_assert(B_COUNT <= 24, "barrier region");
@@ -291,13 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bh = b * a.Hkv + hk;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t & 1, k0 = klo + t * BN, sk = t % KST;
-        if (t >= KST && !mbar_wait(&bars[B_KEMPTY0 + sk], ((t / KST) - 1) & 1, abort_flag)) break;
+        if (t >= KST && !mbar_wait(&bars[B_KEMPTY0 + sk], ((t / KST) - 1) & 1, abort_flag, a.wait_limit)) break;
         mbar_expect_tx(&bars[B_KFULL0 + sk], L::kTile);
 #pragma unroll
         for (int db = 0; db < D / 64; ++db)
           tma_load_3d(smem + L::kK + sk * L::kTile + db * (BN * 128), &tmk, db * 64, k0, bh, &bars[B_KFULL0 + sk]);
         ++kissued;
-        if (t >= 2 && !mbar_wait(&bars[B_VEMPTY0 + s], ((t >> 1) - 1) & 1, abort_flag)) break;
+        if (t >= 2 && !mbar_wait(&bars[B_VEMPTY0 + s], ((t >> 1) - 1) & 1, abort_flag, a.wait_limit)) break;
         mbar_expect_tx(&bars[B_VFULL0 + s], L::kVTile);
 #pragma unroll
         for (int db = 0; db < DV / 64; ++db)
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MK 1, 2: one buffer per head; MK 3: the shared tile goes to ring slot t % kMaskRing
         for (int h = 0; h < (MK != 3 && has_b ? 2 : 1); ++h) {
           const int slot = MK == 3 ? t % L::kMaskRing : h, use = MK == 3 ? t / L::kMaskRing : t;
-          if (use >= 1 && !mbar_wait(&bars[B_MEMPTY_A + slot], (use - 1) & 1, abort_flag)) {
+          if (use >= 1 && !mbar_wait(&bars[B_MEMPTY_A + slot], (use - 1) & 1, abort_flag, a.wait_limit)) {
             fine = false;
             break;
           }
@@ -352,8 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < BN / 16; ++kk)
         mma_ts(o_tmem, p_tmem + kk * 8, sdesc(vs + kk * 2048, BN * 128, 1024), id_pv, (t > 0 || kk > 0) ? 1u : 0u);
     };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_Q], 0, abort_flag)) &&
-              __all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0], 0, abort_flag));
+    // failure-path test hook: first a wait that nothing completes
+    bool ok = !(a.stall && !__all_sync(0xffffffffu, mbar_wait(&bars[B_STALL], 0, abort_flag, a.wait_limit))) &&
+              __all_sync(0xffffffffu, mbar_wait(&bars[B_Q], 0, abort_flag, a.wait_limit)) &&
+              __all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0], 0, abort_flag, a.wait_limit));
     if (ok) {
       tc_fence_after();
       if (lane == 0) {
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; ok && t < ntiles; ++t) {
       const int s = t & 1, k0 = klo + t * BN;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL0 + s], (t >> 1) & 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL0 + s], (t >> 1) & 1, abort_flag, a.wait_limit))) break;
       if (k0 + BN > total) {  // stale slots may hold NaN/Inf: zero those V rows
         const int first = max(0, total - k0);
         uint8_t *vb = smem + L::kV + s * L::kVTile;
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_A], t & 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_A], t & 1, abort_flag, a.wait_limit))) break;
       tc_fence_after();
       if (lane == 0) {
         issue_pv(t, tmem + 0, tmem + 256);
@@ -390,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       const bool next = t + 1 < ntiles;
       if (next) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0 + (t + 1) % KST], ((t + 1) / KST) & 1, abort_flag)))
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&bars[B_KFULL0 + (t + 1) % KST], ((t + 1) / KST) & 1, abort_flag, a.wait_limit)))
           break;
         tc_fence_after();
         if (lane == 0) {
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       if (has_b) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_B], t & 1, abort_flag))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_PFULL_B], t & 1, abort_flag, a.wait_limit))) break;
         tc_fence_after();
         if (lane == 0) {
           issue_pv(t, tmem + 128, tmem + 384);
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = klo + t * BN;
       const bool edge = !(k0 + BN - 1 < total && (!a.causal || k0 + BN - 1 <= qa_first) &&
                           (a.window < 0 || qa_last - k0 < a.window));
-      if (!__all_sync(0xffffffffu, mbar_wait(sfull, t & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(sfull, t & 1, abort_flag, a.wait_limit))) {
         ok = false;
         break;
       }
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this row's mask values for keys [k0, k0 + 128), 16-byte chunks of the 128B-swizzled
         // tile (row-broadcast masks hold one row)
         const int mbuf = MK == 3 ? t % L::kMaskRing : wg, muse = MK == 3 ? t / L::kMaskRing : t;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_MFULL_A + mbuf], muse & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_MFULL_A + mbuf], muse & 1, abort_flag, a.wait_limit))) {
           ok = false;
           break;
         }
@@ -569,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_ref = m_new;
       if (__any_sync(0xffffffffu, need) && t > 0) {
         // O holds PV of tiles < t: wait for the last of them, then scale it in TMEM
-        if (!__all_sync(0xffffffffu, mbar_wait(ofull, (t - 1) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(ofull, (t - 1) & 1, abort_flag, a.wait_limit))) {
           ok = false;
           break;
         }
@@ -590,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(pfull);
     }
     // epilogue: out = O / l
-    const bool fin = ok && !*abort_flag && mbar_wait(ofull, (ntiles - 1) & 1, abort_flag);
+    const bool fin = ok && !*abort_flag && mbar_wait(ofull, (ntiles - 1) & 1, abort_flag, a.wait_limit);
     if (__all_sync(0xffffffffu, fin)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -694,6 +700,8 @@ template <typename T, int MK, bool MIXED> gqa_status launch_t(const Call &c) {
   a.mask_bcast_h = c.mask_sh == 0;
   a.mask_bcast_i = c.mask_si == 0;
   a.bias_mul = 1.f / p.scale;
+  a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitLimitCycles;
+  a.stall = c.stall;
   const bool sc = p.softcap > 0.f;
   if (sc) {
     a.score_mul = p.scale / p.softcap;

@@ -34,7 +34,7 @@ TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decode", "gqa_rope_append_kv",
             "gqa_status_string", "gqa_abi_version", "gqa_attention_decode_noalloc", "gqa_attention_decode_paged",
             "gqa_attention_decode_masked", "gqa_attention_prefill_masked", "gqa_attention_decode_q8",
-            "gqa_attention_prefill_q8"]
+            "gqa_attention_prefill_q8", "gqa_test_stall_waits"]
 MASK_KEEP, MASK_ADD = 1, 2
 PAGE = 64  # positions per page of a paged cache
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES
@@ -103,6 +103,8 @@ def _load():
     lib.gqa_status_string.restype = ctypes.c_char_p
     lib.gqa_abi_version.argtypes = []
     lib.gqa_abi_version.restype = i32
+    lib.gqa_test_stall_waits.argtypes = [ctypes.c_int64]
+    lib.gqa_test_stall_waits.restype = i32
     return lib
 
 
@@ -249,6 +251,12 @@ def gqa_status_string(status: int) -> str:
 
 def gqa_abi_version() -> int:
     return int(lib.gqa_abi_version())
+
+
+def gqa_test_stall_waits(cycles: int) -> int:
+    """Failure-path test hook (see include/gqa.h): > 0 makes the kernels' first wait run out
+    after that many SM cycles; 0 restores normal operation."""
+    return int(lib.gqa_test_stall_waits(int(cycles)))
 
 
 def check(status: int, what: str = "") -> None:

@@ -64,7 +64,7 @@ def test_mask_struct_layout_matches_header(g, tmp_path):
 
 
 def test_version_and_status_strings(g):
-    assert g.gqa_abi_version() == 5
+    assert g.gqa_abi_version() == 6
     for s in range(6):
         assert g.gqa_status_string(s) and g.gqa_status_string(s) != "unknown status"
     assert g.gqa_status_string(99) == "unknown status"
@@ -316,3 +316,10 @@ def test_noalloc_validates_before_touching_its_scratch(g, kw, code):
 def test_noalloc_rejects_pointers_like_decode(g):
     assert call_noalloc(g, good_params(g), q=None) == 1
     assert call_noalloc(g, good_params(g), out=FAKE + 2) == 1
+
+
+def test_stall_hook_arguments(g):
+    """The failure-path test hook takes a non-negative cycle count (0 = normal operation)
+    and launches nothing by itself."""
+    assert g.gqa_test_stall_waits(-1) == g.GQA_ERR_INVALID_ARG
+    assert g.gqa_test_stall_waits(0) == g.GQA_OK
