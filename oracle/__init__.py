@@ -84,6 +84,9 @@ def _load():
         lib.oracle_attend_row.argtypes = [vp, vp, vp, i64, i64, vp, i32, i32, i32, f64, f64, i32, f64, vp]
         lib.oracle_attend_row.restype = None
         lib.oracle_attention.argtypes = [i32] * 10 + [f64, f64] + [i32] * 5 + [vp] * 6 + [i64, vp]
+        # B, Hq, Hkv, D, Dv, curr, cap, dtype; scale, softcap; window, causal, smooth; q, k, v,
+        # nonpad, sink, rows; nrows; out
+        lib.oracle_attention_nonpad.argtypes = [i32] * 8 + [f64, f64] + [i32] * 3 + [vp] * 6 + [i64, vp]
         lib.oracle_ring_valid.argtypes = [i32] * 3
         lib.oracle_ring_valid.restype = i32
         lib.oracle_ring_status.argtypes = [i32] * 4
@@ -240,6 +243,34 @@ def attention(p: dict, q_rot, present_k, present_v, seqlens_k, head_sink=None, r
                          int(p.get("causal", 1)), int(p.get("do_rotary", 0)), int(p.get("smooth_softmax", 0)),
                          int(past_is_separate), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(seq), _ptr(sink),
                          _ptr(ridx), n, _ptr(out))
+    if rows is None:
+        return out.reshape(B, curr, Hq, Dv)
+    return out
+
+
+def attention_nonpad(p: dict, q, k_cache, v_cache, nonpad_kv_seqlen, head_sink=None, rows=None) -> np.ndarray:
+    """Attention in fp64 over a padded K/V cache ([P4] "Layouts and semantics": opset-24
+    nonpad_kv_seqlen).  Sequence b has n_b = nonpad_kv_seqlen[b] valid keys (rows [0, n_b) of
+    its cache, p["cap_present"] rows); its q_len queries are the last q_len valid tokens
+    (query i at position n_b - q_len + i); n_b < q_len or n_b > cap gives zeros.  Same
+    conventions as attention() otherwise (q as it enters the scores; rows selection)."""
+    lib = _load()
+    dt = p["dtype"]
+    qb = _bits(q, dt)
+    kb, vb = _bits(k_cache, dt), _bits(v_cache, dt)
+    npd = np.ascontiguousarray(nonpad_kv_seqlen, dtype=np.int64)
+    sink = None if head_sink is None else np.ascontiguousarray(head_sink, dtype=np.float32)
+    B, Hq, D, curr, Dv = p["batch"], p["q_heads"], p["head_dim"], p["q_len"], v_dim(p)
+    if rows is None:
+        ridx, n = None, B * curr * Hq
+    else:
+        ridx = np.ascontiguousarray(rows, dtype=np.int64)
+        n = ridx.shape[0]
+    out = np.zeros((n, Dv), dtype=np.float64)
+    lib.oracle_attention_nonpad(B, Hq, p["kv_heads"], D, Dv, curr, p["cap_present"], DTYPE_CODES[dt],
+                                float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)), int(p.get("window", -1)),
+                                int(p.get("causal", 1)), int(p.get("smooth_softmax", 0)), _ptr(qb), _ptr(kb),
+                                _ptr(vb), _ptr(npd), _ptr(sink), _ptr(ridx), n, _ptr(out))
     if rows is None:
         return out.reshape(B, curr, Hq, Dv)
     return out

@@ -357,6 +357,52 @@ void oracle_attention(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv,
 }
 
 /* ------------------------------------------------------------------------------------
+ * A K/V cache with padding ([P4] "Layouts and semantics": the opset-24 nonpad_kv_seqlen
+ * input; "Compute paths": padding frontiers).  Sequence b has n = nonpad_kv_seqlen[b]
+ * valid keys, rows [0, n) of the cache; rows at or past n are padding and never seen.  The
+ * curr queries are the last curr of the n valid tokens (bottom-right alignment, as for the
+ * causal band), so query i sits at absolute position n - curr + i, and the band predicate
+ * is oracle_visible's with total = n.  A sequence with n < curr or n > cap cannot hold its
+ * own queries and gives zeros (the caller reports it).
+ * ---------------------------------------------------------------------------------- */
+void oracle_attention_nonpad(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv, int32_t curr, int32_t cap,
+                             int32_t dtype, double scale, double softcap, int32_t window, int32_t causal,
+                             int32_t smooth_softmax, const void *q, const void *k_cache, const void *v_cache,
+                             const int64_t *nonpad, const float *head_sink, const int64_t *rows, int64_t nrows,
+                             double *out) {
+  int G = Hq / Hkv;
+  if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  int64_t count = rows ? nrows : (int64_t)B * curr * Hq;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t t = 0; t < count; ++t) {
+    int64_t r = rows ? rows[t] : t;
+    int hq = (int)(r % Hq);
+    int i = (int)((r / Hq) % curr);
+    int b = (int)(r / ((int64_t)Hq * curr));
+    double *o = out + (size_t)t * Dv;
+    int64_t n = nonpad[b];
+    if (n < curr || n > cap) {
+      for (int d = 0; d < Dv; ++d) o[d] = 0.0;
+      continue;
+    }
+    int hk = hq / G;
+    int64_t q_abs = n - curr + i;
+    double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
+    uint8_t *vis = (uint8_t *)malloc((size_t)cap);
+    for (int64_t j = 0; j < cap; ++j) vis[j] = (uint8_t)oracle_visible(q_abs, j, n, causal, window);
+    int has_sink = head_sink != NULL || smooth_softmax;
+    double z = head_sink ? (double)head_sink[hq] : 0.0;
+    int64_t row0 = ((int64_t)b * Hkv + hk) * cap;
+    oracle_attend_row(qv, k_cache, v_cache, row0, cap, vis, D, Dv, dtype, scale, softcap, has_sink, z, o);
+    free(vis);
+    free(qv);
+  }
+}
+
+/* ------------------------------------------------------------------------------------
  * Ring layout of the present cache ([P1] "Sliding window": sliding_window_cache, the
  * physical rolling KV buffer whose memory is bounded by the window; [P3] Summary: a window
  * is a per-layer setting).  The cache has cap slots and absolute position p lives in slot
