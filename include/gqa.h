@@ -262,6 +262,23 @@ gqa_status gqa_attention_prefill_masked(const gqa_params *p, const gqa_mask *mas
                                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                         void *stream);
 
+/* Attention over a K/V cache with padding ([P4] "Layouts and semantics": the opset-24
+ * nonpad_kv_seqlen input; "Compute paths": padding frontiers skip unavailable blocks).
+ * nonpad_kv_seqlen is int64 [B] on the device (8-byte aligned): sequence b has n_b valid
+ * keys, rows [0, n_b) of k_cache [B, Hkv, cap_present, D] / v_cache [B, Hkv, cap_present,
+ * Dv]; rows at or past n_b are padding and are never read.  The q_len queries
+ * ([B, q_len, Hq*D], used as given: do_rotary must be 0) are the last q_len of the n_b valid
+ * tokens, so query i sits at absolute position n_b - q_len + i and the causal band, the
+ * window, the sink, the softcap and the fully-masked-row rule apply as for
+ * gqa_attention_prefill with seqlens_k = n_b - q_len (attention only: nothing is
+ * appended).  A sequence with n_b < q_len or n_b > cap_present gets zeros and
+ * GQA_DEV_BAD_SEQLEN.  kv_ring must be 0.  Kernel: the split-KV decode kernel when its
+ * envelope holds the shape, else the tensor-core prefill (bf16/f16) or the fp32 kernel; the
+ * workspace is gqa_workspace_bytes(p).  Errors as for gqa_attention_prefill. */
+gqa_status gqa_attention_nonpad(const gqa_params *p, const int64_t *nonpad_kv_seqlen, const void *q,
+                                const void *k_cache, const void *v_cache, const float *head_sink, void *out,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
 /* f8 KV cache.  The pages leave a quantized cache out of their own designs ([P1] puts
  * i8/i4/f8 KV out of its scope; [P2] "What changed" rejects quantized KV); this is the
  * plainest reading for an f8 cache.  present_k [B, Hkv, cap_present, D] and present_v

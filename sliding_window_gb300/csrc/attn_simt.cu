@@ -25,6 +25,7 @@ struct SimtArgs {
   const void *q, *kc, *vc;  // q [B, curr, Hq, D]; caches [B, Hkv, cap, D] and [B, Hkv, cap, Dv]
   void *out;
   const int32_t *seqlens;
+  const int64_t *nonpad;  // padded cache: valid keys per sequence (replaces seqlens)
   const float *head_sink;
   int32_t *status;
   int Hq, Hkv, G, D, Dv, curr, cap, cap_past, past_separate, rope_len, do_rotary, window, causal, has_sink;
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   const int i0 = blockIdx.x * kRows;
   const int hk = hq / a.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int past = a.seqlens[b];
+  const int past = load_past(a.seqlens, a.nonpad, b, a.curr, a.cap);
   int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
   if (MASKED && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // mask too short
   T *out = reinterpret_cast<T *>(a.out);
@@ -183,6 +184,7 @@ template <typename T> gqa_status launch_t(const Call &c) {
   a.vc = c.present_v;
   a.out = c.out;
   a.seqlens = c.seqlens;
+  a.nonpad = c.nonpad;
   a.head_sink = c.head_sink;
   a.status = c.status;
   a.Hq = p.q_heads;

@@ -63,6 +63,15 @@ __device__ __forceinline__ int sequence_status(int past, int curr, int cap_prese
   return 0;
 }
 
+// The past length of sequence b: seqlens_k[b], or, for a padded cache (nonpad != NULL, the
+// opset-24 nonpad_kv_seqlen: n valid keys, the curr queries the last curr of them),
+// n - curr; an n outside [curr, cap] gives -1, which sequence_status rejects.
+__device__ __forceinline__ int load_past(const int32_t *seqlens, const int64_t *nonpad, int b, int curr, int cap) {
+  if (!nonpad) return seqlens[b];
+  const long long n = nonpad[b];
+  return (n >= curr && n <= cap) ? (int)(n - curr) : -1;
+}
+
 __device__ __forceinline__ void report(int32_t *status, int bits) {
   if (status && bits) atomicOr(status, bits);
 }

@@ -53,6 +53,7 @@ struct DecodeArgs {
   void *present_k, *present_v;
   void *out;              // [B, curr, Hq, DV]
   const int32_t *seqlens;
+  const int64_t *nonpad;  // padded cache: valid keys per sequence (replaces seqlens)
   const float *head_sink;
   float *part_acc;      // [B*Hkv][S][R][DV]
   float *part_ml;       // [B*Hkv][S][R][2]
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // the past length, the sink logits and the raw query rows are loaded together: their
   // latencies overlap
-  const int past = a.seqlens[b];
+  const int past = load_past(a.seqlens, a.nonpad, b, a.curr, a.cap);
   const float smul = Q8 ? a.score_mul * a.k_scale[hkv] : a.score_mul;  // the K scale joins the score scale
   const float vsc = Q8 ? a.v_scale[hkv] : 1.f;                           // and the V scale the output
   const float zsink = (threadIdx.x < R && a.head_sink) ? a.head_sink[hkv * a.G + threadIdx.x % a.G] : 0.f;
@@ -1079,6 +1080,7 @@ gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   a.present_v = c.present_v;
   a.out = c.out;
   a.seqlens = c.seqlens;
+  a.nonpad = c.nonpad;
   a.head_sink = c.head_sink;
   a.part_acc = reinterpret_cast<float *>(c.ws + wl.part_acc_off);
   a.part_ml = reinterpret_cast<float *>(c.ws + wl.part_ml_off);

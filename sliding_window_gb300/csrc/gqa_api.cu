@@ -288,11 +288,16 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
                          const void *past_k, const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
                          const void *sin_cache, const float *head_sink, void *out, void *present_k, void *present_v,
                          void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream,
-                         const gqa_mask *mask = nullptr) {
+                         const gqa_mask *mask = nullptr, const int64_t *nonpad = nullptr) {
   Call c;
-  gqa_status s = make_call(c, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink, out, present_k,
-                           present_v, dev_status, stream);
+  gqa_status s = make_call(c, p, q, k, v, past_k, past_v, nonpad ? reinterpret_cast<const int32_t *>(nonpad) : seqlens_k,
+                           cos_cache, sin_cache, head_sink, out, present_k, present_v, dev_status, stream);
   if (s != GQA_OK) return s;
+  if (nonpad) {  // a padded cache: the kernels read the valid lengths instead of seqlens_k
+    c.seqlens = nullptr;
+    c.nonpad = nonpad;
+    if (mode == kPrefill && decode_plan(c.p, device_sm_count()).eligible) mode = kDecode;
+  }
   if (!out || !aligned16(out)) return GQA_ERR_INVALID_ARG;
   const bool rotate = c.append && p->do_rotary;
   const WsLayout wl = workspace_layout(c.p, rotate);
@@ -400,6 +405,16 @@ gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *
                                 int32_t *dev_status, void *stream) {
   return gqa::run_attention(gqa::kDecode, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_attention_nonpad(const gqa_params *p, const int64_t *nonpad_kv_seqlen, const void *q,
+                                const void *k_cache, const void *v_cache, const float *head_sink, void *out,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  if (!p || !nonpad_kv_seqlen || (reinterpret_cast<uintptr_t>(nonpad_kv_seqlen) & 7u)) return GQA_ERR_INVALID_ARG;
+  if (p->kv_ring || p->do_rotary) return GQA_ERR_INVALID_ARG;  // a plain cache, q as given
+  return gqa::run_attention(gqa::kPrefill, p, q, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                            head_sink, out, const_cast<void *>(k_cache), const_cast<void *>(v_cache), workspace,
+                            workspace_bytes, dev_status, stream, nullptr, nonpad_kv_seqlen);
 }
 
 gqa_status gqa_attention_decode_masked(const gqa_params *p, const gqa_mask *mask, const void *q, const void *k,

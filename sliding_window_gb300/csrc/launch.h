@@ -21,6 +21,7 @@ struct Call {
   const void *k = nullptr, *v = nullptr;
   const void *past_k = nullptr, *past_v = nullptr;
   const int32_t *seqlens = nullptr;
+  const int64_t *nonpad = nullptr;  // padded cache: valid keys per sequence (replaces seqlens)
   const void *cos = nullptr, *sin = nullptr;
   const float *head_sink = nullptr;
   void *out = nullptr;

@@ -53,6 +53,7 @@ constexpr float kRescaleLog2 = 8.f;  // rescale O only when the max grows by mor
 struct PrefillArgs {
   void *out;
   const int32_t *seqlens;
+  const int64_t *nonpad;  // padded cache: valid keys per sequence (replaces seqlens)
   const float *head_sink;
   int32_t *status;
   int Hq, Hkv, G, curr, cap, cap_past, past_separate, rope_len, do_rotary, window, causal, has_sink;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = gridDim.y - 1 - blockIdx.y;
   const int q0 = qt * BM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int past = a.seqlens[b];
+  const int past = load_past(a.seqlens, a.nonpad, b, a.curr, a.cap);
   int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
   if (MK && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // the mask must cover every key
   T *out = reinterpret_cast<T *>(a.out);
@@ -681,6 +682,7 @@ template <typename T, int MK, bool MIXED> gqa_status launch_t(const Call &c) {
   PrefillArgs a;
   a.out = c.out;
   a.seqlens = c.seqlens;
+  a.nonpad = c.nonpad;
   a.head_sink = c.head_sink;
   a.status = c.status;
   a.Hq = p.q_heads;

@@ -34,7 +34,7 @@ TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decode", "gqa_rope_append_kv",
             "gqa_status_string", "gqa_abi_version", "gqa_attention_decode_noalloc", "gqa_attention_decode_paged",
             "gqa_attention_decode_masked", "gqa_attention_prefill_masked", "gqa_attention_decode_q8",
-            "gqa_attention_prefill_q8", "gqa_test_stall_waits"]
+            "gqa_attention_prefill_q8", "gqa_test_stall_waits", "gqa_attention_nonpad"]
 MASK_KEEP, MASK_ADD = 1, 2
 PAGE = 64  # positions per page of a paged cache
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES
@@ -103,6 +103,8 @@ def _load():
     lib.gqa_status_string.restype = ctypes.c_char_p
     lib.gqa_abi_version.argtypes = []
     lib.gqa_abi_version.restype = i32
+    lib.gqa_attention_nonpad.argtypes = [pp] + [vp] * 7 + [sz, vp, vp]
+    lib.gqa_attention_nonpad.restype = i32
     lib.gqa_test_stall_waits.argtypes = [ctypes.c_int64]
     lib.gqa_test_stall_waits.restype = i32
     return lib
@@ -251,6 +253,15 @@ def gqa_status_string(status: int) -> str:
 
 def gqa_abi_version() -> int:
     return int(lib.gqa_abi_version())
+
+
+def gqa_attention_nonpad(p, nonpad_kv_seqlen, q, k_cache, v_cache, head_sink, out, workspace, dev_status,
+                         stream=None) -> int:
+    """Attention over a padded K/V cache: nonpad_kv_seqlen int64 [B] valid keys per sequence,
+    the queries the last q_len of them (see include/gqa.h)."""
+    return int(lib.gqa_attention_nonpad(ctypes.byref(p), _ptr(nonpad_kv_seqlen), _ptr(q), _ptr(k_cache),
+                                        _ptr(v_cache), _ptr(head_sink), _ptr(out), _ptr(workspace),
+                                        _nbytes(workspace), _ptr(dev_status), _stream(stream)))
 
 
 def gqa_test_stall_waits(cycles: int) -> int:

@@ -323,3 +323,22 @@ def test_stall_hook_arguments(g):
     and launches nothing by itself."""
     assert g.gqa_test_stall_waits(-1) == g.GQA_ERR_INVALID_ARG
     assert g.gqa_test_stall_waits(0) == g.GQA_OK
+
+
+def call_nonpad(g, p, nonpad=FAKE, **ptrs):
+    names = ["q", "k_cache", "v_cache", "head_sink", "out", "workspace"]
+    vals = {n: FAKE for n in names}
+    vals.update(ptrs)
+    a = [ctypes.c_void_p(vals[n]) if vals[n] is not None else None for n in names]
+    npd = ctypes.c_void_p(nonpad) if nonpad is not None else None
+    return g.lib.gqa_attention_nonpad(ctypes.byref(p), npd, a[0], a[1], a[2], a[3], a[4], a[5], 0, None, None)
+
+
+@pytest.mark.parametrize("kw,ptrs,code", [
+    (dict(), dict(nonpad=None), 1), (dict(), dict(nonpad=FAKE + 4), 1),  # int64 lengths, 8-byte aligned
+    (dict(do_rotary=1, rope_len=64), dict(), 1),                        # q is used as given
+    (dict(kv_ring=1, window=1000), dict(), 1),                          # a plain cache only
+    (dict(), dict(q=None), 1), (dict(), dict(out=FAKE + 2), 1), (dict(kv_heads=3), dict(), 1),
+])
+def test_nonpad_invalid_arguments(g, kw, ptrs, code):
+    assert call_nonpad(g, good_params(g, **kw), **ptrs) == code
