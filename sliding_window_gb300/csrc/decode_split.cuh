@@ -81,9 +81,10 @@ template <int D, int DV, int MT, int NST, bool Q8 = false> struct Smem {
   static constexpr int kTileBytes = KT * D * kEs;  // one K tile; the V tile follows it
   static constexpr int kVTileBytes = KT * DV * kEs;
   static constexpr int kStageBytes = kTileBytes + kVTileBytes;
-  // Q8: every warp widens its 16 keys of the stage to f16 here (the layout of a 16-bit
-  // stage), right after the stages, so the two form one region for the merge below
-  static constexpr int kConvBytes = Q8 ? KT * (D + DV) * 2 : 0;
+  // Q8: every warp widens the V codes of its 16 keys of the stage to f16 here (the layout of
+  // a 16-bit V tile), right after the stages, so the two form one region for the merge below;
+  // K codes go from the stage straight into MMA fragments
+  static constexpr int kConvBytes = Q8 ? KT * DV * 2 : 0;
   static constexpr int kReuseBytes = NST * kStageBytes + kConvBytes;
   static constexpr int kQRows = MT * 16;
   static constexpr int kStagesOff = 0;
@@ -174,18 +175,14 @@ template <typename T> __device__ __forceinline__ uint4 to_half8(const uint4 &x) 
   return r;
 }
 
-// Sixteen E4M3 codes (one 16-byte chunk) as sixteen f16 values, two 16-byte chunks.  Each
-// code goes through the pair conversion with both halves equal, so no lane order is assumed.
+// Sixteen E4M3 codes (one 16-byte chunk) as sixteen f16 values, two 16-byte chunks: one pair
+// conversion per two neighbouring codes (the low byte of the pair becomes the low half, as
+// the f16 pair layout of a 16-bit tile wants; the lane order was checked on the GPU).
 __device__ __forceinline__ void widen16(const uint4 &codes, uint4 &lo, uint4 &hi) {
   const uint32_t in[4] = {codes.x, codes.y, codes.z, codes.w};
   uint32_t out[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t c0 = (in[j >> 1] >> (16 * (j & 1))) & 0xFFu, c1 = (in[j >> 1] >> (16 * (j & 1) + 8)) & 0xFFu;
-    const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(c0 | (c0 << 8))) & 0xFFFFu;
-    const uint32_t h1 = e4m3x2_to_f16x2((uint16_t)(c1 | (c1 << 8))) & 0xFFFFu;
-    out[j] = h0 | (h1 << 16);
-  }
+  for (int j = 0; j < 8; ++j) out[j] = e4m3x2_to_f16x2((uint16_t)(in[j >> 1] >> (16 * (j & 1))));
   lo = make_uint4(out[0], out[1], out[2], out[3]);
   hi = make_uint4(out[4], out[5], out[6], out[7]);
 }
@@ -562,29 +559,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     if constexpr (MK) {
       if (t + 1 < ntiles) load_mask(t + 1, mnext);
     }
+    const uint8_t *k8 = stages + s * L::kStageBytes;  // Q8: the stage's K codes
     if constexpr (Q8) {
-      // widen this warp's 16 keys of the stage (rows of 128 codes, 128B-swizzled) to f16 in
-      // the layout of a 16-bit stage; only this warp reads these rows
+      // widen the V codes of this warp's 16 keys of the stage (rows of 128 codes,
+      // 128B-swizzled) to f16 in the layout of a 16-bit V tile; only this warp reads these rows
       static_assert(!Q8 || (D == 128 && DV == 128), "f8 cache: D = Dv = 128");
-      const uint8_t *k8 = stages + s * L::kStageBytes, *v8 = k8 + L::kTileBytes;
-      uint8_t *kc = smem + L::kConvOff, *vc = kc + KT * D * 2;
+      const uint8_t *v8 = k8 + L::kTileBytes;
+      uint8_t *vc = smem + L::kConvOff;
       const int r = 16 * warp + (lane >> 1);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int c = (lane & 1) * 4 + cc;  // codes [16c, 16c + 16) of the row
         const int e0 = 2 * c, e1 = 2 * c + 1;  // their f16 chunks
         uint4 lo, hi;
-        widen16(*reinterpret_cast<const uint4 *>(k8 + r * 128 + ((c ^ (r & 7)) << 4)), lo, hi);
-        *reinterpret_cast<uint4 *>(kc + (e0 >> 3) * (KT * 128) + sw128(r, e0 & 7)) = lo;
-        *reinterpret_cast<uint4 *>(kc + (e1 >> 3) * (KT * 128) + sw128(r, e1 & 7)) = hi;
         widen16(*reinterpret_cast<const uint4 *>(v8 + r * 128 + ((c ^ (r & 7)) << 4)), lo, hi);
         *reinterpret_cast<uint4 *>(vc + (e0 >> 3) * (KT * 128) + sw128(r, e0 & 7)) = lo;
         *reinterpret_cast<uint4 *>(vc + (e1 >> 3) * (KT * 128) + sw128(r, e1 & 7)) = hi;
       }
       __syncwarp();
     }
-    const uint32_t ks_u32 = Q8 ? smem_u32(smem + L::kConvOff) : smem_u32(stages + s * L::kStageBytes);
-    const uint32_t vs_u32 = ks_u32 + (Q8 ? KT * D * 2 : L::kTileBytes);
+    const uint32_t ks_u32 = smem_u32(stages + s * L::kStageBytes);
+    const uint32_t vs_u32 = Q8 ? smem_u32(smem + L::kConvOff) : ks_u32 + L::kTileBytes;
 
     // ---- S = Q K^T over this warp's 16 keys, the k steps split over two independent
     // accumulator chains (even and odd steps) that are added at the end
@@ -598,7 +593,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t kb0, kb1, kb2, kb3;
-      {
+      if constexpr (Q8) {
+        // the B fragments straight from the codes: key row 16*warp + lane/4 (+8), head dims
+        // 16*ks + 2*(lane%4) (+8), i.e. a pair of neighbouring bytes of 16-byte chunk ks of
+        // the row, one pair conversion each
+        const int r0 = 16 * warp + (lane >> 2), o = 2 * (lane & 3);
+        const uint8_t *c0 = k8 + r0 * 128 + ((ks ^ (r0 & 7)) << 4) + o;
+        const uint8_t *c1 = c0 + 8 * 128;  // row r0 + 8: the same swizzle phase
+        kb0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0));
+        kb1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0 + 8));
+        kb2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1));
+        kb3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1 + 8));
+      } else {
         const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
         const int kch = 2 * ks + ((lane >> 3) & 1);
         ldsm_x4(ks_u32 + (kch >> 3) * (KT * 128) + sw128(krow, kch & 7), kb0, kb1, kb2, kb3);
@@ -696,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int first = max(0, total - kb);
       for (int idx = lane; idx < (16 - first) * VCH; idx += 32) {
         const int r = 16 * warp + first + idx / VCH, ch = idx % VCH;
-        *reinterpret_cast<uint4 *>((Q8 ? smem + L::kConvOff + KT * D * 2 : stages + s * L::kStageBytes + L::kTileBytes) +
+        *reinterpret_cast<uint4 *>((Q8 ? smem + L::kConvOff : stages + s * L::kStageBytes + L::kTileBytes) +
                                    (ch >> 3) * (KT * 128) +
                                    sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
       }
@@ -1133,10 +1139,10 @@ gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
 template <typename T, bool CL, bool MK, bool MIXED, bool Q8>
 gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   const int D = c.p.head_dim, DV = c.Dv;
-  if constexpr (Q8) {  // f8 cache: D = Dv = 128, four 16 KB stages and a 32 KB f16 tile
+  if constexpr (Q8) {  // f8 cache: D = Dv = 128, five 16 KB stages and a 16 KB f16 V tile
     if (D == 128 && DV == 128 && !MK && !MIXED) {
-      if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 4, CL, false, true>(c, dp, a);
-      if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 4, CL, false, true>(c, dp, a);
+      if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 5, CL, false, true>(c, dp, a);
+      if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 5, CL, false, true>(c, dp, a);
     }
   } else if constexpr (!MIXED) {
     if (D == 128 && DV == 128) {
