@@ -59,10 +59,13 @@
  * only W + curr - 1 slots whatever the sequence length.  Requires window >= 1 and
  * window + q_len - 1 <= cap_present (else GQA_ERR_CAPACITY: a key the step sees would
  * already be overwritten), cap_present a multiple of 64 (else GQA_ERR_UNSUPPORTED),
- * present aliasing past (the ring is updated in place; else GQA_ERR_INVALID_ARG), and the
- * decode entry points on the split-KV kernel's shapes (bf16/f16; prefill returns
- * GQA_ERR_UNSUPPORTED).  seqlens_k is the absolute past length and may exceed cap_present;
- * the band predicate is unchanged.  gqa_rope_append_kv appends into a ring the same way.
+ * present aliasing past (the ring is updated in place; else GQA_ERR_INVALID_ARG), and either
+ * the decode entry points on the split-KV kernel's shapes (bf16/f16), or
+ * gqa_attention_prefill (a prompt, or a chunk of one, appended into the ring; bf16/f16 and
+ * cap_present a multiple of 128, since the tensor-core prefill reads 128-position tiles);
+ * other combinations return GQA_ERR_UNSUPPORTED.  seqlens_k is the absolute past length and
+ * may exceed cap_present; the band predicate is unchanged.  gqa_rope_append_kv appends into
+ * a ring the same way.
  *
  * Ownership and memory: the caller owns every buffer; all pointers except the params and
  * mask structs are device pointers, 16-byte aligned (seqlens_k, head_sink and the f8
@@ -93,7 +96,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 6
+#define GQA_ABI_VERSION 7
 
 typedef int32_t gqa_status;
 #define GQA_OK 0
@@ -218,6 +221,20 @@ gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const 
                                       const float *head_sink, void *out, void *k_pool, void *v_pool,
                                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                       void *stream);
+
+/* Prefill (a prompt, or a chunk of one over the pages already filled) into the same paged
+ * cache: the arguments, pages, table rules and errors of gqa_attention_decode_paged, with
+ * gqa_attention_prefill's semantics and kernels: the RoPE/append kernel writes the step's
+ * rows through the table (every page of the step's band checked first, the same decision
+ * as the attention kernel's), then the tensor-core prefill reads the band as 128-position
+ * tiles, each two pages.  bf16/f16 only (f32 returns GQA_ERR_UNSUPPORTED).  The workspace
+ * holds the rotated queries when do_rotary (gqa_workspace_bytes). */
+gqa_status gqa_attention_prefill_paged(const gqa_params *p, const void *q, const void *k, const void *v,
+                                       const int32_t *seqlens_k, const int32_t *block_table, int32_t max_pages,
+                                       int32_t num_pages, const void *cos_cache, const void *sin_cache,
+                                       const float *head_sink, void *out, void *k_pool, void *v_pool,
+                                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                       void *stream);
 
 /* Attention mask ([P4] "Layouts and semantics": boolean and FLOAT additive broadcast
  * masks next to the bottom-right causal band; [P2] "What changed": attention_bias summed

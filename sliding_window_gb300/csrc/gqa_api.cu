@@ -304,7 +304,11 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   const DecodePlan dp = decode_plan(c.p, device_sm_count());
   // the split decode kernel appends and rotates itself; every other path runs K1 first
   const bool fused = mode == kDecode && dp.eligible;
-  if (p->kv_ring && !fused) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads a ring
+  // a ring is read by the split decode kernel, and by the tensor-core prefill when its
+  // 128-key tiles never straddle the wrap (capacity a multiple of 128; no mask)
+  if (p->kv_ring && !fused &&
+      (mode != kPrefill || p->dtype == GQA_F32 || mask || p->cap_present % 128 != 0))
+    return GQA_ERR_UNSUPPORTED;
   if (mask) {
     if (!mask->data || (mask->kind != GQA_MASK_KEEP && mask->kind != GQA_MASK_ADD)) return GQA_ERR_INVALID_ARG;
     if (mask->kind == GQA_MASK_ADD && (reinterpret_cast<uintptr_t>(mask->data) & (c.esize - 1)))
@@ -457,15 +461,20 @@ gqa_status gqa_attention_prefill_q8(const gqa_params *p, const void *q, const vo
                                v_scale, out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
 
-gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const void *k, const void *v,
-                                      const int32_t *seqlens_k, const int32_t *block_table, int32_t max_pages,
-                                      int32_t num_pages, const void *cos_cache, const void *sin_cache,
-                                      const float *head_sink, void *out, void *k_pool, void *v_pool,
-                                      void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                                      void *stream) {
-  gqa::Call c;
-  gqa_status s = gqa::make_call(c, p, q, k, v, nullptr, nullptr, seqlens_k, cos_cache, sin_cache, head_sink, out,
-                                k_pool, v_pool, dev_status, stream);
+}  // extern "C"
+
+namespace gqa {
+namespace {
+
+// A paged cache: decode runs the split-KV kernel (which appends through the table itself);
+// prefill runs the RoPE/append kernel through the table, then the tensor-core prefill.
+gqa_status run_paged(Mode mode, const gqa_params *p, const void *q, const void *k, const void *v,
+                     const int32_t *seqlens_k, const int32_t *block_table, int32_t max_pages, int32_t num_pages,
+                     const void *cos_cache, const void *sin_cache, const float *head_sink, void *out, void *k_pool,
+                     void *v_pool, void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  Call c;
+  gqa_status s = make_call(c, p, q, k, v, nullptr, nullptr, seqlens_k, cos_cache, sin_cache, head_sink, out, k_pool,
+                           v_pool, dev_status, stream);
   if (s != GQA_OK) return s;
   if (p->kv_ring) return GQA_ERR_INVALID_ARG;
   if (c.Dv != p->head_dim) return GQA_ERR_UNSUPPORTED;  // pages hold K and V rows of one width
@@ -473,18 +482,58 @@ gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const 
   if (max_pages < 1 || num_pages < 1) return GQA_ERR_INVALID_ARG;
   if ((long long)max_pages * 64 != p->cap_present) return GQA_ERR_CAPACITY;
   if ((long long)num_pages * p->kv_heads > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
-  if (!out || !gqa::aligned16(out)) return GQA_ERR_INVALID_ARG;
+  if (!out || !aligned16(out)) return GQA_ERR_INVALID_ARG;
   c.block_table = block_table;
   c.max_pages = max_pages;
   c.num_pages = num_pages;
-  const gqa::DecodePlan dp = gqa::decode_plan(c.p, gqa::device_sm_count());
-  if (!dp.eligible) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads pages
-  const gqa::WsLayout wl = gqa::workspace_layout(c.p, c.append && p->do_rotary);
-  const size_t need = dp.splits > 1 && !dp.cluster ? wl.total : 0;
-  if (need > 0 && (!workspace || !gqa::aligned16(workspace) || workspace_bytes < need)) return GQA_ERR_WORKSPACE;
+  const bool rotate = c.append && p->do_rotary;
+  const WsLayout wl = workspace_layout(c.p, rotate);
+  if (mode == kDecode) {
+    const DecodePlan dp = decode_plan(c.p, device_sm_count());
+    if (!dp.eligible) return GQA_ERR_UNSUPPORTED;  // only the split decode kernel reads pages in decode
+    const size_t need = dp.splits > 1 && !dp.cluster ? wl.total : 0;
+    if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return GQA_ERR_WORKSPACE;
+    c.ws = static_cast<char *>(workspace);
+    c.ws_bytes = workspace_bytes;
+    return launch_decode_split(c, dp, wl);
+  }
+  if (p->dtype == GQA_F32) return GQA_ERR_UNSUPPORTED;  // the tensor-core prefill reads pages
+  const size_t need = rotate ? wl.q_rot_off + wl.q_rot_bytes : 0;
+  if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return GQA_ERR_WORKSPACE;
   c.ws = static_cast<char *>(workspace);
   c.ws_bytes = workspace_bytes;
-  return gqa::launch_decode_split(c, dp, wl);
+  if (c.append) {
+    c.q_rot = rotate ? c.ws + wl.q_rot_off : nullptr;
+    s = launch_rope_append(c);
+    if (s != GQA_OK) return s;
+    if (rotate) c.q = c.q_rot;
+  }
+  return launch_prefill_tc(c);
+}
+
+}  // namespace
+}  // namespace gqa
+
+extern "C" {
+
+gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const void *k, const void *v,
+                                      const int32_t *seqlens_k, const int32_t *block_table, int32_t max_pages,
+                                      int32_t num_pages, const void *cos_cache, const void *sin_cache,
+                                      const float *head_sink, void *out, void *k_pool, void *v_pool,
+                                      void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                      void *stream) {
+  return gqa::run_paged(gqa::kDecode, p, q, k, v, seqlens_k, block_table, max_pages, num_pages, cos_cache, sin_cache,
+                        head_sink, out, k_pool, v_pool, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_attention_prefill_paged(const gqa_params *p, const void *q, const void *k, const void *v,
+                                       const int32_t *seqlens_k, const int32_t *block_table, int32_t max_pages,
+                                       int32_t num_pages, const void *cos_cache, const void *sin_cache,
+                                       const float *head_sink, void *out, void *k_pool, void *v_pool,
+                                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                       void *stream) {
+  return gqa::run_paged(gqa::kPrefill, p, q, k, v, seqlens_k, block_table, max_pages, num_pages, cos_cache,
+                        sin_cache, head_sink, out, k_pool, v_pool, workspace, workspace_bytes, dev_status, stream);
 }
 
 gqa_status gqa_rope_append_kv(const gqa_params *p, const void *q, const void *k, const void *v, const void *past_k,

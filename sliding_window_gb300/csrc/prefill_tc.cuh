@@ -63,6 +63,11 @@ struct PrefillArgs {
   float bias_mul;  // 1 / scale: an additive value joins the raw dot product before scaling
   long long wait_limit;  // SM cycles after which a pipeline wait gives up
   int stall;             // test hook: the first wait is on a barrier nothing completes
+  // ring cache: position p in row p % cap (cap a multiple of 128); paged cache: pools
+  // [num_pages * Hkv][64][D], table [B][max_pages] names the page of positions [64n, 64n + 64)
+  int ring;
+  const int32_t *table;
+  int max_pages, num_pages;
 };
 
 template <int D, int DV, int MK> struct PSmem {
@@ -244,8 +249,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qt * BM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int past = load_past(a.seqlens, a.nonpad, b, a.curr, a.cap);
-  int st = sequence_status(past, a.curr, a.cap, a.cap_past, a.past_separate, a.do_rotary, a.rope_len);
+  int st = sequence_status(past, a.curr, a.ring ? INT_MAX : a.cap, a.cap_past, a.past_separate, a.do_rotary,
+                           a.rope_len);
   if (MK && !st && (long long)past + a.curr > a.mask_keys) st = GQA_DEV_BAD_SEQLEN;  // the mask must cover every key
+  if (a.table && !st) {
+    // every page of the sequence's band must exist: the same decision in every CTA of the
+    // sequence and in the append kernel
+    const int lo_seq = a.window > 0 ? max(0, past - a.window + 1) : 0, tot = past + a.curr;
+    const int32_t *trow = a.table + (size_t)b * a.max_pages;
+    bool bad = false;
+    for (int n = lo_seq / 64 + (int)threadIdx.x; n * 64 < tot; n += blockDim.x)
+      bad |= trow[n] < 0 || trow[n] >= a.num_pages;
+    if (__syncthreads_or(bad)) st = GQA_DEV_BAD_PAGE;
+  }
   T *out = reinterpret_cast<T *>(a.out);
   const int nrows = min(BM, a.curr - q0);
   if (st) {
@@ -260,6 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qa_first = past + q0, qa_last = past + q0 + nrows - 1;
   int klo = a.window > 0 ? max(0, qa_first - a.window + 1) : 0;
   if (MK) klo &= ~15;  // the mask's TMA coordinate: a multiple of 16 bytes
+  // a ring or paged cache: tiles start on 128-position boundaries, so a tile never straddles
+  // the ring's wrap and is two whole pages; the extra keys fall outside the band (masked)
+  if (a.ring || a.table) klo &= ~(BN - 1);
   const int khi = a.causal ? min(total, qa_last + 1) : total;
   const int ntiles = (khi - klo + BN - 1) / BN;  // >= 1: every row sees itself
 
@@ -293,19 +312,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (has_b) tma_load_4d(smem + L::kQB + db * (BM * 128), &tmq, db * 64, hA + 1, q0, b, &bars[B_Q]);
       }
       const int bh = b * a.Hkv + hk;
+      // (row, group) of the 64 keys from k0 in the K/V tensor maps: contiguous [B*Hkv][cap],
+      // ring [B*Hkv][cap] at row k0 % cap, pool [num_pages*Hkv][64] at the page of k0.  Only
+      // the pages of the sequence's band were checked: a 64-key half before the band's first
+      // page or past its last key reads the nearest checked page instead (those keys are
+      // never visible; rows past the last key have their V cleared before PV)
+      const int32_t *trow = a.table ? a.table + (size_t)b * a.max_pages : nullptr;
+      const int first_page = (a.window > 0 ? max(0, past - a.window + 1) : 0) / 64, last_page = (total - 1) / 64;
+      auto half_coord = [&](int k0, int &row, int &group) {
+        if (trow) {
+          group = trow[min(max(k0 / 64, first_page), last_page)] * a.Hkv + hk;
+          row = 0;
+        } else {
+          group = bh;
+          row = a.ring ? k0 % a.cap : k0;
+        }
+      };
+      // one 128-key tile of a K or V tensor map: a single box, or two 64-row boxes of pages
+      auto load_tile = [&](uint8_t *dst, const CUtensorMap *map, int k0, int cols, uint64_t *bar) {
+#pragma unroll 1
+        for (int db = 0; db < cols / 64; ++db) {
+          int row, group;
+          half_coord(k0, row, group);
+          tma_load_3d(dst + db * (BN * 128), map, db * 64, row, group, bar);
+          if (trow) {
+            half_coord(k0 + 64, row, group);
+            tma_load_3d(dst + db * (BN * 128) + 64 * 128, map, db * 64, row, group, bar);
+          }
+        }
+      };
       for (int t = 0; t < ntiles; ++t) {
         const int s = t & 1, k0 = klo + t * BN, sk = t % KST;
         if (t >= KST && !mbar_wait(&bars[B_KEMPTY0 + sk], ((t / KST) - 1) & 1, abort_flag, a.wait_limit)) break;
         mbar_expect_tx(&bars[B_KFULL0 + sk], L::kTile);
-#pragma unroll
-        for (int db = 0; db < D / 64; ++db)
-          tma_load_3d(smem + L::kK + sk * L::kTile + db * (BN * 128), &tmk, db * 64, k0, bh, &bars[B_KFULL0 + sk]);
+        load_tile(smem + L::kK + sk * L::kTile, &tmk, k0, D, &bars[B_KFULL0 + sk]);
         ++kissued;
         if (t >= 2 && !mbar_wait(&bars[B_VEMPTY0 + s], ((t >> 1) - 1) & 1, abort_flag, a.wait_limit)) break;
         mbar_expect_tx(&bars[B_VFULL0 + s], L::kVTile);
-#pragma unroll
-        for (int db = 0; db < DV / 64; ++db)
-          tma_load_3d(smem + L::kV + s * L::kVTile + db * (BN * 128), &tmv, db * 64, k0, bh, &bars[B_VFULL0 + s]);
+        load_tile(smem + L::kV + s * L::kVTile, &tmv, k0, DV, &bars[B_VFULL0 + s]);
         ++vissued;
       }
     }
@@ -656,10 +700,12 @@ template <typename T, int D, int DV, bool SC, int MK> gqa_status launch_cfg(cons
   static_assert(L::kAlloc <= 227 * 1024, "shared memory per CTA");
   const gqa_params &p = c.p;
   CUtensorMap tq, tk, tv, tm;
-  const long long outer = (long long)p.batch * p.kv_heads;
+  const bool paged = c.block_table != nullptr;
+  const long long outer = paged ? (long long)c.num_pages * p.kv_heads : (long long)p.batch * p.kv_heads;
+  const int rows = paged ? 64 : p.cap_present, box_rows = paged ? 64 : BN;
   if (!encode_q_map(&tq, c.q, D, p.q_heads, p.q_len, p.batch, BM, 2)) return GQA_ERR_CUDA;
-  if (!encode_kv_map(&tk, c.present_k, D, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
-  if (!encode_kv_map(&tv, c.present_v, DV, p.cap_present, outer, BN, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_map(&tk, c.present_k, D, rows, outer, box_rows, 2)) return GQA_ERR_CUDA;
+  if (!encode_kv_map(&tv, c.present_v, DV, rows, outer, box_rows, 2)) return GQA_ERR_CUDA;
   if (MK) {
     const int es = MK >= 2 ? 2 : 1;
     if (!encode_mask_map(&tm, c.mask, c.mask_keys, p.q_len, p.q_heads, p.batch, c.mask_si * es, c.mask_sh * es,
@@ -704,6 +750,10 @@ template <typename T, int MK, bool MIXED> gqa_status launch_t(const Call &c) {
   a.bias_mul = 1.f / p.scale;
   a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitLimitCycles;
   a.stall = c.stall;
+  a.ring = p.kv_ring;
+  a.table = c.block_table;
+  a.max_pages = c.max_pages;
+  a.num_pages = c.num_pages;
   const bool sc = p.softcap > 0.f;
   if (sc) {
     a.score_mul = p.scale / p.softcap;

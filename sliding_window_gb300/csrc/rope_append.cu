@@ -53,6 +53,10 @@ struct RopeArgs {
   int32_t *status;
   int B, Hq, Hkv, D, Dv, curr, cap_present, cap_past, rope_len, do_rotary, past_separate;
   int ring;  // present is a ring: position p in slot p % cap_present
+  // paged cache: present_k/v are pools [num_pages][Hkv][64][D]; table [B][max_pages] names the
+  // page of positions [64n, 64n + 64); the pages of the step's band must all exist
+  const int32_t *table;
+  int max_pages, num_pages, window;
   // f8 cache: present_k/v hold E4M3 codes of x / scale (fp32 division), one scale per kv head
   int q8;
   const float *k_scale, *v_scale;
@@ -82,8 +86,17 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
   const int b = blockIdx.x / a.curr;
   const int i = blockIdx.x % a.curr;
   const int past = a.seqlens[b];
-  const int st = sequence_status(past, a.curr, a.ring ? INT_MAX : a.cap_present, a.cap_past, a.past_separate,
-                                 a.do_rotary, a.rope_len);
+  int st = sequence_status(past, a.curr, a.ring ? INT_MAX : a.cap_present, a.cap_past, a.past_separate,
+                           a.do_rotary, a.rope_len);
+  if (a.table && !st) {
+    // every page the step reads or writes must exist (the same decision in every block of
+    // the sequence and in the attention kernel: nothing of a rejected sequence is written)
+    const int total = past + a.curr, lo = a.window > 0 ? max(0, past - a.window + 1) : 0;
+    const int32_t *trow = a.table + (size_t)b * a.max_pages;
+    bool bad = false;
+    for (int n = lo / 64 + (int)threadIdx.x; n * 64 < total; n += blockDim.x) bad |= trow[n] < 0 || trow[n] >= a.num_pages;
+    if (__syncthreads_or(bad)) st = GQA_DEV_BAD_PAGE;
+  }
   if (st) {
     if (threadIdx.x == 0 && i == 0) report(a.status, st);
     return;
@@ -97,11 +110,16 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
   const T *cosr = reinterpret_cast<const T *>(a.cos) + (size_t)pos * half;
   const T *sinr = reinterpret_cast<const T *>(a.sin) + (size_t)pos * half;
   const size_t slot = a.ring ? pos % a.cap_present : pos;
+  // row of kv head h for this position: (b, h, slot), or (page, h, pos % 64) of a pool
+  auto cache_row = [&](int h) -> size_t {
+    if (a.table) return ((size_t)a.table[(size_t)b * a.max_pages + pos / 64] * a.Hkv + h) * 64 + pos % 64;
+    return ((size_t)b * a.Hkv + h) * a.cap_present + slot;
+  };
   for (int it = threadIdx.x; it < items; it += blockDim.x) {
     if (it >= items_qk) {  // v: a plain copy of one 16-byte chunk (or its codes)
       const int h = (it - items_qk) / v_per_head, c = ((it - items_qk) % v_per_head) * N;
       const T *src = reinterpret_cast<const T *>(a.v) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.Dv;
-      const size_t row = ((size_t)b * a.Hkv + h) * a.cap_present + slot;
+      const size_t row = cache_row(h);
       if (a.q8) {
         const uint4 x = *reinterpret_cast<const uint4 *>(src + c);
         store_codes<T, N>(reinterpret_cast<uint8_t *>(a.present_v) + row * a.Dv + c, reinterpret_cast<const T *>(&x),
@@ -124,7 +142,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
     } else {
       const int h = head - nq;
       src = reinterpret_cast<const T *>(a.k) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.D;
-      const size_t row = ((size_t)b * a.Hkv + h) * a.cap_present + slot;
+      const size_t row = cache_row(h);
       if (a.q8) {  // the row in the dtype as without quantization, then its codes
         uint4 y1, y2;
         T *p1 = reinterpret_cast<T *>(&y1), *p2 = reinterpret_cast<T *>(&y2);
@@ -209,6 +227,10 @@ template <typename T> static gqa_status launch_t(const Call &c) {
   a.curr = p.q_len;
   a.cap_present = p.cap_present;
   a.ring = p.kv_ring;
+  a.table = c.block_table;
+  a.max_pages = c.max_pages;
+  a.num_pages = c.num_pages;
+  a.window = p.window;
   a.cap_past = p.cap_past;
   a.rope_len = p.rope_len;
   a.do_rotary = p.do_rotary;

@@ -34,7 +34,8 @@ TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decode", "gqa_rope_append_kv",
             "gqa_status_string", "gqa_abi_version", "gqa_attention_decode_noalloc", "gqa_attention_decode_paged",
             "gqa_attention_decode_masked", "gqa_attention_prefill_masked", "gqa_attention_decode_q8",
-            "gqa_attention_prefill_q8", "gqa_test_stall_waits", "gqa_attention_nonpad"]
+            "gqa_attention_prefill_q8", "gqa_test_stall_waits", "gqa_attention_nonpad",
+            "gqa_attention_prefill_paged"]
 MASK_KEEP, MASK_ADD = 1, 2
 PAGE = 64  # positions per page of a paged cache
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES
@@ -90,8 +91,9 @@ def _load():
     lib.gqa_rope_append_kv.restype = i32
     lib.gqa_attention_decode_noalloc.argtypes = [pp] + [vp] * 12 + [vp, vp]
     lib.gqa_attention_decode_noalloc.restype = i32
-    lib.gqa_attention_decode_paged.argtypes = [pp] + [vp] * 5 + [i32, i32] + [vp] * 7 + [sz, vp, vp]
-    lib.gqa_attention_decode_paged.restype = i32
+    for name in ("gqa_attention_decode_paged", "gqa_attention_prefill_paged"):
+        getattr(lib, name).argtypes = [pp] + [vp] * 5 + [i32, i32] + [vp] * 7 + [sz, vp, vp]
+        getattr(lib, name).restype = i32
     lib.gqa_attention_decode_masked.argtypes = [pp, ctypes.POINTER(GqaMask)] + [vp] * 13 + [sz, vp, vp]
     lib.gqa_attention_decode_masked.restype = i32
     lib.gqa_attention_prefill_masked.argtypes = [pp, ctypes.POINTER(GqaMask)] + [vp] * 13 + [sz, vp, vp]
@@ -229,15 +231,27 @@ def gqa_attention_prefill_q8(p, q, k, v, seqlens_k, cos_cache, sin_cache, head_s
                out, present_k8, present_v8, workspace, dev_status, stream)
 
 
+def _paged(name, p, q, k, v, seqlens_k, block_table, num_pages, cos_cache, sin_cache, head_sink, out, k_pool, v_pool,
+           workspace, dev_status, stream):
+    return int(getattr(lib, name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(seqlens_k), _ptr(block_table),
+                                  int(block_table.shape[1]), int(num_pages), _ptr(cos_cache), _ptr(sin_cache),
+                                  _ptr(head_sink), _ptr(out), _ptr(k_pool), _ptr(v_pool), _ptr(workspace),
+                                  _nbytes(workspace), _ptr(dev_status), _stream(stream)))
+
+
 def gqa_attention_decode_paged(p, q, k, v, seqlens_k, block_table, num_pages, cos_cache, sin_cache, head_sink, out,
                                k_pool, v_pool, workspace, dev_status, stream=None) -> int:
     """Decode over a paged cache: pools [num_pages, Hkv, 64, D], block_table int32
     [B, max_pages] on the device (see include/gqa.h)."""
-    return int(lib.gqa_attention_decode_paged(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(seqlens_k),
-                                              _ptr(block_table), int(block_table.shape[1]), int(num_pages),
-                                              _ptr(cos_cache), _ptr(sin_cache), _ptr(head_sink), _ptr(out),
-                                              _ptr(k_pool), _ptr(v_pool), _ptr(workspace), _nbytes(workspace),
-                                              _ptr(dev_status), _stream(stream)))
+    return _paged("gqa_attention_decode_paged", p, q, k, v, seqlens_k, block_table, num_pages, cos_cache, sin_cache,
+                  head_sink, out, k_pool, v_pool, workspace, dev_status, stream)
+
+
+def gqa_attention_prefill_paged(p, q, k, v, seqlens_k, block_table, num_pages, cos_cache, sin_cache, head_sink, out,
+                                k_pool, v_pool, workspace, dev_status, stream=None) -> int:
+    """Prefill (or a chunk of one) into a paged cache (see include/gqa.h)."""
+    return _paged("gqa_attention_prefill_paged", p, q, k, v, seqlens_k, block_table, num_pages, cos_cache, sin_cache,
+                  head_sink, out, k_pool, v_pool, workspace, dev_status, stream)
 
 
 def gqa_rope_append_kv(p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, q_rot, present_k, present_v,

@@ -64,7 +64,7 @@ def test_mask_struct_layout_matches_header(g, tmp_path):
 
 
 def test_version_and_status_strings(g):
-    assert g.gqa_abi_version() == 6
+    assert g.gqa_abi_version() == 7
     for s in range(6):
         assert g.gqa_status_string(s) and g.gqa_status_string(s) != "unknown status"
     assert g.gqa_status_string(99) == "unknown status"
@@ -131,18 +131,22 @@ def test_invalid_pointers_rejected(g, ptrs, code):
 def test_ring_rules(g):
     ring = good_params(g, kv_ring=1, window=1000, cap_present=1024, q_len=4)
     assert call(g, ring, past_k=FAKE + 4096, past_v=FAKE + 4096) == 1  # a ring is updated in place
-    assert call(g, ring, fn="gqa_attention_prefill") == 2            # only the decode kernel reads a ring
+    # prefill reads a ring in 128-position tiles: a capacity that is not a multiple of 128,
+    # fp32 and masks are not supported
+    assert call(g, good_params(g, kv_ring=1, window=1000, cap_present=1088, q_len=4), fn="gqa_attention_prefill") == 2
+    assert call(g, good_params(g, kv_ring=1, window=1000, cap_present=1024, q_len=4, dtype="f32"),
+                fn="gqa_attention_prefill") == 2
     assert call(g, good_params(g, kv_ring=1, window=1000, cap_present=1024, q_len=4, dtype="f32")) == 2
 
 
-def call_paged(g, p, table=FAKE, max_pages=16, num_pages=40, ws_bytes=0, **ptrs):
+def call_paged(g, p, table=FAKE, max_pages=16, num_pages=40, ws_bytes=0, fn="gqa_attention_decode_paged", **ptrs):
     names = ["q", "k", "v", "seqlens_k", "cos", "sin", "head_sink", "out", "k_pool", "v_pool", "workspace"]
     vals = {n: FAKE for n in names}
     vals.update(ptrs)
     a = [ctypes.c_void_p(vals[n]) if vals[n] is not None else None for n in names]
     tab = ctypes.c_void_p(table) if table is not None else None
-    return g.lib.gqa_attention_decode_paged(ctypes.byref(p), a[0], a[1], a[2], a[3], tab, max_pages, num_pages,
-                                            a[4], a[5], a[6], a[7], a[8], a[9], a[10], ws_bytes, None, None)
+    return getattr(g.lib, fn)(ctypes.byref(p), a[0], a[1], a[2], a[3], tab, max_pages, num_pages,
+                              a[4], a[5], a[6], a[7], a[8], a[9], a[10], ws_bytes, None, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -151,11 +155,16 @@ def call_paged(g, p, table=FAKE, max_pages=16, num_pages=40, ws_bytes=0, **ptrs)
     (dict(max_pages=15), 3),                              # cap_present must be 64 * max_pages
     (dict(out=None), 1), (dict(k_pool=FAKE + 8), 1),
 ])
-def test_paged_invalid_arguments(g, kw, code):
-    assert call_paged(g, good_params(g), **kw) == code
+@pytest.mark.parametrize("fn", ["gqa_attention_decode_paged", "gqa_attention_prefill_paged"])
+def test_paged_invalid_arguments(g, kw, code, fn):
+    assert call_paged(g, good_params(g), fn=fn, **kw) == code
 
 
 def test_paged_rejects_ring_and_unsupported_shapes(g):
+    pf = "gqa_attention_prefill_paged"
+    assert call_paged(g, good_params(g, kv_ring=1, window=1000), fn=pf) == 1
+    assert call_paged(g, good_params(g, v_head_dim=64), fn=pf) == 2
+    assert call_paged(g, good_params(g, dtype="f32"), fn=pf) == 2           # the tensor-core prefill reads pages
     assert call_paged(g, good_params(g, kv_ring=1, window=1000)) == 1
     assert call_paged(g, good_params(g, v_head_dim=64)) == 2       # pages hold K and V rows of one width
     assert call_paged(g, good_params(g, dtype="f32")) == 2          # only the split decode kernel reads pages
