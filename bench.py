@@ -386,16 +386,19 @@ def run_workload(w, steps, warmup, rank, world, local_rank, with_e2e=True):
     launches = w.layers * kpl * steps
 
     # the dominant kernel: a fused decode step is nothing but its launches (one per layer),
-    # so the kernel's average launch time is the step's time per launch; otherwise the step's
-    # two launches (RoPE/append, then attention) replayed from a graph that records CUDA
-    # events around every attention launch
+    # so the kernel's average launch time is the step's time per launch; otherwise the step
+    # is a RoPE/append launch then the attention launch per layer
     if kpl == 1:
         k_time = elapsed / (steps * w.layers)
         k_units = units / w.layers
         k_how = "step graph: the step is this kernel's launches only (ms_per_step / launches per step)"
     else:
-        k_time, k_how = time_attention_launches(sets, steps, stream, warmup)
+        # the step's attention launches: the step graph's time less a graph of the step's
+        # RoPE/append launches alone (same buffers, same launches)
+        t_app = max_over_ranks(time_append_launches(sets, steps, stream, warmup), world, device)
+        k_time = max(elapsed - t_app, 0.0) / (steps * w.layers)
         k_units = kunits / w.layers
+        k_how = "step graph less a graph of the step's RoPE/append launches alone"
     e2e = None
     if with_e2e:
         if world > 1:
@@ -430,93 +433,23 @@ def warm_graphs(graphs, stream, warmup, per_graph):
     stream.synchronize()
 
 
-_CUDART = None
-
-
-def _cudart():
-    """The CUDA runtime library this process already loaded (through torch)."""
-    global _CUDART
-    if _CUDART is None:
-        import ctypes
-        import glob
-        names = ["libcudart.so.13", "libcudart.so.12", "libcudart.so"]
-        cands = names + sorted(glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib",
-                                                      "libcudart.so*"))) + ["/usr/local/cuda/lib64/libcudart.so"]
-        for n in cands:
-            try:
-                lib = ctypes.CDLL(n)
-                lib.cudaEventElapsedTime.restype = ctypes.c_int
-                _CUDART = lib
-                break
-            except OSError:
-                continue
-        if _CUDART is None:
-            raise RuntimeError("libcudart not found")
-    return _CUDART
-
-
-def event_ms(a, b) -> float:
-    """Milliseconds between two completed timing events.  Events recorded as nodes of a
-    CUDA graph are read with cudaEventElapsedTime directly (torch's own check refuses them)."""
-    import ctypes
-    try:
-        return a.elapsed_time(b)
-    except RuntimeError:
-        ms = ctypes.c_float(0.0)
-        rc = _cudart().cudaEventElapsedTime(ctypes.byref(ms), ctypes.c_void_p(a.cuda_event),
-                                            ctypes.c_void_p(b.cuda_event))
-        if rc != 0:
-            raise RuntimeError("cudaEventElapsedTime failed with %d" % rc)
-        return ms.value
-
-
-def time_attention_launches(sets, steps, stream, warmup):
-    """Average duration of the step's attention launch: each step as its two launches
-    (the RoPE/append call, then the attention-only call, which launches the attention
-    kernel with the same arguments as the combined call), CUDA events recorded on the
-    launching stream right before and after every attention launch, all inside CUDA graphs
-    of the same steps.  Returns (seconds per launch, how it was timed)."""
+def time_append_launches(sets, steps, stream, warmup):
+    """Seconds for `steps` steps' RoPE/append launches alone (each layer's append call, the
+    launch that precedes the attention launch in a step), replayed from CUDA graphs over
+    the same buffer sets exactly like the step graphs."""
     n = len(sets)
-    per_graph = max(1, min(steps, 4))
+    per_graph = max(1, min(steps, 64))
 
-    def step_fn(s, evs):
+    def step_fn(s):
         def f(stream):
             for L in range(len(s.layers)):
                 s.append_layer(L, stream)
-                a = torch.cuda.Event(enable_timing=True, external=True)
-                b = torch.cuda.Event(enable_timing=True, external=True)
-                a.record(stream)
-                s.attend_layer(L, stream)
-                b.record(stream)
-                evs.append((a, b))
         return f
 
-    def run(use_graphs):
-        graphs = []
-        done = 0
-        while done < steps:
-            k = min(per_graph, steps - done)
-            evs = []
-            fns = [step_fn(sets[(done + i) % n], evs) for i in range(k)]
-            graphs.append((capture(fns, stream) if use_graphs else Eager(fns, stream), evs))
-            done += k
-        graphs[0][0].replay()  # first launch uploads the graph
-        stream.synchronize()
-        total, count = 0.0, 0
-        for g, evs in graphs:
-            g.replay()
-            stream.synchronize()
-            for a, b in evs:
-                total += event_ms(a, b) / 1e3
-                count += 1
-        return total / max(1, count)
-
-    if USE_GRAPHS:
-        try:
-            return run(True), "CUDA events around each attention launch inside graphs of the step's two calls"
-        except RuntimeError:
-            torch.cuda.synchronize()
-    return run(False), "CUDA events around each attention launch of the step's two calls, launched directly"
+    graphs = plan_graphs([step_fn(x) for x in sets], steps, per_graph, stream)
+    stream.synchronize()
+    warm_graphs(graphs, stream, warmup, per_graph)
+    return time_graphs(graphs, stream)
 
 
 def kernels_per_layer(w) -> int:
@@ -745,10 +678,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graphs", action="store_true", help="launch steps directly (for profilers)")
+    ap.add_argument("--read-floor", action="store_true",
+                    help="print the time a bare kernel needs to stream each decode workload's bytes, then exit")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="run the workload with this batch instead (smaller cases for profilers; implies --only)")
     args = ap.parse_args()
+    if args.read_floor:
+        print(json.dumps({"read_floor": read_floor()}))
+        return
     global USE_GRAPHS
     USE_GRAPHS = not args.no_graphs
     w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = w.scaled(batch=args.batch)
+        args.only = True
     if args.steps is None:
         args.steps = DEFAULT_STEPS.get(args.workload, 1000)
     args.warmup = max(3, args.warmup)
@@ -837,9 +780,11 @@ def report(args, r, world, headline):
                    "l2": "rotating buffer sets totalling > 3x L2 (inputs larger than L2)",
                    "tokens_per_s": round(w.batch * w.q_len * steps * world / r["elapsed"], 1),
                    "peaks": src, **({"mask": "additive bias [B, 1, S, cap] %s, device-resident" % w.dtype}
-                                    if w.mask else {})},
+                                    if w.mask else {}),
+                   **({"batch_override": True} if w.batch != WORKLOADS[w.name].batch else {})},
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": punit,
-                     "frac": round(achieved / peak, 4), "traffic": load_traffic(w.name),
+                     "frac": round(achieved / peak, 4),
+                     "traffic": load_traffic(w.name) if w.batch == WORKLOADS[w.name].batch else None,
                      "kernel": kernel_name(w), "kernel_ms": round(r["k_time"] * 1e3, 6), "peak_source": psrc,
                      "kernel_timing": r["k_how"]},
         "clocks": r["clocks"],
@@ -853,6 +798,131 @@ def report(args, r, world, headline):
         line["cpu_baseline"] = {"value": round(v, 6), "unit": u, "cores": cores, "kind": "oracle",
                                 "sample": sample, "seconds": round(t, 2)}
     return line
+
+
+# --------------------------------------------------------------------------------------
+# read floor: how long one launch that only streams N bytes from HBM takes on this GPU
+# --------------------------------------------------------------------------------------
+_FLOOR_SRC = r"""
+#include <cuda_runtime.h>
+#include <stdint.h>
+// Each CTA streams its contiguous slice of the buffer into shared memory with bulk async copies
+// (32 KB each, `stages` in flight, mbarrier completion), touching one word per copy; the only
+// global write is an impossible checksum match.  Launched with programmatic stream
+// serialization, like the attention kernels.
+__global__ void __launch_bounds__(128) read_floor(const uint8_t *src, size_t nbytes, float *out, int stages) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + stages * 32768);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&bars[s])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  const size_t per = ((nbytes + gridDim.x - 1) / gridDim.x + 32767) / 32768 * 32768;
+  const size_t lo = blockIdx.x * per, hi = lo + per < nbytes ? lo + per : nbytes;
+  const int ntiles = hi > lo ? (int)((hi - lo + 32767) / 32768) : 0;
+  auto issue = [&](int t) {
+    const int s = t % stages;
+    const size_t off = lo + (size_t)t * 32768;
+    const uint32_t bytes = (uint32_t)(hi - off < 32768 ? hi - off : 32768);
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&bars[s]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"((uint32_t)__cvta_generic_to_shared(sm + s * 32768)), "l"(src + off), "r"(bytes), "r"(bar)
+                 : "memory");
+  };
+  if (threadIdx.x == 0)
+    for (int t = 0; t < (stages < ntiles ? stages : ntiles); ++t) issue(t);
+  uint32_t acc = 0;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % stages;
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&bars[s]);
+    uint32_t ok = 0;
+    for (long long it = 0; !ok; ++it) {
+      asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                   "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(bar), "r"((t / stages) & 1) : "memory");
+      if (!ok && it > (1ll << 26)) {  // bounded, never expected to give up: the host sees -1
+        out[blockIdx.x] = -1.f;
+        ok = 1;
+      }
+    }
+    acc ^= reinterpret_cast<const uint32_t *>(sm + s * 32768)[threadIdx.x];
+    __syncthreads();
+    if (threadIdx.x == 0 && t + stages < ntiles) issue(t + stages);
+  }
+  if (acc == 0x9E3779B9u) out[blockIdx.x] = 1.f;
+}
+extern "C" int read_floor_launch(const void *src, size_t nbytes, float *out, int grid, int stages, void *stream) {
+  const int smem = stages * 32768 + 1024;
+  if (cudaFuncSetAttribute(read_floor, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  return (int)cudaLaunchKernelEx(&cfg, read_floor, (const uint8_t *)src, nbytes, out, stages);
+}
+"""
+
+
+def read_floor(device_index=0):
+    """Per decode workload: the time one launch that only streams the workload's algorithmic
+    bytes per launch from HBM takes (best of a few grid shapes), launched back to back from
+    CUDA graphs over L2-cold buffers with programmatic dependent launch like the attention
+    kernels.  A context figure for the decode roofline: no kernel that reads those bytes in
+    one launch can do better on this GPU."""
+    import ctypes
+    import tempfile
+    d = tempfile.mkdtemp(prefix="gqa_floor_")
+    src, so = os.path.join(d, "floor.cu"), os.path.join(d, "floor.so")
+    open(src, "w").write(_FLOOR_SRC)
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared", "-Xcompiler", "-fPIC",
+                    src, "-o", so], check=True, capture_output=True)
+    lib = ctypes.CDLL(so)
+    lib.read_floor_launch.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p]
+    dev = torch.device("cuda", device_index)
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    st = torch.cuda.Stream(dev)
+    out = torch.zeros(4 * sms, device=dev)
+    res = {}
+    for name in ("decode_window_bf16", "specdecode_rotary_f16", "decode_long_bf16"):
+        w = WORKLOADS[name]
+        seqs = [draw_seqlens(w)] * w.layers
+        nb = int(step_work(w, seqs)[0] * 1e9 / w.layers) // 32768 * 32768
+        nbuf = max(2, -(-(4 * L2_BYTES) // nb))
+        bufs = [torch.empty(nb, dtype=torch.uint8, device=dev).random_(0, 255) for _ in range(nbuf)]
+        best = None
+        for grid, stages in ((2 * sms, 3), (2 * sms, 2), (sms, 6)):
+            def launch(i):
+                assert lib.read_floor_launch(bufs[i % nbuf].data_ptr(), nb, out.data_ptr(), grid, stages,
+                                             st.cuda_stream) == 0
+            n = 32 if nb < (1 << 30) else 8
+            with torch.cuda.stream(st):
+                for i in range(4):
+                    launch(i)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for i in range(n):
+                    launch(i)
+            g.replay()
+            st.synchronize()
+            t = time_graphs([g] * 4, st) / (4 * n)
+            if (out < 0).any():
+                raise RuntimeError("read floor: a bounded wait gave up")
+            best = t if best is None else min(best, t)
+        res[name] = {"bytes_per_launch": nb, "floor_us": round(best * 1e6, 3), "floor_gbs": round(nb / best / 1e9, 1)}
+        del bufs
+    return res
 
 
 def load_traffic(name):
