@@ -251,11 +251,14 @@ class Step:
                                    c.head_sink, L["out"], c.past_k, c.past_v, L["ws"], L["status"], stream), "step")
 
     def append_layer(self, i, stream):
-        """The RoPE/append call of layer i alone (the split-KV decode appends itself)."""
+        """The RoPE/append call of layer i alone: what the combined call's first launch does
+        (rotated queries written only when the workload rotates; the split-KV decode
+        appends itself)."""
         L = self.layers[i]
         c = L["c"]
+        q_rot = L["q_rot"] if self.w.do_rotary else None
         self.g.check(self.g.gqa_rope_append_kv(L["p"], c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin,
-                                               L["q_rot"], c.past_k, c.past_v, L["status"], stream), "append")
+                                               q_rot, c.past_k, c.past_v, L["status"], stream), "append")
 
     def attend_layer(self, i, stream):
         """The attention-only call of layer i (present already holds the step; q arrives

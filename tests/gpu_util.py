@@ -16,9 +16,42 @@ TOL_F32 = 2e-5
 TOL_ABS, TOL_REL = 1e-2, 1e-2
 
 
+GUARD_BYTES = 4096  # margin on each side of a guarded buffer (a multiple of 16: the interior stays aligned)
+
+
+class Guarded:
+    """A device tensor placed inside a larger buffer whose margins hold a seeded random bit
+    pattern; check() asserts the margins are bit for bit what they were, so a kernel that
+    writes past either end of the tensor fails the test (the stand-in for a bounds checker)."""
+    _seed = 0
+
+    def __init__(self, shape, dtype, device, fill=None):
+        esize = torch.empty((), dtype=dtype).element_size()
+        self.g = GUARD_BYTES // esize
+        n = int(np.prod(shape))
+        self.whole = torch.empty(n + 2 * self.g, dtype=dtype, device=device)
+        Guarded._seed += 1
+        gen = torch.Generator(device="cpu").manual_seed(9000 + Guarded._seed)
+        pattern = torch.randint(0, 256, (2 * GUARD_BYTES,), dtype=torch.uint8, generator=gen).to(device)
+        raw = self.whole.view(torch.uint8)
+        raw[:GUARD_BYTES].copy_(pattern[:GUARD_BYTES])
+        raw[raw.numel() - GUARD_BYTES:].copy_(pattern[GUARD_BYTES:])
+        self.pattern = pattern
+        self.t = self.whole[self.g:self.g + n].view(shape)
+        if fill is not None:
+            self.t.copy_(fill) if torch.is_tensor(fill) else self.t.fill_(fill)
+
+    def check(self, what: str):
+        raw = self.whole.view(torch.uint8)
+        assert torch.equal(raw[:GUARD_BYTES], self.pattern[:GUARD_BYTES]), "%s: write before the buffer" % what
+        assert torch.equal(raw[raw.numel() - GUARD_BYTES:], self.pattern[GUARD_BYTES:]), \
+            "%s: write past the buffer" % what
+
+
 def run_gpu(case: Case, mode: str, separate_present: bool = False, attend_only: bool = False,
             status_init: int = 0, workspace=None):
-    """Run one call on cuda:0.  Returns dict(out, present_k, present_v, status) on the device."""
+    """Run one call on cuda:0.  Returns dict(out, present_k, present_v, status) on the device.
+    out and present sit inside guarded buffers whose margins are checked after the call."""
     from sliding_window_gb300 import gqa
     dev = torch.device("cuda:0")
 
@@ -26,16 +59,24 @@ def run_gpu(case: Case, mode: str, separate_present: bool = False, attend_only: 
         return None if x is None else x.to(dev)
 
     q, k, v = d(case.q), d(case.k), d(case.v)
-    past_k, past_v, seq = d(case.past_k), d(case.past_v), d(case.seqlens_k)
+    seq = d(case.seqlens_k)
     cos, sin, sink = d(case.cos), d(case.sin), d(case.head_sink)
     p = gqa.params_from_dict(case.params)
+    gk = Guarded(case.past_k.shape, case.past_k.dtype, dev, fill=case.past_k.to(dev))
+    gv = Guarded(case.past_v.shape, case.past_v.dtype, dev, fill=case.past_v.to(dev))
+    guards = [(gk, "present_k"), (gv, "present_v")]
+    past_k, past_v = gk.t, gv.t
     if separate_present:
-        present_k = torch.full_like(past_k, float("nan"))
-        present_v = torch.full_like(past_v, float("nan"))
+        pk_g = Guarded(case.past_k.shape, case.past_k.dtype, dev, fill=float("nan"))
+        pv_g = Guarded(case.past_v.shape, case.past_v.dtype, dev, fill=float("nan"))
+        guards = [(gk, "past_k"), (gv, "past_v"), (pk_g, "present_k"), (pv_g, "present_v")]
+        present_k, present_v = pk_g.t, pv_g.t
     else:
         present_k, present_v = past_k, past_v
     dv = case.w.v_head_dim or case.w.head_dim
-    out = torch.full((q.shape[0], q.shape[1], case.w.q_heads * dv), float("nan"), dtype=q.dtype, device=dev)
+    go = Guarded((q.shape[0], q.shape[1], case.w.q_heads * dv), q.dtype, dev, fill=float("nan"))
+    guards.append((go, "out"))
+    out = go.t
     status = torch.full((1,), status_init, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device=dev)
@@ -51,6 +92,8 @@ def run_gpu(case: Case, mode: str, separate_present: bool = False, attend_only: 
         gqa.check(fn(p, q, k, v, past_k, past_v, seq, cos, sin, sink, out, present_k, present_v, workspace, status),
                   mode)
     torch.cuda.synchronize()
+    for g, what in guards:
+        g.check(what)
     return dict(out=out, present_k=present_k, present_v=present_v, status=int(status.item()), workspace=workspace)
 
 
