@@ -307,6 +307,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                : "r"(addr));
 }
 
+// transpose of an 8x8 matrix of 16-bit values held one row-pair per lane (the ldmatrix
+// fragment layout: lane i has row i/4, columns 2(i%4) and 2(i%4) + 1)
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 template <typename T> struct Mma16816;
 template <> struct Mma16816<__nv_bfloat16> {
   static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {

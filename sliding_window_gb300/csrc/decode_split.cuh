@@ -22,10 +22,12 @@
 //
 // Pipeline: four warps, each takes 16 keys of every 64-key tile: S = Q K^T and O += P V on
 // mma.sync m16n8k16 (fp32 accumulate), online softmax in the exp2 domain with a lazily
-// moved reference max.  K and V tiles arrive by TMA (128B swizzle) through an NST-stage
-// mbarrier ring; warp 0 refills a stage as soon as all four warps have released it, and
-// before loading the tile that holds the group's new rows it writes them to present (K
-// rotated) so the TMA reads them back.  The CTA merges its warps in shared memory; a
+// moved reference max.  A group of at most 8 query rows runs the transposed products
+// S^T = K Q^T and O^T += V^T P^T instead (keys, then V's head dims, as the MMA's 16-row
+// side; the rows as its 8 columns), which halves the MMAs.  K and V tiles arrive by TMA
+// (128B swizzle) through an NST-stage mbarrier ring; the last of the four warps to release
+// a stage refills it, and before loading the tile that holds the group's new rows it
+// writes them to present (K rotated) so the TMA reads them back.  The CTA merges its warps in shared memory; a
 // one-chunk group finishes in place, otherwise the CTA writes (m, l, acc) and the last CTA
 // of the group (atomic ticket, no spin-wait) adds the sink once, normalizes and writes out.
 // Launched with programmatic stream serialization: the prologue overlaps the previous
@@ -81,9 +83,9 @@ template <int D, int DV, int MT, int NST, bool Q8 = false> struct Smem {
   static constexpr int kTileBytes = KT * D * kEs;  // one K tile; the V tile follows it
   static constexpr int kVTileBytes = KT * DV * kEs;
   static constexpr int kStageBytes = kTileBytes + kVTileBytes;
-  // Q8: every warp widens the V codes of its 16 keys of the stage to f16 here (the layout of
-  // a 16-bit V tile), right after the stages, so the two form one region for the merge below;
-  // K codes go from the stage straight into MMA fragments
+  // Q8, 16-row form: every warp widens the V codes of its 16 keys of the stage to f16 here
+  // (the layout of a 16-bit V tile), right after the stages, so the two form one region for
+  // the merge below; K codes go from the stage straight into MMA fragments
   static constexpr int kConvBytes = Q8 ? KT * DV * 2 : 0;
   static constexpr int kReuseBytes = NST * kStageBytes + kConvBytes;
   static constexpr int kQRows = MT * 16;
@@ -248,15 +250,22 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
   __syncwarp();
 }
 
-// Q8: the cache holds E4M3 codes (one scale per kv head for K and V).  Each warp widens its
-// keys of a stage to f16 in shared memory and the MMAs run on f16 (q converted exactly);
-// the K scale joins the score scale and the V scale the output.
-template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false>
+// Q8: the cache holds E4M3 codes (one scale per kv head for K and V) and the MMAs run on
+// f16 (q converted exactly); the K scale joins the score scale and the V scale the output.
+// The 16-row form converts K's codes straight into fragments and widens each warp's V rows
+// to f16 in shared memory; the transposed form converts both straight from ldmatrix loads
+// of the codes.
+// TR: a group of at most 8 query rows runs the transposed products S^T = K Q^T and
+// O^T += V^T P^T, with the warp's 16 keys (then 16 head dims of V) as the MMA's M and the
+// rows as its N of 8: half the MMAs of the 16-row form, and the Q fragments stay in
+// registers for the whole chunk.
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false, bool TR = false>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         DecodeArgs a) {
   using L = Smem<D, DV, MT, NST, Q8>;
   using M = Mma16816<typename std::conditional<Q8, __half, T>::type>;
+  static_assert(!TR || (MT == 1 && !MK && D % 32 == 0 && DV % 16 == 0), "transposed form: one 16-row tile, no mask");
   constexpr int QROWS = L::kQRows;
   constexpr int DCH = D / 8;    // 16-byte chunks per q / K row
   constexpr int VCH = DV / 8;   // 16-byte chunks per V row
@@ -495,6 +504,44 @@ __global__ void __launch_bounds__(kThreads, 2)
       row_ok[mt][h] = row < R;
       qa_row[mt][h] = past + (row < R ? row / a.G : 0);
     }
+  // transposed form: this thread's Q^T fragments (query row lane/4, head dims 16ks + 2(lane%4)
+  // and + 8), its rows 2(lane%4) + j, their running maxima, sums and O^T accumulators
+  uint32_t qf[TR ? D / 16 : 1][2];
+  float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};
+  float acct[TR ? DV / 16 : 1][4];
+  int qa_t[2];
+  bool ok_t[2];
+  if constexpr (TR && Q8) {
+    // f8 cache: k step ks covers head dims 16ks + 4t + {0, 1} (as k = 2t, 2t + 1) and
+    // 16ks + 4t + {2, 3} (as k = 2t + 8, 2t + 9), the order in which K's codes arrive below
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int ch = 2 * ks + ((lane & 3) >> 1);  // 16-byte chunk of head dims 16ks + 4t .. + 3
+      const uint2 w = *reinterpret_cast<const uint2 *>(qs + (ch >> 3) * (QROWS * 128) + sw128(lane >> 2, ch & 7) +
+                                                       (lane & 1) * 8);
+      qf[ks][0] = w.x;
+      qf[ks][1] = w.y;
+    }
+  } else if constexpr (TR) {
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks += 2) {
+      const int ch = 2 * ks + (lane >> 3);  // chunks 2ks .. 2ks + 3 of query row lane % 8
+      ldsm_x4(qs_u32 + (ch >> 3) * (QROWS * 128) + sw128(lane & 7, ch & 7), qf[ks][0], qf[ks][1], qf[ks + 1][0],
+              qf[ks + 1][1]);
+    }
+  }
+  if constexpr (TR) {
+#pragma unroll
+    for (int dm = 0; dm < DV / 16; ++dm)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acct[dm][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int row = 2 * (lane & 3) + j;
+      ok_t[j] = row < R;
+      qa_t[j] = past + (row < R ? row / a.G : 0);
+    }
+  }
   bool aborted = false;
   int t_fail = ntiles;
 
@@ -560,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (t + 1 < ntiles) load_mask(t + 1, mnext);
     }
     const uint8_t *k8 = stages + s * L::kStageBytes;  // Q8: the stage's K codes
-    if constexpr (Q8) {
+    if constexpr (Q8 && !TR) {
       // widen the V codes of this warp's 16 keys of the stage (rows of 128 codes,
       // 128B-swizzled) to f16 in the layout of a 16-bit V tile; only this warp reads these rows
       static_assert(!Q8 || (D == 128 && DV == 128), "f8 cache: D = Dv = 128");
@@ -580,149 +627,269 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const uint32_t ks_u32 = smem_u32(stages + s * L::kStageBytes);
     const uint32_t vs_u32 = Q8 ? smem_u32(smem + L::kConvOff) : ks_u32 + L::kTileBytes;
-
-    // ---- S = Q K^T over this warp's 16 keys, the k steps split over two independent
-    // accumulator chains (even and odd steps) that are added at the end
-    float sacc[MT][2][4], sodd[MT][2][4];
+    if constexpr (TR) {
+      // ---- S^T = K Q^T over this warp's 16 keys: lane (g, t) = (lane/4, lane%4) holds keys
+      // g and g + 8 of rows 2t and 2t + 1; even and odd k steps in two chains
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t kc[4];  // f8: the codes of two k steps
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t af[4];  // A = 16 keys x 16 head dims of K
+        if constexpr (Q8) {
+          // one 8x8 matrix of 16-bit pairs per 8 keys: lane (g, t) gets codes 16ks + 4t .. + 3
+          // of key g (then g + 8), widened in the head-dim order of the Q fragments
+          if ((ks & 1) == 0) {
+            const int krow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
+            const int kch = ks + (lane >> 4);
+            ldsm_x4(ks_u32 + krow * 128 + ((kch ^ (krow & 7)) << 4), kc[0], kc[1], kc[2], kc[3]);
+          }
+          const uint32_t w0 = kc[2 * (ks & 1)], w1 = kc[2 * (ks & 1) + 1];
+          af[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xFFFFu));
+          af[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
+          af[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xFFFFu));
+          af[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
+        } else {
+          const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
+          const int kch = 2 * ks + ((lane >> 3) & 1);
+          ldsm_x4(ks_u32 + (kch >> 3) * (KT * 128) + sw128(krow, kch & 7), af[0], af[2], af[1], af[3]);
+        }
+        M::run((ks & 1) ? s1 : s0, af, qf[ks][0], qf[ks][1]);
+      }
+      // ---- scale, softcap, band mask (frontier warps only)
+      const bool edge = !(kb >= c0 && kb + 15 < c1 && (!a.causal || kb + 15 <= q_abs_min) &&
+                          (a.window < 0 || q_abs_max - kb < a.window));
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+      for (int e = 0; e < 4; ++e) {
+        float x = s0[e] + s1[e];
+        x = a.cap_mul != 0.f ? tanh_fast(x * smul) * a.cap_mul : x * smul;
+        if (edge) {
+          const int key = kb + (lane >> 2) + 8 * (e >> 1);
+          const int qa = qa_t[e & 1];
+          const bool vis = ok_t[e & 1] && key >= c0 && key < c1 && (!a.causal || key <= qa) &&
+                           (a.window < 0 || qa - key < a.window);
+          if (!vis) x = -INFINITY;
+        }
+        s0[e] = x;
+      }
+      // ---- online softmax: a row's 16 keys sit in the 8 lanes of equal lane % 4
+      float p[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][n][e] = sodd[mt][n][e] = 0.f;
+      for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(s0[j], s0[2 + j]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (mx > mr[j] + kRescaleLog2 || (mr[j] == -INFINITY && mx != -INFINITY)) {
+          const float alpha = ex2(mr[j] - mx);  // 0 while nothing was visible
+          lr[j] *= alpha;
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t kb0, kb1, kb2, kb3;
+          for (int dm = 0; dm < DV / 16; ++dm) {
+            acct[dm][j] *= alpha;
+            acct[dm][2 + j] *= alpha;
+          }
+          mr[j] = mx;
+        }
+        const float m_use = mr[j] == -INFINITY ? 0.f : mr[j];
+        p[j] = ex2(s0[j] - m_use);
+        p[2 + j] = ex2(s0[2 + j] - m_use);
+        lr[j] += p[j] + p[2 + j];
+      }
+      // P^T as the B operand (keys 2t, 2t + 1 (+ 8) of row g): each 8x8 block transposed
+      const uint32_t pb0 = movm_t(M::pack(p[0], p[1])), pb1 = movm_t(M::pack(p[2], p[3]));
+      if (kb + 16 > total) {
+        const int first = max(0, total - kb);
+        if constexpr (Q8) {  // the V codes in the stage (code 0 is +0)
+          for (int idx = lane; idx < (16 - first) * 8; idx += 32) {
+            const int r = 16 * warp + first + idx / 8, ch = idx % 8;
+            *reinterpret_cast<uint4 *>(stages + s * L::kStageBytes + L::kTileBytes + r * 128 + ((ch ^ (r & 7)) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+        } else {
+          for (int idx = lane; idx < (16 - first) * VCH; idx += 32) {
+            const int r = 16 * warp + first + idx / VCH, ch = idx % VCH;
+            *reinterpret_cast<uint4 *>(stages + s * L::kStageBytes + L::kTileBytes + (ch >> 3) * (KT * 128) +
+                                       sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        __syncwarp();
+      }
+      // ---- O^T += V^T P^T: A = 16 head dims x 16 keys of V (transposing loads)
       if constexpr (Q8) {
-        // the B fragments straight from the codes: key row 16*warp + lane/4 (+8), head dims
-        // 16*ks + 2*(lane%4) (+8), i.e. a pair of neighbouring bytes of 16-byte chunk ks of
-        // the row, one pair conversion each
-        const int r0 = 16 * warp + (lane >> 2), o = 2 * (lane & 3);
-        const uint8_t *c0 = k8 + r0 * 128 + ((ks ^ (r0 & 7)) << 4) + o;
-        const uint8_t *c1 = c0 + 8 * 128;  // row r0 + 8: the same swizzle phase
-        kb0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0));
-        kb1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0 + 8));
-        kb2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1));
-        kb3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1 + 8));
+        // one transposed 8x8 matrix of 16-bit code pairs per 8 keys and 16 head dims: lane
+        // (g, t) gets codes 16dm + 2g, 2g + 1 of keys 2t and 2t + 1; a byte permute pairs
+        // them by head dim, so A's row g is head dim 16dm + 2g and row g + 8 is 16dm + 2g + 1
+        const uint32_t vc_u32 = ks_u32 + L::kTileBytes;
+#pragma unroll
+        for (int dm = 0; dm < DV / 16; dm += 2) {
+          uint32_t w[4];
+          const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int vch = dm + (lane >> 4);
+          ldsm_x4_t(vc_u32 + vrow * 128 + ((vch ^ (vrow & 7)) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t x0 = __byte_perm(w[2 * h], 0, 0x3120), x1 = __byte_perm(w[2 * h + 1], 0, 0x3120);
+            uint32_t af[4];
+            af[0] = e4m3x2_to_f16x2((uint16_t)(x0 & 0xFFFFu));
+            af[1] = e4m3x2_to_f16x2((uint16_t)(x0 >> 16));
+            af[2] = e4m3x2_to_f16x2((uint16_t)(x1 & 0xFFFFu));
+            af[3] = e4m3x2_to_f16x2((uint16_t)(x1 >> 16));
+            M::run(acct[dm + h], af, pb0, pb1);
+          }
+        }
       } else {
-        const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
-        const int kch = 2 * ks + ((lane >> 3) & 1);
-        ldsm_x4(ks_u32 + (kch >> 3) * (KT * 128) + sw128(krow, kch & 7), kb0, kb1, kb2, kb3);
-      }
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t af[4];
-        const int qrow = 16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int qch = 2 * ks + (lane >> 4);
-        ldsm_x4(qs_u32 + (qch >> 3) * (QROWS * 128) + sw128(qrow, qch & 7), af[0], af[1], af[2], af[3]);
-        M::run((ks & 1) ? sodd[mt][0] : sacc[mt][0], af, kb0, kb1);
-        M::run((ks & 1) ? sodd[mt][1] : sacc[mt][1], af, kb2, kb3);
-      }
-    }
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][n][e] += sodd[mt][n][e];
-
-    // ---- scale, softcap, band mask (only on warps whose keys cross a frontier)
-    const bool edge = !(kb >= c0 && kb + 15 < c1 && (!a.causal || kb + 15 <= q_abs_min) &&
-                        (a.window < 0 || q_abs_max - kb < a.window));
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float x = sacc[mt][n][e];
-          bool dropped = false;
-          if constexpr (MK) {
-            const uint32_t bits = (mcur[mt][n][e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-            if (a.mask_kind == 1) {
-              dropped = bits == 0;
-            } else {
-              T bv;
-              *reinterpret_cast<uint16_t *>(&bv) = (uint16_t)bits;
-              x = fmaf(to_f32(bv), a.mask_mul, x);  // the bias joins before the scale and softcap
-            }
-          }
-          x = a.cap_mul != 0.f ? tanh_fast(x * smul) * a.cap_mul : x * smul;
-          if (dropped) x = -INFINITY;
-          if (edge) {
-            const int key = kb + 8 * n + 2 * (lane & 3) + (e & 1);
-            const int qa = qa_row[mt][e >> 1];
-            const bool vis = row_ok[mt][e >> 1] && key >= c0 && key < c1 && (!a.causal || key <= qa) &&
-                             (a.window < 0 || qa - key < a.window);
-            if (!vis) x = -INFINITY;
-          }
-          sacc[mt][n][e] = x;
+        for (int dm = 0; dm < DV / 16; ++dm) {
+          uint32_t af[4];
+          const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int vch = 2 * dm + (lane >> 4);
+          ldsm_x4_t(vs_u32 + (vch >> 3) * (KT * 128) + sw128(vrow, vch & 7), af[0], af[2], af[1], af[3]);
+          M::run(acct[dm], af, pb0, pb1);
         }
-
-    // ---- online softmax, reference max moved lazily (rows lane/4 and lane/4 + 8)
-    uint32_t pa[MT][4];
+      }
+    } else {
+      // ---- S = Q K^T over this warp's 16 keys, the k steps split over two independent
+      // accumulator chains (even and odd steps) that are added at the end
+      float sacc[MT][2][4], sodd[MT][2][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      float p[2][4];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float mx = fmaxf(fmaxf(sacc[mt][0][2 * h], sacc[mt][0][2 * h + 1]),
-                         fmaxf(sacc[mt][1][2 * h], sacc[mt][1][2 * h + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        if (mx > m[mt][h] + kRescaleLog2 || (m[mt][h] == -INFINITY && mx != -INFINITY)) {
-          const float alpha = ex2(m[mt][h] - mx);  // 0 while nothing was visible
-          l[mt][h] *= alpha;
-#pragma unroll
-          for (int dn = 0; dn < DV / 8; ++dn) {
-            acc[mt][dn][2 * h] *= alpha;
-            acc[mt][dn][2 * h + 1] *= alpha;
-          }
-          m[mt][h] = mx;
-        }
-        const float m_use = m[mt][h] == -INFINITY ? 0.f : m[mt][h];
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float pv = ex2(sacc[mt][n][2 * h + e] - m_use);
-            p[n][2 * h + e] = pv;
-            l[mt][h] += pv;
-          }
-      }
-      pa[mt][0] = M::pack(p[0][0], p[0][1]);
-      pa[mt][1] = M::pack(p[0][2], p[0][3]);
-      pa[mt][2] = M::pack(p[1][0], p[1][1]);
-      pa[mt][3] = M::pack(p[1][2], p[1][3]);
-    }
-
-    // ---- stale V rows (slots >= total) may hold NaN/Inf: zero them so 0 * V stays 0
-    const bool stale = kb + 16 > total;
-    if (stale) {
-      const int first = max(0, total - kb);
-      for (int idx = lane; idx < (16 - first) * VCH; idx += 32) {
-        const int r = 16 * warp + first + idx / VCH, ch = idx % VCH;
-        *reinterpret_cast<uint4 *>((Q8 ? smem + L::kConvOff : stages + s * L::kStageBytes + L::kTileBytes) +
-                                   (ch >> 3) * (KT * 128) +
-                                   sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-    }
-
-    // ---- O += P V over this warp's 16 keys
+          for (int e = 0; e < 4; ++e) sacc[mt][n][e] = sodd[mt][n][e] = 0.f;
 #pragma unroll
-    for (int dd = 0; dd < DV / 16; ++dd) {
-      uint32_t v0, v1, v2, v3;
-      const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
-      const int vch = 2 * dd + (lane >> 4);
-      ldsm_x4_t(vs_u32 + (vch >> 3) * (KT * 128) + sw128(vrow, vch & 7), v0, v1, v2, v3);
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t kb0, kb1, kb2, kb3;
+        if constexpr (Q8) {
+          // the B fragments straight from the codes: key row 16*warp + lane/4 (+8), head dims
+          // 16*ks + 2*(lane%4) (+8), i.e. a pair of neighbouring bytes of 16-byte chunk ks of
+          // the row, one pair conversion each
+          const int r0 = 16 * warp + (lane >> 2), o = 2 * (lane & 3);
+          const uint8_t *c0 = k8 + r0 * 128 + ((ks ^ (r0 & 7)) << 4) + o;
+          const uint8_t *c1 = c0 + 8 * 128;  // row r0 + 8: the same swizzle phase
+          kb0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0));
+          kb1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0 + 8));
+          kb2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1));
+          kb3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1 + 8));
+        } else {
+          const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
+          const int kch = 2 * ks + ((lane >> 3) & 1);
+          ldsm_x4(ks_u32 + (kch >> 3) * (KT * 128) + sw128(krow, kch & 7), kb0, kb1, kb2, kb3);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t af[4];
+          const int qrow = 16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int qch = 2 * ks + (lane >> 4);
+          ldsm_x4(qs_u32 + (qch >> 3) * (QROWS * 128) + sw128(qrow, qch & 7), af[0], af[1], af[2], af[3]);
+          M::run((ks & 1) ? sodd[mt][0] : sacc[mt][0], af, kb0, kb1);
+          M::run((ks & 1) ? sodd[mt][1] : sacc[mt][1], af, kb2, kb3);
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mt][n][e] += sodd[mt][n][e];
+
+      // ---- scale, softcap, band mask (only on warps whose keys cross a frontier)
+      const bool edge = !(kb >= c0 && kb + 15 < c1 && (!a.causal || kb + 15 <= q_abs_min) &&
+                          (a.window < 0 || q_abs_max - kb < a.window));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x = sacc[mt][n][e];
+            bool dropped = false;
+            if constexpr (MK) {
+              const uint32_t bits = (mcur[mt][n][e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+              if (a.mask_kind == 1) {
+                dropped = bits == 0;
+              } else {
+                T bv;
+                *reinterpret_cast<uint16_t *>(&bv) = (uint16_t)bits;
+                x = fmaf(to_f32(bv), a.mask_mul, x);  // the bias joins before the scale and softcap
+              }
+            }
+            x = a.cap_mul != 0.f ? tanh_fast(x * smul) * a.cap_mul : x * smul;
+            if (dropped) x = -INFINITY;
+            if (edge) {
+              const int key = kb + 8 * n + 2 * (lane & 3) + (e & 1);
+              const int qa = qa_row[mt][e >> 1];
+              const bool vis = row_ok[mt][e >> 1] && key >= c0 && key < c1 && (!a.causal || key <= qa) &&
+                               (a.window < 0 || qa - key < a.window);
+              if (!vis) x = -INFINITY;
+            }
+            sacc[mt][n][e] = x;
+          }
+
+      // ---- online softmax, reference max moved lazily (rows lane/4 and lane/4 + 8)
+      uint32_t pa[MT][4];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        M::run(acc[mt][2 * dd], pa[mt], v0, v1);
-        M::run(acc[mt][2 * dd + 1], pa[mt], v2, v3);
+        float p[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float mx = fmaxf(fmaxf(sacc[mt][0][2 * h], sacc[mt][0][2 * h + 1]),
+                           fmaxf(sacc[mt][1][2 * h], sacc[mt][1][2 * h + 1]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          if (mx > m[mt][h] + kRescaleLog2 || (m[mt][h] == -INFINITY && mx != -INFINITY)) {
+            const float alpha = ex2(m[mt][h] - mx);  // 0 while nothing was visible
+            l[mt][h] *= alpha;
+#pragma unroll
+            for (int dn = 0; dn < DV / 8; ++dn) {
+              acc[mt][dn][2 * h] *= alpha;
+              acc[mt][dn][2 * h + 1] *= alpha;
+            }
+            m[mt][h] = mx;
+          }
+          const float m_use = m[mt][h] == -INFINITY ? 0.f : m[mt][h];
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float pv = ex2(sacc[mt][n][2 * h + e] - m_use);
+              p[n][2 * h + e] = pv;
+              l[mt][h] += pv;
+            }
+        }
+        pa[mt][0] = M::pack(p[0][0], p[0][1]);
+        pa[mt][1] = M::pack(p[0][2], p[0][3]);
+        pa[mt][2] = M::pack(p[1][0], p[1][1]);
+        pa[mt][3] = M::pack(p[1][2], p[1][3]);
+      }
+
+      // ---- stale V rows (slots >= total) may hold NaN/Inf: zero them so 0 * V stays 0
+      const bool stale = kb + 16 > total;
+      if (stale) {
+        const int first = max(0, total - kb);
+        for (int idx = lane; idx < (16 - first) * VCH; idx += 32) {
+          const int r = 16 * warp + first + idx / VCH, ch = idx % VCH;
+          *reinterpret_cast<uint4 *>((Q8 ? smem + L::kConvOff : stages + s * L::kStageBytes + L::kTileBytes) +
+                                     (ch >> 3) * (KT * 128) +
+                                     sw128(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+
+      // ---- O += P V over this warp's 16 keys
+#pragma unroll
+      for (int dd = 0; dd < DV / 16; ++dd) {
+        uint32_t v0, v1, v2, v3;
+        const int vrow = 16 * warp + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int vch = 2 * dd + (lane >> 4);
+        ldsm_x4_t(vs_u32 + (vch >> 3) * (KT * 128) + sw128(vrow, vch & 7), v0, v1, v2, v3);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          M::run(acc[mt][2 * dd], pa[mt], v0, v1);
+          M::run(acc[mt][2 * dd + 1], pa[mt], v2, v3);
+        }
       }
     }
-    if (stale) fence_proxy_async_smem();
+    if (kb + 16 > total) fence_proxy_async_smem();
     __syncwarp();
     // the last of the four warps to finish with the stage refills it: nobody waits for the
     // others (the count only grows; every fourth arrival is a tile's last)
@@ -750,19 +917,36 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // -------------------------------------------------------------- merge the 4 warps
   // per-warp row statistics (outside the stages: safe while aborted copies still land)
+  if constexpr (TR) {
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float lv = l[mt][h];
-      lv += __shfl_xor_sync(0xffffffffu, lv, 1);
-      lv += __shfl_xor_sync(0xffffffffu, lv, 2);
-      if ((lane & 3) == 0) {
-        const int row = 16 * mt + (lane >> 2) + 8 * h;
-        red_m[warp * QROWS + row] = m[mt][h];
+    for (int j = 0; j < 2; ++j) {
+      float lv = lr[j];
+      lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+      lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+      lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+      if (lane < 4) {
+        const int row = 2 * lane + j;
+        red_m[warp * QROWS + row] = mr[j];
         red_l[warp * QROWS + row] = lv;
+        red_m[warp * QROWS + 8 + row] = -INFINITY;  // rows 8-15 of the tile: none
+        red_l[warp * QROWS + 8 + row] = 0.f;
       }
     }
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float lv = l[mt][h];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+        if ((lane & 3) == 0) {
+          const int row = 16 * mt + (lane >> 2) + 8 * h;
+          red_m[warp * QROWS + row] = m[mt][h];
+          red_l[warp * QROWS + row] = lv;
+        }
+      }
+  }
   // one decision for the whole CTA (a timed-out wait anywhere aborts it), taken by the
   // barrier that publishes the statistics
   aborted = __syncthreads_or(aborted || flags[0] != 0);
@@ -783,6 +967,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (nchunks == 1) return;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) m[mt][0] = m[mt][1] = -INFINITY;
+      mr[0] = mr[1] = -INFINITY;
       for (int i = threadIdx.x; i < kWarps * QROWS; i += kThreads) red_m[i] = -INFINITY;
       __syncthreads();  // uniform branch; thread 0 has drained the copies
     } else {
@@ -814,21 +999,46 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   constexpr int AST = L::kAccStride;
   float *wacc = reinterpret_cast<float *>(stages);  // [kWarps][QROWS][AST]
+  if constexpr (TR) {
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int row = 16 * mt + (lane >> 2) + 8 * h;
-      if (row >= R) continue;  // padding rows of the MMA tile are never read
+    for (int j = 0; j < 2; ++j) {
+      const int row = 2 * (lane & 3) + j;
+      if (row >= R) continue;  // padding rows are never read
       float mm = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, red_m[w * QROWS + row]);
-      const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
-      float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane & 3);
+      const float f = ex2(mr[j] - (mm == -INFINITY ? 0.f : mm));
+      if constexpr (Q8) {  // head dims 16dm + 2(lane/4) and + 1
+        float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane >> 2);
 #pragma unroll
-      for (int dn = 0; dn < DV / 8; ++dn)
-        *reinterpret_cast<float2 *>(dst + 8 * dn) = make_float2(acc[mt][dn][2 * h] * f, acc[mt][dn][2 * h + 1] * f);
+        for (int dm = 0; dm < DV / 16; ++dm)
+          *reinterpret_cast<float2 *>(dst + 16 * dm) = make_float2(acct[dm][j] * f, acct[dm][2 + j] * f);
+      } else {  // head dims 16dm + lane/4 and + 8
+        float *dst = wacc + ((size_t)warp * QROWS + row) * AST + (lane >> 2);
+#pragma unroll
+        for (int dm = 0; dm < DV / 16; ++dm) {
+          dst[16 * dm] = acct[dm][j] * f;
+          dst[16 * dm + 8] = acct[dm][2 + j] * f;
+        }
+      }
     }
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = 16 * mt + (lane >> 2) + 8 * h;
+        if (row >= R) continue;  // padding rows of the MMA tile are never read
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, red_m[w * QROWS + row]);
+        const float f = ex2(m[mt][h] - (mm == -INFINITY ? 0.f : mm));
+        float *dst = wacc + ((size_t)warp * QROWS + row) * AST + 2 * (lane & 3);
+#pragma unroll
+        for (int dn = 0; dn < DV / 8; ++dn)
+          *reinterpret_cast<float2 *>(dst + 8 * dn) = make_float2(acc[mt][dn][2 * h] * f, acc[mt][dn][2 * h + 1] * f);
+      }
+  }
   __syncthreads();
   auto merged = [&](int idx4) {  // float4 idx4 of the CTA's [R][DV] accumulator
     const float4 *w4 = reinterpret_cast<const float4 *>(wacc) + (idx4 / (DV / 4)) * (AST / 4) + idx4 % (DV / 4);
@@ -1030,7 +1240,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false>
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false, bool TR = false>
 gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   using L = Smem<D, DV, MT, NST, Q8>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
@@ -1046,7 +1256,7 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
     if (!encode_kv_tile_map(&tk, c.present_k, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
     if (!encode_kv_tile_map(&tv, c.present_v, DV, rows, outer, KT, 2)) return GQA_ERR_CUDA;
   }
-  auto kern = decode_split_kernel<T, D, DV, MT, NST, CL, MK, Q8>;
+  auto kern = decode_split_kernel<T, D, DV, MT, NST, CL, MK, Q8, TR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -1141,14 +1351,21 @@ gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   const int D = c.p.head_dim, DV = c.Dv;
   if constexpr (Q8) {  // f8 cache: D = Dv = 128, five 16 KB stages and a 16 KB f16 V tile
     if (D == 128 && DV == 128 && !MK && !MIXED) {
+      if (dp.mtiles == 1 && dp.rows <= 8) return launch_cfg<T, 128, 128, 1, 5, CL, false, true, true>(c, dp, a);
       if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 5, CL, false, true>(c, dp, a);
       if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 5, CL, false, true>(c, dp, a);
     }
   } else if constexpr (!MIXED) {
     if (D == 128 && DV == 128) {
+      if constexpr (!MK) {  // at most 8 rows: the transposed form
+        if (dp.rows <= 8) return launch_cfg<T, 128, 128, 1, 3, CL, false, false, true>(c, dp, a);
+      }
       if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 3, CL, MK>(c, dp, a);
       if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 3, CL, MK>(c, dp, a);
     } else if (D == 64 && DV == 64) {
+      if constexpr (!MK) {  // at most 8 rows: the transposed form
+        if (dp.rows <= 8) return launch_cfg<T, 64, 64, 1, 6, CL, false, false, true>(c, dp, a);
+      }
       if (dp.mtiles == 1) return launch_cfg<T, 64, 64, 1, 6, CL, MK>(c, dp, a);
       if (dp.mtiles == 2) return launch_cfg<T, 64, 64, 2, 6, CL, MK>(c, dp, a);
       if (dp.mtiles == 3) return launch_cfg<T, 64, 64, 3, 6, CL, MK>(c, dp, a);
@@ -1156,9 +1373,15 @@ gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
     }
   } else {
     if (D == 128 && DV == 64) {
+      if constexpr (!MK) {  // at most 8 rows: the transposed form
+        if (dp.rows <= 8) return launch_cfg<T, 128, 64, 1, 4, CL, false, false, true>(c, dp, a);
+      }
       if (dp.mtiles == 1) return launch_cfg<T, 128, 64, 1, 4, CL, MK>(c, dp, a);
       if (dp.mtiles == 2) return launch_cfg<T, 128, 64, 2, 4, CL, MK>(c, dp, a);
     } else if (D == 64 && DV == 128) {
+      if constexpr (!MK) {  // at most 8 rows: the transposed form
+        if (dp.rows <= 8) return launch_cfg<T, 64, 128, 1, 4, CL, false, false, true>(c, dp, a);
+      }
       if (dp.mtiles == 1) return launch_cfg<T, 64, 128, 1, 4, CL, MK>(c, dp, a);
       if (dp.mtiles == 2) return launch_cfg<T, 64, 128, 2, 4, CL, MK>(c, dp, a);
     }

@@ -76,7 +76,7 @@ def check(c, k8, v8, ks, vs, what):
     assert_close(out_rows(out, c), ref, c.w.dtype, what)
 
 
-SPLIT = list(itertools.product(["bf16", "f16"], [(4, 1), (8, 4)], [(3000, 300), (20000, -1)]))
+SPLIT = list(itertools.product(["bf16", "f16"], [(4, 1), (2, 3), (4, 3), (8, 4)], [(3000, 300), (20000, -1)]))
 
 
 @pytest.mark.parametrize("dtype,gc,capw", SPLIT)

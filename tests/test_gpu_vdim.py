@@ -39,7 +39,7 @@ def check(c, mode, dtype, what, separate=False):
     assert_close(out_rows(r["out"], c), ref, dtype, what)
 
 
-DECODE = list(itertools.product(["bf16", "f16"], DIMS, [(4, 1), (8, 4)], [(3000, 300), (20000, -1)]))
+DECODE = list(itertools.product(["bf16", "f16"], DIMS, [(4, 1), (2, 3), (4, 3), (8, 4)], [(3000, 300), (20000, -1)]))
 
 
 @pytest.mark.parametrize("dtype,dims,gc,capw", DECODE)
