@@ -104,8 +104,12 @@ def _load():
         lib.oracle_encode_e4m3.restype = ctypes.c_uint8
         lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
         lib.oracle_decode_e4m3.restype = f64
-        lib.oracle_rope_append_q8.argtypes = [i32] * 10 + [vp] * 11 + [ctypes.POINTER(i32)]
-        lib.oracle_attention_q8.argtypes = [i32] * 9 + [f64, f64] + [i32] * 4 + [vp] * 8 + [i64, vp]
+        lib.oracle_encode_i8.argtypes = [ctypes.c_float]
+        lib.oracle_encode_i8.restype = ctypes.c_int8
+        lib.oracle_decode_i8.argtypes = [ctypes.c_int8]
+        lib.oracle_decode_i8.restype = f64
+        lib.oracle_rope_append_q8.argtypes = [i32] * 10 + [vp] * 11 + [ctypes.POINTER(i32), i32]
+        lib.oracle_attention_q8.argtypes = [i32] * 9 + [f64, f64] + [i32] * 4 + [vp] * 8 + [i64, vp, i32]
         lib.oracle_has_openmp.restype = i32
         _lib = lib
         return lib
@@ -447,11 +451,29 @@ def decode_e4m3(codes) -> np.ndarray:
     return np.array([lib.oracle_decode_e4m3(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
 
 
+def encode_i8(x) -> np.ndarray:
+    """int8 codes of float32 values: nearest, ties to even, saturating at -128 and 127
+    (infinities included), NaN to 0."""
+    lib = _load()
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    return np.array([lib.oracle_encode_i8(float(v)) for v in a.ravel()], dtype=np.int8).reshape(a.shape)
+
+
+def decode_i8(codes) -> np.ndarray:
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.int8)
+    return np.array([lib.oracle_decode_i8(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+KV_FORMATS = {"e4m3": 0, "int8": 1}
+
+
 def rope_append_q8(p: dict, q, k, v, present_k8, present_v8, seqlens_k, k_scale, v_scale, cos_cache=None,
-                   sin_cache=None):
-    """Append into an E4M3 cache in place: K (rotated, rounded to the dtype) and V divided by
-    their kv head's scale in fp32 and encoded.  present_k8 [B, Hkv, cap, D] and present_v8
-    [B, Hkv, cap, Dv] are uint8 arrays updated in place.  Returns (q_rot, status_bits)."""
+                   sin_cache=None, fmt="e4m3"):
+    """Append into a quantized cache in place: K (rotated, rounded to the dtype) and V divided
+    by their kv head's scale in fp32 and encoded as `fmt` codes ("e4m3" or "int8", one byte
+    each).  present_k8 [B, Hkv, cap, D] and present_v8 [B, Hkv, cap, Dv] are uint8 arrays (the
+    codes' bytes) updated in place.  Returns (q_rot, status_bits)."""
     lib = _load()
     dt = p["dtype"]
     q, k, v = _bits(q, dt), _bits(k, dt), _bits(v, dt)
@@ -467,13 +489,13 @@ def rope_append_q8(p: dict, q, k, v, present_k8, present_v8, seqlens_k, k_scale,
     lib.oracle_rope_append_q8(p["batch"], p["q_heads"], p["kv_heads"], p["head_dim"], v_dim(p), p["q_len"],
                               p["cap_present"], p.get("rope_len", 0), DTYPE_CODES[dt], int(p.get("do_rotary", 0)),
                               _ptr(q), _ptr(k), _ptr(v), _ptr(seq), _ptr(cs), _ptr(sn), _ptr(ks), _ptr(vs),
-                              _ptr(q_rot), _ptr(present_k8), _ptr(present_v8), ctypes.byref(st))
+                              _ptr(q_rot), _ptr(present_k8), _ptr(present_v8), ctypes.byref(st), KV_FORMATS[fmt])
     return q_rot, int(st.value)
 
 
 def attention_q8(p: dict, q_rot, present_k8, present_v8, seqlens_k, k_scale, v_scale, head_sink=None,
-                 rows=None) -> np.ndarray:
-    """Attention in fp64 over the dequantized E4M3 cache (code * scale of its kv head)."""
+                 rows=None, fmt="e4m3") -> np.ndarray:
+    """Attention in fp64 over the dequantized cache (code * scale of its kv head; `fmt` codes)."""
     lib = _load()
     dt = p["dtype"]
     qb = _bits(q_rot, dt)
@@ -494,7 +516,7 @@ def attention_q8(p: dict, q_rot, present_k8, present_v8, seqlens_k, k_scale, v_s
                             DTYPE_CODES[dt], float(p.get("scale", 0.0)), float(p.get("softcap", 0.0)),
                             int(p.get("window", -1)), int(p.get("causal", 1)), int(p.get("do_rotary", 0)),
                             int(p.get("smooth_softmax", 0)), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(ks), _ptr(vs),
-                            _ptr(seq), _ptr(sink), _ptr(ridx), n, _ptr(out))
+                            _ptr(seq), _ptr(sink), _ptr(ridx), n, _ptr(out), KV_FORMATS[fmt])
     if rows is None:
         return out.reshape(B, curr, Hq, Dv)
     return out

@@ -750,11 +750,34 @@ uint8_t oracle_encode_e4m3(float x) {
   return (uint8_t)(sign | (uint8_t)((E + 7) << 3) | (uint8_t)(n - 8.0));
 }
 
+/* The second quantized reading: an int8 cache.  Each element holds a two's-complement code
+ * in [-128, 127] with the same per-kv-head scales; the stored value is code * scale.  The
+ * code follows the ONNX QuantizeLinear convention with a zero point of 0:
+ *     code = saturate(round(fp32(x) / fp32(scale)))
+ * rounded half to even and saturated at -128 and 127 (infinities too); NaN, which that
+ * convention leaves undefined, gives 0. */
+int8_t oracle_encode_i8(float x) {
+  if (isnan(x)) return 0;
+  double r = rint((double)x); /* the default rounding mode: nearest, ties to even */
+  if (r > 127.0) r = 127.0;
+  if (r < -128.0) r = -128.0;
+  return (int8_t)r;
+}
+double oracle_decode_i8(int8_t c) { return (double)c; }
+
+/* fmt 0: E4M3 codes; fmt 1: int8 codes */
+static uint8_t encode_code(float x, int32_t fmt) {
+  return fmt == 1 ? (uint8_t)oracle_encode_i8(x) : oracle_encode_e4m3(x);
+}
+static double decode_code(uint8_t c, int32_t fmt) {
+  return fmt == 1 ? oracle_decode_i8((int8_t)c) : oracle_decode_e4m3(c);
+}
+
 void oracle_rope_append_q8(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Dv, int32_t curr, int32_t cap,
                            int32_t rope_len, int32_t dtype, int32_t do_rotary, const void *q, const void *k,
                            const void *v, const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
                            const float *k_scale, const float *v_scale, void *q_rot, uint8_t *present_k,
-                           uint8_t *present_v, int32_t *status_out) {
+                           uint8_t *present_v, int32_t *status_out, int32_t fmt) {
   size_t es = elem_size(dtype);
   int32_t status_all = 0;
   void *row = malloc(es * (size_t)(D > Dv ? D : Dv));
@@ -771,11 +794,11 @@ void oracle_rope_append_q8(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_
           rotate_row(k, src, cos_cache, sin_cache, (size_t)(past + i) * (D / 2), D, dtype, row, 0);
         else
           memcpy(row, (const char *)k + src * es, (size_t)D * es);
-        for (int d = 0; d < D; ++d) present_k[dst + d] = oracle_encode_e4m3(load_f32(row, d, dtype) / k_scale[h]);
+        for (int d = 0; d < D; ++d) present_k[dst + d] = encode_code(load_f32(row, d, dtype) / k_scale[h], fmt);
         size_t src_v = (((size_t)b * curr + i) * Hkv + h) * Dv;
         size_t dst_v = (((size_t)b * Hkv + h) * cap + (size_t)(past + i)) * Dv;
         for (int d = 0; d < Dv; ++d)
-          present_v[dst_v + d] = oracle_encode_e4m3(load_f32(v, src_v + d, dtype) / v_scale[h]);
+          present_v[dst_v + d] = encode_code(load_f32(v, src_v + d, dtype) / v_scale[h], fmt);
       }
     if (q_rot) {
       for (int i = 0; i < curr; ++i)
@@ -797,7 +820,7 @@ void oracle_attention_q8(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t 
                          int32_t causal, int32_t do_rotary, int32_t smooth_softmax, const void *q,
                          const uint8_t *present_k, const uint8_t *present_v, const float *k_scale,
                          const float *v_scale, const int32_t *seqlens_k, const float *head_sink,
-                         const int64_t *rows, int64_t nrows, double *out) {
+                         const int64_t *rows, int64_t nrows, double *out, int32_t fmt) {
   int G = Hq / Hkv;
   if (scale == 0.0) scale = 1.0 / sqrt((double)D);
   int64_t count = rows ? nrows : (int64_t)B * curr * Hq;
@@ -822,8 +845,8 @@ void oracle_attention_q8(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t 
     double *kd = (double *)malloc(sizeof(double) * (size_t)(total * D));
     double *vd = (double *)malloc(sizeof(double) * (size_t)(total * Dv));
     size_t kb = ((size_t)b * Hkv + hk) * (size_t)cap * D, vb = ((size_t)b * Hkv + hk) * (size_t)cap * Dv;
-    for (int64_t j = 0; j < total * D; ++j) kd[j] = oracle_decode_e4m3(present_k[kb + (size_t)j]) * (double)k_scale[hk];
-    for (int64_t j = 0; j < total * Dv; ++j) vd[j] = oracle_decode_e4m3(present_v[vb + (size_t)j]) * (double)v_scale[hk];
+    for (int64_t j = 0; j < total * D; ++j) kd[j] = decode_code(present_k[kb + (size_t)j], fmt) * (double)k_scale[hk];
+    for (int64_t j = 0; j < total * Dv; ++j) vd[j] = decode_code(present_v[vb + (size_t)j], fmt) * (double)v_scale[hk];
     double *qv = (double *)malloc(sizeof(double) * (size_t)D);
     for (int d = 0; d < D; ++d) qv[d] = load_elem(q, (size_t)r * D + d, dtype);
     uint8_t *vis = (uint8_t *)malloc((size_t)total);
