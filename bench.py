@@ -204,7 +204,7 @@ class Step:
             L = dict(c=c, p=p, p_attend=gqa.params_from_dict(dict(c.params, do_rotary=0)), ws=ws,
                      out=torch.empty_like(c.q), q_rot=torch.empty_like(c.q),
                      status=torch.zeros(1, dtype=torch.int32, device=device))
-            if w.kv_q8:  # the cache is f8 codes: the dtype caches are replaced by them
+            if w.kv_q8:  # the cache is one-byte codes: the dtype caches are replaced by them
                 c.past_k, c.past_v = c.extra["k8"], c.extra["v8"]
             if w.mask:  # device-resident like the cache (a bias computed or reused on the device)
                 L["mask_t"] = c.extra["mask"]
@@ -224,7 +224,8 @@ class Step:
             self.layers.append(L)
         self.fn = gqa.gqa_attention_decode if w.mode == "decode" else gqa.gqa_attention_prefill
         self.fn_masked = gqa.gqa_attention_decode_masked if w.mode == "decode" else gqa.gqa_attention_prefill_masked
-        self.fn_q8 = gqa.gqa_attention_decode_q8 if w.mode == "decode" else gqa.gqa_attention_prefill_q8
+        sfx = "i8" if w.kv_q8 == 2 else "q8"
+        self.fn_q8 = getattr(gqa, "gqa_attention_%s_%s" % ("decode" if w.mode == "decode" else "prefill", sfx))
         # all layers' outputs side by side, for one device->host copy per step
         self.out_all = torch.empty(sum(L["out"].numel() for L in self.layers), dtype=self.layers[0]["out"].dtype,
                                    device=device)
@@ -278,7 +279,7 @@ class Step:
     def call(self, L, p, q, k, v, past_k, past_v, seqlens, cos, sin, sink, out, present_k, present_v, ws, st,
              stream):
         """The layer's public call: the masked entry point when the workload has a mask, the
-        f8-cache one when its cache is quantized."""
+        quantized-cache one (f8 or int8) when its cache is quantized."""
         if self.w.kv_q8:
             c = L["c"]
             return self.fn_q8(p, q, k, v, seqlens, cos, sin, sink, c.extra["k_scale"], c.extra["v_scale"], out,
@@ -610,7 +611,8 @@ class OracleSample:
                                     mask=_storage(c.extra["mask"]) if "mask" in c.extra else None,
                                     q8=None if "k8" not in c.extra else (
                                         c.extra["k8"].numpy().copy(), c.extra["v8"].numpy().copy(),
-                                        c.extra["k_scale"].numpy(), c.extra["v_scale"].numpy())))
+                                        c.extra["k_scale"].numpy(), c.extra["v_scale"].numpy(),
+                                        "int8" if w.kv_q8 == 2 else "e4m3")))
         self.units = units
         self.sample = desc + (" x %d layers" % self.w.layers if self.w.layers > 1 else "")
 
@@ -618,10 +620,10 @@ class OracleSample:
         o = self.oracle
         for L in self.layers:
             if L["q8"] is not None:
-                k8, v8, ks, vs = L["q8"]
+                k8, v8, ks, vs, fmt = L["q8"]
                 q_rot, _ = o.rope_append_q8(L["p"], L["q"], L["k"], L["v"], k8, v8, L["seq"], ks, vs, L["cos"],
-                                            L["sin"])
-                o.attention_q8(L["p"], q_rot, k8, v8, L["seq"], ks, vs, L["sink"], rows=L["rows"])
+                                            L["sin"], fmt=fmt)
+                o.attention_q8(L["p"], q_rot, k8, v8, L["seq"], ks, vs, L["sink"], rows=L["rows"], fmt=fmt)
                 continue
             if L["p"].get("kv_ring", 0):
                 q_rot, pk, pv, _ = o.rope_append_ring(L["p"], L["q"], L["k"], L["v"], L["pk"], L["pv"], L["seq"],
@@ -664,7 +666,7 @@ SUB_WORKLOADS = {"prefill_sink_softcap_bf16": 8, "decode_window_bf16": 1000, "sp
 DEFAULT_STEPS = {"decode_window_bf16": 20000, "specdecode_rotary_f16": 2000, "decode_long_bf16": 200,
                  "prefill_sink_softcap_bf16": 100, "prefill_fp32_tiny": 5000, "decode_window_ring_bf16": 20000,
                  "decode_window_paged_bf16": 20000, "decode_window_vdim_bf16": 20000, "prefill_bias_bf16": 80,
-                 "decode_window_q8_bf16": 20000}
+                 "decode_window_q8_bf16": 20000, "decode_window_i8_bf16": 20000}
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (the SIMT path's
 # ALU roofline; no measured figure exists for it)
 FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12

@@ -96,7 +96,7 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 7
+#define GQA_ABI_VERSION 8
 
 typedef int32_t gqa_status;
 #define GQA_OK 0
@@ -309,8 +309,8 @@ gqa_status gqa_attention_nonpad(const gqa_params *p, const int64_t *nonpad_kv_se
  * (no separate past; k = v = NULL for attention only); q, out, k, v, cos/sin keep the
  * params' dtype; kv_ring returns GQA_ERR_UNSUPPORTED.  Same workspace (gqa_workspace_bytes),
  * status and errors as gqa_attention_decode / gqa_attention_prefill.  Decode with D = Dv =
- * 128 inside the split-KV kernel's envelope runs that kernel (f8 tiles by TMA, widened to f16
- * in shared memory per warp, f16 MMAs); every other shape runs the CUDA-core kernel. */
+ * 128 inside the split-KV kernel's envelope runs that kernel (f8 tiles by TMA, converted to
+ * f16 MMA operands); every other shape runs the CUDA-core kernel. */
 gqa_status gqa_attention_decode_q8(const gqa_params *p, const void *q, const void *k, const void *v,
                                    const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
@@ -320,6 +320,24 @@ gqa_status gqa_attention_prefill_q8(const gqa_params *p, const void *q, const vo
                                     const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
                                     const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                                     uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
+                                    int32_t *dev_status, void *stream);
+
+/* int8 KV cache: the same layouts, scales, arguments, kernels and errors as the f8 calls
+ * above, with each element a two's-complement code in [-128, 127] whose stored value is
+ * code * scale.  The pages define no integer format either; this is the plainest reading,
+ * the ONNX QuantizeLinear convention with a zero point of 0: the step's rows are appended
+ * as round(fp32(x) / scale), ties to even, saturating at -128 and 127 (infinities too), and
+ * NaN, which that convention leaves undefined, as 0.  The split-KV kernel converts the codes
+ * to f16 exactly (every int8 value is an f16 value). */
+gqa_status gqa_attention_decode_i8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                   const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                   const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                   int8_t *present_k, int8_t *present_v, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream);
+gqa_status gqa_attention_prefill_i8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                    const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                    int8_t *present_k, int8_t *present_v, void *workspace, size_t workspace_bytes,
                                     int32_t *dev_status, void *stream);
 
 /* Static description of a status code. */

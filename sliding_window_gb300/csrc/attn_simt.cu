@@ -35,13 +35,14 @@ struct SimtArgs {
   const void *mask;
   int mask_kind, mask_keys;
   long long msb, msh, msi;
-  const float *k_scale, *v_scale;  // f8 cache: one scale per kv head (Q8 kernels)
+  const float *k_scale, *v_scale;  // quantized cache: one scale per kv head (Q8 kernels)
 };
 
 // MASKED: a mask is given (compiled out otherwise); SAMEV: Dv == D (the common case keeps
-// one load per element of both tiles and no V-width arithmetic); Q8: the caches hold E4M3
-// codes, the K scale joins the score scale and the V scale the output
-template <typename T, bool MASKED, bool SAMEV, bool Q8>
+// one load per element of both tiles and no V-width arithmetic); Q8: the caches hold
+// one-byte codes (E4M3, or int8 when I8), the K scale joins the score scale and the V scale
+// the output
+template <typename T, bool MASKED, bool SAMEV, bool Q8, bool I8 = false>
 __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
   extern __shared__ float sm[];
   const int D = a.D, Dv = SAMEV ? a.D : a.Dv, Dw = SAMEV ? D : (D > Dv ? D : Dv);
@@ -99,8 +100,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
       const int j = idx / Dw, d = idx % Dw;
       const bool in = kt + j < hi;
       if (Q8) {
-        if (SAMEV || d < D) ks[j * (D + 1) + d] = in ? e4m3_to_f32(kc8[(size_t)(kt + j) * D + d]) : 0.f;
-        if (SAMEV || d < Dv) vs[j * Dv + d] = in ? e4m3_to_f32(vc8[(size_t)(kt + j) * Dv + d]) : 0.f;
+        if (SAMEV || d < D) ks[j * (D + 1) + d] = in ? code_to_f32<I8>(kc8[(size_t)(kt + j) * D + d]) : 0.f;
+        if (SAMEV || d < Dv) vs[j * Dv + d] = in ? code_to_f32<I8>(vc8[(size_t)(kt + j) * Dv + d]) : 0.f;
       } else {
         if (SAMEV || d < D) ks[j * (D + 1) + d] = in ? to_f32(kc[(size_t)(kt + j) * D + d]) : 0.f;
         if (SAMEV || d < Dv) vs[j * Dv + d] = in ? to_f32(vc[(size_t)(kt + j) * Dv + d]) : 0.f;
@@ -217,7 +218,8 @@ template <typename T> gqa_status launch_t(const Call &c) {
   dim3 grid((p.q_len + kRows - 1) / kRows, p.q_heads, p.batch);
   const bool masked = c.mask != nullptr, samev = c.Dv == D;
   if (masked && c.q8) return GQA_ERR_UNSUPPORTED;
-  auto kern = c.q8 ? (samev ? attn_simt_kernel<T, false, true, true> : attn_simt_kernel<T, false, false, true>)
+  auto kern = c.q8 == 2 ? (samev ? attn_simt_kernel<T, false, true, true, true> : attn_simt_kernel<T, false, false, true, true>)
+              : c.q8 ? (samev ? attn_simt_kernel<T, false, true, true> : attn_simt_kernel<T, false, false, true>)
               : masked ? (samev ? attn_simt_kernel<T, true, true, false> : attn_simt_kernel<T, true, false, false>)
                        : (samev ? attn_simt_kernel<T, false, true, false> : attn_simt_kernel<T, false, false, false>);
   kern<<<grid, 128, smem, c.stream>>>(a);

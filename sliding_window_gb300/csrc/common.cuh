@@ -53,6 +53,55 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
   return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
+// int8 codes of a quantized KV cache: to a code, round half to even and saturate at -128
+// and 127 (infinities too), NaN to 0; from a code, exact.  The pair conversion biases each
+// code by 128 (its sign bit flipped) and places it in the low byte of an f16 whose high
+// byte is 0x64, i.e. 1024 + code + 128, then subtracts 1152 (0x6480): both steps are exact.
+__device__ __forceinline__ uint8_t f32_to_s8(float x) {
+  int r;
+  asm("cvt.rni.sat.s32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  r = min(max(r, -128), 127);
+  return isnan(x) ? (uint8_t)0 : (uint8_t)(r & 0xFF);
+}
+__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint16_t codes) {
+  const uint32_t w = __byte_perm((uint32_t)codes ^ 0x8080u, 0x64646464u, 0x5140);
+  uint32_t r;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0x64806480u));
+  return r;
+}
+__device__ __forceinline__ float s8_to_f32(uint8_t c) { return (float)(int8_t)c; }
+
+// one-byte cache codes: E4M3, or int8 when I8
+template <bool I8> __device__ __forceinline__ uint8_t f32_to_code(float x) {
+  if constexpr (I8) return f32_to_s8(x);
+  else return f32_to_e4m3(x);
+}
+template <bool I8> __device__ __forceinline__ uint32_t codes2_to_f16x2(uint16_t codes) {
+  if constexpr (I8) return s8x2_to_f16x2(codes);
+  else return e4m3x2_to_f16x2(codes);
+}
+// The four codes of w as two f16x2 words: PAIRS 0 takes bytes (0, 1) into lo and (2, 3)
+// into hi; PAIRS 1 takes bytes (0, 2) into lo and (1, 3) into hi (lower byte, lower half).
+// int8: one bias for the four codes, then one byte permute and one subtraction per pair.
+template <bool I8, int PAIRS>
+__device__ __forceinline__ void codes4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  if constexpr (I8) {
+    const uint32_t x = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(x, 0x64646464u, PAIRS ? 0x4240 : 0x4140);
+    const uint32_t b = __byte_perm(x, 0x64646464u, PAIRS ? 0x4341 : 0x4342);
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+  } else {
+    const uint32_t x = PAIRS ? __byte_perm(w, 0, 0x3120) : w;
+    lo = e4m3x2_to_f16x2((uint16_t)(x & 0xFFFFu));
+    hi = e4m3x2_to_f16x2((uint16_t)(x >> 16));
+  }
+}
+template <bool I8> __device__ __forceinline__ float code_to_f32(uint8_t c) {
+  if constexpr (I8) return s8_to_f32(c);
+  else return e4m3_to_f32(c);
+}
+
 // Per-sequence validity shared by every kernel: the same rule decides what is appended
 // and which outputs are zeroed.  Returns GQA_DEV_* bits (0 = valid).
 __device__ __forceinline__ int sequence_status(int past, int curr, int cap_present, int cap_past,

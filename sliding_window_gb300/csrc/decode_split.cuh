@@ -155,12 +155,13 @@ __device__ __forceinline__ void rotate8(const T *x1p, const T *x2p, const T *cp,
   }
 }
 
-// Eight values of the dtype as eight E4M3 codes of x / scale (fp32 division), one 8-byte word.
-template <typename T> __device__ __forceinline__ uint2 codes8(const uint4 &x, float scale) {
+// Eight values of the dtype as eight codes (E4M3, or int8 when I8) of x / scale (fp32
+// division), one 8-byte word.
+template <typename T, bool I8> __device__ __forceinline__ uint2 codes8(const uint4 &x, float scale) {
   const T *e = reinterpret_cast<const T *>(&x);
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j >> 2] |= (uint32_t)f32_to_e4m3(__fdiv_rn(to_f32(e[j]), scale)) << (8 * (j & 3));
+  for (int j = 0; j < 8; ++j) w[j >> 2] |= (uint32_t)f32_to_code<I8>(__fdiv_rn(to_f32(e[j]), scale)) << (8 * (j & 3));
   return make_uint2(w[0], w[1]);
 }
 
@@ -180,11 +181,11 @@ template <typename T> __device__ __forceinline__ uint4 to_half8(const uint4 &x) 
 // Sixteen E4M3 codes (one 16-byte chunk) as sixteen f16 values, two 16-byte chunks: one pair
 // conversion per two neighbouring codes (the low byte of the pair becomes the low half, as
 // the f16 pair layout of a 16-bit tile wants; the lane order was checked on the GPU).
-__device__ __forceinline__ void widen16(const uint4 &codes, uint4 &lo, uint4 &hi) {
+template <bool I8> __device__ __forceinline__ void widen16(const uint4 &codes, uint4 &lo, uint4 &hi) {
   const uint32_t in[4] = {codes.x, codes.y, codes.z, codes.w};
   uint32_t out[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) out[j] = e4m3x2_to_f16x2((uint16_t)(in[j >> 1] >> (16 * (j & 1))));
+  for (int j = 0; j < 4; ++j) codes4_to_f16x2<I8, 0>(in[j], out[2 * j], out[2 * j + 1]);
   lo = make_uint4(out[0], out[1], out[2], out[3]);
   hi = make_uint4(out[4], out[5], out[6], out[7]);
 }
@@ -194,7 +195,7 @@ __device__ __forceinline__ void widen16(const uint4 &codes, uint4 &lo, uint4 &hi
 // generic-proxy stores visible to TMA reads.
 // `staged` (shared memory, or null): the rows as [curr][D + DV] copied in at the kernel's
 // start, read instead of k and v.
-template <typename T, int D, int DV, bool Q8 = false>
+template <typename T, int D, int DV, bool Q8 = false, bool I8 = false>
 __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, int past, int r0, int r1, int lane,
                                             const uint8_t *staged = nullptr) {
   const T *kin = reinterpret_cast<const T *>(a.k), *vin = reinterpret_cast<const T *>(a.v);
@@ -224,11 +225,11 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
           rotate8<T>(krow + c, krow + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c, y1,
                      y2);
         const float sc = a.k_scale[h];
-        *reinterpret_cast<uint2 *>(p8 + dst + c) = codes8<T>(y1, sc);
-        *reinterpret_cast<uint2 *>(p8 + dst + D / 2 + c) = codes8<T>(y2, sc);
+        *reinterpret_cast<uint2 *>(p8 + dst + c) = codes8<T, I8>(y1, sc);
+        *reinterpret_cast<uint2 *>(p8 + dst + D / 2 + c) = codes8<T, I8>(y2, sc);
       } else {
         *reinterpret_cast<uint2 *>(p8 + row * DV + c) =
-            codes8<T>(*reinterpret_cast<const uint4 *>(vrow + c), a.v_scale[h]);
+            codes8<T, I8>(*reinterpret_cast<const uint4 *>(vrow + c), a.v_scale[h]);
       }
     } else if (isk) {
       const size_t dst = row * D;
@@ -259,7 +260,8 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
 // O^T += V^T P^T, with the warp's 16 keys (then 16 head dims of V) as the MMA's M and the
 // rows as its N of 8: half the MMAs of the 16-row form, and the Q fragments stay in
 // registers for the whole chunk.
-template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false, bool TR = false>
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false, bool TR = false,
+          bool I8 = false>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         DecodeArgs a) {
@@ -424,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (warp == 0) cp_async_wait_all();
         __syncwarp();
       }
-      append_rows<T, D, DV, Q8>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane,
+      append_rows<T, D, DV, Q8, I8>(a, b, hkv, past, max(past, k0), min(total, k0 + KT), lane,
                                 staged ? newrows : nullptr);
     }
     if (lane == 0) {
@@ -619,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int c = (lane & 1) * 4 + cc;  // codes [16c, 16c + 16) of the row
         const int e0 = 2 * c, e1 = 2 * c + 1;  // their f16 chunks
         uint4 lo, hi;
-        widen16(*reinterpret_cast<const uint4 *>(v8 + r * 128 + ((c ^ (r & 7)) << 4)), lo, hi);
+        widen16<I8>(*reinterpret_cast<const uint4 *>(v8 + r * 128 + ((c ^ (r & 7)) << 4)), lo, hi);
         *reinterpret_cast<uint4 *>(vc + (e0 >> 3) * (KT * 128) + sw128(r, e0 & 7)) = lo;
         *reinterpret_cast<uint4 *>(vc + (e1 >> 3) * (KT * 128) + sw128(r, e1 & 7)) = hi;
       }
@@ -644,10 +646,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             ldsm_x4(ks_u32 + krow * 128 + ((kch ^ (krow & 7)) << 4), kc[0], kc[1], kc[2], kc[3]);
           }
           const uint32_t w0 = kc[2 * (ks & 1)], w1 = kc[2 * (ks & 1) + 1];
-          af[0] = e4m3x2_to_f16x2((uint16_t)(w0 & 0xFFFFu));
-          af[2] = e4m3x2_to_f16x2((uint16_t)(w0 >> 16));
-          af[1] = e4m3x2_to_f16x2((uint16_t)(w1 & 0xFFFFu));
-          af[3] = e4m3x2_to_f16x2((uint16_t)(w1 >> 16));
+          codes4_to_f16x2<I8, 0>(w0, af[0], af[2]);
+          codes4_to_f16x2<I8, 0>(w1, af[1], af[3]);
         } else {
           const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
           const int kch = 2 * ks + ((lane >> 3) & 1);
@@ -727,12 +727,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           ldsm_x4_t(vc_u32 + vrow * 128 + ((vch ^ (vrow & 7)) << 4), w[0], w[1], w[2], w[3]);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t x0 = __byte_perm(w[2 * h], 0, 0x3120), x1 = __byte_perm(w[2 * h + 1], 0, 0x3120);
             uint32_t af[4];
-            af[0] = e4m3x2_to_f16x2((uint16_t)(x0 & 0xFFFFu));
-            af[1] = e4m3x2_to_f16x2((uint16_t)(x0 >> 16));
-            af[2] = e4m3x2_to_f16x2((uint16_t)(x1 & 0xFFFFu));
-            af[3] = e4m3x2_to_f16x2((uint16_t)(x1 >> 16));
+            codes4_to_f16x2<I8, 1>(w[2 * h], af[0], af[1]);
+            codes4_to_f16x2<I8, 1>(w[2 * h + 1], af[2], af[3]);
             M::run(acct[dm + h], af, pb0, pb1);
           }
         }
@@ -766,10 +763,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int r0 = 16 * warp + (lane >> 2), o = 2 * (lane & 3);
           const uint8_t *c0 = k8 + r0 * 128 + ((ks ^ (r0 & 7)) << 4) + o;
           const uint8_t *c1 = c0 + 8 * 128;  // row r0 + 8: the same swizzle phase
-          kb0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0));
-          kb1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c0 + 8));
-          kb2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1));
-          kb3 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(c1 + 8));
+          kb0 = codes2_to_f16x2<I8>(*reinterpret_cast<const uint16_t *>(c0));
+          kb1 = codes2_to_f16x2<I8>(*reinterpret_cast<const uint16_t *>(c0 + 8));
+          kb2 = codes2_to_f16x2<I8>(*reinterpret_cast<const uint16_t *>(c1));
+          kb3 = codes2_to_f16x2<I8>(*reinterpret_cast<const uint16_t *>(c1 + 8));
         } else {
           const int krow = 16 * warp + ((lane >> 4) << 3) + (lane & 7);
           const int kch = 2 * ks + ((lane >> 3) & 1);
@@ -1240,7 +1237,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false, bool TR = false>
+template <typename T, int D, int DV, int MT, int NST, bool CL, bool MK, bool Q8 = false, bool TR = false,
+          bool I8 = false>
 gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   using L = Smem<D, DV, MT, NST, Q8>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
@@ -1256,7 +1254,7 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
     if (!encode_kv_tile_map(&tk, c.present_k, D, rows, outer, KT, 2)) return GQA_ERR_CUDA;
     if (!encode_kv_tile_map(&tv, c.present_v, DV, rows, outer, KT, 2)) return GQA_ERR_CUDA;
   }
-  auto kern = decode_split_kernel<T, D, DV, MT, NST, CL, MK, Q8, TR>;
+  auto kern = decode_split_kernel<T, D, DV, MT, NST, CL, MK, Q8, TR, I8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) != cudaSuccess)
     return GQA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -1280,10 +1278,10 @@ gqa_status launch_cfg(const Call &c, const DecodePlan &dp, const DecodeArgs &a) 
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-template <typename T, bool CL, bool MK, bool MIXED, bool Q8>
+template <typename T, bool CL, bool MK, bool MIXED, bool Q8, bool I8>
 gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a);
 
-template <typename T, bool MK, bool MIXED, bool Q8 = false>
+template <typename T, bool MK, bool MIXED, bool Q8 = false, bool I8 = false>
 gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   const gqa_params &p = c.p;
   DecodeArgs a;
@@ -1339,21 +1337,21 @@ gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   a.v_scale = c.v_scale;
   a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitLimitCycles;
   a.stall = c.stall;
-  if (dp.cluster) return dispatch<T, true, MK, MIXED, Q8>(c, dp, a);
-  return dispatch<T, false, MK, MIXED, Q8>(c, dp, a);
+  if (dp.cluster) return dispatch<T, true, MK, MIXED, Q8, I8>(c, dp, a);
+  return dispatch<T, false, MK, MIXED, Q8, I8>(c, dp, a);
 }
 
 // (D, DV, MT, NST): equal head dims (MIXED false; at D = 128 three 32 KB stages, two CTAs per
 // SM) or V head dim != Q/K head dim (MIXED true, up to 32 query rows per group; four stages
 // of 24 KB)
-template <typename T, bool CL, bool MK, bool MIXED, bool Q8>
+template <typename T, bool CL, bool MK, bool MIXED, bool Q8, bool I8>
 gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
   const int D = c.p.head_dim, DV = c.Dv;
   if constexpr (Q8) {  // f8 cache: D = Dv = 128, five 16 KB stages and a 16 KB f16 V tile
     if (D == 128 && DV == 128 && !MK && !MIXED) {
-      if (dp.mtiles == 1 && dp.rows <= 8) return launch_cfg<T, 128, 128, 1, 5, CL, false, true, true>(c, dp, a);
-      if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 5, CL, false, true>(c, dp, a);
-      if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 5, CL, false, true>(c, dp, a);
+      if (dp.mtiles == 1 && dp.rows <= 8) return launch_cfg<T, 128, 128, 1, 5, CL, false, true, true, I8>(c, dp, a);
+      if (dp.mtiles == 1) return launch_cfg<T, 128, 128, 1, 5, CL, false, true, false, I8>(c, dp, a);
+      if (dp.mtiles == 2) return launch_cfg<T, 128, 128, 2, 5, CL, false, true, false, I8>(c, dp, a);
     }
   } else if constexpr (!MIXED) {
     if (D == 128 && DV == 128) {
@@ -1391,11 +1389,11 @@ gqa_status dispatch(const Call &c, const DecodePlan &dp, const DecodeArgs &a) {
 
 // The decode launch for one dtype switch; each .cu file instantiates one (MK, MIXED) pair
 // (masked or not, equal or different head dims), so the sets compile in parallel.
-template <bool MK, bool MIXED, bool Q8 = false>
+template <bool MK, bool MIXED, bool Q8 = false, bool I8 = false>
 gqa_status launch_decode_split_impl(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   switch (c.p.dtype) {
-    case GQA_F16: return launch_t<__half, MK, MIXED, Q8>(c, dp, wl);
-    case GQA_BF16: return launch_t<__nv_bfloat16, MK, MIXED, Q8>(c, dp, wl);
+    case GQA_F16: return launch_t<__half, MK, MIXED, Q8, I8>(c, dp, wl);
+    case GQA_BF16: return launch_t<__nv_bfloat16, MK, MIXED, Q8, I8>(c, dp, wl);
   }
   return GQA_ERR_UNSUPPORTED;
 }

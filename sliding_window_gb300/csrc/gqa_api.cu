@@ -346,10 +346,10 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
   return launch_prefill_tc(c);
 }
 
-// f8 (E4M3) cache: the step's K/V quantized on append, attention over code * scale.  The
-// split decode kernel takes D = Dv = 128 shapes in its envelope; everything else runs the
-// RoPE/append kernel and the CUDA-core kernel.
-gqa_status run_attention_q8(Mode mode, const gqa_params *p, const void *q, const void *k, const void *v,
+// Quantized cache (fmt 1: E4M3 codes, fmt 2: int8 codes): the step's K/V quantized on
+// append, attention over code * scale.  The split decode kernel takes D = Dv = 128 shapes in
+// its envelope; everything else runs the RoPE/append kernel and the CUDA-core kernel.
+gqa_status run_attention_q8(Mode mode, int fmt, const gqa_params *p, const void *q, const void *k, const void *v,
                             const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
                             const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                             uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
@@ -362,7 +362,7 @@ gqa_status run_attention_q8(Mode mode, const gqa_params *p, const void *q, const
   if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
     return GQA_ERR_INVALID_ARG;
   if (!out || !aligned16(out)) return GQA_ERR_INVALID_ARG;
-  c.q8 = 1;
+  c.q8 = fmt;
   c.k_scale = k_scale;
   c.v_scale = v_scale;
   const bool rotate = c.append && p->do_rotary;
@@ -373,7 +373,7 @@ gqa_status run_attention_q8(Mode mode, const gqa_params *p, const void *q, const
   if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return GQA_ERR_WORKSPACE;
   c.ws = static_cast<char *>(workspace);
   c.ws_bytes = workspace_bytes;
-  if (fused) return launch_decode_split_q8(c, dp, wl);
+  if (fused) return fmt == 2 ? launch_decode_split_i8(c, dp, wl) : launch_decode_split_q8(c, dp, wl);
   if (c.append) {
     c.q_rot = rotate ? c.ws + wl.q_rot_off : nullptr;
     s = launch_rope_append(c);
@@ -448,8 +448,8 @@ gqa_status gqa_attention_decode_q8(const gqa_params *p, const void *q, const voi
                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                                    uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
                                    int32_t *dev_status, void *stream) {
-  return gqa::run_attention_q8(gqa::kDecode, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale,
-                               out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
+  return gqa::run_attention_q8(gqa::kDecode, 1, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
+                               v_scale, out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
 
 gqa_status gqa_attention_prefill_q8(const gqa_params *p, const void *q, const void *k, const void *v,
@@ -457,8 +457,28 @@ gqa_status gqa_attention_prefill_q8(const gqa_params *p, const void *q, const vo
                                     const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                                     uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
                                     int32_t *dev_status, void *stream) {
-  return gqa::run_attention_q8(gqa::kPrefill, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
+  return gqa::run_attention_q8(gqa::kPrefill, 1, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
                                v_scale, out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_attention_decode_i8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                   const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                   const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                   int8_t *present_k, int8_t *present_v, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream) {
+  return gqa::run_attention_q8(gqa::kDecode, 2, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
+                               v_scale, out, reinterpret_cast<uint8_t *>(present_k),
+                               reinterpret_cast<uint8_t *>(present_v), workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_attention_prefill_i8(const gqa_params *p, const void *q, const void *k, const void *v,
+                                    const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
+                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
+                                    int8_t *present_k, int8_t *present_v, void *workspace, size_t workspace_bytes,
+                                    int32_t *dev_status, void *stream) {
+  return gqa::run_attention_q8(gqa::kPrefill, 2, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
+                               v_scale, out, reinterpret_cast<uint8_t *>(present_k),
+                               reinterpret_cast<uint8_t *>(present_v), workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -39,7 +39,7 @@ struct Call {
   int mask_kind = 0, mask_keys = 0;
   long long mask_sb = 0, mask_sh = 0, mask_si = 0;
   // f8 cache: present_k/v hold E4M3 codes; the stored value is code * scale of the kv head
-  int q8 = 0;
+  int q8 = 0;  // one-byte cache codes: 1 E4M3, 2 int8
   const float *k_scale = nullptr, *v_scale = nullptr;
   int32_t *status = nullptr;
   // failure-path test hook (gqa_test_stall_waits): the limit of the kernels' pipeline waits
@@ -109,6 +109,7 @@ gqa_status launch_decode_split(const Call &c, const DecodePlan &dp, const WsLayo
 gqa_status launch_decode_split_masked(const Call &c, const DecodePlan &dp, const WsLayout &wl);
 gqa_status launch_decode_split_vdim(const Call &c, const DecodePlan &dp, const WsLayout &wl);  // Dv != D
 gqa_status launch_decode_split_q8(const Call &c, const DecodePlan &dp, const WsLayout &wl);    // f8 cache, D = Dv = 128
+gqa_status launch_decode_split_i8(const Call &c, const DecodePlan &dp, const WsLayout &wl);    // int8 cache, D = Dv = 128
 gqa_status launch_prefill_tc(const Call &c);
 gqa_status launch_prefill_tc_masked(const Call &c);  // c.mask set: kind 1 or 2
 gqa_status launch_prefill_tc_vdim(const Call &c);    // Dv != D, no mask

@@ -57,19 +57,20 @@ struct RopeArgs {
   // page of positions [64n, 64n + 64); the pages of the step's band must all exist
   const int32_t *table;
   int max_pages, num_pages, window;
-  // f8 cache: present_k/v hold E4M3 codes of x / scale (fp32 division), one scale per kv head
+  // quantized cache: present_k/v hold one-byte codes of x / scale (fp32 division), one scale
+  // per kv head: E4M3 when q8 == 1, int8 when q8 == 2
   int q8;
   const float *k_scale, *v_scale;
 };
 
 // N consecutive codes of x[e] / scale, stored as one N-byte word
-template <typename T, int N> __device__ __forceinline__ void store_codes(uint8_t *dst, const T *x, float scale) {
+template <typename T, int N, bool I8> __device__ __forceinline__ void store_codes(uint8_t *dst, const T *x, float scale) {
   uint32_t w[N / 4];
 #pragma unroll
   for (int j = 0; j < N / 4; ++j) {
     w[j] = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) w[j] |= (uint32_t)f32_to_e4m3(__fdiv_rn(to_f32(x[4 * j + e]), scale)) << (8 * e);
+    for (int e = 0; e < 4; ++e) w[j] |= (uint32_t)f32_to_code<I8>(__fdiv_rn(to_f32(x[4 * j + e]), scale)) << (8 * e);
   }
   if constexpr (N == 8)
     *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
@@ -122,8 +123,11 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
       const size_t row = cache_row(h);
       if (a.q8) {
         const uint4 x = *reinterpret_cast<const uint4 *>(src + c);
-        store_codes<T, N>(reinterpret_cast<uint8_t *>(a.present_v) + row * a.Dv + c, reinterpret_cast<const T *>(&x),
-                          a.v_scale[h]);
+        uint8_t *v8 = reinterpret_cast<uint8_t *>(a.present_v) + row * a.Dv + c;
+        if (a.q8 == 2)
+          store_codes<T, N, true>(v8, reinterpret_cast<const T *>(&x), a.v_scale[h]);
+        else
+          store_codes<T, N, false>(v8, reinterpret_cast<const T *>(&x), a.v_scale[h]);
         continue;
       }
       T *dst = reinterpret_cast<T *>(a.present_v) + row * a.Dv;
@@ -153,8 +157,13 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
           y2 = *reinterpret_cast<const uint4 *>(src + half + c);
         }
         uint8_t *k8 = reinterpret_cast<uint8_t *>(a.present_k) + row * a.D;
-        store_codes<T, N>(k8 + c, p1, a.k_scale[h]);
-        store_codes<T, N>(k8 + half + c, p2, a.k_scale[h]);
+        if (a.q8 == 2) {
+          store_codes<T, N, true>(k8 + c, p1, a.k_scale[h]);
+          store_codes<T, N, true>(k8 + half + c, p2, a.k_scale[h]);
+        } else {
+          store_codes<T, N, false>(k8 + c, p1, a.k_scale[h]);
+          store_codes<T, N, false>(k8 + half + c, p2, a.k_scale[h]);
+        }
         continue;
       }
       dst = reinterpret_cast<T *>(a.present_k) + row * a.D;

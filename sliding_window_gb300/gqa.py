@@ -35,7 +35,7 @@ EXPORTED = ["gqa_workspace_bytes", "gqa_attention_prefill", "gqa_attention_decod
             "gqa_status_string", "gqa_abi_version", "gqa_attention_decode_noalloc", "gqa_attention_decode_paged",
             "gqa_attention_decode_masked", "gqa_attention_prefill_masked", "gqa_attention_decode_q8",
             "gqa_attention_prefill_q8", "gqa_test_stall_waits", "gqa_attention_nonpad",
-            "gqa_attention_prefill_paged"]
+            "gqa_attention_prefill_paged", "gqa_attention_decode_i8", "gqa_attention_prefill_i8"]
 MASK_KEEP, MASK_ADD = 1, 2
 PAGE = 64  # positions per page of a paged cache
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GQA_NOALLOC_SCRATCH_BYTES
@@ -98,7 +98,8 @@ def _load():
     lib.gqa_attention_decode_masked.restype = i32
     lib.gqa_attention_prefill_masked.argtypes = [pp, ctypes.POINTER(GqaMask)] + [vp] * 13 + [sz, vp, vp]
     lib.gqa_attention_prefill_masked.restype = i32
-    for name in ("gqa_attention_decode_q8", "gqa_attention_prefill_q8"):
+    for name in ("gqa_attention_decode_q8", "gqa_attention_prefill_q8", "gqa_attention_decode_i8",
+                 "gqa_attention_prefill_i8"):
         getattr(lib, name).argtypes = [pp] + [vp] * 13 + [sz, vp, vp]
         getattr(lib, name).restype = i32
     lib.gqa_status_string.argtypes = [i32]
@@ -228,6 +229,20 @@ def gqa_attention_prefill_q8(p, q, k, v, seqlens_k, cos_cache, sin_cache, head_s
                              present_k8, present_v8, workspace, dev_status, stream=None) -> int:
     """Prefill over an f8 (E4M3) cache with per-kv-head scales (see include/gqa.h)."""
     return _q8("gqa_attention_prefill_q8", p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale,
+               out, present_k8, present_v8, workspace, dev_status, stream)
+
+
+def gqa_attention_decode_i8(p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale, out,
+                            present_k8, present_v8, workspace, dev_status, stream=None) -> int:
+    """Decode over an int8 cache with per-kv-head scales (see include/gqa.h)."""
+    return _q8("gqa_attention_decode_i8", p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale,
+               out, present_k8, present_v8, workspace, dev_status, stream)
+
+
+def gqa_attention_prefill_i8(p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale, out,
+                             present_k8, present_v8, workspace, dev_status, stream=None) -> int:
+    """Prefill over an int8 cache with per-kv-head scales (see include/gqa.h)."""
+    return _q8("gqa_attention_prefill_i8", p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale, v_scale,
                out, present_k8, present_v8, workspace, dev_status, stream)
 
 

@@ -50,7 +50,7 @@ class Workload:
     kv_paged: int = 0       # 1: the cache is a shared pool of 64-position pages behind a block table
     mask: str = ""          # "add": an additive attention bias [B, 1, S, cap] of the dtype, N(0,1)
     v_head_dim: int = 0     # Dv; 0: the same as head_dim
-    kv_q8: int = 0          # 1: the cache holds f8 E4M3 codes with one scale per kv head for K and V
+    kv_q8: int = 0          # the cache holds one-byte codes with one scale per kv head for K and V: 1 f8 E4M3, 2 int8
 
     @property
     def layers(self) -> int:
@@ -96,6 +96,9 @@ WORKLOADS = {
         # the windowed decode over an f8 cache (one byte per cached element)
         Workload("decode_window_q8_bf16", 9, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
                  windows=(1024,), kv_q8=1),
+        # the same with an int8 cache
+        Workload("decode_window_i8_bf16", 10, "decode", "bf16", 8, 32, 8, 128, 1, 4096, 512, 4095,
+                 windows=(1024,), kv_q8=2),
         # the long prompt with a dense additive attention bias, broadcast over the heads
         Workload("prefill_bias_bf16", 7, "prefill", "bf16", 2, 64, 8, 128, 8192, 8192, 0, 0,
                  windows=(4096,), softcap=50.0, head_sink=True, mask="add"),
@@ -208,13 +211,17 @@ def make_case(w: Workload, layer: int = 0, device="cpu", seed_offset: int = 0, g
     elif w.mask:
         raise ValueError(w.mask)
     if w.kv_q8:
-        # f8 cache: the past as random finite E4M3 codes (sign, exponent field 1..11, fraction)
-        # drawn directly as bytes, scales U[0.01, 0.02] per kv head; q/k/v stay in the dtype
+        # quantized cache: the past as random codes drawn directly as bytes (f8: finite E4M3
+        # codes, sign, exponent field 1..11, fraction; int8: uniform over [-127, 127]), scales
+        # U[0.01, 0.02] per kv head; q/k/v stay in the dtype
         qg = torch.Generator(device=dev)
         qg.manual_seed(7000 + w.index + 104729 * layer + 7919 * seed_offset)
         Dv = w.v_head_dim or D
 
         def codes(*shape):
+            if w.kv_q8 == 2:
+                return torch.randint(-127, 128, shape, generator=qg, device=dev, dtype=torch.int32).to(
+                    torch.int8).view(torch.uint8)
             sign = torch.randint(0, 2, shape, generator=qg, device=dev, dtype=torch.int32) << 7
             expo = torch.randint(1, 12, shape, generator=qg, device=dev, dtype=torch.int32) << 3
             frac = torch.randint(0, 8, shape, generator=qg, device=dev, dtype=torch.int32)

@@ -64,7 +64,7 @@ def test_mask_struct_layout_matches_header(g, tmp_path):
 
 
 def test_version_and_status_strings(g):
-    assert g.gqa_abi_version() == 7
+    assert g.gqa_abi_version() == 8
     for s in range(6):
         assert g.gqa_status_string(s) and g.gqa_status_string(s) != "unknown status"
     assert g.gqa_status_string(99) == "unknown status"
@@ -286,7 +286,8 @@ def call_q8(g, p, fn="gqa_attention_decode_q8", **ptrs):
     return getattr(g.lib, fn)(ctypes.byref(p), *a, 0, None, None)
 
 
-@pytest.mark.parametrize("fn", ["gqa_attention_decode_q8", "gqa_attention_prefill_q8"])
+@pytest.mark.parametrize("fn", ["gqa_attention_decode_q8", "gqa_attention_prefill_q8", "gqa_attention_decode_i8",
+                                "gqa_attention_prefill_i8"])
 @pytest.mark.parametrize("ptrs,code", [
     (dict(k_scale=None), 1), (dict(v_scale=None), 1), (dict(k_scale=FAKE + 2), 1),  # scales: fp32, aligned
     (dict(present_k=FAKE + 8), 1), (dict(out=None), 1), (dict(q=None), 1),
@@ -295,7 +296,8 @@ def test_q8_invalid_arguments(g, fn, ptrs, code):
     assert call_q8(g, good_params(g), fn, **ptrs) == code
 
 
-@pytest.mark.parametrize("fn", ["gqa_attention_decode_q8", "gqa_attention_prefill_q8"])
+@pytest.mark.parametrize("fn", ["gqa_attention_decode_q8", "gqa_attention_prefill_q8", "gqa_attention_decode_i8",
+                                "gqa_attention_prefill_i8"])
 def test_q8_rejects_a_ring(g, fn):
     assert call_q8(g, good_params(g, kv_ring=1, window=1000), fn) == 2
 

@@ -161,11 +161,12 @@ def test_prefill_bias_bf16():
     torch.cuda.empty_cache()
 
 
-def test_decode_window_q8_bf16():
-    """The windowed decode over an f8 cache at full size through gqa_attention_decode_q8:
-    the appended codes bit for bit, sampled rows against the f8 oracle."""
+@pytest.mark.parametrize("name,fmt", [("decode_window_q8_bf16", "e4m3"), ("decode_window_i8_bf16", "int8")])
+def test_decode_window_quantized_cache(name, fmt):
+    """The windowed decode over a quantized cache (f8 or int8) at full size through its
+    entry point: the appended codes bit for bit, sampled rows against the oracle."""
     from sliding_window_gb300 import gqa
-    w = WORKLOADS["decode_window_q8_bf16"]
+    w = WORKLOADS[name]
     c = make_case(w, device="cpu")
     k8, v8 = c.extra["k8"].numpy().copy(), c.extra["v8"].numpy().copy()
     ks, vs = c.extra["k_scale"].numpy(), c.extra["v_scale"].numpy()
@@ -174,17 +175,17 @@ def test_decode_window_q8_bf16():
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device="cuda")
     gk, gv = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
-    gqa.check(gqa.gqa_attention_decode_q8(p, c.q.cuda(), c.k.cuda(), c.v.cuda(), c.seqlens_k.cuda(), None, None,
-                                          None, c.extra["k_scale"].cuda(), c.extra["v_scale"].cuda(), out, gk, gv,
-                                          ws, st), "q8")
+    fn = gqa.gqa_attention_decode_q8 if fmt == "e4m3" else gqa.gqa_attention_decode_i8
+    gqa.check(fn(p, c.q.cuda(), c.k.cuda(), c.v.cuda(), c.seqlens_k.cuda(), None, None, None,
+                 c.extra["k_scale"].cuda(), c.extra["v_scale"].cuda(), out, gk, gv, ws, st), fmt)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     rk, rv = k8.copy(), v8.copy()
     q_rot, s = oracle.rope_append_q8(c.params, storage(c.q), storage(c.k), storage(c.v), rk, rv,
-                                     c.seqlens_k.numpy(), ks, vs)
+                                     c.seqlens_k.numpy(), ks, vs, fmt=fmt)
     assert s == 0
     np.testing.assert_array_equal(gk.cpu().numpy(), rk)
     np.testing.assert_array_equal(gv.cpu().numpy(), rv)
     rows = sample_rows(w)
-    ref = oracle.attention_q8(c.params, q_rot, rk, rv, c.seqlens_k.numpy(), ks, vs, None, rows=rows)
+    ref = oracle.attention_q8(c.params, q_rot, rk, rv, c.seqlens_k.numpy(), ks, vs, None, rows=rows, fmt=fmt)
     assert_close(out_rows(out, c, rows), ref, w.dtype, w.name)
