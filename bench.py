@@ -37,7 +37,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from sliding_window_gb300.inputs import WORKLOADS, draw_seqlens, make_case  # noqa: E402
+from sliding_window_gb300.inputs import MASK_BLOCK, WORKLOADS, block_live, draw_seqlens, make_case  # noqa: E402
 
 METRIC = "attention TFLOP/s (prefill) & KV-read HBM GB/s (decode), % of GB300 roofline"
 L2_BYTES = 129 * 2 ** 20
@@ -83,7 +83,16 @@ def visible_pairs(w, seqlens, window):
         qa = np.arange(past, past + w.q_len, dtype=np.int64)
         hi = qa + 1 if w.causal else np.full_like(qa, past + w.q_len)
         lo = np.zeros_like(qa) if window < 0 else np.maximum(0, qa - window + 1)
-        pairs += int(np.maximum(0, hi - lo).sum())
+        hi = np.maximum(hi, lo)
+        if w.mask == "blocks":
+            # keys of [lo, hi) in key blocks of the query block's parity (the checkerboard)
+            bs = MASK_BLOCK
+            par = (np.arange(w.q_len, dtype=np.int64) // bs) % 2
+            below = lambda x: x // (2 * bs) * bs + np.clip(x % (2 * bs) - bs * par, 0, bs)  # noqa: E731
+            assert block_live(0, 0) and block_live(1, 1) and not block_live(0, 1) and not block_live(1, 0)
+            pairs += int((below(hi) - below(lo)).sum())
+        else:
+            pairs += int((hi - lo).sum())
     return pairs * w.q_heads
 
 
@@ -208,7 +217,7 @@ class Step:
                 c.past_k, c.past_v = c.extra["k8"], c.extra["v8"]
             if w.mask:  # device-resident like the cache (a bias computed or reused on the device)
                 L["mask_t"] = c.extra["mask"]
-                L["mask"] = gqa.mask_from_tensor(L["mask_t"], gqa.MASK_ADD)
+                L["mask"] = gqa.mask_from_tensor(L["mask_t"], gqa.MASK_KEEP if w.mask == "blocks" else gqa.MASK_ADD)
             if w.kv_paged:  # the same rows, moved into a shuffled pool of 64-position pages
                 B, Hkv, cap, D = c.past_k.shape
                 mp = cap // gqa.PAGE
@@ -463,7 +472,9 @@ def kernels_per_layer(w) -> int:
     mtiles = (rows + 15) // 16
     fused = w.mode == "decode" and w.dtype != "f32" and (
         mtiles <= 2 if vdim(w) != w.head_dim else (w.head_dim == 128 and mtiles <= 2) or (w.head_dim == 64 and mtiles <= 4))
-    return 1 if fused else 2
+    if fused:
+        return 1
+    return 3 if w.mask == "blocks" else 2  # a boolean mask adds its block-map kernel
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -633,7 +644,8 @@ class OracleSample:
             q_rot, pk, pv, _ = o.rope_append(L["p"], L["q"], L["k"], L["v"], L["pk"], L["pv"], L["seq"], L["cos"],
                                              L["sin"], present_k=L["pk"], present_v=L["pv"])
             if L["mask"] is not None:
-                o.attention_masked(L["p"], q_rot, pk, pv, L["seq"], L["mask"], "add", L["sink"], rows=L["rows"])
+                o.attention_masked(L["p"], q_rot, pk, pv, L["seq"], L["mask"], "bool" if self.w.mask == "blocks" else "add",
+                                   L["sink"], rows=L["rows"])
                 continue
             o.attention(L["p"], q_rot, pk, pv, L["seq"], L["sink"], rows=L["rows"])
         return self.units
@@ -666,7 +678,7 @@ SUB_WORKLOADS = {"prefill_sink_softcap_bf16": 8, "decode_window_bf16": 1000, "sp
 DEFAULT_STEPS = {"decode_window_bf16": 20000, "specdecode_rotary_f16": 2000, "decode_long_bf16": 200,
                  "prefill_sink_softcap_bf16": 100, "prefill_fp32_tiny": 5000, "decode_window_ring_bf16": 20000,
                  "decode_window_paged_bf16": 20000, "decode_window_vdim_bf16": 20000, "prefill_bias_bf16": 80,
-                 "decode_window_q8_bf16": 20000, "decode_window_i8_bf16": 20000}
+                 "decode_window_q8_bf16": 20000, "decode_window_i8_bf16": 20000, "prefill_blocksparse_bf16": 100}
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (the SIMT path's
 # ALU roofline; no measured figure exists for it)
 FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
@@ -785,7 +797,9 @@ def report(args, r, world, headline):
                    "l2": "rotating buffer sets totalling > 3x L2 (inputs larger than L2)",
                    "tokens_per_s": round(w.batch * w.q_len * steps * world / r["elapsed"], 1),
                    "peaks": src, **({"mask": "additive bias [B, 1, S, cap] %s, device-resident" % w.dtype}
-                                    if w.mask else {}),
+                                    if w.mask == "add" else {}),
+                   **({"mask": "boolean [B, 1, S, cap]: 128 x 128 blocks kept in a checkerboard, device-resident; "
+                               "the FLOP count takes the kept keys only"} if w.mask == "blocks" else {}),
                    **({"batch_override": True} if w.batch != WORKLOADS[w.name].batch else {})},
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": punit,
                      "frac": round(achieved / peak, 4),

@@ -209,6 +209,15 @@ WsLayout workspace_layout(const gqa_params &p, bool need_q_rot) {
     w.tickets_bytes = groups * sizeof(int32_t);
     off = align_up(off + w.tickets_bytes, kAlign);
   }
+  // the block map of a boolean mask on the tensor-core prefill (any call with more than one
+  // query token that the prefill kernel can take): one bit per (b, q head, 128-row query
+  // tile, 16-key chunk of the cache), the largest any mask shape needs
+  const int dv = p.v_head_dim ? p.v_head_dim : p.head_dim;
+  if (p.q_len > 1 && p.dtype != GQA_F32 && dv == p.head_dim && (p.head_dim == 64 || p.head_dim == 128)) {
+    w.blockmap_off = off;
+    w.blockmap_bytes = (size_t)p.batch * p.q_heads * ((p.q_len + 127) / 128) * ((p.cap_present + 511) / 512) * 4;
+    off = align_up(off + w.blockmap_bytes, kAlign);
+  }
   w.total = off;
   return w;
 }
@@ -342,7 +351,15 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
     if (rotate) c.q = c.q_rot;
   }
   if (mode == kDecode || p->dtype == GQA_F32) return launch_attention_simt(c);
-  if (mask) return mask_tma_ok(c) ? launch_prefill_tc_masked(c) : launch_attention_simt(c);
+  if (mask) {
+    if (!mask_tma_ok(c)) return launch_attention_simt(c);
+    // a boolean mask's block map lets the prefill skip the key tiles it removes entirely,
+    // when the workspace has room for it (it is optional)
+    if (c.mask_kind == GQA_MASK_KEEP && wl.blockmap_bytes > 0 && c.ws && aligned16(c.ws) &&
+        workspace_bytes >= wl.blockmap_off + wl.blockmap_bytes)
+      c.blockmap = reinterpret_cast<uint32_t *>(c.ws + wl.blockmap_off);
+    return launch_prefill_tc_masked(c);
+  }
   return launch_prefill_tc(c);
 }
 

@@ -38,6 +38,8 @@ struct Call {
   const void *mask = nullptr;
   int mask_kind = 0, mask_keys = 0;
   long long mask_sb = 0, mask_sh = 0, mask_si = 0;
+  // boolean mask on the tensor-core prefill: room for its block map in the workspace, or null
+  uint32_t *blockmap = nullptr;
   // f8 cache: present_k/v hold E4M3 codes; the stored value is code * scale of the kv head
   int q8 = 0;  // one-byte cache codes: 1 E4M3, 2 int8
   const float *k_scale = nullptr, *v_scale = nullptr;
@@ -72,6 +74,7 @@ struct WsLayout {
   size_t part_acc_off = 0, part_acc_bytes = 0;
   size_t part_ml_off = 0, part_ml_bytes = 0;
   size_t tickets_off = 0, tickets_bytes = 0;
+  size_t blockmap_off = 0, blockmap_bytes = 0;  // a boolean mask's block map (tensor-core prefill)
   size_t total = 0;
 };
 

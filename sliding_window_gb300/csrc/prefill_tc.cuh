@@ -68,7 +68,28 @@ struct PrefillArgs {
   int ring;
   const int32_t *table;
   int max_pages, num_pages;
+  // boolean mask (MK 1): the block map of the mask, or null.  Bit c of word w of row
+  // ((bm * bm_heads + hm) * bm_qtiles + qm) says whether any key of 16-key chunk 32w + c is
+  // kept in the rows of 128-row query tile qm (a broadcast dimension has coordinate 0)
+  const uint32_t *blockmap;
+  int bm_heads, bm_qtiles, bm_words;
 };
+
+// Whether the boolean mask keeps any key of [k0, k0 + 128) in this CTA's query tile for
+// head h0 (or h0 + 1 when `two`): 8 bits of the block map from chunk k0 / 16.
+__device__ __forceinline__ bool tile_kept(const PrefillArgs &a, int b, int h0, bool two, int qt, int k0) {
+  const int c = k0 >> 4, w = c >> 5, sh = c & 31;
+  const int bm = a.mask_bcast_b ? 0 : b, qm = a.mask_bcast_i ? 0 : qt;
+  for (int hh = 0; hh < (two && !a.mask_bcast_h ? 2 : 1); ++hh) {
+    const int hm = a.mask_bcast_h ? 0 : h0 + hh;
+    const uint32_t *row = a.blockmap + (((size_t)bm * a.bm_heads + hm) * a.bm_qtiles + qm) * a.bm_words;
+    uint64_t x = w < a.bm_words ? row[w] : 0u;
+    if (w + 1 < a.bm_words) x |= (uint64_t)row[w + 1] << 32;
+    if ((x >> sh) & 0xFFu) return true;
+  }
+  return false;
+}
+
 
 template <int D, int DV, int MK> struct PSmem {
   static constexpr int kTile = BM * D * 2;    // one Q or K tile
@@ -87,7 +108,10 @@ template <int D, int DV, int MK> struct PSmem {
   static constexpr int kBar = kM + kMaskBufs * kMaskTile;
   static constexpr int kTmemSlot = kBar + 24 * 8;
   static constexpr int kFlag = kTmemSlot + 8;
-  static constexpr int kBytes = kFlag + 8;
+  // MK 1 with a block map: the count and the indices of the key tiles the mask keeps
+  static constexpr int kMaxLive = 508;
+  static constexpr int kLive = kFlag + 8;
+  static constexpr int kBytes = kLive + 4 + kMaxLive * 2;
   // more than half of an SM's shared memory, so a CTA (512 TMEM columns) is always alone
   // on its SM and can never sit blocked in tcgen05.alloc behind another one
   static constexpr int kAlloc = (kBytes + 1024) > 116 * 1024 ? (kBytes + 1024) : 116 * 1024;
@@ -280,7 +304,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the ring's wrap and is two whole pages; the extra keys fall outside the band (masked)
   if (a.ring || a.table) klo &= ~(BN - 1);
   const int khi = a.causal ? min(total, qa_last + 1) : total;
-  const int ntiles = (khi - klo + BN - 1) / BN;  // >= 1: every row sees itself
+  const int ntiles_band = (khi - klo + BN - 1) / BN;  // >= 1: every row sees itself
+  // boolean mask with a block map: only the tiles where the mask keeps a key of this query
+  // tile are streamed, in order (every role walks the same list); otherwise every tile
+  int *nlive = reinterpret_cast<int *>(smem + L::kLive);
+  uint16_t *live = reinterpret_cast<uint16_t *>(smem + L::kLive + 4);
+  const bool skip = MK == 1 && a.blockmap != nullptr && ntiles_band <= L::kMaxLive;
+  if (skip && warp == 0) {
+    int n = 0;
+    for (int t0 = 0; t0 < ntiles_band; t0 += 32) {
+      const int t = t0 + lane;
+      const bool keep = t < ntiles_band && tile_kept(a, b, hA, has_b, qt, klo + t * BN);
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      if (keep) live[n + __popc(m & ((1u << lane) - 1u))] = (uint16_t)t;
+      n += __popc(m);
+    }
+    if (lane == 0) *nlive = n;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i)
@@ -294,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int ntiles = skip ? *nlive : ntiles_band;  // tiles streamed
   // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,256+DV) O_B [384,384+DV); P_X overwrites
   // the first 64 columns of S_X as packed pairs
   int kissued = 0, vissued = 0;      // producer thread: TMA tiles issued
@@ -342,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (int t = 0; t < ntiles; ++t) {
-        const int s = t & 1, k0 = klo + t * BN, sk = t % KST;
+        const int s = t & 1, k0 = klo + (skip ? live[t] : t) * BN, sk = t % KST;
         if (t >= KST && !mbar_wait(&bars[B_KEMPTY0 + sk], ((t / KST) - 1) & 1, abort_flag, a.wait_limit)) break;
         mbar_expect_tx(&bars[B_KFULL0 + sk], L::kTile);
         load_tile(smem + L::kK + sk * L::kTile, &tmk, k0, D, &bars[B_KFULL0 + sk]);
@@ -361,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = (uint32_t)mrows * 128u * (MK >= 2 ? 2u : 1u);
       const int mb = a.mask_bcast_b ? 0 : b, mq = a.mask_bcast_i ? 0 : q0;
       for (int t = 0; t < ntiles; ++t) {
-        const int k0 = klo + t * BN;
+        const int k0 = klo + (skip ? live[t] : t) * BN;
         bool fine = true;
         // MK 1, 2: one buffer per head; MK 3: the shared tile goes to ring slot t % kMaskRing
         for (int h = 0; h < (MK != 3 && has_b ? 2 : 1); ++h) {
@@ -402,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // failure-path test hook: first a wait that nothing completes
     bool ok = !(a.stall && !__all_sync(0xffffffffu, mbar_wait(&bars[B_STALL], 0, abort_flag, a.wait_limit))) &&
-              __all_sync(0xffffffffu, mbar_wait(&bars[B_Q], 0, abort_flag, a.wait_limit)) &&
+              __all_sync(0xffffffffu, mbar_wait(&bars[B_Q], 0, abort_flag, a.wait_limit)) && (MK != 1 || ntiles > 0) &&
               __all_sync(0xffffffffu, mbar_wait(&bars[B_KFULL0], 0, abort_flag, a.wait_limit));
     if (ok) {
       tc_fence_after();
@@ -419,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
     for (int t = 0; ok && t < ntiles; ++t) {
-      const int s = t & 1, k0 = klo + t * BN;
+      const int s = t & 1, k0 = klo + (skip ? live[t] : t) * BN;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_VFULL0 + s], (t >> 1) & 1, abort_flag, a.wait_limit))) break;
       if (k0 + BN > total) {  // stale slots may hold NaN/Inf: zero those V rows
         const int first = max(0, total - k0);
@@ -490,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = a.has_sink ? 1.f : 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      const int k0 = klo + t * BN;
+      const int k0 = klo + (skip ? live[t] : t) * BN;
       const bool edge = !(k0 + BN - 1 < total && (!a.causal || k0 + BN - 1 <= qa_first) &&
                           (a.window < 0 || qa_last - k0 < a.window));
       if (!__all_sync(0xffffffffu, mbar_wait(sfull, t & 1, abort_flag, a.wait_limit))) {
@@ -641,8 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(pfull);
     }
     // epilogue: out = O / l
-    const bool fin = ok && !*abort_flag && mbar_wait(ofull, (ntiles - 1) & 1, abort_flag, a.wait_limit);
-    if (__all_sync(0xffffffffu, fin)) {
+    const bool none = MK == 1 && ntiles == 0;  // the mask keeps no key of this query tile
+    const bool fin = ok && !*abort_flag && (none || mbar_wait(ofull, (ntiles - 1) & 1, abort_flag, a.wait_limit));
+    if (__all_sync(0xffffffffu, fin) && none) {
+      T *orow = out + (((size_t)b * a.curr + q0 + row) * a.Hq + hq) * DV;
+      if (row < nrows)
+        for (int c = 0; c < DV; c += 8) *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
+    } else if (__all_sync(0xffffffffu, fin)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       T *orow = out + (((size_t)b * a.curr + q0 + row) * a.Hq + hq) * DV;
@@ -754,6 +800,10 @@ template <typename T, int MK, bool MIXED> gqa_status launch_t(const Call &c) {
   a.table = c.block_table;
   a.max_pages = c.max_pages;
   a.num_pages = c.num_pages;
+  a.blockmap = MK == 1 ? c.blockmap : nullptr;
+  a.bm_heads = c.mask_sh == 0 ? 1 : p.q_heads;
+  a.bm_qtiles = c.mask_si == 0 ? 1 : (p.q_len + BM - 1) / BM;
+  a.bm_words = (((c.mask_keys < p.cap_present ? c.mask_keys : p.cap_present) + 15) / 16 + 31) / 32;
   const bool sc = p.softcap > 0.f;
   if (sc) {
     a.score_mul = p.scale / p.softcap;

@@ -48,7 +48,8 @@ class Workload:
     garbage_std: float = 10.0
     kv_ring: int = 0        # 1: the cache is a ring of `cap` slots, position p in slot p % cap
     kv_paged: int = 0       # 1: the cache is a shared pool of 64-position pages behind a block table
-    mask: str = ""          # "add": an additive attention bias [B, 1, S, cap] of the dtype, N(0,1)
+    mask: str = ""          # "add": an additive attention bias [B, 1, S, cap] of the dtype, N(0,1);
+                            # "blocks": a block-sparse boolean mask [B, 1, S, cap] (block_live)
     v_head_dim: int = 0     # Dv; 0: the same as head_dim
     kv_q8: int = 0          # the cache holds one-byte codes with one scale per kv head for K and V: 1 f8 E4M3, 2 int8
 
@@ -102,11 +103,22 @@ WORKLOADS = {
         # the long prompt with a dense additive attention bias, broadcast over the heads
         Workload("prefill_bias_bf16", 7, "prefill", "bf16", 2, 64, 8, 128, 8192, 8192, 0, 0,
                  windows=(4096,), softcap=50.0, head_sink=True, mask="add"),
+        # the long prompt with a block-sparse boolean mask: half of the 128 x 128 blocks removed
+        Workload("prefill_blocksparse_bf16", 11, "prefill", "bf16", 2, 64, 8, 128, 8192, 8192, 0, 0,
+                 windows=(4096,), softcap=50.0, head_sink=True, mask="blocks"),
     ]
 }
 
 WORKLOAD_ORDER = ["prefill_fp32_tiny", "decode_window_bf16", "prefill_sink_softcap_bf16",
                   "specdecode_rotary_f16", "decode_long_bf16"]
+
+
+MASK_BLOCK = 128  # rows and keys of one block of the "blocks" mask
+
+
+def block_live(qb, kb):
+    """Whether block (query block qb, key block kb) of the "blocks" mask keeps its keys."""
+    return (qb + kb) % 2 == 0
 
 
 def rope_tables(rope_len: int, head_dim: int, theta: float, dtype: str, device="cpu"):
@@ -208,6 +220,11 @@ def make_case(w: Workload, layer: int = 0, device="cpu", seed_offset: int = 0, g
         for b in range(B):
             m[b].copy_(torch.randn(1, L, cap, generator=mg, device=dev, dtype=torch.float32))
         extra["mask"] = m
+    elif w.mask == "blocks":  # a fixed checkerboard of 128 x 128 blocks, every key of a live block kept
+        qb = torch.arange(L, device=dev) // MASK_BLOCK
+        kb = torch.arange(cap, device=dev) // MASK_BLOCK
+        live = block_live(qb[:, None], kb[None, :]).to(torch.uint8)
+        extra["mask"] = live[None, None].expand(B, 1, L, cap).contiguous()
     elif w.mask:
         raise ValueError(w.mask)
     if w.kv_q8:

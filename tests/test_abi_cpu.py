@@ -265,10 +265,15 @@ def test_workspace_sizes(g):
     S = bound_splits(8, 8, 4096, 1024)
     assert S == 4
     assert ws(batch=8, q_heads=32, kv_heads=8, cap_present=4096, window=1024) == decode_ws(8, 8, 4, 128, S)
-    # more than 32 query rows per group at D=128: the SIMT kernel, no split workspace
-    assert ws(q_heads=64, kv_heads=2, q_len=2, window=-1) == 0
-    # prefill-sized q_len never needs decode partials
-    assert ws(batch=2, q_heads=64, kv_heads=8, q_len=8192, cap_present=8192, window=4096) == 0
+    # more than 32 query rows per group at D=128: the SIMT kernel, no split workspace; with more
+    # than one query token the boolean-mask block map: one bit per (b, q head, 128-row query
+    # tile, 16-key chunk of the cache), 32 chunks a word
+    blockmap = lambda B, Hq, L, cap: B * Hq * -(-L // 128) * -(-cap // 512) * 4
+    assert ws(q_heads=64, kv_heads=2, q_len=2, window=-1) == blockmap(2, 64, 2, 1024)
+    # prefill-sized q_len never needs decode partials, only the block map
+    assert ws(batch=2, q_heads=64, kv_heads=8, q_len=8192, cap_present=8192, window=4096) == blockmap(2, 64, 8192, 8192)
+    assert ws(batch=2, q_heads=64, kv_heads=8, q_len=8192, cap_present=8192, window=4096, dtype="f32") == 0
+    assert ws(batch=2, q_heads=8, kv_heads=2, q_len=300, cap_present=1024, head_dim=128, v_head_dim=64) == 0
 
 
 def test_binding_refuses_host_tensors(g):

@@ -3,11 +3,13 @@ definitions: decode reads every visible K row (D elements) and V row (Dv element
 (b, kv head) once, plus q read, out written and the new K/V read and appended; prefill does
 2·D (scores) + 2·Dv (weighted sum) flops per visible (query, key) pair.  Also the launch
 count the bench claims per layer."""
+import dataclasses
+
 import numpy as np
 import pytest
 
 import bench
-from sliding_window_gb300.inputs import WORKLOADS
+from sliding_window_gb300.inputs import WORKLOADS, make_case
 
 
 def test_decode_bytes_by_hand():
@@ -87,3 +89,21 @@ def test_headline_is_the_largest_single_gpu_workload_and_subrecords_cover_the_re
              "decode_long_bf16"]
     assert bench.HEADLINE == "decode_long_bf16"
     assert set(bench.SUB_WORKLOADS) | {bench.HEADLINE} == set(named)
+
+
+@pytest.mark.parametrize("q_len,cap,window", [(300, 300, -1), (700, 700, 200), (1000, 1000, 4096)])
+def test_block_sparse_pairs_by_brute_force(q_len, cap, window):
+    """The FLOP count of the block-sparse boolean workload counts the keys its mask keeps
+    inside the band: brute force over the mask the input generator builds."""
+    w = WORKLOADS["prefill_blocksparse_bf16"].scaled(batch=1)
+    w = dataclasses.replace(w, q_len=q_len, cap=cap, windows=(window,), q_heads=1, kv_heads=1)
+    c = make_case(w, device="cpu")
+    m = c.extra["mask"][0, 0].numpy().astype(bool)
+    seqs = [np.array([0], dtype=np.int32)]
+    qa = np.arange(q_len)[:, None]
+    k = np.arange(cap)[None, :]
+    band = (k <= qa) & ((window < 0) | (qa - k < window))
+    want = int((band & m).sum()) * 2 * (w.head_dim + w.head_dim)
+    units, kunits, _ = bench.step_work(w, seqs)
+    assert units == pytest.approx(want / 1e12, rel=0, abs=1e-18)
+    assert 0 < (band & m).sum() < band.sum()

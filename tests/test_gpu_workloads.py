@@ -132,22 +132,24 @@ def test_decode_window_paged_bf16():
     assert_close(out_rows(out, c), ref, w.dtype, w.name)
 
 
-def test_prefill_bias_bf16():
-    """The long prompt with a dense additive bias [B, 1, S, S] through the masked prefill
-    entry point (TMA-staged mask): sampled rows (band edges included) against the masked
-    oracle, the appended rows bit for bit."""
+@pytest.mark.parametrize("name,kind", [("prefill_bias_bf16", "add"), ("prefill_blocksparse_bf16", "bool")])
+def test_prefill_masked_workload(name, kind):
+    """The long prompt with a mask [B, 1, S, S] through the masked prefill entry point
+    (TMA-staged mask): a dense additive bias, or a block-sparse boolean mask whose removed
+    128 x 128 blocks the kernel skips through its block map.  Sampled rows (band edges
+    included) against the masked oracle, the appended rows bit for bit."""
     from sliding_window_gb300 import gqa
-    w = WORKLOADS["prefill_bias_bf16"]
+    w = WORKLOADS[name]
     c = make_case(w, device="cuda:0")
     host = make_host(c)
-    mask_host = storage(c.extra["mask"])
+    mask_host = storage(c.extra["mask"]) if kind == "add" else c.extra["mask"].cpu().numpy()
     p = gqa.params_from_dict(c.params)
     out = torch.full_like(c.q, float("nan"))
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = torch.zeros(max(16, gqa.gqa_workspace_bytes(p)), dtype=torch.uint8, device="cuda")
-    m = gqa.mask_from_tensor(c.extra["mask"], gqa.MASK_ADD)
+    m = gqa.mask_from_tensor(c.extra["mask"], gqa.MASK_ADD if kind == "add" else gqa.MASK_KEEP)
     gqa.check(gqa.gqa_attention_prefill_masked(p, m, c.q, c.k, c.v, c.past_k, c.past_v, c.seqlens_k, c.cos, c.sin,
-                                               c.head_sink, out, c.past_k, c.past_v, ws, st), "prefill bias")
+                                               c.head_sink, out, c.past_k, c.past_v, ws, st), name)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     q_rot, pk, pv, s = oracle.rope_append(c.params, host["q"], host["k"], host["v"], host["past_k"],
@@ -156,7 +158,7 @@ def test_prefill_bias_bf16():
     assert s == 0
     np.testing.assert_array_equal(storage(c.past_k[:, :, : w.q_len]), pk[:, :, : w.q_len])
     rows = sample_rows(w)
-    ref = oracle.attention_masked(c.params, q_rot, pk, pv, host["seq"], mask_host, "add", host["sink"], rows=rows)
+    ref = oracle.attention_masked(c.params, q_rot, pk, pv, host["seq"], mask_host, kind, host["sink"], rows=rows)
     assert_close(out_rows(out, c, rows), ref, w.dtype, w.name)
     torch.cuda.empty_cache()
 
