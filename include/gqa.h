@@ -140,8 +140,10 @@ typedef struct gqa_params {
 } gqa_params;
 
 /* Bytes of device workspace that gqa_attention_prefill / gqa_attention_decode need for
- * these params (the larger of the two).  Depends only on the params.  The workspace must
- * be zero-filled before its first use; every call leaves its counters at zero again.
+ * these params (the larger of the two), plus, for params with more than one query token
+ * that the tensor-core prefill can take, room for a boolean mask's block map
+ * (gqa_attention_prefill_masked).  Depends only on the params.  The workspace must be
+ * zero-filled before its first use; every call leaves its counters at zero again.
  * Returns 0 for params that fail validation. */
 size_t gqa_workspace_bytes(const gqa_params *p);
 
@@ -271,7 +273,12 @@ gqa_status gqa_attention_decode_masked(const gqa_params *p, const gqa_mask *mask
  * semantics plus *mask, as for gqa_attention_decode_masked.  bf16/f16 with head_dim 64 or
  * 128 and a mask whose data address and non-zero strides (in bytes) are multiples of 16
  * run the tensor-core kernel, which stages the mask by TMA; any other mask, and f32, run
- * the CUDA-core kernel (same results within the dtype's tolerance, slower). */
+ * the CUDA-core kernel (same results within the dtype's tolerance, slower).  A boolean
+ * (GQA_MASK_KEEP) mask on the tensor-core kernel skips the 128-key tiles in which it keeps
+ * no key of a 128-row query tile ([P4] "Compute paths": an all-false block is skipped) when
+ * workspace_bytes >= gqa_workspace_bytes(p): a first kernel writes the mask's block map into
+ * the workspace.  With a smaller workspace every tile is streamed; the results are the same
+ * (keys the mask removes never contribute; a skipped tile is never read at all). */
 gqa_status gqa_attention_prefill_masked(const gqa_params *p, const gqa_mask *mask, const void *q, const void *k,
                                         const void *v, const void *past_k, const void *past_v,
                                         const int32_t *seqlens_k, const void *cos_cache, const void *sin_cache,
