@@ -14,6 +14,9 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
 def sample_rows(w, n=192, seed=0):
+    """Output rows compared at full size: n random rows, the band-edge rows, and one row of
+    every CTA's output: a random row of each 128-row query tile for every q head (prefill),
+    a random row of each (b, kv head) group (decode)."""
     rng = np.random.default_rng(seed)
     B, L, H = w.batch, w.q_len, w.q_heads
     rows = set(rng.integers(0, B * L * H, size=n).tolist())
@@ -21,6 +24,16 @@ def sample_rows(w, n=192, seed=0):
         for i in sorted({0, L - 1, L // 2, min(L - 1, 127), min(L - 1, 128), min(L - 1, 4095), min(L - 1, 4096)}):
             for h in (0, H - 1):
                 rows.add((b * L + i) * H + h)
+    G = H // w.kv_heads
+    for b in range(B):
+        if w.mode == "prefill":
+            for t0 in range(0, L, 128):
+                i = t0 + int(rng.integers(0, min(128, L - t0)))
+                rows.update((b * L + i) * H + h for h in range(H))
+        else:
+            for hk in range(w.kv_heads):
+                i, g = int(rng.integers(0, L)), int(rng.integers(0, G))
+                rows.add((b * L + i) * H + hk * G + g)
     return np.array(sorted(rows), dtype=np.int64)
 
 
