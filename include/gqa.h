@@ -111,6 +111,14 @@ typedef int32_t gqa_status;
 #define GQA_DEV_BAD_ROPE_POS 2 /* past_b + curr > rope_len with do_rotary */
 #define GQA_DEV_TIMEOUT 4      /* a bounded pipeline wait gave up; outputs invalid */
 #define GQA_DEV_BAD_PAGE 8     /* a block-table entry the step uses is outside [0, num_pages) */
+#define GQA_DEV_BOUNDS 16      /* bounds-checked debug build only: a store that would have left
+                                  its buffer was skipped (never set by the product build) */
+/* The bounds-checked debug build (the package's build(checked=True), compiled with
+ * -DGQA_BOUNDS_CHECK into its own folder) has the same entry points; every global store of
+ * its kernels is checked against the extent of its buffer, derived from the call.  It also
+ * exports the gqa_test_bounds_check probe: given a device int32 [64] buffer and a status
+ * word, it makes one store inside and one past a declared extent of 32 elements, so that a
+ * test sees the second store skipped and GQA_DEV_BOUNDS set. */
 
 typedef enum { GQA_F32 = 0, GQA_F16 = 1, GQA_BF16 = 2 } gqa_dtype;
 

@@ -1,6 +1,11 @@
 """Build libgqa.so in-tree: each .cu under csrc/ compiled by nvcc for sm_103a in parallel,
 then linked into sliding_window_gb300/_build/libgqa.so (static cudart, no -lcuda: the TMA
-tensor-map encoder is reached through the runtime's driver entry point)."""
+tensor-map encoder is reached through the runtime's driver entry point).
+
+build(checked=True) builds the bounds-checked debug library instead, into _build_checked/
+(-DGQA_BOUNDS_CHECK: every global store checked against its buffer's extent; a store that
+would leave its buffer is skipped and sets GQA_DEV_BOUNDS).  The binding loads it when
+GQA_CHECKED_BUILD=1 is set."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -15,6 +20,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgqa.so")
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(BUILD_CHECKED, "libgqa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
@@ -36,16 +43,17 @@ def _stale(lib: str, sources: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, checked: bool = False) -> str:
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    if not force and not _stale(LIB, sources):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    out_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    if not force and not _stale(lib, sources):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DGQA_BOUNDS_CHECK"] if checked else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -57,14 +65,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if verbose or ptxas_info:
         for _, err in results:
             sys.stderr.write(err)
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [cc, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                checked="--checked" in sys.argv))

@@ -36,6 +36,7 @@ struct SimtArgs {
   int mask_kind, mask_keys;
   long long msb, msh, msi;
   const float *k_scale, *v_scale;  // quantized cache: one scale per kv head (Q8 kernels)
+  GQA_EXTENTS
 };
 
 // MASKED: a mask is given (compiled out otherwise); SAMEV: Dv == D (the common case keeps
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && hq == 0) report(a.status, st);
     for (int idx = threadIdx.x; idx < nrows * Dv; idx += blockDim.x) {
       int r = idx / Dv, d = idx % Dv;
+      GQA_GUARD((((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d, 1, a.ext.out, a.status)
       out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d] = from_f32<T>(0.f);
     }
     return;
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(SimtArgs a) {
     }
     for (int s2 = 0; s2 < dslots; ++s2) {
       const int d = lane + 32 * s2;
+      GQA_GUARD((((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d, 1, a.ext.out, a.status)
       out[(((size_t)b * a.curr + i0 + r) * a.Hq + hq) * Dv + d] = from_f32<T>(acc[t][s2] * num_scale / den * out_scale);
     }
   }
@@ -212,6 +215,9 @@ template <typename T> gqa_status launch_t(const Call &c) {
   a.msi = c.mask_si;
   a.k_scale = c.k_scale;
   a.v_scale = c.v_scale;
+#ifdef GQA_BOUNDS_CHECK
+  a.ext = extents_of(c, WsLayout{});
+#endif
   const int D = p.head_dim;
   size_t smem = sizeof(float) * (kRows * D + kKeys * (D + 1) + kKeys * c.Dv + 4 * kKeys);
   // D, Dv <= 128: at most 41.5 KB of shared memory, under the 48 KB default limit

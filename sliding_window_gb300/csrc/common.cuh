@@ -125,6 +125,28 @@ __device__ __forceinline__ void report(int32_t *status, int bits) {
   if (status && bits) atomicOr(status, bits);
 }
 
+// Bounds-checked debug build (-DGQA_BOUNDS_CHECK; the stand-in for a memory checker): every
+// global store of the kernels is preceded by GQA_GUARD(first element, elements, the buffer's
+// extent in elements, status), which skips a store that would leave its buffer and sets
+// GQA_DEV_BOUNDS.  The extents come from the call (Extents, filled on the host).  In the
+// product build the guard expands to nothing.
+#ifdef GQA_BOUNDS_CHECK
+constexpr int kDevBounds = 16;
+__device__ __forceinline__ bool store_ok(size_t off, size_t n, size_t extent, int32_t *status) {
+  if (off + n <= extent) return true;
+  report(status, kDevBounds);
+  return false;
+}
+#define GQA_GUARD(off, n, extent, status) \
+  if (::gqa::store_ok((size_t)(off), (size_t)(n), (size_t)(extent), (status)))
+#define GQA_EXTENTS Extents ext;
+#define GQA_EXT(field) a.ext.field
+#else
+#define GQA_EXT(field) ((size_t)0)
+#define GQA_GUARD(off, n, extent, status)
+#define GQA_EXTENTS
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

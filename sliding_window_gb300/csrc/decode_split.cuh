@@ -76,6 +76,7 @@ struct DecodeArgs {
   const float *k_scale, *v_scale;  // f8 cache (Q8 kernels): one scale per kv head
   long long wait_limit;  // SM cycles after which a pipeline wait gives up
   int stall;             // test hook: the first wait is on a barrier nothing completes
+  GQA_EXTENTS
 };
 
 template <int D, int DV, int MT, int NST, bool Q8 = false> struct Smem {
@@ -225,14 +226,18 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
           rotate8<T>(krow + c, krow + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c, y1,
                      y2);
         const float sc = a.k_scale[h];
-        *reinterpret_cast<uint2 *>(p8 + dst + c) = codes8<T, I8>(y1, sc);
-        *reinterpret_cast<uint2 *>(p8 + dst + D / 2 + c) = codes8<T, I8>(y2, sc);
+        GQA_GUARD(dst + c, D / 2 + 8, a.ext.pk, a.status) {
+          *reinterpret_cast<uint2 *>(p8 + dst + c) = codes8<T, I8>(y1, sc);
+          *reinterpret_cast<uint2 *>(p8 + dst + D / 2 + c) = codes8<T, I8>(y2, sc);
+        }
       } else {
+        GQA_GUARD(row * DV + c, 8, a.ext.pv, a.status)
         *reinterpret_cast<uint2 *>(p8 + row * DV + c) =
             codes8<T, I8>(*reinterpret_cast<const uint4 *>(vrow + c), a.v_scale[h]);
       }
     } else if (isk) {
       const size_t dst = row * D;
+      GQA_GUARD(dst + c, D / 2 + 8, a.ext.pk, a.status)
       if (a.do_rotary) {
         uint4 y1, y2;
         rotate8<T>(krow + c, krow + D / 2 + c, cs + (size_t)pos * (D / 2) + c, sn + (size_t)pos * (D / 2) + c, y1,
@@ -244,6 +249,7 @@ __device__ __forceinline__ void append_rows(const DecodeArgs &a, int b, int h, i
         *reinterpret_cast<uint4 *>(pk + dst + D / 2 + c) = *reinterpret_cast<const uint4 *>(krow + D / 2 + c);
       }
     } else {
+      GQA_GUARD(row * DV + c, 8, a.ext.pv, a.status)
       *reinterpret_cast<uint4 *>(pv + row * DV + c) = *reinterpret_cast<const uint4 *>(vrow + c);
     }
   }
@@ -363,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (threadIdx.x == 0 && hkv == 0) report(a.status, st);
       for (int idx = threadIdx.x; idx < R * DV; idx += kThreads) {
         const int r = idx / DV, d = idx % DV, i = r / a.G, g = r % a.G;
+        GQA_GUARD((((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d, 1, a.ext.out, a.status)
         out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d] = from_f32<T>(0.f);
       }
     }
@@ -385,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (threadIdx.x == 0 && hkv == 0) report(a.status, GQA_DEV_BAD_PAGE);
         for (int idx = threadIdx.x; idx < R * DV; idx += kThreads) {
           const int r = idx / DV, d = idx % DV, i = r / a.G, g = r % a.G;
+          GQA_GUARD((((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d, 1, a.ext.out, a.status)
           out[(((size_t)b * a.curr + i) * a.Hq + hkv * a.G + g) * DV + d] = from_f32<T>(0.f);
         }
       }
@@ -956,8 +964,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       report(a.status, GQA_DEV_TIMEOUT);
       if (!CL && nchunks > 1) {
         __threadfence();
-        const int old = atomicAdd(&a.tickets[bh], 1);
-        if (old == nchunks - 1) a.tickets[bh] = 0;
+        GQA_GUARD(bh, 1, a.ext.tickets, a.status) {
+          const int old = atomicAdd(&a.tickets[bh], 1);
+          if (old == nchunks - 1) a.tickets[bh] = 0;
+        }
       }
     }
     if constexpr (CL) {
@@ -1076,6 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
       const float inv = __frcp_rn(den) * vsc;
+      GQA_GUARD((((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4, 4, a.ext.out, a.status)
       store4(o, num.x * inv, num.y * inv, num.z * inv, num.w * inv);
     }
     return;
@@ -1149,6 +1160,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
       const float inv = __frcp_rn(den) * vsc;
+      GQA_GUARD((((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4, 4, a.ext.out, a.status)
       store4(o, sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
     }
     return;  // nothing reads this CTA's shared memory any more
@@ -1159,14 +1171,20 @@ __global__ void __launch_bounds__(kThreads, 2)
   {
     const size_t base = gbase + (size_t)split * R;
     float4 *pacc = reinterpret_cast<float4 *>(a.part_acc + base * DV);
-    for (int idx = threadIdx.x; idx < R * DV / 4; idx += kThreads) pacc[idx] = merged(idx);
+    for (int idx = threadIdx.x; idx < R * DV / 4; idx += kThreads) {
+      GQA_GUARD(base * DV + 4 * (size_t)idx, 4, a.ext.part_acc, a.status)
+      pacc[idx] = merged(idx);
+    }
     for (int r = threadIdx.x; r < R; r += kThreads)
+      GQA_GUARD(2 * (base + r), 2, a.ext.part_ml, a.status)
       reinterpret_cast<float2 *>(a.part_ml)[base + r] = make_float2(row_m[r], row_l[r]);
   }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int old = atomicAdd(&a.tickets[bh], 1);
+    int old = 0;
+    GQA_GUARD(bh, 1, a.ext.tickets, a.status)
+    old = atomicAdd(&a.tickets[bh], 1);
     flags[1] = old == nchunks - 1;
   }
   __syncthreads();
@@ -1174,7 +1192,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // -------------------------------------------------------------- last CTA: combine
   __threadfence();
-  if (threadIdx.x == 0) a.tickets[bh] = 0;
+  if (threadIdx.x == 0) {
+    GQA_GUARD(bh, 1, a.ext.tickets, a.status)
+    a.tickets[bh] = 0;
+  }
   // chunk statistics staged in shared memory with all loads in flight at once
   float *cm = reinterpret_cast<float *>(stages);  // [nchunks][R] max, then scale factor
   float *cl = cm + a.splits * R;                    // [nchunks][R] sum
@@ -1233,6 +1254,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float den = row_l[r] > 0.f ? row_l[r] : 1.f;  // no visible key: the sums are 0
     T *o = out + (((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4;
     const float inv = __frcp_rn(den) * vsc;
+    GQA_GUARD((((size_t)b * a.curr + i) * a.Hq + hq) * DV + d4 * 4, 4, a.ext.out, a.status)
     store4(o, sum[u].x * inv, sum[u].y * inv, sum[u].z * inv, sum[u].w * inv);
   }
 }
@@ -1337,6 +1359,9 @@ gqa_status launch_t(const Call &c, const DecodePlan &dp, const WsLayout &wl) {
   a.v_scale = c.v_scale;
   a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitLimitCycles;
   a.stall = c.stall;
+#ifdef GQA_BOUNDS_CHECK
+  a.ext = extents_of(c, wl);
+#endif
   if (dp.cluster) return dispatch<T, true, MK, MIXED, Q8, I8>(c, dp, a);
   return dispatch<T, false, MK, MIXED, Q8, I8>(c, dp, a);
 }

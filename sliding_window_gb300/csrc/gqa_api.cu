@@ -15,6 +15,9 @@
 
 #include "gqa.h"
 #include "launch.h"
+#ifdef GQA_BOUNDS_CHECK
+#include "common.cuh"
+#endif
 
 namespace gqa {
 namespace {
@@ -356,8 +359,10 @@ gqa_status run_attention(Mode mode, const gqa_params *p, const void *q, const vo
     // a boolean mask's block map lets the prefill skip the key tiles it removes entirely,
     // when the workspace has room for it (it is optional)
     if (c.mask_kind == GQA_MASK_KEEP && wl.blockmap_bytes > 0 && c.ws && aligned16(c.ws) &&
-        workspace_bytes >= wl.blockmap_off + wl.blockmap_bytes)
+        workspace_bytes >= wl.blockmap_off + wl.blockmap_bytes) {
       c.blockmap = reinterpret_cast<uint32_t *>(c.ws + wl.blockmap_off);
+      c.blockmap_extent = wl.blockmap_bytes / 4;
+    }
     return launch_prefill_tc_masked(c);
   }
   return launch_prefill_tc(c);
@@ -600,6 +605,30 @@ const char *gqa_status_string(gqa_status s) {
 }
 
 int32_t gqa_abi_version(void) { return GQA_ABI_VERSION; }
+
+#ifdef GQA_BOUNDS_CHECK
+}  // extern "C"
+namespace gqa {
+namespace {
+// one store inside a declared extent of 32 elements, one past it (the buffer itself is
+// larger, so nothing leaves the allocation whether or not the guard works)
+__global__ void bounds_probe_kernel(int32_t *buf, int32_t *status) {
+  GQA_GUARD(8, 1, 32, status)
+  buf[8] = 5;
+  GQA_GUARD(40, 1, 32, status)
+  buf[40] = 7;
+}
+}  // namespace
+}  // namespace gqa
+extern "C" {
+/* Bounds-checked debug build only: checks that a guarded store outside its declared extent
+ * is skipped and reported (buf: device int32 [64]). */
+gqa_status gqa_test_bounds_check(int32_t *buf, int32_t *dev_status, void *stream) {
+  if (!buf || !dev_status) return GQA_ERR_INVALID_ARG;
+  gqa::bounds_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(buf, dev_status);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+#endif
 
 gqa_status gqa_test_stall_waits(int64_t cycles) {
   if (cycles < 0) return GQA_ERR_INVALID_ARG;

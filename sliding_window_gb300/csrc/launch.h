@@ -10,6 +10,13 @@
 
 namespace gqa {
 
+// Element counts of the buffers a kernel writes (the bounds-checked debug build checks every
+// store against them): out, present K and V (or their page pools), the rotated queries,
+// and the workspace's partials, tickets and block map.
+struct Extents {
+  size_t out = 0, pk = 0, pv = 0, qrot = 0, part_acc = 0, part_ml = 0, tickets = 0, map = 0;
+};
+
 // One validated call: shapes and attributes plus every pointer the kernels need.
 struct Call {
   gqa_params p;          // scale already resolved (0 -> 1/sqrt(D))
@@ -40,6 +47,7 @@ struct Call {
   long long mask_sb = 0, mask_sh = 0, mask_si = 0;
   // boolean mask on the tensor-core prefill: room for its block map in the workspace, or null
   uint32_t *blockmap = nullptr;
+  size_t blockmap_extent = 0;  // its words
   // f8 cache: present_k/v hold E4M3 codes; the stored value is code * scale of the kv head
   int q8 = 0;  // one-byte cache codes: 1 E4M3, 2 int8
   const float *k_scale = nullptr, *v_scale = nullptr;
@@ -82,6 +90,24 @@ struct WsLayout {
 // the upper bound that sizes the workspace.
 DecodePlan decode_plan(const gqa_params &p, int sms);
 WsLayout workspace_layout(const gqa_params &p, bool need_q_rot);
+
+// The element counts of a call's buffers (the bounds-checked debug build).
+inline Extents extents_of(const Call &c, const WsLayout &wl) {
+  Extents e;
+  const gqa_params &p = c.p;
+  e.out = (size_t)p.batch * p.q_len * p.q_heads * c.Dv;
+  const size_t rows = c.block_table ? (size_t)c.num_pages * p.kv_heads * 64 : (size_t)p.batch * p.kv_heads * p.cap_present;
+  e.pk = rows * p.head_dim;
+  e.pv = rows * c.Dv;
+  e.qrot = c.q_rot ? (size_t)p.batch * p.q_len * p.q_heads * p.head_dim : 0;
+  if (c.ws) {
+    e.part_acc = wl.part_acc_bytes / 4;
+    e.part_ml = wl.part_ml_bytes / 4;
+    e.tickets = wl.tickets_bytes / 4;
+    e.map = wl.blockmap_bytes / 4;
+  }
+  return e;
+}
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda link).
 // 3D map over a [outer, mid, inner] tensor of 16-bit elements with a 128B-swizzled box of

@@ -73,6 +73,7 @@ struct PrefillArgs {
   // kept in the rows of 128-row query tile qm (a broadcast dimension has coordinate 0)
   const uint32_t *blockmap;
   int bm_heads, bm_qtiles, bm_words;
+  GQA_EXTENTS
 };
 
 // Whether the boolean mask keeps any key of [k0, k0 + 128) in this CTA's query tile for
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && qt == 0 && blockIdx.x == 0) report(a.status, st);
     for (int idx = threadIdx.x; idx < (has_b ? 2 : 1) * nrows * DV; idx += blockDim.x) {
       const int hh = idx / (nrows * DV), r = (idx / DV) % nrows, d = idx % DV;
+      GQA_GUARD((((size_t)b * a.curr + q0 + r) * a.Hq + hA + hh) * DV + d, 1, a.ext.out, a.status)
       out[(((size_t)b * a.curr + q0 + r) * a.Hq + hA + hh) * DV + d] = from_f32<T>(0.f);
     }
     return;
@@ -687,7 +689,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__all_sync(0xffffffffu, fin) && none) {
       T *orow = out + (((size_t)b * a.curr + q0 + row) * a.Hq + hq) * DV;
       if (row < nrows)
-        for (int c = 0; c < DV; c += 8) *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < DV; c += 8) {
+          GQA_GUARD((((size_t)b * a.curr + q0 + row) * a.Hq + hq) * DV + c, 8, a.ext.out, a.status)
+          *reinterpret_cast<uint4 *>(orow + c) = make_uint4(0, 0, 0, 0);
+        }
     } else if (__all_sync(0xffffffffu, fin)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -705,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.y = pack2<T>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
             v.z = pack2<T>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
             v.w = pack2<T>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            GQA_GUARD((((size_t)b * a.curr + q0 + row) * a.Hq + hq) * DV + c * 32 + e, 8, a.ext.out, a.status)
             *reinterpret_cast<uint4 *>(orow + c * 32 + e) = v;
           }
         }
@@ -804,6 +810,9 @@ template <typename T, int MK, bool MIXED> gqa_status launch_t(const Call &c) {
   a.bm_heads = c.mask_sh == 0 ? 1 : p.q_heads;
   a.bm_qtiles = c.mask_si == 0 ? 1 : (p.q_len + BM - 1) / BM;
   a.bm_words = (((c.mask_keys < p.cap_present ? c.mask_keys : p.cap_present) + 15) / 16 + 31) / 32;
+#ifdef GQA_BOUNDS_CHECK
+  a.ext = extents_of(c, WsLayout{});
+#endif
   const bool sc = p.softcap > 0.f;
   if (sc) {
     a.score_mul = p.scale / p.softcap;

@@ -12,7 +12,9 @@ namespace {
 // keeps a key of 16-key chunk 32w + c.  Each warp reads whole rows, 16 bytes per lane.
 __global__ void __launch_bounds__(256) mask_blockmap_kernel(const uint8_t *mask, long long sb, long long sh,
                                                             long long si, int q_len, int keys, int heads, int qtiles,
-                                                            int words, uint32_t *map) {
+                                                            int words, uint32_t *map,
+                                                            [[maybe_unused]] size_t map_extent,
+                                                            [[maybe_unused]] int32_t *status) {
   const int qm = blockIdx.x, hm = blockIdx.y, bm = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = si == 0 ? 0 : qm * 128;
@@ -41,6 +43,7 @@ __global__ void __launch_bounds__(256) mask_blockmap_kernel(const uint8_t *mask,
     if (threadIdx.x == 0) {
       uint32_t x = 0;
       for (int i = 0; i < 8; ++i) x |= part[i];
+      GQA_GUARD((size_t)(out - map) + w, 1, map_extent, status)
       out[w] = x;
     }
     __syncthreads();
@@ -58,7 +61,7 @@ gqa_status launch_prefill_tc_masked(const Call &c) {
       const int words = ((keys + 15) / 16 + 31) / 32;
       mask_blockmap_kernel<<<dim3(qtiles, heads, c.mask_sb == 0 ? 1 : p.batch), 256, 0, c.stream>>>(
           static_cast<const uint8_t *>(c.mask), c.mask_sb, c.mask_sh, c.mask_si, p.q_len, keys, heads, qtiles, words,
-          c.blockmap);
+          c.blockmap, c.blockmap_extent, c.status);
       if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }
     return launch_prefill_tc_any<1, false>(c);

@@ -61,6 +61,7 @@ struct RopeArgs {
   // per kv head: E4M3 when q8 == 1, int8 when q8 == 2
   int q8;
   const float *k_scale, *v_scale;
+  GQA_EXTENTS
 };
 
 // N consecutive codes of x[e] / scale, stored as one N-byte word
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
       const int h = (it - items_qk) / v_per_head, c = ((it - items_qk) % v_per_head) * N;
       const T *src = reinterpret_cast<const T *>(a.v) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.Dv;
       const size_t row = cache_row(h);
+      GQA_GUARD(row * a.Dv + c, N, a.ext.pv, a.status)
       if (a.q8) {
         const uint4 x = *reinterpret_cast<const uint4 *>(src + c);
         uint8_t *v8 = reinterpret_cast<uint8_t *>(a.present_v) + row * a.Dv + c;
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
         continue;
       }
       T *dst = reinterpret_cast<T *>(a.present_v) + row * a.Dv;
+      GQA_GUARD(row * a.Dv + c, N, a.ext.pv, a.status)
       *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<const uint4 *>(src + c);
       continue;
     }
@@ -139,10 +142,13 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
     const T *src;
     T *dst;
     bool rot = a.do_rotary;
+    [[maybe_unused]] size_t dst_off, dst_ext;  // the store's buffer: first element, extent
     if (head < nq) {
       size_t off = (((size_t)b * a.curr + i) * a.Hq + head) * a.D;
       src = reinterpret_cast<const T *>(a.q) + off;
       dst = reinterpret_cast<T *>(a.q_rot) + off;
+      dst_off = off;
+      dst_ext = GQA_EXT(qrot);
     } else {
       const int h = head - nq;
       src = reinterpret_cast<const T *>(a.k) + (((size_t)b * a.curr + i) * a.Hkv + h) * a.D;
@@ -157,6 +163,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
           y2 = *reinterpret_cast<const uint4 *>(src + half + c);
         }
         uint8_t *k8 = reinterpret_cast<uint8_t *>(a.present_k) + row * a.D;
+        GQA_GUARD(row * a.D + c, half + N, a.ext.pk, a.status)
         if (a.q8 == 2) {
           store_codes<T, N, true>(k8 + c, p1, a.k_scale[h]);
           store_codes<T, N, true>(k8 + half + c, p2, a.k_scale[h]);
@@ -167,7 +174,10 @@ __global__ void __launch_bounds__(256) rope_append_kernel(RopeArgs a) {
         continue;
       }
       dst = reinterpret_cast<T *>(a.present_k) + row * a.D;
+      dst_off = row * a.D;
+      dst_ext = GQA_EXT(pk);
     }
+    GQA_GUARD(dst_off + c, half + N, dst_ext, a.status)
     if (rot) {
       rotate_chunk<T>(src + c, src + half + c, cosr + c, sinr + c, dst + c, dst + half + c);
     } else {
@@ -185,7 +195,9 @@ template <typename T>
 __global__ void __launch_bounds__(256) copy_past_words_kernel(const uint4 *past_k, const uint4 *past_v, uint4 *pres_k,
                                                               uint4 *pres_v, const int32_t *seqlens, int Hkv,
                                                               int cap_past, int cap_present, int D, int Dv,
-                                                              int curr, int rope_len, int do_rotary) {
+                                                              int curr, int rope_len, int do_rotary,
+                                                              [[maybe_unused]] Extents ext,
+                                                              [[maybe_unused]] int32_t *status) {
   constexpr int N = 16 / sizeof(T);
   const int bh = blockIdx.x;
   const int b = bh / Hkv;
@@ -198,10 +210,13 @@ __global__ void __launch_bounds__(256) copy_past_words_kernel(const uint4 *past_
   uint4 *dk = pres_k + (size_t)bh * cap_present * kw;
   uint4 *dv = pres_v + (size_t)bh * cap_present * vw;
   for (size_t w = (size_t)blockIdx.y * blockDim.x + threadIdx.x; w < words; w += (size_t)gridDim.y * blockDim.x) {
-    if (w < kwords)
+    if (w < kwords) {
+      GQA_GUARD(((size_t)bh * cap_present * kw + w) * N, N, ext.pk, status)
       dk[w] = sk[w];
-    else
+    } else {
+      GQA_GUARD(((size_t)bh * cap_present * vw + w - kwords) * N, N, ext.pv, status)
       dv[w - kwords] = sv[w - kwords];
+    }
   }
 }
 
@@ -211,7 +226,8 @@ template <typename T> static gqa_status launch_copy_t(const Call &c) {
   copy_past_words_kernel<T><<<grid, 256, 0, c.stream>>>(
       reinterpret_cast<const uint4 *>(c.past_k), reinterpret_cast<const uint4 *>(c.past_v),
       reinterpret_cast<uint4 *>(c.present_k), reinterpret_cast<uint4 *>(c.present_v), c.seqlens, p.kv_heads,
-      p.cap_past, p.cap_present, p.head_dim, c.Dv, p.q_len, p.rope_len, p.do_rotary);
+      p.cap_past, p.cap_present, p.head_dim, c.Dv, p.q_len, p.rope_len, p.do_rotary, extents_of(c, WsLayout{}),
+      c.status);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -247,6 +263,9 @@ template <typename T> static gqa_status launch_t(const Call &c) {
   a.q8 = c.q8;
   a.k_scale = c.k_scale;
   a.v_scale = c.v_scale;
+#ifdef GQA_BOUNDS_CHECK
+  a.ext = extents_of(c, WsLayout{});
+#endif
   if (c.past_separate) {
     const gqa_status st = launch_copy_t<T>(c);
     if (st != GQA_OK) return st;

@@ -17,7 +17,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libgqa.so")
+# GQA_CHECKED_BUILD=1: the bounds-checked debug library (build(checked=True))
+LIB_PATH = os.path.join(_HERE, "_build_checked" if os.environ.get("GQA_CHECKED_BUILD") == "1" else "_build",
+                        "libgqa.so")
 
 GQA_OK = 0
 GQA_ERR_INVALID_ARG = 1
@@ -28,6 +30,8 @@ GQA_ERR_WORKSPACE = 5
 GQA_DEV_BAD_SEQLEN = 1
 GQA_DEV_BAD_ROPE_POS = 2
 GQA_DEV_TIMEOUT = 4
+GQA_DEV_BAD_PAGE = 8
+GQA_DEV_BOUNDS = 16  # bounds-checked debug build only
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 TORCH_DTYPE_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
