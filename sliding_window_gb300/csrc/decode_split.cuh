@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // ---- S^T = K Q^T over this warp's 16 keys: lane (g, t) = (lane/4, lane%4) holds keys
       // g and g + 8 of rows 2t and 2t + 1; even and odd k steps in two chains
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t kc[4];  // f8: the codes of two k steps
+      uint32_t kc[4];  // one-byte caches: the codes of two k steps
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t af[4];  // A = 16 keys x 16 head dims of K

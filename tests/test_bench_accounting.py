@@ -49,11 +49,13 @@ def test_prefill_flops_by_hand(dv):
 @pytest.mark.parametrize("name,launches", [
     ("prefill_fp32_tiny", 2), ("decode_window_bf16", 1), ("prefill_sink_softcap_bf16", 2),
     ("specdecode_rotary_f16", 1), ("decode_long_bf16", 1), ("decode_window_ring_bf16", 1),
-    ("decode_window_paged_bf16", 1), ("decode_window_vdim_bf16", 1), ("prefill_bias_bf16", 2)])
+    ("decode_window_paged_bf16", 1), ("decode_window_vdim_bf16", 1), ("prefill_bias_bf16", 2),
+    ("decode_window_q8_bf16", 1), ("decode_window_i8_bf16", 1), ("prefill_blocksparse_bf16", 3)])
 def test_kernels_per_layer(name, launches):
     """One fused launch for the split-KV decode (it appends and rotates itself), else the
-    RoPE/append kernel and the attention kernel.  The speculative decode's 8 q heads x 4
-    tokens = 32 rows per group at D = 128 fit the split kernel."""
+    RoPE/append kernel and the attention kernel, with the block-map kernel between them for a
+    boolean mask.  The speculative decode's 8 q heads x 4 tokens = 32 rows per group at
+    D = 128 fit the split kernel."""
     w = WORKLOADS[name]
     assert bench.kernels_per_layer(w) == launches
 
