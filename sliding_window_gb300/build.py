@@ -2,10 +2,11 @@
 then linked into sliding_window_gb300/_build/libgqa.so (static cudart, no -lcuda: the TMA
 tensor-map encoder is reached through the runtime's driver entry point).
 
-build(checked=True) builds the bounds-checked debug library instead, into _build_checked/
+build(checked=True) builds the debug library instead, into _build_checked/: bounds-checked
 (-DGQA_BOUNDS_CHECK: every global store checked against its buffer's extent; a store that
-would leave its buffer is skipped and sets GQA_DEV_BOUNDS).  The binding loads it when
-GQA_CHECKED_BUILD=1 is set."""
+would leave its buffer is skipped and sets GQA_DEV_BOUNDS) and traced (-DGQA_NVTX: every
+C-ABI call is an NVTX range named after it).  The binding loads it when GQA_CHECKED_BUILD=1
+is set."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -23,6 +24,7 @@ LIB = os.path.join(BUILD, "libgqa.so")
 BUILD_CHECKED = os.path.join(PKG, "_build_checked")
 LIB_CHECKED = os.path.join(BUILD_CHECKED, "libgqa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+DEBUG_DEFINES = ["-DGQA_BOUNDS_CHECK", "-DGQA_NVTX"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
 
@@ -50,7 +52,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, 
         return lib
     os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DGQA_BOUNDS_CHECK"] if checked else [])
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (DEBUG_DEFINES if checked else [])
 
     def compile_one(src):
         obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")

@@ -420,6 +420,7 @@ gqa_status gqa_attention_prefill(const gqa_params *p, const void *q, const void 
                                  const void *cos_cache, const void *sin_cache, const float *head_sink, void *out,
                                  void *present_k, void *present_v, void *workspace, size_t workspace_bytes,
                                  int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_attention(gqa::kPrefill, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
@@ -429,6 +430,7 @@ gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *
                                 const void *cos_cache, const void *sin_cache, const float *head_sink, void *out,
                                 void *present_k, void *present_v, void *workspace, size_t workspace_bytes,
                                 int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_attention(gqa::kDecode, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
@@ -436,6 +438,7 @@ gqa_status gqa_attention_decode(const gqa_params *p, const void *q, const void *
 gqa_status gqa_attention_nonpad(const gqa_params *p, const int64_t *nonpad_kv_seqlen, const void *q,
                                 const void *k_cache, const void *v_cache, const float *head_sink, void *out,
                                 void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   if (!p || !nonpad_kv_seqlen || (reinterpret_cast<uintptr_t>(nonpad_kv_seqlen) & 7u)) return GQA_ERR_INVALID_ARG;
   if (p->kv_ring || p->do_rotary) return GQA_ERR_INVALID_ARG;  // a plain cache, q as given
   return gqa::run_attention(gqa::kPrefill, p, q, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
@@ -449,6 +452,7 @@ gqa_status gqa_attention_decode_masked(const gqa_params *p, const gqa_mask *mask
                                        const float *head_sink, void *out, void *present_k, void *present_v,
                                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                        void *stream) {
+  GQA_TRACE_CALL();
   if (!mask) return GQA_ERR_INVALID_ARG;
   return gqa::run_attention(gqa::kDecode, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream, mask);
@@ -460,6 +464,7 @@ gqa_status gqa_attention_prefill_masked(const gqa_params *p, const gqa_mask *mas
                                         const float *head_sink, void *out, void *present_k, void *present_v,
                                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                         void *stream) {
+  GQA_TRACE_CALL();
   if (!mask) return GQA_ERR_INVALID_ARG;
   return gqa::run_attention(gqa::kPrefill, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, head_sink,
                             out, present_k, present_v, workspace, workspace_bytes, dev_status, stream, mask);
@@ -470,6 +475,7 @@ gqa_status gqa_attention_decode_q8(const gqa_params *p, const void *q, const voi
                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                                    uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
                                    int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_attention_q8(gqa::kDecode, 1, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
                                v_scale, out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
@@ -479,6 +485,7 @@ gqa_status gqa_attention_prefill_q8(const gqa_params *p, const void *q, const vo
                                     const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                                     uint8_t *present_k, uint8_t *present_v, void *workspace, size_t workspace_bytes,
                                     int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_attention_q8(gqa::kPrefill, 1, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
                                v_scale, out, present_k, present_v, workspace, workspace_bytes, dev_status, stream);
 }
@@ -488,6 +495,7 @@ gqa_status gqa_attention_decode_i8(const gqa_params *p, const void *q, const voi
                                    const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                                    int8_t *present_k, int8_t *present_v, void *workspace, size_t workspace_bytes,
                                    int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_attention_q8(gqa::kDecode, 2, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
                                v_scale, out, reinterpret_cast<uint8_t *>(present_k),
                                reinterpret_cast<uint8_t *>(present_v), workspace, workspace_bytes, dev_status, stream);
@@ -498,6 +506,7 @@ gqa_status gqa_attention_prefill_i8(const gqa_params *p, const void *q, const vo
                                     const float *head_sink, const float *k_scale, const float *v_scale, void *out,
                                     int8_t *present_k, int8_t *present_v, void *workspace, size_t workspace_bytes,
                                     int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_attention_q8(gqa::kPrefill, 2, p, q, k, v, seqlens_k, cos_cache, sin_cache, head_sink, k_scale,
                                v_scale, out, reinterpret_cast<uint8_t *>(present_k),
                                reinterpret_cast<uint8_t *>(present_v), workspace, workspace_bytes, dev_status, stream);
@@ -564,6 +573,7 @@ gqa_status gqa_attention_decode_paged(const gqa_params *p, const void *q, const 
                                       const float *head_sink, void *out, void *k_pool, void *v_pool,
                                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                       void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_paged(gqa::kDecode, p, q, k, v, seqlens_k, block_table, max_pages, num_pages, cos_cache, sin_cache,
                         head_sink, out, k_pool, v_pool, workspace, workspace_bytes, dev_status, stream);
 }
@@ -574,6 +584,7 @@ gqa_status gqa_attention_prefill_paged(const gqa_params *p, const void *q, const
                                        const float *head_sink, void *out, void *k_pool, void *v_pool,
                                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                        void *stream) {
+  GQA_TRACE_CALL();
   return gqa::run_paged(gqa::kPrefill, p, q, k, v, seqlens_k, block_table, max_pages, num_pages, cos_cache,
                         sin_cache, head_sink, out, k_pool, v_pool, workspace, workspace_bytes, dev_status, stream);
 }
@@ -582,6 +593,7 @@ gqa_status gqa_rope_append_kv(const gqa_params *p, const void *q, const void *k,
                               const void *past_v, const int32_t *seqlens_k, const void *cos_cache,
                               const void *sin_cache, void *q_rot, void *present_k, void *present_v,
                               int32_t *dev_status, void *stream) {
+  GQA_TRACE_CALL();
   gqa::Call c;
   if (!k || !v) return GQA_ERR_INVALID_ARG;
   gqa_status s = gqa::make_call(c, p, q, k, v, past_k, past_v, seqlens_k, cos_cache, sin_cache, nullptr, nullptr,

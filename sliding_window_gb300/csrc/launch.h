@@ -8,7 +8,23 @@
 
 #include "gqa.h"
 
+#ifdef GQA_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace gqa {
+
+// Tracing (-DGQA_NVTX, on in the bounds-checked debug build): every C-ABI call is one NVTX
+// range named after the call, so that a profiler attributes the kernels it launches to it.
+#ifdef GQA_NVTX
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+#define GQA_TRACE_CALL() ::gqa::NvtxRange gqa_trace_range_(__func__)
+#else
+#define GQA_TRACE_CALL()
+#endif
 
 // Element counts of the buffers a kernel writes (the bounds-checked debug build checks every
 // store against them): out, present K and V (or their page pools), the rotated queries,
