@@ -16,11 +16,11 @@ import torch
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-# every kernel and store path: split decode (cluster and ticket combines, fused append, ring,
-# pages, f8 and int8 codes), tensor-core prefill (masks with the block map), RoPE/append,
-# the CUDA-core kernel, the past copy
+# every kernel and store path: split decode (cluster and ticket combines, fused append, pages,
+# f8 and int8 codes), tensor-core prefill (masks with the block map), RoPE/append, the
+# CUDA-core kernel, the past copy
 SUITES = ["tests/test_gpu_decode.py", "tests/test_gpu_prefill.py", "tests/test_gpu_rope_append.py",
-          "tests/test_gpu_ring.py", "tests/test_gpu_paged.py", "tests/test_gpu_mask_skip.py::test_dead_tiles_are_never_read",
+          "tests/test_gpu_paged.py", "tests/test_gpu_mask_skip.py::test_dead_tiles_are_never_read",
           "tests/test_gpu_q8.py::test_split_decode_q8", "tests/test_gpu_q8.py::test_cuda_core_q8"]
 
 
