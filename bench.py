@@ -673,6 +673,9 @@ def cpu_baseline(w, budget_s=12.0):
 # workloads, each reported in the same line with its own timing, roofline, e2e and oracle
 # baseline; a sub-workload runs at least this many steps, so its timed region is >= ~10 ms
 HEADLINE = "decode_long_bf16"
+# measured after those, each in its own try: the quantized caches and the block-sparse
+# boolean mask (a failure there is reported in its record and leaves the others intact)
+EXTRA_WORKLOADS = {"decode_window_q8_bf16": 1000, "decode_window_i8_bf16": 1000, "prefill_blocksparse_bf16": 8}
 SUB_WORKLOADS = {"prefill_sink_softcap_bf16": 8, "decode_window_bf16": 1000, "specdecode_rotary_f16": 100,
                  "prefill_fp32_tiny": 300}
 DEFAULT_STEPS = {"decode_window_bf16": 20000, "specdecode_rotary_f16": 2000, "decode_long_bf16": 200,
@@ -732,15 +735,29 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     r = run_workload(w, args.steps, args.warmup, rank, world, local_rank, with_e2e=not args.no_e2e)
-    subs = []
+    subs, extras = [], []
     if not args.only and args.workload == HEADLINE:
         for name, min_steps in SUB_WORKLOADS.items():
             subs.append(run_workload(WORKLOADS[name], max(args.steps, min_steps), args.warmup, rank, world,
                                      local_rank, with_e2e=not args.no_e2e))
+        for name, min_steps in EXTRA_WORKLOADS.items():
+            try:
+                extras.append(run_workload(WORKLOADS[name], max(args.steps, min_steps), args.warmup, rank, world,
+                                           local_rank, with_e2e=not args.no_e2e))
+            except Exception as e:  # noqa: BLE001  (reported in the workload's record)
+                extras.append({"w": WORKLOADS[name], "error": "%s: %s" % (type(e).__name__, str(e)[:300])})
     if rank == 0:
         line = report(args, r, world, headline=True)
         if subs:
             line["workloads"] = {x["w"].name: report(args, x, world, headline=False) for x in subs}
+        for x in extras:
+            rec = {"error": x["error"]} if "error" in x else None
+            if rec is None:
+                try:
+                    rec = report(args, x, world, headline=False)
+                except Exception as e:  # noqa: BLE001
+                    rec = {"error": "%s: %s" % (type(e).__name__, str(e)[:300])}
+            line["workloads"][x["w"].name] = rec
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
